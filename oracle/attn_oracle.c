@@ -1,0 +1,210 @@
+/*
+ * fp64 CPU oracle for masked scaled dot-product self-attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and
+ * bench.py's cpu_baseline / reference arm may load this library.  It shares
+ * no code, header, table or helper with the CUDA path in
+ * transformer_self_attention_gb300/, and the product never calls it.
+ *
+ * What it computes (the plain definition, no tiling, no online softmax):
+ *
+ *   For a query head a with key/value head g(a), position i:
+ *     s_ij   = (q_i^(a) . k_j^(g(a))) * scale            for allowed (i, j)
+ *     alpha  = softmax_j(s_ij)                             over allowed j only
+ *     z_i    = sum_j alpha_ij v_j^(g(a))
+ *     LSE_i  = ln sum_j exp(s_ij)                          (natural log)
+ *
+ *   - "Trasformer 浅析" (atffang.github.io), section 缩放点积注意力: the
+ *     score e_ij = q_i.k_j / sqrt(d_k), row-wise Softmax, output = weights x V.
+ *   - same page, section 填充掩码与因果掩码: the additive mask M with -inf;
+ *     a -inf entry gets exactly zero weight, so skipping the pair is the same
+ *     thing as adding -inf to it, which is what this file does.
+ *   - "Transformer 架构及其变体" (aaai.latere.ai), section 带显式形状的因果自注意力:
+ *     the shape-explicit form with H_q query heads, H_kv key/value heads and a
+ *     query-head -> kv-head map g(a).  The page leaves g open; this oracle takes
+ *     the contiguous-group reading g(a) = a / (H_q / H_kv), which is the uniform
+ *     grouping described in "Transformer 演进与变体" (ai.icyfenix.cn), section
+ *     GQA：分组查询注意力 (g = 1 is MQA, g = h is MHA).
+ *   - Mask kinds, "Transformer 演进与变体", section 稀疏注意力: a sliding window
+ *     of half-width w (position i sees |i - j| <= w, width 2w+1) and local +
+ *     global attention where global tokens see every position and are seen by
+ *     every position.  The causal window (0 <= i - j <= w) is the causal mask
+ *     of the 填充掩码与因果掩码 section intersected with that window.
+ *
+ * Arithmetic is fp64 throughout; inputs arrive as float32 arrays (which hold
+ * bf16 and fp32 values exactly) and are widened element by element.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* mask kinds: same numbering as the library's public header, restated here */
+enum {
+    ORACLE_MASK_FULL = 0,
+    ORACLE_MASK_CAUSAL = 1,
+    ORACLE_MASK_SLIDING = 2,        /* |i - j| <= w                       */
+    ORACLE_MASK_CAUSAL_SLIDING = 3, /* 0 <= i - j <= w                    */
+    ORACLE_MASK_LOCAL_GLOBAL = 4    /* |i - j| <= w  or  i in G or j in G */
+};
+
+/* Allowed(i, j) for one mask kind.  is_global is a 0/1 array of length S
+ * (may be NULL when the kind is not LOCAL_GLOBAL).  Returns 1 or 0; returns
+ * 0 for a kind this file does not know. */
+int oracle_allowed(int kind, long i, long j, long S, long w,
+                   const unsigned char* is_global)
+{
+    if (i < 0 || j < 0 || i >= S || j >= S) return 0;
+    long diff = i - j;
+    switch (kind) {
+    case ORACLE_MASK_FULL: return 1;
+    case ORACLE_MASK_CAUSAL: return j <= i;
+    case ORACLE_MASK_SLIDING: return labs(diff) <= w;
+    case ORACLE_MASK_CAUSAL_SLIDING: return diff >= 0 && diff <= w;
+    case ORACLE_MASK_LOCAL_GLOBAL:
+        if (labs(diff) <= w) return 1;
+        return (is_global[i] != 0) || (is_global[j] != 0);
+    default: return 0;
+    }
+}
+
+static unsigned char* make_global_flags(long S, const int* G, int nG)
+{
+    unsigned char* f = (unsigned char*)calloc((size_t)(S > 0 ? S : 1), 1);
+    if (!f) return NULL;
+    for (int t = 0; t < nG; ++t)
+        if (G[t] >= 0 && G[t] < S) f[G[t]] = 1;
+    return f;
+}
+
+/*
+ * Attention for an explicit list of query rows.
+ *
+ * K, V      : float32 [B, Hkv, S, d], contiguous.
+ * Qrows     : float32 [n, d], the query vectors of the requested rows.
+ * row_b/a/i : batch index, query-head index and position of each row.
+ * O         : fp64 [n, d] output (z_i of the shape-explicit form).
+ * LSE       : fp64 [n] output, ln sum_j exp(s_ij); -inf for a row with no
+ *             allowed key (cannot happen for the five kinds, every row sees
+ *             itself), in which case O is set to 0.
+ * Returns 0 on success, -1 on bad arguments or allocation failure.
+ */
+int oracle_attention_rows(const float* K, const float* V,
+                          int B, int Hq, int Hkv, int S, int d,
+                          double scale, int kind, int window,
+                          const int* G, int nG,
+                          const float* Qrows, const int* row_b, const int* row_a,
+                          const int* row_i, long n,
+                          double* O, double* LSE)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 0 || d < 1 || Hq % Hkv != 0) return -1;
+    unsigned char* is_global = make_global_flags(S, G, nG);
+    if (!is_global) return -1;
+    const int group = Hq / Hkv; /* query heads per kv head */
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!s || !acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < n; ++r) {
+            if (!s || !acc) continue;
+            const int b = row_b[r], a = row_a[r];
+            const long i = row_i[r];
+            const int ga = a / group; /* g(a) */
+            const float* q = Qrows + (size_t)r * d;
+            const float* Kh = K + ((size_t)b * Hkv + ga) * (size_t)S * d;
+            const float* Vh = V + ((size_t)b * Hkv + ga) * (size_t)S * d;
+
+            /* scores s_ij over allowed j, and their maximum */
+            double m = -INFINITY;
+            for (long j = 0; j < S; ++j) {
+                if (!oracle_allowed(kind, i, j, S, window, is_global)) continue;
+                const float* k = Kh + (size_t)j * d;
+                double dot = 0.0;
+                for (int t = 0; t < d; ++t) dot += (double)q[t] * (double)k[t];
+                s[j] = dot * scale;
+                if (s[j] > m) m = s[j];
+            }
+            for (int t = 0; t < d; ++t) acc[t] = 0.0;
+            double l = 0.0;
+            if (m != -INFINITY) {
+                /* softmax numerators exp(s_ij - m), their sum, and the
+                   weighted sum of value rows */
+                for (long j = 0; j < S; ++j) {
+                    if (!oracle_allowed(kind, i, j, S, window, is_global)) continue;
+                    const double e = exp(s[j] - m);
+                    l += e;
+                    const float* v = Vh + (size_t)j * d;
+                    for (int t = 0; t < d; ++t) acc[t] += e * (double)v[t];
+                }
+            }
+            double* o = O + (size_t)r * d;
+            if (l > 0.0) {
+                for (int t = 0; t < d; ++t) o[t] = acc[t] / l;
+                LSE[r] = m + log(l);
+            } else {
+                for (int t = 0; t < d; ++t) o[t] = 0.0;
+                LSE[r] = -INFINITY;
+            }
+        }
+        free(s);
+        free(acc);
+    }
+    free(is_global);
+    return failed ? -1 : 0;
+}
+
+/* Number of allowed keys of every row i in [0, S): counts[i]. */
+int oracle_row_counts(int kind, int S, int window, const int* G, int nG, long* counts)
+{
+    unsigned char* is_global = make_global_flags(S, G, nG);
+    if (!is_global) return -1;
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < S; ++i) {
+        long c = 0;
+        for (long j = 0; j < S; ++j) c += oracle_allowed(kind, i, j, S, window, is_global);
+        counts[i] = c;
+    }
+    free(is_global);
+    return 0;
+}
+
+/*
+ * Brute-force tile classes: for every (row tile, column tile) of size
+ * tm x tn over the S x S pair grid, enumerate each (i, j) inside the tile
+ * (pairs beyond S count as not allowed) and write
+ *   0 = SKIP    (no allowed pair),
+ *   1 = FULL    (every pair of the tm x tn tile lies inside S x S and is allowed),
+ *   2 = PARTIAL (anything else).
+ * classes is uint8 [ceil(S/tm), ceil(S/tn)], row-major.
+ */
+int oracle_tile_classes(int kind, int S, int window, const int* G, int nG,
+                        int tm, int tn, unsigned char* classes)
+{
+    if (tm < 1 || tn < 1) return -1;
+    unsigned char* is_global = make_global_flags(S, G, nG);
+    if (!is_global) return -1;
+    const long nt_m = (S + tm - 1) / tm, nt_n = (S + tn - 1) / tn;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long ti = 0; ti < nt_m; ++ti) {
+        for (long tj = 0; tj < nt_n; ++tj) {
+            long allowed = 0;
+            for (long i = ti * tm; i < (ti + 1) * tm; ++i)
+                for (long j = tj * tn; j < (tj + 1) * tn; ++j)
+                    allowed += oracle_allowed(kind, i, j, S, window, is_global);
+            unsigned char c;
+            if (allowed == 0) c = 0;
+            else if (allowed == (long)tm * tn) c = 1;
+            else c = 2;
+            classes[ti * nt_n + tj] = c;
+        }
+    }
+    free(is_global);
+    return 0;
+}
