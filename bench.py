@@ -1,0 +1,347 @@
+"""Benchmark: attention forward useful TFLOP/s on one GB300 (per process), JSON line on rank 0.
+
+Workload (default): causal MHA prefill B=2, H=32, S=4096, d=128, bf16, seeded
+synthetic N(0,1) inputs with query heads 16-31 doubled.  Useful FLOPs count 4*d
+per allowed (i, j) pair only (masked pairs are not counted).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Each timed step is one attn_forward over the whole batch (all heads, all rows);
+L2 is flushed (a 256 MiB write) before every step and the step is timed with
+CUDA events on the launching stream.  Under torchrun every rank runs its own
+replica of the workload (the forward pass has no exchange step); the reported
+value is all ranks' useful FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "attention fwd useful TFLOP/s and % of GB300 dense BF16 tensor peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["transformer_self_attention_gb300/csrc/attn_fwd_tc.cu",
+                  "transformer_self_attention_gb300/csrc/sm103_ptx.h",
+                  "transformer_self_attention_gb300/csrc/kernels.h"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if current."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+_INPUTS = {}
+
+
+def _oracle_inputs(w: wl.Workload):
+    if w.name not in _INPUTS:
+        Qc, Kc, Vc = wl.make_inputs(w)
+        _INPUTS[w.name] = (Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy())
+    return _INPUTS[w.name]
+
+
+def cpu_baseline(w: wl.Workload, target_s: float = 12.0, frac: float | None = None):
+    """The fp64 oracle, as it stands, on a strided sample of the workload's rows."""
+    import numpy as np
+    n_cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
+    import oracle
+    oracle.build()
+    Qf, Kf, Vf = _oracle_inputs(w)
+    pairs = wl.allowed_pairs_per_head(w)
+
+    def run(stride):
+        bb, aa, ii = np.meshgrid(np.arange(w.B), np.arange(w.Hq), np.arange(0, w.S, stride), indexing="ij")
+        rb, ra, ri = bb.ravel(), aa.ravel(), ii.ravel()
+        t0 = time.perf_counter()
+        oracle.attention_rows(Kf, Vf, w.Hq, w.scale, w.kind, w.window, list(w.globals_idx), Qf[rb, ra, ri],
+                              rb, ra, ri)
+        dt = time.perf_counter() - t0
+        # useful flops of the sampled rows: rows are strided uniformly, so the sample holds 1/stride of the pairs
+        rows_frac = len(ri) / (w.B * w.Hq * w.S)
+        return dt, 4.0 * w.d * pairs * w.B * w.Hq * rows_frac, len(ri)
+
+    if frac is None:
+        dt, fl, _ = run(64)
+        rate = fl / max(dt, 1e-6)
+        want = min(1.0, rate * target_s / wl.useful_flops(w))
+        stride = max(1, int(round(1.0 / max(want, 1e-9))))
+    else:
+        stride = max(1, int(round(1.0 / frac)))
+    dt, fl, n = run(stride)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"every {stride}th query row of every (batch, head): {n} rows, "
+                      f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    n_cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
+    # one calibration sample fixes the per-step sample so the whole run takes a few minutes
+    cal = cpu_baseline(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    frac_stride = int(re.search(r"every (\d+)th", cal["sample"]).group(1))
+    times, flops = [], 0.0
+    for s in range(args.warmup + args.steps):
+        r = cpu_baseline(w, frac=1.0 / frac_stride)
+        if s >= args.warmup:
+            times.append(r["seconds"])
+            flops = r["value"] * r["seconds"] * 1e12
+    t = sum(times) / len(times)
+    value = flops / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+                       "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx)},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+                             "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_self_attention_gb300 as tsa
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    Qc, Kc, Vc = wl.make_inputs(w)
+    Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind,
+                         window=w.window, global_idx=list(w.globals_idx))
+    O = torch.empty_like(Q)
+    LSE = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_fwd = 1 + (1 if (w.kind == wl.MASK_LOCAL_GLOBAL and w.globals_idx) else 0) * 2
+
+    def fwd():
+        plan(Q, K, V, O=O, LSE=LSE, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize(dev)
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {code}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        fwd()
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during the timed steps: {code}")
+
+    useful = wl.useful_flops(w)
+    value = world * useful / (mean_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+
+    # end to end through the C ABI: pinned host inputs -> device, forward, O and LSE -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        hQ, hK, hV = (t.pin_memory() for t in (Qc, Kc, Vc))
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype, pin_memory=True)
+        dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+        dO, dL = torch.empty_like(O), torch.empty_like(LSE)
+        n_e2e = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            dQ.copy_(hQ, non_blocking=True); dK.copy_(hK, non_blocking=True); dV.copy_(hV, non_blocking=True)
+            plan(dQ, dK, dV, O=dO, LSE=dL, stream=stream)
+            hO.copy_(dO, non_blocking=True); hL.copy_(dL, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        bi = sum(t.numel() * t.element_size() for t in (Qc, Kc, Vc))
+        bo = O.numel() * O.element_size() + LSE.numel() * LSE.element_size()
+        e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    achieved = useful / (mean_ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": ncu_traffic(w.name), "peak_source": f"{pk_src} bf16_tflops (burst, cuBLAS)",
+                "kernel": "attn_fwd_tc_kernel"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+                       "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
+                       "useful_gflop_per_step": useful / 1e9, "l2": "flushed before every step (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": {"measured": 100.0 * achieved / peak, "nominal": 100.0 * achieved / NOMINAL_BF16_TFLOPS,
+                            "peak_source": pk_src},
+            "roofline": roofline, "gpu_launches": args.steps * launches_per_fwd,
+            "wall_s_timed_region": wall}
+    if e2e:
+        line["e2e"] = e2e
+    if clk:
+        line["clocks"] = clk
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=wl.CAUSAL_MHA_4K.name, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.BY_NAME[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

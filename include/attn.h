@@ -1,0 +1,186 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) self-attention forward library.
+ *
+ * The operation.  For every batch b, query head a (key/value head g(a)) and
+ * query position i:
+ *
+ *     s_ij  = scale * (q_i^(a) . k_j^(g(a)))          for every allowed key j
+ *     O_i   = sum_j softmax_j(s_ij) * v_j^(g(a))
+ *     LSE_i = ln sum_j exp(s_ij)                       (natural logarithm)
+ *
+ *   - Scaled dot-product attention Softmax(Q K^T / sqrt(d_k)) V and its
+ *     row-wise softmax: "Trasformer 浅析" (atffang.github.io), section
+ *     缩放点积注意力.  `scale` is applied exactly as passed; callers pass
+ *     1/sqrt(d_k) for the textbook form.
+ *   - Masks as an additive M with -inf entries (a -inf entry carries exactly
+ *     zero weight): same page, section 填充掩码与因果掩码.  A disallowed pair is
+ *     never evaluated; the mask is a predicate, not a stored matrix.
+ *   - Shapes with H_q query heads sharing H_kv key/value heads through a map
+ *     g(a): "Transformer 架构及其变体" (aaai.latere.ai), section
+ *     带显式形状的因果自注意力.  This library fixes g(a) = a / (H_q / H_kv)
+ *     (contiguous groups), the uniform grouping of "Transformer 演进与变体"
+ *     (ai.icyfenix.cn), section GQA：分组查询注意力; H_kv = 1 is MQA and
+ *     H_kv = H_q is MHA.
+ *   - Sliding-window and local + global masks: "Transformer 演进与变体",
+ *     section 稀疏注意力 (window of half-width w; global tokens attend to every
+ *     position and every position attends to them).
+ *
+ * Tensor layouts (all contiguous, row-major, the head dimension fastest):
+ *     Q, O : [B, H_q,  S, d_k]     K, V : [B, H_kv, S, d_k]     LSE : [B, H_q, S] float32
+ * Element type: ATTN_BF16 -> Q, K, V, O are bfloat16 (fp32 accumulation);
+ *               ATTN_F32  -> Q, K, V, O are float32.
+ * Every pointer passed to attn_forward is a device pointer of the current
+ * CUDA device and must be 16-byte aligned.
+ *
+ * Ownership: the caller owns Q, K, V, O, LSE and the stream.  A handle owns
+ * its schedule, its tensor-map templates and, for the local + global mask, a
+ * device scratch area sized at attn_create; attn_destroy frees them.
+ *
+ * Threading: a handle may be reused for any tensors of the shape it was
+ * created for, on any stream, but not by two calls in flight at once (the
+ * local + global scratch would be shared).  Distinct handles are independent.
+ *
+ * Errors: every entry point returns an attn_status.  Argument errors are
+ * detected on the host before anything is launched.  attn_forward is
+ * asynchronous: device-side watchdog errors (a bounded wait that ran out) are
+ * recorded in the handle's device error word and read by
+ * attn_poll_device_error, which synchronises the device.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,      /* a size, pointer, mask argument or scale is invalid  */
+    ATTN_ERR_UNSUPPORTED = 2,      /* valid in principle but not built (e.g. d_k = 96)     */
+    ATTN_ERR_CUDA = 3,             /* a CUDA runtime / driver call failed                  */
+    ATTN_ERR_DEVICE_TIMEOUT = 4,   /* a kernel's bounded wait ran out (watchdog)           */
+    ATTN_ERR_OOM = 5               /* device or host allocation failed at attn_create      */
+} attn_status;
+
+typedef enum {
+    ATTN_MASK_FULL = 0,            /* every j                                              */
+    ATTN_MASK_CAUSAL = 1,          /* j <= i                                               */
+    ATTN_MASK_SLIDING = 2,         /* |i - j| <= window                                    */
+    ATTN_MASK_CAUSAL_SLIDING = 3,  /* 0 <= i - j <= window  (window = max distance;       */
+                                   /*  "4096 keys including self" is window = 4095)       */
+    ATTN_MASK_LOCAL_GLOBAL = 4     /* |i - j| <= window, or i in G, or j in G              */
+} attn_mask_kind;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+typedef struct attn_plan* attn_handle;
+
+/*
+ * attn_create -- validate the problem, build the tile schedule on the host,
+ * upload it, and allocate the handle's device buffers.
+ *
+ *   out        : receives the handle (set to NULL on failure).
+ *   B, Hq, Hkv : batch, query heads, key/value heads; Hq % Hkv == 0.
+ *   S          : sequence length, 1 <= S <= 1<<20.
+ *   d_k        : head width; 64 or 128 (others: ATTN_ERR_UNSUPPORTED).
+ *   dtype      : ATTN_BF16 or ATTN_F32.
+ *   scale      : score multiplier, finite and > 0.
+ *   kind       : mask kind.
+ *   window     : half-width w (>= 0) for the window kinds, ignored otherwise.
+ *   global_idx : host array of n_global positions in [0, S) (LOCAL_GLOBAL
+ *                only; duplicates are removed; copied, the caller keeps it).
+ *   n_global   : 0 <= n_global <= 4096; must be 0 for other kinds.
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ */
+attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k,
+                        attn_dtype dtype, float scale, attn_mask_kind kind, int window,
+                        const int* global_idx, int n_global);
+
+/*
+ * attn_forward -- enqueue the forward pass on `stream` (a cudaStream_t, NULL
+ * for the legacy default stream) and return without waiting.
+ *
+ *   Q, K, V : inputs in the layouts above.        O : output, same shape as Q.
+ *   LSE     : float32 [B, Hq, S] output, or NULL to skip it.
+ * Every row sees at least itself, so every O row is a convex combination of
+ * V rows and every LSE entry is finite.
+ * Errors: ATTN_ERR_INVALID_ARG (NULL handle or pointer, misaligned pointer),
+ *         ATTN_ERR_CUDA (launch failure).  With the environment variable
+ *         ATTN_DEBUG=1 the call synchronises and also reports
+ *         ATTN_ERR_DEVICE_TIMEOUT.
+ */
+attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void* V,
+                         void* O, float* LSE, void* stream);
+
+/* attn_destroy -- free the handle's device and host memory (synchronises the
+ * device first).  NULL is accepted and ignored. */
+attn_status attn_destroy(attn_handle h);
+
+/* attn_status_string -- static English text of a status code. */
+const char* attn_status_string(attn_status s);
+
+/*
+ * Schedule introspection (host only, no device work).
+ *
+ * The schedule is a list of work items of ATTN_WORK_INTS ints each:
+ *   [0] bh          b * Hq + a  (query head a of batch b)
+ *   [1] q_tile      query rows [q_tile * ATTN_TILE, (q_tile + 1) * ATTN_TILE) ∩ [0, S)
+ *                   (for ATTN_WORK_GLOBAL_ROWS items: rows G[q_tile * ATTN_TILE + r])
+ *   [2] kv_begin    first key tile evaluated (keys [kv * ATTN_TILE, ...))
+ *   [3] kv_end      one past the last key tile evaluated
+ *   [4] full_begin  key tiles in [full_begin, full_end) are FULL: every pair is
+ *   [5] full_end    allowed and no mask is applied; the other tiles of
+ *                   [kv_begin, kv_end) are PARTIAL and evaluate the mask predicate
+ *   [6] flags       ATTN_WORK_GLOBAL_COLS: after the key tiles, also evaluate
+ *                   the gathered global keys G not inside [kv_begin, kv_end) tiles;
+ *                   ATTN_WORK_GLOBAL_ROWS: the item's rows are the global rows
+ *   [7] n_gtiles    number of gathered global-key tiles (ATTN_WORK_GLOBAL_COLS)
+ * Items are ordered by decreasing number of tiles (longest first).
+ * For LOCAL_GLOBAL, rows in G are computed only by ATTN_WORK_GLOBAL_ROWS items,
+ * which run after all other items.
+ */
+#define ATTN_TILE 128
+#define ATTN_WORK_INTS 8
+#define ATTN_WORK_GLOBAL_COLS 1
+#define ATTN_WORK_GLOBAL_ROWS 2
+
+/*
+ * attn_schedule_host -- build the schedule attn_create would build for these
+ * arguments, on the host only (no CUDA call; usable without a GPU).
+ *   Arguments B .. n_global: as for attn_create (validated the same way).
+ *   items   : output, room for `cap` items (cap * ATTN_WORK_INTS ints); may be
+ *             NULL with cap = 0 to query the sizes only.
+ *   n_items : receives the total number of items.
+ *   n_first : receives the number of items of the first launch; the remaining
+ *             items (ATTN_WORK_GLOBAL_ROWS) form a second launch.
+ * Returns ATTN_ERR_INVALID_ARG if cap is nonzero but smaller than the total.
+ */
+attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window,
+                               const int* global_idx, int n_global, int* items, int cap,
+                               int* n_items, int* n_first);
+
+/*
+ * attn_poll_device_error -- synchronise the device, read the handle's device
+ * error word into *code (0 = none, otherwise a bit set of the role whose
+ * bounded wait ran out), clear it, and return ATTN_ERR_DEVICE_TIMEOUT if it
+ * was nonzero.
+ */
+attn_status attn_poll_device_error(attn_handle h, int* code);
+
+/*
+ * attn_set_watchdog -- test hook for the failure-detection path.
+ *   limit_ns : wall-clock limit of every bounded wait inside the kernels
+ *              (default 2e9 ns).
+ *   withhold : 0 = normal; 1 = the producer of the tensor-core kernel never
+ *              loads V, so the first wait for V runs out: the kernel records
+ *              ATTN_ERR_DEVICE_TIMEOUT in the error word, releases its tensor
+ *              memory and returns (output contents are then undefined).
+ */
+attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_ATTN_H */

@@ -1,0 +1,133 @@
+"""CUDA path vs the fp64 oracle, element by element (GPU).
+
+Small shapes compare every output; the five full-size workloads run in the
+launch configuration bench.py times and compare sampled rows, plus
+properties that hold at any size (finite everywhere, every output row a convex
+combination of value rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import compare, oracle_rows, run_cuda, sample_rows, small
+
+pytestmark = pytest.mark.gpu
+
+K_ALL = (wl.MASK_FULL, wl.MASK_CAUSAL, wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING, wl.MASK_LOCAL_GLOBAL)
+
+
+def _full_compare(w):
+    Qc, Kc, Vc = wl.make_inputs(w)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    bb, aa, ii = np.meshgrid(np.arange(w.B), np.arange(w.Hq), np.arange(w.S), indexing="ij")
+    rows = np.stack([bb.ravel(), aa.ravel(), ii.ravel()], axis=1)
+    O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, rows)
+    return compare(w, O.float().cpu().numpy().reshape(-1, w.d), LSE.cpu().numpy().ravel(), O_ref, L_ref)
+
+
+# ------------------------------------------------------------------ small shapes, every output
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 300])
+@pytest.mark.parametrize("kind", K_ALL)
+def test_bf16_d128_kinds_and_ragged_lengths(kind, S):
+    G = sorted({0, S // 2, S - 1}) if kind == wl.MASK_LOCAL_GLOBAL else ()
+    _full_compare(small("s", 1, 2, 2, S, 128, "bf16", kind, window=37, globals_idx=G))
+
+
+@pytest.mark.parametrize("Hkv", [1, 2, 8])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_gqa_and_mqa(Hkv, d):
+    _full_compare(small("g", 2, 8, Hkv, 257, d, "bf16", wl.MASK_CAUSAL))
+
+
+@pytest.mark.parametrize("w_", [0, 1, 127, 128, 129, 255])
+@pytest.mark.parametrize("kind", [wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING])
+def test_bf16_windows_straddling_tile_edges(kind, w_):
+    _full_compare(small("w", 1, 2, 1, 520, 64, "bf16", kind, window=w_))
+
+
+@pytest.mark.parametrize("G", [[0], [519], [127, 128], [0, 1, 2, 3, 255, 256, 400], list(range(0, 520, 5))])
+def test_bf16_local_global_placements(G):
+    _full_compare(small("lg", 1, 3, 3, 520, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G))
+
+
+def test_bf16_local_global_many_globals():
+    """More than one gathered tile of global tokens (129 globals)."""
+    _full_compare(small("lg2", 1, 2, 1, 700, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=9,
+                        globals_idx=list(range(3, 700, 5))[:129]))
+
+
+@pytest.mark.parametrize("kind", K_ALL)
+@pytest.mark.parametrize("S", [1, 100, 257])
+def test_f32_path_kinds(kind, S):
+    G = sorted({0, S - 1}) if kind == wl.MASK_LOCAL_GLOBAL else ()
+    _full_compare(small("f", 1, 4, 2, S, 64, "f32", kind, window=19, globals_idx=G))
+
+
+def test_f32_d128():
+    _full_compare(small("f128", 2, 2, 1, 200, 128, "f32", wl.MASK_CAUSAL))
+
+
+def test_window_zero_returns_own_value_row():
+    """w = 0: each row sees only itself, so O_i = v_i and LSE_i = s_ii."""
+    w = small("w0", 1, 2, 2, 300, 128, "bf16", wl.MASK_SLIDING, window=0)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    assert torch.equal(O.cpu(), Vc)
+    s_ii = (Qc.double() * Kc.double()).sum(-1) * w.scale
+    assert torch.allclose(LSE.cpu().double(), s_ii, atol=1e-3)
+
+
+def test_sharp_softmax_triggers_rescale():
+    """Scores growing along the row force the lazy O rescale on many tiles."""
+    w = small("sharp", 1, 2, 2, 1024, 128, "bf16", wl.MASK_CAUSAL)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    ramp = torch.linspace(0, 6, w.S).view(1, 1, w.S, 1)
+    Kc = (Kc.float() + ramp * Qc.float().mean(dim=2, keepdim=True).sign()).to(torch.bfloat16)
+    Qc = (Qc.float() * 3).to(torch.bfloat16)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    bb, aa, ii = np.meshgrid(np.arange(w.B), np.arange(w.Hq), np.arange(w.S), indexing="ij")
+    rows = np.stack([bb.ravel(), aa.ravel(), ii.ravel()], axis=1)
+    O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, rows)
+    compare(w, O.float().cpu().numpy().reshape(-1, w.d), LSE.cpu().numpy().ravel(), O_ref, L_ref)
+
+
+def test_handle_reuse_and_distinct_buffers():
+    w = small("reuse", 1, 4, 2, 384, 128, "bf16", wl.MASK_CAUSAL)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    O1, L1, plan = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    w2 = w.with_(seed=99)
+    Q2, K2, V2 = wl.make_inputs(w2)
+    O2, L2, _ = run_cuda(w2, Q2.cuda(), K2.cuda(), V2.cuda(), plan=plan)
+    O1b, L1b, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), plan=plan)
+    assert torch.equal(O1, O1b) and torch.equal(L1, L1b)
+    assert not torch.equal(O1, O2)
+
+
+# ------------------------------------------------------------------ the five workloads
+
+def test_tiny_full_f32_every_output():
+    _full_compare(wl.TINY_FULL_F32)
+
+
+@pytest.mark.parametrize("w", [wl.CAUSAL_MHA_4K, wl.SWA_GQA_16K, wl.LONGFORMER_8K, wl.CAUSAL_GQA_32K],
+                         ids=lambda w: w.name)
+def test_full_size_workload_sampled_rows(w):
+    Qc, Kc, Vc = wl.make_inputs(w)
+    Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
+    O, LSE, _ = run_cuda(w, Q, K, V)
+    # properties at full size: every output finite and inside the per-column value range of its kv head
+    assert bool(torch.isfinite(O).all()) and bool(torch.isfinite(LSE).all())
+    g = w.Hq // w.Hkv
+    vmax = V.float().amax(dim=2).repeat_interleave(g, dim=1)  # [B, Hq, d]
+    vmin = V.float().amin(dim=2).repeat_interleave(g, dim=1)
+    assert bool((O.float() <= vmax[:, :, None, :] + 2e-2).all())
+    assert bool((O.float() >= vmin[:, :, None, :] - 2e-2).all())
+    # sampled rows against the oracle
+    rows = sample_rows(w)
+    O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, rows)
+    r = torch.as_tensor(rows, device=O.device)
+    O_s = O[r[:, 0], r[:, 1], r[:, 2]].float().cpu().numpy()
+    L_s = LSE[r[:, 0], r[:, 1], r[:, 2]].cpu().numpy()
+    compare(w, O_s, L_s, O_ref, L_ref)

@@ -1,0 +1,155 @@
+"""The host tile schedule against brute force from the oracle's mask predicate (bit-exact).
+
+For every listed key tile the schedule's class (FULL / PARTIAL) must equal the
+oracle's enumerated class; unlisted tiles must be SKIP (for local + global: hold
+no allowed pair outside the global rows and columns); and simulating what the
+kernels evaluate from the work items -- FULL tiles whole, PARTIAL tiles through
+the in-tile predicate, gathered global keys, the dense global-row pass -- must
+count exactly the allowed pairs of every row, each once.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import transformer_self_attention_gb300 as tsa
+import workloads as wl
+
+T = tsa.TILE
+
+
+def _kernel_interval(kind, i, S, w):
+    """The per-row key interval the kernels use on PARTIAL tiles (before global columns)."""
+    lo = np.zeros_like(i)
+    hi = np.full_like(i, S - 1)
+    if kind == tsa.MASK_CAUSAL:
+        hi = i.copy()
+    elif kind == tsa.MASK_CAUSAL_SLIDING:
+        lo, hi = i - w, i.copy()
+    elif kind in (tsa.MASK_SLIDING, tsa.MASK_LOCAL_GLOBAL):
+        lo, hi = i - w, i + w
+    return lo, np.minimum(hi, S - 1)
+
+
+def _simulate(items, n_first, kind, S, w, G, check_classes=True):
+    """Per-row count of the pairs the kernels evaluate as allowed, for batch-head 0."""
+    isg = np.zeros(S, dtype=bool)
+    isg[list(G)] = True
+    Garr = np.array(sorted(G), dtype=np.int64)
+    counts = np.zeros(S, dtype=np.int64)
+    classes = oracle.tile_classes(kind, S, w, list(G)) if check_classes else None
+    lg = kind == tsa.MASK_LOCAL_GLOBAL
+    seen_tiles = set()
+    for n, it in enumerate(items):
+        bh, qt, kb, ke, fb, fe, flags, ngt = (int(x) for x in it)
+        if bh != 0:
+            continue
+        if flags & tsa.WORK_GLOBAL_ROWS:
+            assert n >= n_first
+            rows = Garr[qt * T:(qt + 1) * T]
+            assert kb == 0 and ke == (S + T - 1) // T
+            counts[rows] += S
+            continue
+        assert n < n_first
+        assert (qt not in seen_tiles), "query tile listed twice"
+        seen_tiles.add(qt)
+        i = np.arange(qt * T, min(S, (qt + 1) * T))
+        lo, hi = _kernel_interval(kind, i, S, w)
+        keep = ~isg[i] if lg else np.ones(i.size, dtype=bool)
+        assert kb <= fb <= fe <= ke
+        for t in range(kb, ke):
+            j = np.arange(t * T, min(S, (t + 1) * T))
+            full = fb <= t < fe
+            if check_classes:
+                assert classes[qt, t] == (1 if full else 2), (qt, t, classes[qt, t], full)
+            if full:
+                counts[i[keep]] += j.size
+            else:
+                ok = ((j[None, :] >= lo[:, None]) & (j[None, :] <= hi[:, None]))
+                if lg:
+                    ok |= isg[j][None, :]
+                counts[i[keep]] += ok[keep].sum(axis=1)
+        if check_classes and not lg:
+            for t in set(range(classes.shape[1])) - set(range(kb, ke)):
+                assert classes[qt, t] == 0, (qt, t)
+        if flags & tsa.WORK_GLOBAL_COLS:
+            assert lg and ngt == (len(G) + T - 1) // T
+            outside = (Garr < kb * T) | (Garr >= ke * T)
+            counts[i[keep]] += int(outside.sum())
+    assert seen_tiles == set(range((S + T - 1) // T))
+    return counts
+
+
+def _check(kind, S, w=0, G=(), B=1, Hq=2, Hkv=1, check_classes=True):
+    items, n_first = tsa.attn_schedule_host(B, Hq, Hkv, S, kind, w, list(G))
+    nq = (S + T - 1) // T
+    n_grows = B * Hq * ((len(G) + T - 1) // T) if (kind == tsa.MASK_LOCAL_GLOBAL and G) else 0
+    assert len(items) == B * Hq * nq + n_grows and n_first == B * Hq * nq
+    # every (bh, q_tile) exactly once among the first-launch items
+    pairs = {(int(a), int(b)) for a, b in items[:n_first, :2]}
+    assert pairs == {(bh, q) for bh in range(B * Hq) for q in range(nq)}
+    # longest first
+    cost = (items[:n_first, 3] - items[:n_first, 2]) + items[:n_first, 7]
+    assert np.all(np.diff(cost) <= 0)
+    counts = _simulate(items, n_first, kind, S, w, set(G), check_classes)
+    expect = oracle.row_counts(kind, S, w, list(G))
+    assert np.array_equal(counts, expect)
+
+
+SWEEP_S = [1, 2, 127, 128, 129, 300, 515]
+
+
+@pytest.mark.parametrize("S", SWEEP_S)
+@pytest.mark.parametrize("kind", [tsa.MASK_FULL, tsa.MASK_CAUSAL])
+def test_schedule_dense_kinds(kind, S):
+    _check(kind, S)
+
+
+@pytest.mark.parametrize("S", SWEEP_S)
+@pytest.mark.parametrize("w", [0, 1, 3, 127, 128, 129, 200, 600])
+@pytest.mark.parametrize("kind", [tsa.MASK_SLIDING, tsa.MASK_CAUSAL_SLIDING])
+def test_schedule_window_kinds(kind, S, w):
+    _check(kind, S, w)
+
+
+@pytest.mark.parametrize("S,w,G", [
+    (1, 0, [0]), (129, 3, [0]), (129, 3, [128]), (300, 5, [0, 127, 128, 299]), (300, 0, []),
+    (515, 60, [3, 4, 5, 200, 511, 514]), (515, 300, [0, 100]), (700, 1, list(range(0, 700, 3))),
+    (1000, 128, [127, 128, 255, 256, 999]),
+])
+def test_schedule_local_global(S, w, G):
+    _check(tsa.MASK_LOCAL_GLOBAL, S, w, G)
+
+
+@pytest.mark.parametrize("w", [wl.TINY_FULL_F32, wl.CAUSAL_MHA_4K, wl.SWA_GQA_16K, wl.LONGFORMER_8K],
+                         ids=lambda w: w.name)
+def test_schedule_workloads(w):
+    _check(w.kind, w.S, w.window, w.globals_idx, B=1, Hq=2, Hkv=1)
+
+
+def test_schedule_long_causal_classes():
+    """The 32K causal workload: classes only (the coverage follows for interval masks)."""
+    w = wl.CAUSAL_GQA_32K
+    items, n_first = tsa.attn_schedule_host(1, 1, 1, w.S, w.kind, 0, [])
+    classes = oracle.tile_classes(w.kind, w.S, 0, [])
+    got = np.zeros_like(classes)
+    for it in items:
+        _, qt, kb, ke, fb, fe, _, _ = (int(x) for x in it)
+        for t in range(kb, ke):
+            got[qt, t] = 1 if fb <= t < fe else 2
+    assert np.array_equal(got, classes)
+
+
+def test_schedule_heads_and_batches():
+    items, n_first = tsa.attn_schedule_host(3, 8, 2, 300, tsa.MASK_CAUSAL, 0, [])
+    per_bh = {}
+    for it in items:
+        per_bh.setdefault(int(it[0]), []).append(tuple(int(x) for x in it[1:]))
+    ref = sorted(per_bh[0])
+    assert sorted(per_bh) == list(range(24))
+    assert all(sorted(v) == ref for v in per_bh.values())
+
+
+def test_duplicate_globals_are_removed():
+    a, _ = tsa.attn_schedule_host(1, 1, 1, 300, tsa.MASK_LOCAL_GLOBAL, 5, [7, 7, 250, 7])
+    b, _ = tsa.attn_schedule_host(1, 1, 1, 300, tsa.MASK_LOCAL_GLOBAL, 5, [7, 250])
+    assert np.array_equal(a, b)

@@ -1,0 +1,181 @@
+"""GB300 (sm_103a) self-attention forward: Python binding of libattn.so.
+
+Argument marshalling only.  Every step of the forward pass runs in the CUDA
+kernels of libattn.so; there is no CPU or PyTorch fallback.  If the library is
+missing (not built), importing this module raises.
+
+Low-level functions mirror the C ABI of ``include/attn.h`` (same names, integer
+pointers); :class:`Attention` wraps a handle for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_OOM = range(6)
+MASK_FULL, MASK_CAUSAL, MASK_SLIDING, MASK_CAUSAL_SLIDING, MASK_LOCAL_GLOBAL = range(5)
+ATTN_BF16, ATTN_F32 = 0, 1
+TILE = 128
+WORK_INTS = 8
+WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
+
+EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
+            "attn_poll_device_error", "attn_set_watchdog")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libattn.so not built at {LIB_PATH}; run __graft_entry__.build() "
+                          "(the library has no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    I, P, F, LL = ctypes.c_int, ctypes.c_void_p, ctypes.c_float, ctypes.c_longlong
+    lib.attn_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I, F, I, I, P, I]
+    lib.attn_create.restype = I
+    lib.attn_forward.argtypes = [P, P, P, P, P, P, P]
+    lib.attn_forward.restype = I
+    lib.attn_destroy.argtypes = [P]
+    lib.attn_destroy.restype = I
+    lib.attn_status_string.argtypes = [I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_schedule_host.argtypes = [I, I, I, I, I, I, P, I, P, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+    lib.attn_schedule_host.restype = I
+    lib.attn_poll_device_error.argtypes = [P, ctypes.POINTER(I)]
+    lib.attn_poll_device_error.restype = I
+    lib.attn_set_watchdog.argtypes = [P, LL, I]
+    lib.attn_set_watchdog.restype = I
+    return lib
+
+
+_lib = _load()
+
+
+def _int_array(xs: Optional[Sequence[int]]):
+    xs = list(xs or [])
+    arr = (ctypes.c_int * max(len(xs), 1))(*xs)
+    return arr, len(xs)
+
+
+# ---------------------------------------------------------------- C ABI, same names
+
+def attn_status_string(status: int) -> str:
+    return _lib.attn_status_string(int(status)).decode()
+
+
+def attn_create(B, Hq, Hkv, S, d_k, dtype, scale, kind, window=0, global_idx=None) -> int:
+    """Returns a handle (int); raises AttnError on a non-OK status."""
+    h = ctypes.c_void_p()
+    g, ng = _int_array(global_idx)
+    st = _lib.attn_create(ctypes.byref(h), int(B), int(Hq), int(Hkv), int(S), int(d_k), int(dtype),
+                          float(scale), int(kind), int(window), ctypes.cast(g, ctypes.c_void_p) if ng else None, ng)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_create")
+    return h.value
+
+
+def attn_forward(handle: int, q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int = 0,
+                 stream: int = 0) -> int:
+    """Enqueue the forward pass; returns the status (does not raise)."""
+    return _lib.attn_forward(handle, q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr or None, stream or None)
+
+
+def attn_destroy(handle: int) -> int:
+    return _lib.attn_destroy(handle)
+
+
+def attn_poll_device_error(handle: int):
+    code = ctypes.c_int(0)
+    st = _lib.attn_poll_device_error(handle, ctypes.byref(code))
+    return st, code.value
+
+
+def attn_set_watchdog(handle: int, limit_ns: int, withhold: int = 0) -> int:
+    return _lib.attn_set_watchdog(handle, int(limit_ns), int(withhold))
+
+
+def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):
+    """Host-only schedule: (items int32 [n, 8], n_first).  Raises AttnError on bad arguments."""
+    g, ng = _int_array(global_idx)
+    gp = ctypes.cast(g, ctypes.c_void_p) if ng else None
+    n, n_first = ctypes.c_int(0), ctypes.c_int(0)
+    st = _lib.attn_schedule_host(int(B), int(Hq), int(Hkv), int(S), int(kind), int(window), gp, ng, None, 0,
+                                 ctypes.byref(n), ctypes.byref(n_first))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_schedule_host")
+    items = np.zeros((max(n.value, 1), WORK_INTS), dtype=np.int32)
+    st = _lib.attn_schedule_host(int(B), int(Hq), int(Hkv), int(S), int(kind), int(window), gp, ng,
+                                 items.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n),
+                                 ctypes.byref(n_first))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_schedule_host")
+    return items[: n.value], n_first.value
+
+
+# ---------------------------------------------------------------- torch convenience
+
+class Attention:
+    """A plan (handle) for one problem shape; call with CUDA torch tensors.
+
+    Q: [B, Hq, S, d], K/V: [B, Hkv, S, d], contiguous, bf16 (or fp32 for dtype="f32").
+    Returns (O, LSE) with O like Q and LSE float32 [B, Hq, S].
+    """
+
+    def __init__(self, B, Hq, Hkv, S, d, dtype="bf16", scale=None, kind=MASK_CAUSAL, window=0,
+                 global_idx=None):
+        import math
+        self.shape = (int(B), int(Hq), int(Hkv), int(S), int(d))
+        self.dtype = dtype
+        self.scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+        self.kind, self.window = int(kind), int(window)
+        self.global_idx = list(global_idx or [])
+        self.handle = attn_create(B, Hq, Hkv, S, d, ATTN_BF16 if dtype == "bf16" else ATTN_F32, self.scale,
+                                  self.kind, self.window, self.global_idx)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            attn_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __call__(self, Q, K, V, O=None, LSE=None, stream=None, want_lse=True):
+        import torch
+        B, Hq, Hkv, S, d = self.shape
+        tdt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        for name, t, h in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv)):
+            if not t.is_cuda or t.dtype != tdt or not t.is_contiguous() or tuple(t.shape) != (B, h, S, d):
+                raise ValueError(f"{name} must be a contiguous CUDA {tdt} tensor of shape {(B, h, S, d)}")
+        if O is None:
+            O = torch.empty_like(Q)
+        if LSE is None and want_lse:
+            LSE = torch.empty((B, Hq, S), dtype=torch.float32, device=Q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(Q.device)
+        st = attn_forward(self.handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                          LSE.data_ptr() if LSE is not None else 0, stream.cuda_stream)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_forward")
+        return O, LSE
+
+    def poll_device_error(self):
+        return attn_poll_device_error(self.handle)
+
+    def set_watchdog(self, limit_ns: int, withhold: int = 0):
+        st = attn_set_watchdog(self.handle, limit_ns, withhold)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_set_watchdog")

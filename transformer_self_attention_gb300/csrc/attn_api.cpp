@@ -1,0 +1,312 @@
+// Host implementation of the C ABI declared in include/attn.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "attn.h"
+#include "kernels.h"
+#include "schedule.h"
+
+struct attn_plan {
+    int B = 0, Hq = 0, Hkv = 0, S = 0, d = 0;
+    attn_dtype dtype = ATTN_BF16;
+    float scale = 0.f;
+    int kind = 0, window = 0;
+    std::vector<int> globals;
+    attn::Schedule sched;
+    // device buffers owned by the handle
+    int4* d_work = nullptr;
+    int* d_globals = nullptr;
+    unsigned* d_gbits = nullptr;
+    unsigned char* d_isg = nullptr;
+    int* d_err = nullptr;
+    void* d_qg = nullptr;
+    void* d_kg = nullptr;
+    void* d_vg = nullptr;
+    // tensor maps of the last pointers seen (re-encoded when they change)
+    const void* last_q = nullptr;
+    const void* last_k = nullptr;
+    const void* last_v = nullptr;
+    const void* last_o = nullptr;
+    attn::TcParams tp{};
+    bool debug = false;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 3-D bf16 map over [heads, rows, d] (d fastest), box {64, 128, 1}, 128-byte
+// swizzle; rows past `rows` read as zeros and are not written by stores.
+bool encode_map(CUtensorMap* map, const void* base, int d, long rows, long heads) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    cuuint32_t box[3] = {64, ATTN_TILE, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by attn_create and attn_schedule_host.
+attn_status validate_shape(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window, const int* global_idx,
+                           int n_global) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || S < 1 || S > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+    if ((int)kind < ATTN_MASK_FULL || (int)kind > ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_INVALID_ARG;
+    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
+                          kind == ATTN_MASK_LOCAL_GLOBAL;
+    if (windowed && window < 0) return ATTN_ERR_INVALID_ARG;
+    if (n_global < 0 || n_global > 4096) return ATTN_ERR_INVALID_ARG;
+    if (n_global > 0 && (kind != ATTN_MASK_LOCAL_GLOBAL || !global_idx)) return ATTN_ERR_INVALID_ARG;
+    for (int t = 0; t < n_global; ++t)
+        if (global_idx[t] < 0 || global_idx[t] >= S) return ATTN_ERR_INVALID_ARG;
+    if ((long)B * Hq > (1L << 30)) return ATTN_ERR_UNSUPPORTED;
+    if (n_global > 0 && (long)B * Hq + 2L * B * Hkv > 65535L) return ATTN_ERR_UNSUPPORTED;  // gather grid.y
+    return ATTN_OK;
+}
+
+std::vector<int> sorted_unique(const int* idx, int n) {
+    std::vector<int> g(idx, idx + n);
+    std::sort(g.begin(), g.end());
+    g.erase(std::unique(g.begin(), g.end()), g.end());
+    return g;
+}
+
+template <class T>
+cudaError_t upload(T** dst, const T* src, size_t n) {
+    if (n == 0) return cudaSuccess;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(dst), n * sizeof(T));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(*dst, src, n * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+void free_plan(attn_plan* h) {
+    if (!h) return;
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg};
+    for (void* b : bufs)
+        if (b) cudaFree(b);
+    delete h;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+    switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "device watchdog: a bounded wait ran out";
+    case ATTN_ERR_OOM: return "out of memory";
+    }
+    return "unknown status";
+}
+
+attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k, attn_dtype dtype, float scale,
+                        attn_mask_kind kind, int window, const int* global_idx, int n_global) {
+    if (!out) return ATTN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, global_idx, n_global);
+    if (vs != ATTN_OK) return vs;
+    if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
+                          kind == ATTN_MASK_LOCAL_GLOBAL;
+
+    attn_plan* h = new (std::nothrow) attn_plan();
+    if (!h) return ATTN_ERR_OOM;
+    h->B = B; h->Hq = Hq; h->Hkv = Hkv; h->S = S; h->d = d_k; h->dtype = dtype; h->scale = scale;
+    h->kind = kind; h->window = windowed ? window : 0;
+    h->globals = sorted_unique(global_idx, n_global);
+    const char* dbg = std::getenv("ATTN_DEBUG");
+    h->debug = dbg && dbg[0] == '1';
+
+    attn::ScheduleInput in{B, Hq, Hkv, S, (int)kind, h->window, h->globals};
+    attn_status st = attn::build_schedule(in, &h->sched);
+    if (st != ATTN_OK) { free_plan(h); return st; }
+
+    const int nG = (int)h->globals.size();
+    cudaError_t e = cudaSuccess;
+    auto fail = [&](cudaError_t err) {
+        free_plan(h);
+        return err == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
+    };
+    if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(int))) != cudaSuccess) return fail(e);
+    if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess) return fail(e);
+    if (nG > 0) {
+        if ((e = upload(&h->d_globals, h->globals.data(), h->globals.size())) != cudaSuccess) return fail(e);
+        std::vector<unsigned char> isg(S, 0);
+        for (int g : h->globals) isg[g] = 1;
+        if ((e = upload(&h->d_isg, isg.data(), isg.size())) != cudaSuccess) return fail(e);
+    }
+    if (dtype == ATTN_BF16) {
+        if ((e = upload(reinterpret_cast<int**>(&h->d_work), h->sched.items.data(), h->sched.items.size())) !=
+            cudaSuccess)
+            return fail(e);
+        if ((e = upload(&h->d_gbits, h->sched.global_bits.data(), h->sched.global_bits.size())) != cudaSuccess)
+            return fail(e);
+        attn::TcParams& p = h->tp;
+        if (nG > 0) {
+            const size_t qg = (size_t)B * Hq * nG * d_k * 2, kg = (size_t)B * Hkv * nG * d_k * 2;
+            if ((e = cudaMalloc(&h->d_qg, qg)) != cudaSuccess) return fail(e);
+            if ((e = cudaMalloc(&h->d_kg, kg)) != cudaSuccess) return fail(e);
+            if ((e = cudaMalloc(&h->d_vg, kg)) != cudaSuccess) return fail(e);
+            if (!encode_map(&p.tm_qg, h->d_qg, d_k, nG, (long)B * Hq) ||
+                !encode_map(&p.tm_kg, h->d_kg, d_k, nG, (long)B * Hkv) ||
+                !encode_map(&p.tm_vg, h->d_vg, d_k, nG, (long)B * Hkv)) {
+                free_plan(h);
+                return ATTN_ERR_CUDA;
+            }
+        }
+        p.work = h->d_work;
+        p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;
+        p.kind = kind; p.window = h->window;
+        p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+        p.globals = h->d_globals;
+        p.n_global = nG;
+        p.global_bits = h->d_gbits;
+        p.err = h->d_err;
+        p.watchdog_ns = 2000000000LL;
+        p.withhold_v = 0;
+    }
+    *out = h;
+    return ATTN_OK;
+}
+
+attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         void* stream_ptr) {
+    if (!h || !Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    cudaError_t e = cudaSuccess;
+    const int nG = (int)h->globals.size();
+
+    if (h->dtype == ATTN_F32) {
+        attn::F32Params p{};
+        p.q = static_cast<const float*>(Q); p.k = static_cast<const float*>(K); p.v = static_cast<const float*>(V);
+        p.o = static_cast<float*>(O); p.lse = LSE;
+        p.B = h->B; p.Hq = h->Hq; p.Hkv = h->Hkv; p.S = h->S; p.group = h->Hq / h->Hkv;
+        p.kind = h->kind; p.window = h->window; p.scale = h->scale;
+        p.globals = h->d_globals; p.n_global = nG; p.is_global = h->d_isg;
+        e = attn::launch_f32_forward(p, h->d, stream);
+    } else {
+        attn::TcParams& p = h->tp;
+        if (Q != h->last_q) {
+            if (!encode_map(&p.tm_q, Q, h->d, h->S, (long)h->B * h->Hq)) return ATTN_ERR_CUDA;
+            h->last_q = Q;
+        }
+        if (K != h->last_k) {
+            if (!encode_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv)) return ATTN_ERR_CUDA;
+            h->last_k = K;
+        }
+        if (V != h->last_v) {
+            if (!encode_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv)) return ATTN_ERR_CUDA;
+            h->last_v = V;
+        }
+        if (O != h->last_o) {
+            if (!encode_map(&p.tm_o, O, h->d, h->S, (long)h->B * h->Hq)) return ATTN_ERR_CUDA;
+            h->last_o = O;
+        }
+        p.o = O;
+        p.lse = LSE;
+        if (nG > 0) {
+            attn::GatherParams g{};
+            g.q = static_cast<const uint16_t*>(Q); g.k = static_cast<const uint16_t*>(K);
+            g.v = static_cast<const uint16_t*>(V);
+            g.qg = static_cast<uint16_t*>(h->d_qg); g.kg = static_cast<uint16_t*>(h->d_kg);
+            g.vg = static_cast<uint16_t*>(h->d_vg);
+            g.globals = h->d_globals; g.n_global = nG;
+            g.BHq = h->B * h->Hq; g.BHkv = h->B * h->Hkv; g.S = h->S; g.d = h->d;
+            if ((e = attn::launch_gather_globals(g, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
+        p.item_offset = 0;
+        if ((e = attn::launch_tc_forward(p, h->d, h->sched.n_main, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (h->sched.n_grows > 0) {
+            p.item_offset = h->sched.n_main;
+            e = attn::launch_tc_forward(p, h->d, h->sched.n_grows, stream);
+        }
+    }
+    if (e != cudaSuccess) return ATTN_ERR_CUDA;
+    if (h->debug) {
+        int code = 0;
+        return attn_poll_device_error(h, &code);
+    }
+    return ATTN_OK;
+}
+
+attn_status attn_destroy(attn_handle h) {
+    if (!h) return ATTN_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_plan(h);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window,
+                               const int* global_idx, int n_global, int* items, int cap, int* n_items,
+                               int* n_first) {
+    if (!n_items || !n_first || cap < 0 || (cap > 0 && !items)) return ATTN_ERR_INVALID_ARG;
+    attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, global_idx, n_global);
+    if (vs != ATTN_OK) return vs;
+    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
+                          kind == ATTN_MASK_LOCAL_GLOBAL;
+    attn::ScheduleInput in{B, Hq, Hkv, S, (int)kind, windowed ? window : 0, sorted_unique(global_idx, n_global)};
+    attn::Schedule sched;
+    attn_status st = attn::build_schedule(in, &sched);
+    if (st != ATTN_OK) return st;
+    const int n = (int)(sched.items.size() / ATTN_WORK_INTS);
+    *n_items = n;
+    *n_first = sched.n_main;
+    if (cap == 0) return ATTN_OK;
+    if (cap < n) return ATTN_ERR_INVALID_ARG;
+    std::memcpy(items, sched.items.data(), sched.items.size() * sizeof(int));
+    return ATTN_OK;
+}
+
+attn_status attn_poll_device_error(attn_handle h, int* code) {
+    if (!h || !code) return ATTN_ERR_INVALID_ARG;
+    *code = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemcpy(code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (*code != 0 && cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return *code ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold) {
+    if (!h || limit_ns <= 0 || (withhold != 0 && withhold != 1)) return ATTN_ERR_INVALID_ARG;
+    h->tp.watchdog_ns = limit_ns;
+    h->tp.withhold_v = withhold;
+    return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,432 @@
+// Tensor-core attention forward for sm_103a (bf16 in, fp32 accumulation).
+//
+// One CTA computes one work item: 128 query rows of one (batch, query head)
+// against the key tiles the host schedule lists for them.  The pages' design
+// (tiling Q into blocks, streaming K/V blocks, keeping a running row max m and
+// sum l and writing only O back -- "Transformer 演进与变体" (ai.icyfenix.cn),
+// section Flash Attention; the m/l recurrence also in "Trasformer 浅析",
+// section 长序列的三条优化路线) is mapped onto Blackwell as follows:
+//
+//   warp 4 (producer) : TMA loads of the Q tile (once) and of every K and V
+//                       tile into 128B-swizzled shared memory.
+//   warp 5 (MMA)      : one thread issues tcgen05.mma: S = Q K^T into tensor
+//                       memory (fp32), then O += P V with P read from tensor
+//                       memory (bf16) and O accumulated in tensor memory.
+//   warps 0-3         : one thread per query row.  Load the row of S from
+//                       tensor memory, apply the mask on PARTIAL tiles, update
+//                       the running max/sum with exp2 on log2(e)-prescaled
+//                       scores, write P (bf16) back over S, and rescale the O
+//                       row only when the running max grew by more than 2^8
+//                       (the final division by l keeps the result exact).
+//                       Epilogue: O / l -> bf16 -> swizzled smem -> TMA store;
+//                       LSE = (m + log2 l) ln 2.
+//
+// Tensor memory: S/P in columns [0, 128), O in [128, 128 + d); 256 columns per
+// CTA, so two CTAs share an SM and one's softmax overlaps the other's MMAs.
+// Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
+// out records an error bit, raises a CTA-wide abort flag and the CTA drains
+// its in-flight copies and MMAs (again bounded), frees tensor memory and exits.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm103_ptx.h"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;            // query rows per CTA
+constexpr int BN = 128;            // keys per tile
+constexpr int NTHREADS = 192;      // 4 softmax warps + producer + MMA
+constexpr int WARP_PRODUCER = 4;
+constexpr int WARP_MMA = 5;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the max grew by > 2^8
+
+enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
+
+template <int D>
+struct Cfg {
+    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 64-column swizzled block
+    static constexpr int NSUB = D / 64;           // 64-column blocks per row
+    static constexpr int TILE_BYTES = BM * D * 2; // one Q / K / V tile
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_V + TILE_BYTES;
+    static constexpr int SMEM_USED = OFF_BAR + 128;
+    // at least ~80 KB so no more than two CTAs share an SM (tensor memory holds two)
+    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > 82 * 1024) ? SMEM_USED + 1024 : 82 * 1024;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t TMEM_S = 0;
+    static constexpr uint32_t TMEM_O = 128;
+};
+
+enum Bar { B_Q = 0, B_KFULL, B_KEMPTY, B_VFULL, B_VEMPTY, B_SFULL, B_PFULL, B_OFULL, NBAR };
+
+struct Shared {  // small control block after the tiles
+    uint64_t bar[NBAR];
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+// Bounded wait: polls the barrier; every 128 polls checks the CTA abort flag
+// and the wall clock.  Returns false (after raising the abort flag and the
+// error bit) if the limit ran out or another role aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Shared* sh, const TcParams& p,
+                                             int role) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 127u) == 0) {
+            if (sh->abort) return false;
+            if ((long long)(globaltimer() - t0) > p.watchdog_ns) {
+                sh->abort = 1;
+                atomicOr(p.err, role);
+                return false;
+            }
+        }
+    }
+}
+
+// Drain wait used after an abort: no abort check, only the clock.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const TcParams& p) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if ((long long)(globaltimer() - t0) > p.watchdog_ns) return;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared* sh = reinterpret_cast<Shared*>(smem + C::OFF_BAR);
+    const uint32_t s_q = smem_u32(smem + C::OFF_Q);
+    const uint32_t s_k = smem_u32(smem + C::OFF_K);
+    const uint32_t s_v = smem_u32(smem + C::OFF_V);
+    auto bar = [&](int b) { return smem_u32(&sh->bar[b]); };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int item = p.item_offset + blockIdx.x;
+    const int4 w0 = p.work[2 * item];
+    const int4 w1 = p.work[2 * item + 1];
+    const int bh = w0.x, q_tile = w0.y, kv_begin = w0.z, kv_end = w0.w;
+    const int full_begin = w1.x, full_end = w1.y, flags = w1.z, n_gt = w1.w;
+    const bool grows = (flags & ATTN_WORK_GLOBAL_ROWS) != 0;
+    const int n_band = kv_end - kv_begin;
+    const int n_iter = n_band + ((flags & ATTN_WORK_GLOBAL_COLS) ? n_gt : 0);
+    const int b = bh / p.Hq, a = bh - b * p.Hq;
+    const int bkv = b * p.Hkv + a / p.group;  // g(a) = a / (Hq / Hkv)
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), i == B_PFULL ? 128u : 1u);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == WARP_PRODUCER && lane == 0) {
+        prefetch_tmap(grows ? &p.tm_qg : &p.tm_q);
+        prefetch_tmap(&p.tm_k);
+        prefetch_tmap(&p.tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == WARP_PRODUCER) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const CUtensorMap* qmap = grows ? &p.tm_qg : &p.tm_q;
+            mbar_arrive_expect_tx(bar(B_Q), C::TILE_BYTES);
+            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * 64, q_tile * BM, bh);
+            int k_loaded = 0, v_loaded = 0;
+            bool ok = true;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const bool in_band = it < n_band;
+                const CUtensorMap* km = in_band ? &p.tm_k : &p.tm_kg;
+                const CUtensorMap* vm = in_band ? &p.tm_v : &p.tm_vg;
+                const int row = in_band ? (kv_begin + it) * BN : (it - n_band) * BN;
+                if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
+                mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * 64, row, bkv);
+                ++k_loaded;
+                if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
+                if (p.withhold_v) continue;
+                mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * 64, row, bkv);
+                ++v_loaded;
+            }
+            if (sh->abort) {  // let the copies this thread issued land before the CTA exits
+                drain_wait(bar(B_Q), 0, p);
+                if (k_loaded) drain_wait(bar(B_KFULL), (k_loaded - 1) & 1, p);
+                if (v_loaded) drain_wait(bar(B_VFULL), (v_loaded - 1) & 1, p);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+            const uint32_t t_s = tmem + C::TMEM_S, t_o = tmem + C::TMEM_O;
+            int last_bar = -1, last_par = 0;
+            bool ok = wait_bounded(bar(B_Q), 0, sh, p, ERR_MMA);
+            for (int it = 0; it < n_iter && ok; ++it) {
+                if (!(ok = wait_bounded(bar(B_KFULL), it & 1, sh, p, ERR_MMA))) break;
+                // S/P share tensor columns: PV(it-1) must have consumed P before S is overwritten
+                if (it > 0 && !(ok = wait_bounded(bar(B_OFULL), (it - 1) & 1, sh, p, ERR_MMA))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
+                           k > 0);
+                }
+                mma_commit(bar(B_SFULL));
+                mma_commit(bar(B_KEMPTY));
+                last_bar = B_KEMPTY; last_par = it & 1;
+                if (!(ok = wait_bounded(bar(B_PFULL), it & 1, sh, p, ERR_MMA))) break;
+                if (!(ok = wait_bounded(bar(B_VFULL), it & 1, sh, p, ERR_MMA))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    // P: 16 keys = 8 packed bf16x2 columns; V: 16 key rows of 128 B each
+                    mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * 16 * 128, C::SUB, 1024), idesc_pv,
+                           (it > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar(B_OFULL));
+                mma_commit(bar(B_VEMPTY));
+                last_bar = B_VEMPTY; last_par = it & 1;
+            }
+            if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, p);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int r = threadIdx.x;  // row within the tile == tensor-memory lane
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_s = t_lane + C::TMEM_S, t_o = t_lane + C::TMEM_O;
+        // global position of this thread's query row
+        long i;
+        bool row_valid;
+        if (grows) {
+            const int gr = q_tile * BM + r;
+            row_valid = gr < p.n_global;
+            i = row_valid ? p.globals[gr] : 0;
+        } else {
+            i = (long)q_tile * BM + r;
+            row_valid = i < p.S;
+        }
+        // allowed key interval of this row for the window part of the mask
+        long lo = 0, hi = p.S - 1;
+        if (!grows) {
+            if (p.kind == ATTN_MASK_CAUSAL) hi = i;
+            else if (p.kind == ATTN_MASK_CAUSAL_SLIDING) { lo = i - p.window; hi = i; }
+            else if (p.kind == ATTN_MASK_SLIDING || p.kind == ATTN_MASK_LOCAL_GLOBAL) { lo = i - p.window; hi = i + p.window; }
+            if (hi > p.S - 1) hi = p.S - 1;
+        }
+        const bool lg = (p.kind == ATTN_MASK_LOCAL_GLOBAL) && !grows;
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int it = 0; it < n_iter; ++it) {
+            // warp-uniform exit: the tensor-memory accesses below are warp-collective
+            if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // ---- mask of this tile: allowed in-tile columns are [a0, a1] plus set bits of gb
+            bool partial = true;
+            long a0 = 0, a1 = -1;
+            uint32_t gb[4] = {0u, 0u, 0u, 0u};
+            if (it < n_band) {
+                const int t = kv_begin + it;
+                partial = t < full_begin || t >= full_end;
+                if (partial) {
+                    a0 = lo - (long)t * BN;
+                    a1 = hi - (long)t * BN;
+                    if (lg) {
+                        const uint4 g4 = *reinterpret_cast<const uint4*>(p.global_bits + 4 * t);
+                        gb[0] = g4.x; gb[1] = g4.y; gb[2] = g4.z; gb[3] = g4.w;
+                    }
+                }
+            } else {
+                // gathered global keys: allowed when outside this item's key tiles
+                const int g0 = (it - n_band) * BN;
+                const long band_lo = (long)kv_begin * BN, band_hi = (long)kv_end * BN;
+                for (int c = 0; c < BN; ++c) {
+                    const int gi = g0 + c;
+                    if (gi < p.n_global) {
+                        const long gpos = __ldg(p.globals + gi);
+                        if (gpos < band_lo || gpos >= band_hi) gb[c >> 5] |= 1u << (c & 31);
+                    }
+                }
+            }
+            auto score = [&](uint32_t raw, int c) -> float {
+                if (partial && !((c >= a0 && c <= a1) || ((gb[c >> 5] >> (c & 31)) & 1u))) return -INFINITY;
+                return __uint_as_float(raw);
+            };
+            // ---- pass 1: row max of the (masked) scores
+            float mx = -INFINITY;
+            {
+                uint32_t raw[32];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    tmem_ld32(t_s + c * 32, raw);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, score(raw[e], c * 32 + e));
+                }
+            }
+            // ---- running max, with the lazy rescale
+            mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
+            const bool grow = mx > m + RESCALE_THRESHOLD;  // false when mx is -inf; true on the first finite max
+            const float m_new = grow ? mx : m;
+            const float alpha = grow ? ex2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first finite max
+            const bool fix_o = grow && it > 0 && m != -INFINITY;
+            if (__any_sync(0xffffffffu, fix_o)) {
+                uint32_t o[32];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+                    const float f = fix_o ? alpha : 1.f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tmem_st32(t_o + c * 32, o);
+                }
+            }
+            l *= alpha;
+            m = m_new;
+            const float ref = (m == -INFINITY) ? 0.f : m;
+            // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P written over the S columns.
+            // Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
+            // [32h, 32h+32), which only overlap S columns this thread has already read.
+            float sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r0[32], r1[32], pk[32];
+                tmem_ld32(t_s + h * 64, r0);
+                tmem_ld32(t_s + h * 64 + 32, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ex2(fmaf(score(r0[2 * e], h * 64 + 2 * e), sl2, -ref));
+                    const float p1 = ex2(fmaf(score(r0[2 * e + 1], h * 64 + 2 * e + 1), sl2, -ref));
+                    const float p2 = ex2(fmaf(score(r1[2 * e], h * 64 + 32 + 2 * e), sl2, -ref));
+                    const float p3 = ex2(fmaf(score(r1[2 * e + 1], h * 64 + 33 + 2 * e), sl2, -ref));
+                    sum += (p0 + p1) + (p2 + p3);
+                    pk[e] = pack_bf16x2(p0, p1);
+                    pk[16 + e] = pack_bf16x2(p2, p3);
+                }
+                tmem_st32(t_s + h * 32, pk);
+            }
+            l += sum;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_PFULL));
+        }
+        // ---- epilogue
+        if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(B_OFULL), (n_iter - 1) & 1, sh, p, ERR_SOFTMAX));
+        tc_fence_after();
+        ok = named_bar_and(1, 128, ok);  // the same decision in all four softmax warps
+        if (ok) {
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (!grows) {
+                // O row -> bf16 -> 128B-swizzled staging in the (now idle) Q buffer -> TMA store
+                uint8_t* stage = smem + C::OFF_Q;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+                    const int sub = c >> 1;              // 64-column block
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = (c & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
+                        uint4* dst = reinterpret_cast<uint4*>(stage + sub * C::SUB + r * 128 + ((chunk ^ (r & 7)) << 4));
+                        *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 0) {
+                    for (int s = 0; s < C::NSUB; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
+                    tma_store_commit_and_wait_read();
+                }
+            } else if (row_valid) {
+                // global rows: scattered row stores
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
+                                                __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
+                        dst[c * 4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            } else {
+                // rows past the gathered count: still take part in the warp-wide loads
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+                }
+            }
+            if (p.lse && row_valid) p.lse[(size_t)bh * p.S + i] = lse;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
+    using C = Cfg<D>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    attn_fwd_tc_kernel<D><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
+    if (n_items <= 0) return cudaSuccess;
+    if (d == 128) return launch<128>(p, n_items, stream);
+    if (d == 64) return launch<64>(p, n_items, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

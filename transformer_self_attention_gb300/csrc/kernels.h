@@ -1,0 +1,61 @@
+// Kernel parameter blocks and launchers shared by the host code and the CUDA
+// translation units of the library.  Internal; the public ABI is attn.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace attn {
+
+// Parameters of the tensor-core (tcgen05) forward kernel.  Passed by value
+// as a __grid_constant__ so the TMA descriptors live in parameter space.
+struct TcParams {
+    CUtensorMap tm_q;    // Q  [B*Hq,  S, d] bf16, box {64, 128, 1}, 128B swizzle
+    CUtensorMap tm_k;    // K  [B*Hkv, S, d]
+    CUtensorMap tm_v;    // V  [B*Hkv, S, d]
+    CUtensorMap tm_o;    // O  [B*Hq,  S, d] (TMA store)
+    CUtensorMap tm_qg;   // gathered global query rows  [B*Hq,  nG, d]
+    CUtensorMap tm_kg;   // gathered global keys         [B*Hkv, nG, d]
+    CUtensorMap tm_vg;   // gathered global values       [B*Hkv, nG, d]
+    const int4* work;    // 2 int4 per work item (attn.h schedule layout)
+    int item_offset;     // first work item of this launch
+    int S, Hq, Hkv, group;
+    int kind, window;
+    float scale_log2;    // scale * log2(e)
+    const int* globals;  // sorted global positions (device)
+    int n_global;
+    const unsigned* global_bits;  // 4 words per key tile
+    void* o;             // O base (scattered stores of the global rows)
+    float* lse;          // may be null
+    int* err;            // device error word
+    long long watchdog_ns;
+    int withhold_v;      // test hook: producer never loads V
+};
+
+// Parameters of the fp32 CUDA-core kernel.
+struct F32Params {
+    const float* q; const float* k; const float* v;
+    float* o; float* lse;
+    int B, Hq, Hkv, S, group;
+    int kind, window;
+    float scale;
+    const int* globals; int n_global;
+    const unsigned char* is_global;  // [S] flags (local + global only)
+};
+
+// Gather of the global rows of Q, K, V into dense scratch tensors.
+struct GatherParams {
+    const uint16_t* q; const uint16_t* k; const uint16_t* v;  // bf16 bits
+    uint16_t* qg; uint16_t* kg; uint16_t* vg;
+    const int* globals; int n_global;
+    int BHq, BHkv, S, d;
+};
+
+cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
+cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
+cudaError_t launch_gather_globals(const GatherParams& p, cudaStream_t stream);
+
+}  // namespace attn

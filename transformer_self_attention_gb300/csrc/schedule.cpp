@@ -1,0 +1,150 @@
+// Host-side tile schedule builder (see schedule.h).
+#include "schedule.h"
+
+#include <algorithm>
+#include <cstdint>
+
+namespace attn {
+namespace {
+
+constexpr int T = ATTN_TILE;
+
+// Allowed key interval [lo(i), hi(i)] of row i for the window part of a mask
+// (global rows / columns are handled separately).  Both ends are
+// non-decreasing in i for every kind, which the tile classification uses.
+struct RowBand {
+    int kind, S, w;
+    long lo(long i) const {
+        switch (kind) {
+        case ATTN_MASK_SLIDING:
+        case ATTN_MASK_LOCAL_GLOBAL:
+        case ATTN_MASK_CAUSAL_SLIDING: return std::max(0L, i - w);
+        default: return 0;
+        }
+    }
+    long hi(long i) const {
+        switch (kind) {
+        case ATTN_MASK_CAUSAL:
+        case ATTN_MASK_CAUSAL_SLIDING: return std::min<long>(i, S - 1);
+        case ATTN_MASK_SLIDING:
+        case ATTN_MASK_LOCAL_GLOBAL: return std::min<long>(S - 1, i + w);
+        default: return S - 1;
+        }
+    }
+};
+
+}  // namespace
+
+attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
+    const int S = in.S;
+    const int nq = (S + T - 1) / T, nk = (S + T - 1) / T;
+    const bool lg = in.kind == ATTN_MASK_LOCAL_GLOBAL;
+    const int nG = lg ? (int)in.globals.size() : 0;
+    RowBand band{in.kind, S, in.window};
+
+    // prefix count of global positions: cntG[x] = #globals < x
+    std::vector<int> is_g(S, 0), cntG(S + 1, 0);
+    for (int g : in.globals) is_g[g] = 1;
+    for (int x = 0; x < S; ++x) cntG[x + 1] = cntG[x] + is_g[x];
+    auto globals_in = [&](long a, long b) -> long {  // #globals in [a, b]
+        if (b < a) return 0;
+        return cntG[b + 1] - cntG[a];
+    };
+
+    struct Proto { int q_tile, kv_begin, kv_end, full_begin, full_end, flags, n_gtiles; };
+    std::vector<Proto> protos;
+    protos.reserve(nq);
+    const int n_gtiles = (nG + T - 1) / T;
+
+    for (int qt = 0; qt < nq; ++qt) {
+        const long r0 = (long)qt * T;
+        const long r1 = std::min<long>(S, r0 + T) - 1;
+        const bool rows_full = (r0 + T - 1) < S;
+        const int kv_begin = (int)(band.lo(r0) / T);
+        const int kv_end = (int)(band.hi(r1) / T) + 1;
+        int full_begin = -1, full_end = -1;
+        for (int t = kv_begin; t < kv_end; ++t) {
+            const long c0 = (long)t * T, c1 = c0 + T - 1;
+            const long c1s = std::min<long>(c1, S - 1);
+            // at least one allowed pair: some row's interval meets [c0, c1s]
+            bool any = false;
+            for (long i = r0; i <= r1 && !any; ++i)
+                any = band.lo(i) <= c1s && band.hi(i) >= c0;
+            if (!any) return ATTN_ERR_UNSUPPORTED;  // interval masks never leave holes
+            bool full = rows_full && c1 < S;
+            if (full) {
+                if (!lg) {
+                    full = band.lo(r0 + T - 1) <= c0 && band.hi(r0) >= c1;
+                } else {
+                    for (long i = r0; i <= r0 + T - 1 && full; ++i) {
+                        if (is_g[i]) continue;
+                        const long lo = band.lo(i), hi = band.hi(i);
+                        // columns of [c0, c1] outside [lo, hi] must all be global
+                        const long a1 = c0, b1 = std::min(c1, lo - 1);
+                        const long a2 = std::max(c0, hi + 1), b2 = c1;
+                        long need = 0, have = 0;
+                        if (b1 >= a1) { need += b1 - a1 + 1; have += globals_in(a1, b1); }
+                        if (b2 >= a2) { need += b2 - a2 + 1; have += globals_in(a2, b2); }
+                        full = need == have;
+                    }
+                }
+            }
+            if (full) {
+                if (full_begin < 0) { full_begin = t; full_end = t + 1; }
+                else if (full_end == t) full_end = t + 1;
+                else return ATTN_ERR_UNSUPPORTED;  // FULL tiles must be contiguous
+            }
+        }
+        if (full_begin < 0) full_begin = full_end = kv_begin;
+        int flags = 0, ngt = 0;
+        if (lg && nG > 0) {
+            const long band_lo = (long)kv_begin * T, band_hi = (long)kv_end * T;  // [lo, hi)
+            const long inside = globals_in(band_lo, std::min<long>(band_hi, S) - 1);
+            if (inside < nG) { flags |= ATTN_WORK_GLOBAL_COLS; ngt = n_gtiles; }
+        }
+        protos.push_back({qt, kv_begin, kv_end, full_begin, full_end, flags, ngt});
+    }
+
+    // longest first; equal cost -> later query tile first, then head order so
+    // that the query heads of one key/value group run side by side
+    std::vector<int> order(protos.size());
+    for (size_t k = 0; k < order.size(); ++k) order[k] = (int)k;
+    auto cost = [&](const Proto& p) { return (p.kv_end - p.kv_begin) + p.n_gtiles; };
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+        const int cx = cost(protos[x]), cy = cost(protos[y]);
+        if (cx != cy) return cx > cy;
+        return protos[x].q_tile > protos[y].q_tile;
+    });
+
+    const int BH = in.B * in.Hq;
+    out->items.clear();
+    out->items.reserve((size_t)(protos.size() + (size_t)n_gtiles) * BH * ATTN_WORK_INTS);
+    for (int k : order) {
+        const Proto& p = protos[k];
+        for (int bh = 0; bh < BH; ++bh) {
+            const int it[ATTN_WORK_INTS] = {bh, p.q_tile, p.kv_begin, p.kv_end,
+                                            p.full_begin, p.full_end, p.flags, p.n_gtiles};
+            out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
+        }
+    }
+    out->n_main = (int)protos.size() * BH;
+
+    // dense pass for the global rows: every key, FULL except a ragged last tile
+    out->n_grows = 0;
+    if (lg && nG > 0) {
+        const int full_end = (S % T == 0) ? nk : nk - 1;
+        for (int gt = 0; gt < n_gtiles; ++gt)
+            for (int bh = 0; bh < BH; ++bh) {
+                const int it[ATTN_WORK_INTS] = {bh, gt, 0, nk, 0, full_end, ATTN_WORK_GLOBAL_ROWS, 0};
+                out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
+                ++out->n_grows;
+            }
+    }
+    out->n_kv_tiles = nk;
+    out->n_global_tiles = n_gtiles;
+    out->global_bits.assign((size_t)nk * 4, 0u);
+    for (int g : in.globals) out->global_bits[(size_t)(g / T) * 4 + (g % T) / 32] |= 1u << (g % 32);
+    return ATTN_OK;
+}
+
+}  // namespace attn

@@ -1,0 +1,39 @@
+// Host-side tile schedule of the attention forward pass.
+//
+// The S x S pair grid is cut into ATTN_TILE x ATTN_TILE tiles.  For every query
+// tile the builder lists the key tiles holding at least one allowed pair and
+// splits them into FULL tiles (every pair allowed, no mask evaluated) and
+// PARTIAL tiles (mask predicate evaluated per pair); key tiles with no allowed
+// pair are skipped.  This is the block-skipping that sparse attention needs
+// because a dense product cannot skip zeros ("第 8 章 现代大模型架构"
+// (theaiera.top), 8.3.4 稀疏模式的线性化), applied to the masks of
+// "Transformer 演进与变体" (ai.icyfenix.cn), section 稀疏注意力.
+#pragma once
+
+#include <vector>
+
+#include "attn.h"
+
+namespace attn {
+
+struct ScheduleInput {
+    int B, Hq, Hkv, S;
+    int kind;                 // attn_mask_kind
+    int window;
+    std::vector<int> globals; // sorted, unique, in [0, S)
+};
+
+struct Schedule {
+    std::vector<int> items;   // ATTN_WORK_INTS ints per item
+    int n_main = 0;           // items of the first launch
+    int n_grows = 0;          // ATTN_WORK_GLOBAL_ROWS items (second launch)
+    int n_kv_tiles = 0;
+    int n_global_tiles = 0;
+    std::vector<unsigned> global_bits;  // 4 words per key tile: bit c set if key tile*128+c is global
+};
+
+// Builds the schedule.  Returns ATTN_OK, or ATTN_ERR_UNSUPPORTED if a query
+// tile's FULL key tiles are not contiguous (cannot happen for the five kinds).
+attn_status build_schedule(const ScheduleInput& in, Schedule* out);
+
+}  // namespace attn
