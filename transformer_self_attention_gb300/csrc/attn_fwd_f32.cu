@@ -59,8 +59,9 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK) attn_fwd_f32_kernel(F32Pa
     };
 
     const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL;
+    const bool g_row = lg && p.n_global > 0 && p.is_global[i];
     long lo = 0, hi = p.S - 1;
-    if (lg && p.is_global[i]) {
+    if (g_row) {
         // a global row sees every key
     } else if (p.kind == ATTN_MASK_CAUSAL) {
         hi = i;
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK) attn_fwd_f32_kernel(F32Pa
         hi = i + p.window < p.S - 1 ? i + p.window : p.S - 1;
     }
     for (long j = lo; j <= hi; ++j) visit(j);
-    if (lg && !p.is_global[i])
+    if (lg && !g_row)
         for (int t = 0; t < p.n_global; ++t) {
             const long j = p.globals[t];
             if (j < lo || j > hi) visit(j);

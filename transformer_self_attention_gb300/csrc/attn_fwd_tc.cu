@@ -367,31 +367,26 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     for (int s = 0; s < C::NSUB; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
                     tma_store_commit_and_wait_read();
                 }
-            } else if (row_valid) {
-                // global rows: scattered row stores
+            } else {
+                // global rows: scattered row stores.  The tensor-memory loads are warp-collective,
+                // so every lane executes them; only rows past the gathered count skip the stores.
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32(t_o + c * 32, o);
                     tmem_wait_ld();
+                    if (row_valid) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t pk[4];
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t pk[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            pk[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
-                                                __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
-                        dst[c * 4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            for (int e = 0; e < 4; ++e)
+                                pk[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
+                                                    __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
+                            dst[c * 4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        }
                     }
-                }
-            } else {
-                // rows past the gathered count: still take part in the warp-wide loads
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
                 }
             }
             if (p.lse && row_valid) p.lse[(size_t)bh * p.S + i] = lse;
