@@ -98,6 +98,73 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
         if ((long long)(globaltimer() - t0) > p.watchdog_ns) return;
 }
 
+// Mask of one PARTIAL tile as seen by one query row: allowed in-tile columns are
+// [a0, a1] (clamped to [-1, BN]) plus the set bits of g0..g3 (global keys).
+struct TileMask {
+    int a0, a1;
+    uint32_t g0, g1, g2, g3;
+};
+
+template <bool MASKED>
+__device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask& mk) {
+    if (!MASKED) return __uint_as_float(raw);
+    const uint32_t gw = c < 32 ? mk.g0 : c < 64 ? mk.g1 : c < 96 ? mk.g2 : mk.g3;
+    const bool in = (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
+    return in ? __uint_as_float(raw) : -INFINITY;
+}
+
+// Row maximum of the (masked) raw scores of this thread's row, columns [0, BN).
+template <bool MASKED>
+__device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            m8[e & 7] = fmaxf(m8[e & 7], tile_score<MASKED>(r0[e], h * 64 + e, mk));
+            m8[e & 7] = fmaxf(m8[e & 7], tile_score<MASKED>(r1[e], h * 64 + 32 + e, mk));
+        }
+    }
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+        for (int j = 0; j < k; ++j) m8[j] = fmaxf(m8[j], m8[j + k]);
+    return m8[0];
+}
+
+// P = exp2(s * sl2 - ref) written as bf16 over the S columns; returns the row sum.
+// Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
+// [32h, 32h+32), which only overlap S columns this thread has already read.
+template <bool MASKED>
+__device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref) {
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32], pk[32];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(tile_score<MASKED>(r0[2 * e], h * 64 + 2 * e, mk), sl2, -ref));
+            const float p1 = ex2(fmaf(tile_score<MASKED>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk), sl2, -ref));
+            const float p2 = ex2(fmaf(tile_score<MASKED>(r1[2 * e], h * 64 + 32 + 2 * e, mk), sl2, -ref));
+            const float p3 = ex2(fmaf(tile_score<MASKED>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk), sl2, -ref));
+            s4[0] += p0; s4[1] += p1; s4[2] += p2; s4[3] += p3;
+            pk[e] = pack_bf16x2(p0, p1);
+            pk[16 + e] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(t_s + h * 32, pk);
+    }
+    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D>;
@@ -243,49 +310,41 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            // ---- mask of this tile: allowed in-tile columns are [a0, a1] plus set bits of gb
+            // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate)
             bool partial = true;
-            long a0 = 0, a1 = -1;
-            uint32_t gb[4] = {0u, 0u, 0u, 0u};
+            TileMask mk{0, -1, 0u, 0u, 0u, 0u};
             if (it < n_band) {
                 const int t = kv_begin + it;
                 partial = t < full_begin || t >= full_end;
                 if (partial) {
-                    a0 = lo - (long)t * BN;
-                    a1 = hi - (long)t * BN;
+                    const long c0 = (long)t * BN;
+                    mk.a0 = (int)max(-1L, min((long)BN, lo - c0));
+                    mk.a1 = (int)max(-1L, min((long)BN, hi - c0));
                     if (lg) {
                         const uint4 g4 = *reinterpret_cast<const uint4*>(p.global_bits + 4 * t);
-                        gb[0] = g4.x; gb[1] = g4.y; gb[2] = g4.z; gb[3] = g4.w;
+                        mk.g0 = g4.x; mk.g1 = g4.y; mk.g2 = g4.z; mk.g3 = g4.w;
                     }
                 }
             } else {
-                // gathered global keys: allowed when outside this item's key tiles
+                // gathered global keys: allowed when outside this item's key tiles.
+                // Lane l tests columns l, l+32, l+64, l+96; ballots give every lane the bits.
                 const int g0 = (it - n_band) * BN;
                 const long band_lo = (long)kv_begin * BN, band_hi = (long)kv_end * BN;
-                for (int c = 0; c < BN; ++c) {
-                    const int gi = g0 + c;
+                uint32_t bits[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int gi = g0 + k * 32 + lane;
+                    bool in = false;
                     if (gi < p.n_global) {
                         const long gpos = __ldg(p.globals + gi);
-                        if (gpos < band_lo || gpos >= band_hi) gb[c >> 5] |= 1u << (c & 31);
+                        in = gpos < band_lo || gpos >= band_hi;
                     }
+                    bits[k] = __ballot_sync(0xffffffffu, in);
                 }
+                mk.g0 = bits[0]; mk.g1 = bits[1]; mk.g2 = bits[2]; mk.g3 = bits[3];
             }
-            auto score = [&](uint32_t raw, int c) -> float {
-                if (partial && !((c >= a0 && c <= a1) || ((gb[c >> 5] >> (c & 31)) & 1u))) return -INFINITY;
-                return __uint_as_float(raw);
-            };
             // ---- pass 1: row max of the (masked) scores
-            float mx = -INFINITY;
-            {
-                uint32_t raw[32];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(t_s + c * 32, raw);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, score(raw[e], c * 32 + e));
-                }
-            }
+            float mx = partial ? tile_row_max<true>(t_s, mk) : tile_row_max<false>(t_s, mk);
             // ---- running max, with the lazy rescale
             mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
             const bool grow = mx > m + RESCALE_THRESHOLD;  // false when mx is -inf; true on the first finite max
@@ -307,28 +366,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             l *= alpha;
             m = m_new;
             const float ref = (m == -INFINITY) ? 0.f : m;
-            // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P written over the S columns.
-            // Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
-            // [32h, 32h+32), which only overlap S columns this thread has already read.
-            float sum = 0.f;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r0[32], r1[32], pk[32];
-                tmem_ld32(t_s + h * 64, r0);
-                tmem_ld32(t_s + h * 64 + 32, r1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(score(r0[2 * e], h * 64 + 2 * e), sl2, -ref));
-                    const float p1 = ex2(fmaf(score(r0[2 * e + 1], h * 64 + 2 * e + 1), sl2, -ref));
-                    const float p2 = ex2(fmaf(score(r1[2 * e], h * 64 + 32 + 2 * e), sl2, -ref));
-                    const float p3 = ex2(fmaf(score(r1[2 * e + 1], h * 64 + 33 + 2 * e), sl2, -ref));
-                    sum += (p0 + p1) + (p2 + p3);
-                    pk[e] = pack_bf16x2(p0, p1);
-                    pk[16 + e] = pack_bf16x2(p2, p3);
-                }
-                tmem_st32(t_s + h * 32, pk);
-            }
+            // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P over the S columns
+            const float sum = partial ? tile_exp_store<true>(t_s, mk, sl2, ref)
+                                      : tile_exp_store<false>(t_s, mk, sl2, ref);
             l += sum;
             tmem_wait_st();
             tc_fence_before();
