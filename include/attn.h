@@ -180,6 +180,42 @@ attn_status attn_poll_device_error(attn_handle h, int* code);
  */
 attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold);
 
+/*
+ * attn_forward_noalloc -- the bf16 forward pass for callers that cannot
+ * allocate device memory (no cudaMalloc, no cudaFree, no allocating library
+ * call): code running inside a memory pool it does not own, runtimes that
+ * forbid allocation after start-up, processes whose device footprint must stay
+ * fixed.  The pages describe no such interface; it is a deployment
+ * convenience of this library.
+ *
+ *   B .. n_global : as for attn_create with dtype ATTN_BF16 (validated the same
+ *                   way; the schedule is built on the host on every call).
+ *   Q, K, V, O, LSE, stream : as for attn_forward (caller-owned device
+ *                   buffers; LSE may be NULL).
+ *
+ * Instead of handle-owned buffers, the call keeps its scratch (error word,
+ * work list, global-token list and bits, gathered global rows) in one fixed
+ * device array of ATTN_NOALLOC_SCRATCH_BYTES, a file-scope __device__ object
+ * that every GPU which loads this library holds until the process exits.
+ * A problem whose scratch does not fit returns ATTN_ERR_UNSUPPORTED before
+ * anything is launched (the work list takes 32 bytes per (batch, head,
+ * 128-row tile); the local + global mask adds B*(Hq + 2*Hkv)*n_global*d_k*2
+ * bytes).
+ *
+ * The first call on a device looks up the array's address (once per device,
+ * with that device current); make that first call before any stream capture.
+ * Every call shares the one array and leaves its contents behind: calls that
+ * overlap on the GPU (two streams, or two host threads) race and must be
+ * serialised by the caller.  The call copies its schedule from host memory
+ * with cudaMemcpyAsync on `stream` and returns without waiting for the kernels.
+ * Errors: as attn_create and attn_forward, plus ATTN_ERR_UNSUPPORTED above.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d_k, float scale,
+                                 attn_mask_kind kind, int window, const int* global_idx,
+                                 int n_global, const void* Q, const void* K, const void* V,
+                                 void* O, float* LSE, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,7 +26,8 @@ WORK_INTS = 8
 WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
 
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
-            "attn_poll_device_error", "attn_set_watchdog")
+            "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class AttnError(RuntimeError):
@@ -55,6 +56,8 @@ def _load():
     lib.attn_poll_device_error.restype = I
     lib.attn_set_watchdog.argtypes = [P, LL, I]
     lib.attn_set_watchdog.restype = I
+    lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
+    lib.attn_forward_noalloc.restype = I
     return lib
 
 
@@ -102,6 +105,19 @@ def attn_poll_device_error(handle: int):
 
 def attn_set_watchdog(handle: int, limit_ns: int, withhold: int = 0) -> int:
     return _lib.attn_set_watchdog(handle, int(limit_ns), int(withhold))
+
+
+def attn_forward_noalloc(B, Hq, Hkv, S, d_k, scale, kind, window, global_idx, q_ptr, k_ptr, v_ptr, o_ptr,
+                         lse_ptr=0, stream=0) -> int:
+    """The bf16 forward pass without any device allocation (fixed library-owned scratch); returns the status.
+
+    For callers that cannot allocate device memory.  Calls that overlap on the GPU race on the shared
+    scratch; the first call on a device should come before any stream capture.
+    """
+    g, ng = _int_array(global_idx)
+    return _lib.attn_forward_noalloc(int(B), int(Hq), int(Hkv), int(S), int(d_k), float(scale), int(kind),
+                                     int(window), ctypes.cast(g, ctypes.c_void_p) if ng else None, ng,
+                                     q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr or None, stream or None)
 
 
 def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):
