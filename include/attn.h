@@ -170,6 +170,16 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
 attn_status attn_poll_device_error(attn_handle h, int* code);
 
 /*
+ * attn_selftest_exp2 -- test hook: y[i] = the exp2 approximation the library's
+ * FMA-pipe exponential evaluates (range reduction x = j + f, j = round(x), and a
+ * degree-3 polynomial for 2^f on [-1/2, 1/2], max relative error 7.5e-5 for
+ * x >= -125; inputs below -125 are clamped to -125).  x, y: device float
+ * arrays of n elements; enqueued on `stream`.  Errors: ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_CUDA.
+ */
+attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
+
+/*
  * attn_set_watchdog -- test hook for the failure-detection path.
  *   limit_ns : wall-clock limit of every bounded wait inside the kernels
  *              (default 2e9 ns).

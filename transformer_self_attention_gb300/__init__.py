@@ -26,7 +26,7 @@ WORK_INTS = 8
 WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
 
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
-            "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc")
+            "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -58,6 +58,8 @@ def _load():
     lib.attn_set_watchdog.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
+    lib.attn_selftest_exp2.argtypes = [P, P, I, P]
+    lib.attn_selftest_exp2.restype = I
     return lib
 
 
@@ -118,6 +120,11 @@ def attn_forward_noalloc(B, Hq, Hkv, S, d_k, scale, kind, window, global_idx, q_
     return _lib.attn_forward_noalloc(int(B), int(Hq), int(Hkv), int(S), int(d_k), float(scale), int(kind),
                                      int(window), ctypes.cast(g, ctypes.c_void_p) if ng else None, ng,
                                      q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr or None, stream or None)
+
+
+def attn_selftest_exp2(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> int:
+    """Test hook: the library's FMA-pipe exp2 applied elementwise (device float arrays)."""
+    return _lib.attn_selftest_exp2(x_ptr, y_ptr, int(n), stream or None)
 
 
 def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):

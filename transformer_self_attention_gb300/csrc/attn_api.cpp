@@ -57,20 +57,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D bf16 map over [heads, rows, d] (d fastest), box {64, 128, 1}, 128-byte
+// 3-D bf16 map over [heads, rows, d] (d fastest), box {64, box_rows, 1}, 128-byte
 // swizzle; rows past `rows` read as zeros and are not written by stores.
-bool encode_map(CUtensorMap* map, const void* base, int d, long rows, long heads) {
+bool encode_map(CUtensorMap* map, const void* base, int d, long rows, long heads, unsigned box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, ATTN_TILE, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+constexpr unsigned kTileRows = ATTN_TILE;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -180,9 +182,9 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
             if ((e = cudaMalloc(&h->d_qg, qg)) != cudaSuccess) return fail(e);
             if ((e = cudaMalloc(&h->d_kg, kg)) != cudaSuccess) return fail(e);
             if ((e = cudaMalloc(&h->d_vg, kg)) != cudaSuccess) return fail(e);
-            if (!encode_map(&p.tm_qg, h->d_qg, d_k, nG, (long)B * Hq) ||
-                !encode_map(&p.tm_kg, h->d_kg, d_k, nG, (long)B * Hkv) ||
-                !encode_map(&p.tm_vg, h->d_vg, d_k, nG, (long)B * Hkv)) {
+            if (!encode_map(&p.tm_qg, h->d_qg, d_k, nG, (long)B * Hq, kTileRows) ||
+                !encode_map(&p.tm_kg, h->d_kg, d_k, nG, (long)B * Hkv, kTileRows) ||
+                !encode_map(&p.tm_vg, h->d_vg, d_k, nG, (long)B * Hkv, kTileRows)) {
                 free_plan(h);
                 return ATTN_ERR_CUDA;
             }
@@ -223,19 +225,19 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
     } else {
         attn::TcParams& p = h->tp;
         if (Q != h->last_q) {
-            if (!encode_map(&p.tm_q, Q, h->d, h->S, (long)h->B * h->Hq)) return ATTN_ERR_CUDA;
+            if (!encode_map(&p.tm_q, Q, h->d, h->S, (long)h->B * h->Hq, kTileRows)) return ATTN_ERR_CUDA;
             h->last_q = Q;
         }
         if (K != h->last_k) {
-            if (!encode_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv)) return ATTN_ERR_CUDA;
+            if (!encode_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
             h->last_k = K;
         }
         if (V != h->last_v) {
-            if (!encode_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv)) return ATTN_ERR_CUDA;
+            if (!encode_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
             h->last_v = V;
         }
         if (O != h->last_o) {
-            if (!encode_map(&p.tm_o, O, h->d, h->S, (long)h->B * h->Hq)) return ATTN_ERR_CUDA;
+            if (!encode_map(&p.tm_o, O, h->d, h->S, (long)h->B * h->Hq, kTileRows)) return ATTN_ERR_CUDA;
             h->last_o = O;
         }
         p.o = O;
@@ -300,6 +302,12 @@ attn_status attn_poll_device_error(attn_handle h, int* code) {
     if (cudaMemcpy(code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
     if (*code != 0 && cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
     return *code ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream) {
+    if (!x || !y || n < 0) return ATTN_ERR_INVALID_ARG;
+    return attn::launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                                 : ATTN_ERR_CUDA;
 }
 
 attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold) {

@@ -14,6 +14,7 @@
 
 #include "attn.h"
 #include "kernels.h"
+#include "sm103_ptx.h"
 
 namespace attn {
 namespace {
@@ -104,7 +105,24 @@ __global__ void gather_globals_kernel(GatherParams p) {
     for (int t = threadIdx.x; t < p.d / 8; t += blockDim.x) d4[t] = s4[t];
 }
 
+// Evaluates the softmax warps' FMA-pipe exp2 (exp2_poly2) elementwise, for its test.
+__global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
+    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    const float2 v = make_float2(x[i], i + 1 < n ? x[i + 1] : 0.f);
+    const float2 r = ptx::exp2_poly2(v);
+    y[i] = r.x;
+    if (i + 1 < n) y[i + 1] = r.y;
+}
+
 }  // namespace
+
+cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    const int pairs = (n + 1) / 2;
+    exp2_selftest_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream) {
     const long n_rows = (long)p.B * p.Hq * p.S;

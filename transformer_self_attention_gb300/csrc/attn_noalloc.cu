@@ -67,13 +67,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     return fn;
 }
 
-// bf16 [heads, rows, d] map, box {64, 128, 1}, 128-byte swizzle (the layout the kernel expects)
-bool map3d(CUtensorMap* m, const void* base, int d, long rows, long heads) {
+// bf16 [heads, rows, d] map, box {64, box_rows, 1}, 128-byte swizzle (the layout the kernel expects)
+bool map3d(CUtensorMap* m, const void* base, int d, long rows, long heads, unsigned box_rows) {
     auto enc = encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
-    cuuint32_t box[3] = {64, ATTN_TILE, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -142,12 +142,13 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
         return ATTN_ERR_CUDA;
 
     attn::TcParams p{};
-    if (!map3d(&p.tm_q, Q, d_k, S, (long)B * Hq) || !map3d(&p.tm_k, K, d_k, S, (long)B * Hkv) ||
-        !map3d(&p.tm_v, V, d_k, S, (long)B * Hkv) || !map3d(&p.tm_o, O, d_k, S, (long)B * Hq))
+    constexpr unsigned T = ATTN_TILE;
+    if (!map3d(&p.tm_q, Q, d_k, S, (long)B * Hq, T) || !map3d(&p.tm_k, K, d_k, S, (long)B * Hkv, T) ||
+        !map3d(&p.tm_v, V, d_k, S, (long)B * Hkv, T) || !map3d(&p.tm_o, O, d_k, S, (long)B * Hq, T))
         return ATTN_ERR_CUDA;
-    if (nG > 0 && (!map3d(&p.tm_qg, sc + off_qg, d_k, nG, (long)B * Hq) ||
-                   !map3d(&p.tm_kg, sc + off_kg, d_k, nG, (long)B * Hkv) ||
-                   !map3d(&p.tm_vg, sc + off_vg, d_k, nG, (long)B * Hkv)))
+    if (nG > 0 && (!map3d(&p.tm_qg, sc + off_qg, d_k, nG, (long)B * Hq, T) ||
+                   !map3d(&p.tm_kg, sc + off_kg, d_k, nG, (long)B * Hkv, T) ||
+                   !map3d(&p.tm_vg, sc + off_vg, d_k, nG, (long)B * Hkv, T)))
         return ATTN_ERR_CUDA;
     p.work = reinterpret_cast<const int4*>(sc + off_work);
     p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;

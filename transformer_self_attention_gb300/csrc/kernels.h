@@ -20,7 +20,7 @@ struct TcParams {
     CUtensorMap tm_qg;   // gathered global query rows  [B*Hq,  nG, d]
     CUtensorMap tm_kg;   // gathered global keys         [B*Hkv, nG, d]
     CUtensorMap tm_vg;   // gathered global values       [B*Hkv, nG, d]
-    const int4* work;    // 2 int4 per work item (attn.h schedule layout)
+    const int4* work;    // 4 int4 per work item (attn.h schedule layout)
     int item_offset;     // first work item of this launch
     int S, Hq, Hkv, group;
     int kind, window;
@@ -57,5 +57,6 @@ struct GatherParams {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
 cudaError_t launch_gather_globals(const GatherParams& p, cudaStream_t stream);
+cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
 
 }  // namespace attn
