@@ -136,7 +136,13 @@ const char* attn_status_string(attn_status s);
  *   [6] flags       ATTN_WORK_GLOBAL_COLS: after the key tiles, also evaluate
  *                   the gathered global keys G not inside [kv_begin, kv_end) tiles;
  *                   ATTN_WORK_GLOBAL_ROWS: the item's rows are the global rows
- *   [7] n_gtiles    number of gathered global-key tiles (ATTN_WORK_GLOBAL_COLS)
+ *   [7] n_gtiles    number of gathered global-key tiles (ATTN_WORK_GLOBAL_COLS);
+ *                   for ATTN_WORK_GLOBAL_ROWS items: the index of the item's key
+ *                   chunk.  The global-row pass splits the key tiles into chunks of
+ *                   equal length (one item per chunk, gathered row tile and head);
+ *                   each chunk yields a partial softmax result and a merge step
+ *                   combines them: O = sum_c e^LSE_c O_c / sum_c e^LSE_c,
+ *                   LSE = ln sum_c e^LSE_c.
  * Items are ordered by decreasing number of tiles (longest first).
  * For LOCAL_GLOBAL, rows in G are computed only by ATTN_WORK_GLOBAL_ROWS items,
  * which run after all other items.
@@ -210,7 +216,8 @@ attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold);
  * A problem whose scratch does not fit returns ATTN_ERR_UNSUPPORTED before
  * anything is launched (the work list takes 32 bytes per (batch, head,
  * 128-row tile); the local + global mask adds B*(Hq + 2*Hkv)*n_global*d_k*2
- * bytes).
+ * bytes of gathered rows and B*Hq*n_global*chunks*(d_k+1)*4 bytes of partial
+ * results of the chunked global-row pass).
  *
  * The first call on a device looks up the array's address (once per device,
  * with that device current); make that first call before any stream capture.

@@ -39,15 +39,21 @@ def _simulate(items, n_first, kind, S, w, G, check_classes=True):
     classes = oracle.tile_classes(kind, S, w, list(G)) if check_classes else None
     lg = kind == tsa.MASK_LOCAL_GLOBAL
     seen_tiles = set()
+    chunks = {}
     for n, it in enumerate(items):
         bh, qt, kb, ke, fb, fe, flags, ngt = (int(x) for x in it)
         if bh != 0:
             continue
         if flags & tsa.WORK_GLOBAL_ROWS:
+            # one key chunk [kb, ke) of the dense pass over the gathered global rows
             assert n >= n_first
             rows = Garr[qt * T:(qt + 1) * T]
-            assert kb == 0 and ke == (S + T - 1) // T
-            counts[rows] += S
+            nk = (S + T - 1) // T
+            assert 0 <= kb <= fb <= fe <= ke <= nk
+            assert fe <= S // T                        # FULL only for whole key tiles
+            assert ke - fe <= 1 and (fe == ke or ke == nk)
+            chunks.setdefault(qt, []).append((ngt, kb, ke))
+            counts[rows] += min(ke * T, S) - kb * T
             continue
         assert n < n_first
         assert (qt not in seen_tiles), "query tile listed twice"
@@ -76,14 +82,24 @@ def _simulate(items, n_first, kind, S, w, G, check_classes=True):
             outside = (Garr < kb * T) | (Garr >= ke * T)
             counts[i[keep]] += int(outside.sum())
     assert seen_tiles == set(range((S + T - 1) // T))
+    nk = (S + T - 1) // T
+    for qt, cs in chunks.items():  # the chunks of each gathered row tile cover [0, nk) once, in order
+        cs.sort()
+        assert [c for c, _, _ in cs] == list(range(len(cs)))
+        assert cs[0][1] == 0 and cs[-1][2] == nk
+        assert all(cs[k][2] == cs[k + 1][1] for k in range(len(cs) - 1))
     return counts
 
 
 def _check(kind, S, w=0, G=(), B=1, Hq=2, Hkv=1, check_classes=True):
     items, n_first = tsa.attn_schedule_host(B, Hq, Hkv, S, kind, w, list(G))
     nq = (S + T - 1) // T
-    n_grows = B * Hq * ((len(G) + T - 1) // T) if (kind == tsa.MASK_LOCAL_GLOBAL and G) else 0
-    assert len(items) == B * Hq * nq + n_grows and n_first == B * Hq * nq
+    assert n_first == B * Hq * nq
+    if kind == tsa.MASK_LOCAL_GLOBAL and G:
+        n_chunks = 1 + max(int(it[7]) for it in items[n_first:])
+        assert len(items) - n_first == B * Hq * ((len(G) + T - 1) // T) * n_chunks
+    else:
+        assert len(items) == n_first
     # every (bh, q_tile) exactly once among the first-launch items
     pairs = {(int(a), int(b)) for a, b in items[:n_first, :2]}
     assert pairs == {(bh, q) for bh in range(B * Hq) for q in range(nq)}

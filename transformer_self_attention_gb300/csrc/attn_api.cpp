@@ -32,6 +32,7 @@ struct attn_plan {
     void* d_qg = nullptr;
     void* d_kg = nullptr;
     void* d_vg = nullptr;
+    float* d_part = nullptr;  // partial results of the chunked global-row pass
     // tensor maps of the last pointers seen (re-encoded when they change)
     const void* last_q = nullptr;
     const void* last_k = nullptr;
@@ -110,7 +111,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 
 void free_plan(attn_plan* h) {
     if (!h) return;
-    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg};
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part};
     for (void* b : bufs)
         if (b) cudaFree(b);
     delete h;
@@ -182,6 +183,12 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
             if ((e = cudaMalloc(&h->d_qg, qg)) != cudaSuccess) return fail(e);
             if ((e = cudaMalloc(&h->d_kg, kg)) != cudaSuccess) return fail(e);
             if ((e = cudaMalloc(&h->d_vg, kg)) != cudaSuccess) return fail(e);
+            if (h->sched.n_chunks > 1) {
+                const size_t rows = (size_t)B * Hq * nG * h->sched.n_chunks;
+                if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_part), rows * (d_k + 1) * sizeof(float))) !=
+                    cudaSuccess)
+                    return fail(e);
+            }
             if (!encode_map(&p.tm_qg, h->d_qg, d_k, nG, (long)B * Hq, kTileRows) ||
                 !encode_map(&p.tm_kg, h->d_kg, d_k, nG, (long)B * Hkv, kTileRows) ||
                 !encode_map(&p.tm_vg, h->d_vg, d_k, nG, (long)B * Hkv, kTileRows)) {
@@ -199,6 +206,9 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         p.err = h->d_err;
         p.watchdog_ns = 2000000000LL;
         p.withhold_v = 0;
+        p.n_chunks = h->sched.n_chunks;
+        p.part_o = h->d_part;
+        p.part_lse = h->d_part ? h->d_part + (size_t)B * Hq * nG * h->sched.n_chunks * d_k : nullptr;
     }
     *out = h;
     return ATTN_OK;
@@ -257,6 +267,14 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         if (h->sched.n_grows > 0) {
             p.item_offset = h->sched.n_main;
             e = attn::launch_tc_forward(p, h->d, h->sched.n_grows, stream);
+            if (e == cudaSuccess && h->sched.n_chunks > 1) {
+                attn::MergeParams mp{};
+                mp.part_o = p.part_o; mp.part_lse = p.part_lse;
+                mp.o = static_cast<uint16_t*>(O); mp.lse = LSE;
+                mp.globals = h->d_globals; mp.n_global = nG; mp.n_chunks = h->sched.n_chunks;
+                mp.BHq = h->B * h->Hq; mp.S = h->S; mp.d = h->d;
+                e = attn::launch_merge_global_rows(mp, stream);
+            }
         }
     }
     if (e != cudaSuccess) return ATTN_ERR_CUDA;

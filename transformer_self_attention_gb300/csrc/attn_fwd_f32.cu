@@ -8,6 +8,7 @@
 // Keys are visited only where the mask allows them: the row's window interval,
 // then (local + global) the global keys outside it, or every key for a
 // global row ("Transformer 演进与变体", section 稀疏注意力).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -105,6 +106,34 @@ __global__ void gather_globals_kernel(GatherParams p) {
     for (int t = threadIdx.x; t < p.d / 8; t += blockDim.x) d4[t] = s4[t];
 }
 
+// Combines the key chunks of the global-row pass.  One warp per (head, global
+// row); lanes split d.  Chunk c holds O_c (its own softmax-weighted average) and
+// LSE_c = ln of its sum of exponentials, so the whole row is
+//   O = sum_c e^(LSE_c - M) O_c / sum_c e^(LSE_c - M),  LSE = M + ln sum_c e^(LSE_c - M)
+// with M = max_c LSE_c: the same softmax normalisation, applied across chunks.
+__global__ void merge_global_rows_kernel(MergeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long row = (long)blockIdx.x * (blockDim.x >> 5) + warp;
+    if (row >= (long)p.BHq * p.n_global) return;
+    const long bh = row / p.n_global;
+    const int gr = (int)(row - bh * p.n_global);
+    const float* lse_c = p.part_lse + row * p.n_chunks;
+    float M = -INFINITY;
+    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, lse_c[c]);
+    float W = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // d <= 128: 4 elements per lane
+    for (int c = 0; c < p.n_chunks; ++c) {
+        const float wc = expf(lse_c[c] - M);
+        W += wc;
+        const float* oc = p.part_o + (row * p.n_chunks + c) * p.d;
+        for (int e = 0; e < p.d / 32; ++e) acc[e] = fmaf(wc, oc[lane + 32 * e], acc[e]);
+    }
+    const long pos = p.globals[gr];
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o) + (bh * p.S + pos) * p.d;
+    for (int e = 0; e < p.d / 32; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);
+    if (p.lse && lane == 0) p.lse[bh * p.S + pos] = M + logf(W);
+}
+
 // Evaluates the softmax warps' FMA-pipe exp2 (exp2_poly2) elementwise, for its test.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
     const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -116,6 +145,13 @@ __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
 }
 
 }  // namespace
+
+cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream) {
+    const long rows = (long)p.BHq * p.n_global;
+    if (rows <= 0) return cudaSuccess;
+    merge_global_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;

@@ -98,6 +98,24 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
         if ((long long)(globaltimer() - t0) > p.watchdog_ns) return;
 }
 
+// Bounded busy wait on the non-blocking test (lowest wake-up latency; for the
+// single MMA-issuing thread, which has nothing else to do meanwhile).
+__device__ __forceinline__ bool spin_bounded(uint32_t bar, uint32_t parity, Shared* sh, const TcParams& p, int role) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((n & 1023u) == 0) {
+            if (sh->abort) return false;
+            if ((long long)(globaltimer() - t0) > p.watchdog_ns) {
+                sh->abort = 1;
+                atomicOr(p.err, role);
+                return false;
+            }
+        }
+    }
+}
+
 // Mask of one PARTIAL tile as seen by one query row: allowed in-tile columns are
 // [a0, a1] (clamped to [-1, BN]) plus the set bits of g0..g3 (global keys).
 struct TileMask {
@@ -249,7 +267,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             for (int it = 0; it < n_iter && ok; ++it) {
                 if (!(ok = wait_bounded(bar(B_KFULL), it & 1, sh, p, ERR_MMA))) break;
                 // S/P share tensor columns: PV(it-1) must have consumed P before S is overwritten
-                if (it > 0 && !(ok = wait_bounded(bar(B_OFULL), (it - 1) & 1, sh, p, ERR_MMA))) break;
+                if (it > 0 && !(ok = spin_bounded(bar(B_OFULL), (it - 1) & 1, sh, p, ERR_MMA))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
@@ -260,7 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 mma_commit(bar(B_SFULL));
                 mma_commit(bar(B_KEMPTY));
                 last_bar = B_KEMPTY; last_par = it & 1;
-                if (!(ok = wait_bounded(bar(B_PFULL), it & 1, sh, p, ERR_MMA))) break;
+                if (!(ok = spin_bounded(bar(B_PFULL), it & 1, sh, p, ERR_MMA))) break;
                 if (!(ok = wait_bounded(bar(B_VFULL), it & 1, sh, p, ERR_MMA))) break;
                 tc_fence_after();
 #pragma unroll
@@ -407,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     for (int s = 0; s < C::NSUB; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
                     tma_store_commit_and_wait_read();
                 }
-            } else {
+            } else if (p.n_chunks == 1) {
                 // global rows: scattered row stores.  The tensor-memory loads are warp-collective,
                 // so every lane executes them; only rows past the gathered count skip the stores.
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D);
@@ -428,8 +446,26 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                         }
                     }
                 }
+            } else {
+                // one key chunk of a global row: fp32 partial O (normalised by this chunk's
+                // sum) and partial LSE, combined later by the merge kernel
+                const size_t slot = ((size_t)bh * p.n_global + (q_tile * BM + r)) * p.n_chunks + n_gt;
+                float4* dst = reinterpret_cast<float4*>(p.part_o + slot * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[c * 8 + q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                                         __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+                    }
+                }
+                if (row_valid) p.part_lse[slot] = lse;
             }
-            if (p.lse && row_valid) p.lse[(size_t)bh * p.S + i] = lse;
+            if (p.lse && row_valid && !(grows && p.n_chunks > 1)) p.lse[(size_t)bh * p.S + i] = lse;
         }
     }
 

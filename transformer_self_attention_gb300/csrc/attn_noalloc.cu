@@ -121,7 +121,13 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     const size_t qg_bytes = (size_t)B * Hq * nG * d_k * 2, kg_bytes = (size_t)B * Hkv * nG * d_k * 2;
     const size_t off_kg = off_qg + round256(qg_bytes);
     const size_t off_vg = off_kg + round256(kg_bytes);
-    const size_t total = off_vg + round256(kg_bytes);
+    // key chunks of the global-row pass: the chunk index is int [7] of those items
+    int n_chunks = 1;
+    for (int t = n_first; t < n_items; ++t) n_chunks = std::max(n_chunks, items[(size_t)t * ATTN_WORK_INTS + 7] + 1);
+    const size_t part_rows = n_chunks > 1 ? (size_t)B * Hq * nG * n_chunks : 0;
+    const size_t off_part_o = off_vg + round256(kg_bytes);
+    const size_t off_part_lse = off_part_o + round256(part_rows * d_k * sizeof(float));
+    const size_t total = off_part_lse + round256(part_rows * sizeof(float));
     if (total > kScratchBytes) return ATTN_ERR_UNSUPPORTED;
 
     void* base = nullptr;
@@ -164,6 +170,9 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     p.err = reinterpret_cast<int*>(sc + off_err);
     p.watchdog_ns = 2000000000LL;
     p.withhold_v = 0;
+    p.n_chunks = n_chunks;
+    p.part_o = n_chunks > 1 ? reinterpret_cast<float*>(sc + off_part_o) : nullptr;
+    p.part_lse = n_chunks > 1 ? reinterpret_cast<float*>(sc + off_part_lse) : nullptr;
 
     if (nG > 0) {
         attn::GatherParams g{};
@@ -180,6 +189,14 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     if (n_items > n_first) {
         p.item_offset = n_first;
         if (attn::launch_tc_forward(p, d_k, n_items - n_first, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (n_chunks > 1) {
+            attn::MergeParams mp{};
+            mp.part_o = p.part_o; mp.part_lse = p.part_lse;
+            mp.o = static_cast<uint16_t*>(O); mp.lse = LSE;
+            mp.globals = p.globals; mp.n_global = nG; mp.n_chunks = n_chunks;
+            mp.BHq = B * Hq; mp.S = S; mp.d = d_k;
+            if (attn::launch_merge_global_rows(mp, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
     }
     return ATTN_OK;
 }

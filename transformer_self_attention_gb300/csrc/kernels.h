@@ -33,6 +33,10 @@ struct TcParams {
     int* err;            // device error word
     long long watchdog_ns;
     int withhold_v;      // test hook: producer never loads V
+    // global-row pass split into key chunks (n_chunks > 1): partial results per chunk
+    float* part_o;       // [B*Hq, n_global, n_chunks, d] fp32, each normalised by its own sum
+    float* part_lse;     // [B*Hq, n_global, n_chunks]
+    int n_chunks;
 };
 
 // Parameters of the fp32 CUDA-core kernel.
@@ -54,7 +58,17 @@ struct GatherParams {
     int BHq, BHkv, S, d;
 };
 
+// Merge of the global-row pass's key chunks into O (bf16, rows G) and LSE.
+struct MergeParams {
+    const float* part_o; const float* part_lse;
+    uint16_t* o;         // bf16 bits of O [B*Hq, S, d]
+    float* lse;          // may be null
+    const int* globals; int n_global, n_chunks;
+    int BHq, S, d;
+};
+
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
+cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
 cudaError_t launch_gather_globals(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);

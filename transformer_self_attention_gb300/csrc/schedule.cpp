@@ -8,6 +8,8 @@ namespace attn {
 namespace {
 
 constexpr int T = ATTN_TILE;
+// CTAs the global-row pass aims for (about two per SM of a 152-SM GPU)
+constexpr int kGlobalRowTargetCtas = 304;
 
 // Allowed key interval [lo(i), hi(i)] of row i for the window part of a mask
 // (global rows / columns are handled separately).  Both ends are
@@ -129,16 +131,28 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
     }
     out->n_main = (int)protos.size() * BH;
 
-    // dense pass for the global rows: every key, FULL except a ragged last tile
+    // dense pass for the global rows: every key, FULL except a ragged last tile.
+    // The key tiles are split into chunks (one work item each) so that the pass has
+    // enough CTAs; each chunk writes a partial result that a merge step combines.
     out->n_grows = 0;
+    out->n_chunks = 1;
     if (lg && nG > 0) {
         const int full_end = (S % T == 0) ? nk : nk - 1;
-        for (int gt = 0; gt < n_gtiles; ++gt)
-            for (int bh = 0; bh < BH; ++bh) {
-                const int it[ATTN_WORK_INTS] = {bh, gt, 0, nk, 0, full_end, ATTN_WORK_GLOBAL_ROWS, 0};
-                out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
-                ++out->n_grows;
-            }
+        const int base = BH * n_gtiles;
+        int chunks = (kGlobalRowTargetCtas + base - 1) / base;
+        chunks = std::max(1, std::min(chunks, nk));
+        const int per = (nk + chunks - 1) / chunks;
+        chunks = (nk + per - 1) / per;  // no empty chunk
+        out->n_chunks = chunks;
+        for (int c = 0; c < chunks; ++c)
+            for (int gt = 0; gt < n_gtiles; ++gt)
+                for (int bh = 0; bh < BH; ++bh) {
+                    const int kb = c * per, ke = std::min(nk, kb + per);
+                    const int fe = std::max(kb, std::min(ke, full_end));  // FULL tiles [kb, fe)
+                    const int it[ATTN_WORK_INTS] = {bh, gt, kb, ke, kb, fe, ATTN_WORK_GLOBAL_ROWS, c};
+                    out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
+                    ++out->n_grows;
+                }
     }
     out->n_kv_tiles = nk;
     out->n_global_tiles = n_gtiles;
