@@ -14,6 +14,11 @@ row i of head a (kv head g(a) = a // (Hq // Hkv)):
 following "Trasformer 浅析" (atffang.github.io), sections 缩放点积注意力 and
 填充掩码与因果掩码, and "Transformer 架构及其变体" (aaai.latere.ai), section
 带显式形状的因果自注意力.
+
+``decode`` is the key/value-cache form ("Trasformer 浅析", sections 推理：KV 缓存
+and 交叉注意力; "第 8 章 现代大模型架构" (theaiera.top), section
+预填充创建缓存，解码复用缓存): S_q new query rows per sequence at positions
+cache_len[b] - S_q + i against the cache_len[b] cached keys and values.
 """
 from __future__ import annotations
 
@@ -60,6 +65,10 @@ def _load():
             lib.oracle_row_counts.restype = I
             lib.oracle_tile_classes.argtypes = [I, I, I, P, I, I, I, P]
             lib.oracle_tile_classes.restype = I
+            lib.oracle_decode_allowed.argtypes = [I, L, L, L, L]
+            lib.oracle_decode_allowed.restype = I
+            lib.oracle_decode.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double, I, I, P, P, P]
+            lib.oracle_decode.restype = I
             _lib = lib
     return _lib
 
@@ -140,3 +149,34 @@ def tile_classes(kind, S, window=0, globals_idx=None, tm=128, tn=128) -> np.ndar
     if lib.oracle_tile_classes(int(kind), int(S), int(window), _ptr(g), ng, int(tm), int(tn), _ptr(out)) != 0:
         raise ValueError("oracle_tile_classes failed")
     return out
+
+
+def decode_allowed(kind, t, j, L, window=0) -> bool:
+    """The decode mask predicate: query at position t, key j, cache length L."""
+    return bool(_load().oracle_decode_allowed(int(kind), int(t), int(j), int(L), int(window)))
+
+
+def decode(Q, K, V, cache_len, scale, kind, window=0):
+    """Key/value-cache attention.
+
+    Q [B, Hq, S_q, d]; K, V [B, Hkv, S_cap, d] (the cache); cache_len [B] ints.
+    Row i of sequence b sits at position cache_len[b] - S_q + i.  Kinds FULL
+    (cross-attention: every cached key), CAUSAL and CAUSAL_SLIDING.
+    Returns (O [B, Hq, S_q, d], LSE [B, Hq, S_q]) in float64.
+    """
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    B, Hq, S_q, d = Q.shape
+    Bk, Hkv, S_cap, dk = K.shape
+    assert Bk == B and dk == d and V.shape == K.shape
+    lens = np.ascontiguousarray(np.asarray(cache_len, dtype=np.int32).reshape(-1))
+    assert lens.size == B
+    O = np.empty((B, Hq, S_q, d), dtype=np.float64)
+    LSE = np.empty((B, Hq, S_q), dtype=np.float64)
+    rc = lib.oracle_decode(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, S_q, S_cap, d, float(scale), int(kind),
+                           int(window), _ptr(lens), _ptr(O), _ptr(LSE))
+    if rc != 0:
+        raise ValueError("oracle_decode rejected its arguments")
+    return O, LSE

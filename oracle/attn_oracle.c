@@ -208,3 +208,113 @@ int oracle_tile_classes(int kind, int S, int window, const int* G, int nG,
     free(is_global);
     return 0;
 }
+
+/*
+ * Decode / key-value-cache attention: S_q new query positions per sequence
+ * against a cache that holds cache_len[b] positions of sequence b.
+ *
+ *   - "Trasformer 浅析" (atffang.github.io), section 推理：KV 缓存: the output at
+ *     step t is Softmax(q_t K_{1:t}^T / sqrt(d_k)) V_{1:t}, the query of the new
+ *     position against every cached key and value up to and including it.
+ *   - "第 8 章 现代大模型架构" (theaiera.top), section 预填充创建缓存，解码复用缓存:
+ *     prefill may run in chunks, decode handles one new position per sequence,
+ *     and batches are ragged (sequence r holds S_r cached positions).  A chunk
+ *     of S_q new positions is read here as the last S_q positions of the cache:
+ *     row i of sequence b sits at position t = cache_len[b] - S_q + i, and its
+ *     own key and value are already in the cache.
+ *   - "Trasformer 浅析", section 交叉注意力: the same formula with queries from
+ *     the decoder and keys/values from the encoder; the score matrix is
+ *     n_dec x n_enc and every encoder position is visible (kind FULL).
+ *
+ * Kinds: FULL (all j < cache_len[b]), CAUSAL (j <= t), CAUSAL_SLIDING
+ * (t - w <= j <= t).  Other kinds return -1.
+ *
+ * Q   : float32 [B, Hq, S_q, d]      K, V : float32 [B, Hkv, S_cap, d]
+ * O   : fp64 [B, Hq, S_q, d]         LSE  : fp64 [B, Hq, S_q]
+ * Cache entries at positions >= cache_len[b] are never read.
+ * Returns 0, or -1 on bad arguments (a cache length outside [1, S_cap], or
+ * below S_q for the causal kinds) or allocation failure.
+ */
+int oracle_decode_allowed(int kind, long t, long j, long L, long w)
+{
+    if (j < 0 || j >= L) return 0;
+    switch (kind) {
+    case ORACLE_MASK_FULL: return 1;
+    case ORACLE_MASK_CAUSAL: return j <= t;
+    case ORACLE_MASK_CAUSAL_SLIDING: return j <= t && t - j <= w;
+    default: return 0;
+    }
+}
+
+int oracle_decode(const float* Q, const float* K, const float* V,
+                  int B, int Hq, int Hkv, int S_q, int S_cap, int d,
+                  double scale, int kind, int window, const int* cache_len,
+                  double* O, double* LSE)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || S_q < 1 || S_cap < 1 || d < 1 || Hq % Hkv != 0) return -1;
+    if (kind != ORACLE_MASK_FULL && kind != ORACLE_MASK_CAUSAL && kind != ORACLE_MASK_CAUSAL_SLIDING)
+        return -1;
+    if (kind == ORACLE_MASK_CAUSAL_SLIDING && window < 0) return -1;
+    for (int b = 0; b < B; ++b) {
+        if (cache_len[b] < 1 || cache_len[b] > S_cap) return -1;
+        if (kind != ORACLE_MASK_FULL && cache_len[b] < S_q) return -1;
+    }
+    const int group = Hq / Hkv;
+    const long n = (long)B * Hq * S_q;
+    int failed = 0;
+
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)S_cap);
+        double* acc = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!s || !acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < n; ++r) {
+            if (!s || !acc) continue;
+            const int b = (int)(r / ((long)Hq * S_q));
+            const int a = (int)((r / S_q) % Hq);
+            const long i = r % S_q;
+            const long L = cache_len[b];
+            const long t = L - S_q + i; /* position of this query row */
+            const int ga = a / group;   /* g(a) */
+            const float* q = Q + (size_t)r * d;
+            const float* Kh = K + ((size_t)b * Hkv + ga) * (size_t)S_cap * d;
+            const float* Vh = V + ((size_t)b * Hkv + ga) * (size_t)S_cap * d;
+
+            double m = -INFINITY;
+            for (long j = 0; j < L; ++j) {
+                if (!oracle_decode_allowed(kind, t, j, L, window)) continue;
+                const float* k = Kh + (size_t)j * d;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
+                s[j] = dot * scale;
+                if (s[j] > m) m = s[j];
+            }
+            for (int c = 0; c < d; ++c) acc[c] = 0.0;
+            double l = 0.0;
+            if (m != -INFINITY) {
+                for (long j = 0; j < L; ++j) {
+                    if (!oracle_decode_allowed(kind, t, j, L, window)) continue;
+                    const double e = exp(s[j] - m);
+                    l += e;
+                    const float* v = Vh + (size_t)j * d;
+                    for (int c = 0; c < d; ++c) acc[c] += e * (double)v[c];
+                }
+            }
+            double* o = O + (size_t)r * d;
+            if (l > 0.0) {
+                for (int c = 0; c < d; ++c) o[c] = acc[c] / l;
+                LSE[r] = m + log(l);
+            } else {
+                for (int c = 0; c < d; ++c) o[c] = 0.0;
+                LSE[r] = -INFINITY;
+            }
+        }
+        free(s);
+        free(acc);
+    }
+    return failed ? -1 : 0;
+}

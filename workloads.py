@@ -116,3 +116,111 @@ def allowed_pairs_per_head(w: Workload) -> int:
 def useful_flops(w: Workload) -> int:
     """4 * d flops per allowed pair (2d for the score, 2d for the weighted sum)."""
     return 4 * w.d * allowed_pairs_per_head(w) * w.B * w.Hq
+
+
+# ----------------------------------------------------------------------------- decode
+# Key/value-cache attention: S_q new query rows per sequence against a cache of
+# capacity S_cap holding cache_len[b] positions of sequence b (ragged batch).
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    S_q: int
+    S_cap: int
+    d: int
+    kind: int
+    window: int = 0
+    seed: int = 0
+    len_min: int = 0        # cache lengths drawn uniformly from [len_min, S_cap]; 0 = all S_cap
+    dtype: str = "bf16"
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    def with_(self, **kw) -> "DecodeWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# Long-context GQA decode (the 32K GQA head layout, one new token per sequence,
+# eight sequences with ragged cache lengths in [16K, 32K]).
+DECODE_GQA_32K = DecodeWorkload("decode_gqa_B8_Hq64_Hkv8_Sq1_cache32768_d128", 8, 64, 8, 1, 32768, 128,
+                                MASK_CAUSAL, seed=10, len_min=16384)
+# Four new positions per sequence (a chunk of prefill or of speculative tokens).
+DECODE_GQA_CHUNK4 = DecodeWorkload("decode_gqa_B8_Hq32_Hkv8_Sq4_cache8192_d128", 8, 32, 8, 4, 8192, 128,
+                                   MASK_CAUSAL, seed=11, len_min=1024)
+# Multi-query decode: every query head shares one key/value head.
+DECODE_MQA_16K = DecodeWorkload("decode_mqa_B16_Hq32_Hkv1_Sq1_cache16384_d128", 16, 32, 1, 1, 16384, 128,
+                                MASK_CAUSAL, seed=12, len_min=2048)
+# Sliding-window GQA decode (the window of the 16K sliding-window workload).
+DECODE_SWA_16K = DecodeWorkload("decode_swa_B4_Hq32_Hkv8_Sq1_cache16384_d128_w4095", 4, 32, 8, 1, 16384, 128,
+                                MASK_CAUSAL_SLIDING, window=4095, seed=13, len_min=4096)
+# Cross-attention: 32 decoder rows against a 4096-position encoder output, d = 64.
+CROSS_MHA_4K = DecodeWorkload("cross_mha_B4_H16_Sq32_enc4096_d64", 4, 16, 16, 32, 4096, 64, MASK_FULL,
+                              seed=14)
+
+DECODE_ALL = (DECODE_GQA_32K, DECODE_GQA_CHUNK4, DECODE_MQA_16K, DECODE_SWA_16K, CROSS_MHA_4K)
+DECODE_BY_NAME = {w.name: w for w in DECODE_ALL}
+
+
+def make_decode_inputs(w: DecodeWorkload, device: Optional[str] = None, stale_fill: float = 0.0):
+    """Seeded Q [B,Hq,S_q,d], K, V [B,Hkv,S_cap,d] and cache lengths [B] (list of int).
+
+    Draw order: Q, K, V (iid N(0, 1)), then the cache lengths.  Cache positions at
+    or beyond a sequence's length are stale: they are set to ``stale_fill``
+    (NaN in the tests, so that reading one shows up).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    Q = torch.randn(w.B, w.Hq, w.S_q, w.d, generator=g, dtype=torch.float32)
+    K = torch.randn(w.B, w.Hkv, w.S_cap, w.d, generator=g, dtype=torch.float32)
+    V = torch.randn(w.B, w.Hkv, w.S_cap, w.d, generator=g, dtype=torch.float32)
+    if w.len_min > 0:
+        lens = torch.randint(w.len_min, w.S_cap + 1, (w.B,), generator=g).tolist()
+    else:
+        lens = [w.S_cap] * w.B
+    for b, L in enumerate(lens):
+        K[b, :, L:] = stale_fill
+        V[b, :, L:] = stale_fill
+    Q, K, V = (t.to(w.torch_dtype) for t in (Q, K, V))
+    if device is not None:
+        Q, K, V = (t.to(device) for t in (Q, K, V))
+    return Q, K, V, lens
+
+
+def decode_keys_per_row(w: DecodeWorkload, L: int, i: int) -> int:
+    """Closed-form count of the keys query row i sees in a sequence with L cached positions."""
+    if w.kind == MASK_FULL:
+        return L
+    t = L - w.S_q + i
+    if w.kind == MASK_CAUSAL:
+        return t + 1
+    return min(t, w.window) + 1  # causal sliding window
+
+
+def decode_useful_flops(w: DecodeWorkload, lens) -> int:
+    """4 * d flops per allowed (query row, key) pair."""
+    pairs = sum(decode_keys_per_row(w, L, i) for L in lens for i in range(w.S_q))
+    return 4 * w.d * pairs * w.Hq
+
+
+def decode_bytes(w: DecodeWorkload, lens) -> int:
+    """Algorithmic HBM bytes of one decode call: every key and value row some query of the
+    group sees, read once per (sequence, kv head), plus Q and O (2 bytes) and LSE (4 bytes)."""
+    el = 2 if w.dtype == "bf16" else 4
+    kv_rows = 0
+    for L in lens:
+        if w.kind == MASK_CAUSAL_SLIDING:
+            lo = max(0, L - w.S_q - w.window)
+        else:
+            lo = 0
+        kv_rows += L - lo
+    kv = 2 * kv_rows * w.Hkv * w.d * el
+    qo = 2 * w.B * w.Hq * w.S_q * w.d * el
+    return kv + qo + 4 * w.B * w.Hq * w.S_q
