@@ -233,6 +233,93 @@ attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d_k, float s
                                  int n_global, const void* Q, const void* K, const void* V,
                                  void* O, float* LSE, void* stream);
 
+/*
+ * ---------------------------------------------------------------- decode
+ * Decode / key-value-cache attention: S_q new query rows per sequence
+ * against a cache of keys and values.
+ *
+ *   - The step-t output Softmax(q_t K_{1:t}^T / sqrt(d_k)) V_{1:t} of a new
+ *     query against every cached key and value: "Trasformer 浅析"
+ *     (atffang.github.io), section 推理：KV 缓存.
+ *   - Ragged batches (sequence r holds S_r cached positions) and prefill run in
+ *     chunks: "第 8 章 现代大模型架构" (theaiera.top), section
+ *     预填充创建缓存，解码复用缓存.  Row i of sequence b is the position
+ *     t = cache_len[b] - S_q + i; its own key and value are already in the cache.
+ *   - Cross-attention (queries from the decoder, keys and values from the
+ *     encoder, an n_dec x n_enc score matrix): "Trasformer 浅析", section
+ *     交叉注意力.  Use ATTN_MASK_FULL with the encoder output as the cache.
+ *
+ * Mask kinds: ATTN_MASK_FULL (every j < cache_len[b]), ATTN_MASK_CAUSAL
+ * (j <= t), ATTN_MASK_CAUSAL_SLIDING (t - window <= j <= t).  The other kinds
+ * return ATTN_ERR_UNSUPPORTED.
+ *
+ * Layouts (contiguous, head dimension fastest, bfloat16):
+ *     Q, O : [B, Hq, S_q, d_k]     K, V (the cache) : [B, Hkv, S_cap, d_k]
+ *     LSE  : [B, Hq, S_q] float32 (natural logarithm), may be NULL.
+ * Cache positions at or past cache_len[b] are never used; they may hold
+ * anything, NaN included.
+ *
+ * Limits: B <= ATTN_DECODE_MAX_BATCH; (Hq / Hkv) * S_q <= ATTN_DECODE_MAX_ROWS
+ * (all query rows of a kv head's group go through one tile); d_k 64 or 128.
+ *
+ * Ownership and threading as for attn_create: the handle owns an error word,
+ * the arrival counters and the partial-result area of split sequences; a
+ * handle must not be used by two calls in flight at once.
+ */
+#define ATTN_DECODE_MAX_BATCH 1024
+#define ATTN_DECODE_MAX_ROWS 64
+typedef struct attn_decode_plan* attn_decode_handle;
+
+/*
+ * attn_decode_create -- validate the shape and allocate the handle.
+ *   B, Hq, Hkv : batch (1 .. ATTN_DECODE_MAX_BATCH), query heads, kv heads
+ *                (Hq % Hkv == 0; query head a uses kv head a / (Hq / Hkv)).
+ *   S_q        : new query rows per sequence (>= 1).
+ *   S_cap      : cache capacity in positions (>= 1; >= S_q for the causal kinds).
+ *   d_k, scale, kind, window : as for attn_create (window: CAUSAL_SLIDING only).
+ * Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ */
+attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, int S_q, int S_cap,
+                               int d_k, float scale, attn_mask_kind kind, int window);
+
+/*
+ * attn_decode_forward -- enqueue one decode step on `stream` and return.
+ *   Q, K, V, O, LSE : device pointers (16-byte aligned) in the layouts above.
+ *   cache_len       : HOST array of B lengths, each in [1, S_cap], and >= S_q
+ *                     for the causal kinds; read before the call returns.
+ * The keys of each sequence are cut into chunks of 128-key tiles so that the
+ * launch fills the GPU; a sequence split into several chunks is combined on
+ * the device by the last of its chunks to finish.
+ * Errors: ATTN_ERR_INVALID_ARG (pointers, lengths), ATTN_ERR_CUDA.  Device
+ * watchdog errors are read by attn_decode_poll_device_error; after one, the
+ * outputs of that call are undefined (the handle stays usable).
+ */
+attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void* K, const void* V,
+                                const int* cache_len, void* O, float* LSE, void* stream);
+
+/* attn_decode_poll_device_error -- as attn_poll_device_error, for a decode handle. */
+attn_status attn_decode_poll_device_error(attn_decode_handle h, int* code);
+
+/* attn_decode_destroy -- free the handle (synchronises the device first); NULL is ignored. */
+attn_status attn_decode_destroy(attn_decode_handle h);
+
+/*
+ * attn_decode_schedule_host -- the chunking attn_decode_forward uses, on the
+ * host only (no CUDA call).  Sequence b covers the key tiles
+ * [lo_b, hi_b) with hi_b = ceil(cache_len[b] / ATTN_TILE) and lo_b = 0, or for
+ * CAUSAL_SLIDING lo_b = max(0, cache_len[b] - S_q - window) / ATTN_TILE; it is
+ * cut into chunks of *tiles_per_chunk tiles (the last one shorter), and its
+ * chunks are numbered chunk_prefix[b] .. chunk_prefix[b+1]-1.  One launch runs
+ * chunk_prefix[B] x Hkv CTAs.
+ *   n_sm           : multiprocessors to fill (the CTAs of one launch aim at one
+ *                    per multiprocessor).
+ *   chunk_prefix   : output, B + 1 ints.
+ * Errors: ATTN_ERR_INVALID_ARG (shape or lengths as for the calls above).
+ */
+attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_mask_kind kind, int window,
+                                      const int* cache_len, int n_sm, int* tiles_per_chunk,
+                                      int* chunk_prefix);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,145 @@
+"""Decode / key-value-cache attention on the GPU vs the fp64 decode oracle (every output).
+
+The stale part of every cache (positions at or past a sequence's length) is filled
+with NaN, so a kernel that reads a stale key or value fails the finiteness check.
+Outputs are NaN-poisoned before each call, so an unwritten row fails too.  Small
+shapes cover every kind, both head widths, the 16/32/64 packed-row widths, ragged
+lengths on and off tile edges, one-position caches and sequences split into many
+key chunks (merged on the device); the five decode workloads run at full size in
+the launch configuration bench.py times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_util import BF16_MAX_ABS, BF16_REL_L2, LSE_ABS
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, Q, K, V, lens, plan=None, reps=1):
+    import transformer_self_attention_gb300 as tsa
+    if plan is None:
+        plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind,
+                                   window=w.window)
+    out = []
+    for _ in range(reps):
+        O = torch.full_like(Q, float("nan"))
+        LSE = torch.full((w.B, w.Hq, w.S_q), float("nan"), dtype=torch.float32, device=Q.device)
+        plan(Q, K, V, lens, O=O, LSE=LSE)
+        torch.cuda.synchronize()
+        st, code = plan.poll_device_error()
+        assert st == 0 and code == 0, f"device error word {code}"
+        out.append((O.float().cpu().numpy(), LSE.cpu().numpy()))
+    return out, plan
+
+
+def _compare(O, LSE, O_ref, L_ref):
+    assert np.isfinite(O).all(), "non-finite output (stale cache read or unwritten row)"
+    assert np.isfinite(LSE).all(), "non-finite LSE"
+    diff = O.astype(np.float64) - O_ref
+    max_abs = float(np.abs(diff).max())
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(O_ref), 1e-30))
+    lse = float(np.abs(LSE.astype(np.float64) - L_ref).max())
+    assert max_abs <= BF16_MAX_ABS, f"max abs error {max_abs:.3e}"
+    assert rel <= BF16_REL_L2, f"relative L2 error {rel:.3e}"
+    assert lse <= LSE_ABS, f"LSE error {lse:.3e}"
+    return max_abs, rel, lse
+
+
+def _check(w, reps=1):
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w, stale_fill=float("nan"))
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens, reps=reps)
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale,
+                                 w.kind, w.window)
+    res = [_compare(O, LSE, O_ref, L_ref) for O, LSE in outs]
+    if reps > 1:  # the same bits every call (the arrival counters wrap back to zero)
+        assert all(np.array_equal(outs[0][0], o) and np.array_equal(outs[0][1], l) for o, l in outs[1:])
+    return res[0]
+
+
+def _dw(name, B, Hq, Hkv, S_q, S_cap, d, kind, window=0, len_min=0, seed=21):
+    return wl.DecodeWorkload(name, B, Hq, Hkv, S_q, S_cap, d, kind, window=window, seed=seed, len_min=len_min)
+
+
+@pytest.mark.parametrize("kind", [wl.MASK_FULL, wl.MASK_CAUSAL, wl.MASK_CAUSAL_SLIDING])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_kinds_ragged(kind, d):
+    """Ragged lengths in [S_q, 700]: chunks of one tile each, merged on the device."""
+    _check(_dw("k", 5, 8, 2, 2, 700, d, kind, window=150, len_min=2))
+
+
+@pytest.mark.parametrize("Hq,Hkv,S_q", [(8, 8, 1), (8, 1, 1), (16, 2, 2), (32, 1, 1), (8, 2, 8), (64, 1, 1),
+                                        (8, 8, 7)])
+def test_decode_packed_row_widths(Hq, Hkv, S_q):
+    """group * S_q from 1 to 64 packed rows (16-, 32- and 64-column tiles)."""
+    _check(_dw("r", 3, Hq, Hkv, S_q, 520, 128, wl.MASK_CAUSAL, len_min=S_q))
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 128, 129, 255, 256, 257])
+def test_decode_cache_length_edges(L):
+    """Cache lengths at and around tile edges, down to a single cached position."""
+    w = _dw("e", 1, 4, 1, 1, 300, 128, wl.MASK_CAUSAL)
+    Qc, Kc, Vc, _ = wl.make_decode_inputs(w.with_(S_cap=300), stale_fill=float("nan"))
+    Kc[:, :, L:] = float("nan")
+    Vc[:, :, L:] = float("nan")
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), [L])
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), [L], w.scale, w.kind)
+    _compare(*outs[0], O_ref, L_ref)
+
+
+@pytest.mark.parametrize("w_", [0, 1, 127, 128, 129, 300])
+def test_decode_sliding_windows(w_):
+    _check(_dw("w", 2, 8, 2, 3, 900, 64, wl.MASK_CAUSAL_SLIDING, window=w_, len_min=3))
+
+
+def test_cross_attention_more_decoder_rows_than_encoder_positions():
+    """FULL mask with encoder lengths shorter than the 32 decoder rows."""
+    w = _dw("c", 3, 2, 2, 32, 64, 64, wl.MASK_FULL)
+    Qc, Kc, Vc, _ = wl.make_decode_inputs(w)
+    lens = [1, 17, 64]
+    for b, L in enumerate(lens):
+        Kc[b, :, L:] = float("nan")
+        Vc[b, :, L:] = float("nan")
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens)
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale, w.kind)
+    _compare(*outs[0], O_ref, L_ref)
+
+
+def test_decode_sharp_scores_rescale():
+    """Query rows scaled by 30 so the running max jumps between tiles (the lazy rescale path)."""
+    w = _dw("s", 2, 8, 2, 1, 1500, 128, wl.MASK_CAUSAL, len_min=900)
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w, stale_fill=float("nan"))
+    Qc = (Qc.float() * 30).to(torch.bfloat16)
+    Kc[:, :, :, :] = Kc.float() * torch.linspace(0.2, 1.5, 1500)[None, None, :, None]
+    for b, L in enumerate(lens):
+        Kc[b, :, L:] = float("nan")
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens)
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale, w.kind)
+    _compare(*outs[0], O_ref, L_ref)
+
+
+def test_decode_repeated_calls_are_identical():
+    _check(_dw("rep", 4, 16, 2, 1, 2000, 128, wl.MASK_CAUSAL, len_min=500), reps=3)
+
+
+def test_decode_step_equals_prefill_row():
+    """One decode step over a full cache gives the prefill kernel's last row (to the bf16 bound)."""
+    import transformer_self_attention_gb300 as tsa
+    S, d = 600, 128
+    w = wl.Workload("p", 1, 8, 2, S, d, "bf16", wl.MASK_CAUSAL, seed=5)
+    Q, K, V = (t.cuda() for t in wl.make_inputs(w))
+    O_pre, L_pre = tsa.Attention(1, 8, 2, S, d, kind=wl.MASK_CAUSAL)(Q, K, V)
+    dec = tsa.DecodeAttention(1, 8, 2, 1, S, d, kind=wl.MASK_CAUSAL)
+    O_dec, L_dec = dec(Q[:, :, S - 1:].contiguous(), K, V, [S])
+    torch.cuda.synchronize()
+    assert (O_dec.float() - O_pre[:, :, S - 1:].float()).abs().max().item() <= 2 * BF16_MAX_ABS
+    assert (L_dec - L_pre[:, :, S - 1:]).abs().max().item() <= 2 * LSE_ABS
+
+
+@pytest.mark.parametrize("w", wl.DECODE_ALL, ids=lambda w: w.name)
+def test_decode_workloads_full_size(w):
+    """The decode workloads at full size, every output against the oracle."""
+    _check(w)

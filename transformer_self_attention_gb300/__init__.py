@@ -26,8 +26,12 @@ WORK_INTS = 8
 WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
 
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
-            "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2")
+            "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
+            "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
+            "attn_decode_schedule_host")
 NOALLOC_SCRATCH_BYTES = 8 << 20
+DECODE_MAX_BATCH = 1024
+DECODE_MAX_ROWS = 64
 
 
 class AttnError(RuntimeError):
@@ -60,6 +64,16 @@ def _load():
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
     lib.attn_selftest_exp2.restype = I
+    lib.attn_decode_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I, F, I, I]
+    lib.attn_decode_create.restype = I
+    lib.attn_decode_forward.argtypes = [P, P, P, P, P, P, P, P]
+    lib.attn_decode_forward.restype = I
+    lib.attn_decode_poll_device_error.argtypes = [P, ctypes.POINTER(I)]
+    lib.attn_decode_poll_device_error.restype = I
+    lib.attn_decode_destroy.argtypes = [P]
+    lib.attn_decode_destroy.restype = I
+    lib.attn_decode_schedule_host.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I), P]
+    lib.attn_decode_schedule_host.restype = I
     return lib
 
 
@@ -143,6 +157,97 @@ def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):
     if st != ATTN_OK:
         raise AttnError(st, "attn_schedule_host")
     return items[: n.value], n_first.value
+
+
+# ---------------------------------------------------------------- decode (key/value cache)
+
+def attn_decode_create(B, Hq, Hkv, S_q, S_cap, d_k, scale, kind, window=0) -> int:
+    """Returns a decode handle (int); raises AttnError on a non-OK status."""
+    h = ctypes.c_void_p()
+    st = _lib.attn_decode_create(ctypes.byref(h), int(B), int(Hq), int(Hkv), int(S_q), int(S_cap), int(d_k),
+                                 float(scale), int(kind), int(window))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode_create")
+    return h.value
+
+
+def attn_decode_forward(handle: int, q_ptr: int, k_ptr: int, v_ptr: int, cache_len, o_ptr: int,
+                        lse_ptr: int = 0, stream: int = 0) -> int:
+    """Enqueue one decode step (cache_len: host sequence of B ints); returns the status."""
+    lens, n = _int_array(cache_len)
+    return _lib.attn_decode_forward(handle, q_ptr, k_ptr, v_ptr, ctypes.cast(lens, ctypes.c_void_p), o_ptr,
+                                    lse_ptr or None, stream or None)
+
+
+def attn_decode_poll_device_error(handle: int):
+    code = ctypes.c_int(0)
+    st = _lib.attn_decode_poll_device_error(handle, ctypes.byref(code))
+    return st, code.value
+
+
+def attn_decode_destroy(handle: int) -> int:
+    return _lib.attn_decode_destroy(handle)
+
+
+def attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, cache_len, n_sm):
+    """Host-only decode chunking: (tiles_per_chunk, chunk_prefix int32 [B + 1]).  Raises AttnError."""
+    lens, n = _int_array(cache_len)
+    tpc = ctypes.c_int(0)
+    prefix = np.zeros(int(B) + 1, dtype=np.int32)
+    st = _lib.attn_decode_schedule_host(int(B), int(Hkv), int(S_q), int(S_cap), int(kind), int(window),
+                                        ctypes.cast(lens, ctypes.c_void_p), int(n_sm), ctypes.byref(tpc),
+                                        prefix.ctypes.data_as(ctypes.c_void_p))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode_schedule_host")
+    return tpc.value, prefix
+
+
+class DecodeAttention:
+    """A decode plan: S_q new query rows per sequence against a key/value cache.
+
+    Q: [B, Hq, S_q, d] bf16; K, V (the cache): [B, Hkv, S_cap, d] bf16; cache_len: B host ints.
+    Row i of sequence b sits at position cache_len[b] - S_q + i.  Returns (O like Q, LSE float32
+    [B, Hq, S_q]).
+    """
+
+    def __init__(self, B, Hq, Hkv, S_q, S_cap, d, scale=None, kind=MASK_CAUSAL, window=0):
+        import math
+        self.shape = (int(B), int(Hq), int(Hkv), int(S_q), int(S_cap), int(d))
+        self.scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+        self.kind, self.window = int(kind), int(window)
+        self.handle = attn_decode_create(B, Hq, Hkv, S_q, S_cap, d, self.scale, self.kind, self.window)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            attn_decode_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __call__(self, Q, K, V, cache_len, O=None, LSE=None, stream=None, want_lse=True):
+        import torch
+        B, Hq, Hkv, S_q, S_cap, d = self.shape
+        for name, t, shape in (("Q", Q, (B, Hq, S_q, d)), ("K", K, (B, Hkv, S_cap, d)), ("V", V, (B, Hkv, S_cap, d))):
+            if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shape:
+                raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor of shape {shape}")
+        if O is None:
+            O = torch.empty_like(Q)
+        if LSE is None and want_lse:
+            LSE = torch.empty((B, Hq, S_q), dtype=torch.float32, device=Q.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(Q.device)
+        st = attn_decode_forward(self.handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(), list(cache_len),
+                                 O.data_ptr(), LSE.data_ptr() if LSE is not None else 0, stream.cuda_stream)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_decode_forward")
+        return O, LSE
+
+    def poll_device_error(self):
+        return attn_decode_poll_device_error(self.handle)
 
 
 # ---------------------------------------------------------------- torch convenience

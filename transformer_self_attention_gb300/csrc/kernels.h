@@ -67,6 +67,32 @@ struct MergeParams {
     int BHq, S, d;
 };
 
+// Decode / key-value-cache attention (attn_decode.cu).  One CTA streams a chunk of
+// key tiles of one (sequence, kv head) against all the query rows of that kv head's
+// group (group * S_q rows, padded to NP columns of the transposed score tile).
+constexpr int kDecodeMaxBatch = 1024;
+struct DecodeParams {
+    CUtensorMap tm_q;    // Q as 2-D [B*Hq*S_q, d] bf16, box {64, NP}, 128B swizzle
+    CUtensorMap tm_k;    // K cache [B*Hkv, S_cap, d], box {64, 128, 1}
+    CUtensorMap tm_v;    // V cache [B*Hkv, S_cap, d]
+    void* o;             // O [B, Hq, S_q, d] bf16
+    float* lse;          // [B, Hq, S_q], may be null
+    float* part_o;       // split sequences: [slot][NP][d] fp32 partial O (normalised by its own sum)
+    float* part_lse;     // [slot][NP]
+    unsigned* counters;  // [B*Hkv] arrival counters of the split sequences (wrap to 0)
+    int* err;
+    long long watchdog_ns;
+    int B, Hq, Hkv, group, S_q, S_cap, rows;  // rows = group * S_q
+    int kind, window;
+    float scale_log2;
+    int tiles_per_chunk;
+    int total_chunks;    // grid.x; slot of CTA (x, g) = g * total_chunks + x
+    int len[kDecodeMaxBatch];                // cache length of each sequence
+    int chunk_prefix[kDecodeMaxBatch + 1];   // first chunk of each sequence
+};
+
+cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);
+
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
 cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
