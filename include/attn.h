@@ -287,12 +287,14 @@ attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, 
  *   Q, K, V, O, LSE : device pointers (16-byte aligned) in the layouts above.
  *   cache_len       : HOST array of B lengths, each in [1, S_cap], and >= S_q
  *                     for the causal kinds; read before the call returns.
- * The keys of each sequence are cut into chunks of 128-key tiles so that the
- * launch fills the GPU; a sequence split into several chunks is combined on
- * the device by the last of its chunks to finish.
+ * The (sequence, kv head) units are laid end to end as one list of 128-key
+ * tiles and a persistent grid of one CTA per multiprocessor takes equal shares
+ * of it; a unit cut between CTAs is combined on the device by the last of them
+ * to finish.
  * Errors: ATTN_ERR_INVALID_ARG (pointers, lengths), ATTN_ERR_CUDA.  Device
- * watchdog errors are read by attn_decode_poll_device_error; after one, the
- * outputs of that call are undefined (the handle stays usable).
+ * watchdog errors are read by attn_decode_poll_device_error; the outputs of
+ * that call are then undefined (the poll resets the handle's counters, so the
+ * handle stays usable).
  */
 attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void* K, const void* V,
                                 const int* cache_len, void* O, float* LSE, void* stream);
@@ -300,25 +302,30 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
 /* attn_decode_poll_device_error -- as attn_poll_device_error, for a decode handle. */
 attn_status attn_decode_poll_device_error(attn_decode_handle h, int* code);
 
+/*
+ * attn_decode_set_grid_limit -- test hook: run at most max_ctas CTAs (>= 1) per
+ * launch instead of one per multiprocessor, so that small problems exercise long
+ * shares spanning several units.  Errors: ATTN_ERR_INVALID_ARG.
+ */
+attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas);
+
 /* attn_decode_destroy -- free the handle (synchronises the device first); NULL is ignored. */
 attn_status attn_decode_destroy(attn_decode_handle h);
 
 /*
- * attn_decode_schedule_host -- the chunking attn_decode_forward uses, on the
- * host only (no CUDA call).  Sequence b covers the key tiles
- * [lo_b, hi_b) with hi_b = ceil(cache_len[b] / ATTN_TILE) and lo_b = 0, or for
- * CAUSAL_SLIDING lo_b = max(0, cache_len[b] - S_q - window) / ATTN_TILE; it is
- * cut into chunks of *tiles_per_chunk tiles (the last one shorter), and its
- * chunks are numbered chunk_prefix[b] .. chunk_prefix[b+1]-1.  One launch runs
- * chunk_prefix[B] x Hkv CTAs.
- *   n_sm           : multiprocessors to fill (the CTAs of one launch aim at one
- *                    per multiprocessor).
- *   chunk_prefix   : output, B + 1 ints.
- * Errors: ATTN_ERR_INVALID_ARG (shape or lengths as for the calls above).
+ * attn_decode_schedule_host -- the work split attn_decode_forward uses, on the
+ * host only (no CUDA call).  Sequence b needs the key tiles [lo_b, hi_b) with
+ * hi_b = ceil(cache_len[b] / ATTN_TILE) and lo_b = 0, or for CAUSAL_SLIDING
+ * lo_b = max(0, cache_len[b] - S_q - window) / ATTN_TILE.  With
+ * n_b = hi_b - lo_b, tile_prefix[b] = n_0 + ... + n_{b-1}; unit (b, g) covers
+ * the indices [Hkv * tile_prefix[b] + g * n_b, ... + n_b) of one list of
+ * T = Hkv * tile_prefix[B] tiles, and CTA k of the *n_cta = min(n_sm, T) CTAs
+ * takes the indices [k * T / n_cta, (k + 1) * T / n_cta) (integer division).
+ *   tile_prefix : output, B + 1 ints.
+ * Errors: ATTN_ERR_INVALID_ARG (n_sm < 1, shape or lengths as for the calls above).
  */
 attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_mask_kind kind, int window,
-                                      const int* cache_len, int n_sm, int* tiles_per_chunk,
-                                      int* chunk_prefix);
+                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix);
 
 #ifdef __cplusplus
 }

@@ -1,14 +1,19 @@
-"""The decode chunking (host only) against brute force from the oracle's decode predicate.
+"""The decode work split (host only) against brute force from the oracle's decode predicate.
 
-The key tiles a CTA streams are derived from (tiles_per_chunk, chunk_prefix) exactly
-as the kernel derives them; the chunks of every sequence must cover its key-tile
-range once, in order and without empty chunks, and that range must hold every key
-some query row of the sequence is allowed to see (and begin at the first tile
-holding one).  Bit-exact; no GPU.
+The kernel's arithmetic is restated here: unit (b, g) covers the indices
+[Hkv * prefix[b] + g * n_b, ... + n_b) of one list of T tiles, and CTA k takes
+[k*T/n_cta, (k+1)*T/n_cta).  Checked bit-exactly, without a GPU:
+  * every key tile a sequence needs (some query row may see one of its keys, by
+    enumeration of the oracle's predicate) is in its range, and the range starts
+    and ends at such tiles;
+  * every tile of every unit belongs to exactly one CTA, and the shares differ in
+    size by at most one tile;
+  * only a CTA's first and last stretches can be partial units, and the partial-
+    result slots the writers use (2k for a first stretch, 2k+1 for a last one)
+    are exactly the slots the merge of each unit enumerates.
 """
 import random
 
-import numpy as np
 import pytest
 
 import oracle
@@ -18,20 +23,11 @@ T = tsa.TILE
 KINDS = (tsa.MASK_FULL, tsa.MASK_CAUSAL, tsa.MASK_CAUSAL_SLIDING)
 
 
-def _kernel_chunks(tpc, prefix, b, kind, S_q, window, L):
-    """The key tiles of each chunk of sequence b, as the kernel computes them."""
-    t_lo = max(0, L - S_q - window) // T if kind == tsa.MASK_CAUSAL_SLIDING else 0
-    t_hi = (L + T - 1) // T
-    out = []
-    for c in range(prefix[b + 1] - prefix[b]):
-        t0 = t_lo + c * tpc
-        n = min(t_hi, t0 + tpc) - t0
-        out.append((t0, t0 + n))
-    return out
+def _tile_lo(kind, S_q, window, L):
+    return max(0, L - S_q - window) // T if kind == tsa.MASK_CAUSAL_SLIDING else 0
 
 
 def _needed_tiles(kind, S_q, window, L):
-    """Key tiles holding at least one key some row may see (brute force over the predicate)."""
     tiles = set()
     for i in range(S_q):
         t = L - S_q + i
@@ -41,59 +37,104 @@ def _needed_tiles(kind, S_q, window, L):
     return tiles
 
 
+def _stretches(Hkv, prefix, n_cta, total, k):
+    """The kernel's walk over CTA k's share: list of (b, g, first_tile_in_unit, count, whole)."""
+    i, end = k * total // n_cta, (k + 1) * total // n_cta
+    out = []
+    while i < end:
+        b = max(x for x in range(len(prefix) - 1) if Hkv * prefix[x] <= i)
+        n_b = prefix[b + 1] - prefix[b]
+        r = i - Hkv * prefix[b]
+        g, t_in = r // n_b, r % n_b
+        unit_begin = Hkv * prefix[b] + g * n_b
+        count = min(end, unit_begin + n_b) - i
+        out.append((b, g, t_in, count, t_in == 0 and count == n_b))
+        i += count
+    return out
+
+
+def _share_of(i, n_cta, total):
+    return ((i + 1) * n_cta + total - 1) // total - 1
+
+
 def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
-    tpc, prefix = tsa.attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, lens, n_sm)
-    assert tpc >= 1 and prefix[0] == 0
+    n_cta, prefix = tsa.attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, lens, n_sm)
+    prefix = [int(x) for x in prefix]
+    total = Hkv * prefix[B]
+    assert n_cta == min(n_sm, total)
+    # ranges of the sequences
     for b, L in enumerate(lens):
-        chunks = _kernel_chunks(tpc, prefix, b, kind, S_q, window, L)
-        assert 1 <= len(chunks) <= 256
-        assert all(e > s for s, e in chunks), "empty chunk"
-        assert all(chunks[k][1] == chunks[k + 1][0] for k in range(len(chunks) - 1))
-        covered = set(range(chunks[0][0], chunks[-1][1]))
+        lo = _tile_lo(kind, S_q, window, L)
+        hi = (L + T - 1) // T
+        assert prefix[b + 1] - prefix[b] == hi - lo
         need = _needed_tiles(kind, S_q, window, L)
-        assert need <= covered
-        assert min(covered) == min(need) and max(covered) == max(need)
-    n_cta = int(prefix[-1]) * Hkv
-    assert n_cta <= n_sm + B * Hkv
-    return tpc, prefix
+        assert need <= set(range(lo, hi)) and min(need) == lo and max(need) == hi - 1
+    # cover, balance, partial stretches and their slots
+    seen = {}
+    writer_slots = {}
+    sizes = []
+    for k in range(n_cta):
+        st = _stretches(Hkv, prefix, n_cta, total, k)
+        sizes.append(sum(c for _, _, _, c, _ in st))
+        for idx, (b, g, t_in, count, whole) in enumerate(st):
+            for t in range(t_in, t_in + count):
+                assert (b, g, t) not in seen
+                seen[(b, g, t)] = k
+            if not whole:
+                assert idx == 0 or idx == len(st) - 1, "a partial stretch in the middle of a share"
+                writer_slots.setdefault((b, g), set()).add(2 * k + (0 if idx == 0 else 1))
+    assert len(seen) == total
+    assert max(sizes) - min(sizes) <= 1
+    for (b, g), slots in writer_slots.items():
+        n_b = prefix[b + 1] - prefix[b]
+        unit_begin = Hkv * prefix[b] + g * n_b
+        k0, k1 = _share_of(unit_begin, n_cta, total), _share_of(unit_begin + n_b - 1, n_cta, total)
+        k0_first = k0 * total // n_cta == unit_begin
+        merge = {2 * k0 + (0 if k0_first else 1)} | {2 * kk for kk in range(k0 + 1, k1 + 1)}
+        assert slots == merge, (b, g, slots, merge)
+        assert len(slots) == k1 - k0 + 1 >= 2
+    return n_cta, prefix
 
 
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("S_q", [1, 2, 5])
-def test_decode_chunks_cover_the_allowed_keys(kind, S_q):
+def test_decode_split_covers_the_allowed_keys(kind, S_q):
     rng = random.Random(kind * 10 + S_q)
     for trial in range(6):
         B = rng.randint(1, 5)
         Hkv = rng.choice([1, 2, 8])
-        S_cap = rng.choice([S_q, 127, 128, 129, 300, 1000])
-        S_cap = max(S_cap, S_q)
+        S_cap = max(rng.choice([S_q, 127, 128, 129, 300, 1000]), S_q)
         lens = [rng.randint(S_q if kind != tsa.MASK_FULL else 1, S_cap) for _ in range(B)]
         window = rng.choice([0, 1, 127, 128, 200])
-        _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm=rng.choice([1, 7, 152]))
+        _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm=rng.choice([1, 3, 7, 152]))
 
 
-def test_decode_chunks_fill_the_gpu_for_long_caches():
-    """Eight long sequences with 8 kv heads: chunks sized so the launch is about one CTA per SM."""
+def test_decode_split_long_ragged_batch():
+    """Eight ragged 16K..30K caches with 8 kv heads on 152 SMs: equal shares, units cut across CTAs."""
     lens = [16384 + 2000 * b for b in range(8)]
-    tpc, prefix = tsa.attn_decode_schedule_host(8, 8, 1, 32768, tsa.MASK_CAUSAL, 0, lens, 152)
-    n_cta = int(prefix[-1]) * 8
-    assert 152 <= n_cta <= 152 + 64
-    total_tiles = sum((L + T - 1) // T for L in lens) * 8
-    assert tpc == -(-total_tiles // 152)
+    n_cta, prefix = tsa.attn_decode_schedule_host(8, 8, 1, 32768, tsa.MASK_CAUSAL, 0, lens, 152)
+    total = 8 * int(prefix[-1])
+    assert n_cta == 152
+    sizes = [(k + 1) * total // 152 - k * total // 152 for k in range(152)]
+    assert max(sizes) - min(sizes) <= 1
 
 
-def test_decode_chunk_cap_per_sequence():
-    """A single very long sequence on a large GPU is not split into more than 256 chunks."""
-    tpc, prefix = tsa.attn_decode_schedule_host(1, 1, 1, 1 << 20, tsa.MASK_CAUSAL, 0, [1 << 20], 100000)
-    assert prefix[1] <= 256 and tpc * prefix[1] >= (1 << 20) // T
+def test_decode_split_single_huge_unit():
+    """One long sequence with one kv head is spread over every CTA."""
+    n_cta, prefix = tsa.attn_decode_schedule_host(1, 1, 1, 1 << 20, tsa.MASK_CAUSAL, 0, [1 << 20], 152)
+    assert n_cta == 152 and prefix[1] == (1 << 20) // T
+
+
+def test_decode_split_fewer_tiles_than_sms():
+    n_cta, prefix = tsa.attn_decode_schedule_host(2, 1, 1, 300, tsa.MASK_CAUSAL, 0, [1, 200], 152)
+    assert n_cta == 3 and list(prefix) == [0, 1, 3]
 
 
 def test_decode_sliding_window_skips_old_tiles():
     """The causal window reads only the tiles of the last window + S_q positions."""
     L, w = 16384, 4095
-    tpc, prefix = tsa.attn_decode_schedule_host(1, 8, 1, L, tsa.MASK_CAUSAL_SLIDING, w, [L], 152)
-    chunks = _kernel_chunks(tpc, prefix, 0, tsa.MASK_CAUSAL_SLIDING, 1, w, L)
-    assert chunks[0][0] == (L - 1 - w) // T and chunks[-1][1] == L // T
+    n_cta, prefix = tsa.attn_decode_schedule_host(1, 8, 1, L, tsa.MASK_CAUSAL_SLIDING, w, [L], 152)
+    assert prefix[1] == L // T - (L - 1 - w) // T
 
 
 @pytest.mark.parametrize("args,status", [
@@ -114,8 +155,8 @@ def test_decode_schedule_validation(args, status):
 
 
 def test_cross_attention_lengths_may_be_shorter_than_the_query_rows():
-    tpc, prefix = tsa.attn_decode_schedule_host(2, 4, 32, 4096, tsa.MASK_FULL, 0, [3, 4096], 152)
-    assert prefix[1] == 1
+    n_cta, prefix = tsa.attn_decode_schedule_host(2, 4, 32, 4096, tsa.MASK_FULL, 0, [3, 4096], 152)
+    assert list(prefix) == [0, 1, 33]
 
 
 @pytest.mark.parametrize("kw,status", [

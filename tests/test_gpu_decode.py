@@ -19,11 +19,13 @@ from gpu_util import BF16_MAX_ABS, BF16_REL_L2, LSE_ABS
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, Q, K, V, lens, plan=None, reps=1):
+def _run(w, Q, K, V, lens, plan=None, reps=1, grid_limit=None):
     import transformer_self_attention_gb300 as tsa
     if plan is None:
         plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind,
                                    window=w.window)
+    if grid_limit:
+        plan.set_grid_limit(grid_limit)
     out = []
     for _ in range(reps):
         O = torch.full_like(Q, float("nan"))
@@ -49,9 +51,9 @@ def _compare(O, LSE, O_ref, L_ref):
     return max_abs, rel, lse
 
 
-def _check(w, reps=1):
+def _check(w, reps=1, grid_limit=None):
     Qc, Kc, Vc, lens = wl.make_decode_inputs(w, stale_fill=float("nan"))
-    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens, reps=reps)
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens, reps=reps, grid_limit=grid_limit)
     O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale,
                                  w.kind, w.window)
     res = [_compare(O, LSE, O_ref, L_ref) for O, LSE in outs]
@@ -69,6 +71,33 @@ def _dw(name, B, Hq, Hkv, S_q, S_cap, d, kind, window=0, len_min=0, seed=21):
 def test_decode_kinds_ragged(kind, d):
     """Ragged lengths in [S_q, 700]: chunks of one tile each, merged on the device."""
     _check(_dw("k", 5, 8, 2, 2, 700, d, kind, window=150, len_min=2))
+
+
+@pytest.mark.parametrize("limit", [1, 2, 3, 7, 20])
+@pytest.mark.parametrize("kind", [wl.MASK_FULL, wl.MASK_CAUSAL, wl.MASK_CAUSAL_SLIDING])
+def test_decode_long_shares(kind, limit):
+    """A small grid: every CTA walks many tiles of several units (whole units in the middle of
+    a share, partial ones at its ends), with the rescale, buffer-parity and merge paths."""
+    _check(_dw("L", 4, 8, 2, 2, 1500, 128, kind, window=600, len_min=300), grid_limit=limit)
+
+
+@pytest.mark.parametrize("limit", [1, 5])
+@pytest.mark.parametrize("Hq,Hkv,S_q,d", [(8, 1, 1, 128), (32, 1, 1, 64), (16, 1, 4, 128)])
+def test_decode_long_shares_row_widths(Hq, Hkv, S_q, d, limit):
+    _check(_dw("Lr", 3, Hq, Hkv, S_q, 1100, d, wl.MASK_CAUSAL, len_min=S_q + 200), grid_limit=limit)
+
+
+def test_decode_long_shares_sharp_rescale():
+    """Long shares with sharpening scores, so rows rescale many times within one CTA."""
+    w = _dw("sL", 2, 8, 2, 1, 3000, 128, wl.MASK_CAUSAL, len_min=2500)
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w, stale_fill=float("nan"))
+    Qc = (Qc.float() * 30).to(torch.bfloat16)
+    Kc[:, :, :, :] = Kc.float() * torch.linspace(0.2, 2.0, 3000)[None, None, :, None]
+    for b, L in enumerate(lens):
+        Kc[b, :, L:] = float("nan")
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens, grid_limit=3)
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale, w.kind)
+    _compare(*outs[0], O_ref, L_ref)
 
 
 @pytest.mark.parametrize("Hq,Hkv,S_q", [(8, 8, 1), (8, 1, 1), (16, 2, 2), (32, 1, 1), (8, 2, 8), (64, 1, 1),

@@ -28,7 +28,7 @@ WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
             "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
-            "attn_decode_schedule_host")
+            "attn_decode_schedule_host", "attn_decode_set_grid_limit")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -74,6 +74,8 @@ def _load():
     lib.attn_decode_destroy.restype = I
     lib.attn_decode_schedule_host.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I), P]
     lib.attn_decode_schedule_host.restype = I
+    lib.attn_decode_set_grid_limit.argtypes = [P, I]
+    lib.attn_decode_set_grid_limit.restype = I
     return lib
 
 
@@ -190,16 +192,16 @@ def attn_decode_destroy(handle: int) -> int:
 
 
 def attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, cache_len, n_sm):
-    """Host-only decode chunking: (tiles_per_chunk, chunk_prefix int32 [B + 1]).  Raises AttnError."""
+    """Host-only decode work split: (n_cta, tile_prefix int32 [B + 1]).  Raises AttnError."""
     lens, n = _int_array(cache_len)
-    tpc = ctypes.c_int(0)
+    n_cta = ctypes.c_int(0)
     prefix = np.zeros(int(B) + 1, dtype=np.int32)
     st = _lib.attn_decode_schedule_host(int(B), int(Hkv), int(S_q), int(S_cap), int(kind), int(window),
-                                        ctypes.cast(lens, ctypes.c_void_p), int(n_sm), ctypes.byref(tpc),
+                                        ctypes.cast(lens, ctypes.c_void_p), int(n_sm), ctypes.byref(n_cta),
                                         prefix.ctypes.data_as(ctypes.c_void_p))
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode_schedule_host")
-    return tpc.value, prefix
+    return n_cta.value, prefix
 
 
 class DecodeAttention:
@@ -248,6 +250,12 @@ class DecodeAttention:
 
     def poll_device_error(self):
         return attn_decode_poll_device_error(self.handle)
+
+    def set_grid_limit(self, max_ctas: int):
+        """Test hook: at most max_ctas CTAs per launch (long shares on small problems)."""
+        st = _lib.attn_decode_set_grid_limit(self.handle, int(max_ctas))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_decode_set_grid_limit")
 
 
 # ---------------------------------------------------------------- torch convenience

@@ -10,43 +10,49 @@
 // 预填充创建缓存，解码复用缓存, and the n_dec x n_enc cross-attention of
 // "Trasformer 浅析", section 交叉注意力.
 //
-// The work is bound by HBM: every key and value byte is used by group * S_q
-// query rows only.  So one CTA takes ALL query rows of one kv head's group
-// (a GQA/MQA group reads its shared cache once, "第 8 章", 8.2.2 on MQA's
-// single HBM read for h heads) and the tensor-core products are transposed so
-// that the 128 keys of a tile fill the MMA's M dimension and the packed query
-// rows its N dimension (NP = 16, 32 or 64 columns):
+// The work is bound by HBM: every key and value byte serves only the
+// group * S_q query rows of its kv head.  So a CTA takes ALL query rows of one
+// kv head's group at once (a GQA/MQA group reads its shared cache once,
+// "第 8 章", 8.2.2 on MQA's single HBM read for h heads), and the tensor-core
+// products are transposed so that the 128 keys of a tile fill the MMA's M
+// dimension and the packed query rows its N dimension (NP = 16, 32 or 64):
 //
 //   S^T [128 keys x NP]  = K_tile [128 x d]  . Q^T [d x NP]      (both K-major)
 //   O^T [d x NP]        += V_tile^T [d x 128] . P^T [128 x NP]   (V MN-major)
 //
-//   warp 4 (producer) : TMA loads of the packed Q rows (once) and of the K and
-//                       V tiles into a STAGES-deep ring of 128B-swizzled tiles.
+// Balance: the grid is persistent (one CTA per SM).  All (sequence, kv head)
+// units are laid end to end as one list of key tiles and every CTA takes an
+// equal contiguous share of it, so a CTA may finish the end of one unit and
+// start the next.  A unit cut between CTAs yields partial results (O
+// normalised by its own sum, and its LSE) that the last CTA of the unit to
+// finish combines with weights e^{LSE_c - LSE} (an arrival counter per unit
+// that wraps back to zero).
+//
+//   warp 4 (producer) : TMA loads of each unit's packed Q rows (double-
+//                       buffered) and of the K and V tiles into a STAGES-deep
+//                       ring of 128B-swizzled tiles.
 //   warp 5 (MMA)      : one thread issues QK(n+1) before PV(n) so that the
 //                       softmax of tile n+1 overlaps the PV of tile n (S^T is
 //                       double-buffered in tensor memory, P^T in shared memory).
 //   warps 0-3         : thread t owns key t of the tile (tensor-memory lane t)
-//                       and, for O^T, component t of d.  Row maxima over the
-//                       128 keys come from warp reductions plus a 4-warp
-//                       exchange; the running max/sum use exp2 on log2(e)-
-//                       prescaled scores with the lazy rescale (only when a
-//                       row's max grew by more than 2^8).  P^T goes to shared
-//                       memory in the MMA's K-major swizzled layout.
-//
-// Long caches are split into chunks of key tiles (several CTAs per sequence
-// and kv head); each chunk writes its O normalised by its own sum and its
-// LSE, and the last CTA of the sequence to finish (an atomic arrival counter
-// that wraps back to zero) combines them with weights e^{LSE_c - LSE}.
+//                       and component t of d in O^T.  Running max m and sums
+//                       in exp2 units of log2(e)-prescaled scores.  A tile
+//                       first checks every allowed score against its row's
+//                       running max; only when one exceeds it by more than 2^8
+//                       (always on a unit's first tile) are the exact tile
+//                       maxima formed (warp max reductions plus a 4-warp
+//                       exchange) and O^T and the sums rescaled.  P^T goes to
+//                       shared memory in the MMA's K-major swizzled layout.
 //
 // Stale cache entries (positions >= cache_len[b]) are never used: their scores
-// are masked, and the V rows of the last tile past the cache length are zeroed
-// in shared memory before the PV product (0 * NaN would otherwise be NaN).
-// Every mbarrier wait is bounded by the watchdog limit (see attn_fwd_tc.cu).
+// are masked, and the V rows of a sequence's last tile past its length are
+// zeroed in shared memory before the PV product (0 * NaN would be NaN).
+// Every mbarrier wait is bounded by the watchdog limit; after a wait runs out
+// the CTA records an error bit, drains its copies and MMAs and exits.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
 #include "kernels.h"
-#include "schedule.h"
 #include "sm103_ptx.h"
 
 namespace attn {
@@ -68,11 +74,12 @@ template <int D, int NP>
 struct DCfg {
     static constexpr int TB = BN * D * 2;         // one K or V tile
     static constexpr int SUB = BN * 128;          // one 64-column block of a K/V tile
-    static constexpr int QB = NP * 128;           // one 64-column block of the Q rows
+    static constexpr int QT = NP * D * 2;         // one packed Q tile
+    static constexpr int QB = NP * 128;           // one 64-column block of it
     static constexpr int PB = NP * 128;           // one 64-key half of a P^T buffer
     static constexpr int ZERO = (D == 64) ? SUB : 0;  // rows 64..127 of V^T when d = 64 (zeros)
     static constexpr int CTL = 8192;
-    static constexpr int FIXED = NP * D * 2 + 2 * 2 * PB + ZERO + CTL + 1024;
+    static constexpr int FIXED = 2 * QT + 2 * 2 * PB + ZERO + CTL + 1024;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / (2 * TB);
     static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
     static_assert(STAGES >= 2, "shared memory");
@@ -80,42 +87,41 @@ struct DCfg {
     static constexpr int OFF_K = OFF_V + STAGES * TB;
     static constexpr int OFF_Z = OFF_K + STAGES * TB;
     static constexpr int OFF_Q = OFF_Z + ZERO;
-    static constexpr int OFF_P = OFF_Q + NP * D * 2;
+    static constexpr int OFF_P = OFF_Q + 2 * QT;
     static constexpr int OFF_CTL = OFF_P + 2 * 2 * PB;
     static constexpr int SMEM_ALLOC = OFF_CTL + CTL + 1024;
     static constexpr uint32_t TMEM_COLS = (3 * NP <= 64) ? 64 : (3 * NP <= 128) ? 128 : 256;
     static constexpr uint32_t TMEM_S = 0;       // S^T buffers: columns [0, NP) and [NP, 2 NP)
     static constexpr uint32_t TMEM_O = 2 * NP;  // O^T: columns [2 NP, 3 NP)
-    // merge weights of a split sequence live in the (idle) K ring at the end
-    static constexpr int MAX_MERGE_CHUNKS = STAGES * TB / (NP * 4);
-    static_assert(MAX_MERGE_CHUNKS >= kDecodeMaxChunksPerSeq, "merge weights must fit the K ring");
 };
 
 enum Bar {
-    B_Q = 0,
-    B_KFULL = 1,
+    B_QFULL = 0,                      // 2: packed Q tile loaded
+    B_QEMPTY = B_QFULL + 2,           // 2: last QK of its unit done (MMA commit)
+    B_KFULL = B_QEMPTY + 2,
     B_KEMPTY = B_KFULL + MAX_STAGES,
     B_VFULL = B_KEMPTY + MAX_STAGES,
     B_VEMPTY = B_VFULL + MAX_STAGES,
     B_SFULL = B_VEMPTY + MAX_STAGES,  // 2: S^T buffer ready (MMA commit)
-    B_PFULL = B_SFULL + 2,            // 2: P^T buffer written, S^T buffer read (128 arrivals)
-    B_PFREE = B_PFULL + 2,            // 2: PV done with the P^T buffer (MMA commit)
-    B_OFULL = B_PFREE + 2,            // every PV (MMA commit)
-    NBAR = B_OFULL + 1
+    B_PFULL = B_SFULL + 2,            // 2: P^T written, S^T read, O^T rescaled / read out (128 arrivals)
+    B_PFREE = B_PFULL + 2,            // 2: PV(n) done, n of that parity (MMA commit)
+    NBAR = B_PFREE + 2
 };
 
 template <int NP>
 struct DShared {
     uint64_t bar[NBAR];
+    alignas(16) float m[NP];   // running max of each packed row (log2 units)
+    alignas(16) float alpha[NP];
+    alignas(16) float inv_l[NP];
+    alignas(16) float lse[NP];
+    int lo[NP], hi[NP];        // allowed key interval of each packed row in the current unit
+    int wmax[4][NP];           // per-warp tile maxima (order-preserving int encoding)
+    float lsum[4][NP];
     uint32_t tmem_base;
     volatile int abort;
     int is_last;
-    int flag[2];          // a row of this tile needs O and l rescaled
-    int wmax[2][4][NP];   // per-warp tile maxima, order-preserving int encoding
-    int lo[NP], hi[NP];   // allowed key interval of each packed row
-    float m[NP], alpha[NP];
-    float lsum[4][NP];
-    float l[NP], lse[NP];
+    int flag;                  // a row of this tile needs O^T and the sums rescaled
 };
 
 struct Watch {
@@ -157,6 +163,203 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
+// named barrier with an OR reduction of one predicate
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
+// ---------------------------------------------------------------- the shared tile list
+// First index of CTA k's share, and the CTA whose share holds index i.
+__device__ __forceinline__ long long share_begin(const DecodeParams& p, int k) {
+    return (long long)k * p.total_tiles / p.n_cta;
+}
+__device__ __forceinline__ int share_of(const DecodeParams& p, long long i) {
+    return (int)(((i + 1) * p.n_cta + p.total_tiles - 1) / p.total_tiles - 1);
+}
+
+// One unit's stretch of a CTA's share.
+struct Seg {
+    int b, g;
+    int L;             // cache length of the sequence
+    int n_unit;        // key tiles of the unit
+    int tile0;         // first key tile (absolute) of this stretch
+    int count;         // tiles in this stretch
+    long long unit_begin;
+    bool whole;        // the stretch is the whole unit
+};
+
+__device__ __forceinline__ Seg seg_at(const DecodeParams& p, long long i, long long end) {
+    int lo = 0, hi = p.B - 1;  // last sequence whose first index is <= i
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)p.Hkv * p.tile_prefix[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    Seg s;
+    s.b = lo;
+    s.n_unit = p.tile_prefix[lo + 1] - p.tile_prefix[lo];
+    const long long r = i - (long long)p.Hkv * p.tile_prefix[lo];
+    s.g = (int)(r / s.n_unit);
+    const int t_in = (int)(r - (long long)s.g * s.n_unit);
+    s.unit_begin = (long long)p.Hkv * p.tile_prefix[lo] + (long long)s.g * s.n_unit;
+    s.count = (int)(min(end, s.unit_begin + s.n_unit) - i);
+    s.whole = t_in == 0 && s.count == s.n_unit;
+    s.L = p.len[lo];
+    const int t_lo = p.kind == ATTN_MASK_CAUSAL_SLIDING ? max(0, s.L - p.S_q - p.window) / BN : 0;
+    s.tile0 = t_lo + t_in;
+    return s;
+}
+
+// Position in a CTA's share: stretch j (its Seg s), tile q of it.
+struct Walk {
+    long long i;   // first index of the current stretch
+    Seg s;
+    int j, q;
+    bool valid;
+};
+__device__ __forceinline__ Walk walk_begin(const DecodeParams& p, long long begin, long long end) {
+    Walk w;
+    w.i = begin;
+    w.j = 0;
+    w.q = 0;
+    w.valid = begin < end;
+    if (w.valid) w.s = seg_at(p, begin, end);
+    return w;
+}
+__device__ __forceinline__ void walk_next(const DecodeParams& p, Walk& w, long long end) {
+    if (!w.valid) return;
+    if (++w.q < w.s.count) return;
+    w.i += w.s.count;
+    ++w.j;
+    w.q = 0;
+    w.valid = w.i < end;
+    if (w.valid) w.s = seg_at(p, w.i, end);
+}
+
+// Partial-result slot of a stretch: 2k for the first stretch of CTA k's share, 2k+1 for its
+// last (only these two can be partial).
+__device__ __forceinline__ int part_slot(int k, bool first_of_share) { return 2 * k + (first_of_share ? 0 : 1); }
+
+// Combine the partial results of unit (b, g) once all its stretches have arrived.  Warp w
+// takes rows w, w+4, ...; every load of a phase is independent of the others, so the whole
+// merge costs a few L2 round trips: (1) lane l reads LSE_c of partial c = l (+32, ...) for
+// all the warp's rows, and warp reductions give M = max_c LSE_c and W = sum_c e^{LSE_c - M};
+// (2) lane l accumulates d components [l*D/32, (l+1)*D/32) of sum_c e^{LSE_c - M} O_c / W,
+// four partials and all rows at a time.  scratch_m / scratch_w: NP floats of shared memory.
+template <int D, int NP>
+__device__ void merge_unit(const DecodeParams& p, const Seg& s, int warp, int lane, float* scratch_m,
+                           float* scratch_w) {
+    const int k0 = share_of(p, s.unit_begin), k1 = share_of(p, s.unit_begin + s.n_unit - 1);
+    const int nseg = k1 - k0 + 1;
+    const bool k0_first = share_begin(p, k0) == s.unit_begin;
+    auto slot = [&](int c) -> size_t { return (size_t)(c == 0 ? part_slot(k0, k0_first) : part_slot(k0 + c, true)); };
+    const int row0 = (s.b * p.Hq + s.g * p.group) * p.S_q;
+    constexpr int PER = D / 32;
+    constexpr int R = NP / 4;  // rows per warp at most
+    // ---- (1) M and W of every row of this warp
+    float M[R], W[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i) { M[i] = -INFINITY; W[i] = 0.f; }
+    for (int c0 = 0; c0 < nseg; c0 += 32) {
+        const int c = c0 + lane;
+        float lv[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int r = warp + 4 * i;
+            lv[i] = (c < nseg && r < p.rows) ? __ldcg(p.part_lse + slot(c) * NP + r) : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            float mx = lv[i];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float m_new = fmaxf(M[i], mx);
+            float e = (lv[i] == -INFINITY) ? 0.f : __expf(lv[i] - m_new);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
+            W[i] = (M[i] == -INFINITY ? 0.f : W[i] * __expf(M[i] - m_new)) + e;
+            M[i] = m_new;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int r = warp + 4 * i;
+        if (lane == 0 && r < p.rows) {
+            scratch_m[r] = M[i];
+            scratch_w[r] = 1.f / W[i];
+            if (p.lse) p.lse[row0 + r] = M[i] + __logf(W[i]);
+        }
+    }
+    __syncwarp();
+    // ---- (2) O = sum_c e^{LSE_c - M} O_c / W
+    float acc[R][PER];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[i][e] = 0.f;
+    // loads of CB partials for all rows are issued before any of them is used (the cache-global
+    // loads are ordered, so program order decides how many are in flight)
+    constexpr int CB = NP <= 32 ? 2 : 1;
+    for (int c0 = 0; c0 < nseg; c0 += CB) {
+        float lv[CB][R];
+        float ov[CB][R][PER];
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+            const int c = c0 + u;
+            const size_t sl = slot(c < nseg ? c : 0);
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = warp + 4 * i;
+                lv[u][i] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < PER; ++e) ov[u][i][e] = 0.f;
+                if (c < nseg && r < p.rows) {
+                    lv[u][i] = __ldcg(p.part_lse + sl * NP + r);
+                    const float* src = p.part_o + (sl * NP + r) * D + lane * PER;
+                    if (PER == 4) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                        ov[u][i][0] = v.x; ov[u][i][1 % PER] = v.y; ov[u][i][2 % PER] = v.z; ov[u][i][3 % PER] = v.w;
+                    } else {
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                        ov[u][i][0] = v.x; ov[u][i][1 % PER] = v.y;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < CB; ++u)
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int r = warp + 4 * i;
+                if (r < p.rows) {
+                    const float w = lv[u][i] == -INFINITY ? 0.f : __expf(lv[u][i] - scratch_m[r]) * scratch_w[r];
+#pragma unroll
+                    for (int e = 0; e < PER; ++e) acc[i][e] += w * ov[u][i][e];
+                }
+            }
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int r = warp + 4 * i;
+        if (r < p.rows) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + (size_t)(row0 + r) * D + lane * PER;
+            if (PER == 4)
+                *reinterpret_cast<uint2*>(dst) =
+                    make_uint2(pack_bf16x2(acc[i][0], acc[i][1 % PER]), pack_bf16x2(acc[i][2 % PER], acc[i][3 % PER]));
+            else
+                *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[i][0], acc[i][1 % PER]);
+        }
+    }
+}
+
 template <int D, int NP>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<D, NP>;
@@ -173,50 +376,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- work of this CTA: sequence b, kv head g, key tiles [t0, t0 + n_iter)
-    const int x = blockIdx.x, g = blockIdx.y;
-    int b = 0;
-    {
-        int lo = 0, hi = p.B - 1;  // last sequence whose first chunk is <= x
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (p.chunk_prefix[mid] <= x) lo = mid; else hi = mid - 1;
-        }
-        b = lo;
-    }
-    const int chunk = x - p.chunk_prefix[b];
-    const int n_chunks = p.chunk_prefix[b + 1] - p.chunk_prefix[b];
-    const int L = p.len[b];
-    const bool sliding = p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    const int t_lo = sliding ? max(0, L - p.S_q - p.window) / BN : 0;
-    const int t_hi = (L + BN - 1) / BN;
-    const int t0 = t_lo + chunk * p.tiles_per_chunk;
-    const int n_iter = min(t_hi, t0 + p.tiles_per_chunk) - t0;  // >= 1 by construction of the chunks
-    const int bkv = b * p.Hkv + g;
-    const int row0 = (b * p.Hq + g * p.group) * p.S_q;  // first packed query row
-    // tightest bounds over the valid rows: a tile inside [max_lo, min_hi] needs no mask
-    const int max_lo = sliding ? L - 1 - p.window : 0;
-    const int min_hi = p.kind == ATTN_MASK_FULL ? L - 1 : L - p.S_q;
-    const int tail = (L % BN == 0) ? 0 : L % BN;  // valid keys of the last cache tile (0 = whole)
+    const int k = blockIdx.x;
+    const long long share0 = share_begin(p, k), share1 = share_begin(p, k + 1);
+    const int n_tiles = (int)(share1 - share0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == B_PFULL || i == B_PFULL + 1) ? 128u : 1u);
         sh->abort = 0;
-        sh->flag[0] = sh->flag[1] = 0;
+        sh->flag = 0;
         fence_barrier_init();
-    }
-    if (threadIdx.x < NP) {
-        const int r = threadIdx.x;
-        int lo = 0, hi = L - 1;
-        if (r < p.rows && p.kind != ATTN_MASK_FULL) {
-            const int pos = L - p.S_q + r % p.S_q;  // position of this query row
-            hi = pos;
-            if (sliding) lo = max(0, pos - p.window);
-        }
-        sh->lo[r] = lo;
-        sh->hi[r] = hi;
-        sh->m[r] = -INFINITY;
     }
     if (C::ZERO) {  // zero block standing in for V^T rows 64..127 when d = 64
         for (int i = threadIdx.x; i < C::ZERO / 16; i += NTHREADS)
@@ -240,32 +408,43 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            mbar_arrive_expect_tx(bar(B_Q), NP * D * 2);
-            for (int s = 0; s < D / 64; ++s) tma_load_2d(s_q + s * C::QB, &p.tm_q, bar(B_Q), s * 64, row0);
-            int k_loaded = 0, v_loaded = 0;
+            int n = 0, j = 0, k_loaded = 0, v_loaded = 0, q_loaded = 0;
             bool ok = true;
-            for (int n = 0; n < n_iter && ok; ++n) {
-                const int st = n % C::STAGES, round = n / C::STAGES;
-                const int key = (t0 + n) * BN;
-                if (n >= C::STAGES && !(ok = wait_bounded(bar(B_KEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
+            for (long long i = share0; i < share1 && ok; ++j) {
+                const Seg s = seg_at(p, i, share1);
+                i += s.count;
+                if (j >= 2 && !(ok = wait_bounded(bar(B_QEMPTY + (j & 1)), ((j >> 1) - 1) & 1, wd, ERR_PRODUCER)))
                     break;
-                mbar_arrive_expect_tx(bar(B_KFULL + st), C::TB);
-                for (int s = 0; s < D / 64; ++s)
-                    tma_load_3d(s_k + st * C::TB + s * C::SUB, &p.tm_k, bar(B_KFULL + st), s * 64, key, bkv);
-                k_loaded = n + 1;
-                if (n >= C::STAGES && !(ok = wait_bounded(bar(B_VEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
-                    break;
-                mbar_arrive_expect_tx(bar(B_VFULL + st), C::TB);
-                for (int s = 0; s < D / 64; ++s)
-                    tma_load_3d(s_v + st * C::TB + s * C::SUB, &p.tm_v, bar(B_VFULL + st), s * 64, key, bkv);
-                v_loaded = n + 1;
+                mbar_arrive_expect_tx(bar(B_QFULL + (j & 1)), C::QT);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_2d(s_q + (j & 1) * C::QT + c * C::QB, &p.tm_q, bar(B_QFULL + (j & 1)), c * 64,
+                                (s.b * p.Hq + s.g * p.group) * p.S_q);
+                q_loaded = j + 1;
+                const int bkv = s.b * p.Hkv + s.g;
+                for (int q = 0; q < s.count && ok; ++q, ++n) {
+                    const int st = n % C::STAGES, round = n / C::STAGES;
+                    const int key = (s.tile0 + q) * BN;
+                    if (n >= C::STAGES && !(ok = wait_bounded(bar(B_KEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
+                        break;
+                    mbar_arrive_expect_tx(bar(B_KFULL + st), C::TB);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(s_k + st * C::TB + c * C::SUB, &p.tm_k, bar(B_KFULL + st), c * 64, key, bkv);
+                    k_loaded = n + 1;
+                    if (n >= C::STAGES && !(ok = wait_bounded(bar(B_VEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
+                        break;
+                    mbar_arrive_expect_tx(bar(B_VFULL + st), C::TB);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(s_v + st * C::TB + c * C::SUB, &p.tm_v, bar(B_VFULL + st), c * 64, key, bkv);
+                    v_loaded = n + 1;
+                }
             }
             if (sh->abort) {  // let the copies in flight land before the CTA exits
-                drain_wait(bar(B_Q), 0, wd);
-                for (int n = max(0, k_loaded - C::STAGES); n < k_loaded; ++n)
-                    drain_wait(bar(B_KFULL + n % C::STAGES), (n / C::STAGES) & 1, wd);
-                for (int n = max(0, v_loaded - C::STAGES); n < v_loaded; ++n)
-                    drain_wait(bar(B_VFULL + n % C::STAGES), (n / C::STAGES) & 1, wd);
+                for (int jj = max(0, q_loaded - 2); jj < q_loaded; ++jj)
+                    drain_wait(bar(B_QFULL + (jj & 1)), (jj >> 1) & 1, wd);
+                for (int nn = max(0, k_loaded - C::STAGES); nn < k_loaded; ++nn)
+                    drain_wait(bar(B_KFULL + nn % C::STAGES), (nn / C::STAGES) & 1, wd);
+                for (int nn = max(0, v_loaded - C::STAGES); nn < v_loaded; ++nn)
+                    drain_wait(bar(B_VFULL + nn % C::STAGES), (nn / C::STAGES) & 1, wd);
             }
         }
     } else if (warp == WARP_MMA) {
@@ -278,48 +457,49 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
             return D == 128 ? (uint32_t)C::SUB : (uint32_t)(s_z - (s_v + st * C::TB));
         };
         int last_bar = -1, last_par = 0;  // the last commit (drained after an abort)
-        auto issue_qk = [&](int n) {
+        // QK of the CTA's tile n at walk position w (lane 0 only)
+        auto issue_qk = [&](int n, const Walk& w) -> bool {
             const int st = n % C::STAGES;
+            if (w.q == 0 && !wait_bounded(bar(B_QFULL + (w.j & 1)), (w.j >> 1) & 1, wd, ERR_MMA)) return false;
+            if (!wait_bounded(bar(B_KFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA)) return false;
+            tc_fence_after();
             const uint32_t t_s = tmem + C::TMEM_S + (n & 1) * NP;
+            const uint32_t sq = s_q + (w.j & 1) * C::QT;
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t a = s_k + st * C::TB + (k >> 2) * C::SUB + (k & 3) * 32;
-                const uint32_t bq = s_q + (k >> 2) * C::QB + (k & 3) * 32;
-                mma_ss(t_s, sdesc_sw128(a, 16, 1024), sdesc_sw128(bq, 16, 1024), idesc_qk, k > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t a = s_k + st * C::TB + (kk >> 2) * C::SUB + (kk & 3) * 32;
+                const uint32_t bq = sq + (kk >> 2) * C::QB + (kk & 3) * 32;
+                mma_ss(t_s, sdesc_sw128(a, 16, 1024), sdesc_sw128(bq, 16, 1024), idesc_qk, kk > 0);
             }
             mma_commit(bar(B_SFULL + (n & 1)));
             mma_commit(bar(B_KEMPTY + st));
             last_bar = B_SFULL + (n & 1);
             last_par = (n >> 1) & 1;
+            if (w.q == w.s.count - 1) mma_commit(bar(B_QEMPTY + (w.j & 1)));
+            return true;
         };
+        Walk wq = walk_begin(p, share0, share1);  // tile of the next QK
+        Walk wp = wq;                             // tile of the next PV
         bool ok = true;
-        if (lane == 0) {
-            ok = wait_bounded(bar(B_Q), 0, wd, ERR_MMA) && wait_bounded(bar(B_KFULL), 0, wd, ERR_MMA);
-            if (ok) {
-                tc_fence_after();
-                issue_qk(0);
-            }
-        }
+        if (lane == 0 && wq.valid) ok = issue_qk(0, wq);
+        walk_next(p, wq, share1);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         // The whole warp runs the loop (the exit is warp-uniform); lane 0 waits and issues.
-        for (int n = 0; n < n_iter && ok; ++n) {
+        for (int n = 0; n < n_tiles && ok; ++n) {
             const int st = n % C::STAGES;
             if (lane == 0) {
-                if (n + 1 < n_iter) {
-                    ok = wait_bounded(bar(B_KFULL + (n + 1) % C::STAGES), ((n + 1) / C::STAGES) & 1, wd, ERR_MMA);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_qk(n + 1);  // S^T buffer (n+1)&1 was released by the softmax before PV(n-1)
-                    }
-                }
+                if (wq.valid) ok = issue_qk(n + 1, wq);  // S^T buffer (n+1)&1 was released before PV(n-1)
                 if (ok) ok = wait_bounded(bar(B_PFULL + (n & 1)), (n >> 1) & 1, wd, ERR_MMA);
                 if (ok) ok = wait_bounded(bar(B_VFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA);
             }
+            walk_next(p, wq, share1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            if (tail != 0 && t0 + n == t_hi - 1) {
-                // the last cache tile: zero the V rows at and past the cache length.  Every lane
-                // observes the completed copy itself (the phase cannot advance before this PV).
+            const int tile = wp.s.tile0 + wp.q;
+            const int tail = wp.s.L % BN;
+            if (tail != 0 && tile == (wp.s.L - 1) / BN) {
+                // a sequence's last cache tile: zero the V rows at and past its length.  Every
+                // lane observes the completed copy itself (the phase cannot advance before this PV).
                 const bool seen = lane == 0 || wait_bounded(bar(B_VFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA);
                 if (!__all_sync(0xffffffffu, seen)) {
                     ok = false;
@@ -327,9 +507,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 }
                 uint8_t* vt = smem + C::OFF_V + st * C::TB;
                 const int nbytes = (BN - tail) * 128;
-                for (int s = 0; s < D / 64; ++s)
-                    for (int i = lane * 16; i < nbytes; i += 32 * 16)
-                        *reinterpret_cast<uint4*>(vt + s * C::SUB + tail * 128 + i) = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < D / 64; ++c)
+                    for (int x = lane * 16; x < nbytes; x += 32 * 16)
+                        *reinterpret_cast<uint4*>(vt + c * C::SUB + tail * 128 + x) = make_uint4(0, 0, 0, 0);
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -338,136 +518,171 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 const uint32_t t_o = tmem + C::TMEM_O;
                 const uint32_t pb = s_p + (n & 1) * 2 * C::PB;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint32_t a = s_v + st * C::TB + k * 16 * 128;  // 16 keys of 128-byte rows
-                    const uint32_t bp = pb + (k >> 2) * C::PB + (k & 3) * 32;
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint32_t a = s_v + st * C::TB + kk * 16 * 128;  // 16 keys of 128-byte rows
+                    const uint32_t bp = pb + (kk >> 2) * C::PB + (kk & 3) * 32;
                     mma_ss(t_o, sdesc_sw128(a, v_lbo(st), 1024), sdesc_sw128(bp, 16, 1024), idesc_pv,
-                           (n > 0 || k > 0) ? 1u : 0u);
+                           (wp.q > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_OFULL));
                 mma_commit(bar(B_VEMPTY + st));
                 mma_commit(bar(B_PFREE + (n & 1)));
                 last_bar = B_PFREE + (n & 1);
                 last_par = (n >> 1) & 1;
             }
+            walk_next(p, wp, share1);
         }
         if (lane == 0 && sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, wd);
     } else {
         // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
+        // Every thread runs the same sequence of named barriers whatever happens: waits are
+        // per thread and bounded, and after an abort they return at once and the remaining
+        // tiles are computed on whatever is in memory (the error word is set; outputs are
+        // then undefined), so no barrier is ever left incomplete.
         const int t = threadIdx.x;  // key within the tile == tensor-memory lane; d index of O^T
         const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
         const float sl2 = p.scale_log2;
-        // waits of the four softmax warps end with the same outcome in all of them (the
-        // loop below has named barriers, so every exit must be taken by all 128 threads)
-        auto sm_wait = [&](int b_, uint32_t parity) {
-            return named_bar_and(1, 128, wait_bounded(bar(b_), parity, wd, ERR_SOFTMAX));
-        };
-        float lp[NP];  // this thread's share of every row's sum
-#pragma unroll
-        for (int r = 0; r < NP; ++r) lp[r] = 0.f;
-        bool ok = true;
-        for (int n = 0; n < n_iter; ++n) {
-            const int par = n & 1;
-            if (!sm_wait(B_SFULL + par, (n >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const int j = (t0 + n) * BN + t;  // this thread's key
-            const bool full = (t0 + n) * BN >= max_lo && (t0 + n) * BN + BN - 1 <= min_hi;
-            const uint32_t t_s = t_lane + C::TMEM_S + par * NP;
-            // ---- pass 1: masked tile maxima of every row
-#pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
-                uint32_t v[16];
-                tmem_ld16(t_s + c * 16, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = c * 16 + e;
-                    float s = __uint_as_float(v[e]);
-                    if (!full && !(j >= sh->lo[r] && j <= sh->hi[r])) s = -INFINITY;
-                    const int mx = __reduce_max_sync(0xffffffffu, ordered(s));
-                    if (lane == 0) sh->wmax[par][warp][r] = mx;
-                }
-            }
-            named_bar_sync(1, 128);
-            if (t == 0) sh->flag[par ^ 1] = 0;  // the next tile's flag: its last readers are past this barrier
-            if (t < NP) {
-                const int k4 = max(max(sh->wmax[par][0][t], sh->wmax[par][1][t]),
-                                   max(sh->wmax[par][2][t], sh->wmax[par][3][t]));
-                const float tmax = unordered(k4) * sl2;  // -inf stays -inf (scale > 0)
-                const float m_old = sh->m[t];
-                const bool grow = tmax > m_old + RESCALE_THRESHOLD;  // true on the first finite max
-                const float m_new = grow ? tmax : m_old;
-                sh->m[t] = m_new;
-                sh->alpha[t] = grow ? ex2(m_old - m_new) : 1.f;
-                if (grow && m_old != -INFINITY) sh->flag[par] = 1;
-            }
-            named_bar_sync(1, 128);
-            if (sh->flag[par]) {
-                // some row's max grew: scale the sums and (after PV(n-1)) the O^T columns
-#pragma unroll
-                for (int r = 0; r < NP; ++r) lp[r] *= sh->alpha[r];
-                if (!sm_wait(B_OFULL, (n - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < NP / 16; ++c) {
-                    uint32_t o[16];
-                    tmem_ld16(t_lane + C::TMEM_O + c * 16, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * sh->alpha[c * 16 + e]);
-                    tmem_st16(t_lane + C::TMEM_O + c * 16, o);
-                }
-                tmem_wait_st();
-            }
-            // ---- the P^T buffer of this parity is free once PV(n-2) is done
-            if (n >= 2 && !sm_wait(B_PFREE + par, ((n >> 1) - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            // ---- pass 2: P = exp2(s * scale * log2 e - m) -> bf16 P^T (K-major, 128B swizzle)
-            const uint32_t pb = s_p + par * 2 * C::PB + (t >> 6) * C::PB;
-            const int kk = t & 63;
-#pragma unroll
-            for (int c = 0; c < NP / 16; ++c) {
-                uint32_t v[16];
-                tmem_ld16(t_s + c * 16, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float pr[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int r = c * 16 + e + u;
-                        const bool in = full || (j >= sh->lo[r] && j <= sh->hi[r]);
-                        const float m = sh->m[r];
-                        pr[u] = in ? ex2(fmaf(__uint_as_float(v[e + u]), sl2, -m)) : 0.f;
-                        lp[r] += pr[u];
-                    }
-                    const uint32_t pk = pack_bf16x2(pr[0], pr[1]);
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int r = c * 16 + e + u;
-                        const uint32_t addr = pb + r * 128 + ((((kk >> 3) ^ (r & 7))) << 4) + (kk & 7) * 2;
-                        st_shared_u16(addr, (uint16_t)(u ? (pk >> 16) : (pk & 0xffffu)));
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_PFULL + par));
-        }
-        // ---- epilogue
+        auto wait = [&](int b_, uint32_t parity) { wait_bounded(bar(b_), parity, wd, ERR_SOFTMAX); };
+        // PV(m) done.  A parity wait only tells the last two phases apart, so it must never run
+        // more than one phase ahead of the barrier: PFREE[m & 1] completes once per PV of that
+        // parity, and this thread has already waited for PV(m - 2) on it (tile m's wait for its
+        // P^T buffer), whereas a barrier completing on every PV could still be two PVs behind.
+        auto wait_pv = [&](int m) { wait(B_PFREE + (m & 1), (m >> 1) & 1); };
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
-        if (ok) ok = sm_wait(B_OFULL, (n_iter - 1) & 1);  // ok is the same in all 128 threads here
-        tc_fence_after();
-        if (ok) {
-            // every row's sum: warp sums, then the four warps
+        const bool sliding = p.kind == ATTN_MASK_CAUSAL_SLIDING;
+        float lp[NP];  // this thread's share of every row's sum
+        int n = 0;     // the CTA's tile counter
+        int j = 0;     // stretch counter
+        for (long long i = share0; i < share1; ++j) {
+            const Seg s = seg_at(p, i, share1);
+            i += s.count;
+            const int row0 = (s.b * p.Hq + s.g * p.group) * p.S_q;
+            // tightest bounds over the valid rows: a tile inside [max_lo, min_hi] needs no mask
+            const int max_lo = sliding ? s.L - 1 - p.window : 0;
+            const int min_hi = p.kind == ATTN_MASK_FULL ? s.L - 1 : s.L - p.S_q;
+            if (t < NP) {
+                int lo = 0, hi = s.L - 1;
+                if (t < p.rows && p.kind != ATTN_MASK_FULL) {
+                    const int pos = s.L - p.S_q + t % p.S_q;  // position of this query row
+                    hi = pos;
+                    if (sliding) lo = max(0, pos - p.window);
+                }
+                sh->lo[t] = lo;
+                sh->hi[t] = hi;
+                sh->m[t] = -INFINITY;
+            }
+#pragma unroll
+            for (int r = 0; r < NP; ++r) lp[r] = 0.f;
+            named_bar_sync(1, 128);
+            for (int q = 0; q < s.count; ++q, ++n) {
+                const int par = n & 1;
+                wait(B_SFULL + par, (n >> 1) & 1);
+                if (n >= 2) wait(B_PFREE + par, ((n >> 1) - 1) & 1);  // PV(n-2) is done with this P^T buffer
+                tc_fence_after();
+                const int tile = s.tile0 + q;
+                const int jkey = tile * BN + t;  // this thread's key
+                const bool full = tile * BN >= max_lo && tile * BN + BN - 1 <= min_hi;
+                const uint32_t t_s = t_lane + C::TMEM_S + par * NP;
+                const uint32_t pb = s_p + par * 2 * C::PB + (t >> 6) * C::PB;
+                const int kk = t & 63;
+                float ts[NP];  // this tile's share of every row's sum
+                // P = exp2(s * scale * log2 e - m) against the running max m -> bf16 P^T (K-major,
+                // 128B swizzle); returns whether an allowed score exceeds m by more than the threshold
+                auto exp_pass = [&]() -> bool {
+                    bool over = false;
+#pragma unroll
+                    for (int c = 0; c < NP / 16; ++c) {
+                        uint32_t v[16];
+                        float mr[16];
+                        tmem_ld16(t_s + c * 16, v);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            const float4 m4 = *reinterpret_cast<const float4*>(sh->m + c * 16 + e);
+                            mr[e] = m4.x; mr[e + 1] = m4.y; mr[e + 2] = m4.z; mr[e + 3] = m4.w;
+                        }
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            float pr[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int r = c * 16 + e + u;
+                                const bool in = full || (jkey >= sh->lo[r] && jkey <= sh->hi[r]);
+                                const float x = fmaf(__uint_as_float(v[e + u]), sl2, -mr[e + u]);
+                                over |= in && x > RESCALE_THRESHOLD;
+                                pr[u] = in ? ex2(x) : 0.f;
+                                ts[r] = pr[u];
+                            }
+                            const uint32_t pk = pack_bf16x2(pr[0], pr[1]);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int r = c * 16 + e + u;
+                                const uint32_t addr = pb + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2;
+                                st_shared_u16(addr, (uint16_t)(u ? (pk >> 16) : (pk & 0xffffu)));
+                            }
+                        }
+                    }
+                    return over;
+                };
+                if (named_bar_or(1, 128, exp_pass())) {
+                    // ---- a row's max grew (always on a unit's first tile): exact masked tile maxima,
+                    // new running maxima and rescale factors, then P again.  Every reader of the
+                    // previous flag has passed the barrier above.
+                    if (t == 0) sh->flag = 0;
+#pragma unroll
+                    for (int c = 0; c < NP / 16; ++c) {
+                        uint32_t v[16];
+                        tmem_ld16(t_s + c * 16, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = c * 16 + e;
+                            float sv = __uint_as_float(v[e]);
+                            if (!full && !(jkey >= sh->lo[r] && jkey <= sh->hi[r])) sv = -INFINITY;
+                            const int mx = __reduce_max_sync(0xffffffffu, ordered(sv));
+                            if (lane == 0) sh->wmax[warp][r] = mx;
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                    if (t < NP) {
+                        const int k4 = max(max(sh->wmax[0][t], sh->wmax[1][t]), max(sh->wmax[2][t], sh->wmax[3][t]));
+                        const float tmax = unordered(k4) * sl2;  // -inf stays -inf (scale > 0)
+                        const float m_old = sh->m[t];
+                        const bool grow = tmax > m_old + RESCALE_THRESHOLD;  // true on a row's first finite max
+                        const float m_new = grow ? tmax : m_old;
+                        sh->m[t] = m_new;
+                        sh->alpha[t] = grow ? ex2(m_old - m_new) : 1.f;
+                        if (grow && m_old != -INFINITY) sh->flag = 1;
+                    }
+                    named_bar_sync(1, 128);
+                    if (sh->flag) {
+                        // scale the sums and, once PV(n-1) (same unit: m_old was finite) is done, O^T
+#pragma unroll
+                        for (int r = 0; r < NP; ++r) lp[r] *= sh->alpha[r];
+                        wait_pv(n - 1);
+                        tc_fence_after();
+#pragma unroll
+                        for (int c = 0; c < NP / 16; ++c) {
+                            uint32_t o[16];
+                            tmem_ld16(t_lane + C::TMEM_O + c * 16, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * sh->alpha[c * 16 + e]);
+                            tmem_st16(t_lane + C::TMEM_O + c * 16, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    exp_pass();  // cannot exceed now (every row's m is at least its tile max)
+                }
+#pragma unroll
+                for (int r = 0; r < NP; ++r) lp[r] += ts[r];
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(B_PFULL + par));
+            }
+            // ---- end of the stretch: its last PV (tile n - 1) -> O, or a partial result
+            wait_pv(n - 1);
+            tc_fence_after();
 #pragma unroll
             for (int r = 0; r < NP; ++r) {
                 float v = lp[r];
@@ -478,11 +693,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
             named_bar_sync(1, 128);
             if (t < NP) {
                 const float l = (sh->lsum[0][t] + sh->lsum[1][t]) + (sh->lsum[2][t] + sh->lsum[3][t]);
-                sh->l[t] = l > 0.f ? 1.f / l : 0.f;
+                sh->inv_l[t] = l > 0.f ? 1.f / l : 0.f;
                 sh->lse[t] = l > 0.f ? (sh->m[t] + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
             named_bar_sync(1, 128);
-            const size_t slot = (size_t)g * p.total_chunks + x;
+            const size_t slot = (size_t)part_slot(k, j == 0);
 #pragma unroll
             for (int c = 0; c < NP / 16; ++c) {
                 uint32_t o[16];
@@ -493,54 +708,36 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                     for (int e = 0; e < 16; ++e) {
                         const int r = c * 16 + e;
                         if (r < p.rows) {
-                            const float val = __uint_as_float(o[e]) * sh->l[r];
-                            if (n_chunks == 1) out[(size_t)(row0 + r) * D + t] = __float2bfloat16_rn(val);
+                            const float val = __uint_as_float(o[e]) * sh->inv_l[r];
+                            if (s.whole) out[(size_t)(row0 + r) * D + t] = __float2bfloat16_rn(val);
                             else p.part_o[(slot * NP + r) * D + t] = val;
                         }
                     }
                 }
             }
             if (t < p.rows) {
-                if (n_chunks == 1) {
+                if (s.whole) {
                     if (p.lse) p.lse[row0 + t] = sh->lse[t];
                 } else {
                     p.part_lse[slot * NP + t] = sh->lse[t];
                 }
             }
-        }
-        if (n_chunks > 1) {
-            // arrival of this chunk (also after an abort, so the counter keeps wrapping to 0)
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (t == 0) sh->is_last = atomicInc(p.counters + bkv, (unsigned)(n_chunks - 1)) == (unsigned)(n_chunks - 1);
-            named_bar_sync(1, 128);
-            if (ok && sh->is_last) {
+            // O^T has been read: the next PV into it follows this CTA's next PFULL arrival
+            tc_fence_before();
+            if (!s.whole) {
                 __threadfence();
-                // weights e^{LSE_c - LSE} of every chunk and row, in the idle K ring
-                float* wts = reinterpret_cast<float*>(smem + C::OFF_K);  // [n_chunks][NP]
-                const size_t slot0 = (size_t)g * p.total_chunks + p.chunk_prefix[b];
-                if (t < p.rows) {
-                    float M = -INFINITY;
-                    for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + (slot0 + c) * NP + t));
-                    float W = 0.f;
-                    for (int c = 0; c < n_chunks; ++c) {
-                        const float w = __expf(__ldcg(p.part_lse + (slot0 + c) * NP + t) - M);
-                        wts[c * NP + t] = w;
-                        W += w;
-                    }
-                    const float inv = 1.f / W;
-                    for (int c = 0; c < n_chunks; ++c) wts[c * NP + t] *= inv;
-                    if (p.lse) p.lse[row0 + t] = M + __logf(W);
+                named_bar_sync(1, 128);
+                if (t == 0) {
+                    const int nseg = share_of(p, s.unit_begin + s.n_unit - 1) - share_of(p, s.unit_begin) + 1;
+                    sh->is_last =
+                        atomicInc(p.counters + s.b * p.Hkv + s.g, (unsigned)(nseg - 1)) == (unsigned)(nseg - 1);
                 }
                 named_bar_sync(1, 128);
-                if (t < D) {
-                    for (int r = 0; r < p.rows; ++r) {
-                        float acc = 0.f;
-                        for (int c = 0; c < n_chunks; ++c)
-                            acc += wts[c * NP + r] * __ldcg(p.part_o + ((slot0 + c) * NP + r) * D + t);
-                        out[(size_t)(row0 + r) * D + t] = __float2bfloat16_rn(acc);
-                    }
+                if (sh->is_last) {
+                    __threadfence();
+                    merge_unit<D, NP>(p, s, warp, lane, sh->alpha, sh->lse);
                 }
+                named_bar_sync(1, 128);  // alpha / lse are the merge's scratch; the next stretch resets m
             }
         }
     }
@@ -563,15 +760,14 @@ cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    const dim3 grid(p.total_chunks, p.Hkv);
-    attn_decode_kernel<D, NP><<<grid, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_decode_kernel<D, NP><<<p.n_cta, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream) {
-    if (p.total_chunks <= 0) return cudaSuccess;
+    if (p.n_cta <= 0 || p.total_tiles <= 0) return cudaSuccess;
     if (d == 128) {
         if (np == 16) return launch<128, 16>(p, stream);
         if (np == 32) return launch<128, 32>(p, stream);

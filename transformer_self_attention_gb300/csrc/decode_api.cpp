@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -17,6 +18,7 @@ struct attn_decode_plan {
     int kind = 0, window = 0;
     float scale = 0.f;
     int n_sm = 0;
+    int grid_limit = 0;  // test hook: 0 = one CTA per multiprocessor
     size_t part_slots = 0;
     int* d_err = nullptr;
     unsigned* d_counters = nullptr;
@@ -119,8 +121,8 @@ attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
-    // grid.x <= ceil(n_sm / Hkv) + B (see build_decode_schedule), one slot per CTA
-    h->part_slots = (size_t)Hkv * ((h->n_sm + Hkv - 1) / Hkv + B);
+    // two partial-result slots per CTA of the persistent grid (its first and last stretch)
+    h->part_slots = 2 * (size_t)h->n_sm;
     if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(int))) != cudaSuccess) return fail(e);
     if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess) return fail(e);
     if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_counters), sizeof(unsigned) * B * Hkv)) != cudaSuccess)
@@ -165,12 +167,13 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
         h->last_v = V;
     }
     attn::DecodeSchedule sched;
-    attn::build_decode_schedule(h->B, h->Hkv, h->S_q, h->kind, h->window, cache_len, h->n_sm, &sched);
-    if ((size_t)sched.chunk_prefix[h->B] * h->Hkv > h->part_slots) return ATTN_ERR_UNSUPPORTED;  // cannot happen
+    const int ctas = h->grid_limit > 0 ? std::min(h->grid_limit, h->n_sm) : h->n_sm;
+    attn::build_decode_schedule(h->B, h->Hkv, h->S_q, h->kind, h->window, cache_len, ctas, &sched);
+    if (2 * (size_t)sched.n_cta > h->part_slots) return ATTN_ERR_UNSUPPORTED;  // cannot happen: n_cta <= n_sm
     for (int b = 0; b < h->B; ++b) p.len[b] = cache_len[b];
-    for (int b = 0; b <= h->B; ++b) p.chunk_prefix[b] = sched.chunk_prefix[b];
-    p.tiles_per_chunk = sched.tiles_per_chunk;
-    p.total_chunks = sched.chunk_prefix[h->B];
+    for (int b = 0; b <= h->B; ++b) p.tile_prefix[b] = sched.tile_prefix[b];
+    p.n_cta = sched.n_cta;
+    p.total_tiles = sched.total_tiles;
     p.o = O;
     p.lse = LSE;
     cudaError_t e = attn::launch_decode(p, h->d, h->np, static_cast<cudaStream_t>(stream));
@@ -182,8 +185,18 @@ attn_status attn_decode_poll_device_error(attn_decode_handle h, int* code) {
     *code = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
     if (cudaMemcpy(code, h->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (*code != 0 && cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (*code != 0) {
+        // an aborted CTA leaves its units' arrival counters part-way: start them again
+        if (cudaMemset(h->d_err, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaMemset(h->d_counters, 0, sizeof(unsigned) * h->B * h->Hkv) != cudaSuccess) return ATTN_ERR_CUDA;
+    }
     return *code ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas) {
+    if (!h || max_ctas < 1) return ATTN_ERR_INVALID_ARG;
+    h->grid_limit = max_ctas;
+    return ATTN_OK;
 }
 
 attn_status attn_decode_destroy(attn_decode_handle h) {
@@ -194,8 +207,8 @@ attn_status attn_decode_destroy(attn_decode_handle h) {
 }
 
 attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_mask_kind kind, int window,
-                                      const int* cache_len, int n_sm, int* tiles_per_chunk, int* chunk_prefix) {
-    if (!tiles_per_chunk || !chunk_prefix || n_sm < 1) return ATTN_ERR_INVALID_ARG;
+                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix) {
+    if (!n_cta || !tile_prefix || n_sm < 1) return ATTN_ERR_INVALID_ARG;
     attn_status vs = validate_decode(B, Hkv, Hkv, S_q, S_cap, kind, window);
     if (vs != ATTN_OK) return vs;
     vs = validate_lengths(B, S_q, S_cap, kind, cache_len);
@@ -203,8 +216,8 @@ attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_m
     attn::DecodeSchedule sched;
     attn::build_decode_schedule(B, Hkv, S_q, kind, kind == ATTN_MASK_CAUSAL_SLIDING ? window : 0, cache_len, n_sm,
                                 &sched);
-    *tiles_per_chunk = sched.tiles_per_chunk;
-    for (int b = 0; b <= B; ++b) chunk_prefix[b] = sched.chunk_prefix[b];
+    *n_cta = sched.n_cta;
+    for (int b = 0; b <= B; ++b) tile_prefix[b] = sched.tile_prefix[b];
     return ATTN_OK;
 }
 

@@ -67,9 +67,12 @@ struct MergeParams {
     int BHq, S, d;
 };
 
-// Decode / key-value-cache attention (attn_decode.cu).  One CTA streams a chunk of
-// key tiles of one (sequence, kv head) against all the query rows of that kv head's
-// group (group * S_q rows, padded to NP columns of the transposed score tile).
+// Decode / key-value-cache attention (attn_decode.cu).  A persistent grid of n_cta
+// CTAs shares the key tiles of all (sequence, kv head) units in one linear order:
+// unit (b, g) covers indices [Hkv * tile_prefix[b] + g * n_b, ... + n_b) with
+// n_b = tile_prefix[b+1] - tile_prefix[b], and CTA k takes indices
+// [k * T / n_cta, (k+1) * T / n_cta), T = Hkv * tile_prefix[B].  A CTA processes the
+// query rows of a kv head's group (group * S_q rows, padded to NP columns).
 constexpr int kDecodeMaxBatch = 1024;
 struct DecodeParams {
     CUtensorMap tm_q;    // Q as 2-D [B*Hq*S_q, d] bf16, box {64, NP}, 128B swizzle
@@ -77,18 +80,18 @@ struct DecodeParams {
     CUtensorMap tm_v;    // V cache [B*Hkv, S_cap, d]
     void* o;             // O [B, Hq, S_q, d] bf16
     float* lse;          // [B, Hq, S_q], may be null
-    float* part_o;       // split sequences: [slot][NP][d] fp32 partial O (normalised by its own sum)
-    float* part_lse;     // [slot][NP]
-    unsigned* counters;  // [B*Hkv] arrival counters of the split sequences (wrap to 0)
+    float* part_o;       // units split over CTAs: [2 * n_cta][NP][d] fp32 partial O (normalised by its own sum)
+    float* part_lse;     // [2 * n_cta][NP]
+    unsigned* counters;  // [B*Hkv] arrival counters of split units (wrap to 0)
     int* err;
     long long watchdog_ns;
     int B, Hq, Hkv, group, S_q, S_cap, rows;  // rows = group * S_q
     int kind, window;
     float scale_log2;
-    int tiles_per_chunk;
-    int total_chunks;    // grid.x; slot of CTA (x, g) = g * total_chunks + x
+    int n_cta;
+    long long total_tiles;                   // T
     int len[kDecodeMaxBatch];                // cache length of each sequence
-    int chunk_prefix[kDecodeMaxBatch + 1];   // first chunk of each sequence
+    int tile_prefix[kDecodeMaxBatch + 1];    // key tiles of the sequences before b (per kv head)
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);

@@ -168,22 +168,14 @@ void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi) {
 
 void build_decode_schedule(int B, int Hkv, int S_q, int kind, int window, const int* lens, int n_sm,
                            DecodeSchedule* out) {
-    std::vector<int> n(B);
-    long total = 0;
-    int longest = 0;
+    out->tile_prefix.assign(B + 1, 0);
     for (int b = 0; b < B; ++b) {
         int lo, hi;
         decode_tile_range(kind, S_q, window, lens[b], &lo, &hi);
-        n[b] = hi - lo;
-        total += (long)n[b] * Hkv;
-        longest = std::max(longest, n[b]);
+        out->tile_prefix[b + 1] = out->tile_prefix[b] + (hi - lo);
     }
-    long c = (total + std::max(1, n_sm) - 1) / std::max(1, n_sm);
-    c = std::max<long>(c, (longest + kDecodeMaxChunksPerSeq - 1) / kDecodeMaxChunksPerSeq);
-    c = std::max<long>(c, 1);
-    out->tiles_per_chunk = (int)c;
-    out->chunk_prefix.assign(B + 1, 0);
-    for (int b = 0; b < B; ++b) out->chunk_prefix[b + 1] = out->chunk_prefix[b] + (int)((n[b] + c - 1) / c);
+    out->total_tiles = (long long)Hkv * out->tile_prefix[B];
+    out->n_cta = (int)std::min<long long>(std::max(1, n_sm), out->total_tiles);
 }
 
 }  // namespace attn

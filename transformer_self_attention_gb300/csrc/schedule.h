@@ -37,22 +37,18 @@ struct Schedule {
 // tile's FULL key tiles are not contiguous (cannot happen for the five kinds).
 attn_status build_schedule(const ScheduleInput& in, Schedule* out);
 
-// Decode: chunks of key tiles per sequence (see attn_decode_schedule_host).
+// Decode: key tiles per sequence and the size of the persistent grid
+// (see attn_decode_schedule_host).
 struct DecodeSchedule {
-    int tiles_per_chunk = 1;
-    std::vector<int> chunk_prefix;  // B + 1 entries
+    int n_cta = 1;
+    long long total_tiles = 0;
+    std::vector<int> tile_prefix;  // B + 1 entries
 };
-
-// Most chunks one sequence may be split into (the merge keeps one weight per
-// chunk and row in shared memory).
-constexpr int kDecodeMaxChunksPerSeq = 256;
 
 // First and one-past-last key tile a sequence with L cached positions needs.
 void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi);
 
-// Chooses the chunk length so that Hkv * (number of chunks) is about n_sm, and
-// no sequence has more than kDecodeMaxChunksPerSeq chunks.  Lengths are assumed
-// validated.
+// Lengths are assumed validated.
 void build_decode_schedule(int B, int Hkv, int S_q, int kind, int window, const int* lens, int n_sm,
                            DecodeSchedule* out);
 
