@@ -6,6 +6,10 @@ per allowed (i, j) pair only (masked pairs are not counted).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
+A decode workload name (decode_* / cross_*) times one decode step instead: S_q new
+query rows per sequence against a key/value cache resident in HBM (same metric,
+useful TFLOP/s; its roofline is HBM bandwidth over the algorithmic bytes).
+
 Each timed step is one attn_forward over the whole batch (all heads, all rows);
 L2 is flushed (a 256 MiB write) before every step and the step is timed with
 CUDA events on the launching stream.  Under torchrun every rank runs its own
@@ -36,6 +40,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 KERNEL_SOURCES = ["transformer_self_attention_gb300/csrc/attn_fwd_tc.cu",
                   "transformer_self_attention_gb300/csrc/sm103_ptx.h",
                   "transformer_self_attention_gb300/csrc/kernels.h"]
+DECODE_KERNEL_SOURCES = ["transformer_self_attention_gb300/csrc/attn_decode.cu",
+                         "transformer_self_attention_gb300/csrc/sm103_ptx.h",
+                         "transformer_self_attention_gb300/csrc/kernels.h"]
 
 
 def peaks():
@@ -47,23 +54,23 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload_name: str):
+def ncu_traffic(workload_name: str, kernel: str = "attn_fwd_tc", sources=KERNEL_SOURCES):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if current."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_tc_{workload_name}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_hash(sources):
         return None
     return float(m_bytes.group(1))
 
@@ -325,18 +332,208 @@ def run_ours(args, w):
     return 0
 
 
+# ----------------------------------------------------------------------------- decode
+def _decode_oracle_inputs(w):
+    key = ("decode", w.name)
+    if key not in _INPUTS:
+        Qc, Kc, Vc, lens = wl.make_decode_inputs(w)
+        _INPUTS[key] = (Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens)
+    return _INPUTS[key]
+
+
+def cpu_baseline_decode(w, target_s: float = 12.0, n_seq: int | None = None):
+    """The fp64 decode oracle, as it stands, on the first n_seq sequences of the batch."""
+    n_cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
+    import oracle
+    oracle.build()
+    Qf, Kf, Vf, lens = _decode_oracle_inputs(w)
+
+    def run(nb):
+        t0 = time.perf_counter()
+        oracle.decode(Qf[:nb], Kf[:nb], Vf[:nb], lens[:nb], w.scale, w.kind, w.window)
+        dt = time.perf_counter() - t0
+        return dt, wl.decode_useful_flops(w, lens[:nb])
+
+    if n_seq is None:
+        dt, fl = run(1)
+        per_seq = dt
+        n_seq = max(1, min(w.B, int(target_s / max(per_seq, 1e-6))))
+    dt, fl = run(n_seq)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle", "seconds": round(dt, 3), "n_seq": n_seq,
+            "sample": f"the first {n_seq} of {w.B} sequences (all heads and new rows), "
+                      f"{fl / 1e9:.2f} useful GFLOP, fp64 C oracle with OpenMP"}
+
+
+def _decode_config(w, lens):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S_q": w.S_q, "S_cap": w.S_cap, "d": w.d,
+            "mask": wl.MASK_NAMES[w.kind], "window": w.window, "cache_len": list(lens),
+            "cache": "resident in HBM (the step's inputs are the new query rows)"}
+
+
+def run_reference_decode(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    cal = cpu_baseline_decode(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    times, r = [], None
+    for s in range(args.warmup + args.steps):
+        r = cpu_baseline_decode(w, n_seq=cal["n_seq"])
+        if s >= args.warmup:
+            times.append(r["seconds"])
+    t = sum(times) / len(times)
+    value = r["value"] * r["seconds"] / t
+    _, _, _, lens = _decode_oracle_inputs(w)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _decode_config(w, lens),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_decode(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_self_attention_gb300 as tsa
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w)
+    Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
+    plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind, window=w.window)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((w.B, w.Hq, w.S_q), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        plan(Q, K, V, lens, O=O, LSE=LSE, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {code}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    mean_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    if world > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during the timed steps: {code}")
+    useful = wl.decode_useful_flops(w, lens)
+    nbytes = wl.decode_bytes(w, lens)
+    value = world * useful / (mean_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+
+    # end to end through the C ABI: the new query rows from pinned host memory, the step, O and
+    # LSE back to pinned host memory (the cache stays resident, as it does across decode steps)
+    e2e = None
+    if not args.no_e2e:
+        hQ = Qc.pin_memory()
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype, pin_memory=True)
+        dQ, dO, dL = torch.empty_like(Q), torch.empty_like(O), torch.empty_like(LSE)
+        n_e2e = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            dQ.copy_(hQ, non_blocking=True)
+            plan(dQ, K, V, lens, O=dO, LSE=dL, stream=stream)
+            hO.copy_(dO, non_blocking=True); hL.copy_(dL, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            flush.zero_()
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": Qc.numel() * Qc.element_size(),
+               "d2h_bytes_per_step": O.numel() * O.element_size() + LSE.numel() * LSE.element_size(),
+               "note": "includes the 256 MiB L2 flush of each step"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    achieved = nbytes / (mean_ms * 1e-3) / 1e9
+    peak = float(pk["hbm_gbs"])
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": ncu_traffic(w.name, "attn_decode", DECODE_KERNEL_SOURCES),
+                "algorithmic_bytes": nbytes, "peak_source": f"{pk_src} hbm_gbs (copy bandwidth)",
+                "kernel": "attn_decode_kernel"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(_decode_config(w, lens), useful_gflop_per_step=useful / 1e9,
+                           l2="flushed before every step (256 MiB write)",
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "roofline": roofline, "gpu_launches": args.steps, "wall_s_timed_region": wall}
+    if e2e:
+        line["e2e"] = e2e
+    if clk:
+        line["clocks"] = clk
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_decode(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=wl.CAUSAL_MHA_4K.name, choices=sorted(wl.BY_NAME))
+    ap.add_argument("--workload", default=wl.CAUSAL_MHA_4K.name,
+                    choices=sorted(wl.BY_NAME) + sorted(wl.DECODE_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in wl.DECODE_BY_NAME:
+        w = wl.DECODE_BY_NAME[args.workload]
+        return run_reference_decode(args, w) if args.impl == "reference" else run_ours_decode(args, w)
     w = wl.BY_NAME[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
