@@ -131,7 +131,8 @@ __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask&
     return in ? __uint_as_float(raw) : -INFINITY;
 }
 
-// Row maximum of the (masked) raw scores of this thread's row, columns [0, BN).
+// Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
+// three-input max instructions, eight independent chains.
 template <bool MASKED>
 __device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
     float m8[8];
@@ -144,24 +145,24 @@ __device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) 
         tmem_ld32(t_s + h * 64 + 32, r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            m8[e & 7] = fmaxf(m8[e & 7], tile_score<MASKED>(r0[e], h * 64 + e, mk));
-            m8[e & 7] = fmaxf(m8[e & 7], tile_score<MASKED>(r1[e], h * 64 + 32 + e, mk));
+        for (int e = 0; e < 32; e += 2) {
+            const int k = (e >> 1) & 7;
+            m8[k] = fmax3(m8[k], tile_score<MASKED>(r0[e], h * 64 + e, mk), tile_score<MASKED>(r0[e + 1], h * 64 + e + 1, mk));
+            m8[k] = fmax3(m8[k], tile_score<MASKED>(r1[e], h * 64 + 32 + e, mk),
+                          tile_score<MASKED>(r1[e + 1], h * 64 + 33 + e, mk));
         }
     }
-#pragma unroll
-    for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-        for (int j = 0; j < k; ++j) m8[j] = fmaxf(m8[j], m8[j + k]);
-    return m8[0];
+    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
 // P = exp2(s * sl2 - ref) written as bf16 over the S columns; returns the row sum.
 // Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
-// [32h, 32h+32), which only overlap S columns this thread has already read.
+// [32h, 32h+32), which only overlap S columns this thread has already read.  The
+// scale-and-subtract and the running sums use the packed two-lane fp32 instructions.
 template <bool MASKED>
 __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref) {
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t r0[32], r1[32], pk[32];
@@ -170,17 +171,21 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(tile_score<MASKED>(r0[2 * e], h * 64 + 2 * e, mk), sl2, -ref));
-            const float p1 = ex2(fmaf(tile_score<MASKED>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk), sl2, -ref));
-            const float p2 = ex2(fmaf(tile_score<MASKED>(r1[2 * e], h * 64 + 32 + 2 * e, mk), sl2, -ref));
-            const float p3 = ex2(fmaf(tile_score<MASKED>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk), sl2, -ref));
-            s4[0] += p0; s4[1] += p1; s4[2] += p2; s4[3] += p3;
+            const float2 x01 = __ffma2_rn(make_float2(tile_score<MASKED>(r0[2 * e], h * 64 + 2 * e, mk),
+                                                      tile_score<MASKED>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk)),
+                                          sl2x2, nref);
+            const float2 x23 = __ffma2_rn(make_float2(tile_score<MASKED>(r1[2 * e], h * 64 + 32 + 2 * e, mk),
+                                                      tile_score<MASKED>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk)),
+                                          sl2x2, nref);
+            const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+            acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+            acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
             pk[e] = pack_bf16x2(p0, p1);
             pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
     }
-    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
 template <int D>
