@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             bool ok = wait_bounded(bar(B_Q), 0, sh, p, ERR_MMA);
             for (int it = 0; it < n_iter && ok; ++it) {
                 if (!(ok = wait_bounded(bar(B_KFULL), it & 1, sh, p, ERR_MMA))) break;
-                // S/P share tensor columns: PV(it-1) must have consumed P before S is overwritten
-                if (it > 0 && !(ok = spin_bounded(bar(B_OFULL), (it - 1) & 1, sh, p, ERR_MMA))) break;
+                // S/P share tensor columns.  No wait for PV(it-1) here: the MMAs one thread issues
+                // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
