@@ -61,6 +61,9 @@ def _load():
             lib.oracle_attention_rows.argtypes = [P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I,
                                                   P, P, P, P, L, P, P]
             lib.oracle_attention_rows.restype = I
+            lib.oracle_attention_rows_bias.argtypes = [P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P,
+                                                       P, P, P, P, L, P, P]
+            lib.oracle_attention_rows_bias.restype = I
             lib.oracle_row_counts.argtypes = [I, I, I, P, I, P]
             lib.oracle_row_counts.restype = I
             lib.oracle_tile_classes.argtypes = [I, I, I, P, I, I, I, P]
@@ -69,6 +72,8 @@ def _load():
             lib.oracle_decode_allowed.restype = I
             lib.oracle_decode.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double, I, I, P, P, P]
             lib.oracle_decode.restype = I
+            lib.oracle_decode_bias.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double, I, I, P, P, P, P]
+            lib.oracle_decode_bias.restype = I
             _lib = lib
     return _lib
 
@@ -82,11 +87,20 @@ def _globals_array(globals_idx):
     return g, int(g.size)
 
 
-def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row_a, row_i):
+def _slopes(alibi, Hq):
+    if alibi is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(alibi, dtype=np.float64).reshape(-1))
+    assert a.size == Hq
+    return a
+
+
+def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row_a, row_i, alibi=None):
     """Oracle outputs for an explicit list of rows.
 
     K, V: float32-castable arrays [B, Hkv, S, d]; Qrows: [n, d] query vectors of
     the rows; row_b / row_a / row_i: [n] batch, query head and position.
+    alibi: optional [Hq] slopes m_a of the additive bias -m_a |i - j|.
     Returns (O [n, d] float64, LSE [n] float64).
     """
     lib = _load()
@@ -102,21 +116,22 @@ def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row
     g, ng = _globals_array(globals_idx)
     O = np.empty((n, d), dtype=np.float64)
     LSE = np.empty((n,), dtype=np.float64)
-    rc = lib.oracle_attention_rows(_ptr(K), _ptr(V), B, Hq, Hkv, S, d, float(scale), int(kind),
-                                   int(window), _ptr(g), ng, _ptr(Qrows), _ptr(rb), _ptr(ra), _ptr(ri),
-                                   n, _ptr(O), _ptr(LSE))
+    sl = _slopes(alibi, Hq)
+    rc = lib.oracle_attention_rows_bias(_ptr(K), _ptr(V), B, Hq, Hkv, S, d, float(scale), int(kind),
+                                        int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None,
+                                        _ptr(Qrows), _ptr(rb), _ptr(ra), _ptr(ri), n, _ptr(O), _ptr(LSE))
     if rc != 0:
         raise ValueError("oracle_attention_rows rejected its arguments")
     return O, LSE
 
 
-def attention(Q, K, V, scale, kind, window=0, globals_idx=None):
+def attention(Q, K, V, scale, kind, window=0, globals_idx=None, alibi=None):
     """Whole-tensor oracle: Q [B, Hq, S, d], K/V [B, Hkv, S, d] -> (O [B,Hq,S,d], LSE [B,Hq,S]) fp64."""
     Q = np.ascontiguousarray(Q, dtype=np.float32)
     B, Hq, S, d = Q.shape
     bb, aa, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
     O, LSE = attention_rows(K, V, Hq, scale, kind, window, globals_idx, Q.reshape(-1, d),
-                            bb.ravel(), aa.ravel(), ii.ravel())
+                            bb.ravel(), aa.ravel(), ii.ravel(), alibi=alibi)
     return O.reshape(B, Hq, S, d), LSE.reshape(B, Hq, S)
 
 
@@ -156,7 +171,7 @@ def decode_allowed(kind, t, j, L, window=0) -> bool:
     return bool(_load().oracle_decode_allowed(int(kind), int(t), int(j), int(L), int(window)))
 
 
-def decode(Q, K, V, cache_len, scale, kind, window=0):
+def decode(Q, K, V, cache_len, scale, kind, window=0, alibi=None):
     """Key/value-cache attention.
 
     Q [B, Hq, S_q, d]; K, V [B, Hkv, S_cap, d] (the cache); cache_len [B] ints.
@@ -175,8 +190,9 @@ def decode(Q, K, V, cache_len, scale, kind, window=0):
     assert lens.size == B
     O = np.empty((B, Hq, S_q, d), dtype=np.float64)
     LSE = np.empty((B, Hq, S_q), dtype=np.float64)
-    rc = lib.oracle_decode(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, S_q, S_cap, d, float(scale), int(kind),
-                           int(window), _ptr(lens), _ptr(O), _ptr(LSE))
+    sl = _slopes(alibi, Hq)
+    rc = lib.oracle_decode_bias(_ptr(Q), _ptr(K), _ptr(V), B, Hq, Hkv, S_q, S_cap, d, float(scale), int(kind),
+                                int(window), _ptr(lens), _ptr(sl) if sl is not None else None, _ptr(O), _ptr(LSE))
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return O, LSE

@@ -89,6 +89,14 @@ static unsigned char* make_global_flags(long S, const int* G, int nG)
  *             itself), in which case O is set to 0.
  * Returns 0 on success, -1 on bad arguments or allocation failure.
  */
+int oracle_attention_rows_bias(const float* K, const float* V,
+                               int B, int Hq, int Hkv, int S, int d,
+                               double scale, int kind, int window,
+                               const int* G, int nG, const double* alibi,
+                               const float* Qrows, const int* row_b, const int* row_a,
+                               const int* row_i, long n,
+                               double* O, double* LSE);
+
 int oracle_attention_rows(const float* K, const float* V,
                           int B, int Hq, int Hkv, int S, int d,
                           double scale, int kind, int window,
@@ -96,6 +104,30 @@ int oracle_attention_rows(const float* K, const float* V,
                           const float* Qrows, const int* row_b, const int* row_a,
                           const int* row_i, long n,
                           double* O, double* LSE)
+{
+    return oracle_attention_rows_bias(K, V, B, Hq, Hkv, S, d, scale, kind, window, G, nG, NULL,
+                                      Qrows, row_b, row_a, row_i, n, O, LSE);
+}
+
+/*
+ * The same with an additive score bias b_ij (alibi == NULL: none):
+ *   logits_ij = scale * q_i . k_j + b_ij,   b_ij = -alibi[a] * |i - j|
+ * - the additive-bias form: "Transformer 架构及其变体" (aaai.latere.ai), the
+ *   unified view of sequence and graph attention, logits = q.k / sqrt(d_k) + b_ij;
+ * - ALiBi's distance penalty, -m |i - j| with one fixed slope per head: "Trasformer
+ *   浅析" (atffang.github.io), section 线性偏置注意力; written -m_h (i - j) for
+ *   j <= i under the causal mask in "Transformer 架构及其变体", section 加性偏置：ALiBi,
+ *   which is the same value there.
+ * alibi: fp64 [Hq], one slope per query head (the pages give no values; callers
+ * pass them).
+ */
+int oracle_attention_rows_bias(const float* K, const float* V,
+                               int B, int Hq, int Hkv, int S, int d,
+                               double scale, int kind, int window,
+                               const int* G, int nG, const double* alibi,
+                               const float* Qrows, const int* row_b, const int* row_a,
+                               const int* row_i, long n,
+                               double* O, double* LSE)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 0 || d < 1 || Hq % Hkv != 0) return -1;
     unsigned char* is_global = make_global_flags(S, G, nG);
@@ -129,6 +161,7 @@ int oracle_attention_rows(const float* K, const float* V,
                 double dot = 0.0;
                 for (int t = 0; t < d; ++t) dot += (double)q[t] * (double)k[t];
                 s[j] = dot * scale;
+                if (alibi) s[j] -= alibi[a] * (double)labs(i - j);
                 if (s[j] > m) m = s[j];
             }
             for (int t = 0; t < d; ++t) acc[t] = 0.0;
@@ -246,10 +279,24 @@ int oracle_decode_allowed(int kind, long t, long j, long L, long w)
     }
 }
 
+int oracle_decode_bias(const float* Q, const float* K, const float* V,
+                       int B, int Hq, int Hkv, int S_q, int S_cap, int d,
+                       double scale, int kind, int window, const int* cache_len,
+                       const double* alibi, double* O, double* LSE);
+
 int oracle_decode(const float* Q, const float* K, const float* V,
                   int B, int Hq, int Hkv, int S_q, int S_cap, int d,
                   double scale, int kind, int window, const int* cache_len,
                   double* O, double* LSE)
+{
+    return oracle_decode_bias(Q, K, V, B, Hq, Hkv, S_q, S_cap, d, scale, kind, window, cache_len, NULL, O, LSE);
+}
+
+/* Decode with the ALiBi bias -alibi[a] * |t - j| (t the row's position; NULL: none). */
+int oracle_decode_bias(const float* Q, const float* K, const float* V,
+                       int B, int Hq, int Hkv, int S_q, int S_cap, int d,
+                       double scale, int kind, int window, const int* cache_len,
+                       const double* alibi, double* O, double* LSE)
 {
     if (B < 1 || Hq < 1 || Hkv < 1 || S_q < 1 || S_cap < 1 || d < 1 || Hq % Hkv != 0) return -1;
     if (kind != ORACLE_MASK_FULL && kind != ORACLE_MASK_CAUSAL && kind != ORACLE_MASK_CAUSAL_SLIDING)
@@ -291,6 +338,7 @@ int oracle_decode(const float* Q, const float* K, const float* V,
                 double dot = 0.0;
                 for (int c = 0; c < d; ++c) dot += (double)q[c] * (double)k[c];
                 s[j] = dot * scale;
+                if (alibi) s[j] -= alibi[a] * (double)labs(t - j);
                 if (s[j] > m) m = s[j];
             }
             for (int c = 0; c < d; ++c) acc[c] = 0.0;
