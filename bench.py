@@ -218,6 +218,8 @@ def run_ours(args, w):
     Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind,
                          window=w.window, global_idx=list(w.globals_idx))
+    if args.alibi:
+        plan.set_alibi(wl.alibi_slopes(w.Hq))
     O = torch.empty_like(Q)
     LSE = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -315,6 +317,7 @@ def run_ours(args, w):
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
                        "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
                        "useful_gflop_per_step": useful / 1e9, "l2": "flushed before every step (256 MiB write)",
+                       "score_bias": "alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_peak": {"measured": 100.0 * achieved / peak, "nominal": 100.0 * achieved / NOMINAL_BF16_TFLOPS,
                             "peak_source": pk_src},
@@ -410,6 +413,8 @@ def run_ours_decode(args, w):
     Qc, Kc, Vc, lens = wl.make_decode_inputs(w)
     Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
     plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind, window=w.window)
+    if args.alibi:
+        plan.set_alibi(wl.alibi_slopes(w.Hq))
     O = torch.empty_like(Q)
     LSE = torch.empty((w.B, w.Hq, w.S_q), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -503,6 +508,7 @@ def run_ours_decode(args, w):
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(_decode_config(w, lens), useful_gflop_per_step=useful / 1e9,
+                           score_bias="alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
                            l2="flushed before every step (256 MiB write)",
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
             "roofline": roofline, "gpu_launches": args.steps, "wall_s_timed_region": wall}
@@ -528,6 +534,8 @@ def main():
                     choices=sorted(wl.BY_NAME) + sorted(wl.DECODE_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--alibi", action="store_true",
+                    help="add the ALiBi score bias with slopes 2^(-8(a+1)/H) (same workload, same metric)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -186,6 +186,23 @@ attn_status attn_poll_device_error(attn_handle h, int* code);
 attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
 
 /*
+ * attn_set_alibi -- add the ALiBi score bias to every later attn_forward of this
+ * handle: logits_ij = scale * q_i . k_j + b_ij with b_ij = -slopes[a] * |i - j|.
+ *   - The additive-bias form logits = q.k / sqrt(d_k) + b_ij and ALiBi's
+ *     -m_h (i - j), j <= i: "Transformer 架构及其变体" (aaai.latere.ai), sections
+ *     加性偏置：ALiBi and the unified view of sequence and graph attention; the
+ *     distance form -m |i - j|: "Trasformer 浅析" (atffang.github.io), section
+ *     线性偏置注意力.  The pages fix one slope per head but give no values.
+ *   slopes : HOST array of Hq finite floats (query head a uses slopes[a]; copied),
+ *            or NULL to remove the bias.
+ * The bias enters the row max, the weights and the LSE (LSE = ln sum_j e^{logits_ij}).
+ * Errors: ATTN_ERR_INVALID_ARG (NULL handle, non-finite slope),
+ *         ATTN_ERR_UNSUPPORTED (LOCAL_GLOBAL handles), ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ * Must not be called while a forward of this handle is in flight.
+ */
+attn_status attn_set_alibi(attn_handle h, const float* slopes);
+
+/*
  * attn_set_watchdog -- test hook for the failure-detection path.
  *   limit_ns : wall-clock limit of every bounded wait inside the kernels
  *              (default 2e9 ns).
@@ -301,6 +318,13 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
 
 /* attn_decode_poll_device_error -- as attn_poll_device_error, for a decode handle. */
 attn_status attn_decode_poll_device_error(attn_decode_handle h, int* code);
+
+/*
+ * attn_decode_set_alibi -- as attn_set_alibi, for a decode handle: the bias of a
+ * query row at position t is -slopes[a] * |t - j| (t = cache_len[b] - S_q + i).
+ * NULL removes it.  Errors: ATTN_ERR_INVALID_ARG, ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ */
+attn_status attn_decode_set_alibi(attn_decode_handle h, const float* slopes);
 
 /*
  * attn_decode_set_grid_limit -- test hook: run at most max_ctas CTAs (>= 1) per

@@ -28,7 +28,8 @@ WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
             "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
-            "attn_decode_schedule_host", "attn_decode_set_grid_limit")
+            "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
+            "attn_decode_set_alibi")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -60,6 +61,10 @@ def _load():
     lib.attn_poll_device_error.restype = I
     lib.attn_set_watchdog.argtypes = [P, LL, I]
     lib.attn_set_watchdog.restype = I
+    lib.attn_set_alibi.argtypes = [P, P]
+    lib.attn_set_alibi.restype = I
+    lib.attn_decode_set_alibi.argtypes = [P, P]
+    lib.attn_decode_set_alibi.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -119,6 +124,18 @@ def attn_poll_device_error(handle: int):
     code = ctypes.c_int(0)
     st = _lib.attn_poll_device_error(handle, ctypes.byref(code))
     return st, code.value
+
+
+def _float_array(xs):
+    xs = [float(x) for x in xs]
+    return (ctypes.c_float * max(len(xs), 1))(*xs)
+
+
+def attn_set_alibi(handle: int, slopes=None) -> int:
+    """ALiBi bias -slopes[a] |i - j| on later forwards of this handle (None removes it); returns the status."""
+    if slopes is None:
+        return _lib.attn_set_alibi(handle, None)
+    return _lib.attn_set_alibi(handle, ctypes.cast(_float_array(slopes), ctypes.c_void_p))
 
 
 def attn_set_watchdog(handle: int, limit_ns: int, withhold: int = 0) -> int:
@@ -251,6 +268,17 @@ class DecodeAttention:
     def poll_device_error(self):
         return attn_decode_poll_device_error(self.handle)
 
+    def set_alibi(self, slopes=None):
+        """Add the ALiBi score bias -slopes[a] |t - j| (one slope per query head); None removes it."""
+        if slopes is None:
+            st = _lib.attn_decode_set_alibi(self.handle, None)
+        else:
+            if len(slopes) != self.shape[1]:
+                raise ValueError("one slope per query head")
+            st = _lib.attn_decode_set_alibi(self.handle, ctypes.cast(_float_array(slopes), ctypes.c_void_p))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_decode_set_alibi")
+
     def set_grid_limit(self, max_ctas: int):
         """Test hook: at most max_ctas CTAs per launch (long shares on small problems)."""
         st = _lib.attn_decode_set_grid_limit(self.handle, int(max_ctas))
@@ -315,3 +343,11 @@ class Attention:
         st = attn_set_watchdog(self.handle, limit_ns, withhold)
         if st != ATTN_OK:
             raise AttnError(st, "attn_set_watchdog")
+
+    def set_alibi(self, slopes=None):
+        """Add the ALiBi score bias -slopes[a] |i - j| (one slope per query head); None removes it."""
+        if slopes is not None and len(slopes) != self.shape[1]:
+            raise ValueError("one slope per query head")
+        st = attn_set_alibi(self.handle, slopes)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_set_alibi")

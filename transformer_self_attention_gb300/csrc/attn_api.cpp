@@ -33,6 +33,7 @@ struct attn_plan {
     void* d_kg = nullptr;
     void* d_vg = nullptr;
     float* d_part = nullptr;  // partial results of the chunked global-row pass
+    float* d_alibi = nullptr;  // ALiBi slopes [Hq] (attn_set_alibi), or null
     // tensor maps of the last pointers seen (re-encoded when they change)
     const void* last_q = nullptr;
     const void* last_k = nullptr;
@@ -111,7 +112,8 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 
 void free_plan(attn_plan* h) {
     if (!h) return;
-    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part};
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part,
+                    h->d_alibi};
     for (void* b : bufs)
         if (b) cudaFree(b);
     delete h;
@@ -231,6 +233,7 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         p.B = h->B; p.Hq = h->Hq; p.Hkv = h->Hkv; p.S = h->S; p.group = h->Hq / h->Hkv;
         p.kind = h->kind; p.window = h->window; p.scale = h->scale;
         p.globals = h->d_globals; p.n_global = nG; p.is_global = h->d_isg;
+        p.alibi = h->d_alibi;
         e = attn::launch_f32_forward(p, h->d, stream);
     } else {
         attn::TcParams& p = h->tp;
@@ -326,6 +329,27 @@ attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream) {
     if (!x || !y || n < 0) return ATTN_ERR_INVALID_ARG;
     return attn::launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
                                                                                                  : ATTN_ERR_CUDA;
+}
+
+attn_status attn_set_alibi(attn_handle h, const float* slopes) {
+    if (!h) return ATTN_ERR_INVALID_ARG;
+    if (!slopes) {  // back to no bias
+        if (h->d_alibi) cudaFree(h->d_alibi);
+        h->d_alibi = nullptr;
+        h->tp.alibi = nullptr;
+        return ATTN_OK;
+    }
+    for (int a = 0; a < h->Hq; ++a)
+        if (!std::isfinite(slopes[a])) return ATTN_ERR_INVALID_ARG;
+    if (h->kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
+    if (!h->d_alibi) {
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->d_alibi), sizeof(float) * h->Hq);
+        if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
+    }
+    if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    h->tp.alibi = h->d_alibi;
+    return ATTN_OK;
 }
 
 attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold) {

@@ -115,6 +115,8 @@ struct DShared {
     alignas(16) float alpha[NP];
     alignas(16) float inv_l[NP];
     alignas(16) float lse[NP];
+    alignas(16) float bm[NP];  // ALiBi: slope of the row's head times log2(e)
+    alignas(16) float bp[NP];  // ALiBi: the row's position t
     int lo[NP], hi[NP];        // allowed key interval of each packed row in the current unit
     int wmax[4][NP];           // per-warp tile maxima (order-preserving int encoding)
     float lsum[4][NP];
@@ -360,7 +362,7 @@ __device__ void merge_unit(const DecodeParams& p, const Seg& s, int warp, int la
     }
 }
 
-template <int D, int NP>
+template <int D, int NP, bool ALIBI>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<D, NP>;
     extern __shared__ uint8_t smem_raw[];
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 const int bkv = s.b * p.Hkv + s.g;
                 for (int q = 0; q < s.count && ok; ++q, ++n) {
                     const int st = n % C::STAGES, round = n / C::STAGES;
-                    const int key = (s.tile0 + q) * BN;
+                    const int key = (s.tile0 + (ALIBI ? s.count - 1 - q : q)) * BN;
                     if (n >= C::STAGES && !(ok = wait_bounded(bar(B_KEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
                         break;
                     mbar_arrive_expect_tx(bar(B_KFULL + st), C::TB);
@@ -495,7 +497,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
             walk_next(p, wq, share1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            const int tile = wp.s.tile0 + wp.q;
+            const int tile = wp.s.tile0 + (ALIBI ? wp.s.count - 1 - wp.q : wp.q);
             const int tail = wp.s.L % BN;
             if (tail != 0 && tile == (wp.s.L - 1) / BN) {
                 // a sequence's last cache tile: zero the V rows at and past its length.  Every
@@ -569,6 +571,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 sh->lo[t] = lo;
                 sh->hi[t] = hi;
                 sh->m[t] = -INFINITY;
+                if constexpr (ALIBI) {  // bias -m_a |t_row - j| in log2 units
+                    const int rr = t < p.rows ? t : 0;
+                    sh->bm[t] = p.alibi[s.g * p.group + rr / p.S_q] * 1.4426950408889634f;
+                    sh->bp[t] = (float)(s.L - p.S_q + rr % p.S_q);
+                }
             }
 #pragma unroll
             for (int r = 0; r < NP; ++r) lp[r] = 0.f;
@@ -578,7 +585,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 wait(B_SFULL + par, (n >> 1) & 1);
                 if (n >= 2) wait(B_PFREE + par, ((n >> 1) - 1) & 1);  // PV(n-2) is done with this P^T buffer
                 tc_fence_after();
-                const int tile = s.tile0 + q;
+                // with ALiBi the stretch runs from its newest key tile down (the bias falls with
+                // the distance from the row's position, so the running max is set early)
+                const int tile = s.tile0 + (ALIBI ? s.count - 1 - q : q);
                 const int jkey = tile * BN + t;  // this thread's key
                 const bool full = tile * BN >= max_lo && tile * BN + BN - 1 <= min_hi;
                 const uint32_t t_s = t_lane + C::TMEM_S + par * NP;
@@ -598,6 +607,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                         for (int e = 0; e < 16; e += 4) {
                             const float4 m4 = *reinterpret_cast<const float4*>(sh->m + c * 16 + e);
                             mr[e] = m4.x; mr[e + 1] = m4.y; mr[e + 2] = m4.z; mr[e + 3] = m4.w;
+                        }
+                        if constexpr (ALIBI) {  // fold the bias into the subtracted max
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                mr[e] = fmaf(sh->bm[c * 16 + e], fabsf(sh->bp[c * 16 + e] - (float)jkey), mr[e]);
                         }
                         tmem_wait_ld();
 #pragma unroll
@@ -637,6 +651,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                         for (int e = 0; e < 16; ++e) {
                             const int r = c * 16 + e;
                             float sv = __uint_as_float(v[e]);
+                            if constexpr (ALIBI)  // log2 units with the bias
+                                sv = fmaf(sv, sl2, -sh->bm[r] * fabsf(sh->bp[r] - (float)jkey));
                             if (!full && !(jkey >= sh->lo[r] && jkey <= sh->hi[r])) sv = -INFINITY;
                             const int mx = __reduce_max_sync(0xffffffffu, ordered(sv));
                             if (lane == 0) sh->wmax[warp][r] = mx;
@@ -645,7 +661,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                     named_bar_sync(1, 128);
                     if (t < NP) {
                         const int k4 = max(max(sh->wmax[0][t], sh->wmax[1][t]), max(sh->wmax[2][t], sh->wmax[3][t]));
-                        const float tmax = unordered(k4) * sl2;  // -inf stays -inf (scale > 0)
+                        const float tmax = ALIBI ? unordered(k4) : unordered(k4) * sl2;  // -inf stays -inf
                         const float m_old = sh->m[t];
                         const bool grow = tmax > m_old + RESCALE_THRESHOLD;  // true on a row's first finite max
                         const float m_new = grow ? tmax : m_old;
@@ -750,18 +766,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
     }
 }
 
-template <int D, int NP>
-cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
+template <int D, int NP, bool ALIBI>
+cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
     using C = DCfg<D, NP>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_ALLOC);
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NP, ALIBI>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attn_decode_kernel<D, NP><<<p.n_cta, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_decode_kernel<D, NP, ALIBI><<<p.n_cta, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int D, int NP>
+cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
+    return p.alibi ? launch_one<D, NP, true>(p, stream) : launch_one<D, NP, false>(p, stream);
 }
 
 }  // namespace

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK) attn_fwd_f32_kernel(F32Pa
     float qv[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) { qv[e] = q[lane + 32 * e]; acc[e] = 0.f; }
+    const float slope = p.alibi ? p.alibi[a] : 0.f;
     float m = -INFINITY, l = 0.f;
 
     auto visit = [&](long j) {
@@ -49,7 +50,8 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK) attn_fwd_f32_kernel(F32Pa
         for (int e = 0; e < E; ++e) dot = fmaf(qv[e], k[lane + 32 * e], dot);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        const float s = dot * p.scale;
+        float s = dot * p.scale;
+        if (p.alibi) s -= slope * fabsf((float)(i - j));  // additive bias -m_a |i - j|
         const float m_new = fmaxf(m, s);
         const float c = expf(m - m_new);  // 0 on the first key
         const float e_s = expf(s - m_new);

@@ -46,7 +46,11 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the 
 
 enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 
-template <int D>
+// BIAS: 0 none; 1 ALiBi added per element (symmetric kinds, |i - j|); 2 ALiBi under the
+// causal kinds, added by the tensor core (see the MMA role).
+enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2 };
+
+template <int D, int BIAS = BIAS_NONE>
 struct Cfg {
     static constexpr int SUB = BM * 128;          // bytes of one 128-row x 64-column swizzled block
     static constexpr int NSUB = D / 64;           // 64-column blocks per row
@@ -55,7 +59,10 @@ struct Cfg {
     static constexpr int OFF_K = OFF_Q + TILE_BYTES;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
     static constexpr int OFF_BAR = OFF_V + TILE_BYTES;
-    static constexpr int SMEM_USED = OFF_BAR + 128;
+    // BIAS_ALIBI_MMA: a ones block and a bias block, each 128 rows x 16 bf16 (K-major, no swizzle)
+    static constexpr int OFF_BA = OFF_BAR + 1024;
+    static constexpr int OFF_BB = OFF_BA + 4096;
+    static constexpr int SMEM_USED = (BIAS == BIAS_ALIBI_MMA) ? OFF_BB + 4096 : OFF_BAR + 128;
     // at least ~80 KB so no more than two CTAs share an SM (tensor memory holds two)
     static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > 82 * 1024) ? SMEM_USED + 1024 : 82 * 1024;
     static constexpr uint32_t TMEM_COLS = 256;
@@ -188,9 +195,83 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
-template <int D>
+// The same two passes with the additive bias -m_a |i - j| of ALiBi, in log2 units:
+// x = s * sl2 - mL * |base - c| for in-tile column c, with mL = m_a log2(e) and
+// base = i - (first key of the tile).  Under the causal kinds every allowed key has
+// j <= i, so |base - c| = base - c and the bias is linear in c (ABS = false); the
+// symmetric kinds take the absolute value.  Masked scores are -inf and stay -inf.
+template <bool ABS>
+__device__ __forceinline__ float2 alibi_pair(float base, int c, float mL, float sub) {
+    // -mL * |base - c| - sub and -mL * |base - c - 1| - sub
+    if constexpr (ABS)
+        return make_float2(fmaf(-mL, fabsf(base - (float)c), -sub), fmaf(-mL, fabsf(base - (float)(c + 1)), -sub));
+    else
+        return __ffma2_rn(make_float2((float)c, (float)(c + 1)), make_float2(mL, mL),
+                          make_float2(fmaf(-mL, base, -sub), fmaf(-mL, base, -sub)));
+}
+
+// Row maximum of x (log2 units, no further scaling).
+template <bool MASKED, bool ABS>
+__device__ __forceinline__ float tile_row_max_alibi(uint32_t t_s, const TileMask& mk, float sl2, float mL,
+                                                    float base) {
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const int c0 = h * 64 + e, c1 = h * 64 + 32 + e;
+            const float2 x0 = __ffma2_rn(make_float2(tile_score<MASKED>(r0[e], c0, mk), tile_score<MASKED>(r0[e + 1], c0 + 1, mk)),
+                                         sl2x2, alibi_pair<ABS>(base, c0, mL, 0.f));
+            const float2 x1 = __ffma2_rn(make_float2(tile_score<MASKED>(r1[e], c1, mk), tile_score<MASKED>(r1[e + 1], c1 + 1, mk)),
+                                         sl2x2, alibi_pair<ABS>(base, c1, mL, 0.f));
+            const int k = (e >> 1) & 7;
+            m8[k] = fmax3(m8[k], x0.x, x0.y);
+            m8[k] = fmax3(m8[k], x1.x, x1.y);
+        }
+    }
+    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+template <bool MASKED, bool ABS>
+__device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                                      float mL, float base) {
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32], pk[32];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c0 = h * 64 + 2 * e, c1 = h * 64 + 32 + 2 * e;
+            const float2 x01 = __ffma2_rn(make_float2(tile_score<MASKED>(r0[2 * e], c0, mk), tile_score<MASKED>(r0[2 * e + 1], c0 + 1, mk)),
+                                          sl2x2, alibi_pair<ABS>(base, c0, mL, ref));
+            const float2 x23 = __ffma2_rn(make_float2(tile_score<MASKED>(r1[2 * e], c1, mk), tile_score<MASKED>(r1[2 * e + 1], c1 + 1, mk)),
+                                          sl2x2, alibi_pair<ABS>(base, c1, mL, ref));
+            const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+            acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+            acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
+            pk[e] = pack_bf16x2(p0, p1);
+            pk[16 + e] = pack_bf16x2(p2, p3);
+        }
+        tmem_st32(t_s + h * 32, pk);
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+template <int D, int BIAS>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, BIAS>;
+    constexpr bool ALIBI = BIAS == BIAS_ALIBI_ELEM;  // the per-element bias passes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared* sh = reinterpret_cast<Shared*>(smem + C::OFF_BAR);
@@ -210,6 +291,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     const bool grows = (flags & ATTN_WORK_GLOBAL_ROWS) != 0;
     const int n_band = kv_end - kv_begin;
     const int n_iter = n_band + ((flags & ATTN_WORK_GLOBAL_COLS) ? n_gt : 0);
+    // Band key tile of iteration it.  With the causal ALiBi bias the tiles run from the diagonal
+    // downwards: the bias is 0 at j = i and falls with the distance, so a row's running max is
+    // set by its first tile and the lazy rescale stays rare.
+    constexpr bool REV = BIAS == BIAS_ALIBI_MMA;
+    auto band_tile = [&](int it) { return REV ? kv_end - 1 - it : kv_begin + it; };
     const int b = bh / p.Hq, a = bh - b * p.Hq;
     const int bkv = b * p.Hkv + a / p.group;  // g(a) = a / (Hq / Hkv)
 
@@ -217,6 +303,27 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), i == B_PFULL ? 128u : 1u);
         sh->abort = 0;
         fence_barrier_init();
+    }
+    if constexpr (BIAS == BIAS_ALIBI_MMA) {
+        // Under the causal kinds -m_a |i - j| = -m_a i + m_a (c0 + c) for key c of a tile starting at
+        // c0: the softmax of a row ignores the -m_a i and m_a c0 terms until the end (they are folded
+        // into the running max and the LSE), and the tensor core adds m_a c / scale to S with one
+        // extra K = 16 product: ones [128 x 16] . B^T, B row c = m_a c / scale split into three
+        // bf16 terms (hi + mid + lo, about 24 significant bits; the products with one are exact).
+        const float sb = p.alibi[a] * 1.4426950408889634f / p.scale_log2;  // m_a / scale
+        for (int idx = threadIdx.x; idx < BM * 16; idx += NTHREADS) {
+            const int m = idx >> 4, k = idx & 15;
+            const uint32_t off = (m >> 3) * 256 + (k >> 3) * 128 + (m & 7) * 16 + (k & 7) * 2;
+            const float v = sb * (float)m;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            const float r1 = v - __bfloat162float(hi);
+            const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+            *reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_BA + off) = __float2bfloat16_rn(k < 3 ? 1.f : 0.f);
+            *reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_BB + off) =
+                k == 0 ? hi : k == 1 ? mid : k == 2 ? lo : __float2bfloat16_rn(0.f);
+        }
+        fence_proxy_async_smem();
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(&sh->tmem_base), C::TMEM_COLS);
@@ -244,7 +351,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 const bool in_band = it < n_band;
                 const CUtensorMap* km = in_band ? &p.tm_k : &p.tm_kg;
                 const CUtensorMap* vm = in_band ? &p.tm_v : &p.tm_vg;
-                const int row = in_band ? (kv_begin + it) * BN : (it - n_band) * BN;
+                const int row = in_band ? band_tile(it) * BN : (it - n_band) * BN;
                 if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
                 mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
                 for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * 64, row, bkv);
@@ -280,6 +387,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
                            k > 0);
                 }
+                if constexpr (BIAS == BIAS_ALIBI_MMA)
+                    mma_ss(t_s, sdesc_plain(smem_u32(smem + C::OFF_BA), 128, 256),
+                           sdesc_plain(smem_u32(smem + C::OFF_BB), 128, 256), idesc_qk, 1u);
                 mma_commit(bar(B_SFULL));
                 mma_commit(bar(B_KEMPTY));
                 last_bar = B_KEMPTY; last_par = it & 1;
@@ -324,6 +434,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         }
         const bool lg = (p.kind == ATTN_MASK_LOCAL_GLOBAL) && !grows;
         const float sl2 = p.scale_log2;
+        const float mL = (BIAS != BIAS_NONE) ? p.alibi[a] * 1.4426950408889634f : 0.f;  // ALiBi slope, log2 units
+        const bool causal_kind = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
@@ -337,7 +449,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             bool partial = true;
             TileMask mk{0, -1, 0u, 0u, 0u, 0u};
             if (it < n_band) {
-                const int t = kv_begin + it;
+                const int t = band_tile(it);
                 partial = t < full_begin || t >= full_end;
                 if (partial) {
                     const long c0 = (long)t * BN;
@@ -366,10 +478,27 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 }
                 mk.g0 = bits[0]; mk.g1 = bits[1]; mk.g2 = bits[2]; mk.g3 = bits[3];
             }
-            // ---- pass 1: row max of the (masked) scores
-            float mx = partial ? tile_row_max<true>(t_s, mk) : tile_row_max<false>(t_s, mk);
+            // ---- pass 1: row max of the (masked) scores, in log2 units
+            float mx;
+            float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
+            if constexpr (ALIBI) {
+                base = (float)(i - (long)band_tile(it) * BN);
+                if (causal_kind)
+                    mx = partial ? tile_row_max_alibi<true, false>(t_s, mk, sl2, mL, base)
+                                 : tile_row_max_alibi<false, false>(t_s, mk, sl2, mL, base);
+                else
+                    mx = partial ? tile_row_max_alibi<true, true>(t_s, mk, sl2, mL, base)
+                                 : tile_row_max_alibi<false, true>(t_s, mk, sl2, mL, base);
+            } else {
+                mx = partial ? tile_row_max<true>(t_s, mk) : tile_row_max<false>(t_s, mk);
+                mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
+                if constexpr (BIAS == BIAS_ALIBI_MMA) {
+                    // the tile's constant part of the bias, m_a (c0 - i), in log2 units
+                    base = mL * (float)((long)band_tile(it) * BN - i);
+                    mx += base;  // -inf stays -inf
+                }
+            }
             // ---- running max, with the lazy rescale
-            mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
             const bool grow = mx > m + RESCALE_THRESHOLD;  // false when mx is -inf; true on the first finite max
             const float m_new = grow ? mx : m;
             const float alpha = grow ? ex2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first finite max
@@ -390,8 +519,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             m = m_new;
             const float ref = (m == -INFINITY) ? 0.f : m;
             // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P over the S columns
-            const float sum = partial ? tile_exp_store<true>(t_s, mk, sl2, ref)
-                                      : tile_exp_store<false>(t_s, mk, sl2, ref);
+            float sum;
+            if constexpr (ALIBI) {
+                if (causal_kind)
+                    sum = partial ? tile_exp_store_alibi<true, false>(t_s, mk, sl2, ref, mL, base)
+                                  : tile_exp_store_alibi<false, false>(t_s, mk, sl2, ref, mL, base);
+                else
+                    sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base)
+                                  : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base);
+            } else {
+                const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
+                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff) : tile_exp_store<false>(t_s, mk, sl2, r_eff);
+            }
             l += sum;
             tmem_wait_st();
             tc_fence_before();
@@ -482,17 +621,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-template <int D>
+template <int D, int BIAS>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
-    using C = Cfg<D>;
+    using C = Cfg<D, BIAS>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_ALLOC);
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BIAS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attn_fwd_tc_kernel<D><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_fwd_tc_kernel<D, BIAS><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -500,8 +639,17 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
-    if (d == 128) return launch<128>(p, n_items, stream);
-    if (d == 64) return launch<64>(p, n_items, stream);
+    const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
+    if (p.alibi && causal) {
+        if (d == 128) return launch<128, BIAS_ALIBI_MMA>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_ALIBI_MMA>(p, n_items, stream);
+    } else if (p.alibi) {
+        if (d == 128) return launch<128, BIAS_ALIBI_ELEM>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_ALIBI_ELEM>(p, n_items, stream);
+    } else {
+        if (d == 128) return launch<128, BIAS_NONE>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_NONE>(p, n_items, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -23,6 +23,7 @@ struct attn_decode_plan {
     int* d_err = nullptr;
     unsigned* d_counters = nullptr;
     float* d_part = nullptr;
+    float* d_alibi = nullptr;  // ALiBi slopes [Hq] (attn_decode_set_alibi), or null
     const void* last_q = nullptr;
     const void* last_k = nullptr;
     const void* last_v = nullptr;
@@ -90,6 +91,7 @@ void free_decode(attn_decode_plan* h) {
     if (h->d_err) cudaFree(h->d_err);
     if (h->d_counters) cudaFree(h->d_counters);
     if (h->d_part) cudaFree(h->d_part);
+    if (h->d_alibi) cudaFree(h->d_alibi);
     delete h;
 }
 
@@ -191,6 +193,26 @@ attn_status attn_decode_poll_device_error(attn_decode_handle h, int* code) {
         if (cudaMemset(h->d_counters, 0, sizeof(unsigned) * h->B * h->Hkv) != cudaSuccess) return ATTN_ERR_CUDA;
     }
     return *code ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+attn_status attn_decode_set_alibi(attn_decode_handle h, const float* slopes) {
+    if (!h) return ATTN_ERR_INVALID_ARG;
+    if (!slopes) {
+        if (h->d_alibi) cudaFree(h->d_alibi);
+        h->d_alibi = nullptr;
+        h->p.alibi = nullptr;
+        return ATTN_OK;
+    }
+    for (int a = 0; a < h->Hq; ++a)
+        if (!std::isfinite(slopes[a])) return ATTN_ERR_INVALID_ARG;
+    if (!h->d_alibi) {
+        cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->d_alibi), sizeof(float) * h->Hq);
+        if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
+    }
+    if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    h->p.alibi = h->d_alibi;
+    return ATTN_OK;
 }
 
 attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas) {

@@ -37,6 +37,7 @@ struct TcParams {
     float* part_o;       // [B*Hq, n_global, n_chunks, d] fp32, each normalised by its own sum
     float* part_lse;     // [B*Hq, n_global, n_chunks]
     int n_chunks;
+    const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
 };
 
 // Parameters of the fp32 CUDA-core kernel.
@@ -48,6 +49,7 @@ struct F32Params {
     float scale;
     const int* globals; int n_global;
     const unsigned char* is_global;  // [S] flags (local + global only)
+    const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
 };
 
 // Gather of the global rows of Q, K, V into dense scratch tensors.
@@ -90,6 +92,7 @@ struct DecodeParams {
     float scale_log2;
     int n_cta;
     long long total_tiles;                   // T
+    const float* alibi;                      // [Hq] slopes of the bias -m_a |t - j| (device), or null
     int len[kDecodeMaxBatch];                // cache length of each sequence
     int tile_prefix[kDecodeMaxBatch + 1];    // key tiles of the sequences before b (per kv head)
 };

@@ -240,6 +240,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn
 // Shared-memory matrix descriptor, 128-byte swizzle:
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4, 32-45 stride
 //   byte offset >> 4, bits 46-47 = 1 (descriptor version), 61-63 = 2 (128B swizzle).
+// The same without swizzling (canonical K-major layout of 8-row x 16-byte core matrices):
+// lbo = byte stride between the core matrices along K, sbo = along M/N; bits 61-63 = 0.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);

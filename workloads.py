@@ -224,3 +224,10 @@ def decode_bytes(w: DecodeWorkload, lens) -> int:
     kv = 2 * kv_rows * w.Hkv * w.d * el
     qo = 2 * w.B * w.Hq * w.S_q * w.d * el
     return kv + qo + 4 * w.B * w.Hq * w.S_q
+
+
+def alibi_slopes(H: int):
+    """Slopes m_a = 2^(-8 (a + 1) / H) for H heads, a geometric sequence.  The pages fix one
+    slope per head for the ALiBi bias -m_a |i - j| but give no values; this common choice
+    is an input recipe, not something the pages state."""
+    return [2.0 ** (-8.0 * (a + 1) / H) for a in range(H)]
