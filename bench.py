@@ -214,13 +214,19 @@ def run_ours(args, w):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    Qc, Kc, Vc = wl.make_inputs(w)
+    if args.fp8:
+        Qc, Kc, Vc, descales = wl.make_fp8_inputs(w)
+        plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind,
+                             window=w.window)
+        plan.set_fp8_descale(*descales)
+    else:
+        Qc, Kc, Vc = wl.make_inputs(w)
+        plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind,
+                             window=w.window, global_idx=list(w.globals_idx))
     Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
-    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind,
-                         window=w.window, global_idx=list(w.globals_idx))
     if args.alibi:
         plan.set_alibi(wl.alibi_slopes(w.Hq))
-    O = torch.empty_like(Q)
+    O = torch.empty(Q.shape, dtype=torch.bfloat16 if args.fp8 else Q.dtype, device=dev)
     LSE = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -307,13 +313,16 @@ def run_ours(args, w):
         return 0
 
     achieved = useful / (mean_ms * 1e-3) / 1e12
-    peak = float(pk["bf16_tflops"])
+    peak = float(pk["bf16_tflops"]) * (2.0 if args.fp8 else 1.0)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": ncu_traffic(w.name), "peak_source": f"{pk_src} bf16_tflops (burst, cuBLAS)",
+                "traffic": None if args.fp8 else ncu_traffic(w.name),
+                "peak_source": (f"{pk_src} bf16_tflops (burst, cuBLAS) x 2, the nominal E4M3:BF16 rate ratio"
+                                if args.fp8 else f"{pk_src} bf16_tflops (burst, cuBLAS)"),
                 "kernel": "attn_fwd_tc_kernel"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3" if args.fp8 else ("bf16" if w.dtype == "bf16" else "f32"),
+            "data": "synthetic" + (" (E4M3, per-tensor scales)" if args.fp8 else ""),
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
                        "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
                        "useful_gflop_per_step": useful / 1e9, "l2": "flushed before every step (256 MiB write)",
@@ -534,6 +543,8 @@ def main():
                     choices=sorted(wl.BY_NAME) + sorted(wl.DECODE_BY_NAME))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="E4M3 Q, K, V with per-tensor scales (prefill workloads; same metric)")
     ap.add_argument("--alibi", action="store_true",
                     help="add the ALiBi score bias with slopes 2^(-8(a+1)/H) (same workload, same metric)")
     args = ap.parse_args()

@@ -28,7 +28,8 @@
  * Tensor layouts (all contiguous, row-major, the head dimension fastest):
  *     Q, O : [B, H_q,  S, d_k]     K, V : [B, H_kv, S, d_k]     LSE : [B, H_q, S] float32
  * Element type: ATTN_BF16 -> Q, K, V, O are bfloat16 (fp32 accumulation);
- *               ATTN_F32  -> Q, K, V, O are float32.
+ *               ATTN_F32  -> Q, K, V, O are float32;
+ *               ATTN_FP8_E4M3 -> Q, K, V are E4M3 bytes, O is bfloat16.
  * Every pointer passed to attn_forward is a device pointer of the current
  * CUDA device and must be 16-byte aligned.
  *
@@ -73,7 +74,14 @@ typedef enum {
     ATTN_MASK_LOCAL_GLOBAL = 4     /* |i - j| <= window, or i in G, or j in G              */
 } attn_mask_kind;
 
-typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+/* ATTN_FP8_E4M3: Q, K, V are 8-bit E4M3 floats with per-tensor descale factors
+ * (attn_set_fp8_descale); O is bfloat16.  The products run in E4M3 with fp32
+ * accumulation, P is rounded to E4M3 for the second product, and the softmax is
+ * fp32 ("Transformer 演进与变体" (ai.icyfenix.cn), section Flash Attention, FP8
+ * support: matrix products in FP8, softmax and accumulation in higher precision;
+ * "第 8 章 现代大模型架构", 8.6.5: scale before the multiply-add, descale at the
+ * output).  d_k = 128 only; not with LOCAL_GLOBAL or the ALiBi bias. */
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 typedef struct attn_plan* attn_handle;
 
@@ -201,6 +209,15 @@ attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
  * Must not be called while a forward of this handle is in flight.
  */
 attn_status attn_set_alibi(attn_handle h, const float* slopes);
+
+/*
+ * attn_set_fp8_descale -- the per-tensor factors of an ATTN_FP8_E4M3 handle: the
+ * real Q is descale_q times the stored E4M3 values, and likewise K and V.  Scores
+ * are scale * descale_q * descale_k * (q8 . k8); O = descale_v * sum_j p_j v8_j / l.
+ * Defaults 1.  Errors: ATTN_ERR_INVALID_ARG (not an E4M3 handle; a factor that is
+ * not finite and > 0).  Must not be called while a forward of the handle is in flight.
+ */
+attn_status attn_set_fp8_descale(attn_handle h, float descale_q, float descale_k, float descale_v);
 
 /*
  * attn_set_watchdog -- test hook for the failure-detection path.

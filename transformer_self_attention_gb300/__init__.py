@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_OOM = range(6)
 MASK_FULL, MASK_CAUSAL, MASK_SLIDING, MASK_CAUSAL_SLIDING, MASK_LOCAL_GLOBAL = range(5)
-ATTN_BF16, ATTN_F32 = 0, 1
+ATTN_BF16, ATTN_F32, ATTN_FP8_E4M3 = 0, 1, 2
 TILE = 128
 WORK_INTS = 8
 WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
@@ -29,7 +29,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
-            "attn_decode_set_alibi")
+            "attn_decode_set_alibi", "attn_set_fp8_descale")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -65,6 +65,8 @@ def _load():
     lib.attn_set_alibi.restype = I
     lib.attn_decode_set_alibi.argtypes = [P, P]
     lib.attn_decode_set_alibi.restype = I
+    lib.attn_set_fp8_descale.argtypes = [P, F, F, F]
+    lib.attn_set_fp8_descale.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -277,7 +279,7 @@ class DecodeAttention:
                 raise ValueError("one slope per query head")
             st = _lib.attn_decode_set_alibi(self.handle, ctypes.cast(_float_array(slopes), ctypes.c_void_p))
         if st != ATTN_OK:
-            raise AttnError(st, "attn_decode_set_alibi")
+            raise AttnError(st, "attn_decode_set_alibi", "attn_set_fp8_descale")
 
     def set_grid_limit(self, max_ctas: int):
         """Test hook: at most max_ctas CTAs per launch (long shares on small problems)."""
@@ -303,8 +305,8 @@ class Attention:
         self.scale = float(scale) if scale is not None else 1.0 / math.sqrt(d)
         self.kind, self.window = int(kind), int(window)
         self.global_idx = list(global_idx or [])
-        self.handle = attn_create(B, Hq, Hkv, S, d, ATTN_BF16 if dtype == "bf16" else ATTN_F32, self.scale,
-                                  self.kind, self.window, self.global_idx)
+        code = {"bf16": ATTN_BF16, "f32": ATTN_F32, "e4m3": ATTN_FP8_E4M3}[dtype]
+        self.handle = attn_create(B, Hq, Hkv, S, d, code, self.scale, self.kind, self.window, self.global_idx)
 
     def close(self):
         if getattr(self, "handle", None):
@@ -320,12 +322,12 @@ class Attention:
     def __call__(self, Q, K, V, O=None, LSE=None, stream=None, want_lse=True):
         import torch
         B, Hq, Hkv, S, d = self.shape
-        tdt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        tdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn}[self.dtype]
         for name, t, h in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv)):
             if not t.is_cuda or t.dtype != tdt or not t.is_contiguous() or tuple(t.shape) != (B, h, S, d):
                 raise ValueError(f"{name} must be a contiguous CUDA {tdt} tensor of shape {(B, h, S, d)}")
         if O is None:
-            O = torch.empty_like(Q)
+            O = torch.empty(Q.shape, dtype=torch.bfloat16 if self.dtype == "e4m3" else Q.dtype, device=Q.device)
         if LSE is None and want_lse:
             LSE = torch.empty((B, Hq, S), dtype=torch.float32, device=Q.device)
         if stream is None:
@@ -343,6 +345,12 @@ class Attention:
         st = attn_set_watchdog(self.handle, limit_ns, withhold)
         if st != ATTN_OK:
             raise AttnError(st, "attn_set_watchdog")
+
+    def set_fp8_descale(self, descale_q: float, descale_k: float, descale_v: float):
+        """Per-tensor factors of E4M3 inputs (real value = factor x stored value)."""
+        st = _lib.attn_set_fp8_descale(self.handle, float(descale_q), float(descale_k), float(descale_v))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_set_fp8_descale")
 
     def set_alibi(self, slopes=None):
         """Add the ALiBi score bias -slopes[a] |i - j| (one slope per query head); None removes it."""

@@ -74,6 +74,20 @@ bool encode_map(CUtensorMap* map, const void* base, int d, long rows, long heads
     return r == CUDA_SUCCESS;
 }
 
+// The same for E4M3 tensors (bytes): box {128, box_rows, 1}, one 128-byte swizzled row.
+bool encode_map_e4m3(CUtensorMap* map, const void* base, int d, long rows, long heads, unsigned box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)rows * d};
+    cuuint32_t box[3] = {128, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 constexpr unsigned kTileRows = ATTN_TILE;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -139,11 +153,12 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
                         attn_mask_kind kind, int window, const int* global_idx, int n_global) {
     if (!out) return ATTN_ERR_INVALID_ARG;
     *out = nullptr;
-    if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 && dtype != ATTN_F32 && dtype != ATTN_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, global_idx, n_global);
     if (vs != ATTN_OK) return vs;
     if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_FP8_E4M3 && (d_k != 128 || kind == ATTN_MASK_LOCAL_GLOBAL)) return ATTN_ERR_UNSUPPORTED;
     const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
                           kind == ATTN_MASK_LOCAL_GLOBAL;
 
@@ -173,7 +188,7 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         for (int g : h->globals) isg[g] = 1;
         if ((e = upload(&h->d_isg, isg.data(), isg.size())) != cudaSuccess) return fail(e);
     }
-    if (dtype == ATTN_BF16) {
+    if (dtype == ATTN_BF16 || dtype == ATTN_FP8_E4M3) {
         if ((e = upload(reinterpret_cast<int**>(&h->d_work), h->sched.items.data(), h->sched.items.size())) !=
             cudaSuccess)
             return fail(e);
@@ -209,6 +224,8 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         p.watchdog_ns = 2000000000LL;
         p.withhold_v = 0;
         p.n_chunks = h->sched.n_chunks;
+        p.fp8 = dtype == ATTN_FP8_E4M3;
+        p.o_scale = 1.f;
         p.part_o = h->d_part;
         p.part_lse = h->d_part ? h->d_part + (size_t)B * Hq * nG * h->sched.n_chunks * d_k : nullptr;
     }
@@ -237,16 +254,17 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         e = attn::launch_f32_forward(p, h->d, stream);
     } else {
         attn::TcParams& p = h->tp;
+        auto in_map = h->dtype == ATTN_FP8_E4M3 ? encode_map_e4m3 : encode_map;
         if (Q != h->last_q) {
-            if (!encode_map(&p.tm_q, Q, h->d, h->S, (long)h->B * h->Hq, kTileRows)) return ATTN_ERR_CUDA;
+            if (!in_map(&p.tm_q, Q, h->d, h->S, (long)h->B * h->Hq, kTileRows)) return ATTN_ERR_CUDA;
             h->last_q = Q;
         }
         if (K != h->last_k) {
-            if (!encode_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
+            if (!in_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
             h->last_k = K;
         }
         if (V != h->last_v) {
-            if (!encode_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
+            if (!in_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
             h->last_v = V;
         }
         if (O != h->last_o) {
@@ -341,7 +359,7 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     }
     for (int a = 0; a < h->Hq; ++a)
         if (!std::isfinite(slopes[a])) return ATTN_ERR_INVALID_ARG;
-    if (h->kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
+    if (h->kind == ATTN_MASK_LOCAL_GLOBAL || h->dtype == ATTN_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
     if (!h->d_alibi) {
         cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->d_alibi), sizeof(float) * h->Hq);
         if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
@@ -349,6 +367,17 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     h->tp.alibi = h->d_alibi;
+    return ATTN_OK;
+}
+
+attn_status attn_set_fp8_descale(attn_handle h, float descale_q, float descale_k, float descale_v) {
+    if (!h) return ATTN_ERR_INVALID_ARG;
+    if (h->dtype != ATTN_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
+    if (!std::isfinite(descale_q) || !std::isfinite(descale_k) || !std::isfinite(descale_v) || !(descale_q > 0.f) ||
+        !(descale_k > 0.f) || !(descale_v > 0.f))
+        return ATTN_ERR_INVALID_ARG;
+    h->tp.scale_log2 = (float)((double)h->scale * descale_q * descale_k * 1.4426950408889634);
+    h->tp.o_scale = descale_v;
     return ATTN_OK;
 }
 

@@ -50,11 +50,13 @@ enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 // causal kinds, added by the tensor core (see the MMA role).
 enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2 };
 
-template <int D, int BIAS = BIAS_NONE>
+template <int D, int BIAS = BIAS_NONE, bool F8 = false>
 struct Cfg {
-    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 64-column swizzled block
-    static constexpr int NSUB = D / 64;           // 64-column blocks per row
-    static constexpr int TILE_BYTES = BM * D * 2; // one Q / K / V tile
+    static constexpr int EB = F8 ? 1 : 2;         // bytes per element (E4M3 or bf16)
+    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 128-byte swizzled block
+    static constexpr int XW = 128 / EB;           // elements per 128-byte row of a block
+    static constexpr int NSUB = D / XW;           // blocks per row
+    static constexpr int TILE_BYTES = BM * D * EB; // one Q / K / V tile
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + TILE_BYTES;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
@@ -195,6 +197,42 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
+// tile_exp_store for E4M3 P: four keys per 32-bit tensor-memory column (the A operand
+// layout of the 8-bit MMA), keys 4q..4q+3 of half h in column 16h + q.  P <= 2^8 by the
+// lazy rescale, inside the E4M3 range (448).
+template <bool MASKED>
+__device__ __forceinline__ float tile_exp_store_e4m3(uint32_t t_s, const TileMask& mk, float sl2, float ref) {
+    const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32], pk[16];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float pa[4], pb[4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+                const int c0 = h * 64 + 4 * q + u, c1 = h * 64 + 32 + 4 * q + u;
+                const float2 xa = __ffma2_rn(make_float2(tile_score<MASKED>(r0[4 * q + u], c0, mk),
+                                                         tile_score<MASKED>(r0[4 * q + u + 1], c0 + 1, mk)), sl2x2, nref);
+                const float2 xb = __ffma2_rn(make_float2(tile_score<MASKED>(r1[4 * q + u], c1, mk),
+                                                         tile_score<MASKED>(r1[4 * q + u + 1], c1 + 1, mk)), sl2x2, nref);
+                pa[u] = ex2(xa.x); pa[u + 1] = ex2(xa.y);
+                pb[u] = ex2(xb.x); pb[u + 1] = ex2(xb.y);
+                acc0 = __fadd2_rn(acc0, make_float2(pa[u], pa[u + 1]));
+                acc1 = __fadd2_rn(acc1, make_float2(pb[u], pb[u + 1]));
+            }
+            pk[q] = pack_e4m3x4(pa[0], pa[1], pa[2], pa[3]);
+            pk[8 + q] = pack_e4m3x4(pb[0], pb[1], pb[2], pb[3]);
+        }
+        tmem_st16(t_s + h * 16, pk);
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
 // The same two passes with the additive bias -m_a |i - j| of ALiBi, in log2 units:
 // x = s * sl2 - mL * |base - c| for in-tile column c, with mL = m_a log2(e) and
 // base = i - (first key of the tile).  Under the causal kinds every allowed key has
@@ -268,9 +306,9 @@ __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMa
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
-template <int D, int BIAS>
+template <int D, int BIAS, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<D, BIAS>;
+    using C = Cfg<D, BIAS, F8>;
     constexpr bool ALIBI = BIAS == BIAS_ALIBI_ELEM;  // the per-element bias passes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -344,7 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         if (lane == 0) {
             const CUtensorMap* qmap = grows ? &p.tm_qg : &p.tm_q;
             mbar_arrive_expect_tx(bar(B_Q), C::TILE_BYTES);
-            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * 64, q_tile * BM, bh);
+            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * C::XW, q_tile * BM, bh);
             int k_loaded = 0, v_loaded = 0;
             bool ok = true;
             for (int it = 0; it < n_iter && ok; ++it) {
@@ -354,12 +392,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 const int row = in_band ? band_tile(it) * BN : (it - n_band) * BN;
                 if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
                 mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * 64, row, bkv);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * C::XW, row, bkv);
                 ++k_loaded;
                 if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
                 if (p.withhold_v) continue;
                 mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * 64, row, bkv);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * C::XW, row, bkv);
                 ++v_loaded;
             }
             if (sh->abort) {  // let the copies this thread issued land before the CTA exits
@@ -371,8 +409,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(BM, D, true);
+            constexpr uint32_t idesc_qk = F8 ? idesc_e4m3_f32(BM, BN, false) : idesc_bf16_f32(BM, BN, false);
+            constexpr uint32_t idesc_pv = F8 ? idesc_e4m3_f32(BM, D, true) : idesc_bf16_f32(BM, D, true);
+            constexpr int KS = F8 ? 32 : 16;  // K elements per MMA (32 bytes of a 128-byte row either way)
             const uint32_t t_s = tmem + C::TMEM_S, t_o = tmem + C::TMEM_O;
             int last_bar = -1, last_par = 0;
             bool ok = wait_bounded(bar(B_Q), 0, sh, p, ERR_MMA);
@@ -382,10 +421,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
+                for (int k = 0; k < D / KS; ++k) {
                     const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
-                           k > 0);
+                    if constexpr (F8)
+                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
+                                  k > 0);
+                    else
+                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
+                               k > 0);
                 }
                 if constexpr (BIAS == BIAS_ALIBI_MMA)
                     mma_ss(t_s, sdesc_plain(smem_u32(smem + C::OFF_BA), 128, 256),
@@ -397,10 +440,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 if (!(ok = wait_bounded(bar(B_VFULL), it & 1, sh, p, ERR_MMA))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    // P: 16 keys = 8 packed bf16x2 columns; V: 16 key rows of 128 B each
-                    mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * 16 * 128, C::SUB, 1024), idesc_pv,
-                           (it > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < BN / KS; ++k) {
+                    // P: KS keys = 8 tensor-memory columns (2 bf16 or 4 E4M3 per column);
+                    // V: KS key rows of 128 B each (MN-major: d runs along the row)
+                    if constexpr (F8)
+                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
+                                  (it > 0 || k > 0) ? 1u : 0u);
+                    else
+                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
+                               (it > 0 || k > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(B_OFULL));
                 mma_commit(bar(B_VEMPTY));
@@ -527,6 +575,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 else
                     sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base)
                                   : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base);
+            } else if constexpr (F8) {
+                sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref) : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref);
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
                 sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff) : tile_exp_store<false>(t_s, mk, sl2, r_eff);
@@ -541,7 +591,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         tc_fence_after();
         ok = named_bar_and(1, 128, ok);  // the same decision in all four softmax warps
         if (ok) {
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = l > 0.f ? p.o_scale / l : 0.f;  // o_scale: the V descale of E4M3 inputs
             const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             if (!grows) {
                 // O row -> bf16 -> 128B-swizzled staging in the (now idle) Q buffer -> TMA store
@@ -566,7 +616,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 fence_proxy_async_smem();
                 named_bar_sync(1, 128);
                 if (threadIdx.x == 0) {
-                    for (int s = 0; s < C::NSUB; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
+                    // O is bf16 (64 columns per 128-byte block); with E4M3 inputs the staging runs on
+                    // into the (idle) K buffer that follows the Q buffer
+                    for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
                     tma_store_commit_and_wait_read();
                 }
             } else if (p.n_chunks == 1) {
@@ -621,17 +673,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-template <int D, int BIAS>
+template <int D, int BIAS, bool F8 = false>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
-    using C = Cfg<D, BIAS>;
+    using C = Cfg<D, BIAS, F8>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BIAS>,
+        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BIAS, F8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attn_fwd_tc_kernel<D, BIAS><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_fwd_tc_kernel<D, BIAS, F8><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -640,6 +692,10 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
+    if (p.fp8) {  // E4M3 inputs: d = 128, no bias, no local + global (checked by the host)
+        if (d == 128 && !p.alibi) return launch<128, BIAS_NONE, true>(p, n_items, stream);
+        return cudaErrorInvalidValue;
+    }
     if (p.alibi && causal) {
         if (d == 128) return launch<128, BIAS_ALIBI_MMA>(p, n_items, stream);
         if (d == 64) return launch<64, BIAS_ALIBI_MMA>(p, n_items, stream);

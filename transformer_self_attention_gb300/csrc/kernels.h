@@ -38,6 +38,8 @@ struct TcParams {
     float* part_lse;     // [B*Hq, n_global, n_chunks]
     int n_chunks;
     const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
+    int fp8;             // Q, K, V are E4M3 (scale_log2 includes their descales)
+    float o_scale;       // factor on O at the end (the V descale for E4M3 inputs, else 1)
 };
 
 // Parameters of the fp32 CUDA-core kernel.

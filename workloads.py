@@ -231,3 +231,27 @@ def alibi_slopes(H: int):
     slope per head for the ALiBi bias -m_a |i - j| but give no values; this common choice
     is an input recipe, not something the pages state."""
     return [2.0 ** (-8.0 * (a + 1) / H) for a in range(H)]
+
+
+def make_fp8_inputs(w: Workload):
+    """E4M3 versions of the workload's Q, K, V with per-tensor descale factors.
+
+    Each float32 tensor x of the recipe is scaled by 448 / max|x| (448: the largest finite
+    E4M3 value), rounded to E4M3, and its descale is max|x| / 448.  Returns
+    (Q8, K8, V8, (descale_q, descale_k, descale_v)) on the CPU.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    Q = torch.randn(w.B, w.Hq, w.S, w.d, generator=g, dtype=torch.float32)
+    K = torch.randn(w.B, w.Hkv, w.S, w.d, generator=g, dtype=torch.float32)
+    V = torch.randn(w.B, w.Hkv, w.S, w.d, generator=g, dtype=torch.float32)
+    if w.q_upper_heads_scale != 1.0:
+        Q[:, w.Hq // 2:] *= w.q_upper_heads_scale
+    if w.k_position_offset_std != 0.0:
+        K += torch.randn(w.B, 1, w.S, 1, generator=g, dtype=torch.float32) * w.k_position_offset_std
+    out, ds = [], []
+    for x in (Q, K, V):
+        amax = float(x.abs().max())
+        out.append((x * (448.0 / amax)).to(torch.float8_e4m3fn))
+        ds.append(amax / 448.0)
+    return out[0], out[1], out[2], tuple(ds)
