@@ -74,6 +74,8 @@ def _load():
             lib.oracle_decode.restype = I
             lib.oracle_decode_bias.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double, I, I, P, P, P, P]
             lib.oracle_decode_bias.restype = I
+            lib.oracle_backward.argtypes = [P, P, P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P, P, P, P]
+            lib.oracle_backward.restype = I
             _lib = lib
     return _lib
 
@@ -196,3 +198,30 @@ def decode(Q, K, V, cache_len, scale, kind, window=0, alibi=None):
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return O, LSE
+
+
+def backward(Q, K, V, dO, scale, kind, window=0, globals_idx=None, alibi=None):
+    """Gradients of the attention with respect to Q, K, V for the output gradient dO.
+
+    Q, dO [B, Hq, S, d]; K, V [B, Hkv, S, d].  Returns (dQ, dK, dV) in float64 with the
+    shapes of Q, K, V (dK and dV summed over the query heads of each kv head).
+    """
+    lib = _load()
+    Q = np.ascontiguousarray(Q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    dO = np.ascontiguousarray(dO, dtype=np.float32)
+    B, Hq, S, d = Q.shape
+    Hkv = K.shape[1]
+    assert K.shape == V.shape == (B, Hkv, S, d) and dO.shape == Q.shape
+    g, ng = _globals_array(globals_idx)
+    sl = _slopes(alibi, Hq)
+    dQ = np.empty(Q.shape, dtype=np.float64)
+    dK = np.empty(K.shape, dtype=np.float64)
+    dV = np.empty(V.shape, dtype=np.float64)
+    rc = lib.oracle_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, Hq, Hkv, S, d, float(scale), int(kind),
+                             int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None, _ptr(dQ), _ptr(dK),
+                             _ptr(dV))
+    if rc != 0:
+        raise ValueError("oracle_backward rejected its arguments")
+    return dQ, dK, dV

@@ -38,6 +38,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 /* mask kinds: same numbering as the library's public header, restated here */
 enum {
@@ -364,5 +367,120 @@ int oracle_decode_bias(const float* Q, const float* K, const float* V,
         free(s);
         free(acc);
     }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Backward pass: the gradients of the forward attention above with respect to
+ * Q, K and V, given the output gradient dO.  The pages give no formulas for it;
+ * they say only that the tiled method is exact and serves training ("Transformer
+ * 演进与变体", section Flash Attention), so this is the plain derivative of the
+ * definition, row by row (same mask, same g(a), optional ALiBi slopes):
+ *
+ *   P_ij  = exp(s_ij - LSE_i)            over allowed j  (s_ij as in the forward)
+ *   dV_j += P_ij dO_i                    summed over the query heads of kv head g
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij  (= dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j += scale sum_i dS_ij q_i        summed over the query heads of kv head g
+ *
+ * Q, dO : float32 [B, Hq, S, d]   K, V : float32 [B, Hkv, S, d]
+ * dQ    : fp64 [B, Hq, S, d] (out)   dK, dV : fp64 [B, Hkv, S, d] (out, overwritten)
+ * Rows are computed in parallel; the dK / dV sums over rows are kept per thread
+ * and added at the end, in a fixed order.
+ * Returns 0, or -1 on bad arguments or allocation failure.
+ */
+int oracle_backward(const float* Q, const float* K, const float* V, const float* dO,
+                    int B, int Hq, int Hkv, int S, int d, double scale, int kind, int window,
+                    const int* G, int nG, const double* alibi,
+                    double* dQ, double* dK, double* dV)
+{
+    if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || d < 1 || Hq % Hkv != 0) return -1;
+    unsigned char* is_global = make_global_flags(S, G, nG);
+    if (!is_global) return -1;
+    const int group = Hq / Hkv;
+    const size_t kv_elems = (size_t)B * Hkv * S * d;
+    int nthreads = 1;
+#ifdef _OPENMP
+    nthreads = omp_get_max_threads();
+#endif
+    double* part = (double*)calloc((size_t)nthreads * 2 * kv_elems, sizeof(double));
+    if (!part) { free(is_global); return -1; }
+    int failed = 0;
+    const long n = (long)B * Hq * S;
+
+#pragma omp parallel
+    {
+        int tid = 0;
+#ifdef _OPENMP
+        tid = omp_get_thread_num();
+#endif
+        double* pdK = part + (size_t)tid * 2 * kv_elems;
+        double* pdV = pdK + kv_elems;
+        double* s = (double*)malloc(sizeof(double) * (size_t)S);
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        if (!s || !o) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (long r = 0; r < n; ++r) {
+            if (!s || !o) continue;
+            const int b = (int)(r / ((long)Hq * S));
+            const int a = (int)((r / S) % Hq);
+            const long i = r % S;
+            const int ga = a / group;
+            const size_t kvh = ((size_t)b * Hkv + ga) * (size_t)S * d;
+            const float* q = Q + (size_t)r * d;
+            const float* go = dO + (size_t)r * d;
+            /* forward quantities of the row: scores, max, sum, O */
+            double m = -INFINITY;
+            for (long j = 0; j < S; ++j) {
+                if (!oracle_allowed(kind, i, j, S, window, is_global)) continue;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) dot += (double)q[c] * (double)K[kvh + (size_t)j * d + c];
+                s[j] = dot * scale;
+                if (alibi) s[j] -= alibi[a] * (double)labs(i - j);
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int c = 0; c < d; ++c) o[c] = 0.0;
+            for (long j = 0; j < S; ++j) {
+                if (!oracle_allowed(kind, i, j, S, window, is_global)) continue;
+                const double e = exp(s[j] - m);
+                l += e;
+                for (int c = 0; c < d; ++c) o[c] += e * (double)V[kvh + (size_t)j * d + c];
+            }
+            double Di = 0.0;
+            for (int c = 0; c < d; ++c) { o[c] /= l; Di += (double)go[c] * o[c]; }
+            double* gq = dQ + (size_t)r * d;
+            for (int c = 0; c < d; ++c) gq[c] = 0.0;
+            for (long j = 0; j < S; ++j) {
+                if (!oracle_allowed(kind, i, j, S, window, is_global)) continue;
+                const double P = exp(s[j] - m) / l;
+                double dP = 0.0;
+                for (int c = 0; c < d; ++c) dP += (double)go[c] * (double)V[kvh + (size_t)j * d + c];
+                const double dS = P * (dP - Di);
+                for (int c = 0; c < d; ++c) {
+                    gq[c] += scale * dS * (double)K[kvh + (size_t)j * d + c];
+                    pdK[kvh + (size_t)j * d + c] += scale * dS * (double)q[c];
+                    pdV[kvh + (size_t)j * d + c] += P * (double)go[c];
+                }
+            }
+        }
+        free(s);
+        free(o);
+    }
+    if (!failed) {
+        for (size_t e = 0; e < kv_elems; ++e) { dK[e] = 0.0; dV[e] = 0.0; }
+        for (int t = 0; t < nthreads; ++t) {
+            const double* pdK = part + (size_t)t * 2 * kv_elems;
+            const double* pdV = pdK + kv_elems;
+            for (size_t e = 0; e < kv_elems; ++e) { dK[e] += pdK[e]; dV[e] += pdV[e]; }
+        }
+    }
+    free(part);
+    free(is_global);
     return failed ? -1 : 0;
 }
