@@ -344,6 +344,196 @@ def run_ours(args, w):
     return 0
 
 
+# ----------------------------------------------------------------------------- backward
+BWD_METRIC = "attention bwd useful TFLOP/s and % of GB300 dense BF16 tensor peak"
+BWD_KERNEL_SOURCES = ["transformer_self_attention_gb300/csrc/attn_bwd.cu",
+                      "transformer_self_attention_gb300/csrc/sm103_ptx.h",
+                      "transformer_self_attention_gb300/csrc/kernels.h"]
+
+
+def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int | None = None):
+    """The fp64 backward oracle, as it stands, on whole (batch, kv head) slices of the workload
+    (every query head of the group, every row)."""
+    n_cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
+    import oracle
+    oracle.build()
+    key = ("bwd", w.name)
+    if key not in _INPUTS:
+        Qc, Kc, Vc = wl.make_inputs(w)
+        _INPUTS[key] = tuple(t.float().numpy() for t in (Qc, Kc, Vc, wl.make_grad_output(w)))
+    Qf, Kf, Vf, dOf = _INPUTS[key]
+    group = w.Hq // w.Hkv
+    per_slice = wl.backward_flops(w) / (w.B * w.Hkv)
+
+    def run(n):
+        t0 = time.perf_counter()
+        for k in range(n):
+            b, g = divmod(k % (w.B * w.Hkv), w.Hkv)
+            qs = slice(g * group, (g + 1) * group)
+            oracle.backward(Qf[b:b + 1, qs], Kf[b:b + 1, g:g + 1], Vf[b:b + 1, g:g + 1], dOf[b:b + 1, qs], w.scale,
+                            w.kind, w.window)
+        return time.perf_counter() - t0
+
+    if n_slices is None:
+        dt = run(1)
+        n_slices = max(1, min(w.B * w.Hkv, int(target_s / max(dt, 1e-6))))
+    dt = run(n_slices)
+    fl = per_slice * n_slices
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+            "kind": "oracle", "seconds": round(dt, 3), "n_slices": n_slices,
+            "sample": f"{n_slices} of {w.B * w.Hkv} (batch, kv head) slices in full ({group} query heads each), "
+                      f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
+
+
+def _bwd_config(w, useful):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+            "mask": wl.MASK_NAMES[w.kind], "window": w.window, "pass": "backward (dQ, dK, dV)",
+            "useful_gflop_per_step": useful / 1e9, "flops_per_pair": f"10 d (2.5 x the forward's 4 d)"}
+
+
+def run_reference_backward(args, w):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    cal = cpu_baseline_backward(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    times, r = [], None
+    for s in range(args.warmup + args.steps):
+        r = cpu_baseline_backward(w, n_slices=cal["n_slices"])
+        if s >= args.warmup:
+            times.append(r["seconds"])
+    t = sum(times) / len(times)
+    value = r["value"] * r["seconds"] / t
+    line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _bwd_config(w, wl.backward_flops(w)),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_backward(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import transformer_self_attention_gb300 as tsa
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    dOc = wl.make_grad_output(w)
+    Q, K, V, dO = (t.to(dev) for t in (Qc, Kc, Vc, dOc))
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
+    O, LSE = plan(Q, K, V)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        plan.backward(Q, K, V, O, LSE, dO, dQ, dK, dV, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during warm-up: {code}")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step()
+        ends[s].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    mean_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    if world > 1:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    st, code = plan.poll_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error during the timed steps: {code}")
+    useful = wl.backward_flops(w)
+    value = world * useful / (mean_ms * 1e-3) / 1e12
+    pk, pk_src = peaks()
+
+    # end to end through the C ABI: Q, K, V, O, LSE and dO from pinned host memory, the
+    # backward, dQ, dK and dV back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        hin = [t.pin_memory() for t in (Qc, Kc, Vc, O.cpu(), LSE.cpu(), dOc)]
+        din = [torch.empty_like(t, device=dev) for t in hin]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dQ, dK, dV)]
+        n_e2e = max(3, min(args.steps, 10))
+
+        def e2e_step():
+            for d_, h_ in zip(din, hin):
+                d_.copy_(h_, non_blocking=True)
+            plan.backward(*din[:5], din[5], dQ, dK, dV, stream=stream)
+            for h_, d_ in zip(hout, (dQ, dK, dV)):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    achieved = useful / (mean_ms * 1e-3) / 1e12
+    peak = float(pk["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": f"{pk_src} bf16_tflops (burst, cuBLAS)",
+                "kernel": "the whole backward step (bwd_prep + attn_bwd_dq + attn_bwd_dkdv)"}
+    line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(_bwd_config(w, useful), l2="flushed before every step (256 MiB write)",
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "roofline": roofline, "gpu_launches": 3 * args.steps, "wall_s_timed_region": wall}
+    if e2e:
+        line["e2e"] = e2e
+    if clk:
+        line["clocks"] = clk
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_backward(w)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 # ----------------------------------------------------------------------------- decode
 def _decode_oracle_inputs(w):
     key = ("decode", w.name)
@@ -547,9 +737,16 @@ def main():
                     help="E4M3 Q, K, V with per-tensor scales (prefill workloads; same metric)")
     ap.add_argument("--alibi", action="store_true",
                     help="add the ALiBi score bias with slopes 2^(-8(a+1)/H) (same workload, same metric)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dQ, dK, dV) of a prefill workload instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.backward:
+        if args.workload not in wl.BY_NAME or args.fp8 or args.alibi:
+            ap.error("--backward takes a bf16 prefill workload without --fp8 / --alibi")
+        w = wl.BY_NAME[args.workload]
+        return run_reference_backward(args, w) if args.impl == "reference" else run_ours_backward(args, w)
     if args.workload in wl.DECODE_BY_NAME:
         w = wl.DECODE_BY_NAME[args.workload]
         return run_reference_decode(args, w) if args.impl == "reference" else run_ours_decode(args, w)

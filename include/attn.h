@@ -176,6 +176,16 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
                                int* n_items, int* n_first);
 
 /*
+ * attn_kv_schedule_host -- the key-tile schedule of the backward pass (host only).
+ * One item of ATTN_WORK_INTS ints per key tile: [kv_tile, q_begin, q_end,
+ * full_begin, full_end, 0, 0, 0]: the query tiles [q_begin, q_end) hold every row
+ * that may see a key of the tile, and in [full_begin, full_end) every (row, key)
+ * pair is allowed.  Longest first.  items may be NULL with cap = 0 to query the count.
+ * Errors: ATTN_ERR_INVALID_ARG; ATTN_ERR_UNSUPPORTED for LOCAL_GLOBAL.
+ */
+attn_status attn_kv_schedule_host(int S, attn_mask_kind kind, int window, int* items, int cap, int* n_items);
+
+/*
  * attn_poll_device_error -- synchronise the device, read the handle's device
  * error word into *code (0 = none, otherwise a bit set of the role whose
  * bounded wait ran out), clear it, and return ATTN_ERR_DEVICE_TIMEOUT if it
@@ -209,6 +219,29 @@ attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
  * Must not be called while a forward of this handle is in flight.
  */
 attn_status attn_set_alibi(attn_handle h, const float* slopes);
+
+/*
+ * attn_backward -- the gradients of the forward pass of this handle with respect to
+ * Q, K and V, for the output gradient dO:
+ *     P_ij = exp(s_ij - LSE_i), D_i = dO_i . O_i, dS_ij = P_ij (dO_i . v_j - D_i),
+ *     dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i,
+ * with dK and dV summed over the query heads of each kv head (g(a) as in the forward).
+ * The pages give no backward formulas; they describe the tiled forward as exact and used
+ * to train models ("Transformer 演进与变体" (ai.icyfenix.cn), section Flash Attention),
+ * so this is the derivative of the definition.  P is recomputed tile by tile from the
+ * saved LSE; nothing of size S x S is stored.
+ *   Q, K, V, O, dO : bf16 device tensors in the forward layouts; O and LSE are the
+ *                    outputs of attn_forward for these Q, K, V.
+ *   LSE            : float32 [B, Hq, S] device array (required).
+ *   dQ, dK, dV     : bf16 outputs with the shapes of Q, K, V (overwritten).
+ * Enqueued on `stream`; the first call allocates the handle's backward scratch
+ * (2 * B*Hq*ceil(S/128)*128 floats and the key-tile schedule).
+ * Errors: ATTN_ERR_INVALID_ARG (NULL or misaligned pointer); ATTN_ERR_UNSUPPORTED
+ * (dtype other than ATTN_BF16, LOCAL_GLOBAL, or with the ALiBi bias set);
+ * ATTN_ERR_OOM; ATTN_ERR_CUDA.
+ */
+attn_status attn_backward(attn_handle h, const void* Q, const void* K, const void* V, const void* O,
+                          const float* LSE, const void* dO, void* dQ, void* dK, void* dV, void* stream);
 
 /*
  * attn_set_fp8_descale -- the per-tensor factors of an ATTN_FP8_E4M3 handle: the

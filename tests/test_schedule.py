@@ -169,3 +169,33 @@ def test_duplicate_globals_are_removed():
     a, _ = tsa.attn_schedule_host(1, 1, 1, 300, tsa.MASK_LOCAL_GLOBAL, 5, [7, 7, 250, 7])
     b, _ = tsa.attn_schedule_host(1, 1, 1, 300, tsa.MASK_LOCAL_GLOBAL, 5, [7, 250])
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------ backward key-tile schedule
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 300, 515])
+@pytest.mark.parametrize("kind,w", [(tsa.MASK_FULL, 0), (tsa.MASK_CAUSAL, 0), (tsa.MASK_SLIDING, 3),
+                                    (tsa.MASK_SLIDING, 130), (tsa.MASK_CAUSAL_SLIDING, 0),
+                                    (tsa.MASK_CAUSAL_SLIDING, 200)])
+def test_kv_schedule_matches_brute_force(kind, S, w):
+    """Every key tile once; its query-tile range holds exactly the tiles with an allowed pair, and
+    its FULL range exactly the tiles the oracle's enumeration calls FULL (transposed classes)."""
+    items = tsa.attn_kv_schedule_host(S, kind, w)
+    nk = (S + T - 1) // T
+    assert sorted(int(x) for x in items[:, 0]) == list(range(nk))
+    classes = oracle.tile_classes(kind, S, w, [])  # [q tile, k tile]
+    for kt, qb, qe, fb, fe, *_ in (tuple(int(x) for x in it) for it in items):
+        for qt in range(classes.shape[0]):
+            c = classes[qt, kt]
+            if qb <= qt < qe:
+                assert c == (1 if fb <= qt < fe else 2), (kt, qt, c)
+            else:
+                assert c == 0, (kt, qt)
+    lengths = items[:, 2] - items[:, 1]
+    assert np.all(np.diff(lengths) <= 0)
+
+
+def test_kv_schedule_rejects_local_global():
+    with pytest.raises(tsa.AttnError) as e:
+        tsa.attn_kv_schedule_host(300, tsa.MASK_LOCAL_GLOBAL, 5)
+    assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED

@@ -29,7 +29,8 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
-            "attn_decode_set_alibi", "attn_set_fp8_descale")
+            "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
+            "attn_backward")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -67,6 +68,10 @@ def _load():
     lib.attn_decode_set_alibi.restype = I
     lib.attn_set_fp8_descale.argtypes = [P, F, F, F]
     lib.attn_set_fp8_descale.restype = I
+    lib.attn_kv_schedule_host.argtypes = [I, I, I, P, I, ctypes.POINTER(I)]
+    lib.attn_kv_schedule_host.restype = I
+    lib.attn_backward.argtypes = [P] * 11
+    lib.attn_backward.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -180,6 +185,20 @@ def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):
     return items[: n.value], n_first.value
 
 
+def attn_kv_schedule_host(S, kind, window=0):
+    """Backward key-tile schedule (host only): int32 [n, 8].  Raises AttnError."""
+    n = ctypes.c_int(0)
+    st = _lib.attn_kv_schedule_host(int(S), int(kind), int(window), None, 0, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_kv_schedule_host")
+    items = np.zeros((max(n.value, 1), WORK_INTS), dtype=np.int32)
+    st = _lib.attn_kv_schedule_host(int(S), int(kind), int(window), items.ctypes.data_as(ctypes.c_void_p), n.value,
+                                    ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_kv_schedule_host")
+    return items[: n.value]
+
+
 # ---------------------------------------------------------------- decode (key/value cache)
 
 def attn_decode_create(B, Hq, Hkv, S_q, S_cap, d_k, scale, kind, window=0) -> int:
@@ -279,7 +298,7 @@ class DecodeAttention:
                 raise ValueError("one slope per query head")
             st = _lib.attn_decode_set_alibi(self.handle, ctypes.cast(_float_array(slopes), ctypes.c_void_p))
         if st != ATTN_OK:
-            raise AttnError(st, "attn_decode_set_alibi", "attn_set_fp8_descale")
+            raise AttnError(st, "attn_decode_set_alibi")
 
     def set_grid_limit(self, max_ctas: int):
         """Test hook: at most max_ctas CTAs per launch (long shares on small problems)."""
@@ -345,6 +364,27 @@ class Attention:
         st = attn_set_watchdog(self.handle, limit_ns, withhold)
         if st != ATTN_OK:
             raise AttnError(st, "attn_set_watchdog")
+
+    def backward(self, Q, K, V, O, LSE, dO, dQ=None, dK=None, dV=None, stream=None):
+        """Gradients (dQ, dK, dV) of this plan's forward for the output gradient dO (bf16 tensors;
+        O and LSE from the forward call)."""
+        import torch
+        if dQ is None:
+            dQ = torch.empty_like(Q)
+        if dK is None:
+            dK = torch.empty_like(K)
+        if dV is None:
+            dV = torch.empty_like(V)
+        for name, t in (("O", O), ("dO", dO), ("dQ", dQ)):
+            if t.shape != Q.shape or t.dtype != Q.dtype or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous tensor like Q")
+        if stream is None:
+            stream = torch.cuda.current_stream(Q.device)
+        st = _lib.attn_backward(self.handle, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), LSE.data_ptr(),
+                                dO.data_ptr(), dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), stream.cuda_stream)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_backward")
+        return dQ, dK, dV
 
     def set_fp8_descale(self, descale_q: float, descale_k: float, descale_v: float):
         """Per-tensor factors of E4M3 inputs (real value = factor x stored value)."""

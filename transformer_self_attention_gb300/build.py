@@ -17,7 +17,7 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["attn_api.cpp", "schedule.cpp", "attn_fwd_tc.cu", "attn_fwd_f32.cu", "attn_noalloc.cu", "decode_api.cpp",
-           "attn_decode.cu"]
+           "attn_decode.cu", "attn_bwd.cu"]
 HEADERS = [os.path.join(INCLUDE, "attn.h")] + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
 
 

@@ -34,6 +34,13 @@ struct attn_plan {
     void* d_vg = nullptr;
     float* d_part = nullptr;  // partial results of the chunked global-row pass
     float* d_alibi = nullptr;  // ALiBi slopes [Hq] (attn_set_alibi), or null
+    // backward scratch (first attn_backward call)
+    float* d_lse2 = nullptr;   // [B*Hq, S_pad]
+    float* d_dvec = nullptr;   // [B*Hq, S_pad]
+    int4* d_kvwork = nullptr;  // key-tile items
+    int n_kv_items = 0;
+    const void* last_bwd[7] = {};
+    attn::BwdParams bp{};
     // tensor maps of the last pointers seen (re-encoded when they change)
     const void* last_q = nullptr;
     const void* last_k = nullptr;
@@ -127,7 +134,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 void free_plan(attn_plan* h) {
     if (!h) return;
     void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part,
-                    h->d_alibi};
+                    h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork};
     for (void* b : bufs)
         if (b) cudaFree(b);
     delete h;
@@ -334,6 +341,21 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
     return ATTN_OK;
 }
 
+attn_status attn_kv_schedule_host(int S, attn_mask_kind kind, int window, int* items, int cap, int* n_items) {
+    if (!n_items || cap < 0 || (cap > 0 && !items) || S < 1 || S > (1 << 20)) return ATTN_ERR_INVALID_ARG;
+    if ((int)kind < ATTN_MASK_FULL || (int)kind > ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_INVALID_ARG;
+    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING;
+    if (windowed && window < 0) return ATTN_ERR_INVALID_ARG;
+    std::vector<int> v;
+    attn_status st = attn::build_kv_schedule(S, kind, windowed ? window : 0, &v);
+    if (st != ATTN_OK) return st;
+    *n_items = (int)(v.size() / ATTN_WORK_INTS);
+    if (cap == 0) return ATTN_OK;
+    if (cap < *n_items) return ATTN_ERR_INVALID_ARG;
+    std::memcpy(items, v.data(), v.size() * sizeof(int));
+    return ATTN_OK;
+}
+
 attn_status attn_poll_device_error(attn_handle h, int* code) {
     if (!h || !code) return ATTN_ERR_INVALID_ARG;
     *code = 0;
@@ -367,6 +389,65 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     h->tp.alibi = h->d_alibi;
+    return ATTN_OK;
+}
+
+attn_status attn_backward(attn_handle h, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                          const void* dO, void* dQ, void* dK, void* dV, void* stream_ptr) {
+    if (!h || !Q || !K || !V || !O || !LSE || !dO || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+    const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(LSE) & 3u) return ATTN_ERR_INVALID_ARG;
+    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->d_alibi) return ATTN_ERR_UNSUPPORTED;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    const int nq = (h->S + ATTN_TILE - 1) / ATTN_TILE;
+    const int S_pad = nq * ATTN_TILE;
+    attn::BwdParams& p = h->bp;
+    cudaError_t e = cudaSuccess;
+    if (!h->d_lse2) {
+        const size_t n = (size_t)h->B * h->Hq * S_pad;
+        std::vector<int> items;
+        attn_status st = attn::build_kv_schedule(h->S, h->kind, h->window, &items);
+        if (st != ATTN_OK) return st;
+        h->n_kv_items = (int)(items.size() / ATTN_WORK_INTS);
+        if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_lse2), n * sizeof(float))) != cudaSuccess ||
+            (e = cudaMalloc(reinterpret_cast<void**>(&h->d_dvec), n * sizeof(float))) != cudaSuccess ||
+            (e = upload(reinterpret_cast<int**>(&h->d_kvwork), items.data(), items.size())) != cudaSuccess)
+            return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
+        p.S = h->S; p.S_pad = S_pad; p.Hq = h->Hq; p.Hkv = h->Hkv; p.group = h->Hq / h->Hkv;
+        p.kind = h->kind; p.window = h->window;
+        p.scale = h->scale;
+        p.scale_log2 = (float)((double)h->scale * 1.4426950408889634);
+        p.lse2 = h->d_lse2; p.dvec = h->d_dvec;
+        p.err = h->d_err;
+        p.watchdog_ns = h->tp.watchdog_ns;
+    }
+    // tensor maps (re-encoded when a pointer changes)
+    const long BHq = (long)h->B * h->Hq, BHkv = (long)h->B * h->Hkv;
+    struct M { CUtensorMap* map; const void* ptr; long heads; } maps[] = {
+        {&p.tm_q, Q, BHq}, {&p.tm_k, K, BHkv}, {&p.tm_v, V, BHkv}, {&p.tm_do, dO, BHq},
+        {&p.tm_dq, dQ, BHq}, {&p.tm_dk, dK, BHkv}, {&p.tm_dv, dV, BHkv}};
+    for (int m = 0; m < 7; ++m) {
+        if (maps[m].ptr != h->last_bwd[m]) {
+            if (!encode_map(maps[m].map, maps[m].ptr, h->d, h->S, maps[m].heads, kTileRows)) return ATTN_ERR_CUDA;
+            h->last_bwd[m] = maps[m].ptr;
+        }
+    }
+    attn::BwdPrepParams pp{};
+    pp.o = static_cast<const uint16_t*>(O); pp.dout = static_cast<const uint16_t*>(dO); pp.lse = LSE;
+    pp.lse2 = h->d_lse2; pp.dvec = h->d_dvec;
+    pp.BHq = (int)BHq; pp.S = h->S; pp.S_pad = S_pad; pp.d = h->d;
+    if ((e = attn::launch_bwd_prep(pp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    p.work = h->d_work;  // the forward's first-launch items: one per (batch x head, query tile)
+    if ((e = attn::launch_bwd_dq(p, h->d, h->sched.n_main, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    p.work = h->d_kvwork;
+    p.n_items = h->n_kv_items;
+    if ((e = attn::launch_bwd_dkdv(p, h->d, (int)BHkv * h->n_kv_items, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (h->debug) {
+        int code = 0;
+        return attn_poll_device_error(h, &code);
+    }
     return ATTN_OK;
 }
 

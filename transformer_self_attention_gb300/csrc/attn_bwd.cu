@@ -1,0 +1,604 @@
+// Backward pass of the attention for sm_103a (bf16 in and out, fp32 accumulation).
+//
+// The gradients of the forward definition (the plain derivative: the pages describe
+// the tiled forward as exact and used for training, "Transformer 演进与变体"
+// (ai.icyfenix.cn), section Flash Attention, and give no backward formulas):
+//
+//   P_ij = exp(s_ij - LSE_i),  D_i = dO_i . O_i,  dS_ij = P_ij (dO_i . v_j - D_i)
+//   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,  dV_j = sum_i P_ij dO_i
+//
+// (dK and dV summed over the query heads of each kv head).  P is recomputed from the
+// saved LSE, tile by tile, as the forward computed it; nothing of size S x S is stored.
+//
+//   bwd_prep        : D_i and LSE_i log2(e) into padded per-head vectors (one warp per row).
+//   attn_bwd_dq     : one CTA per forward work item (128 query rows of one head).  For
+//                     each allowed key tile: S = Q K^T and dP = dO V^T (tcgen05, fp32 in
+//                     tensor memory), the four compute warps form dS = P (dP - D) in bf16
+//                     over dP, and dQ += dS K reads dS from tensor memory.
+//   attn_bwd_dkdv   : one CTA per key tile of one kv head, over the query tiles of every
+//                     query head of the group that see it.  S^T = K Q^T and dP^T = V dO^T;
+//                     the compute warps (one thread per key) form P^T and dS^T in bf16 over
+//                     them; dV += P^T dO and dK += dS^T Q accumulate in tensor memory.
+//
+// Both kernels: warp 4 loads with TMA, warp 5 issues the MMAs, warps 0-3 compute.  Every
+// mbarrier wait is bounded; the compute warps run the same sequence of named barriers
+// whatever happens (a wait that ran out returns at once from then on), and the producer
+// and MMA threads drain their copies and products before the CTA exits.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm103_ptx.h"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BT = 128;        // rows / keys per tile
+constexpr int NTHREADS = 192;
+constexpr int WARP_PRODUCER = 4;
+constexpr int WARP_MMA = 5;
+constexpr float LOG2E = 1.4426950408889634f;
+enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_COMPUTE = 4 };
+
+struct Watch {
+    volatile int* abort;
+    int* err;
+    long long ns;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watch& w, int role) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 127u) == 0) {
+            if (*w.abort) return false;
+            if ((long long)(globaltimer() - t0) > w.ns) {
+                *w.abort = 1;
+                atomicOr(w.err, role);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Watch& w) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if ((long long)(globaltimer() - t0) > w.ns) return;
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (both addresses 16-byte aligned,
+// bytes a multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Allowed key interval [lo, hi] of query row i (interval kinds), and the query interval of key j.
+__device__ __forceinline__ void row_band(int kind, int window, long S, long i, long* lo, long* hi) {
+    *lo = 0;
+    *hi = S - 1;
+    if (kind == ATTN_MASK_CAUSAL) *hi = i;
+    else if (kind == ATTN_MASK_CAUSAL_SLIDING) { *lo = i - window; *hi = i; }
+    else if (kind == ATTN_MASK_SLIDING) { *lo = i - window; *hi = i + window; }
+    if (*hi > S - 1) *hi = S - 1;
+}
+__device__ __forceinline__ void key_band(int kind, int window, long S, long j, long* lo, long* hi) {
+    *lo = 0;
+    *hi = S - 1;
+    if (kind == ATTN_MASK_CAUSAL) *lo = j;
+    else if (kind == ATTN_MASK_CAUSAL_SLIDING) { *lo = j; *hi = j + window; }
+    else if (kind == ATTN_MASK_SLIDING) { *lo = j - window; *hi = j + window; }
+    if (*hi > S - 1) *hi = S - 1;
+}
+
+// ------------------------------------------------------------------ pre-pass
+__global__ void bwd_prep_kernel(BwdPrepParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long row = (long)blockIdx.x * 8 + warp;  // over B*Hq*S_pad
+    if (row >= (long)p.BHq * p.S_pad) return;
+    const long bh = row / p.S_pad, i = row - bh * p.S_pad;
+    if (i >= p.S) {
+        if (lane == 0) {
+            p.lse2[row] = INFINITY;  // padding rows: P = 0
+            p.dvec[row] = 0.f;
+        }
+        return;
+    }
+    const long src = (bh * p.S + i) * p.d;
+    float acc = 0.f;
+    for (int c = lane * 8; c < p.d; c += 32 * 8) {
+        const uint4 o4 = *reinterpret_cast<const uint4*>(p.o + src + c);
+        const uint4 g4 = *reinterpret_cast<const uint4*>(p.dout + src + c);
+        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
+            acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+        p.dvec[row] = acc;
+        p.lse2[row] = p.lse[bh * p.S + i] * LOG2E;
+    }
+}
+
+// O row -> bf16 -> 128B-swizzled staging (two 64-column blocks per 128 columns) for a TMA store:
+// thread r writes row r of the tile from tensor-memory columns [col0, col0 + D) times f.
+template <int D>
+__device__ __forceinline__ void stage_row_bf16(uint8_t* stage, uint32_t t_lane, uint32_t col0, int r, float f) {
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + col0 + c * 32, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
+        const int sub = c >> 1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int chunk = (c & 1) * 4 + q;
+            uint4* dst = reinterpret_cast<uint4*>(stage + sub * (BT * 128) + r * 128 + ((chunk ^ (r & 7)) << 4));
+            *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+    }
+}
+
+// Masked score of in-tile column c (allowed columns [a0, a1]); -inf elsewhere.
+template <bool MASKED>
+__device__ __forceinline__ float sc(uint32_t raw, int c, int a0, int a1) {
+    if (!MASKED) return __uint_as_float(raw);
+    return (c >= a0 && c <= a1) ? __uint_as_float(raw) : -INFINITY;
+}
+
+// ------------------------------------------------------------------ dQ kernel
+template <int D>
+struct DqCfg {
+    static constexpr int TB = BT * D * 2;  // one Q / dO / K / V tile
+    static constexpr int SUB = BT * 128;   // one 64-column swizzled block
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_DO = OFF_Q + TB;
+    static constexpr int OFF_K = OFF_DO + TB;      // two stages
+    static constexpr int OFF_V = OFF_K + 2 * TB;   // two stages
+    static constexpr int OFF_CTL = OFF_V + 2 * TB;
+    static constexpr int SMEM_ALLOC = OFF_CTL + 1024 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DQ = 256;
+};
+
+enum DqBar { Q_LOAD = 0, Q_KFULL, Q_KEMPTY = Q_KFULL + 2, Q_VFULL = Q_KEMPTY + 2, Q_VEMPTY = Q_VFULL + 2,
+             Q_SFULL = Q_VEMPTY + 2, Q_DSFULL, Q_DQ, Q_NBAR };
+
+struct BwdShared {
+    uint64_t bar[16];
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using C = DqCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    BwdShared* sh = reinterpret_cast<BwdShared*>(smem + C::OFF_CTL);
+    auto bar = [&](int b) { return smem_u32(&sh->bar[b]); };
+    const Watch wd{&sh->abort, p.err, p.watchdog_ns};
+    const uint32_t s_q = smem_u32(smem + C::OFF_Q), s_do = smem_u32(smem + C::OFF_DO);
+    const uint32_t s_k = smem_u32(smem + C::OFF_K), s_v = smem_u32(smem + C::OFF_V);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int4 w0 = p.work[2 * blockIdx.x], w1 = p.work[2 * blockIdx.x + 1];
+    const int bh = w0.x, q_tile = w0.y, kv_begin = w0.z, kv_end = w0.w;
+    const int full_begin = w1.x, full_end = w1.y;
+    const int n_iter = kv_end - kv_begin;
+    const int b = bh / p.Hq, a = bh - b * p.Hq;
+    const int bkv = b * p.Hkv + a / p.group;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < Q_NBAR; ++i) mbar_init(bar(i), i == Q_DSFULL ? 128u : 1u);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == WARP_PRODUCER && lane == 0) {
+        prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_do); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == WARP_PRODUCER) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(Q_LOAD), 2 * C::TB);
+            for (int s = 0; s < D / 64; ++s) {
+                tma_load_3d(s_q + s * C::SUB, &p.tm_q, bar(Q_LOAD), s * 64, q_tile * BT, bh);
+                tma_load_3d(s_do + s * C::SUB, &p.tm_do, bar(Q_LOAD), s * 64, q_tile * BT, bh);
+            }
+            int k_loaded = 0, v_loaded = 0;
+            bool ok = true;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int st = it & 1, row = (kv_begin + it) * BT;
+                if (it >= 2 && !(ok = wait_bounded(bar(Q_KEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
+                mbar_arrive_expect_tx(bar(Q_KFULL + st), C::TB);
+                for (int s = 0; s < D / 64; ++s)
+                    tma_load_3d(s_k + st * C::TB + s * C::SUB, &p.tm_k, bar(Q_KFULL + st), s * 64, row, bkv);
+                k_loaded = it + 1;
+                if (it >= 2 && !(ok = wait_bounded(bar(Q_VEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
+                mbar_arrive_expect_tx(bar(Q_VFULL + st), C::TB);
+                for (int s = 0; s < D / 64; ++s)
+                    tma_load_3d(s_v + st * C::TB + s * C::SUB, &p.tm_v, bar(Q_VFULL + st), s * 64, row, bkv);
+                v_loaded = it + 1;
+            }
+            if (sh->abort) {
+                drain_wait(bar(Q_LOAD), 0, wd);
+                for (int n = max(0, k_loaded - 2); n < k_loaded; ++n) drain_wait(bar(Q_KFULL + (n & 1)), (n >> 1) & 1, wd);
+                for (int n = max(0, v_loaded - 2); n < v_loaded; ++n) drain_wait(bar(Q_VFULL + (n & 1)), (n >> 1) & 1, wd);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);  // [128 x 128] = A[128 x d] . B[128 x d]^T
+            constexpr uint32_t idesc_q = idesc_bf16_f32(BT, D, true);    // dQ += dS (tensor memory) . K (MN-major)
+            const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP, t_dq = tmem + C::TMEM_DQ;
+            bool ok = wait_bounded(bar(Q_LOAD), 0, wd, ERR_MMA);
+            int last_bar = -1, last_par = 0;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int st = it & 1;
+                if (!(ok = wait_bounded(bar(Q_KFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
+                if (!(ok = wait_bounded(bar(Q_VFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+                const uint32_t sk = s_k + st * C::TB, sv = s_v + st * C::TB;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024), idesc_s, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_dp, sdesc_sw128(s_do + off, 16, 1024), sdesc_sw128(sv + off, 16, 1024), idesc_s, k > 0);
+                }
+                mma_commit(bar(Q_SFULL));
+                mma_commit(bar(Q_VEMPTY + st));
+                last_bar = Q_VEMPTY + st; last_par = (it >> 1) & 1;
+                if (!(ok = wait_bounded(bar(Q_DSFULL), it & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BT / 16; ++k)
+                    mma_ts(t_dq, t_dp + k * 8, sdesc_sw128(sk + k * 16 * 128, C::SUB, 1024), idesc_q,
+                           (it > 0 || k > 0) ? 1u : 0u);
+                mma_commit(bar(Q_KEMPTY + st));
+                last_bar = Q_KEMPTY + st; last_par = (it >> 1) & 1;
+            }
+            if (ok) mma_commit(bar(Q_DQ));
+            if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, wd);
+        }
+    } else {
+        // compute warps: one thread per query row
+        const int r = threadIdx.x;
+        const long i = (long)q_tile * BT + r;
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_s = t_lane + C::TMEM_S, t_dp = t_lane + C::TMEM_DP;
+        const float lse2 = p.lse2[(size_t)bh * p.S_pad + i];
+        const float Di = p.dvec[(size_t)bh * p.S_pad + i];
+        const float sl2 = p.scale_log2;
+        long lo, hi;
+        row_band(p.kind, p.window, p.S, i, &lo, &hi);
+        for (int it = 0; it < n_iter; ++it) {
+            wait_bounded(bar(Q_SFULL), it & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            const int t = kv_begin + it;
+            const bool partial = t < full_begin || t >= full_end;
+            const long c0 = (long)t * BT;
+            const int a0 = (int)max(-1L, min((long)BT, lo - c0)), a1 = (int)max(-1L, min((long)BT, hi - c0));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t s0[32], s1[32], d0[32], d1[32], pk[32];
+                tmem_ld32(t_s + h * 64, s0);
+                tmem_ld32(t_s + h * 64 + 32, s1);
+                tmem_ld32(t_dp + h * 64, d0);
+                tmem_ld32(t_dp + h * 64 + 32, d1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float ds[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = h * 64 + (u >> 1) * 32 + 2 * e + (u & 1);
+                        const uint32_t sr = (u >> 1) ? s1[2 * e + (u & 1)] : s0[2 * e + (u & 1)];
+                        const uint32_t dr = (u >> 1) ? d1[2 * e + (u & 1)] : d0[2 * e + (u & 1)];
+                        const float s = partial ? sc<true>(sr, c, a0, a1) : sc<false>(sr, c, a0, a1);
+                        const float pv = ex2(fmaf(s, sl2, -lse2));
+                        ds[u] = pv * (__uint_as_float(dr) - Di);
+                    }
+                    pk[e] = pack_bf16x2(ds[0], ds[1]);
+                    pk[16 + e] = pack_bf16x2(ds[2], ds[3]);
+                }
+                tmem_st32(t_dp + h * 32, pk);  // dS (bf16 pairs) over the dP columns already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(Q_DSFULL));
+        }
+        // epilogue: dQ * scale -> bf16 -> swizzled staging in the Q buffer -> TMA store
+        wait_bounded(bar(Q_DQ), 0, wd, ERR_COMPUTE);
+        tc_fence_after();
+        stage_row_bf16<D>(smem + C::OFF_Q, t_lane, C::TMEM_DQ, r, p.scale);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0 && !sh->abort) {
+            for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_dq, s_q + s * C::SUB, s * 64, q_tile * BT, bh);
+            tma_store_commit_and_wait_read();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ dK / dV kernel
+template <int D>
+struct KvCfg {
+    static constexpr int TB = BT * D * 2;
+    static constexpr int SUB = BT * 128;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TB;
+    static constexpr int OFF_Q = OFF_V + TB;        // two stages
+    static constexpr int OFF_DO = OFF_Q + 2 * TB;   // two stages
+    static constexpr int OFF_VEC = OFF_DO + 2 * TB; // two stages of 128 LSE (log2) + 128 D
+    static constexpr int OFF_CTL = OFF_VEC + 2 * 1024;
+    static constexpr int SMEM_ALLOC = OFF_CTL + 1024 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DV = 256, TMEM_DK = 256 + D;
+};
+
+enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMPTY + 2, KV_PFULL, KV_DONE, KV_NBAR };
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using C = KvCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    BwdShared* sh = reinterpret_cast<BwdShared*>(smem + C::OFF_CTL);
+    auto bar = [&](int b) { return smem_u32(&sh->bar[b]); };
+    const Watch wd{&sh->abort, p.err, p.watchdog_ns};
+    const uint32_t s_k = smem_u32(smem + C::OFF_K), s_v = smem_u32(smem + C::OFF_V);
+    const uint32_t s_q = smem_u32(smem + C::OFF_Q), s_do = smem_u32(smem + C::OFF_DO);
+    const uint32_t s_vec = smem_u32(smem + C::OFF_VEC);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int bkv = blockIdx.x / p.n_items, item = blockIdx.x - bkv * p.n_items;
+    const int4 w0 = p.work[2 * item], w1 = p.work[2 * item + 1];
+    const int kv_tile = w0.x, q_begin = w0.y, q_end = w0.z, full_begin = w0.w, full_end = w1.x;
+    const int n_q = q_end - q_begin;
+    const int n_iter = p.group * n_q;  // query heads of the group x query tiles
+    const int b = bkv / p.Hkv, g = bkv - b * p.Hkv;
+    auto iter_head = [&](int it) { return b * p.Hq + g * p.group + it / n_q; };
+    auto iter_qtile = [&](int it) { return q_begin + it % n_q; };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < KV_NBAR; ++i) mbar_init(bar(i), i == KV_PFULL ? 128u : 1u);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(&sh->tmem_base), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == WARP_PRODUCER && lane == 0) {
+        prefetch_tmap(&p.tm_q); prefetch_tmap(&p.tm_do); prefetch_tmap(&p.tm_k); prefetch_tmap(&p.tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == WARP_PRODUCER) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar(KV_LOAD), 2 * C::TB);
+            for (int s = 0; s < D / 64; ++s) {
+                tma_load_3d(s_k + s * C::SUB, &p.tm_k, bar(KV_LOAD), s * 64, kv_tile * BT, bkv);
+                tma_load_3d(s_v + s * C::SUB, &p.tm_v, bar(KV_LOAD), s * 64, kv_tile * BT, bkv);
+            }
+            int loaded = 0;
+            bool ok = true;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int st = it & 1, bh = iter_head(it), qt = iter_qtile(it);
+                if (it >= 2 && !(ok = wait_bounded(bar(KV_QEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
+                mbar_arrive_expect_tx(bar(KV_QFULL + st), 2 * C::TB + 1024);
+                for (int s = 0; s < D / 64; ++s) {
+                    tma_load_3d(s_q + st * C::TB + s * C::SUB, &p.tm_q, bar(KV_QFULL + st), s * 64, qt * BT, bh);
+                    tma_load_3d(s_do + st * C::TB + s * C::SUB, &p.tm_do, bar(KV_QFULL + st), s * 64, qt * BT, bh);
+                }
+                const size_t v0 = (size_t)bh * p.S_pad + (size_t)qt * BT;
+                bulk_load(s_vec + st * 1024, p.lse2 + v0, 512, bar(KV_QFULL + st));
+                bulk_load(s_vec + st * 1024 + 512, p.dvec + v0, 512, bar(KV_QFULL + st));
+                loaded = it + 1;
+            }
+            if (sh->abort) {
+                drain_wait(bar(KV_LOAD), 0, wd);
+                for (int n = max(0, loaded - 2); n < loaded; ++n) drain_wait(bar(KV_QFULL + (n & 1)), (n >> 1) & 1, wd);
+            }
+        }
+    } else if (warp == WARP_MMA) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
+            constexpr uint32_t idesc_kv = idesc_bf16_f32(BT, D, true);  // dV, dK += (tensor memory) . (MN-major)
+            const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP;
+            const uint32_t t_dv = tmem + C::TMEM_DV, t_dk = tmem + C::TMEM_DK;
+            bool ok = wait_bounded(bar(KV_LOAD), 0, wd, ERR_MMA);
+            int last_bar = -1, last_par = 0;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int st = it & 1;
+                if (!(ok = wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+                const uint32_t sq = s_q + st * C::TB, sdo = s_do + st * C::TB;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_s, sdesc_sw128(s_k + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idesc_s, k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_dp, sdesc_sw128(s_v + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), idesc_s, k > 0);
+                }
+                mma_commit(bar(KV_SFULL));
+                last_bar = KV_SFULL; last_par = it & 1;
+                if (!(ok = wait_bounded(bar(KV_PFULL), it & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BT / 16; ++k)
+                    mma_ts(t_dv, t_s + k * 8, sdesc_sw128(sdo + k * 16 * 128, C::SUB, 1024), idesc_kv,
+                           (it > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+                for (int k = 0; k < BT / 16; ++k)
+                    mma_ts(t_dk, t_dp + k * 8, sdesc_sw128(sq + k * 16 * 128, C::SUB, 1024), idesc_kv,
+                           (it > 0 || k > 0) ? 1u : 0u);
+                mma_commit(bar(KV_QEMPTY + st));
+                last_bar = KV_QEMPTY + st; last_par = (it >> 1) & 1;
+            }
+            if (ok) mma_commit(bar(KV_DONE));
+            if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, wd);
+        }
+    } else {
+        // compute warps: one thread per key (tensor-memory lane), 128 query columns per tile
+        const int t = threadIdx.x;
+        const long j = (long)kv_tile * BT + t;
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_s = t_lane + C::TMEM_S, t_dp = t_lane + C::TMEM_DP;
+        const float sl2 = p.scale_log2;
+        long ilo, ihi;
+        key_band(p.kind, p.window, p.S, j, &ilo, &ihi);
+        if (j >= p.S) { ilo = 1; ihi = 0; }  // a padding key sees no row
+        for (int it = 0; it < n_iter; ++it) {
+            const int st = it & 1, qt = iter_qtile(it);
+            wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
+            wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            const bool partial = qt < full_begin || qt >= full_end;
+            const long r0 = (long)qt * BT;
+            const int a0 = (int)max(-1L, min((long)BT, ilo - r0)), a1 = (int)max(-1L, min((long)BT, ihi - r0));
+            const float* vlse = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
+            const float* vd = vlse + 128;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t s0[32], s1[32], d0[32], d1[32], pp[32], pd[32];
+                tmem_ld32(t_s + h * 64, s0);
+                tmem_ld32(t_s + h * 64 + 32, s1);
+                tmem_ld32(t_dp + h * 64, d0);
+                tmem_ld32(t_dp + h * 64 + 32, d1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pv[4], ds[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = h * 64 + (u >> 1) * 32 + 2 * e + (u & 1);  // query column
+                        const uint32_t sr = (u >> 1) ? s1[2 * e + (u & 1)] : s0[2 * e + (u & 1)];
+                        const uint32_t dr = (u >> 1) ? d1[2 * e + (u & 1)] : d0[2 * e + (u & 1)];
+                        const float s = partial ? sc<true>(sr, c, a0, a1) : sc<false>(sr, c, a0, a1);
+                        pv[u] = ex2(fmaf(s, sl2, -vlse[c]));
+                        ds[u] = pv[u] * (__uint_as_float(dr) - vd[c]);
+                    }
+                    pp[e] = pack_bf16x2(pv[0], pv[1]);
+                    pp[16 + e] = pack_bf16x2(pv[2], pv[3]);
+                    pd[e] = pack_bf16x2(ds[0], ds[1]);
+                    pd[16 + e] = pack_bf16x2(ds[2], ds[3]);
+                }
+                tmem_st32(t_s + h * 32, pp);   // P^T over the S^T columns already read
+                tmem_st32(t_dp + h * 32, pd);  // dS^T over the dP^T columns already read
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(KV_PFULL));
+        }
+        // epilogue: dV and scale * dK -> bf16 -> swizzled staging (the idle Q stages) -> TMA stores
+        wait_bounded(bar(KV_DONE), 0, wd, ERR_COMPUTE);
+        tc_fence_after();
+        stage_row_bf16<D>(smem + C::OFF_Q, t_lane, C::TMEM_DV, t, 1.f);
+        stage_row_bf16<D>(smem + C::OFF_DO, t_lane, C::TMEM_DK, t, p.scale);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (threadIdx.x == 0 && !sh->abort) {
+            for (int s = 0; s < D / 64; ++s) {
+                tma_store_3d(&p.tm_dv, s_q + s * C::SUB, s * 64, kv_tile * BT, bkv);
+                tma_store_3d(&p.tm_dk, s_do + s * C::SUB, s * 64, kv_tile * BT, bkv);
+            }
+            tma_store_commit_and_wait_read();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <class F>
+cudaError_t configure(F kernel, int smem) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
+    const long rows = (long)p.BHq * p.S_pad;
+    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream) {
+    if (n_items <= 0) return cudaSuccess;
+    static bool c64 = false, c128 = false;
+    cudaError_t e = cudaSuccess;
+    if (d == 128) {
+        if (!c128 && (e = configure(attn_bwd_dq_kernel<128>, DqCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
+        c128 = true;
+        attn_bwd_dq_kernel<128><<<n_items, NTHREADS, DqCfg<128>::SMEM_ALLOC, stream>>>(p);
+    } else if (d == 64) {
+        if (!c64 && (e = configure(attn_bwd_dq_kernel<64>, DqCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
+        c64 = true;
+        attn_bwd_dq_kernel<64><<<n_items, NTHREADS, DqCfg<64>::SMEM_ALLOC, stream>>>(p);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream) {
+    if (n_ctas <= 0) return cudaSuccess;
+    static bool c64 = false, c128 = false;
+    cudaError_t e = cudaSuccess;
+    if (d == 128) {
+        if (!c128 && (e = configure(attn_bwd_dkdv_kernel<128>, KvCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
+        c128 = true;
+        attn_bwd_dkdv_kernel<128><<<n_ctas, NTHREADS, KvCfg<128>::SMEM_ALLOC, stream>>>(p);
+    } else if (d == 64) {
+        if (!c64 && (e = configure(attn_bwd_dkdv_kernel<64>, KvCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
+        c64 = true;
+        attn_bwd_dkdv_kernel<64><<<n_ctas, NTHREADS, KvCfg<64>::SMEM_ALLOC, stream>>>(p);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -101,6 +101,32 @@ struct DecodeParams {
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);
 
+// Backward pass (attn_bwd.cu): a pre-pass (D = dO . O and LSE in log2 units, padded to
+// S_pad rows per head), the dQ kernel (one CTA per forward work item) and the dK/dV kernel
+// (one CTA per key tile and kv head).
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 inputs, box {64, 128, 1}
+    CUtensorMap tm_dq, tm_dk, tm_dv;      // bf16 outputs (TMA stores)
+    const int4* work;     // dQ: the forward items (2 int4 each); dK/dV: the key-tile items
+    int n_items;          // dK/dV: key-tile items per (batch, kv head)
+    int S, S_pad, Hq, Hkv, group, kind, window;
+    float scale_log2;     // scale * log2(e)
+    float scale;
+    const float* lse2;    // [B*Hq, S_pad]: LSE * log2(e); +inf past S
+    const float* dvec;    // [B*Hq, S_pad]: D = dO . O; 0 past S
+    int* err;
+    long long watchdog_ns;
+};
+struct BwdPrepParams {
+    const uint16_t* o; const uint16_t* dout;  // bf16 bits [B*Hq, S, d]
+    const float* lse;                          // [B*Hq, S] (natural log)
+    float* lse2; float* dvec;                  // [B*Hq, S_pad]
+    int BHq, S, S_pad, d;
+};
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream);
+
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
 cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);

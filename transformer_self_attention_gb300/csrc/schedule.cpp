@@ -161,6 +161,57 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
     return ATTN_OK;
 }
 
+attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* items) {
+    if (kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
+    const long w = window;
+    // rows i that see key j form [ilo(j), ihi(j)]; both ends are non-decreasing in j
+    auto ilo = [&](long j) -> long {
+        switch (kind) {
+        case ATTN_MASK_CAUSAL:
+        case ATTN_MASK_CAUSAL_SLIDING: return j;
+        case ATTN_MASK_SLIDING: return std::max(0L, j - w);
+        default: return 0;
+        }
+    };
+    auto ihi = [&](long j) -> long {
+        switch (kind) {
+        case ATTN_MASK_CAUSAL_SLIDING:
+        case ATTN_MASK_SLIDING: return std::min<long>(S - 1, j + w);
+        default: return S - 1;
+        }
+    };
+    const int nk = (S + T - 1) / T;
+    struct Item { int kt, qb, qe, fb, fe; };
+    std::vector<Item> v;
+    for (int kt = 0; kt < nk; ++kt) {
+        const long j0 = (long)kt * T, j1 = std::min<long>(S, j0 + T) - 1;
+        const int qb = (int)(ilo(j0) / T), qe = (int)(ihi(j1) / T) + 1;
+        const bool keys_full = j0 + T - 1 < S;
+        int fb = -1, fe = -1;
+        for (int qt = qb; qt < qe; ++qt) {
+            const long r0 = (long)qt * T;
+            const bool full = keys_full && r0 + T - 1 < S && r0 >= ilo(j1) && r0 + T - 1 <= ihi(j0);
+            if (full) {
+                if (fb < 0) { fb = qt; fe = qt + 1; }
+                else if (fe == qt) fe = qt + 1;
+                else return ATTN_ERR_UNSUPPORTED;  // cannot happen for interval masks
+            }
+        }
+        if (fb < 0) fb = fe = qb;
+        v.push_back({kt, qb, qe, fb, fe});
+    }
+    std::stable_sort(v.begin(), v.end(), [](const Item& x, const Item& y) {
+        if (x.qe - x.qb != y.qe - y.qb) return x.qe - x.qb > y.qe - y.qb;
+        return x.kt < y.kt;
+    });
+    items->clear();
+    for (const Item& it : v) {
+        const int a[ATTN_WORK_INTS] = {it.kt, it.qb, it.qe, it.fb, it.fe, 0, 0, 0};
+        items->insert(items->end(), a, a + ATTN_WORK_INTS);
+    }
+    return ATTN_OK;
+}
+
 void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi) {
     *lo = kind == ATTN_MASK_CAUSAL_SLIDING ? std::max(0, L - S_q - window) / T : 0;
     *hi = (L + T - 1) / T;

@@ -37,6 +37,13 @@ struct Schedule {
 // tile's FULL key tiles are not contiguous (cannot happen for the five kinds).
 attn_status build_schedule(const ScheduleInput& in, Schedule* out);
 
+// Backward (dK, dV): one item per key tile, listing the query tiles whose rows may
+// see one of its keys ("transposed" band), for the interval kinds (not LOCAL_GLOBAL).
+// Item ints: [kv_tile, q_begin, q_end, full_begin, full_end, 0, 0, 0]; query tiles in
+// [full_begin, full_end) have every (i, j) pair allowed; items ordered longest first.
+// Returns ATTN_ERR_UNSUPPORTED for LOCAL_GLOBAL.
+attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* items);
+
 // Decode: key tiles per sequence and the size of the persistent grid
 // (see attn_decode_schedule_host).
 struct DecodeSchedule {

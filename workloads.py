@@ -255,3 +255,19 @@ def make_fp8_inputs(w: Workload):
         out.append((x * (448.0 / amax)).to(torch.float8_e4m3fn))
         ds.append(amax / 448.0)
     return out[0], out[1], out[2], tuple(ds)
+
+
+# ----------------------------------------------------------------------------- backward
+def make_grad_output(w: Workload, device: Optional[str] = None):
+    """Seeded output gradient dO [B, Hq, S, d] in the workload dtype: standard normal entries,
+    drawn from a generator seeded with seed + 1 so it is independent of Q, K and V."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 1)
+    dO = torch.randn(w.B, w.Hq, w.S, w.d, generator=g, dtype=torch.float32).to(w.torch_dtype)
+    return dO if device is None else dO.to(device)
+
+
+def backward_flops(w: Workload) -> int:
+    """10 * d flops per allowed pair: the backward's five products of the (query, key) pair
+    (the score and dP, and the dQ, dK and dV updates), 2d flops each.  2.5 times the forward."""
+    return 10 * w.d * allowed_pairs_per_head(w) * w.B * w.Hq
