@@ -419,7 +419,7 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
         p.kind = h->kind; p.window = h->window;
         p.scale = h->scale;
         p.scale_log2 = (float)((double)h->scale * 1.4426950408889634);
-        p.lse2 = h->d_lse2; p.dvec = h->d_dvec;
+        p.nlse2 = h->d_lse2; p.nd = h->d_dvec;
         p.err = h->d_err;
         p.watchdog_ns = h->tp.watchdog_ns;
     }
@@ -436,7 +436,7 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     }
     attn::BwdPrepParams pp{};
     pp.o = static_cast<const uint16_t*>(O); pp.dout = static_cast<const uint16_t*>(dO); pp.lse = LSE;
-    pp.lse2 = h->d_lse2; pp.dvec = h->d_dvec;
+    pp.nlse2 = h->d_lse2; pp.nd = h->d_dvec;
     pp.BHq = (int)BHq; pp.S = h->S; pp.S_pad = S_pad; pp.d = h->d;
     if ((e = attn::launch_bwd_prep(pp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     p.work = h->d_work;  // the forward's first-launch items: one per (batch x head, query tile)

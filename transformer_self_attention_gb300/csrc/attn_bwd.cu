@@ -10,20 +10,28 @@
 // (dK and dV summed over the query heads of each kv head).  P is recomputed from the
 // saved LSE, tile by tile, as the forward computed it; nothing of size S x S is stored.
 //
-//   bwd_prep        : D_i and LSE_i log2(e) into padded per-head vectors (one warp per row).
+//   bwd_prep        : -D_i and -LSE_i log2(e) into padded per-head vectors (one warp per row).
 //   attn_bwd_dq     : one CTA per forward work item (128 query rows of one head).  For
 //                     each allowed key tile: S = Q K^T and dP = dO V^T (tcgen05, fp32 in
-//                     tensor memory), the four compute warps form dS = P (dP - D) in bf16
-//                     over dP, and dQ += dS K reads dS from tensor memory.
+//                     tensor memory), dS = P (dP - D) in bf16 over dP, and dQ += dS K with
+//                     dS read from tensor memory.
 //   attn_bwd_dkdv   : one CTA per key tile of one kv head, over the query tiles of every
-//                     query head of the group that see it.  S^T = K Q^T and dP^T = V dO^T;
-//                     the compute warps (one thread per key) form P^T and dS^T in bf16 over
-//                     them; dV += P^T dO and dK += dS^T Q accumulate in tensor memory.
+//                     query head of the group that see it.  S^T = K Q^T and dP^T = V dO^T,
+//                     P^T and dS^T in bf16 over them, dV += P^T dO and dK += dS^T Q.
 //
-// Both kernels: warp 4 loads with TMA, warp 5 issues the MMAs, warps 0-3 compute.  Every
-// mbarrier wait is bounded; the compute warps run the same sequence of named barriers
-// whatever happens (a wait that ran out returns at once from then on), and the producer
-// and MMA threads drain their copies and products before the CTA exits.
+// Both kernels split every 128 x 128 tile into two 64-column halves.  Compute warpgroup h
+// (warps 4h .. 4h+3, one thread per tensor-memory lane) owns half h: while it turns half h
+// of tile n into bf16, the tensor core runs the products of the other half, so the
+// element-wise work overlaps the MMAs.  Warp 8 loads with TMA, warp 9 issues the MMAs in
+// the order
+//     S_0(n+1) dP_0(n+1) after the half-0 update of tile n,
+//     S_1(n+1) dP_1(n+1) after the half-1 update of tile n,
+// so each half's tensor-memory columns are rewritten only by products issued after the
+// update that read them (tcgen05 MMAs of one thread run in issue order).
+//
+// Every mbarrier wait is bounded; the compute warps run the same sequence of named
+// barriers whatever happens (a wait that ran out returns at once from then on), and the
+// producer and MMA threads drain their copies and products before the CTA exits.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -35,10 +43,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BT = 128;        // rows / keys per tile
-constexpr int NTHREADS = 192;
-constexpr int WARP_PRODUCER = 4;
-constexpr int WARP_MMA = 5;
+constexpr int BT = 128;         // rows / keys per tile
+constexpr int HALF = 64;        // columns per half tile
+constexpr int NCOMPUTE = 256;   // two warpgroups
+constexpr int NTHREADS = NCOMPUTE + 64;
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
 constexpr float LOG2E = 1.4426950408889634f;
 enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_COMPUTE = 4 };
 
@@ -96,6 +106,12 @@ __device__ __forceinline__ void key_band(int kind, int window, long S, long j, l
     if (*hi > S - 1) *hi = S - 1;
 }
 
+// In-tile allowed columns [a0, a1] (clamped to [-1, BT]) of an interval [lo, hi] and tile start c0.
+__device__ __forceinline__ void tile_interval(long lo, long hi, long c0, int* a0, int* a1) {
+    *a0 = (int)max(-1L, min((long)BT, lo - c0));
+    *a1 = (int)max(-1L, min((long)BT, hi - c0));
+}
+
 // ------------------------------------------------------------------ pre-pass
 __global__ void bwd_prep_kernel(BwdPrepParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,8 +120,8 @@ __global__ void bwd_prep_kernel(BwdPrepParams p) {
     const long bh = row / p.S_pad, i = row - bh * p.S_pad;
     if (i >= p.S) {
         if (lane == 0) {
-            p.lse2[row] = INFINITY;  // padding rows: P = 0
-            p.dvec[row] = 0.f;
+            p.nlse2[row] = -INFINITY;  // padding rows: P = 0
+            p.nd[row] = 0.f;
         }
         return;
     }
@@ -124,38 +140,105 @@ __global__ void bwd_prep_kernel(BwdPrepParams p) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) {
-        p.dvec[row] = acc;
-        p.lse2[row] = p.lse[bh * p.S + i] * LOG2E;
+        p.nd[row] = -acc;
+        p.nlse2[row] = -p.lse[bh * p.S + i] * LOG2E;
     }
 }
 
-// O row -> bf16 -> 128B-swizzled staging (two 64-column blocks per 128 columns) for a TMA store:
-// thread r writes row r of the tile from tensor-memory columns [col0, col0 + D) times f.
-template <int D>
-__device__ __forceinline__ void stage_row_bf16(uint8_t* stage, uint32_t t_lane, uint32_t col0, int r, float f) {
+// 32-column groups g0 .. g0+NG-1 of a 128-row tile in tensor memory (columns col0 + 32 g),
+// times f, as bf16 into 128B-swizzled staging (64-column blocks of 128 rows x 128 B) for a
+// TMA store; thread r writes row r.
+template <int NG>
+__device__ __forceinline__ void stage_groups(uint8_t* stage, uint32_t t_lane, uint32_t col0, int g0, int r, float f) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int k = 0; k < NG; ++k) {
+        const int g = g0 + k;
         uint32_t o[32];
-        tmem_ld32(t_lane + col0 + c * 32, o);
+        tmem_ld32(t_lane + col0 + g * 32, o);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * f, __uint_as_float(o[2 * e + 1]) * f);
-        const int sub = c >> 1;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int chunk = (c & 1) * 4 + q;
-            uint4* dst = reinterpret_cast<uint4*>(stage + sub * (BT * 128) + r * 128 + ((chunk ^ (r & 7)) << 4));
+            const int chunk = (g & 1) * 4 + q;
+            uint4* dst = reinterpret_cast<uint4*>(stage + (g >> 1) * (BT * 128) + r * 128 + ((chunk ^ (r & 7)) << 4));
             *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
     }
 }
 
-// Masked score of in-tile column c (allowed columns [a0, a1]); -inf elsewhere.
+// Score of in-tile column c, -inf outside the allowed columns [a0, a1] on masked tiles.
 template <bool MASKED>
-__device__ __forceinline__ float sc(uint32_t raw, int c, int a0, int a1) {
+__device__ __forceinline__ float masked(uint32_t raw, int c, int a0, int a1) {
     if (!MASKED) return __uint_as_float(raw);
     return (c >= a0 && c <= a1) ? __uint_as_float(raw) : -INFINITY;
+}
+
+// dQ kernel, one thread = one query row: half h of the tile (key columns 64h .. 64h+63).
+// dS = 2^(s sl2 - LSE_i log2 e) (dP - D_i), rounded to bf16 and packed two per column over
+// the first 32 dP columns of the half.
+template <bool MASKED>
+__device__ __forceinline__ void dq_half(uint32_t t_s, uint32_t t_dp, int h, float sl2, float nlse, float nd, int a0,
+                                        int a1) {
+    const float2 sl = make_float2(sl2, sl2), nl = make_float2(nlse, nlse), ndd = make_float2(nd, nd);
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        const int cb = h * HALF + ch * 32;
+        uint32_t s[32], g[32], pd[16];
+        tmem_ld32(t_s + cb, s);
+        tmem_ld32(t_dp + cb, g);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c = cb + 2 * e;
+            const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[2 * e], c, a0, a1),
+                                                    masked<MASKED>(s[2 * e + 1], c + 1, a0, a1)), sl, nl);
+            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), ndd);
+            const float2 ds = __fmul2_rn(pv, dd);
+            pd[e] = pack_bf16x2(ds.x, ds.y);
+        }
+        tmem_st16(t_dp + h * HALF + ch * 16, pd);
+    }
+}
+
+// dK/dV kernel, one thread = one key: half h of the tile (query columns 64h .. 64h+63), with
+// the query rows' -LSE log2 e and -D from shared memory.  P^T and dS^T in bf16, packed over
+// the first 32 columns of the half of S^T and of dP^T.
+template <bool MASKED>
+__device__ __forceinline__ void kv_half(uint32_t t_s, uint32_t t_dp, int h, float sl2, const float* vl,
+                                        const float* vd, int a0, int a1) {
+    const float2 sl = make_float2(sl2, sl2);
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        const int cb = h * HALF + ch * 32;
+        uint32_t s[32], g[32], pp[16], pd[16];
+        tmem_ld32(t_s + cb, s);
+        tmem_ld32(t_dp + cb, g);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            const int c = cb + 2 * e;
+            const float4 nl4 = *reinterpret_cast<const float4*>(vl + c);
+            const float4 nd4 = *reinterpret_cast<const float4*>(vd + c);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int cc = c + 2 * u, k = 2 * (e + u);
+                const float2 nl = u ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
+                const float2 ndd = u ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
+                const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cc, a0, a1),
+                                                        masked<MASKED>(s[k + 1], cc + 1, a0, a1)), sl, nl);
+                const float2 pv = make_float2(ex2(x.x), ex2(x.y));
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[k]), __uint_as_float(g[k + 1])), ndd);
+                const float2 ds = __fmul2_rn(pv, dd);
+                pp[e + u] = pack_bf16x2(pv.x, pv.y);
+                pd[e + u] = pack_bf16x2(ds.x, ds.y);
+            }
+        }
+        tmem_st16(t_s + h * HALF + ch * 16, pp);
+        tmem_st16(t_dp + h * HALF + ch * 16, pd);
+    }
 }
 
 // ------------------------------------------------------------------ dQ kernel
@@ -173,8 +256,8 @@ struct DqCfg {
     static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DQ = 256;
 };
 
-enum DqBar { Q_LOAD = 0, Q_KFULL, Q_KEMPTY = Q_KFULL + 2, Q_VFULL = Q_KEMPTY + 2, Q_VEMPTY = Q_VFULL + 2,
-             Q_SFULL = Q_VEMPTY + 2, Q_DSFULL, Q_DQ, Q_NBAR };
+enum DqBar { Q_LOAD = 0, Q_FULL, Q_EMPTY = Q_FULL + 2, Q_HFULL = Q_EMPTY + 2, Q_HDONE = Q_HFULL + 2,
+             Q_DONE = Q_HDONE + 2, Q_DRAIN, Q_NBAR };
 
 struct BwdShared {
     uint64_t bar[16];
@@ -202,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
     const int bkv = b * p.Hkv + a / p.group;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < Q_NBAR; ++i) mbar_init(bar(i), i == Q_DSFULL ? 128u : 1u);
+        for (int i = 0; i < Q_NBAR; ++i) mbar_init(bar(i), (i == Q_HDONE || i == Q_HDONE + 1) ? 128u : 1u);
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -225,118 +308,110 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
                 tma_load_3d(s_q + s * C::SUB, &p.tm_q, bar(Q_LOAD), s * 64, q_tile * BT, bh);
                 tma_load_3d(s_do + s * C::SUB, &p.tm_do, bar(Q_LOAD), s * 64, q_tile * BT, bh);
             }
-            int k_loaded = 0, v_loaded = 0;
-            bool ok = true;
-            for (int it = 0; it < n_iter && ok; ++it) {
+            int loaded = 0;
+            for (int it = 0; it < n_iter; ++it) {
                 const int st = it & 1, row = (kv_begin + it) * BT;
-                if (it >= 2 && !(ok = wait_bounded(bar(Q_KEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
-                mbar_arrive_expect_tx(bar(Q_KFULL + st), C::TB);
-                for (int s = 0; s < D / 64; ++s)
-                    tma_load_3d(s_k + st * C::TB + s * C::SUB, &p.tm_k, bar(Q_KFULL + st), s * 64, row, bkv);
-                k_loaded = it + 1;
-                if (it >= 2 && !(ok = wait_bounded(bar(Q_VEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
-                mbar_arrive_expect_tx(bar(Q_VFULL + st), C::TB);
-                for (int s = 0; s < D / 64; ++s)
-                    tma_load_3d(s_v + st * C::TB + s * C::SUB, &p.tm_v, bar(Q_VFULL + st), s * 64, row, bkv);
-                v_loaded = it + 1;
+                if (it >= 2 && !wait_bounded(bar(Q_EMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER)) break;
+                mbar_arrive_expect_tx(bar(Q_FULL + st), 2 * C::TB);
+                for (int s = 0; s < D / 64; ++s) {
+                    tma_load_3d(s_k + st * C::TB + s * C::SUB, &p.tm_k, bar(Q_FULL + st), s * 64, row, bkv);
+                    tma_load_3d(s_v + st * C::TB + s * C::SUB, &p.tm_v, bar(Q_FULL + st), s * 64, row, bkv);
+                }
+                loaded = it + 1;
             }
             if (sh->abort) {
                 drain_wait(bar(Q_LOAD), 0, wd);
-                for (int n = max(0, k_loaded - 2); n < k_loaded; ++n) drain_wait(bar(Q_KFULL + (n & 1)), (n >> 1) & 1, wd);
-                for (int n = max(0, v_loaded - 2); n < v_loaded; ++n) drain_wait(bar(Q_VFULL + (n & 1)), (n >> 1) & 1, wd);
+                for (int n = max(0, loaded - 2); n < loaded; ++n) drain_wait(bar(Q_FULL + (n & 1)), (n >> 1) & 1, wd);
             }
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);  // [128 x 128] = A[128 x d] . B[128 x d]^T
-            constexpr uint32_t idesc_q = idesc_bf16_f32(BT, D, true);    // dQ += dS (tensor memory) . K (MN-major)
+            constexpr uint32_t idesc_h = idesc_bf16_f32(BT, HALF, false);  // [128 x 64] = A[128 x d] . B[64 x d]^T
+            constexpr uint32_t idesc_q = idesc_bf16_f32(BT, D, true);      // dQ += dS (tensor memory) . K (MN-major)
             const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP, t_dq = tmem + C::TMEM_DQ;
-            bool ok = wait_bounded(bar(Q_LOAD), 0, wd, ERR_MMA);
-            int last_bar = -1, last_par = 0;
+            // S_h = Q K_h^T and dP_h = dO V_h^T for the key rows 64h .. 64h+63 of stage st
+            auto issue_sdp = [&](int h, int st) {
+                const uint32_t sk = s_k + st * C::TB + h * HALF * 128, sv = s_v + st * C::TB + h * HALF * 128;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_s + h * HALF, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024), idesc_h,
+                           k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_dp + h * HALF, sdesc_sw128(s_do + off, 16, 1024), sdesc_sw128(sv + off, 16, 1024),
+                           idesc_h, k > 0);
+                }
+                mma_commit(bar(Q_HFULL + h));
+            };
+            // dQ += dS_h K_h (64 keys: four K=16 steps)
+            auto issue_dq = [&](int h, int st, bool first) {
+                const uint32_t sk = s_k + st * C::TB;
+#pragma unroll
+                for (int k = 0; k < HALF / 16; ++k)
+                    mma_ts(t_dq, t_dp + h * HALF + k * 8, sdesc_sw128(sk + (h * HALF + k * 16) * 128, C::SUB, 1024),
+                           idesc_q, (first && k == 0) ? 0u : 1u);
+            };
+            bool ok = wait_bounded(bar(Q_LOAD), 0, wd, ERR_MMA) && wait_bounded(bar(Q_FULL), 0, wd, ERR_MMA);
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0, 0);
+                issue_sdp(1, 0);
+            }
             for (int it = 0; it < n_iter && ok; ++it) {
                 const int st = it & 1;
-                if (!(ok = wait_bounded(bar(Q_KFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
-                if (!(ok = wait_bounded(bar(Q_VFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
+                const bool more = it + 1 < n_iter;
+                if (!(ok = wait_bounded(bar(Q_HDONE), it & 1, wd, ERR_MMA))) break;
                 tc_fence_after();
-                const uint32_t sk = s_k + st * C::TB, sv = s_v + st * C::TB;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024), idesc_s, k > 0);
+                issue_dq(0, st, it == 0);
+                if (more) {
+                    if (!(ok = wait_bounded(bar(Q_FULL + (st ^ 1)), ((it + 1) >> 1) & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_sdp(0, st ^ 1);
                 }
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_dp, sdesc_sw128(s_do + off, 16, 1024), sdesc_sw128(sv + off, 16, 1024), idesc_s, k > 0);
-                }
-                mma_commit(bar(Q_SFULL));
-                mma_commit(bar(Q_VEMPTY + st));
-                last_bar = Q_VEMPTY + st; last_par = (it >> 1) & 1;
-                if (!(ok = wait_bounded(bar(Q_DSFULL), it & 1, wd, ERR_MMA))) break;
+                if (!(ok = wait_bounded(bar(Q_HDONE + 1), it & 1, wd, ERR_MMA))) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < BT / 16; ++k)
-                    mma_ts(t_dq, t_dp + k * 8, sdesc_sw128(sk + k * 16 * 128, C::SUB, 1024), idesc_q,
-                           (it > 0 || k > 0) ? 1u : 0u);
-                mma_commit(bar(Q_KEMPTY + st));
-                last_bar = Q_KEMPTY + st; last_par = (it >> 1) & 1;
+                issue_dq(1, st, false);
+                mma_commit(bar(Q_EMPTY + st));
+                if (more) issue_sdp(1, st ^ 1);
             }
-            if (ok) mma_commit(bar(Q_DQ));
-            if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, wd);
+            if (ok) mma_commit(bar(Q_DONE));
+            if (sh->abort) {
+                mma_commit(bar(Q_DRAIN));
+                drain_wait(bar(Q_DRAIN), 0, wd);
+            }
         }
     } else {
-        // compute warps: one thread per query row
-        const int r = threadIdx.x;
+        // compute warps: warpgroup wg owns key columns 64 wg .. 64 wg + 63; one thread per query row
+        const int wg = warp >> 2, r = (warp & 3) * 32 + lane;
         const long i = (long)q_tile * BT + r;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t t_s = t_lane + C::TMEM_S, t_dp = t_lane + C::TMEM_DP;
-        const float lse2 = p.lse2[(size_t)bh * p.S_pad + i];
-        const float Di = p.dvec[(size_t)bh * p.S_pad + i];
+        const float nlse = p.nlse2[(size_t)bh * p.S_pad + i];
+        const float nd = p.nd[(size_t)bh * p.S_pad + i];
         const float sl2 = p.scale_log2;
         long lo, hi;
         row_band(p.kind, p.window, p.S, i, &lo, &hi);
         for (int it = 0; it < n_iter; ++it) {
-            wait_bounded(bar(Q_SFULL), it & 1, wd, ERR_COMPUTE);
+            wait_bounded(bar(Q_HFULL + wg), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
             const int t = kv_begin + it;
-            const bool partial = t < full_begin || t >= full_end;
-            const long c0 = (long)t * BT;
-            const int a0 = (int)max(-1L, min((long)BT, lo - c0)), a1 = (int)max(-1L, min((long)BT, hi - c0));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t s0[32], s1[32], d0[32], d1[32], pk[32];
-                tmem_ld32(t_s + h * 64, s0);
-                tmem_ld32(t_s + h * 64 + 32, s1);
-                tmem_ld32(t_dp + h * 64, d0);
-                tmem_ld32(t_dp + h * 64 + 32, d1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float ds[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = h * 64 + (u >> 1) * 32 + 2 * e + (u & 1);
-                        const uint32_t sr = (u >> 1) ? s1[2 * e + (u & 1)] : s0[2 * e + (u & 1)];
-                        const uint32_t dr = (u >> 1) ? d1[2 * e + (u & 1)] : d0[2 * e + (u & 1)];
-                        const float s = partial ? sc<true>(sr, c, a0, a1) : sc<false>(sr, c, a0, a1);
-                        const float pv = ex2(fmaf(s, sl2, -lse2));
-                        ds[u] = pv * (__uint_as_float(dr) - Di);
-                    }
-                    pk[e] = pack_bf16x2(ds[0], ds[1]);
-                    pk[16 + e] = pack_bf16x2(ds[2], ds[3]);
-                }
-                tmem_st32(t_dp + h * 32, pk);  // dS (bf16 pairs) over the dP columns already read
-            }
+            int a0, a1;
+            tile_interval(lo, hi, (long)t * BT, &a0, &a1);
+            if (t < full_begin || t >= full_end) dq_half<true>(t_s, t_dp, wg, sl2, nlse, nd, a0, a1);
+            else dq_half<false>(t_s, t_dp, wg, sl2, nlse, nd, a0, a1);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(Q_DSFULL));
+            mbar_arrive(bar(Q_HDONE + wg));
         }
         // epilogue: dQ * scale -> bf16 -> swizzled staging in the Q buffer -> TMA store
-        wait_bounded(bar(Q_DQ), 0, wd, ERR_COMPUTE);
+        wait_bounded(bar(Q_DONE), 0, wd, ERR_COMPUTE);
         tc_fence_after();
-        stage_row_bf16<D>(smem + C::OFF_Q, t_lane, C::TMEM_DQ, r, p.scale);
+        stage_groups<D / 64>(smem + C::OFF_Q, t_lane, C::TMEM_DQ, wg * (D / 64), r, p.scale);
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, NCOMPUTE);
         if (threadIdx.x == 0 && !sh->abort) {
             for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_dq, s_q + s * C::SUB, s * 64, q_tile * BT, bh);
             tma_store_commit_and_wait_read();
@@ -360,14 +435,15 @@ struct KvCfg {
     static constexpr int OFF_V = OFF_K + TB;
     static constexpr int OFF_Q = OFF_V + TB;        // two stages
     static constexpr int OFF_DO = OFF_Q + 2 * TB;   // two stages
-    static constexpr int OFF_VEC = OFF_DO + 2 * TB; // two stages of 128 LSE (log2) + 128 D
+    static constexpr int OFF_VEC = OFF_DO + 2 * TB; // two stages of 128 -LSE log2 e + 128 -D
     static constexpr int OFF_CTL = OFF_VEC + 2 * 1024;
     static constexpr int SMEM_ALLOC = OFF_CTL + 1024 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DV = 256, TMEM_DK = 256 + D;
 };
 
-enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMPTY + 2, KV_PFULL, KV_DONE, KV_NBAR };
+enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_HFULL = KV_QEMPTY + 2, KV_HDONE = KV_HFULL + 2,
+             KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -392,7 +468,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
     auto iter_qtile = [&](int it) { return q_begin + it % n_q; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < KV_NBAR; ++i) mbar_init(bar(i), i == KV_PFULL ? 128u : 1u);
+        for (int i = 0; i < KV_NBAR; ++i) mbar_init(bar(i), (i == KV_HDONE || i == KV_HDONE + 1) ? 128u : 1u);
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -416,18 +492,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
                 tma_load_3d(s_v + s * C::SUB, &p.tm_v, bar(KV_LOAD), s * 64, kv_tile * BT, bkv);
             }
             int loaded = 0;
-            bool ok = true;
-            for (int it = 0; it < n_iter && ok; ++it) {
+            for (int it = 0; it < n_iter; ++it) {
                 const int st = it & 1, bh = iter_head(it), qt = iter_qtile(it);
-                if (it >= 2 && !(ok = wait_bounded(bar(KV_QEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER))) break;
+                if (it >= 2 && !wait_bounded(bar(KV_QEMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER)) break;
                 mbar_arrive_expect_tx(bar(KV_QFULL + st), 2 * C::TB + 1024);
                 for (int s = 0; s < D / 64; ++s) {
                     tma_load_3d(s_q + st * C::TB + s * C::SUB, &p.tm_q, bar(KV_QFULL + st), s * 64, qt * BT, bh);
                     tma_load_3d(s_do + st * C::TB + s * C::SUB, &p.tm_do, bar(KV_QFULL + st), s * 64, qt * BT, bh);
                 }
                 const size_t v0 = (size_t)bh * p.S_pad + (size_t)qt * BT;
-                bulk_load(s_vec + st * 1024, p.lse2 + v0, 512, bar(KV_QFULL + st));
-                bulk_load(s_vec + st * 1024 + 512, p.dvec + v0, 512, bar(KV_QFULL + st));
+                bulk_load(s_vec + st * 1024, p.nlse2 + v0, 512, bar(KV_QFULL + st));
+                bulk_load(s_vec + st * 1024 + 512, p.nd + v0, 512, bar(KV_QFULL + st));
                 loaded = it + 1;
             }
             if (sh->abort) {
@@ -437,50 +512,73 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
+            constexpr uint32_t idesc_h = idesc_bf16_f32(BT, HALF, false);
             constexpr uint32_t idesc_kv = idesc_bf16_f32(BT, D, true);  // dV, dK += (tensor memory) . (MN-major)
             const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP;
             const uint32_t t_dv = tmem + C::TMEM_DV, t_dk = tmem + C::TMEM_DK;
-            bool ok = wait_bounded(bar(KV_LOAD), 0, wd, ERR_MMA);
-            int last_bar = -1, last_par = 0;
-            for (int it = 0; it < n_iter && ok; ++it) {
-                const int st = it & 1;
-                if (!(ok = wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_MMA))) break;
-                tc_fence_after();
+            // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for the query rows 64h .. 64h+63 of stage st
+            auto issue_sdp = [&](int h, int st) {
+                const uint32_t sq = s_q + st * C::TB + h * HALF * 128, sdo = s_do + st * C::TB + h * HALF * 128;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_s + h * HALF, sdesc_sw128(s_k + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idesc_h,
+                           k > 0);
+                }
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_dp + h * HALF, sdesc_sw128(s_v + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024),
+                           idesc_h, k > 0);
+                }
+                mma_commit(bar(KV_HFULL + h));
+            };
+            // dV += P^T_h dO_h and dK += dS^T_h Q_h (64 query rows: four K=16 steps each)
+            auto issue_kv = [&](int h, int st, bool first) {
                 const uint32_t sq = s_q + st * C::TB, sdo = s_do + st * C::TB;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_s, sdesc_sw128(s_k + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idesc_s, k > 0);
-                }
+                for (int k = 0; k < HALF / 16; ++k)
+                    mma_ts(t_dv, t_s + h * HALF + k * 8, sdesc_sw128(sdo + (h * HALF + k * 16) * 128, C::SUB, 1024),
+                           idesc_kv, (first && k == 0) ? 0u : 1u);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_dp, sdesc_sw128(s_v + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), idesc_s, k > 0);
-                }
-                mma_commit(bar(KV_SFULL));
-                last_bar = KV_SFULL; last_par = it & 1;
-                if (!(ok = wait_bounded(bar(KV_PFULL), it & 1, wd, ERR_MMA))) break;
+                for (int k = 0; k < HALF / 16; ++k)
+                    mma_ts(t_dk, t_dp + h * HALF + k * 8, sdesc_sw128(sq + (h * HALF + k * 16) * 128, C::SUB, 1024),
+                           idesc_kv, (first && k == 0) ? 0u : 1u);
+            };
+            bool ok = wait_bounded(bar(KV_LOAD), 0, wd, ERR_MMA) && wait_bounded(bar(KV_QFULL), 0, wd, ERR_MMA);
+            if (ok) {
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < BT / 16; ++k)
-                    mma_ts(t_dv, t_s + k * 8, sdesc_sw128(sdo + k * 16 * 128, C::SUB, 1024), idesc_kv,
-                           (it > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-                for (int k = 0; k < BT / 16; ++k)
-                    mma_ts(t_dk, t_dp + k * 8, sdesc_sw128(sq + k * 16 * 128, C::SUB, 1024), idesc_kv,
-                           (it > 0 || k > 0) ? 1u : 0u);
+                issue_sdp(0, 0);
+                issue_sdp(1, 0);
+            }
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const int st = it & 1;
+                const bool more = it + 1 < n_iter;
+                if (!(ok = wait_bounded(bar(KV_HDONE), it & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+                issue_kv(0, st, it == 0);
+                if (more) {
+                    if (!(ok = wait_bounded(bar(KV_QFULL + (st ^ 1)), ((it + 1) >> 1) & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_sdp(0, st ^ 1);
+                }
+                if (!(ok = wait_bounded(bar(KV_HDONE + 1), it & 1, wd, ERR_MMA))) break;
+                tc_fence_after();
+                issue_kv(1, st, false);
                 mma_commit(bar(KV_QEMPTY + st));
-                last_bar = KV_QEMPTY + st; last_par = (it >> 1) & 1;
+                if (more) issue_sdp(1, st ^ 1);
             }
             if (ok) mma_commit(bar(KV_DONE));
-            if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, wd);
+            if (sh->abort) {
+                mma_commit(bar(KV_DRAIN));
+                drain_wait(bar(KV_DRAIN), 0, wd);
+            }
         }
     } else {
-        // compute warps: one thread per key (tensor-memory lane), 128 query columns per tile
-        const int t = threadIdx.x;
+        // compute warps: warpgroup wg owns query columns 64 wg .. 64 wg + 63; one thread per key
+        const int wg = warp >> 2, t = (warp & 3) * 32 + lane;
         const long j = (long)kv_tile * BT + t;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t t_s = t_lane + C::TMEM_S, t_dp = t_lane + C::TMEM_DP;
         const float sl2 = p.scale_log2;
         long ilo, ihi;
@@ -489,52 +587,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
         for (int it = 0; it < n_iter; ++it) {
             const int st = it & 1, qt = iter_qtile(it);
             wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
-            wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
+            wait_bounded(bar(KV_HFULL + wg), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            const bool partial = qt < full_begin || qt >= full_end;
-            const long r0 = (long)qt * BT;
-            const int a0 = (int)max(-1L, min((long)BT, ilo - r0)), a1 = (int)max(-1L, min((long)BT, ihi - r0));
-            const float* vlse = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
-            const float* vd = vlse + 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t s0[32], s1[32], d0[32], d1[32], pp[32], pd[32];
-                tmem_ld32(t_s + h * 64, s0);
-                tmem_ld32(t_s + h * 64 + 32, s1);
-                tmem_ld32(t_dp + h * 64, d0);
-                tmem_ld32(t_dp + h * 64 + 32, d1);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[4], ds[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = h * 64 + (u >> 1) * 32 + 2 * e + (u & 1);  // query column
-                        const uint32_t sr = (u >> 1) ? s1[2 * e + (u & 1)] : s0[2 * e + (u & 1)];
-                        const uint32_t dr = (u >> 1) ? d1[2 * e + (u & 1)] : d0[2 * e + (u & 1)];
-                        const float s = partial ? sc<true>(sr, c, a0, a1) : sc<false>(sr, c, a0, a1);
-                        pv[u] = ex2(fmaf(s, sl2, -vlse[c]));
-                        ds[u] = pv[u] * (__uint_as_float(dr) - vd[c]);
-                    }
-                    pp[e] = pack_bf16x2(pv[0], pv[1]);
-                    pp[16 + e] = pack_bf16x2(pv[2], pv[3]);
-                    pd[e] = pack_bf16x2(ds[0], ds[1]);
-                    pd[16 + e] = pack_bf16x2(ds[2], ds[3]);
-                }
-                tmem_st32(t_s + h * 32, pp);   // P^T over the S^T columns already read
-                tmem_st32(t_dp + h * 32, pd);  // dS^T over the dP^T columns already read
-            }
+            int a0, a1;
+            tile_interval(ilo, ihi, (long)qt * BT, &a0, &a1);
+            const float* vl = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
+            const float* vd = vl + BT;
+            if (qt < full_begin || qt >= full_end) kv_half<true>(t_s, t_dp, wg, sl2, vl, vd, a0, a1);
+            else kv_half<false>(t_s, t_dp, wg, sl2, vl, vd, a0, a1);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(KV_PFULL));
+            mbar_arrive(bar(KV_HDONE + wg));
         }
-        // epilogue: dV and scale * dK -> bf16 -> swizzled staging (the idle Q stages) -> TMA stores
+        // epilogue: warpgroup 0 stages dV in the first Q stage, warpgroup 1 stages scale * dK in
+        // the first dO stage (both idle once every product has completed), then TMA stores
         wait_bounded(bar(KV_DONE), 0, wd, ERR_COMPUTE);
         tc_fence_after();
-        stage_row_bf16<D>(smem + C::OFF_Q, t_lane, C::TMEM_DV, t, 1.f);
-        stage_row_bf16<D>(smem + C::OFF_DO, t_lane, C::TMEM_DK, t, p.scale);
+        if (wg == 0) stage_groups<D / 32>(smem + C::OFF_Q, t_lane, C::TMEM_DV, 0, t, 1.f);
+        else stage_groups<D / 32>(smem + C::OFF_DO, t_lane, C::TMEM_DK, 0, t, p.scale);
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, NCOMPUTE);
         if (threadIdx.x == 0 && !sh->abort) {
             for (int s = 0; s < D / 64; ++s) {
                 tma_store_3d(&p.tm_dv, s_q + s * C::SUB, s * 64, kv_tile * BT, bkv);

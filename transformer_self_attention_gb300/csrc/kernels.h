@@ -112,15 +112,15 @@ struct BwdParams {
     int S, S_pad, Hq, Hkv, group, kind, window;
     float scale_log2;     // scale * log2(e)
     float scale;
-    const float* lse2;    // [B*Hq, S_pad]: LSE * log2(e); +inf past S
-    const float* dvec;    // [B*Hq, S_pad]: D = dO . O; 0 past S
+    const float* nlse2;   // [B*Hq, S_pad]: -LSE * log2(e); -inf past S
+    const float* nd;      // [B*Hq, S_pad]: -D = -dO . O; 0 past S
     int* err;
     long long watchdog_ns;
 };
 struct BwdPrepParams {
     const uint16_t* o; const uint16_t* dout;  // bf16 bits [B*Hq, S, d]
     const float* lse;                          // [B*Hq, S] (natural log)
-    float* lse2; float* dvec;                  // [B*Hq, S_pad]
+    float* nlse2; float* nd;                   // [B*Hq, S_pad]
     int BHq, S, S_pad, d;
 };
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream);
