@@ -19,15 +19,14 @@
 //                     query head of the group that see it.  S^T = K Q^T and dP^T = V dO^T,
 //                     P^T and dS^T in bf16 over them, dV += P^T dO and dK += dS^T Q.
 //
-// Both kernels split every 128 x 128 tile into two 64-column halves.  Compute warpgroup h
-// (warps 4h .. 4h+3, one thread per tensor-memory lane) owns half h: while it turns half h
-// of tile n into bf16, the tensor core runs the products of the other half, so the
-// element-wise work overlaps the MMAs.  Warp 8 loads with TMA, warp 9 issues the MMAs in
-// the order
-//     S_0(n+1) dP_0(n+1) after the half-0 update of tile n,
-//     S_1(n+1) dP_1(n+1) after the half-1 update of tile n,
-// so each half's tensor-memory columns are rewritten only by products issued after the
-// update that read them (tcgen05 MMAs of one thread run in issue order).
+// Both kernels: warps 0-7 compute (warpgroup h owns columns 64h .. 64h+63 of the 128 x 128
+// score tile, one thread per tensor-memory lane), warp 8 loads with TMA, warp 9 issues the
+// MMAs.  The score products are full 128 x 128 x 16 instructions (a 64-column product costs
+// the tensor core as long as a 128-column one); the element-wise work runs in two steps --
+// P from S while dP is still being computed, then dS -- and each kernel orders its MMAs so
+// that the next tile's S is computed while the warps work on the current one.  tcgen05 MMAs
+// of one thread run in issue order, which protects every tensor-memory column that a later
+// product overwrites.
 //
 // Every mbarrier wait is bounded; the compute warps run the same sequence of named
 // barriers whatever happens (a wait that ran out returns at once from then on), and the
@@ -175,95 +174,97 @@ __device__ __forceinline__ float masked(uint32_t raw, int c, int a0, int a1) {
     return (c >= a0 && c <= a1) ? __uint_as_float(raw) : -INFINITY;
 }
 
-// dQ kernel, one thread = one query row: half h of the tile (key columns 64h .. 64h+63).
-// dS = 2^(s sl2 - LSE_i log2 e) (dP - D_i), rounded to bf16 and packed two per column over
-// the first 32 dP columns of the half.
-template <bool MASKED>
-__device__ __forceinline__ void dq_half(uint32_t t_s, uint32_t t_dp, int h, float sl2, float nlse, float nd, int a0,
-                                        int a1) {
-    const float2 sl = make_float2(sl2, sl2), nl = make_float2(nlse, nlse), ndd = make_float2(nd, nd);
+// The element-wise work of one warpgroup on its half of a tile (columns 64h .. 64h+63 of the
+// 128-column score tile; one thread per tensor-memory lane), in two steps so that the first
+// can run while the tensor core still computes dP:
+//   exp_pass: P = 2^(s sl2 - LSE log2 e) in fp32 registers (0 where masked), and optionally P
+//             rounded to bf16 and packed two per column over the first 32 columns of the half;
+//   ds_pass : dS = P (dP - D), rounded to bf16 and packed over the first 32 dP columns of the half.
+// The row's (dQ kernel) or the columns' (dK/dV kernel, from shared memory) -LSE log2 e and -D
+// come in through NL / ND.
+struct RowConst {  // one value for every column: the thread's own query row
+    float v;
+    __device__ __forceinline__ float2 pair(int) const { return make_float2(v, v); }
+};
+struct ColVec {  // one value per column, from a shared-memory vector of 128 floats
+    const float* v;
+    __device__ __forceinline__ float2 pair(int c) const { return *reinterpret_cast<const float2*>(v + c); }
+};
+
+template <bool MASKED, bool STORE_P, class NL>
+__device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, float (&pv)[64]) {
+    const float2 sl = make_float2(sl2, sl2);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int cb = h * HALF + ch * 32;
-        uint32_t s[32], g[32], pd[16];
+        uint32_t s[32], pk[16];
         tmem_ld32(t_s + cb, s);
-        tmem_ld32(t_dp + cb, g);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int c = cb + 2 * e;
             const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[2 * e], c, a0, a1),
-                                                    masked<MASKED>(s[2 * e + 1], c + 1, a0, a1)), sl, nl);
-            const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), ndd);
-            const float2 ds = __fmul2_rn(pv, dd);
-            pd[e] = pack_bf16x2(ds.x, ds.y);
+                                                    masked<MASKED>(s[2 * e + 1], c + 1, a0, a1)), sl, nl.pair(c));
+            pv[ch * 32 + 2 * e] = ex2(x.x);
+            pv[ch * 32 + 2 * e + 1] = ex2(x.y);
+            if (STORE_P) pk[e] = pack_bf16x2(pv[ch * 32 + 2 * e], pv[ch * 32 + 2 * e + 1]);
         }
-        tmem_st16(t_dp + h * HALF + ch * 16, pd);
+        if (STORE_P) tmem_st16(t_s + h * HALF + ch * 16, pk);
     }
 }
 
-// dK/dV kernel, one thread = one key: half h of the tile (query columns 64h .. 64h+63), with
-// the query rows' -LSE log2 e and -D from shared memory.  P^T and dS^T in bf16, packed over
-// the first 32 columns of the half of S^T and of dP^T.
-template <bool MASKED>
-__device__ __forceinline__ void kv_half(uint32_t t_s, uint32_t t_dp, int h, float sl2, const float* vl,
-                                        const float* vd, int a0, int a1) {
-    const float2 sl = make_float2(sl2, sl2);
+template <class ND>
+__device__ __forceinline__ void ds_pass(uint32_t t_dp, int h, ND nd, const float (&pv)[64]) {
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int cb = h * HALF + ch * 32;
-        uint32_t s[32], g[32], pp[16], pd[16];
-        tmem_ld32(t_s + cb, s);
+        uint32_t g[32], pk[16];
         tmem_ld32(t_dp + cb, g);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
+        for (int e = 0; e < 16; ++e) {
             const int c = cb + 2 * e;
-            const float4 nl4 = *reinterpret_cast<const float4*>(vl + c);
-            const float4 nd4 = *reinterpret_cast<const float4*>(vd + c);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int cc = c + 2 * u, k = 2 * (e + u);
-                const float2 nl = u ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
-                const float2 ndd = u ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
-                const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cc, a0, a1),
-                                                        masked<MASKED>(s[k + 1], cc + 1, a0, a1)), sl, nl);
-                const float2 pv = make_float2(ex2(x.x), ex2(x.y));
-                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[k]), __uint_as_float(g[k + 1])), ndd);
-                const float2 ds = __fmul2_rn(pv, dd);
-                pp[e + u] = pack_bf16x2(pv.x, pv.y);
-                pd[e + u] = pack_bf16x2(ds.x, ds.y);
-            }
+            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), nd.pair(c));
+            const float2 ds = __fmul2_rn(make_float2(pv[ch * 32 + 2 * e], pv[ch * 32 + 2 * e + 1]), dd);
+            pk[e] = pack_bf16x2(ds.x, ds.y);
         }
-        tmem_st16(t_s + h * HALF + ch * 16, pp);
-        tmem_st16(t_dp + h * HALF + ch * 16, pd);
+        tmem_st16(t_dp + h * HALF + ch * 16, pk);
     }
 }
 
 // ------------------------------------------------------------------ dQ kernel
+// Tensor memory: three 128-column score regions R0..R2 and dQ.  Tile n keeps S in region
+// (2n) mod 3 and dP in region (2n+1) mod 3, so S of tile n+2 lands in the region that held
+// dP of tile n (free once dQ(n) has read dS) and dP of tile n+1 in the region of S(n) (free
+// once the compute warps have read S(n)).  S(n+2) is therefore computed while the warps work
+// on tile n+1.  K has three shared-memory stages (S runs two tiles ahead), V two.
 template <int D>
 struct DqCfg {
     static constexpr int TB = BT * D * 2;  // one Q / dO / K / V tile
     static constexpr int SUB = BT * 128;   // one 64-column swizzled block
+    static constexpr int KST = 3, VST = 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_DO = OFF_Q + TB;
-    static constexpr int OFF_K = OFF_DO + TB;      // two stages
-    static constexpr int OFF_V = OFF_K + 2 * TB;   // two stages
-    static constexpr int OFF_CTL = OFF_V + 2 * TB;
+    static constexpr int OFF_K = OFF_DO + TB;
+    static constexpr int OFF_V = OFF_K + KST * TB;
+    static constexpr int OFF_CTL = OFF_V + VST * TB;
     static constexpr int SMEM_ALLOC = OFF_CTL + 1024 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DQ = 256;
+    static constexpr uint32_t TMEM_DQ = 384;
 };
 
-enum DqBar { Q_LOAD = 0, Q_FULL, Q_EMPTY = Q_FULL + 2, Q_HFULL = Q_EMPTY + 2, Q_HDONE = Q_HFULL + 2,
-             Q_DONE = Q_HDONE + 2, Q_DRAIN, Q_NBAR };
+enum DqBar { Q_LOAD = 0, Q_KFULL, Q_KEMPTY = Q_KFULL + 3, Q_VFULL = Q_KEMPTY + 3, Q_VEMPTY = Q_VFULL + 2,
+             Q_SFULL = Q_VEMPTY + 2, Q_DPFULL = Q_SFULL + 2, Q_HDONE, Q_DONE = Q_HDONE + 2, Q_DRAIN, Q_NBAR };
+static_assert(Q_NBAR <= 24, "barrier slots");
 
 struct BwdShared {
-    uint64_t bar[16];
+    uint64_t bar[24];
     uint32_t tmem_base;
     volatile int abort;
 };
+
+__device__ __forceinline__ uint32_t region_s(int n) { return (uint32_t)((2 * n) % 3) * 128u; }
+__device__ __forceinline__ uint32_t region_dp(int n) { return (uint32_t)((2 * n + 1) % 3) * 128u; }
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
@@ -308,74 +309,91 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
                 tma_load_3d(s_q + s * C::SUB, &p.tm_q, bar(Q_LOAD), s * 64, q_tile * BT, bh);
                 tma_load_3d(s_do + s * C::SUB, &p.tm_do, bar(Q_LOAD), s * 64, q_tile * BT, bh);
             }
-            int loaded = 0;
+            int k_loaded = 0, v_loaded = 0;
             for (int it = 0; it < n_iter; ++it) {
-                const int st = it & 1, row = (kv_begin + it) * BT;
-                if (it >= 2 && !wait_bounded(bar(Q_EMPTY + st), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER)) break;
-                mbar_arrive_expect_tx(bar(Q_FULL + st), 2 * C::TB);
-                for (int s = 0; s < D / 64; ++s) {
-                    tma_load_3d(s_k + st * C::TB + s * C::SUB, &p.tm_k, bar(Q_FULL + st), s * 64, row, bkv);
-                    tma_load_3d(s_v + st * C::TB + s * C::SUB, &p.tm_v, bar(Q_FULL + st), s * 64, row, bkv);
-                }
-                loaded = it + 1;
+                const int row = (kv_begin + it) * BT, ks = it % 3, vs = it & 1;
+                if (it >= 3 && !wait_bounded(bar(Q_KEMPTY + ks), (it / 3 - 1) & 1, wd, ERR_PRODUCER)) break;
+                mbar_arrive_expect_tx(bar(Q_KFULL + ks), C::TB);
+                for (int s = 0; s < D / 64; ++s)
+                    tma_load_3d(s_k + ks * C::TB + s * C::SUB, &p.tm_k, bar(Q_KFULL + ks), s * 64, row, bkv);
+                k_loaded = it + 1;
+                if (it >= 2 && !wait_bounded(bar(Q_VEMPTY + vs), ((it >> 1) - 1) & 1, wd, ERR_PRODUCER)) break;
+                mbar_arrive_expect_tx(bar(Q_VFULL + vs), C::TB);
+                for (int s = 0; s < D / 64; ++s)
+                    tma_load_3d(s_v + vs * C::TB + s * C::SUB, &p.tm_v, bar(Q_VFULL + vs), s * 64, row, bkv);
+                v_loaded = it + 1;
             }
             if (sh->abort) {
                 drain_wait(bar(Q_LOAD), 0, wd);
-                for (int n = max(0, loaded - 2); n < loaded; ++n) drain_wait(bar(Q_FULL + (n & 1)), (n >> 1) & 1, wd);
+                for (int n = max(0, k_loaded - 3); n < k_loaded; ++n) drain_wait(bar(Q_KFULL + n % 3), (n / 3) & 1, wd);
+                for (int n = max(0, v_loaded - 2); n < v_loaded; ++n) drain_wait(bar(Q_VFULL + (n & 1)), (n >> 1) & 1, wd);
             }
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            constexpr uint32_t idesc_h = idesc_bf16_f32(BT, HALF, false);  // [128 x 64] = A[128 x d] . B[64 x d]^T
-            constexpr uint32_t idesc_q = idesc_bf16_f32(BT, D, true);      // dQ += dS (tensor memory) . K (MN-major)
-            const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP, t_dq = tmem + C::TMEM_DQ;
-            // S_h = Q K_h^T and dP_h = dO V_h^T for the key rows 64h .. 64h+63 of stage st
-            auto issue_sdp = [&](int h, int st) {
-                const uint32_t sk = s_k + st * C::TB + h * HALF * 128, sv = s_v + st * C::TB + h * HALF * 128;
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);  // [128 x 128] = A[128 x d] . B[128 x d]^T
+            constexpr uint32_t idesc_q = idesc_bf16_f32(BT, D, true);    // dQ += dS (tensor memory) . K (MN-major)
+            const uint32_t t_dq = tmem + C::TMEM_DQ;
+            auto issue_s = [&](int n) {  // S(n) = Q K(n)^T
+                const uint32_t sk = s_k + (n % 3) * C::TB, d = tmem + region_s(n);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_s + h * HALF, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024), idesc_h,
-                           k > 0);
+                    mma_ss(d, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024), idesc_s, k > 0);
                 }
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_dp + h * HALF, sdesc_sw128(s_do + off, 16, 1024), sdesc_sw128(sv + off, 16, 1024),
-                           idesc_h, k > 0);
-                }
-                mma_commit(bar(Q_HFULL + h));
+                mma_commit(bar(Q_SFULL + (n & 1)));
             };
-            // dQ += dS_h K_h (64 keys: four K=16 steps)
-            auto issue_dq = [&](int h, int st, bool first) {
-                const uint32_t sk = s_k + st * C::TB;
+            auto issue_dp = [&](int n) {  // dP(n) = dO V(n)^T
+                const uint32_t sv = s_v + (n & 1) * C::TB, d = tmem + region_dp(n);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(d, sdesc_sw128(s_do + off, 16, 1024), sdesc_sw128(sv + off, 16, 1024), idesc_s, k > 0);
+                }
+                mma_commit(bar(Q_DPFULL));
+                mma_commit(bar(Q_VEMPTY + (n & 1)));
+            };
+            auto issue_dq = [&](int n, int h) {  // dQ += dS_h(n) K_h(n) (64 keys: four K=16 steps)
+                const uint32_t sk = s_k + (n % 3) * C::TB, a_t = tmem + region_dp(n) + h * HALF;
 #pragma unroll
                 for (int k = 0; k < HALF / 16; ++k)
-                    mma_ts(t_dq, t_dp + h * HALF + k * 8, sdesc_sw128(sk + (h * HALF + k * 16) * 128, C::SUB, 1024),
-                           idesc_q, (first && k == 0) ? 0u : 1u);
+                    mma_ts(t_dq, a_t + k * 8, sdesc_sw128(sk + (h * HALF + k * 16) * 128, C::SUB, 1024), idesc_q,
+                           (n == 0 && h == 0 && k == 0) ? 0u : 1u);
             };
-            bool ok = wait_bounded(bar(Q_LOAD), 0, wd, ERR_MMA) && wait_bounded(bar(Q_FULL), 0, wd, ERR_MMA);
+            bool ok = wait_bounded(bar(Q_LOAD), 0, wd, ERR_MMA) && wait_bounded(bar(Q_KFULL), 0, wd, ERR_MMA);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                issue_sdp(1, 0);
+                issue_s(0);
+                ok = wait_bounded(bar(Q_VFULL), 0, wd, ERR_MMA);
+            }
+            if (ok) {
+                tc_fence_after();
+                issue_dp(0);
+                if (n_iter > 1 && (ok = wait_bounded(bar(Q_KFULL + 1), 0, wd, ERR_MMA))) {
+                    tc_fence_after();
+                    issue_s(1);
+                }
             }
             for (int it = 0; it < n_iter && ok; ++it) {
-                const int st = it & 1;
-                const bool more = it + 1 < n_iter;
                 if (!(ok = wait_bounded(bar(Q_HDONE), it & 1, wd, ERR_MMA))) break;
                 tc_fence_after();
-                issue_dq(0, st, it == 0);
-                if (more) {
-                    if (!(ok = wait_bounded(bar(Q_FULL + (st ^ 1)), ((it + 1) >> 1) & 1, wd, ERR_MMA))) break;
-                    tc_fence_after();
-                    issue_sdp(0, st ^ 1);
-                }
+                issue_dq(it, 0);
                 if (!(ok = wait_bounded(bar(Q_HDONE + 1), it & 1, wd, ERR_MMA))) break;
                 tc_fence_after();
-                issue_dq(1, st, false);
-                mma_commit(bar(Q_EMPTY + st));
-                if (more) issue_sdp(1, st ^ 1);
+                issue_dq(it, 1);
+                mma_commit(bar(Q_KEMPTY + it % 3));
+                if (it + 1 < n_iter) {
+                    const int n1 = it + 1;
+                    if (!(ok = wait_bounded(bar(Q_VFULL + (n1 & 1)), (n1 >> 1) & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_dp(n1);
+                }
+                if (it + 2 < n_iter) {
+                    const int n2 = it + 2;
+                    if (!(ok = wait_bounded(bar(Q_KFULL + n2 % 3), (n2 / 3) & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_s(n2);
+                }
             }
             if (ok) mma_commit(bar(Q_DONE));
             if (sh->abort) {
@@ -388,20 +406,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
         const int wg = warp >> 2, r = (warp & 3) * 32 + lane;
         const long i = (long)q_tile * BT + r;
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t t_s = t_lane + C::TMEM_S, t_dp = t_lane + C::TMEM_DP;
-        const float nlse = p.nlse2[(size_t)bh * p.S_pad + i];
-        const float nd = p.nd[(size_t)bh * p.S_pad + i];
+        const RowConst nl{p.nlse2[(size_t)bh * p.S_pad + i]}, nd{p.nd[(size_t)bh * p.S_pad + i]};
         const float sl2 = p.scale_log2;
         long lo, hi;
         row_band(p.kind, p.window, p.S, i, &lo, &hi);
+        float pv[64];
         for (int it = 0; it < n_iter; ++it) {
-            wait_bounded(bar(Q_HFULL + wg), it & 1, wd, ERR_COMPUTE);
-            tc_fence_after();
             const int t = kv_begin + it;
             int a0, a1;
             tile_interval(lo, hi, (long)t * BT, &a0, &a1);
-            if (t < full_begin || t >= full_end) dq_half<true>(t_s, t_dp, wg, sl2, nlse, nd, a0, a1);
-            else dq_half<false>(t_s, t_dp, wg, sl2, nlse, nd, a0, a1);
+            wait_bounded(bar(Q_SFULL + (it & 1)), (it >> 1) & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            if (t < full_begin || t >= full_end) exp_pass<true, false>(t_lane + region_s(it), wg, sl2, nl, a0, a1, pv);
+            else exp_pass<false, false>(t_lane + region_s(it), wg, sl2, nl, a0, a1, pv);
+            wait_bounded(bar(Q_DPFULL), it & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            ds_pass(t_lane + region_dp(it), wg, nd, pv);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(Q_HDONE + wg));
@@ -427,6 +447,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
 }
 
 // ------------------------------------------------------------------ dK / dV kernel
+// Per (head, query tile) iteration n the MMA thread issues
+//     S^T(n) | dP^T(n) | dV_0(n) dV_1(n) | S^T(n+1) | dK_0(n) dK_1(n) | dP^T(n+1) | ...
+// dV_h needs warpgroup h's P^T (its exp step), dK_h its dS^T (its dS step).  S^T(n+1) may
+// overwrite the S^T columns once both dV halves are issued (they read P^T from there), and
+// dP^T(n+1) the dP^T columns once both dK halves are; so the exp step of tile n+1 overlaps
+// dK(n) and dP^T(n+1) on the tensor core.
 template <int D>
 struct KvCfg {
     static constexpr int TB = BT * D * 2;
@@ -442,8 +468,9 @@ struct KvCfg {
     static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DV = 256, TMEM_DK = 256 + D;
 };
 
-enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_HFULL = KV_QEMPTY + 2, KV_HDONE = KV_HFULL + 2,
-             KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
+enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMPTY + 2, KV_DPFULL, KV_PDONE,
+             KV_HDONE = KV_PDONE + 2, KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
+static_assert(KV_NBAR <= 24, "barrier slots");
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -468,7 +495,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
     auto iter_qtile = [&](int it) { return q_begin + it % n_q; };
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < KV_NBAR; ++i) mbar_init(bar(i), (i == KV_HDONE || i == KV_HDONE + 1) ? 128u : 1u);
+        for (int i = 0; i < KV_NBAR; ++i) {
+            const bool wg_bar = i == KV_PDONE || i == KV_PDONE + 1 || i == KV_HDONE || i == KV_HDONE + 1;
+            mbar_init(bar(i), wg_bar ? 128u : 1u);
+        }
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -512,61 +542,63 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
         }
     } else if (warp == WARP_MMA) {
         if (lane == 0) {
-            constexpr uint32_t idesc_h = idesc_bf16_f32(BT, HALF, false);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(BT, BT, false);
             constexpr uint32_t idesc_kv = idesc_bf16_f32(BT, D, true);  // dV, dK += (tensor memory) . (MN-major)
             const uint32_t t_s = tmem + C::TMEM_S, t_dp = tmem + C::TMEM_DP;
             const uint32_t t_dv = tmem + C::TMEM_DV, t_dk = tmem + C::TMEM_DK;
-            // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for the query rows 64h .. 64h+63 of stage st
-            auto issue_sdp = [&](int h, int st) {
-                const uint32_t sq = s_q + st * C::TB + h * HALF * 128, sdo = s_do + st * C::TB + h * HALF * 128;
+            auto issue_s = [&](int n) {  // S^T(n) = K Q(n)^T
+                const uint32_t sq = s_q + (n & 1) * C::TB;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_s + h * HALF, sdesc_sw128(s_k + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idesc_h,
-                           k > 0);
+                    mma_ss(t_s, sdesc_sw128(s_k + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), idesc_s, k > 0);
                 }
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
-                    mma_ss(t_dp + h * HALF, sdesc_sw128(s_v + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024),
-                           idesc_h, k > 0);
-                }
-                mma_commit(bar(KV_HFULL + h));
+                mma_commit(bar(KV_SFULL));
             };
-            // dV += P^T_h dO_h and dK += dS^T_h Q_h (64 query rows: four K=16 steps each)
-            auto issue_kv = [&](int h, int st, bool first) {
-                const uint32_t sq = s_q + st * C::TB, sdo = s_do + st * C::TB;
+            auto issue_dp = [&](int n) {  // dP^T(n) = V dO(n)^T
+                const uint32_t sdo = s_do + (n & 1) * C::TB;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    mma_ss(t_dp, sdesc_sw128(s_v + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), idesc_s, k > 0);
+                }
+                mma_commit(bar(KV_DPFULL));
+            };
+            // acc += (tensor-memory operand of half h) . (rows 64h .. 64h+63 of the stage's tile, MN-major)
+            auto issue_half = [&](uint32_t acc, uint32_t a_t, uint32_t tile, int h, bool first) {
 #pragma unroll
                 for (int k = 0; k < HALF / 16; ++k)
-                    mma_ts(t_dv, t_s + h * HALF + k * 8, sdesc_sw128(sdo + (h * HALF + k * 16) * 128, C::SUB, 1024),
-                           idesc_kv, (first && k == 0) ? 0u : 1u);
-#pragma unroll
-                for (int k = 0; k < HALF / 16; ++k)
-                    mma_ts(t_dk, t_dp + h * HALF + k * 8, sdesc_sw128(sq + (h * HALF + k * 16) * 128, C::SUB, 1024),
+                    mma_ts(acc, a_t + h * HALF + k * 8, sdesc_sw128(tile + (h * HALF + k * 16) * 128, C::SUB, 1024),
                            idesc_kv, (first && k == 0) ? 0u : 1u);
             };
             bool ok = wait_bounded(bar(KV_LOAD), 0, wd, ERR_MMA) && wait_bounded(bar(KV_QFULL), 0, wd, ERR_MMA);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0, 0);
-                issue_sdp(1, 0);
+                issue_s(0);
+                issue_dp(0);
             }
             for (int it = 0; it < n_iter && ok; ++it) {
                 const int st = it & 1;
-                const bool more = it + 1 < n_iter;
-                if (!(ok = wait_bounded(bar(KV_HDONE), it & 1, wd, ERR_MMA))) break;
-                tc_fence_after();
-                issue_kv(0, st, it == 0);
-                if (more) {
+                const uint32_t sq = s_q + st * C::TB, sdo = s_do + st * C::TB;
+                for (int h = 0; h < 2 && ok; ++h) {  // dV += P^T_h dO_h
+                    if (!(ok = wait_bounded(bar(KV_PDONE + h), it & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_half(t_dv, t_s, sdo, h, it == 0 && h == 0);
+                }
+                if (!ok) break;
+                if (it + 1 < n_iter) {
                     if (!(ok = wait_bounded(bar(KV_QFULL + (st ^ 1)), ((it + 1) >> 1) & 1, wd, ERR_MMA))) break;
                     tc_fence_after();
-                    issue_sdp(0, st ^ 1);
+                    issue_s(it + 1);
                 }
-                if (!(ok = wait_bounded(bar(KV_HDONE + 1), it & 1, wd, ERR_MMA))) break;
-                tc_fence_after();
-                issue_kv(1, st, false);
+                for (int h = 0; h < 2 && ok; ++h) {  // dK += dS^T_h Q_h
+                    if (!(ok = wait_bounded(bar(KV_HDONE + h), it & 1, wd, ERR_MMA))) break;
+                    tc_fence_after();
+                    issue_half(t_dk, t_dp, sq, h, it == 0 && h == 0);
+                }
+                if (!ok) break;
                 mma_commit(bar(KV_QEMPTY + st));
-                if (more) issue_sdp(1, st ^ 1);
+                if (it + 1 < n_iter) issue_dp(it + 1);
             }
             if (ok) mma_commit(bar(KV_DONE));
             if (sh->abort) {
@@ -584,17 +616,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
         long ilo, ihi;
         key_band(p.kind, p.window, p.S, j, &ilo, &ihi);
         if (j >= p.S) { ilo = 1; ihi = 0; }  // a padding key sees no row
+        float pv[64];
         for (int it = 0; it < n_iter; ++it) {
             const int st = it & 1, qt = iter_qtile(it);
-            wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
-            wait_bounded(bar(KV_HFULL + wg), it & 1, wd, ERR_COMPUTE);
-            tc_fence_after();
             int a0, a1;
             tile_interval(ilo, ihi, (long)qt * BT, &a0, &a1);
-            const float* vl = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
-            const float* vd = vl + BT;
-            if (qt < full_begin || qt >= full_end) kv_half<true>(t_s, t_dp, wg, sl2, vl, vd, a0, a1);
-            else kv_half<false>(t_s, t_dp, wg, sl2, vl, vd, a0, a1);
+            const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
+            wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
+            wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            if (qt < full_begin || qt >= full_end) exp_pass<true, true>(t_s, wg, sl2, ColVec{vec}, a0, a1, pv);
+            else exp_pass<false, true>(t_s, wg, sl2, ColVec{vec}, a0, a1, pv);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(KV_PDONE + wg));
+            wait_bounded(bar(KV_DPFULL), it & 1, wd, ERR_COMPUTE);
+            tc_fence_after();
+            ds_pass(t_dp, wg, ColVec{vec + BT}, pv);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(KV_HDONE + wg));
