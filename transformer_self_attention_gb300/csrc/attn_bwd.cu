@@ -184,11 +184,18 @@ __device__ __forceinline__ float masked(uint32_t raw, int c, int a0, int a1) {
 // come in through NL / ND.
 struct RowConst {  // one value for every column: the thread's own query row
     float v;
-    __device__ __forceinline__ float2 pair(int) const { return make_float2(v, v); }
+    __device__ __forceinline__ float4 quad(int) const { return make_float4(v, v, v, v); }
 };
-struct ColVec {  // one value per column, from a shared-memory vector of 128 floats
-    const float* v;
-    __device__ __forceinline__ float2 pair(int c) const { return *reinterpret_cast<const float2*>(v + c); }
+struct ColVec {  // one value per column, from a 16-byte aligned shared-memory vector of 128 floats;
+                 // every lane reads the same 16 bytes (one broadcast wavefront per 4 columns)
+    uint32_t v;  // shared-memory address
+    __device__ __forceinline__ float4 quad(int c) const {
+        float4 r;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                     : "r"(v + 4u * (uint32_t)c));
+        return r;
+    }
 };
 
 template <bool MASKED, bool STORE_P, class NL>
@@ -201,13 +208,19 @@ __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, 
         tmem_ld32(t_s + cb, s);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 16; e += 2) {
             const int c = cb + 2 * e;
-            const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[2 * e], c, a0, a1),
-                                                    masked<MASKED>(s[2 * e + 1], c + 1, a0, a1)), sl, nl.pair(c));
-            pv[ch * 32 + 2 * e] = ex2(x.x);
-            pv[ch * 32 + 2 * e + 1] = ex2(x.y);
-            if (STORE_P) pk[e] = pack_bf16x2(pv[ch * 32 + 2 * e], pv[ch * 32 + 2 * e + 1]);
+            const float4 n4 = nl.quad(c);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int k = 2 * (e + u);
+                const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cb + k, a0, a1),
+                                                        masked<MASKED>(s[k + 1], cb + k + 1, a0, a1)),
+                                            sl, u ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y));
+                pv[ch * 32 + k] = ex2(x.x);
+                pv[ch * 32 + k + 1] = ex2(x.y);
+                if (STORE_P) pk[e + u] = pack_bf16x2(pv[ch * 32 + k], pv[ch * 32 + k + 1]);
+            }
         }
         if (STORE_P) tmem_st16(t_s + h * HALF + ch * 16, pk);
     }
@@ -222,11 +235,16 @@ __device__ __forceinline__ void ds_pass(uint32_t t_dp, int h, ND nd, const float
         tmem_ld32(t_dp + cb, g);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int c = cb + 2 * e;
-            const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), nd.pair(c));
-            const float2 ds = __fmul2_rn(make_float2(pv[ch * 32 + 2 * e], pv[ch * 32 + 2 * e + 1]), dd);
-            pk[e] = pack_bf16x2(ds.x, ds.y);
+        for (int e = 0; e < 16; e += 2) {
+            const float4 n4 = nd.quad(cb + 2 * e);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int k = 2 * (e + u);
+                const float2 dd = __fadd2_rn(make_float2(__uint_as_float(g[k]), __uint_as_float(g[k + 1])),
+                                             u ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y));
+                const float2 ds = __fmul2_rn(make_float2(pv[ch * 32 + k], pv[ch * 32 + k + 1]), dd);
+                pk[e + u] = pack_bf16x2(ds.x, ds.y);
+            }
         }
         tmem_st16(t_dp + h * HALF + ch * 16, pk);
     }
@@ -621,7 +639,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
             const int st = it & 1, qt = iter_qtile(it);
             int a0, a1;
             tile_interval(ilo, ihi, (long)qt * BT, &a0, &a1);
-            const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
+            const uint32_t vec = s_vec + st * 1024;  // -LSE log2 e of the tile's 128 query rows, then -D
             wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
             wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
@@ -632,7 +650,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
             mbar_arrive(bar(KV_PDONE + wg));
             wait_bounded(bar(KV_DPFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            ds_pass(t_dp, wg, ColVec{vec + BT}, pv);
+            ds_pass(t_dp, wg, ColVec{vec + 4 * BT}, pv);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(KV_HDONE + wg));
