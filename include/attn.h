@@ -186,6 +186,18 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
 attn_status attn_kv_schedule_host(int S, attn_mask_kind kind, int window, int* items, int cap, int* n_items);
 
 /*
+ * attn_bwd_dq_schedule_host -- the work items of the backward's dQ launch (host only):
+ * the first-launch items of attn_schedule_host for these arguments (no global tokens),
+ * stably regrouped so that the items of the kv heads whose K and V fit in 32 MB
+ * (kv_group = max(1, 32 MiB / (4 S d_k)) heads) run together, group by group in
+ * (batch, kv head) order; within a group the forward's longest-first order is kept.
+ * items may be NULL with cap = 0 to query the count.
+ * Errors: ATTN_ERR_INVALID_ARG (bad shape, LOCAL_GLOBAL, cap too small).
+ */
+attn_status attn_bwd_dq_schedule_host(int B, int Hq, int Hkv, int S, int d_k, attn_mask_kind kind, int window,
+                                      int* items, int cap, int* n_items);
+
+/*
  * attn_poll_device_error -- synchronise the device, read the handle's device
  * error word into *code (0 = none, otherwise a bit set of the role whose
  * bounded wait ran out), clear it, and return ATTN_ERR_DEVICE_TIMEOUT if it

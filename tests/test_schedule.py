@@ -199,3 +199,23 @@ def test_kv_schedule_rejects_local_global():
     with pytest.raises(tsa.AttnError) as e:
         tsa.attn_kv_schedule_host(300, tsa.MASK_LOCAL_GLOBAL, 5)
     assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,d,kind,w", [(2, 32, 32, 4096, 128, tsa.MASK_CAUSAL, 0),
+                                                (1, 32, 8, 16384, 128, tsa.MASK_CAUSAL_SLIDING, 4095),
+                                                (1, 64, 8, 32768, 128, tsa.MASK_CAUSAL, 0),
+                                                (3, 6, 2, 300, 64, tsa.MASK_SLIDING, 40),
+                                                (2, 4, 1, 129, 128, tsa.MASK_FULL, 0)])
+def test_bwd_dq_order_is_a_grouped_permutation(B, Hq, Hkv, S, d, kind, w):
+    """The dQ launch runs the forward's first-launch items, each once, grouped by kv head so that
+    about 32 MB of K and V is live at a time, and in the forward's order within a group."""
+    fwd, n_first = tsa.attn_schedule_host(B, Hq, Hkv, S, kind, w)
+    fwd = fwd[:n_first]
+    dq = tsa.attn_bwd_dq_schedule_host(B, Hq, Hkv, S, d, kind, w)
+    assert sorted(map(tuple, dq.tolist())) == sorted(map(tuple, fwd.tolist()))
+    kv_group = max(1, (32 << 20) // (4 * S * d))
+    key = lambda it: ((it[0] // Hq) * Hkv + (it[0] % Hq) // (Hq // Hkv)) // kv_group
+    keys = [key(it) for it in dq.tolist()]
+    assert keys == sorted(keys)
+    for k in set(keys):
+        assert [it for it in dq.tolist() if key(it) == k] == [it for it in fwd.tolist() if key(it) == k]

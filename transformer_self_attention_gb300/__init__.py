@@ -30,7 +30,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
-            "attn_backward")
+            "attn_backward", "attn_bwd_dq_schedule_host")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -72,6 +72,8 @@ def _load():
     lib.attn_kv_schedule_host.restype = I
     lib.attn_backward.argtypes = [P] * 11
     lib.attn_backward.restype = I
+    lib.attn_bwd_dq_schedule_host.argtypes = [I, I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
+    lib.attn_bwd_dq_schedule_host.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -196,6 +198,20 @@ def attn_kv_schedule_host(S, kind, window=0):
                                     ctypes.byref(n))
     if st != ATTN_OK:
         raise AttnError(st, "attn_kv_schedule_host")
+    return items[: n.value]
+
+
+def attn_bwd_dq_schedule_host(B, Hq, Hkv, S, d_k, kind, window=0):
+    """Work items of the backward's dQ launch (host only): int32 [n, 8].  Raises AttnError."""
+    n = ctypes.c_int(0)
+    args = (int(B), int(Hq), int(Hkv), int(S), int(d_k), int(kind), int(window))
+    st = _lib.attn_bwd_dq_schedule_host(*args, None, 0, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_dq_schedule_host")
+    items = np.zeros((max(n.value, 1), WORK_INTS), dtype=np.int32)
+    st = _lib.attn_bwd_dq_schedule_host(*args, items.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_dq_schedule_host")
     return items[: n.value]
 
 

@@ -38,6 +38,7 @@ struct attn_plan {
     float* d_lse2 = nullptr;   // [B*Hq, S_pad]
     float* d_dvec = nullptr;   // [B*Hq, S_pad]
     int4* d_kvwork = nullptr;  // key-tile items
+    int4* d_dqwork = nullptr;  // forward items regrouped by kv head (dQ launch)
     int n_kv_items = 0;
     const void* last_bwd[7] = {};
     attn::BwdParams bp{};
@@ -134,7 +135,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 void free_plan(attn_plan* h) {
     if (!h) return;
     void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part,
-                    h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork};
+                    h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork};
     for (void* b : bufs)
         if (b) cudaFree(b);
     delete h;
@@ -356,6 +357,25 @@ attn_status attn_kv_schedule_host(int S, attn_mask_kind kind, int window, int* i
     return ATTN_OK;
 }
 
+attn_status attn_bwd_dq_schedule_host(int B, int Hq, int Hkv, int S, int d_k, attn_mask_kind kind, int window,
+                                      int* items, int cap, int* n_items) {
+    if (!n_items || cap < 0 || (cap > 0 && !items)) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || S < 1 || S > (1 << 20) || d_k < 1) return ATTN_ERR_INVALID_ARG;
+    if ((int)kind < ATTN_MASK_FULL || (int)kind >= ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_INVALID_ARG;
+    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING;
+    if (windowed && window < 0) return ATTN_ERR_INVALID_ARG;
+    attn::ScheduleInput in{B, Hq, Hkv, S, (int)kind, windowed ? window : 0, {}};
+    attn::Schedule sched;
+    attn_status st = attn::build_schedule(in, &sched);
+    if (st != ATTN_OK) return st;
+    const std::vector<int> v = attn::order_dq_items(sched.items, sched.n_main, Hq, Hkv, attn::dq_kv_group(S, d_k));
+    *n_items = sched.n_main;
+    if (cap == 0) return ATTN_OK;
+    if (cap < *n_items) return ATTN_ERR_INVALID_ARG;
+    std::memcpy(items, v.data(), v.size() * sizeof(int));
+    return ATTN_OK;
+}
+
 attn_status attn_poll_device_error(attn_handle h, int* code) {
     if (!h || !code) return ATTN_ERR_INVALID_ARG;
     *code = 0;
@@ -411,9 +431,12 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
         attn_status st = attn::build_kv_schedule(h->S, h->kind, h->window, &items);
         if (st != ATTN_OK) return st;
         h->n_kv_items = (int)(items.size() / ATTN_WORK_INTS);
+        const std::vector<int> dq_items = attn::order_dq_items(h->sched.items, h->sched.n_main, h->Hq, h->Hkv,
+                                                               attn::dq_kv_group(h->S, h->d));
         if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_lse2), n * sizeof(float))) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&h->d_dvec), n * sizeof(float))) != cudaSuccess ||
-            (e = upload(reinterpret_cast<int**>(&h->d_kvwork), items.data(), items.size())) != cudaSuccess)
+            (e = upload(reinterpret_cast<int**>(&h->d_kvwork), items.data(), items.size())) != cudaSuccess ||
+            (e = upload(reinterpret_cast<int**>(&h->d_dqwork), dq_items.data(), dq_items.size())) != cudaSuccess)
             return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
         p.S = h->S; p.S_pad = S_pad; p.Hq = h->Hq; p.Hkv = h->Hkv; p.group = h->Hq / h->Hkv;
         p.kind = h->kind; p.window = h->window;
@@ -439,7 +462,7 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     pp.nlse2 = h->d_lse2; pp.nd = h->d_dvec;
     pp.BHq = (int)BHq; pp.S = h->S; pp.S_pad = S_pad; pp.d = h->d;
     if ((e = attn::launch_bwd_prep(pp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-    p.work = h->d_work;  // the forward's first-launch items: one per (batch x head, query tile)
+    p.work = h->d_dqwork;  // the forward's first-launch items, grouped by kv head
     if ((e = attn::launch_bwd_dq(p, h->d, h->sched.n_main, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     p.work = h->d_kvwork;
     p.n_items = h->n_kv_items;

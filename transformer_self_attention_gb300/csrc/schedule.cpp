@@ -212,6 +212,27 @@ attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* ite
     return ATTN_OK;
 }
 
+int dq_kv_group(int S, int d_k) {
+    const long per_head = 2L * S * d_k * 2;  // K and V of one kv head, bf16
+    return (int)std::max(1L, std::min(1L << 20, (32L << 20) / std::max(1L, per_head)));
+}
+
+std::vector<int> order_dq_items(const std::vector<int>& items, int n_items, int Hq, int Hkv, int kv_group) {
+    const int group = Hq / Hkv;
+    auto key = [&](int k) {
+        const int bh = items[(size_t)k * ATTN_WORK_INTS];
+        return ((bh / Hq) * Hkv + (bh % Hq) / group) / kv_group;
+    };
+    std::vector<int> order(n_items);
+    for (int k = 0; k < n_items; ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return key(x) < key(y); });
+    std::vector<int> out;
+    out.reserve((size_t)n_items * ATTN_WORK_INTS);
+    for (int k : order) out.insert(out.end(), items.begin() + (size_t)k * ATTN_WORK_INTS,
+                                   items.begin() + (size_t)(k + 1) * ATTN_WORK_INTS);
+    return out;
+}
+
 void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi) {
     *lo = kind == ATTN_MASK_CAUSAL_SLIDING ? std::max(0, L - S_q - window) / T : 0;
     *hi = (L + T - 1) / T;

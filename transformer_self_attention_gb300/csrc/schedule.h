@@ -44,6 +44,14 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out);
 // Returns ATTN_ERR_UNSUPPORTED for LOCAL_GLOBAL.
 attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* items);
 
+// Backward (dQ): the first-launch forward items (one per (batch x query head, query tile))
+// reordered so that the items of about 32 MB worth of key/value heads run together (their
+// K and V stay in L2): stable sort by (batch, kv head) / kv_group, where kv_group is the
+// number of kv heads whose K and V (2 S d_k bf16 each) fit in 32 MB.  Longest first within
+// a group, as in the forward order.
+int dq_kv_group(int S, int d_k);
+std::vector<int> order_dq_items(const std::vector<int>& items, int n_items, int Hq, int Hkv, int kv_group);
+
 // Decode: key tiles per sequence and the size of the persistent grid
 // (see attn_decode_schedule_host).
 struct DecodeSchedule {
