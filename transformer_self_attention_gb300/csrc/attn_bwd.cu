@@ -112,35 +112,61 @@ __device__ __forceinline__ void tile_interval(long lo, long hi, long c0, int* a0
 }
 
 // ------------------------------------------------------------------ pre-pass
-__global__ void bwd_prep_kernel(BwdPrepParams p) {
+// -D_i = -dO_i . O_i and -LSE_i log2 e for every row, padded to whole tiles (padding rows:
+// -inf and 0, so their P is 0).  A row is d/8 lanes reading 16 bytes each of O and dO; a warp
+// handles PREP_ROUNDS groups of 32/(d/8) rows, with every load issued before the reductions.
+constexpr int PREP_ROUNDS = 4;
+constexpr int PREP_WARPS = 8;
+
+__global__ void __launch_bounds__(PREP_WARPS * 32) bwd_prep_kernel(BwdPrepParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long row = (long)blockIdx.x * 8 + warp;  // over B*Hq*S_pad
-    if (row >= (long)p.BHq * p.S_pad) return;
-    const long bh = row / p.S_pad, i = row - bh * p.S_pad;
-    if (i >= p.S) {
-        if (lane == 0) {
-            p.nlse2[row] = -INFINITY;  // padding rows: P = 0
-            p.nd[row] = 0.f;
+    const int L = p.d >> 3, rows_per_round = 32 / L;  // d = 64 or 128: 8 or 16 lanes per row
+    const int sub = lane / L, lc = lane - sub * L;
+    const long total = (long)p.BHq * p.S_pad;
+    const long row0 = ((long)blockIdx.x * PREP_WARPS + warp) * (PREP_ROUNDS * rows_per_round);
+    float acc[PREP_ROUNDS];
+    uint4 o4[PREP_ROUNDS], g4[PREP_ROUNDS];
+#pragma unroll
+    for (int r = 0; r < PREP_ROUNDS; ++r) {
+        const long row = row0 + r * rows_per_round + sub;
+        o4[r] = g4[r] = make_uint4(0, 0, 0, 0);
+        if (row < total) {
+            const long bh = row / p.S_pad, i = row - bh * p.S_pad;
+            if (i < p.S) {
+                const long src = (bh * p.S + i) * p.d + lc * 8;
+                o4[r] = *reinterpret_cast<const uint4*>(p.o + src);
+                g4[r] = *reinterpret_cast<const uint4*>(p.dout + src);
+            }
         }
-        return;
     }
-    const long src = (bh * p.S + i) * p.d;
-    float acc = 0.f;
-    for (int c = lane * 8; c < p.d; c += 32 * 8) {
-        const uint4 o4 = *reinterpret_cast<const uint4*>(p.o + src + c);
-        const uint4 g4 = *reinterpret_cast<const uint4*>(p.dout + src + c);
-        const uint32_t ow[4] = {o4.x, o4.y, o4.z, o4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+    for (int r = 0; r < PREP_ROUNDS; ++r) {
+        const uint32_t ow[4] = {o4[r].x, o4[r].y, o4[r].z, o4[r].w}, gw[4] = {g4[r].x, g4[r].y, g4[r].z, g4[r].w};
+        float a = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            acc = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), acc);
-            acc = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), acc);
+            a = fmaf(__uint_as_float(ow[e] << 16), __uint_as_float(gw[e] << 16), a);
+            a = fmaf(__uint_as_float(ow[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), a);
         }
+        acc[r] = a;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-        p.nd[row] = -acc;
-        p.nlse2[row] = -p.lse[bh * p.S + i] * LOG2E;
+    for (int r = 0; r < PREP_ROUNDS; ++r)
+        for (int off = L >> 1; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+    if (lc == 0) {
+#pragma unroll
+        for (int r = 0; r < PREP_ROUNDS; ++r) {
+            const long row = row0 + r * rows_per_round + sub;
+            if (row >= total) continue;
+            const long bh = row / p.S_pad, i = row - bh * p.S_pad;
+            if (i < p.S) {
+                p.nd[row] = -acc[r];
+                p.nlse2[row] = -p.lse[bh * p.S + i] * LOG2E;
+            } else {
+                p.nd[row] = 0.f;
+                p.nlse2[row] = -INFINITY;
+            }
+        }
     }
 }
 
@@ -688,8 +714,10 @@ cudaError_t configure(F kernel, int smem) {
 }  // namespace
 
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
+    if (p.d != 64 && p.d != 128) return cudaErrorInvalidValue;
     const long rows = (long)p.BHq * p.S_pad;
-    bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
+    const long per_block = (long)PREP_WARPS * PREP_ROUNDS * (32 / (p.d / 8));
+    bwd_prep_kernel<<<(unsigned)((rows + per_block - 1) / per_block), PREP_WARPS * 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
