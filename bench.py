@@ -514,7 +514,8 @@ def run_ours_backward(args, w):
     achieved = useful / (mean_ms * 1e-3) / 1e12
     peak = float(pk["bf16_tflops"])
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": f"{pk_src} bf16_tflops (burst, cuBLAS)",
+                "traffic": ncu_traffic(w.name, "attn_bwd", BWD_KERNEL_SOURCES),
+                "peak_source": f"{pk_src} bf16_tflops (burst, cuBLAS)",
                 "kernel": "the whole backward step (bwd_prep + attn_bwd_dq + attn_bwd_dkdv)"}
     line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
