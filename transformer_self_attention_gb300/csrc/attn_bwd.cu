@@ -297,6 +297,14 @@ struct DqCfg {
     static constexpr uint32_t TMEM_DQ = 384;
 };
 
+// Barriers and why no wait can fall two phases behind (a parity wait would then hang):
+//   Q_KFULL[n%3] / Q_KEMPTY[n%3], Q_VFULL[n&1] / Q_VEMPTY[n&1]: rings; a stage is refilled only after
+//       its empty barrier completed for the tile two (V) or three (K) back.
+//   Q_SFULL[n&1]: S(n+2) is issued only after the dQ update of tile n, i.e. after both warpgroups
+//       arrived on Q_HDONE for n; alternating two barriers keeps S(n+1) and S(n+2) on different ones.
+//   Q_DPFULL: dP(n+1) is issued only after Q_HDONE(n), so the warps wait at most one phase back.
+//   Q_HDONE[h] (128 arrivals): the warpgroup arrives for n+1 only after Q_DPFULL(n+1), which the MMA
+//       thread commits after it has seen Q_HDONE(n).
 enum DqBar { Q_LOAD = 0, Q_KFULL, Q_KEMPTY = Q_KFULL + 3, Q_VFULL = Q_KEMPTY + 3, Q_VEMPTY = Q_VFULL + 2,
              Q_SFULL = Q_VEMPTY + 2, Q_DPFULL = Q_SFULL + 2, Q_HDONE, Q_DONE = Q_HDONE + 2, Q_DRAIN, Q_NBAR };
 static_assert(Q_NBAR <= 24, "barrier slots");
@@ -512,6 +520,13 @@ struct KvCfg {
     static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DV = 256, TMEM_DK = 256 + D;
 };
 
+// Barriers and why no wait can fall two phases behind:
+//   KV_QFULL[n&1] / KV_QEMPTY[n&1]: a Q/dO/vector stage is refilled only after the dK update of the
+//       tile two back, which needs both warpgroups' KV_HDONE for it.
+//   KV_SFULL: S^T(n+1) is issued only after both KV_PDONE(n); KV_DPFULL: dP^T(n+1) only after both
+//       KV_HDONE(n).  A warpgroup waits for either at most one phase back.
+//   KV_PDONE[h] / KV_HDONE[h] (128 arrivals each): arrivals for n+1 need KV_SFULL(n+1) / KV_DPFULL(n+1),
+//       which the MMA thread commits after it has seen the arrivals for n.
 enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMPTY + 2, KV_DPFULL, KV_PDONE,
              KV_HDONE = KV_PDONE + 2, KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
 static_assert(KV_NBAR <= 24, "barrier slots");

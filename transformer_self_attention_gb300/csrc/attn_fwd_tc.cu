@@ -591,7 +591,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         tc_fence_after();
         ok = named_bar_and(1, 128, ok);  // the same decision in all four softmax warps
         if (ok) {
-            const float inv_l = l > 0.f ? p.o_scale / l : 0.f;  // o_scale: the V descale of E4M3 inputs
+            // o_scale: the V descale of E4M3 inputs (bf16 inputs have none; callers may leave it 0)
+            const float inv_l = l > 0.f ? (F8 ? p.o_scale : 1.f) / l : 0.f;
             const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             if (!grows) {
                 // O row -> bf16 -> 128B-swizzled staging in the (now idle) Q buffer -> TMA store
