@@ -64,6 +64,9 @@ def _load():
             lib.oracle_attention_rows_bias.argtypes = [P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P,
                                                        P, P, P, P, L, P, P]
             lib.oracle_attention_rows_bias.restype = I
+            lib.oracle_attention_rows_general.argtypes = [P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P, P, I,
+                                                          I, L, P, P, P, P, L, P, P]
+            lib.oracle_attention_rows_general.restype = I
             lib.oracle_row_counts.argtypes = [I, I, I, P, I, P]
             lib.oracle_row_counts.restype = I
             lib.oracle_tile_classes.argtypes = [I, I, I, P, I, I, I, P]
@@ -97,12 +100,15 @@ def _slopes(alibi, Hq):
     return a
 
 
-def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row_a, row_i, alibi=None):
+def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row_a, row_i, alibi=None,
+                   bias=None):
     """Oracle outputs for an explicit list of rows.
 
     K, V: float32-castable arrays [B, Hkv, S, d]; Qrows: [n, d] query vectors of
     the rows; row_b / row_a / row_i: [n] batch, query head and position.
     alibi: optional [Hq] slopes m_a of the additive bias -m_a |i - j|.
+    bias: optional float32-castable [Bb, Hb, S, ld] bias matrix added to the scaled
+    scores (Bb in {1, B}, Hb in {1, Hq}: size 1 broadcasts; ld >= S).
     Returns (O [n, d] float64, LSE [n] float64).
     """
     lib = _load()
@@ -119,21 +125,29 @@ def attention_rows(K, V, Hq, scale, kind, window, globals_idx, Qrows, row_b, row
     O = np.empty((n, d), dtype=np.float64)
     LSE = np.empty((n,), dtype=np.float64)
     sl = _slopes(alibi, Hq)
-    rc = lib.oracle_attention_rows_bias(_ptr(K), _ptr(V), B, Hq, Hkv, S, d, float(scale), int(kind),
-                                        int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None,
-                                        _ptr(Qrows), _ptr(rb), _ptr(ra), _ptr(ri), n, _ptr(O), _ptr(LSE))
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        Bb, Hb, Sb, ld = bias.shape
+        assert Sb == S and Bb in (1, B) and Hb in (1, Hq) and ld >= S
+    else:
+        Bb = Hb = 1
+        ld = 0
+    rc = lib.oracle_attention_rows_general(_ptr(K), _ptr(V), B, Hq, Hkv, S, d, float(scale), int(kind),
+                                           int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None,
+                                           _ptr(bias) if bias is not None else None, Bb, Hb, ld,
+                                           _ptr(Qrows), _ptr(rb), _ptr(ra), _ptr(ri), n, _ptr(O), _ptr(LSE))
     if rc != 0:
         raise ValueError("oracle_attention_rows rejected its arguments")
     return O, LSE
 
 
-def attention(Q, K, V, scale, kind, window=0, globals_idx=None, alibi=None):
+def attention(Q, K, V, scale, kind, window=0, globals_idx=None, alibi=None, bias=None):
     """Whole-tensor oracle: Q [B, Hq, S, d], K/V [B, Hkv, S, d] -> (O [B,Hq,S,d], LSE [B,Hq,S]) fp64."""
     Q = np.ascontiguousarray(Q, dtype=np.float32)
     B, Hq, S, d = Q.shape
     bb, aa, ii = np.meshgrid(np.arange(B), np.arange(Hq), np.arange(S), indexing="ij")
     O, LSE = attention_rows(K, V, Hq, scale, kind, window, globals_idx, Q.reshape(-1, d),
-                            bb.ravel(), aa.ravel(), ii.ravel(), alibi=alibi)
+                            bb.ravel(), aa.ravel(), ii.ravel(), alibi=alibi, bias=bias)
     return O.reshape(B, Hq, S, d), LSE.reshape(B, Hq, S)
 
 

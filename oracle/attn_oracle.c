@@ -99,6 +99,14 @@ int oracle_attention_rows_bias(const float* K, const float* V,
                                const float* Qrows, const int* row_b, const int* row_a,
                                const int* row_i, long n,
                                double* O, double* LSE);
+int oracle_attention_rows_general(const float* K, const float* V,
+                                  int B, int Hq, int Hkv, int S, int d,
+                                  double scale, int kind, int window,
+                                  const int* G, int nG, const double* alibi,
+                                  const float* bias, int Bb, int Hb, long ld,
+                                  const float* Qrows, const int* row_b, const int* row_a,
+                                  const int* row_i, long n,
+                                  double* O, double* LSE);
 
 int oracle_attention_rows(const float* K, const float* V,
                           int B, int Hq, int Hkv, int S, int d,
@@ -112,18 +120,6 @@ int oracle_attention_rows(const float* K, const float* V,
                                       Qrows, row_b, row_a, row_i, n, O, LSE);
 }
 
-/*
- * The same with an additive score bias b_ij (alibi == NULL: none):
- *   logits_ij = scale * q_i . k_j + b_ij,   b_ij = -alibi[a] * |i - j|
- * - the additive-bias form: "Transformer 架构及其变体" (aaai.latere.ai), the
- *   unified view of sequence and graph attention, logits = q.k / sqrt(d_k) + b_ij;
- * - ALiBi's distance penalty, -m |i - j| with one fixed slope per head: "Trasformer
- *   浅析" (atffang.github.io), section 线性偏置注意力; written -m_h (i - j) for
- *   j <= i under the causal mask in "Transformer 架构及其变体", section 加性偏置：ALiBi,
- *   which is the same value there.
- * alibi: fp64 [Hq], one slope per query head (the pages give no values; callers
- * pass them).
- */
 int oracle_attention_rows_bias(const float* K, const float* V,
                                int B, int Hq, int Hkv, int S, int d,
                                double scale, int kind, int window,
@@ -132,7 +128,36 @@ int oracle_attention_rows_bias(const float* K, const float* V,
                                const int* row_i, long n,
                                double* O, double* LSE)
 {
+    return oracle_attention_rows_general(K, V, B, Hq, Hkv, S, d, scale, kind, window, G, nG, alibi,
+                                         NULL, 1, 1, 0, Qrows, row_b, row_a, row_i, n, O, LSE);
+}
+
+/*
+ * The same with additive score biases b_ij (alibi == NULL and bias == NULL: none):
+ *   logits_ij = scale * q_i . k_j + b_ij,   b_ij = -alibi[a] * |i - j| + bias[b', a', i, j]
+ * - the additive-bias form: "Transformer 架构及其变体" (aaai.latere.ai), the
+ *   unified view of sequence and graph attention, logits = q.k / sqrt(d_k) + b_ij;
+ * - ALiBi's distance penalty, -m |i - j| with one fixed slope per head: "Trasformer
+ *   浅析" (atffang.github.io), section 线性偏置注意力; written -m_h (i - j) for
+ *   j <= i under the causal mask in "Transformer 架构及其变体", section 加性偏置：ALiBi,
+ *   which is the same value there.
+ * alibi: fp64 [Hq], one slope per query head (the pages give no values; callers
+ * pass them).
+ * bias: a given bias matrix, the general b_ij of the same unified form: fp32
+ * [Bb, Hb, S, ld] with Bb in {1, B} and Hb in {1, Hq} (size 1 = the same for every
+ * batch / query head), ld >= S the row stride; b' = (Bb == 1 ? 0 : b), a' likewise.
+ */
+int oracle_attention_rows_general(const float* K, const float* V,
+                                  int B, int Hq, int Hkv, int S, int d,
+                                  double scale, int kind, int window,
+                                  const int* G, int nG, const double* alibi,
+                                  const float* bias, int Bb, int Hb, long ld,
+                                  const float* Qrows, const int* row_b, const int* row_a,
+                                  const int* row_i, long n,
+                                  double* O, double* LSE)
+{
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 0 || d < 1 || Hq % Hkv != 0) return -1;
+    if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq) || ld < S)) return -1;
     unsigned char* is_global = make_global_flags(S, G, nG);
     if (!is_global) return -1;
     const int group = Hq / Hkv; /* query heads per kv head */
@@ -165,6 +190,10 @@ int oracle_attention_rows_bias(const float* K, const float* V,
                 for (int t = 0; t < d; ++t) dot += (double)q[t] * (double)k[t];
                 s[j] = dot * scale;
                 if (alibi) s[j] -= alibi[a] * (double)labs(i - j);
+                if (bias) {
+                    const size_t plane = (size_t)(Bb == 1 ? 0 : b) * Hb + (Hb == 1 ? 0 : a);
+                    s[j] += (double)bias[(plane * (size_t)S + (size_t)i) * (size_t)ld + (size_t)j];
+                }
                 if (s[j] > m) m = s[j];
             }
             for (int t = 0; t < d; ++t) acc[t] = 0.0;
