@@ -226,6 +226,10 @@ def run_ours(args, w):
     Q, K, V = Qc.to(dev), Kc.to(dev), Vc.to(dev)
     if args.alibi:
         plan.set_alibi(wl.alibi_slopes(w.Hq))
+    if args.bias:  # a per-head bias matrix [1, Hq, S, S], bf16 N(0, 2^2), resident in HBM
+        g = torch.Generator(device="cpu").manual_seed(w.seed + 2)
+        bias = (torch.randn(1, w.Hq, w.S, w.S, generator=g) * 2).to(torch.bfloat16).to(dev)
+        plan.set_bias(bias)
     O = torch.empty(Q.shape, dtype=torch.bfloat16 if args.fp8 else Q.dtype, device=dev)
     LSE = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -326,7 +330,8 @@ def run_ours(args, w):
             "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
                        "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
                        "useful_gflop_per_step": useful / 1e9, "l2": "flushed before every step (256 MiB write)",
-                       "score_bias": "alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
+                       "score_bias": ("alibi, slopes 2^(-8(a+1)/H)" if args.alibi else
+                                      "matrix [1, Hq, S, S] bf16 N(0, 2^2)" if args.bias else "none"),
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_peak": {"measured": 100.0 * achieved / peak, "nominal": 100.0 * achieved / NOMINAL_BF16_TFLOPS,
                             "peak_source": pk_src},
@@ -738,11 +743,15 @@ def main():
                     help="E4M3 Q, K, V with per-tensor scales (prefill workloads; same metric)")
     ap.add_argument("--alibi", action="store_true",
                     help="add the ALiBi score bias with slopes 2^(-8(a+1)/H) (same workload, same metric)")
+    ap.add_argument("--bias", action="store_true",
+                    help="add a per-head bias matrix [1, Hq, S, S] (bf16) to the scores (prefill, bf16)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) of a prefill workload instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.bias and (args.fp8 or args.alibi or args.backward or args.workload not in wl.BY_NAME):
+        ap.error("--bias takes a bf16 prefill workload without --fp8 / --alibi / --backward")
     if args.backward:
         if args.workload not in wl.BY_NAME or args.fp8 or args.alibi:
             ap.error("--backward takes a bf16 prefill workload without --fp8 / --alibi")

@@ -233,6 +233,29 @@ attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
 attn_status attn_set_alibi(attn_handle h, const float* slopes);
 
 /*
+ * attn_set_bias -- add a given bias matrix to the scores of every later attn_forward of
+ * this handle: logits_ij = scale * q_i . k_j + b_ij with b_ij = bias[b', a', i, j], the
+ * general b_ij of the unified biased-logits form ("Transformer 架构及其变体"
+ * (aaai.latere.ai), the unified view of sequence and graph attention: the scaled
+ * scores plus a bias b_ij, of which ALiBi's distance penalty is one instance).
+ *   bias : DEVICE bf16 tensor [Bb, Hb, S, ld], 16-byte aligned, owned by the caller and
+ *          read by every later forward (it must stay valid and unchanged while they run);
+ *          NULL removes the bias.
+ *   Bb   : 1 (one matrix for every batch entry) or B;  b' = (Bb == 1 ? 0 : b).
+ *   Hb   : 1 (one matrix for every query head) or Hq;  a' = (Hb == 1 ? 0 : a).
+ *   ld   : row stride in elements, >= S and a multiple of 8 (rows may be padded; the
+ *          padding is never used for the result).
+ * Masked pairs stay masked whatever their bias; the bias enters the row max, the
+ * weights and the LSE.
+ * Errors: ATTN_ERR_INVALID_ARG (NULL handle, misaligned pointer, Bb / Hb / ld out of
+ *         range); ATTN_ERR_UNSUPPORTED (dtype other than ATTN_BF16, LOCAL_GLOBAL, or
+ *         with the ALiBi bias set).
+ * attn_backward of a handle with a bias matrix returns ATTN_ERR_UNSUPPORTED.
+ * Must not be called while a forward of this handle is in flight.
+ */
+attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long ld);
+
+/*
  * attn_backward -- the gradients of the forward pass of this handle with respect to
  * Q, K and V, for the output gradient dO:
  *     P_ij = exp(s_ij - LSE_i), D_i = dO_i . O_i, dS_ij = P_ij (dO_i . v_j - D_i),

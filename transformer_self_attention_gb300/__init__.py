@@ -30,7 +30,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
-            "attn_backward", "attn_bwd_dq_schedule_host")
+            "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -74,6 +74,8 @@ def _load():
     lib.attn_backward.restype = I
     lib.attn_bwd_dq_schedule_host.argtypes = [I, I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.attn_bwd_dq_schedule_host.restype = I
+    lib.attn_set_bias.argtypes = [P, P, I, I, ctypes.c_long]
+    lib.attn_set_bias.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -415,3 +417,25 @@ class Attention:
         st = attn_set_alibi(self.handle, slopes)
         if st != ATTN_OK:
             raise AttnError(st, "attn_set_alibi")
+
+    def set_bias(self, bias=None):
+        """Add a bias matrix b_ij to the scores: a CUDA bf16 tensor [Bb, Hb, S, ld] (Bb in {1, B},
+        Hb in {1, Hq}, ld >= S a multiple of 8; a 3-D [Hb, S, ld] or 2-D [S, ld] tensor is taken as
+        Bb = 1 / Hb = 1).  The tensor is kept referenced by the plan; None removes the bias."""
+        if bias is None:
+            st = _lib.attn_set_bias(self.handle, None, 0, 0, 0)
+            self._bias = None
+        else:
+            import torch
+            t = bias
+            while t.dim() < 4:
+                t = t.unsqueeze(0)
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("bias must be a contiguous CUDA bf16 tensor")
+            Bb, Hb, S, ld = t.shape
+            if S != self.shape[3]:
+                raise ValueError("bias rows must be the sequence length")
+            st = _lib.attn_set_bias(self.handle, t.data_ptr(), int(Bb), int(Hb), int(ld))
+            self._bias = t if st == ATTN_OK else None
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_set_bias")

@@ -96,6 +96,20 @@ bool encode_map_e4m3(CUtensorMap* map, const void* base, int d, long rows, long 
     return r == CUDA_SUCCESS;
 }
 
+// A bias matrix bf16 [planes, S, ld] for L2 prefetches of 128 x 128 boxes (no swizzle).
+bool encode_map_bias(CUtensorMap* map, const void* base, long ld, long S, long planes) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)ld, (cuuint64_t)S, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)(S * ld * 2)};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 constexpr unsigned kTileRows = ATTN_TILE;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -401,7 +415,7 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     }
     for (int a = 0; a < h->Hq; ++a)
         if (!std::isfinite(slopes[a])) return ATTN_ERR_INVALID_ARG;
-    if (h->kind == ATTN_MASK_LOCAL_GLOBAL || h->dtype == ATTN_FP8_E4M3) return ATTN_ERR_UNSUPPORTED;
+    if (h->kind == ATTN_MASK_LOCAL_GLOBAL || h->dtype == ATTN_FP8_E4M3 || h->tp.bias) return ATTN_ERR_UNSUPPORTED;
     if (!h->d_alibi) {
         cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->d_alibi), sizeof(float) * h->Hq);
         if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
@@ -412,6 +426,25 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     return ATTN_OK;
 }
 
+attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long ld) {
+    if (!h) return ATTN_ERR_INVALID_ARG;
+    if (!bias) {  // back to no bias
+        h->tp.bias = nullptr;
+        h->tp.bias_Bb = h->tp.bias_Hb = 0;
+        h->tp.bias_ld = 0;
+        return ATTN_OK;
+    }
+    if (!aligned16(bias) || (Bb != 1 && Bb != h->B) || (Hb != 1 && Hb != h->Hq) || ld < h->S || ld % 8 != 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->tp.alibi) return ATTN_ERR_UNSUPPORTED;
+    if (!encode_map_bias(&h->tp.tm_bias, bias, ld, h->S, (long)Bb * Hb)) return ATTN_ERR_CUDA;
+    h->tp.bias = static_cast<const uint16_t*>(bias);
+    h->tp.bias_Bb = Bb;
+    h->tp.bias_Hb = Hb;
+    h->tp.bias_ld = ld;
+    return ATTN_OK;
+}
+
 attn_status attn_backward(attn_handle h, const void* Q, const void* K, const void* V, const void* O, const float* LSE,
                           const void* dO, void* dQ, void* dK, void* dV, void* stream_ptr) {
     if (!h || !Q || !K || !V || !O || !LSE || !dO || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
@@ -419,7 +452,8 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     for (const void* q : ptrs)
         if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(LSE) & 3u) return ATTN_ERR_INVALID_ARG;
-    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->d_alibi) return ATTN_ERR_UNSUPPORTED;
+    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->d_alibi || h->tp.bias)
+        return ATTN_ERR_UNSUPPORTED;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int nq = (h->S + ATTN_TILE - 1) / ATTN_TILE;
     const int S_pad = nq * ATTN_TILE;

@@ -47,8 +47,8 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units: rescale O only if the 
 enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 
 // BIAS: 0 none; 1 ALiBi added per element (symmetric kinds, |i - j|); 2 ALiBi under the
-// causal kinds, added by the tensor core (see the MMA role).
-enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2 };
+// causal kinds, added by the tensor core (see the MMA role); 3 a given bias matrix b_ij.
+enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2, BIAS_MATRIX = 3 };
 
 template <int D, int BIAS = BIAS_NONE, bool F8 = false>
 struct Cfg {
@@ -131,6 +131,11 @@ struct TileMask {
     int a0, a1;
     uint32_t g0, g1, g2, g3;
 };
+
+__device__ __forceinline__ bool tile_allowed(int c, const TileMask& mk) {
+    const uint32_t gw = c < 32 ? mk.g0 : c < 64 ? mk.g1 : c < 96 ? mk.g2 : mk.g3;
+    return (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
+}
 
 template <bool MASKED>
 __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask& mk) {
@@ -306,6 +311,58 @@ __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMa
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
+// The bias row of this thread for one key tile: 16 loads of 16 bytes (8 keys each), issued
+// before the wait for S so that their latency hides behind it.  brow: the row's bias at the
+// tile's first key (16-byte aligned), or null for rows past the sequence; chunks of 8 keys are
+// read only while they start inside [0, n_valid) (the row stride is a multiple of 8, so a chunk
+// that starts there stays inside the row).
+__device__ __forceinline__ void load_bias_row(uint4 (&bv)[16], const uint16_t* brow, int n_valid) {
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+        bv[q] = (brow != nullptr && q * 8 < n_valid) ? __ldg(reinterpret_cast<const uint4*>(brow + q * 8))
+                                                   : make_uint4(0, 0, 0, 0);
+}
+
+// Pass 1 with a bias matrix: x = s * sl2 + b_ij log2(e), -inf where masked (the mask is applied
+// after the add, so padding values of the bias rows never matter), written back over the S
+// columns as fp32 -- pass 2 then reads x with unit scale and no mask.  Returns the row max of x.
+template <bool MASKED>
+__device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMask& mk, float sl2,
+                                                      const uint4 (&bv)[16]) {
+    constexpr float LOG2E_F = 1.4426950408889634f;
+    const float2 sl2x2 = make_float2(sl2, sl2), l2x2 = make_float2(LOG2E_F, LOG2E_F);
+    float m4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m4[k] = -INFINITY;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {  // 32 keys at a time
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const int c = ch * 32 + e;
+            const uint4 w4 = bv[c >> 3];
+            const int wi = (e >> 1) & 3;
+            const uint32_t w = wi == 0 ? w4.x : wi == 1 ? w4.y : wi == 2 ? w4.z : w4.w;
+            const float2 bb = make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            float2 x = __ffma2_rn(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), sl2x2,
+                                  __fmul2_rn(bb, l2x2));
+            if (MASKED) {
+                x.x = tile_allowed(c, mk) ? x.x : -INFINITY;
+                x.y = tile_allowed(c + 1, mk) ? x.y : -INFINITY;
+            }
+            r[e] = __float_as_uint(x.x);
+            r[e + 1] = __float_as_uint(x.y);
+            const int k = (e >> 1) & 3;
+            m4[k] = fmax3(m4[k], x.x, x.y);
+        }
+        tmem_st32(t_s + ch * 32, r);
+    }
+    tmem_wait_st();
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
 template <int D, int BIAS, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D, BIAS, F8>;
@@ -381,6 +438,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const CUtensorMap* qmap = grows ? &p.tm_qg : &p.tm_q;
+            const int bias_plane = (BIAS == BIAS_MATRIX)
+                                       ? (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
+                                       : 0;
+            if constexpr (BIAS == BIAS_MATRIX) prefetch_tmap(&p.tm_bias);
             mbar_arrive_expect_tx(bar(B_Q), C::TILE_BYTES);
             for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * C::XW, q_tile * BM, bh);
             int k_loaded = 0, v_loaded = 0;
@@ -394,6 +455,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
                 for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * C::XW, row, bkv);
                 ++k_loaded;
+                if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
+                    tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
                 if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
                 if (p.withhold_v) continue;
                 mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
@@ -484,9 +547,20 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         const float mL = (BIAS != BIAS_NONE) ? p.alibi[a] * 1.4426950408889634f : 0.f;  // ALiBi slope, log2 units
         const bool causal_kind = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
+        // bias matrix: this row's plane ([Bb, Hb] broadcast over batch / query heads)
+        const size_t bplane = (BIAS == BIAS_MATRIX)
+                                  ? (size_t)(p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
+                                  : 0;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int it = 0; it < n_iter; ++it) {
+            uint4 bv[BIAS == BIAS_MATRIX ? 16 : 1];  // this row's bias for the tile (issued before the S wait)
+            if constexpr (BIAS == BIAS_MATRIX) {
+                const long c0 = (long)band_tile(it) * BN;
+                const uint16_t* brow =
+                    (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr;
+                load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
+            }
             // warp-uniform exit: the tensor-memory accesses below are warp-collective
             if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
                 ok = false;
@@ -537,6 +611,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 else
                     mx = partial ? tile_row_max_alibi<true, true>(t_s, mk, sl2, mL, base)
                                  : tile_row_max_alibi<false, true>(t_s, mk, sl2, mL, base);
+            } else if constexpr (BIAS == BIAS_MATRIX) {
+                mx = partial ? tile_row_max_matbias<true>(t_s, mk, sl2, bv) : tile_row_max_matbias<false>(t_s, mk, sl2, bv);
             } else {
                 mx = partial ? tile_row_max<true>(t_s, mk) : tile_row_max<false>(t_s, mk);
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
@@ -575,6 +651,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 else
                     sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base)
                                   : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base);
+            } else if constexpr (BIAS == BIAS_MATRIX) {
+                sum = tile_exp_store<false>(t_s, mk, 1.f, ref);  // x is already scaled, biased and masked
             } else if constexpr (F8) {
                 sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref) : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref);
             } else {
@@ -695,6 +773,11 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
     if (p.fp8) {  // E4M3 inputs: d = 128, no bias, no local + global (checked by the host)
         if (d == 128 && !p.alibi) return launch<128, BIAS_NONE, true>(p, n_items, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (p.bias) {  // a bias matrix (bf16 inputs, interval kinds; checked by the host)
+        if (d == 128) return launch<128, BIAS_MATRIX>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_MATRIX>(p, n_items, stream);
         return cudaErrorInvalidValue;
     }
     if (p.alibi && causal) {

@@ -40,6 +40,12 @@ struct TcParams {
     const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
     int fp8;             // Q, K, V are E4M3 (scale_log2 includes their descales)
     float o_scale;       // factor on O at the end (the V descale for E4M3 inputs, else 1)
+    // additive bias matrix (bf16 [bias_Bb, bias_Hb, S, bias_ld], device), or null; tm_bias
+    // covers it as {bias_ld, S, bias_Bb * bias_Hb} with box {128, 128, 1} (L2 prefetches)
+    CUtensorMap tm_bias;
+    const uint16_t* bias;
+    int bias_Bb, bias_Hb;
+    long bias_ld;
 };
 
 // Parameters of the fp32 CUDA-core kernel.
