@@ -418,6 +418,18 @@ attn_status attn_decode_set_alibi(attn_decode_handle h, const float* slopes);
  */
 attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas);
 
+/*
+ * attn_decode_set_merge_mode -- where the partial results of a unit (b, g) split over
+ * several CTAs are combined (O = sum_c e^{LSE_c - M} O_c / W, LSE = M + ln W with
+ * M = max_c LSE_c, W = sum_c e^{LSE_c - M}, the same merge either way):
+ *   0 (default): by a second, small kernel when some unit of the call has 6 or more
+ *                partials, else by the last CTA to finish a part of the unit;
+ *   1          : always by that last CTA;
+ *   2          : always by the merge kernel (one warp per packed row).
+ * Errors: ATTN_ERR_INVALID_ARG (NULL handle, mode outside 0..2).
+ */
+attn_status attn_decode_set_merge_mode(attn_decode_handle h, int mode);
+
 /* attn_decode_destroy -- free the handle (synchronises the device first); NULL is ignored. */
 attn_status attn_decode_destroy(attn_decode_handle h);
 

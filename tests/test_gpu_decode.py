@@ -172,3 +172,48 @@ def test_decode_step_equals_prefill_row():
 def test_decode_workloads_full_size(w):
     """The decode workloads at full size, every output against the oracle."""
     _check(w)
+
+
+def _check_mode(w, mode, grid_limit=None):
+    import transformer_self_attention_gb300 as tsa
+    plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind, window=w.window)
+    plan.set_merge_mode(mode)
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w, stale_fill=float("nan"))
+    outs, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), lens, plan=plan, grid_limit=grid_limit)
+    O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale,
+                                 w.kind, w.window)
+    _compare(*outs[0], O_ref, L_ref)
+    return outs[0]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("Hq,Hkv,S_q,d,kind", [(32, 1, 1, 128, wl.MASK_CAUSAL), (16, 16, 32, 64, wl.MASK_FULL),
+                                               (32, 8, 4, 128, wl.MASK_CAUSAL_SLIDING), (8, 2, 2, 64, wl.MASK_CAUSAL)])
+def test_decode_merge_modes_many_partials(Hq, Hkv, S_q, d, kind, mode):
+    """Few units over every multiprocessor: each unit is split into many partials, merged by the
+    last CTA to finish (mode 1) or by the merge kernel (mode 2)."""
+    _check_mode(_dw("m", 2, Hq, Hkv, S_q, 3000, d, kind, window=700, len_min=S_q + 1500), mode)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("limit", [2, 7])
+def test_decode_merge_modes_long_shares(limit, mode):
+    _check_mode(_dw("ml", 4, 8, 2, 2, 1500, 128, wl.MASK_CAUSAL, len_min=300), mode, grid_limit=limit)
+
+
+@pytest.mark.parametrize("w", [wl.DECODE_MQA_16K, wl.CROSS_MHA_4K], ids=lambda w: w.name)
+def test_decode_merge_modes_agree_full_size(w):
+    """Both merges of the same partials, against the oracle and against each other."""
+    O1, L1 = _check_mode(w, 1)
+    O2, L2 = _check_mode(w, 2)
+    # the same partials summed in another order: at most a bf16 rounding apart (0.0078 near 1)
+    assert np.abs(O1.astype(np.float64) - O2).max() <= BF16_MAX_ABS
+    assert np.abs(L1.astype(np.float64) - L2).max() <= 1e-4
+
+
+def test_decode_merge_mode_rejects_unknown_modes():
+    import transformer_self_attention_gb300 as tsa
+    plan = tsa.DecodeAttention(1, 2, 1, 1, 256, 64)
+    for bad in (-1, 3):
+        with pytest.raises(tsa.AttnError):
+            plan.set_merge_mode(bad)

@@ -30,7 +30,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
-            "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias")
+            "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -76,6 +76,8 @@ def _load():
     lib.attn_bwd_dq_schedule_host.restype = I
     lib.attn_set_bias.argtypes = [P, P, I, I, ctypes.c_long]
     lib.attn_set_bias.restype = I
+    lib.attn_decode_set_merge_mode.argtypes = [P, I]
+    lib.attn_decode_set_merge_mode.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -323,6 +325,12 @@ class DecodeAttention:
         st = _lib.attn_decode_set_grid_limit(self.handle, int(max_ctas))
         if st != ATTN_OK:
             raise AttnError(st, "attn_decode_set_grid_limit")
+
+    def set_merge_mode(self, mode: int):
+        """Where split units are merged: 0 auto, 1 in the decode kernel, 2 by the merge kernel."""
+        st = _lib.attn_decode_set_merge_mode(self.handle, int(mode))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_decode_set_merge_mode")
 
 
 # ---------------------------------------------------------------- torch convenience

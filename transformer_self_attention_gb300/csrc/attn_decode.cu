@@ -740,7 +740,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
             }
             // O^T has been read: the next PV into it follows this CTA's next PFULL arrival
             tc_fence_before();
-            if (!s.whole) {
+            if (!s.whole && !p.defer_merge) {
                 __threadfence();
                 named_bar_sync(1, 128);
                 if (t == 0) {
@@ -766,6 +766,72 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
     }
 }
 
+// Merge of the split units as a kernel of its own (the decode kernel ran with defer_merge):
+// warp w of CTA x takes packed row 4 (x mod R) + w of split unit x / R, R = ceil(rows / 4).
+//   M = max_c LSE_c, W = sum_c e^{LSE_c - M}, O = sum_c e^{LSE_c - M} O_c / W, LSE = M + ln W
+// over the unit's partials c (each normalised by its own sum).  Lane l owns d components
+// [l D/32, (l+1) D/32); eight partials' loads are in flight at a time.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeMergeParams p) {
+    constexpr int PER = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_unit = (p.rows + 3) >> 2;
+    const int u = blockIdx.x / per_unit, r = (blockIdx.x - u * per_unit) * 4 + warp;
+    if (u >= p.n_split || r >= p.rows) return;  // whole warps
+    const int4 e = p.list[u];
+    const int b = e.x, g = e.y, k0 = e.z, nseg = e.w >> 1;
+    const bool k0_first = (e.w & 1) != 0;
+    auto slot = [&](int c) -> size_t { return (size_t)(c == 0 ? 2 * k0 + (k0_first ? 0 : 1) : 2 * (k0 + c)); };
+    float M = -INFINITY;
+    for (int c = lane; c < nseg; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot(c) * p.np + r));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float W = 0.f;
+    for (int c = lane; c < nseg; c += 32) {
+        const float lv = __ldcg(p.part_lse + slot(c) * p.np + r);
+        W += lv == -INFINITY ? 0.f : __expf(lv - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    const float inv_w = W > 0.f ? 1.f / W : 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) acc[q] = 0.f;
+    for (int c0 = 0; c0 < nseg; c0 += 8) {
+        float ov[8][PER], lv[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const int c = c0 + v;
+            lv[v] = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) ov[v][q] = 0.f;
+            if (c < nseg) {
+                const size_t sl = slot(c);
+                lv[v] = __ldcg(p.part_lse + sl * p.np + r);
+                const float* src = p.part_o + (sl * p.np + r) * D + lane * PER;
+                if constexpr (PER == 4) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+                    ov[v][0] = x.x; ov[v][1 % PER] = x.y; ov[v][2 % PER] = x.z; ov[v][3 % PER] = x.w;
+                } else {
+                    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+                    ov[v][0] = x.x; ov[v][1 % PER] = x.y;
+                }
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const float w = lv[v] == -INFINITY ? 0.f : __expf(lv[v] - M) * inv_w;
+#pragma unroll
+            for (int q = 0; q < PER; ++q) acc[q] = fmaf(w, ov[v][q], acc[q]);
+        }
+    }
+    const size_t row = (size_t)(b * p.Hq + g * p.group) * p.S_q + r;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + row * D + lane * PER;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) dst[q] = __float2bfloat16_rn(acc[q]);
+    if (lane == 0 && p.lse) p.lse[row] = W > 0.f ? M + __logf(W) : -INFINITY;
+}
+
 template <int D, int NP, bool ALIBI>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
     using C = DCfg<D, NP>;
@@ -786,6 +852,15 @@ cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_decode_merge(const DecodeMergeParams& p, int d, cudaStream_t stream) {
+    if (p.n_split <= 0) return cudaSuccess;
+    const int grid = p.n_split * ((p.rows + 3) / 4);
+    if (d == 128) decode_merge_kernel<128><<<grid, 128, 0, stream>>>(p);
+    else if (d == 64) decode_merge_kernel<64><<<grid, 128, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream) {
     if (p.n_cta <= 0 || p.total_tiles <= 0) return cudaSuccess;

@@ -19,6 +19,7 @@ struct attn_decode_plan {
     float scale = 0.f;
     int n_sm = 0;
     int grid_limit = 0;  // test hook: 0 = one CTA per multiprocessor
+    int merge_mode = 0;  // split units: 0 auto, 1 merged in the decode kernel, 2 by the merge kernel
     size_t part_slots = 0;
     int* d_err = nullptr;
     unsigned* d_counters = nullptr;
@@ -28,6 +29,7 @@ struct attn_decode_plan {
     const void* last_k = nullptr;
     const void* last_v = nullptr;
     attn::DecodeParams p{};
+    attn::DecodeMergeParams mp{};
 };
 
 namespace {
@@ -178,7 +180,40 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
     p.total_tiles = sched.total_tiles;
     p.o = O;
     p.lse = LSE;
+    // Units split over several CTAs, with the kernel's share arithmetic (CTA k takes the
+    // indices [k T / n, (k + 1) T / n)).  Many partials per unit make the in-kernel merge a
+    // long serial tail on one CTA; from 6 partials on they go to the merge kernel instead
+    // (below that the second launch costs more than it saves).
+    attn::DecodeMergeParams& mp = h->mp;
+    const long long T = sched.total_tiles;
+    const int n = sched.n_cta;
+    auto share_of = [&](long long i) { return (int)(((i + 1) * n + T - 1) / T - 1); };
+    mp.n_split = 0;
+    int max_seg = 1;
+    bool overflow = false;
+    for (int b = 0; b < h->B; ++b) {
+        const int n_unit = sched.tile_prefix[b + 1] - sched.tile_prefix[b];
+        for (int g = 0; g < h->Hkv && n_unit > 0; ++g) {
+            const long long ub = (long long)h->Hkv * sched.tile_prefix[b] + (long long)g * n_unit;
+            const int k0 = share_of(ub), k1 = share_of(ub + n_unit - 1);
+            if (k1 == k0) continue;
+            max_seg = std::max(max_seg, k1 - k0 + 1);
+            if (mp.n_split == attn::kDecodeMaxSplit) { overflow = true; continue; }
+            const bool first = (long long)k0 * T / n == ub;
+            mp.list[mp.n_split++] = make_int4(b, g, k0, 2 * (k1 - k0 + 1) + (first ? 1 : 0));
+        }
+    }
+    const bool defer = !overflow && mp.n_split > 0 && (h->merge_mode == 2 || (h->merge_mode == 0 && max_seg >= 6));
+    p.defer_merge = defer ? 1 : 0;
     cudaError_t e = attn::launch_decode(p, h->d, h->np, static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && defer) {
+        mp.part_o = p.part_o;
+        mp.part_lse = p.part_lse;
+        mp.o = O;
+        mp.lse = LSE;
+        mp.Hq = h->Hq; mp.group = h->Hq / h->Hkv; mp.S_q = h->S_q; mp.rows = p.rows; mp.np = h->np;
+        e = attn::launch_decode_merge(mp, h->d, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -212,6 +247,12 @@ attn_status attn_decode_set_alibi(attn_decode_handle h, const float* slopes) {
     if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     h->p.alibi = h->d_alibi;
+    return ATTN_OK;
+}
+
+attn_status attn_decode_set_merge_mode(attn_decode_handle h, int mode) {
+    if (!h || mode < 0 || mode > 2) return ATTN_ERR_INVALID_ARG;
+    h->merge_mode = mode;
     return ATTN_OK;
 }
 

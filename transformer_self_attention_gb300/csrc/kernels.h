@@ -101,11 +101,24 @@ struct DecodeParams {
     int n_cta;
     long long total_tiles;                   // T
     const float* alibi;                      // [Hq] slopes of the bias -m_a |t - j| (device), or null
+    int defer_merge;                         // split units: leave the partials to the merge kernel
     int len[kDecodeMaxBatch];                // cache length of each sequence
     int tile_prefix[kDecodeMaxBatch + 1];    // key tiles of the sequences before b (per kv head)
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);
+
+// Merge of the units split over several CTAs, as a kernel of its own: one warp per packed row.
+constexpr int kDecodeMaxSplit = 256;
+struct DecodeMergeParams {
+    const float* part_o;    // the decode kernel's partial slots
+    const float* part_lse;
+    void* o;                // O [B, Hq, S_q, d] bf16
+    float* lse;             // [B, Hq, S_q], may be null
+    int Hq, group, S_q, rows, np, n_split;
+    int4 list[kDecodeMaxSplit];  // split unit u: {b, g, k0, 2 * nseg + (unit starts CTA k0's share)}
+};
+cudaError_t launch_decode_merge(const DecodeMergeParams& p, int d, cudaStream_t stream);
 
 // Backward pass (attn_bwd.cu): a pre-pass (D = dO . O and LSE in log2 units, padded to
 // S_pad rows per head), the dQ kernel (one CTA per forward work item) and the dK/dV kernel
