@@ -660,6 +660,7 @@ def run_ours_decode(args, w):
     st, code = plan.poll_device_error()
     if st != 0:
         raise RuntimeError(f"device error during the timed steps: {code}")
+    launches_per_step = plan.launch_count()
     useful = wl.decode_useful_flops(w, lens)
     nbytes = wl.decode_bytes(w, lens)
     value = world * useful / (mean_ms * 1e-3) / 1e12
@@ -716,7 +717,7 @@ def run_ours_decode(args, w):
                            score_bias="alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
                            l2="flushed before every step (256 MiB write)",
                            parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
-            "roofline": roofline, "gpu_launches": args.steps, "wall_s_timed_region": wall}
+            "roofline": roofline, "gpu_launches": args.steps * launches_per_step, "wall_s_timed_region": wall}
     if e2e:
         line["e2e"] = e2e
     if clk:

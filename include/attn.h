@@ -430,6 +430,13 @@ attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas);
  */
 attn_status attn_decode_set_merge_mode(attn_decode_handle h, int mode);
 
+/*
+ * attn_decode_launch_count -- *n = the number of kernels the last attn_decode_forward of
+ * this handle enqueued (1, or 2 with the merge kernel; 0 before the first call).
+ * Errors: ATTN_ERR_INVALID_ARG (NULL argument).
+ */
+attn_status attn_decode_launch_count(attn_decode_handle h, int* n);
+
 /* attn_decode_destroy -- free the handle (synchronises the device first); NULL is ignored. */
 attn_status attn_decode_destroy(attn_decode_handle h);
 

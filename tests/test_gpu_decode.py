@@ -217,3 +217,17 @@ def test_decode_merge_mode_rejects_unknown_modes():
     for bad in (-1, 3):
         with pytest.raises(tsa.AttnError):
             plan.set_merge_mode(bad)
+
+
+def test_decode_launch_count_follows_the_merge():
+    """One kernel per call, two when the split units go to the merge kernel."""
+    import transformer_self_attention_gb300 as tsa
+    w = wl.DECODE_MQA_16K
+    Qc, Kc, Vc, lens = wl.make_decode_inputs(w)
+    Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
+    plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind, window=w.window)
+    assert plan.launch_count() == 0
+    for mode, n in ((1, 1), (2, 2), (0, 2)):  # this workload splits units into more than 6 partials
+        plan.set_merge_mode(mode)
+        _run(w, Q, K, V, lens, plan=plan)
+        assert plan.launch_count() == n

@@ -30,7 +30,8 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_create", "attn_decode_forward", "attn_decode_poll_device_error", "attn_decode_destroy",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
-            "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode")
+            "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode",
+            "attn_decode_launch_count")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -78,6 +79,8 @@ def _load():
     lib.attn_set_bias.restype = I
     lib.attn_decode_set_merge_mode.argtypes = [P, I]
     lib.attn_decode_set_merge_mode.restype = I
+    lib.attn_decode_launch_count.argtypes = [P, ctypes.POINTER(I)]
+    lib.attn_decode_launch_count.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
@@ -325,6 +328,14 @@ class DecodeAttention:
         st = _lib.attn_decode_set_grid_limit(self.handle, int(max_ctas))
         if st != ATTN_OK:
             raise AttnError(st, "attn_decode_set_grid_limit")
+
+    def launch_count(self) -> int:
+        """Kernels the last call enqueued (1, or 2 with the merge kernel)."""
+        n = ctypes.c_int(0)
+        st = _lib.attn_decode_launch_count(self.handle, ctypes.byref(n))
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_decode_launch_count")
+        return n.value
 
     def set_merge_mode(self, mode: int):
         """Where split units are merged: 0 auto, 1 in the decode kernel, 2 by the merge kernel."""

@@ -20,6 +20,7 @@ struct attn_decode_plan {
     int n_sm = 0;
     int grid_limit = 0;  // test hook: 0 = one CTA per multiprocessor
     int merge_mode = 0;  // split units: 0 auto, 1 merged in the decode kernel, 2 by the merge kernel
+    int last_launches = 0;  // kernels the last attn_decode_forward launched
     size_t part_slots = 0;
     int* d_err = nullptr;
     unsigned* d_counters = nullptr;
@@ -206,6 +207,7 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
     const bool defer = !overflow && mp.n_split > 0 && (h->merge_mode == 2 || (h->merge_mode == 0 && max_seg >= 6));
     p.defer_merge = defer ? 1 : 0;
     cudaError_t e = attn::launch_decode(p, h->d, h->np, static_cast<cudaStream_t>(stream));
+    h->last_launches = defer ? 2 : 1;
     if (e == cudaSuccess && defer) {
         mp.part_o = p.part_o;
         mp.part_lse = p.part_lse;
@@ -247,6 +249,12 @@ attn_status attn_decode_set_alibi(attn_decode_handle h, const float* slopes) {
     if (cudaMemcpy(h->d_alibi, slopes, sizeof(float) * h->Hq, cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     h->p.alibi = h->d_alibi;
+    return ATTN_OK;
+}
+
+attn_status attn_decode_launch_count(attn_decode_handle h, int* n) {
+    if (!h || !n) return ATTN_ERR_INVALID_ARG;
+    *n = h->last_launches;
     return ATTN_OK;
 }
 
