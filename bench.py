@@ -207,6 +207,7 @@ def run_ours(args, w):
     import torch.distributed as dist
 
     import transformer_self_attention_gb300 as tsa
+    from transformer_self_attention_gb300.shard import max_over_ranks
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -266,10 +267,7 @@ def run_ours(args, w):
     clk = clocks.stop() if clocks else None
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     mean_ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dev)  # the slowest rank
     st, code = plan.poll_device_error()
     if st != 0:
         raise RuntimeError(f"device error during the timed steps: {code}")
@@ -302,10 +300,7 @@ def run_ours(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)  # the slowest rank
         bi = sum(t.numel() * t.element_size() for t in (Qc, Kc, Vc))
         bo = O.numel() * O.element_size() + LSE.numel() * LSE.element_size()
         e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
@@ -425,6 +420,7 @@ def run_ours_backward(args, w):
     import torch.distributed as dist
 
     import transformer_self_attention_gb300 as tsa
+    from transformer_self_attention_gb300.shard import max_over_ranks
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -468,10 +464,7 @@ def run_ours_backward(args, w):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     mean_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dev)  # the slowest rank
     st, code = plan.poll_device_error()
     if st != 0:
         raise RuntimeError(f"device error during the timed steps: {code}")
@@ -504,10 +497,7 @@ def run_ours_backward(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)  # the slowest rank
         e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
@@ -609,6 +599,7 @@ def run_ours_decode(args, w):
     import torch.distributed as dist
 
     import transformer_self_attention_gb300 as tsa
+    from transformer_self_attention_gb300.shard import max_over_ranks
 
     world, rank, local = dist_setup()
     if world > 1:
@@ -653,10 +644,7 @@ def run_ours_decode(args, w):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     mean_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dev)  # the slowest rank
     st, code = plan.poll_device_error()
     if st != 0:
         raise RuntimeError(f"device error during the timed steps: {code}")
@@ -691,10 +679,7 @@ def run_ours_decode(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)  # the slowest rank
         e2e = {"value": world * useful / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": Qc.numel() * Qc.element_size(),
                "d2h_bytes_per_step": O.numel() * O.element_size() + LSE.numel() * LSE.element_size(),
