@@ -18,6 +18,9 @@
 //                       scores, write P (bf16) back over S, and rescale the O
 //                       row only when the running max grew by more than 2^8
 //                       (the final division by l keeps the result exact).
+//                       P is released in two halves of 64 keys: the MMA thread
+//                       starts O += P V on the first half while the second is
+//                       still being exponentiated.
 //                       Epilogue: O / l -> bf16 -> swizzled smem -> TMA store;
 //                       LSE = (m + log2 l) ln 2.
 //
@@ -72,7 +75,8 @@ struct Cfg {
     static constexpr uint32_t TMEM_O = 128;
 };
 
-enum Bar { B_Q = 0, B_KFULL, B_KEMPTY, B_VFULL, B_VEMPTY, B_SFULL, B_PFULL, B_OFULL, NBAR };
+// B_PFULL / B_PFULL1: the first / second half of P (keys 0-63 / 64-127) is in tensor memory.
+enum Bar { B_Q = 0, B_KFULL, B_KEMPTY, B_VFULL, B_VEMPTY, B_SFULL, B_PFULL, B_PFULL1, B_OFULL, NBAR };
 
 struct Shared {  // small control block after the tiles
     uint64_t bar[NBAR];
@@ -169,12 +173,22 @@ __device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) 
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
+// Announce the first half of P (keys 0-63) to the MMA thread once this thread's stores of it
+// have landed; the thread's O rescale, if any, came before.
+__device__ __forceinline__ void release_first_half(uint32_t bar_half) {
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bar_half);
+}
+
 // P = exp2(s * sl2 - ref) written as bf16 over the S columns; returns the row sum.
 // Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
 // [32h, 32h+32), which only overlap S columns this thread has already read.  The
 // scale-and-subtract and the running sums use the packed two-lane fp32 instructions.
+// The first half is announced on bar_half as soon as it is stored.
 template <bool MASKED>
-__device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref) {
+__device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                               uint32_t bar_half) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -198,6 +212,7 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
             pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
+        if (h == 0) release_first_half(bar_half);
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -206,7 +221,8 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
 // layout of the 8-bit MMA), keys 4q..4q+3 of half h in column 16h + q.  P <= 2^8 by the
 // lazy rescale, inside the E4M3 range (448).
 template <bool MASKED>
-__device__ __forceinline__ float tile_exp_store_e4m3(uint32_t t_s, const TileMask& mk, float sl2, float ref) {
+__device__ __forceinline__ float tile_exp_store_e4m3(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                                    uint32_t bar_half) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -234,6 +250,7 @@ __device__ __forceinline__ float tile_exp_store_e4m3(uint32_t t_s, const TileMas
             pk[8 + q] = pack_e4m3x4(pb[0], pb[1], pb[2], pb[3]);
         }
         tmem_st16(t_s + h * 16, pk);
+        if (h == 0) release_first_half(bar_half);
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -284,7 +301,7 @@ __device__ __forceinline__ float tile_row_max_alibi(uint32_t t_s, const TileMask
 
 template <bool MASKED, bool ABS>
 __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMask& mk, float sl2, float ref,
-                                                      float mL, float base) {
+                                                      float mL, float base, uint32_t bar_half) {
     const float2 sl2x2 = make_float2(sl2, sl2);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -307,6 +324,7 @@ __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMa
             pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
+        if (h == 0) release_first_half(bar_half);
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -395,7 +413,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     const int bkv = b * p.Hkv + a / p.group;  // g(a) = a / (Hq / Hkv)
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), i == B_PFULL ? 128u : 1u);
+        for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == B_PFULL || i == B_PFULL1) ? 128u : 1u);
         sh->abort = 0;
         fence_barrier_init();
     }
@@ -504,6 +522,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / KS; ++k) {
+                    if (k == BN / KS / 2) {  // the second half of P (keys 64-127)
+                        if (!(ok = spin_bounded(bar(B_PFULL1), it & 1, sh, p, ERR_MMA))) break;
+                        tc_fence_after();
+                    }
                     // P: KS keys = 8 tensor-memory columns (2 bf16 or 4 E4M3 per column);
                     // V: KS key rows of 128 B each (MN-major: d runs along the row)
                     if constexpr (F8)
@@ -512,6 +534,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     else
                         mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
                                (it > 0 || k > 0) ? 1u : 0u);
+                }
+                if (!ok) {  // half of this PV was issued: track it so the drain below covers it
+                    mma_commit(bar(B_OFULL));
+                    last_bar = B_OFULL; last_par = it & 1;
+                    break;
                 }
                 mma_commit(bar(B_OFULL));
                 mma_commit(bar(B_VEMPTY));
@@ -646,23 +673,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             float sum;
             if constexpr (ALIBI) {
                 if (causal_kind)
-                    sum = partial ? tile_exp_store_alibi<true, false>(t_s, mk, sl2, ref, mL, base)
-                                  : tile_exp_store_alibi<false, false>(t_s, mk, sl2, ref, mL, base);
+                    sum = partial ? tile_exp_store_alibi<true, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi<false, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
                 else
-                    sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base)
-                                  : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base);
+                    sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
             } else if constexpr (BIAS == BIAS_MATRIX) {
-                sum = tile_exp_store<false>(t_s, mk, 1.f, ref);  // x is already scaled, biased and masked
+                sum = tile_exp_store<false>(t_s, mk, 1.f, ref, bar(B_PFULL));  // x is already scaled, biased and masked
             } else if constexpr (F8) {
-                sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref) : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref);
+                sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref, bar(B_PFULL))
+                              : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
-                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff) : tile_exp_store<false>(t_s, mk, sl2, r_eff);
+                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff, bar(B_PFULL))
+                              : tile_exp_store<false>(t_s, mk, sl2, r_eff, bar(B_PFULL));
             }
             l += sum;
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL));
+            mbar_arrive(bar(B_PFULL1));
         }
         // ---- epilogue
         if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(B_OFULL), (n_iter - 1) & 1, sh, p, ERR_SOFTMAX));
