@@ -185,10 +185,12 @@ __device__ __forceinline__ void release_first_half(uint32_t bar_half) {
 // Half h (keys 64h .. 64h+63) reads S columns [64h, 64h+64) and writes P columns
 // [32h, 32h+32), which only overlap S columns this thread has already read.  The
 // scale-and-subtract and the running sums use the packed two-lane fp32 instructions.
-// The first half is announced on bar_half as soon as it is stored.
-template <bool MASKED>
+// The first half is announced on bar_half as soon as it is stored.  fix() (the row's lazy O
+// rescale and running-sum update) runs after that half is computed and before it is announced:
+// it is off the path from S to the first exponentials, and O is rescaled before O += P V starts.
+template <bool MASKED, typename FixO>
 __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
-                                               uint32_t bar_half) {
+                                               uint32_t bar_half, FixO&& fix) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -212,7 +214,10 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
             pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
-        if (h == 0) release_first_half(bar_half);
+        if (h == 0) {
+            fix();
+            release_first_half(bar_half);
+        }
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
@@ -588,13 +593,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr;
                 load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
             }
-            // warp-uniform exit: the tensor-memory accesses below are warp-collective
-            if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate)
+            // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate).  It does
+            // not depend on S, so it is worked out before the wait for S.
             bool partial = true;
             TileMask mk{0, -1, 0u, 0u, 0u, 0u};
             if (it < n_band) {
@@ -627,6 +627,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 }
                 mk.g0 = bits[0]; mk.g1 = bits[1]; mk.g2 = bits[2]; mk.g3 = bits[3];
             }
+            // warp-uniform exit: the tensor-memory accesses below are warp-collective
+            if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             // ---- pass 1: row max of the (masked) scores, in log2 units
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
@@ -652,26 +658,33 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             // ---- running max, with the lazy rescale
             const bool grow = mx > m + RESCALE_THRESHOLD;  // false when mx is -inf; true on the first finite max
             const float m_new = grow ? mx : m;
-            const float alpha = grow ? ex2(m - m_new) : 1.f;  // exp2(-inf) = 0 on the first finite max
-            const bool fix_o = grow && it > 0 && m != -INFINITY;
-            if (__any_sync(0xffffffffu, fix_o)) {
-                uint32_t o[32];
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
+            const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+            // O *= alpha (rows whose max grew; rare) and l *= alpha.  O is complete up to PV(it-1): the
+            // wait for S(it) covers it, because the MMA thread issues QK(it) after PV(it-1).
+            auto fix = [&]() {
+                float alpha = 1.f;
+                if (grow) alpha = ex2(m - m_new);  // exp2(-inf) = 0 on the first finite max
+                const bool fix_o = grow && it > 0 && m != -INFINITY;
+                if (__any_sync(0xffffffffu, fix_o)) {
                     const float f = fix_o ? alpha : 1.f;
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {  // 16 columns at a time: few registers live
+                        uint32_t o[16];
+                        tmem_ld16(t_o + c * 16, o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tmem_st32(t_o + c * 32, o);
+                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st16(t_o + c * 16, o);
+                    }
                 }
-            }
-            l *= alpha;
-            m = m_new;
-            const float ref = (m == -INFINITY) ? 0.f : m;
+                l *= alpha;
+                m = m_new;
+            };
+            auto no_fix = []() {};
             // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P over the S columns
             float sum;
             if constexpr (ALIBI) {
+                fix();
                 if (causal_kind)
                     sum = partial ? tile_exp_store_alibi<true, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
                                   : tile_exp_store_alibi<false, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
@@ -679,14 +692,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
                                   : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
             } else if constexpr (BIAS == BIAS_MATRIX) {
-                sum = tile_exp_store<false>(t_s, mk, 1.f, ref, bar(B_PFULL));  // x is already scaled, biased and masked
+                fix();
+                sum = tile_exp_store<false>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);  // x is already scaled, biased and masked
             } else if constexpr (F8) {
+                fix();
                 sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref, bar(B_PFULL))
                               : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
-                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff, bar(B_PFULL))
-                              : tile_exp_store<false>(t_s, mk, sl2, r_eff, bar(B_PFULL));
+                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                              : tile_exp_store<false>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
             }
             l += sum;
             tmem_wait_st();
