@@ -109,10 +109,13 @@ __global__ void gather_globals_kernel(GatherParams p) {
 }
 
 // Combines the key chunks of the global-row pass.  One warp per (head, global
-// row); lanes split d.  Chunk c holds O_c (its own softmax-weighted average) and
+// row).  Chunk c holds O_c (its own softmax-weighted average) and
 // LSE_c = ln of its sum of exponentials, so the whole row is
 //   O = sum_c e^(LSE_c - M) O_c / sum_c e^(LSE_c - M),  LSE = M + ln sum_c e^(LSE_c - M)
 // with M = max_c LSE_c: the same softmax normalisation, applied across chunks.
+// Lanes split the chunks for M and the weights (warp reductions), then split d for the
+// weighted sum, each weight broadcast from the lane that computed it; the partial-O loads
+// of eight chunks are issued before their multiply-adds (the merge is latency-bound).
 __global__ void merge_global_rows_kernel(MergeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long row = (long)blockIdx.x * (blockDim.x >> 5) + warp;
@@ -121,18 +124,38 @@ __global__ void merge_global_rows_kernel(MergeParams p) {
     const int gr = (int)(row - bh * p.n_global);
     const float* lse_c = p.part_lse + row * p.n_chunks;
     float M = -INFINITY;
-    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, lse_c[c]);
+    for (int c = lane; c < p.n_chunks; c += 32) M = fmaxf(M, lse_c[c]);
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
     float W = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};  // d <= 128: 4 elements per lane
-    for (int c = 0; c < p.n_chunks; ++c) {
-        const float wc = expf(lse_c[c] - M);
-        W += wc;
-        const float* oc = p.part_o + (row * p.n_chunks + c) * p.d;
-        for (int e = 0; e < p.d / 32; ++e) acc[e] = fmaf(wc, oc[lane + 32 * e], acc[e]);
+    const int nd = p.d / 32;
+    for (int c0 = 0; c0 < p.n_chunks; c0 += 32) {
+        const int c = c0 + lane;
+        const float wl = c < p.n_chunks ? expf(lse_c[c] - M) : 0.f;  // this lane's chunk weight
+        W += wl;
+        const int n_here = min(32, p.n_chunks - c0);
+        const float* ob = p.part_o + (row * p.n_chunks + c0) * p.d;
+        for (int j0 = 0; j0 < n_here; j0 += 8) {
+            float v[8][4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[j][e] = (j0 + j < n_here && e < nd) ? ob[(long)(j0 + j) * p.d + lane + 32 * e] : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float wc = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);  // 0 past the last chunk
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(wc, v[j][e], acc[e]);
+            }
+        }
     }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) W += __shfl_xor_sync(0xffffffffu, W, s);
     const long pos = p.globals[gr];
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o) + (bh * p.S + pos) * p.d;
-    for (int e = 0; e < p.d / 32; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);
+    for (int e = 0; e < nd; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);
     if (p.lse && lane == 0) p.lse[bh * p.S + pos] = M + logf(W);
 }
 
