@@ -141,9 +141,17 @@ __device__ __forceinline__ bool tile_allowed(int c, const TileMask& mk) {
     return (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
 }
 
-template <bool MASKED>
+// Mask forms of a tile, decided once per tile and warp-uniformly:
+//   MASK_NONE  : FULL tile, no predicate;
+//   MASK_UPPER : allowed columns are c <= a1 (a0 <= 0, no global keys) -- the causal diagonal
+//                tiles; one compare and one select per element;
+//   MASK_ANY   : the interval [a0, a1] plus the global-key bits g0..g3.
+enum { MASK_NONE = 0, MASK_UPPER = 1, MASK_ANY = 2 };
+
+template <int MASKED>
 __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask& mk) {
-    if (!MASKED) return __uint_as_float(raw);
+    if (MASKED == MASK_NONE) return __uint_as_float(raw);
+    if (MASKED == MASK_UPPER) return c <= mk.a1 ? __uint_as_float(raw) : -INFINITY;
     const uint32_t gw = c < 32 ? mk.g0 : c < 64 ? mk.g1 : c < 96 ? mk.g2 : mk.g3;
     const bool in = (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
     return in ? __uint_as_float(raw) : -INFINITY;
@@ -151,7 +159,7 @@ __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask&
 
 // Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
 // three-input max instructions, eight independent chains.
-template <bool MASKED>
+template <int MASKED>
 __device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
     float m8[8];
 #pragma unroll
@@ -188,7 +196,7 @@ __device__ __forceinline__ void release_first_half(uint32_t bar_half) {
 // The first half is announced on bar_half as soon as it is stored.  fix() (the row's lazy O
 // rescale and running-sum update) runs after that half is computed and before it is announced:
 // it is off the path from S to the first exponentials, and O is rescaled before O += P V starts.
-template <bool MASKED, typename FixO>
+template <int MASKED, typename FixO>
 __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
                                                uint32_t bar_half, FixO&& fix) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
@@ -225,7 +233,7 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
 // tile_exp_store for E4M3 P: four keys per 32-bit tensor-memory column (the A operand
 // layout of the 8-bit MMA), keys 4q..4q+3 of half h in column 16h + q.  P <= 2^8 by the
 // lazy rescale, inside the E4M3 range (448).
-template <bool MASKED>
+template <int MASKED>
 __device__ __forceinline__ float tile_exp_store_e4m3(uint32_t t_s, const TileMask& mk, float sl2, float ref,
                                                     uint32_t bar_half) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
@@ -276,7 +284,7 @@ __device__ __forceinline__ float2 alibi_pair(float base, int c, float mL, float 
 }
 
 // Row maximum of x (log2 units, no further scaling).
-template <bool MASKED, bool ABS>
+template <int MASKED, bool ABS>
 __device__ __forceinline__ float tile_row_max_alibi(uint32_t t_s, const TileMask& mk, float sl2, float mL,
                                                     float base) {
     const float2 sl2x2 = make_float2(sl2, sl2);
@@ -304,7 +312,7 @@ __device__ __forceinline__ float tile_row_max_alibi(uint32_t t_s, const TileMask
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
 
-template <bool MASKED, bool ABS>
+template <int MASKED, bool ABS>
 __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMask& mk, float sl2, float ref,
                                                       float mL, float base, uint32_t bar_half) {
     const float2 sl2x2 = make_float2(sl2, sl2);
@@ -349,7 +357,7 @@ __device__ __forceinline__ void load_bias_row(uint4 (&bv)[16], const uint16_t* b
 // Pass 1 with a bias matrix: x = s * sl2 + b_ij log2(e), -inf where masked (the mask is applied
 // after the add, so padding values of the bias rows never matter), written back over the S
 // columns as fp32 -- pass 2 then reads x with unit scale and no mask.  Returns the row max of x.
-template <bool MASKED>
+template <int MASKED>
 __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMask& mk, float sl2,
                                                       const uint4 (&bv)[16]) {
     constexpr float LOG2E_F = 1.4426950408889634f;
@@ -627,6 +635,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 }
                 mk.g0 = bits[0]; mk.g1 = bits[1]; mk.g2 = bits[2]; mk.g3 = bits[3];
             }
+            // causal diagonal tiles (no lower bound inside the tile, no global keys): the cheap
+            // mask form, when every row of the warp qualifies
+            const bool upper = __all_sync(0xffffffffu, partial && !lg && it < n_band && mk.a0 <= 0);
             // warp-uniform exit: the tensor-memory accesses below are warp-collective
             if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
                 ok = false;
@@ -639,15 +650,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if constexpr (ALIBI) {
                 base = (float)(i - (long)band_tile(it) * BN);
                 if (causal_kind)
-                    mx = partial ? tile_row_max_alibi<true, false>(t_s, mk, sl2, mL, base)
-                                 : tile_row_max_alibi<false, false>(t_s, mk, sl2, mL, base);
+                    mx = partial ? tile_row_max_alibi<MASK_ANY, false>(t_s, mk, sl2, mL, base)
+                                 : tile_row_max_alibi<MASK_NONE, false>(t_s, mk, sl2, mL, base);
                 else
-                    mx = partial ? tile_row_max_alibi<true, true>(t_s, mk, sl2, mL, base)
-                                 : tile_row_max_alibi<false, true>(t_s, mk, sl2, mL, base);
+                    mx = partial ? tile_row_max_alibi<MASK_ANY, true>(t_s, mk, sl2, mL, base)
+                                 : tile_row_max_alibi<MASK_NONE, true>(t_s, mk, sl2, mL, base);
             } else if constexpr (BIAS == BIAS_MATRIX) {
-                mx = partial ? tile_row_max_matbias<true>(t_s, mk, sl2, bv) : tile_row_max_matbias<false>(t_s, mk, sl2, bv);
+                mx = partial ? tile_row_max_matbias<MASK_ANY>(t_s, mk, sl2, bv) : tile_row_max_matbias<MASK_NONE>(t_s, mk, sl2, bv);
             } else {
-                mx = partial ? tile_row_max<true>(t_s, mk) : tile_row_max<false>(t_s, mk);
+                mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
+                     : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
                     // the tile's constant part of the bias, m_a (c0 - i), in log2 units
@@ -686,22 +698,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if constexpr (ALIBI) {
                 fix();
                 if (causal_kind)
-                    sum = partial ? tile_exp_store_alibi<true, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
-                                  : tile_exp_store_alibi<false, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
+                    sum = partial ? tile_exp_store_alibi<MASK_ANY, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi<MASK_NONE, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
                 else
-                    sum = partial ? tile_exp_store_alibi<true, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
-                                  : tile_exp_store_alibi<false, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
+                    sum = partial ? tile_exp_store_alibi<MASK_ANY, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi<MASK_NONE, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
             } else if constexpr (BIAS == BIAS_MATRIX) {
                 fix();
-                sum = tile_exp_store<false>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);  // x is already scaled, biased and masked
+                sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);  // x is already scaled, biased and masked
             } else if constexpr (F8) {
                 fix();
-                sum = partial ? tile_exp_store_e4m3<true>(t_s, mk, sl2, ref, bar(B_PFULL))
-                              : tile_exp_store_e4m3<false>(t_s, mk, sl2, ref, bar(B_PFULL));
+                sum = partial ? tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL))
+                              : tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
-                sum = partial ? tile_exp_store<true>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                              : tile_exp_store<false>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
+                sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                      : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                              : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
             }
             l += sum;
             tmem_wait_st();
