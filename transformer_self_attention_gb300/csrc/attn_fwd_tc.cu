@@ -708,8 +708,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);  // x is already scaled, biased and masked
             } else if constexpr (F8) {
                 fix();
-                sum = partial ? tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL))
-                              : tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL));
+                sum = !partial ? tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL))
+                      : upper ? tile_exp_store_e4m3<MASK_UPPER>(t_s, mk, sl2, ref, bar(B_PFULL))
+                              : tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
                 sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
