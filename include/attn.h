@@ -216,6 +216,17 @@ attn_status attn_poll_device_error(attn_handle h, int* code);
 attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream);
 
 /*
+ * attn_selftest_device_once -- host-only test hook of the per-device set-up registry
+ * the launchers use for kernel attributes (the dynamic shared-memory opt-in belongs to
+ * a device context, so it is made once per device and kernel, not once per process).
+ * Exercises the registry with fake device ids from several host threads: each
+ * (device, kernel, value) entry must run its set-up exactly once, a failed set-up must
+ * run again on the next call, and distinct devices must not share entries.  Touches no
+ * GPU.  Returns 0 when every check holds, else the number of the first failed check.
+ */
+int attn_selftest_device_once(void);
+
+/*
  * attn_set_alibi -- add the ALiBi score bias to every later attn_forward of this
  * handle: logits_ij = scale * q_i . k_j + b_ij with b_ij = -slopes[a] * |i - j|.
  *   - The additive-bias form logits = q.k / sqrt(d_k) + b_ij and ALiBi's

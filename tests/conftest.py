@@ -26,3 +26,17 @@ def read_golden(name):
             key, *vals = line.split()
             out.setdefault(key, []).append(vals)
     return out
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the error norms of the full-size parity comparisons (also under -q)."""
+    try:
+        from gpu_util import REPORT
+    except Exception:
+        return
+    if not REPORT:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity against the fp64 oracle over the compared outputs")
+    for name in sorted(REPORT):
+        tr.write_line(f"{name}: {REPORT[name]}")

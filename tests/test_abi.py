@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def _declared_functions():
     text = open(os.path.join(ROOT, "include", "attn.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:attn_status|const char\s*\*)\s*(attn_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:attn_status|int|const char\s*\*)\s*(attn_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -79,3 +79,10 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(tsa, "LIB_PATH", str(tmp_path / "libattn.so"))
     with pytest.raises(ImportError):
         tsa._load()
+
+
+def test_kernel_setup_is_made_once_per_device():
+    """The shared-memory opt-in of a kernel belongs to a device context: the launchers' registry
+    runs it once per (device, kernel), from any number of host threads, and again after a
+    failure (fake device ids; no GPU is touched)."""
+    assert tsa.attn_selftest_device_once() == 0

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import small
+from gpu_util import REPORT, small
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +52,9 @@ def _cmp(name, got, ref):
     assert rel <= GRAD_REL_L2, f"{name}: relative L2 error {rel:.3e}"
     assert mx <= GRAD_MAX_REL, f"{name}: max error {mx:.3e} of max |ref|"
     print(f"GRADERR {name} rel_l2 {rel:.3e} max_rel {mx:.3e}")
+    if "every element" in name:
+        REPORT[f"causal_mha_B2_H32_S4096_d128 backward {name}"] = (
+            f"elements {ref.size}  max |error| / max |gradient| {mx:.3e}  rel-L2 {rel:.3e}")
     return rel, mx
 
 
@@ -127,20 +130,25 @@ def test_backward_unsupported_configurations():
 
 def test_backward_full_size_causal_mha_4k():
     """The causal MHA workload (B 2, H 32, S 4096, d 128) at full size, in the launch
-    configuration bench.py times: one (batch, head) slice against the oracle in full, and
-    on every head the identities that hold at any size -- the rows of P sum to one, so
+    configuration bench.py times: every element of dQ, dK and dV against the oracle (one
+    oracle call per (batch, head) slice, exact for MHA), with the norms taken over the whole
+    tensors; and the identities that hold at any size -- the rows of P sum to one, so
     sum_j dV_j = sum_i dO_i, and the rows of dS sum to zero, so sum_j dK_j = 0."""
     w = wl.CAUSAL_MHA_4K
+    assert w.Hq == w.Hkv
     Qc, Kc, Vc = wl.make_inputs(w)
     dOc = wl.make_grad_output(w)
     dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda())
     for t in (dQ, dK, dV):
         assert torch.isfinite(t).all()
-    b, a = 1, 17
-    sl = lambda t: t[b:b + 1, a:a + 1].float().numpy()
-    ref = oracle.backward(sl(Qc), sl(Kc), sl(Vc), sl(dOc), w.scale, w.kind)
-    for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref):
-        _cmp(n, g[b:b + 1, a:a + 1], r)
+    refs = [np.empty(t.shape, dtype=np.float64) for t in (dQ, dK, dV)]
+    for b in range(w.B):
+        for a in range(w.Hq):
+            sl = lambda t: t[b:b + 1, a:a + 1].float().numpy()
+            for r, x in zip(refs, oracle.backward(sl(Qc), sl(Kc), sl(Vc), sl(dOc), w.scale, w.kind)):
+                r[b:b + 1, a:a + 1] = x
+    for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        _cmp(f"{n} (every element)", g, r)
     # identities on every head (fp64 sums of the bf16 gradients)
     dV64 = dV.double().sum(dim=2)
     dO64 = dOc.double().cuda().sum(dim=2)

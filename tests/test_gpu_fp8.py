@@ -1,14 +1,25 @@
 """E4M3 (FP8) inputs on the GPU vs the fp64 oracle over the dequantised values.
 
-The oracle attends over q8 * dq, k8 * dk, v8 * dv exactly; the remaining difference is
-the E4M3 rounding of P before the second product and fp32 accumulation.  Round to
-nearest with 3 mantissa bits gives each weight a relative error of at most 2^-4, with a
-standard deviation of about 2^-4 / sqrt(3) = 0.036.  The error of an output row,
-sum_j delta_j p_j v_j / l, is bounded by 2^-4 * max|v| (all errors of one sign), and
-relative to |O| it is largest where O is an average of many values that cancel (full
-and wide-window rows).  Bounds: max-abs 0.15 (2^-4 times ~2.4, below the largest
-value magnitudes) and relative L2 5e-2 (just under 2^-4).  LSE comes from the fp32
-weights and keeps the bf16 path's 1e-3.
+The oracle attends over q8 * dq, k8 * dk, v8 * dv exactly.  The kernel differs from it
+at a few rounding points only: P is rounded to E4M3 before the second product (with
+the running max of the lazy rescale as its reference, so P <= 2^8), the row sums use
+the unrounded fp32 weights, and O is rounded to bf16 at the end; the products of E4M3
+values are exact and their sums fp32.
+
+Tolerance.  A CPU model of exactly those rounding points (`_e4m3_model`: the kernel's
+per-tile running max with its 2^8 threshold, E4M3 round-to-nearest-even of fp32 P, fp32
+row sums, bf16 rounding of O) is run on the same inputs, and its error against the
+oracle sets the bounds.  Where the model and the kernel take the same rounding decisions
+their outputs agree to fp32 summation order, so:
+  * relative L2 against the oracle <= 1.25 x the model's + 1e-3;
+  * max-abs against the oracle <= 1.5 x the model's + 4e-3 (the worst element can come
+    from a weight whose rounding falls the other way on a midpoint);
+  * relative L2 between the GPU and the model <= 0.25 x the model's own error + 1e-3: the
+    kernel must follow the model much more closely than the model follows the oracle, so
+    a real regression (a lost tile, a wrong scale, a stale P) cannot hide inside the E4M3
+    rounding error.
+The floors cover cases where E4M3 rounding is exact, such as a single key.  LSE comes
+from the fp32 weights and keeps the bf16 path's 1e-3.
 """
 import numpy as np
 import pytest
@@ -16,11 +27,64 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_util import LSE_ABS, sample_rows, small
+from gpu_util import LSE_ABS, REPORT, small
 
 pytestmark = pytest.mark.gpu
 
-FP8_MAX_ABS, FP8_REL_L2 = 0.15, 5e-2
+MAX_ABS_FACTOR, REL_L2_FACTOR, TRACK_FACTOR = 1.5, 1.25, 0.25
+FLOOR_MAX_ABS, FLOOR_REL_L2 = 4e-3, 1e-3
+LOG2E = 1.4426950408889634
+
+
+def _allowed(kind, S, window):
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    if kind == wl.MASK_FULL:
+        return np.ones((S, S), dtype=bool)
+    if kind == wl.MASK_CAUSAL:
+        return j <= i
+    if kind == wl.MASK_SLIDING:
+        return np.abs(i - j) <= window
+    if kind == wl.MASK_CAUSAL_SLIDING:
+        return (j <= i) & (i - j <= window)
+    raise ValueError(kind)
+
+
+def _e4m3_model(w, Q8, K8, V8, dq, dk, dv):
+    """O as the E4M3 kernel rounds it (see the module docstring), float64 [B, Hq, S, d].
+
+    The scores are fp32 sums of exact E4M3 products, as on the tensor core; the weights are
+    fp32 exponentials rounded to E4M3; O is accumulated in float64 and rounded to bf16."""
+    q = Q8.float().numpy()
+    k = K8.float().numpy()
+    v = V8.float().double().numpy()
+    B, Hq, S, d = q.shape
+    g = Hq // k.shape[1]
+    T = 128
+    nt = (S + T - 1) // T
+    ok = _allowed(w.kind, S, w.window)
+    sl2 = np.float32(w.scale * dq * dk * LOG2E)
+    out = np.empty((B, Hq, S, d), dtype=np.float64)
+    for b in range(B):
+        for a in range(Hq):
+            x = np.full((S, nt * T), -np.inf, dtype=np.float32)
+            x[:, :S] = np.where(ok, (q[b, a] @ k[b, a // g].T) * sl2, np.float32(-np.inf))
+            tmax = x.reshape(S, nt, T).max(axis=2)
+            ref = np.empty_like(tmax)
+            m = np.full(S, -np.inf, dtype=np.float32)
+            for t in range(nt):  # the lazy rescale: the reference moves only when the max grows by > 2^8
+                grow = tmax[:, t] > m + 8.0
+                m = np.where(grow, tmax[:, t], m)
+                ref[:, t] = m
+            fin = np.isfinite(ref)
+            refc = np.where(fin, ref, np.float32(0.0))
+            p32 = np.exp2(x[:, :S] - np.repeat(refc, T, axis=1)[:, :S])
+            pr = torch.from_numpy(p32).to(torch.float8_e4m3fn).double().numpy()
+            fac = np.repeat(np.where(fin, np.exp2(refc.astype(np.float64) - m[:, None]), 0.0), T, axis=1)[:, :S]
+            num = (pr * fac) @ v[b, a // g]
+            den = (p32.astype(np.float64) * fac).sum(axis=1)
+            out[b, a] = num / den[:, None] * dv
+    return torch.from_numpy(out).float().to(torch.bfloat16).double().numpy()
 
 
 def _run(w):
@@ -36,14 +100,27 @@ def _run(w):
     return O.float().cpu().numpy(), L.cpu().numpy(), (Q8, K8, V8, dq, dk, dv)
 
 
-def _check(O, L, O_ref, L_ref):
+def _norms(O, O_ref):
+    d = np.asarray(O, dtype=np.float64) - O_ref
+    return float(np.abs(d).max()), float(np.linalg.norm(d) / np.linalg.norm(O_ref))
+
+
+def _check(O, L, O_ref, L_ref, O_model, report=None):
     assert np.isfinite(O).all() and np.isfinite(L).all()
-    d = O.astype(np.float64) - O_ref
-    max_abs = float(np.abs(d).max())
-    rel = float(np.linalg.norm(d) / np.linalg.norm(O_ref))
-    lse = float(np.abs(L - L_ref).max())
-    print(f"fp8 errors: max-abs {max_abs:.3e} rel-L2 {rel:.3e} LSE {lse:.3e}")
-    assert max_abs <= FP8_MAX_ABS and rel <= FP8_REL_L2 and lse <= LSE_ABS, (max_abs, rel, lse)
+    max_abs, rel = _norms(O.reshape(O_ref.shape), O_ref)
+    m_abs, m_rel = _norms(O_model.reshape(O_ref.shape), O_ref)
+    g_abs, g_rel = _norms(O.reshape(O_ref.shape), O_model.reshape(O_ref.shape))
+    lse = float(np.abs(L.reshape(L_ref.shape) - L_ref).max())
+    bound_abs = MAX_ABS_FACTOR * m_abs + FLOOR_MAX_ABS
+    bound_rel = REL_L2_FACTOR * m_rel + FLOOR_REL_L2
+    bound_track = TRACK_FACTOR * m_rel + FLOOR_REL_L2
+    line = (f"rows {O_ref.shape[0] if O_ref.ndim == 2 else O_ref.size // O_ref.shape[-1]}  max-abs {max_abs:.3e} "
+            f"(bound {bound_abs:.3e})  rel-L2 {rel:.3e} (bound {bound_rel:.3e})  LSE {lse:.3e}  "
+            f"GPU vs rounding model rel-L2 {g_rel:.3e} (bound {bound_track:.3e}), max-abs {g_abs:.3e}")
+    print("fp8 errors:", line)
+    if report:
+        REPORT[report] = line
+    assert max_abs <= bound_abs and rel <= bound_rel and g_rel <= bound_track and lse <= LSE_ABS, line
 
 
 @pytest.mark.parametrize("S", [1, 129, 300])
@@ -53,18 +130,28 @@ def test_fp8_kinds(kind, S):
     O, L, (Q8, K8, V8, dq, dk, dv) = _run(w)
     O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
                                     w.kind, w.window)
-    _check(O, L, O_ref * dv, L_ref)
+    _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv))
+
+
+def test_fp8_rounding_model_is_not_trivial():
+    """The model's own error is the E4M3 rounding of P: well above bf16 rounding, well below
+    the raw 2^-4 worst case, on the 300-token causal case."""
+    w = small("f8m", 1, 2, 2, 300, 128, "bf16", wl.MASK_CAUSAL)
+    Q8, K8, V8, (dq, dk, dv) = wl.make_fp8_inputs(w)
+    O_ref, _ = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                w.kind, w.window)
+    m_abs, m_rel = _norms(_e4m3_model(w, Q8, K8, V8, dq, dk, dv), O_ref * dv)
+    assert 1e-3 < m_rel < 2.0 ** -4, m_rel
 
 
 def test_fp8_full_size_causal_4k():
+    """Every output of the causal 4K workload against the oracle, bounds from the model."""
     w = wl.CAUSAL_MHA_4K
     O, L, (Q8, K8, V8, dq, dk, dv) = _run(w)
-    rows = sample_rows(w, n_random=96)
-    Qn = Q8.float().numpy()
-    O_ref, L_ref = oracle.attention_rows(K8.float().numpy(), V8.float().numpy(), w.Hq, w.scale * dq * dk, w.kind,
-                                         w.window, None, Qn[rows[:, 0], rows[:, 1], rows[:, 2]], rows[:, 0],
-                                         rows[:, 1], rows[:, 2])
-    _check(O[rows[:, 0], rows[:, 1], rows[:, 2]], L[rows[:, 0], rows[:, 1], rows[:, 2]], O_ref * dv, L_ref)
+    O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                    w.kind, w.window)
+    _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv),
+           report=f"{w.name} E4M3 (every row)")
 
 
 def test_fp8_unsupported_shapes():

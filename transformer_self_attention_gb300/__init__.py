@@ -31,7 +31,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
             "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode",
-            "attn_decode_launch_count")
+            "attn_decode_launch_count", "attn_selftest_device_once")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -85,6 +85,8 @@ def _load():
     lib.attn_forward_noalloc.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
     lib.attn_selftest_exp2.restype = I
+    lib.attn_selftest_device_once.argtypes = []
+    lib.attn_selftest_device_once.restype = I
     lib.attn_decode_create.argtypes = [ctypes.POINTER(P), I, I, I, I, I, I, F, I, I]
     lib.attn_decode_create.restype = I
     lib.attn_decode_forward.argtypes = [P, P, P, P, P, P, P, P]
@@ -174,6 +176,11 @@ def attn_forward_noalloc(B, Hq, Hkv, S, d_k, scale, kind, window, global_idx, q_
 def attn_selftest_exp2(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> int:
     """Test hook: the library's FMA-pipe exp2 applied elementwise (device float arrays)."""
     return _lib.attn_selftest_exp2(x_ptr, y_ptr, int(n), stream or None)
+
+
+def attn_selftest_device_once() -> int:
+    """Host-only test hook of the per-device kernel set-up registry (0 = every check held)."""
+    return _lib.attn_selftest_device_once()
 
 
 def attn_schedule_host(B, Hq, Hkv, S, kind, window=0, global_idx=None):

@@ -10,9 +10,11 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 #include "attn.h"
+#include "device_once.h"
 #include "kernels.h"
 #include "schedule.h"
 
@@ -50,6 +52,13 @@ struct attn_plan {
     attn::TcParams tp{};
     bool debug = false;
 };
+
+namespace attn {
+DeviceOnce& device_once() {
+    static DeviceOnce registry;
+    return registry;
+}
+}  // namespace attn
 
 namespace {
 
@@ -403,6 +412,39 @@ attn_status attn_selftest_exp2(const float* x, float* y, int n, void* stream) {
     if (!x || !y || n < 0) return ATTN_ERR_INVALID_ARG;
     return attn::launch_exp2_selftest(x, y, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
                                                                                                  : ATTN_ERR_CUDA;
+}
+
+int attn_selftest_device_once(void) {
+    attn::DeviceOnce reg;  // a private registry: the library's own is left untouched
+    static const int kA = 0, kB = 0;
+    const void* fa = &kA;
+    const void* fb = &kB;
+    int runs[4][2] = {};
+    std::mutex mu;
+    auto body = [&](int dev, int k) {
+        return reg.run(dev, k ? fb : fa, 1024, [&] {
+            std::lock_guard<std::mutex> lock(mu);
+            ++runs[dev][k];
+            return cudaSuccess;
+        });
+    };
+    std::vector<std::thread> ts;
+    for (int t = 0; t < 8; ++t)
+        ts.emplace_back([&, t] {
+            for (int r = 0; r < 50; ++r)
+                for (int dev = 0; dev < 4; ++dev) body((dev + t) & 3, (r + t) & 1);
+        });
+    for (auto& t : ts) t.join();
+    for (int dev = 0; dev < 4; ++dev)
+        for (int k = 0; k < 2; ++k)
+            if (runs[dev][k] != 1) return 1;  // once per (device, kernel), whatever the threads
+    int tries = 0;
+    auto failing = [&] { ++tries; return tries < 2 ? cudaErrorInvalidValue : cudaSuccess; };
+    if (reg.run(5, fa, 7, failing) != cudaErrorInvalidValue) return 2;
+    if (reg.seen(5, fa, 7)) return 3;       // a failed set-up is not recorded
+    if (reg.run(5, fa, 7, failing) != cudaSuccess || tries != 2) return 4;
+    if (!reg.seen(5, fa, 7) || reg.seen(6, fa, 7) || reg.seen(5, fa, 8)) return 5;
+    return 0;
 }
 
 attn_status attn_set_alibi(attn_handle h, const float* slopes) {

@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
 
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
 
 template <class F>
 cudaError_t configure(F kernel, int smem) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return smem_opt_in(reinterpret_cast<const void*>(kernel), smem);
 }
 
 }  // namespace
@@ -738,15 +739,12 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
-    static bool c64 = false, c128 = false;
     cudaError_t e = cudaSuccess;
     if (d == 128) {
-        if (!c128 && (e = configure(attn_bwd_dq_kernel<128>, DqCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
-        c128 = true;
+        if ((e = configure(attn_bwd_dq_kernel<128>, DqCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
         attn_bwd_dq_kernel<128><<<n_items, NTHREADS, DqCfg<128>::SMEM_ALLOC, stream>>>(p);
     } else if (d == 64) {
-        if (!c64 && (e = configure(attn_bwd_dq_kernel<64>, DqCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
-        c64 = true;
+        if ((e = configure(attn_bwd_dq_kernel<64>, DqCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
         attn_bwd_dq_kernel<64><<<n_items, NTHREADS, DqCfg<64>::SMEM_ALLOC, stream>>>(p);
     } else {
         return cudaErrorInvalidValue;
@@ -756,15 +754,12 @@ cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t s
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream) {
     if (n_ctas <= 0) return cudaSuccess;
-    static bool c64 = false, c128 = false;
     cudaError_t e = cudaSuccess;
     if (d == 128) {
-        if (!c128 && (e = configure(attn_bwd_dkdv_kernel<128>, KvCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
-        c128 = true;
+        if ((e = configure(attn_bwd_dkdv_kernel<128>, KvCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
         attn_bwd_dkdv_kernel<128><<<n_ctas, NTHREADS, KvCfg<128>::SMEM_ALLOC, stream>>>(p);
     } else if (d == 64) {
-        if (!c64 && (e = configure(attn_bwd_dkdv_kernel<64>, KvCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
-        c64 = true;
+        if ((e = configure(attn_bwd_dkdv_kernel<64>, KvCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
         attn_bwd_dkdv_kernel<64><<<n_ctas, NTHREADS, KvCfg<64>::SMEM_ALLOC, stream>>>(p);
     } else {
         return cudaErrorInvalidValue;

@@ -52,6 +52,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
 
@@ -835,13 +836,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
 template <int D, int NP, bool ALIBI>
 cudaError_t launch_one(const DecodeParams& p, cudaStream_t stream) {
     using C = DCfg<D, NP>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<D, NP, ALIBI>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_decode_kernel<D, NP, ALIBI>), C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
     attn_decode_kernel<D, NP, ALIBI><<<p.n_cta, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }

@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
 
@@ -813,13 +814,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
 template <int D, int BIAS, bool F8 = false>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
     using C = Cfg<D, BIAS, F8>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, BIAS, F8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8>), C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
     attn_fwd_tc_kernel<D, BIAS, F8><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
