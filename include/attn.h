@@ -142,23 +142,28 @@ const char* attn_status_string(attn_status s);
  *   [5] full_end    allowed and no mask is applied; the other tiles of
  *                   [kv_begin, kv_end) are PARTIAL and evaluate the mask predicate
  *   [6] flags       ATTN_WORK_GLOBAL_COLS: after the key tiles, also evaluate
- *                   the gathered global keys G not inside [kv_begin, kv_end) tiles;
- *                   ATTN_WORK_GLOBAL_ROWS: the item's rows are the global rows
- *   [7] n_gtiles    number of gathered global-key tiles (ATTN_WORK_GLOBAL_COLS);
+ *                   the global keys G not inside the [kv_begin, kv_end) tiles,
+ *                   gathered into narrow key tiles of at most ATTN_TILE keys;
+ *                   ATTN_WORK_GLOBAL_ROWS: the item's rows are the global rows;
+ *                   ATTN_WORK_HAS_GLOBAL_ROWS: the item's query tile holds rows of G,
+ *                   whose outputs the item does not write
+ *   [7] n_gtiles    number of gathered global-key tiles (ATTN_WORK_GLOBAL_COLS):
+ *                   ceil(#(G outside the band) / ATTN_TILE);
  *                   for ATTN_WORK_GLOBAL_ROWS items: the index of the item's key
- *                   chunk.  The global-row pass splits the key tiles into chunks of
- *                   equal length (one item per chunk, gathered row tile and head);
- *                   each chunk yields a partial softmax result and a merge step
- *                   combines them: O = sum_c e^LSE_c O_c / sum_c e^LSE_c,
- *                   LSE = ln sum_c e^LSE_c.
- * Items are ordered by decreasing number of tiles (longest first).
- * For LOCAL_GLOBAL, rows in G are computed only by ATTN_WORK_GLOBAL_ROWS items,
- * which run after all other items.
+ *                   chunk.  The global rows' key tiles are split into chunks no
+ *                   longer than the longest query-tile item (one item per chunk,
+ *                   gathered row tile and head); each chunk yields a partial softmax
+ *                   result and the chunk that finishes last combines them:
+ *                   O = sum_c e^LSE_c O_c / sum_c e^LSE_c, LSE = ln sum_c e^LSE_c.
+ * The query-tile items come first, ordered by decreasing number of tiles (longest
+ * first); for LOCAL_GLOBAL the ATTN_WORK_GLOBAL_ROWS items follow them.  All items
+ * run in one launch: rows in G are written only by ATTN_WORK_GLOBAL_ROWS items.
  */
 #define ATTN_TILE 128
 #define ATTN_WORK_INTS 8
 #define ATTN_WORK_GLOBAL_COLS 1
 #define ATTN_WORK_GLOBAL_ROWS 2
+#define ATTN_WORK_HAS_GLOBAL_ROWS 4
 
 /*
  * attn_schedule_host -- build the schedule attn_create would build for these
@@ -167,8 +172,8 @@ const char* attn_status_string(attn_status s);
  *   items   : output, room for `cap` items (cap * ATTN_WORK_INTS ints); may be
  *             NULL with cap = 0 to query the sizes only.
  *   n_items : receives the total number of items.
- *   n_first : receives the number of items of the first launch; the remaining
- *             items (ATTN_WORK_GLOBAL_ROWS) form a second launch.
+ *   n_first : receives the number of query-tile items; the remaining items are
+ *             the ATTN_WORK_GLOBAL_ROWS chunks (all items run in one launch).
  * Returns ATTN_ERR_INVALID_ARG if cap is nonzero but smaller than the total.
  */
 attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window,
@@ -323,21 +328,24 @@ attn_status attn_set_watchdog(attn_handle h, long long limit_ns, int withhold);
  *                   buffers; LSE may be NULL).
  *
  * Instead of handle-owned buffers, the call keeps its scratch (error word,
- * work list, global-token list and bits, gathered global rows) in one fixed
+ * work list, global-token list and bits, and for the local + global mask the
+ * partial results and arrival counters of the global-row chunks) in one fixed
  * device array of ATTN_NOALLOC_SCRATCH_BYTES, a file-scope __device__ object
  * that every GPU which loads this library holds until the process exits.
  * A problem whose scratch does not fit returns ATTN_ERR_UNSUPPORTED before
  * anything is launched (the work list takes 32 bytes per (batch, head,
- * 128-row tile); the local + global mask adds B*(Hq + 2*Hkv)*n_global*d_k*2
- * bytes of gathered rows and B*Hq*n_global*chunks*(d_k+1)*4 bytes of partial
- * results of the chunked global-row pass).
+ * 128-row tile); the local + global mask adds B*Hq*n_global*chunks*(d_k+1)*4
+ * bytes of partial results of the chunked global rows).
  *
  * The first call on a device looks up the array's address (once per device,
  * with that device current); make that first call before any stream capture.
  * Every call shares the one array and leaves its contents behind: calls that
  * overlap on the GPU (two streams, or two host threads) race and must be
- * serialised by the caller.  The call copies its schedule from host memory
- * with cudaMemcpyAsync on `stream` and returns without waiting for the kernels.
+ * serialised by the caller.  The call passes its schedule to the device inside
+ * kernel parameters (copied by the launch; no host buffer is read after the
+ * call returns), clears the counters that must start at zero, and returns
+ * without waiting for the kernels.  Device watchdog bits of every call collect
+ * in the array's error word until attn_forward_noalloc_poll_error reads them.
  * Errors: as attn_create and attn_forward, plus ATTN_ERR_UNSUPPORTED above.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -345,6 +353,26 @@ attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d_k, float s
                                  attn_mask_kind kind, int window, const int* global_idx,
                                  int n_global, const void* Q, const void* K, const void* V,
                                  void* O, float* LSE, void* stream);
+
+/*
+ * attn_forward_noalloc_poll_error -- synchronise the device, read the error word
+ * of attn_forward_noalloc's scratch array on the current device into *code
+ * (0 = none, otherwise a bit set of the kernel roles whose bounded wait ran
+ * out, collected over every call since the last poll), clear it, and return
+ * ATTN_ERR_DEVICE_TIMEOUT if it was nonzero.  Allocates nothing.  The outputs of
+ * a call that set a bit are undefined.  Errors: ATTN_ERR_INVALID_ARG (code NULL),
+ * ATTN_ERR_CUDA.
+ */
+attn_status attn_forward_noalloc_poll_error(int* code);
+
+/*
+ * attn_forward_noalloc_set_watchdog -- test hook of attn_forward_noalloc, as
+ * attn_set_watchdog for a handle: limit_ns bounds every wait inside its kernels
+ * (default 2e9 ns), withhold = 1 makes the producer never load V so the first
+ * wait for V runs out.  Applies to the calls made after it, process-wide.
+ * Errors: ATTN_ERR_INVALID_ARG (limit_ns <= 0, withhold not 0 or 1).
+ */
+attn_status attn_forward_noalloc_set_watchdog(long long limit_ns, int withhold);
 
 /*
  * ---------------------------------------------------------------- decode

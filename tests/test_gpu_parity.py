@@ -62,6 +62,27 @@ def test_bf16_local_global_many_globals():
                         globals_idx=list(range(3, 700, 5))[:129]))
 
 
+def test_local_global_repeated_calls_merge_every_time():
+    """One handle, three calls with other inputs: the chunk counters of the global rows return to
+    zero after every call (two global-row tiles, chunked keys, two gathered key tiles)."""
+    G = sorted(set(range(2, 900, 4)) | {899})  # 226 globals
+    w = small("lgrep", 1, 2, 1, 900, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=20, globals_idx=G)
+    items, n_first = tsa_schedule(w)
+    assert 1 + max(int(it[7]) for it in items[n_first:]) > 1 and max(int(it[7]) for it in items[:n_first]) == 2
+    plan = None
+    for seed in (5, 6, 7):
+        ww = w.with_(seed=seed)
+        Qc, Kc, Vc = wl.make_inputs(ww)
+        O, LSE, plan = run_cuda(ww, Qc.cuda(), Kc.cuda(), Vc.cuda(), plan=plan)
+        O_ref, L_ref = oracle_rows(ww, Qc, Kc, Vc, all_rows(ww))
+        compare(ww, *gather_rows(O, LSE), O_ref, L_ref)
+
+
+def tsa_schedule(w):
+    import transformer_self_attention_gb300 as tsa
+    return tsa.attn_schedule_host(w.B, w.Hq, w.Hkv, w.S, w.kind, w.window, list(w.globals_idx))
+
+
 @pytest.mark.parametrize("kind", K_ALL)
 @pytest.mark.parametrize("S", [1, 100, 257])
 def test_f32_path_kinds(kind, S):

@@ -36,3 +36,25 @@ def test_withheld_load_times_out_and_context_survives():
     O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, rows)
     compare(w, O.float().cpu().numpy().reshape(-1, w.d), LSE.cpu().numpy().ravel(), O_ref, L_ref)
     torch.cuda.synchronize()
+
+
+def test_local_global_abort_keeps_the_chunk_counters_consistent():
+    """Local + global with chunked global rows: every chunk item counts itself in even when its
+    wait ran out, so the counters return to zero and the next call merges correctly."""
+    w = small("wdlg", 1, 2, 2, 700, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=(0, 1, 350, 699))
+    Qc, Kc, Vc = wl.make_inputs(w)
+    Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, kind=w.kind, window=w.window, global_idx=list(w.globals_idx))
+    items, n_first = tsa.attn_schedule_host(w.B, w.Hq, w.Hkv, w.S, w.kind, w.window, list(w.globals_idx))
+    assert 1 + max(int(it[7]) for it in items[n_first:]) > 1  # the global rows are chunked
+    plan.set_watchdog(50_000_000, withhold=1)
+    plan(Q, K, V)
+    st, code = plan.poll_device_error()
+    assert st == tsa.ATTN_ERR_DEVICE_TIMEOUT and code != 0
+    plan.set_watchdog(2_000_000_000, withhold=0)
+    for _ in range(2):
+        O, LSE, _ = run_cuda(w, Q, K, V, plan=plan)
+        bb, aa, ii = np.meshgrid(np.arange(w.B), np.arange(w.Hq), np.arange(w.S), indexing="ij")
+        rows = np.stack([bb.ravel(), aa.ravel(), ii.ravel()], axis=1)
+        O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, rows)
+        compare(w, O.float().cpu().numpy().reshape(-1, w.d), LSE.cpu().numpy().ravel(), O_ref, L_ref)

@@ -4,8 +4,8 @@ For every listed key tile the schedule's class (FULL / PARTIAL) must equal the
 oracle's enumerated class; unlisted tiles must be SKIP (for local + global: hold
 no allowed pair outside the global rows and columns); and simulating what the
 kernels evaluate from the work items -- FULL tiles whole, PARTIAL tiles through
-the in-tile predicate, gathered global keys, the dense global-row pass -- must
-count exactly the allowed pairs of every row, each once.
+the in-tile predicate, the gathered global keys outside a tile's band, the dense
+global-row chunks -- must count exactly the allowed pairs of every row, each once.
 """
 import numpy as np
 import pytest
@@ -77,10 +77,13 @@ def _simulate(items, n_first, kind, S, w, G, check_classes=True):
         if check_classes and not lg:
             for t in set(range(classes.shape[1])) - set(range(kb, ke)):
                 assert classes[qt, t] == 0, (qt, t)
+        n_out = int(((Garr < kb * T) | (Garr >= ke * T)).sum()) if lg else 0
+        assert bool(flags & tsa.WORK_GLOBAL_COLS) == (n_out > 0)
+        assert bool(flags & tsa.WORK_HAS_GLOBAL_ROWS) == bool(lg and isg[i].any())
         if flags & tsa.WORK_GLOBAL_COLS:
-            assert lg and ngt == (len(G) + T - 1) // T
-            outside = (Garr < kb * T) | (Garr >= ke * T)
-            counts[i[keep]] += int(outside.sum())
+            # the gathered tiles hold exactly the global keys outside the band, every one allowed
+            assert lg and ngt == (n_out + T - 1) // T
+            counts[i[keep]] += n_out
     assert seen_tiles == set(range((S + T - 1) // T))
     nk = (S + T - 1) // T
     for qt, cs in chunks.items():  # the chunks of each gathered row tile cover [0, nk) once, in order
@@ -106,6 +109,8 @@ def _check(kind, S, w=0, G=(), B=1, Hq=2, Hkv=1, check_classes=True):
     # longest first
     cost = (items[:n_first, 3] - items[:n_first, 2]) + items[:n_first, 7]
     assert np.all(np.diff(cost) <= 0)
+    if len(items) > n_first:  # global-row chunks are no longer than the longest query-tile item
+        assert np.all(items[n_first:, 3] - items[n_first:, 2] <= max(1, int(cost.max())))
     counts = _simulate(items, n_first, kind, S, w, set(G), check_classes)
     expect = oracle.row_counts(kind, S, w, list(G))
     assert np.array_equal(counts, expect)

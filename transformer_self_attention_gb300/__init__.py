@@ -23,7 +23,7 @@ MASK_FULL, MASK_CAUSAL, MASK_SLIDING, MASK_CAUSAL_SLIDING, MASK_LOCAL_GLOBAL = r
 ATTN_BF16, ATTN_F32, ATTN_FP8_E4M3 = 0, 1, 2
 TILE = 128
 WORK_INTS = 8
-WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS = 1, 2
+WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS, WORK_HAS_GLOBAL_ROWS = 1, 2, 4
 
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
             "attn_poll_device_error", "attn_set_watchdog", "attn_forward_noalloc", "attn_selftest_exp2",
@@ -31,7 +31,8 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_schedule_host", "attn_decode_set_grid_limit", "attn_set_alibi",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
             "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode",
-            "attn_decode_launch_count", "attn_selftest_device_once")
+            "attn_decode_launch_count", "attn_selftest_device_once", "attn_forward_noalloc_poll_error",
+            "attn_forward_noalloc_set_watchdog")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -83,6 +84,10 @@ def _load():
     lib.attn_decode_launch_count.restype = I
     lib.attn_forward_noalloc.argtypes = [I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P]
     lib.attn_forward_noalloc.restype = I
+    lib.attn_forward_noalloc_poll_error.argtypes = [ctypes.POINTER(I)]
+    lib.attn_forward_noalloc_poll_error.restype = I
+    lib.attn_forward_noalloc_set_watchdog.argtypes = [ctypes.c_longlong, I]
+    lib.attn_forward_noalloc_set_watchdog.restype = I
     lib.attn_selftest_exp2.argtypes = [P, P, I, P]
     lib.attn_selftest_exp2.restype = I
     lib.attn_selftest_device_once.argtypes = []
@@ -171,6 +176,18 @@ def attn_forward_noalloc(B, Hq, Hkv, S, d_k, scale, kind, window, global_idx, q_
     return _lib.attn_forward_noalloc(int(B), int(Hq), int(Hkv), int(S), int(d_k), float(scale), int(kind),
                                      int(window), ctypes.cast(g, ctypes.c_void_p) if ng else None, ng,
                                      q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr or None, stream or None)
+
+
+def attn_forward_noalloc_poll_error():
+    """(status, code): synchronise, read and clear the error word of attn_forward_noalloc's scratch."""
+    code = ctypes.c_int(0)
+    st = _lib.attn_forward_noalloc_poll_error(ctypes.byref(code))
+    return st, code.value
+
+
+def attn_forward_noalloc_set_watchdog(limit_ns: int, withhold: int = 0) -> int:
+    """Test hook: wait limit and V-withholding of attn_forward_noalloc's kernels (process-wide)."""
+    return _lib.attn_forward_noalloc_set_watchdog(int(limit_ns), int(withhold))
 
 
 def attn_selftest_exp2(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> int:

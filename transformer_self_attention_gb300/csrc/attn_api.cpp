@@ -31,10 +31,8 @@ struct attn_plan {
     unsigned* d_gbits = nullptr;
     unsigned char* d_isg = nullptr;
     int* d_err = nullptr;
-    void* d_qg = nullptr;
-    void* d_kg = nullptr;
-    void* d_vg = nullptr;
-    float* d_part = nullptr;  // partial results of the chunked global-row pass
+    float* d_part = nullptr;  // partial results of the chunked global-row items
+    unsigned* d_counters = nullptr;  // their arrival counters (each returns to 0 when its tile is merged)
     float* d_alibi = nullptr;  // ALiBi slopes [Hq] (attn_set_alibi), or null
     // backward scratch (first attn_backward call)
     float* d_lse2 = nullptr;   // [B*Hq, S_pad]
@@ -136,7 +134,6 @@ attn_status validate_shape(int B, int Hq, int Hkv, int S, attn_mask_kind kind, i
     for (int t = 0; t < n_global; ++t)
         if (global_idx[t] < 0 || global_idx[t] >= S) return ATTN_ERR_INVALID_ARG;
     if ((long)B * Hq > (1L << 30)) return ATTN_ERR_UNSUPPORTED;
-    if (n_global > 0 && (long)B * Hq + 2L * B * Hkv > 65535L) return ATTN_ERR_UNSUPPORTED;  // gather grid.y
     return ATTN_OK;
 }
 
@@ -157,7 +154,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 
 void free_plan(attn_plan* h) {
     if (!h) return;
-    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_qg, h->d_kg, h->d_vg, h->d_part,
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_part, h->d_counters,
                     h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork};
     for (void* b : bufs)
         if (b) cudaFree(b);
@@ -226,23 +223,15 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         if ((e = upload(&h->d_gbits, h->sched.global_bits.data(), h->sched.global_bits.size())) != cudaSuccess)
             return fail(e);
         attn::TcParams& p = h->tp;
-        if (nG > 0) {
-            const size_t qg = (size_t)B * Hq * nG * d_k * 2, kg = (size_t)B * Hkv * nG * d_k * 2;
-            if ((e = cudaMalloc(&h->d_qg, qg)) != cudaSuccess) return fail(e);
-            if ((e = cudaMalloc(&h->d_kg, kg)) != cudaSuccess) return fail(e);
-            if ((e = cudaMalloc(&h->d_vg, kg)) != cudaSuccess) return fail(e);
-            if (h->sched.n_chunks > 1) {
-                const size_t rows = (size_t)B * Hq * nG * h->sched.n_chunks;
-                if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_part), rows * (d_k + 1) * sizeof(float))) !=
-                    cudaSuccess)
-                    return fail(e);
-            }
-            if (!encode_map(&p.tm_qg, h->d_qg, d_k, nG, (long)B * Hq, kTileRows) ||
-                !encode_map(&p.tm_kg, h->d_kg, d_k, nG, (long)B * Hkv, kTileRows) ||
-                !encode_map(&p.tm_vg, h->d_vg, d_k, nG, (long)B * Hkv, kTileRows)) {
-                free_plan(h);
-                return ATTN_ERR_CUDA;
-            }
+        p.n_gtiles = (nG + (int)kTileRows - 1) / (int)kTileRows;
+        if (nG > 0 && h->sched.n_chunks > 1) {
+            const size_t rows = (size_t)B * Hq * nG * h->sched.n_chunks;
+            const size_t n_ctr = (size_t)B * Hq * p.n_gtiles;
+            if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_part), rows * (d_k + 1) * sizeof(float))) !=
+                    cudaSuccess ||
+                (e = cudaMalloc(reinterpret_cast<void**>(&h->d_counters), n_ctr * sizeof(unsigned))) != cudaSuccess ||
+                (e = cudaMemset(h->d_counters, 0, n_ctr * sizeof(unsigned))) != cudaSuccess)
+                return fail(e);
         }
         p.work = h->d_work;
         p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;
@@ -259,6 +248,7 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         p.o_scale = 1.f;
         p.part_o = h->d_part;
         p.part_lse = h->d_part ? h->d_part + (size_t)B * Hq * nG * h->sched.n_chunks * d_k : nullptr;
+        p.counters = h->d_counters;
     }
     *out = h;
     return ATTN_OK;
@@ -304,30 +294,12 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         }
         p.o = O;
         p.lse = LSE;
-        if (nG > 0) {
-            attn::GatherParams g{};
-            g.q = static_cast<const uint16_t*>(Q); g.k = static_cast<const uint16_t*>(K);
-            g.v = static_cast<const uint16_t*>(V);
-            g.qg = static_cast<uint16_t*>(h->d_qg); g.kg = static_cast<uint16_t*>(h->d_kg);
-            g.vg = static_cast<uint16_t*>(h->d_vg);
-            g.globals = h->d_globals; g.n_global = nG;
-            g.BHq = h->B * h->Hq; g.BHkv = h->B * h->Hkv; g.S = h->S; g.d = h->d;
-            if ((e = attn::launch_gather_globals(g, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-        }
+        p.q = static_cast<const uint16_t*>(Q);
+        p.k = static_cast<const uint16_t*>(K);
+        p.v = static_cast<const uint16_t*>(V);
         p.item_offset = 0;
-        if ((e = attn::launch_tc_forward(p, h->d, h->sched.n_main, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (h->sched.n_grows > 0) {
-            p.item_offset = h->sched.n_main;
-            e = attn::launch_tc_forward(p, h->d, h->sched.n_grows, stream);
-            if (e == cudaSuccess && h->sched.n_chunks > 1) {
-                attn::MergeParams mp{};
-                mp.part_o = p.part_o; mp.part_lse = p.part_lse;
-                mp.o = static_cast<uint16_t*>(O); mp.lse = LSE;
-                mp.globals = h->d_globals; mp.n_global = nG; mp.n_chunks = h->sched.n_chunks;
-                mp.BHq = h->B * h->Hq; mp.S = h->S; mp.d = h->d;
-                e = attn::launch_merge_global_rows(mp, stream);
-            }
-        }
+        // one launch: the query-tile items, then (local + global) the global-row chunks
+        e = attn::launch_tc_forward(p, h->d, h->sched.n_main + h->sched.n_grows, stream);
     }
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
     if (h->debug) {

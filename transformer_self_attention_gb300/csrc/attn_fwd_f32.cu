@@ -1,4 +1,4 @@
-// fp32 attention forward on CUDA cores, and the gather of global-token rows.
+// fp32 attention forward on CUDA cores, and the self-test of the FMA-pipe exp2.
 //
 // The fp32 path keeps full fp32 inputs and arithmetic (TF32 tensor cores
 // would round the inputs to 10 mantissa bits).  One warp owns one query row:
@@ -90,75 +90,6 @@ __global__ void __launch_bounds__(32 * ROWS_PER_BLOCK) attn_fwd_f32_kernel(F32Pa
     if (p.lse && lane == 0) p.lse[row] = l > 0.f ? m + logf(l) : -INFINITY;
 }
 
-// Copy rows globals[r] of Q (per query head) and of K, V (per kv head) into
-// dense [heads, n_global, d] scratch tensors.  blockIdx.x = r, blockIdx.y =
-// head slot over Q heads then K heads then V heads; 16-byte vectors.
-__global__ void gather_globals_kernel(GatherParams p) {
-    const int r = blockIdx.x;
-    int slot = blockIdx.y;
-    const uint16_t* src;
-    uint16_t* dst;
-    long head;
-    if (slot < p.BHq) { src = p.q; dst = p.qg; head = slot; }
-    else if ((slot -= p.BHq) < p.BHkv) { src = p.k; dst = p.kg; head = slot; }
-    else { slot -= p.BHkv; src = p.v; dst = p.vg; head = slot; }
-    const long pos = p.globals[r];
-    const uint4* s4 = reinterpret_cast<const uint4*>(src + (head * p.S + pos) * p.d);
-    uint4* d4 = reinterpret_cast<uint4*>(dst + (head * p.n_global + r) * p.d);
-    for (int t = threadIdx.x; t < p.d / 8; t += blockDim.x) d4[t] = s4[t];
-}
-
-// Combines the key chunks of the global-row pass.  One warp per (head, global
-// row).  Chunk c holds O_c (its own softmax-weighted average) and
-// LSE_c = ln of its sum of exponentials, so the whole row is
-//   O = sum_c e^(LSE_c - M) O_c / sum_c e^(LSE_c - M),  LSE = M + ln sum_c e^(LSE_c - M)
-// with M = max_c LSE_c: the same softmax normalisation, applied across chunks.
-// Lanes split the chunks for M and the weights (warp reductions), then split d for the
-// weighted sum, each weight broadcast from the lane that computed it; the partial-O loads
-// of eight chunks are issued before their multiply-adds (the merge is latency-bound).
-__global__ void merge_global_rows_kernel(MergeParams p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const long row = (long)blockIdx.x * (blockDim.x >> 5) + warp;
-    if (row >= (long)p.BHq * p.n_global) return;
-    const long bh = row / p.n_global;
-    const int gr = (int)(row - bh * p.n_global);
-    const float* lse_c = p.part_lse + row * p.n_chunks;
-    float M = -INFINITY;
-    for (int c = lane; c < p.n_chunks; c += 32) M = fmaxf(M, lse_c[c]);
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-    float W = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // d <= 128: 4 elements per lane
-    const int nd = p.d / 32;
-    for (int c0 = 0; c0 < p.n_chunks; c0 += 32) {
-        const int c = c0 + lane;
-        const float wl = c < p.n_chunks ? expf(lse_c[c] - M) : 0.f;  // this lane's chunk weight
-        W += wl;
-        const int n_here = min(32, p.n_chunks - c0);
-        const float* ob = p.part_o + (row * p.n_chunks + c0) * p.d;
-        for (int j0 = 0; j0 < n_here; j0 += 8) {
-            float v[8][4];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    v[j][e] = (j0 + j < n_here && e < nd) ? ob[(long)(j0 + j) * p.d + lane + 32 * e] : 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float wc = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);  // 0 past the last chunk
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = fmaf(wc, v[j][e], acc[e]);
-            }
-        }
-    }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) W += __shfl_xor_sync(0xffffffffu, W, s);
-    const long pos = p.globals[gr];
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o) + (bh * p.S + pos) * p.d;
-    for (int e = 0; e < nd; ++e) o[lane + 32 * e] = __float2bfloat16_rn(acc[e] / W);
-    if (p.lse && lane == 0) p.lse[bh * p.S + pos] = M + logf(W);
-}
-
 // Evaluates the softmax warps' FMA-pipe exp2 (exp2_poly2) elementwise, for its test.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
     const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -170,13 +101,6 @@ __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
 }
 
 }  // namespace
-
-cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream) {
-    const long rows = (long)p.BHq * p.n_global;
-    if (rows <= 0) return cudaSuccess;
-    merge_global_rows_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(p);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream) {
     if (n <= 0) return cudaSuccess;
@@ -191,13 +115,6 @@ cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream) {
     if (d == 128) attn_fwd_f32_kernel<128><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(p);
     else if (d == 64) attn_fwd_f32_kernel<64><<<grid, 32 * ROWS_PER_BLOCK, 0, stream>>>(p);
     else return cudaErrorInvalidValue;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_gather_globals(const GatherParams& p, cudaStream_t stream) {
-    if (p.n_global <= 0) return cudaSuccess;
-    dim3 grid((unsigned)p.n_global, (unsigned)(p.BHq + 2 * p.BHkv));
-    gather_globals_kernel<<<grid, 32, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -26,6 +26,15 @@
 //
 // Tensor memory: S/P in columns [0, 128), O in [128, 128 + d); 256 columns per
 // CTA, so two CTAs share an SM and one's softmax overlaps the other's MMAs.
+//
+// Local + global ("Transformer 演进与变体", section 稀疏注意力) runs as one launch:
+//   * a query tile's global keys outside its band of key tiles are gathered by the
+//     producer warp (plain loads into the swizzled layout) into narrow key tiles of
+//     32, 64, 96 or 128 columns, every column allowed for every row;
+//   * the global rows are computed by their own items against every key, split into key
+//     chunks; each chunk writes a partial result and the last chunk of a row tile to
+//     finish (an arrival counter) merges them into O and LSE;
+//   * band items skip the stores of the global rows their tile holds.
 // Every wait on an mbarrier is bounded by a wall-clock limit; a wait that runs
 // out records an error bit, raises a CTA-wide abort flag and the CTA drains
 // its in-flight copies and MMAs (again bounded), frees tensor memory and exits.
@@ -83,6 +92,8 @@ struct Shared {  // small control block after the tiles
     uint64_t bar[NBAR];
     uint32_t tmem_base;
     volatile int abort;
+    int g_lo, g_hi;          // gathered keys: the globals before the band are G[0, g_lo), after it G[g_hi, nG)
+    volatile int merge_last; // global-row chunk items: this CTA finished last and merges the chunks
 };
 
 // Bounded wait: polls the barrier; every 128 polls checks the CTA abort flag
@@ -130,32 +141,40 @@ __device__ __forceinline__ bool spin_bounded(uint32_t bar, uint32_t parity, Shar
     }
 }
 
-// Mask of one PARTIAL tile as seen by one query row: allowed in-tile columns are
-// [a0, a1] (clamped to [-1, BN]) plus the set bits of g0..g3 (global keys).
+// Mask of one PARTIAL tile as seen by one query row: the allowed in-tile columns are
+// [a0, a1] (clamped to [-1, BN]) plus the global keys of the tile.  w0..w3 hold them as
+// one bit per column (filled for the MASK_ANY form only), so that testing a column is one
+// bit test and one select.
 struct TileMask {
     int a0, a1;
-    uint32_t g0, g1, g2, g3;
+    uint32_t w0, w1, w2, w3;
 };
 
+// Bits of the columns [32k, 32k + 32) that lie inside [a0, a1].
+__device__ __forceinline__ uint32_t interval_word(int a0, int a1, int k) {
+    const int lo = max(a0 - 32 * k, 0), hi = min(a1 - 32 * k + 1, 32);  // [lo, hi)
+    if (hi <= lo) return 0u;
+    const uint32_t up = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return up & ~((1u << lo) - 1u);
+}
+
 __device__ __forceinline__ bool tile_allowed(int c, const TileMask& mk) {
-    const uint32_t gw = c < 32 ? mk.g0 : c < 64 ? mk.g1 : c < 96 ? mk.g2 : mk.g3;
-    return (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
+    const uint32_t w = c < 32 ? mk.w0 : c < 64 ? mk.w1 : c < 96 ? mk.w2 : mk.w3;
+    return (w >> (c & 31)) & 1u;
 }
 
 // Mask forms of a tile, decided once per tile and warp-uniformly:
 //   MASK_NONE  : FULL tile, no predicate;
 //   MASK_UPPER : allowed columns are c <= a1 (a0 <= 0, no global keys) -- the causal diagonal
 //                tiles; one compare and one select per element;
-//   MASK_ANY   : the interval [a0, a1] plus the global-key bits g0..g3.
+//   MASK_ANY   : the interval [a0, a1] plus the global keys, as the column bits w0..w3.
 enum { MASK_NONE = 0, MASK_UPPER = 1, MASK_ANY = 2 };
 
 template <int MASKED>
 __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask& mk) {
     if (MASKED == MASK_NONE) return __uint_as_float(raw);
     if (MASKED == MASK_UPPER) return c <= mk.a1 ? __uint_as_float(raw) : -INFINITY;
-    const uint32_t gw = c < 32 ? mk.g0 : c < 64 ? mk.g1 : c < 96 ? mk.g2 : mk.g3;
-    const bool in = (c >= mk.a0 && c <= mk.a1) || ((gw >> (c & 31)) & 1u);
-    return in ? __uint_as_float(raw) : -INFINITY;
+    return tile_allowed(c, mk) ? __uint_as_float(raw) : -INFINITY;
 }
 
 // Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
@@ -395,6 +414,147 @@ __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMa
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
+// First index of the sorted list g[0, n) whose value is >= x.
+__device__ __forceinline__ int lower_bound_dev(const int* g, int n, long x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((long)__ldg(g + mid) < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Rows pos(r), r < n_rows, of one [S, D] bf16 head copied with plain loads into a 128-row tile in
+// the layout the TMA loads write (128-byte swizzle: 64-column blocks of BM * 128 bytes, the 16-byte
+// chunk c of row r at chunk position c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32 lanes of
+// one warp take part.
+template <int D, class Pos>
+__device__ __forceinline__ void gather_rows(uint8_t* tile, const uint16_t* head, int n_rows, Pos pos, int lane) {
+    constexpr int CH = D / 8;  // 16-byte chunks per row
+    for (int e = lane; e < n_rows * CH; e += 32) {
+        const int r = e / CH, c = e - r * CH;
+        const long j = pos(r);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (j >= 0) v = __ldg(reinterpret_cast<const uint4*>(head + j * D) + c);
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * (BM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+    }
+}
+
+// Row maximum over the first 32 * nch columns of a gathered-key tile (columns > a1 hold no key).
+__device__ __forceinline__ float narrow_row_max(uint32_t t_s, int nch, int a1) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            const int c = ch * 32 + e;
+            m0 = fmax3(m0, c <= a1 ? __uint_as_float(r[e]) : -INFINITY,
+                       c + 1 <= a1 ? __uint_as_float(r[e + 1]) : -INFINITY);
+            m1 = fmax3(m1, c + 2 <= a1 ? __uint_as_float(r[e + 2]) : -INFINITY,
+                       c + 3 <= a1 ? __uint_as_float(r[e + 3]) : -INFINITY);
+        }
+    }
+    return fmaxf(m0, m1);
+}
+
+// P = exp2(s * sl2 - ref) over the first 32 * nch columns of a gathered-key tile, bf16 P written
+// over S (keys 32ch .. 32ch + 31 in columns 16ch .. 16ch + 15); returns the row sum.  fix() runs
+// once every exponential is computed, then the whole of P is announced on bar_p.
+template <typename FixO>
+__device__ __forceinline__ float narrow_exp_store(uint32_t t_s, int nch, int a1, float sl2, float ref,
+                                                  uint32_t bar_p, FixO&& fix) {
+    const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c = ch * 32 + 2 * e;
+            const float2 x = __ffma2_rn(make_float2(c <= a1 ? __uint_as_float(r[2 * e]) : -INFINITY,
+                                                    c + 1 <= a1 ? __uint_as_float(r[2 * e + 1]) : -INFINITY),
+                                        sl2x2, nref);
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            acc = __fadd2_rn(acc, make_float2(p0, p1));
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + ch * 16, pk);
+    }
+    fix();
+    release_first_half(bar_p);
+    return acc.x + acc.y;
+}
+
+// This thread's O row (tensor memory, fp32) times inv_l, stored as bf16 at dst.  Every lane runs
+// the tensor-memory loads (they are warp-collective); only lanes with `store` write.
+template <int D>
+__device__ __forceinline__ void store_row_direct(uint32_t t_o, void* dst_row, float inv_l, bool store) {
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + c * 32, o);
+        tmem_wait_ld();
+        if (store) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
+                                        __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
+                dst[c * 4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        }
+    }
+}
+
+// One global row from its key chunks.  Chunk c holds O_c (its own softmax-weighted average, fp32)
+// and LSE_c (natural log of its sum of exponentials), so with M = max_c LSE_c the row is
+//   O = sum_c e^(LSE_c - M) O_c / sum_c e^(LSE_c - M),   LSE = M + ln sum_c e^(LSE_c - M):
+// the softmax normalisation carried across chunks.  The partials were written by other CTAs, so
+// they are read through L2 (ld.global.cg).
+template <int D>
+__device__ __forceinline__ void merge_global_row(const TcParams& p, size_t slot0, void* dst_row, float* lse_out) {
+    float M = -INFINITY;
+    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + slot0 + c));
+    float W = 0.f;
+    for (int c = 0; c < p.n_chunks; ++c) W += expf(__ldcg(p.part_lse + slot0 + c) - M);
+    const float inv_w = W > 0.f ? 1.f / W : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll 1
+    for (int cb = 0; cb < D; cb += 32) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        for (int c = 0; c < p.n_chunks; ++c) {
+            const float w = expf(__ldcg(p.part_lse + slot0 + c) - M);
+            const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot0 + c) * D + cb);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = __ldcg(src + q);
+                acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            dst[cb / 8 + q] = make_uint4(pack_bf16x2(acc[8 * q] * inv_w, acc[8 * q + 1] * inv_w),
+                                         pack_bf16x2(acc[8 * q + 2] * inv_w, acc[8 * q + 3] * inv_w),
+                                         pack_bf16x2(acc[8 * q + 4] * inv_w, acc[8 * q + 5] * inv_w),
+                                         pack_bf16x2(acc[8 * q + 6] * inv_w, acc[8 * q + 7] * inv_w));
+    }
+    if (lse_out) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
 template <int D, int BIAS, bool F8>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D, BIAS, F8>;
@@ -429,6 +589,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == B_PFULL || i == B_PFULL1) ? 128u : 1u);
         sh->abort = 0;
+        sh->merge_last = 0;
+        if (flags & ATTN_WORK_GLOBAL_COLS) {  // the global keys outside the band [kv_begin, kv_end) tiles
+            sh->g_lo = lower_bound_dev(p.globals, p.n_global, (long)kv_begin * BN);
+            sh->g_hi = lower_bound_dev(p.globals, p.n_global, (long)kv_end * BN);
+        } else {
+            sh->g_lo = 0;
+            sh->g_hi = p.n_global;
+        }
         fence_barrier_init();
     }
     if constexpr (BIAS == BIAS_ALIBI_MMA) {
@@ -457,7 +625,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         tmem_relinquish();
     }
     if (warp == WARP_PRODUCER && lane == 0) {
-        prefetch_tmap(grows ? &p.tm_qg : &p.tm_q);
+        prefetch_tmap(&p.tm_q);
         prefetch_tmap(&p.tm_k);
         prefetch_tmap(&p.tm_v);
     }
@@ -465,41 +633,88 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    // gathered key tiles (after the band tiles): n_out global keys lie outside the band; tile k holds
+    // the outside keys k * BN .. k * BN + ncols(k) - 1, padded to a multiple of 32 columns
+    const int g_lo = sh->g_lo, g_hi = sh->g_hi;
+    const int n_out = g_lo + (p.n_global - g_hi);
+    auto gathered_cols = [&](int it) { return min(BN, n_out - (it - n_band) * BN); };
+    auto outside_key = [&](int e) -> long { return __ldg(p.globals + (e < g_lo ? e : g_hi + (e - g_lo))); };
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const CUtensorMap* qmap = grows ? &p.tm_qg : &p.tm_q;
-            const int bias_plane = (BIAS == BIAS_MATRIX)
-                                       ? (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
-                                       : 0;
-            if constexpr (BIAS == BIAS_MATRIX) prefetch_tmap(&p.tm_bias);
+        // Lane 0 issues the TMA copies and waits for free buffers; all lanes gather the rows of the
+        // global tokens (plain loads into the swizzled layout, then a proxy fence so the tensor core
+        // sees them, then one arrival).
+        const int bias_plane = (BIAS == BIAS_MATRIX)
+                                   ? (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
+                                   : 0;
+        if constexpr (BIAS == BIAS_MATRIX) {
+            if (lane == 0) prefetch_tmap(&p.tm_bias);
+        }
+        if (grows) {  // query rows G[q_tile * BM + r]; rows past the list are zero
+            const int r0 = q_tile * BM;
+            gather_rows<D>(smem + C::OFF_Q, p.q + (size_t)bh * p.S * D, BM,
+                           [&](int r) -> long { return r0 + r < p.n_global ? (long)__ldg(p.globals + r0 + r) : -1L; },
+                           lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_Q));
+        } else if (lane == 0) {
             mbar_arrive_expect_tx(bar(B_Q), C::TILE_BYTES);
-            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * C::XW, q_tile * BM, bh);
-            int k_loaded = 0, v_loaded = 0;
-            bool ok = true;
-            for (int it = 0; it < n_iter && ok; ++it) {
-                const bool in_band = it < n_band;
-                const CUtensorMap* km = in_band ? &p.tm_k : &p.tm_kg;
-                const CUtensorMap* vm = in_band ? &p.tm_v : &p.tm_vg;
-                const int row = in_band ? band_tile(it) * BN : (it - n_band) * BN;
-                if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
-                mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * C::XW, row, bkv);
-                ++k_loaded;
-                if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
-                    tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
-                if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
-                if (p.withhold_v) continue;
-                mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * C::XW, row, bkv);
-                ++v_loaded;
+            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, &p.tm_q, bar(B_Q), s * C::XW, q_tile * BM, bh);
+        }
+        int k_loaded = 0, v_loaded = 0;
+        bool ok = true;
+        for (int it = 0; it < n_iter && ok; ++it) {
+            const bool in_band = it < n_band;
+            const int row = in_band ? band_tile(it) * BN : 0;
+            // gathered tiles: the outside keys (it - n_band) * BN + r, r < ncols, padded with zero rows
+            const int gcols = in_band ? 0 : gathered_cols(it);
+            const int grows_pad = (gcols + 31) & ~31;
+            auto gpos = [&](int r) -> long { return r < gcols ? outside_key((it - n_band) * BN + r) : -1L; };
+            if (it > 0) {
+                bool w = true;
+                if (lane == 0) w = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
+                if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
             }
-            if (sh->abort) {  // let the copies this thread issued land before the CTA exits
-                drain_wait(bar(B_Q), 0, p);
-                if (k_loaded) drain_wait(bar(B_KFULL), (k_loaded - 1) & 1, p);
-                if (v_loaded) drain_wait(bar(B_VFULL), (v_loaded - 1) & 1, p);
+            if (in_band) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
+                    for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, &p.tm_k, bar(B_KFULL), s * C::XW, row, bkv);
+                }
+            } else {
+                gather_rows<D>(smem + C::OFF_K, p.k + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_KFULL));
             }
+            ++k_loaded;
+            if constexpr (BIAS == BIAS_MATRIX) {  // the softmax reads this tile's bias rows a tile later
+                if (lane == 0) tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
+            }
+            if (it > 0) {
+                bool w = true;
+                if (lane == 0) w = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
+                if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
+            }
+            if (p.withhold_v) continue;
+            if (in_band) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
+                    for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, &p.tm_v, bar(B_VFULL), s * C::XW, row, bkv);
+                }
+            } else {
+                gather_rows<D>(smem + C::OFF_V, p.v + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_VFULL));
+            }
+            ++v_loaded;
+        }
+        if (lane == 0 && sh->abort) {  // let the copies this warp issued land before the CTA exits
+            drain_wait(bar(B_Q), 0, p);
+            if (k_loaded) drain_wait(bar(B_KFULL), (k_loaded - 1) & 1, p);
+            if (v_loaded) drain_wait(bar(B_VFULL), (v_loaded - 1) & 1, p);
         }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
@@ -515,14 +730,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 // S/P share tensor columns.  No wait for PV(it-1) here: the MMAs one thread issues
                 // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
+                // a gathered-key tile is ncols wide (a multiple of 32): N = ncols for S, K = ncols for P V
+                const bool narrow = it >= n_band;
+                const int ncols = narrow ? (gathered_cols(it) + 31) & ~31 : BN;
+                const uint32_t idesc_s = narrow ? idesc_bf16_f32(BM, ncols, false) : idesc_qk;
 #pragma unroll
                 for (int k = 0; k < D / KS; ++k) {
                     const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
                     if constexpr (F8)
-                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
+                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
                                   k > 0);
                     else
-                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_qk,
+                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
                                k > 0);
                 }
                 if constexpr (BIAS == BIAS_ALIBI_MMA)
@@ -532,11 +751,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 mma_commit(bar(B_KEMPTY));
                 last_bar = B_KEMPTY; last_par = it & 1;
                 if (!(ok = spin_bounded(bar(B_PFULL), it & 1, sh, p, ERR_MMA))) break;
+                // a gathered tile's P is announced whole: wait for both arrivals before its products,
+                // so that QK(it+1) is issued only after every softmax thread is done with tile it
+                if (narrow && !(ok = spin_bounded(bar(B_PFULL1), it & 1, sh, p, ERR_MMA))) break;
                 if (!(ok = wait_bounded(bar(B_VFULL), it & 1, sh, p, ERR_MMA))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / KS; ++k) {
-                    if (k == BN / KS / 2) {  // the second half of P (keys 64-127)
+                    if (k * KS >= ncols) break;
+                    if (!narrow && k == BN / KS / 2) {  // the second half of P (keys 64-127)
                         if (!(ok = spin_bounded(bar(B_PFULL1), it & 1, sh, p, ERR_MMA))) break;
                         tc_fence_after();
                     }
@@ -605,8 +828,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate).  It does
             // not depend on S, so it is worked out before the wait for S.
             bool partial = true;
+            bool has_g = false;  // the tile holds global keys (local + global, band tiles)
+            const bool gathered = it >= n_band;
+            int gcols = BN;      // gathered tiles: columns holding keys (all allowed: they lie outside the band)
             TileMask mk{0, -1, 0u, 0u, 0u, 0u};
-            if (it < n_band) {
+            uint4 g4 = make_uint4(0u, 0u, 0u, 0u);
+            if (!gathered) {
                 const int t = band_tile(it);
                 partial = t < full_begin || t >= full_end;
                 if (partial) {
@@ -614,31 +841,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     mk.a0 = (int)max(-1L, min((long)BN, lo - c0));
                     mk.a1 = (int)max(-1L, min((long)BN, hi - c0));
                     if (lg) {
-                        const uint4 g4 = *reinterpret_cast<const uint4*>(p.global_bits + 4 * t);
-                        mk.g0 = g4.x; mk.g1 = g4.y; mk.g2 = g4.z; mk.g3 = g4.w;
+                        g4 = *reinterpret_cast<const uint4*>(p.global_bits + 4 * t);
+                        has_g = (g4.x | g4.y | g4.z | g4.w) != 0u;
                     }
                 }
             } else {
-                // gathered global keys: allowed when outside this item's key tiles.
-                // Lane l tests columns l, l+32, l+64, l+96; ballots give every lane the bits.
-                const int g0 = (it - n_band) * BN;
-                const long band_lo = (long)kv_begin * BN, band_hi = (long)kv_end * BN;
-                uint32_t bits[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int gi = g0 + k * 32 + lane;
-                    bool in = false;
-                    if (gi < p.n_global) {
-                        const long gpos = __ldg(p.globals + gi);
-                        in = gpos < band_lo || gpos >= band_hi;
-                    }
-                    bits[k] = __ballot_sync(0xffffffffu, in);
-                }
-                mk.g0 = bits[0]; mk.g1 = bits[1]; mk.g2 = bits[2]; mk.g3 = bits[3];
+                gcols = gathered_cols(it);
+                mk.a1 = gcols - 1;
             }
-            // causal diagonal tiles (no lower bound inside the tile, no global keys): the cheap
-            // mask form, when every row of the warp qualifies
-            const bool upper = __all_sync(0xffffffffu, partial && !lg && it < n_band && mk.a0 <= 0);
+            // no lower bound inside the tile and no global keys (causal diagonal tiles, the upper edge of
+            // a window): the cheap mask form, when every row of the warp qualifies
+            const bool upper = !gathered && __all_sync(0xffffffffu, partial && !has_g && mk.a0 <= 0);
+            // the general form (and every partial tile of the biased passes, which take no other form):
+            // the interval and the global keys as column bits
+            if (partial && !gathered && (!upper || BIAS != BIAS_NONE)) {
+                mk.w0 = interval_word(mk.a0, mk.a1, 0) | g4.x;
+                mk.w1 = interval_word(mk.a0, mk.a1, 1) | g4.y;
+                mk.w2 = interval_word(mk.a0, mk.a1, 2) | g4.z;
+                mk.w3 = interval_word(mk.a0, mk.a1, 3) | g4.w;
+            }
             // warp-uniform exit: the tensor-memory accesses below are warp-collective
             if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
                 ok = false;
@@ -659,8 +880,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             } else if constexpr (BIAS == BIAS_MATRIX) {
                 mx = partial ? tile_row_max_matbias<MASK_ANY>(t_s, mk, sl2, bv) : tile_row_max_matbias<MASK_NONE>(t_s, mk, sl2, bv);
             } else {
-                mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                     : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                if constexpr (BIAS == BIAS_NONE && !F8) {
+                    if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
+                    else
+                        mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
+                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                } else {
+                    mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
+                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                }
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
                     // the tile's constant part of the bias, m_a (c0 - i), in log2 units
@@ -714,9 +942,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                               : tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
-                sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                      : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                              : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
+                if (BIAS == BIAS_NONE && gathered)
+                    sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, sl2, r_eff, bar(B_PFULL), fix);
+                else
+                    sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                          : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                                  : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
             }
             l += sum;
             tmem_wait_st();
@@ -731,7 +962,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             // o_scale: the V descale of E4M3 inputs (bf16 inputs have none; callers may leave it 0)
             const float inv_l = l > 0.f ? (F8 ? p.o_scale : 1.f) / l : 0.f;
             const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            if (!grows) {
+            // band items of local + global whose tile holds global rows leave those rows to the
+            // global-row items and store the others directly
+            const bool skip_g = !grows && (flags & ATTN_WORK_HAS_GLOBAL_ROWS) &&
+                                ((__ldg(p.global_bits + 4 * q_tile + (r >> 5)) >> (r & 31)) & 1u);
+            if (!grows && (flags & ATTN_WORK_HAS_GLOBAL_ROWS)) {
+                store_row_direct<D>(t_o, static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D, inv_l,
+                                    row_valid && !skip_g);
+            } else if (!grows) {
                 // O row -> bf16 -> 128B-swizzled staging in the (now idle) Q buffer -> TMA store
                 uint8_t* stage = smem + C::OFF_Q;
 #pragma unroll
@@ -760,29 +998,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     tma_store_commit_and_wait_read();
                 }
             } else if (p.n_chunks == 1) {
-                // global rows: scattered row stores.  The tensor-memory loads are warp-collective,
-                // so every lane executes them; only rows past the gathered count skip the stores.
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
-                    if (row_valid) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                pk[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
-                                                    __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
-                            dst[c * 4 + q] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        }
-                    }
-                }
+                // global rows: scattered row stores; rows past the list skip them
+                store_row_direct<D>(t_o, static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D, inv_l, row_valid);
             } else {
                 // one key chunk of a global row: fp32 partial O (normalised by this chunk's
-                // sum) and partial LSE, combined later by the merge kernel
+                // sum) and partial LSE, merged below by the chunk that finishes last
                 const size_t slot = ((size_t)bh * p.n_global + (q_tile * BM + r)) * p.n_chunks + n_gt;
                 float4* dst = reinterpret_cast<float4*>(p.part_o + slot * D);
 #pragma unroll
@@ -799,7 +1019,24 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 }
                 if (row_valid) p.part_lse[slot] = lse;
             }
-            if (p.lse && row_valid && !(grows && p.n_chunks > 1)) p.lse[(size_t)bh * p.S + i] = lse;
+            if (p.lse && row_valid && !skip_g && !(grows && p.n_chunks > 1)) p.lse[(size_t)bh * p.S + i] = lse;
+        }
+        if (grows && p.n_chunks > 1) {
+            // Count this chunk in (also after an abort, so that the counter returns to 0); the chunk
+            // that finishes last merges every chunk of the row tile and resets the counter.
+            __threadfence();  // this thread's partial stores, before the arrival
+            named_bar_sync(1, 128);
+            unsigned* counter = p.counters + (size_t)bh * p.n_gtiles + q_tile;
+            if (threadIdx.x == 0) sh->merge_last = atomicAdd(counter, 1u) == (unsigned)(p.n_chunks - 1);
+            named_bar_sync(1, 128);
+            if (sh->merge_last) {
+                __threadfence();
+                if (row_valid)
+                    merge_global_row<D>(p, ((size_t)bh * p.n_global + (q_tile * BM + r)) * p.n_chunks,
+                                        static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D,
+                                        p.lse ? p.lse + (size_t)bh * p.S + i : nullptr);
+                if (threadIdx.x == 0) *counter = 0u;
+            }
         }
     }
 

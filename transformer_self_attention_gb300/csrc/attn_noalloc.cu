@@ -5,20 +5,26 @@
 // processes that must keep their device footprint fixed after start-up.  For
 // them this entry point takes the problem description and the caller's Q, K,
 // V, O, LSE buffers and keeps every other device byte it needs (error word,
-// work list, global-token list and bits, gathered global rows) in one
-// file-scope __device__ array of ATTN_NOALLOC_SCRATCH_BYTES, which every GPU
-// that loads the library holds until the process exits.
+// work list, global-token list and bits, partial results and arrival counters
+// of the global-row chunks) in one file-scope __device__ array of
+// ATTN_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
+// until the process exits.
 //
 // The first call on a device looks up the array's device address with
 // cudaGetSymbolAddress (once per device, with that device current); make that
 // first call before any stream capture.  All calls share the array and it
 // keeps the last call's contents, so calls that overlap on the GPU (on two
 // streams, or on two host threads) race and must be serialised by the caller.
+// The schedule reaches the device inside kernel parameters (a small copy
+// kernel per 30 KiB), which the launch itself copies: no host buffer is read
+// after the call returns.  The error word collects the watchdog bits of every
+// call until attn_forward_noalloc_poll_error reads and clears it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -34,6 +40,40 @@ constexpr size_t kScratchBytes = ATTN_NOALLOC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+// Byte offset of the error word inside the scratch array (it stays at the front for every problem).
+constexpr size_t kOffErr = 0;
+
+// Watchdog settings of this entry point (attn_forward_noalloc_set_watchdog).
+std::atomic<long long> g_watchdog_ns{2000000000LL};
+std::atomic<int> g_withhold_v{0};
+
+// Host words passed by value: kernel parameters are copied when the launch is made.
+constexpr int kUploadWords = 7680;  // 30 KiB of payload (kernel parameters hold up to 32,764 bytes)
+struct UploadChunk {
+    unsigned* dst;
+    int n;
+    unsigned w[kUploadWords];
+};
+
+__global__ void __launch_bounds__(256) noalloc_upload_kernel(const __grid_constant__ UploadChunk c) {
+    for (int k = threadIdx.x; k < c.n; k += blockDim.x) c.dst[k] = c.w[k];
+}
+
+// Copies n words from the host to dst on `stream`, in launches of kUploadWords words.
+cudaError_t upload_words(unsigned* dst, const void* src, size_t n, cudaStream_t stream) {
+    UploadChunk c;
+    const unsigned* s = static_cast<const unsigned*>(src);
+    for (size_t k = 0; k < n; k += kUploadWords) {
+        c.dst = dst + k;
+        c.n = (int)std::min<size_t>(kUploadWords, n - k);
+        std::memcpy(c.w, s + k, (size_t)c.n * sizeof(unsigned));
+        noalloc_upload_kernel<<<1, 256, 0, stream>>>(c);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 std::mutex g_addr_mu;
 void* g_addr[kMaxDevices] = {};
@@ -113,21 +153,19 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     for (int g : G) bits[(size_t)(g / ATTN_TILE) * 4 + (g % ATTN_TILE) / 32] |= 1u << (g % 32);
 
     // carve the fixed scratch area; refuse problems that do not fit
-    const size_t off_err = 0;
     const size_t off_work = 256;
     const size_t off_glob = off_work + round256(items.size() * sizeof(int));
     const size_t off_bits = off_glob + round256((size_t)nG * sizeof(int));
-    const size_t off_qg = off_bits + round256(bits.size() * sizeof(unsigned));
-    const size_t qg_bytes = (size_t)B * Hq * nG * d_k * 2, kg_bytes = (size_t)B * Hkv * nG * d_k * 2;
-    const size_t off_kg = off_qg + round256(qg_bytes);
-    const size_t off_vg = off_kg + round256(kg_bytes);
-    // key chunks of the global-row pass: the chunk index is int [7] of those items
+    // key chunks of the global rows: the chunk index is int [7] of those items
     int n_chunks = 1;
     for (int t = n_first; t < n_items; ++t) n_chunks = std::max(n_chunks, items[(size_t)t * ATTN_WORK_INTS + 7] + 1);
+    const int n_gtiles = (nG + ATTN_TILE - 1) / ATTN_TILE;
     const size_t part_rows = n_chunks > 1 ? (size_t)B * Hq * nG * n_chunks : 0;
-    const size_t off_part_o = off_vg + round256(kg_bytes);
+    const size_t n_ctr = n_chunks > 1 ? (size_t)B * Hq * n_gtiles : 0;
+    const size_t off_part_o = off_bits + round256(bits.size() * sizeof(unsigned));
     const size_t off_part_lse = off_part_o + round256(part_rows * d_k * sizeof(float));
-    const size_t total = off_part_lse + round256(part_rows * sizeof(float));
+    const size_t off_ctr = off_part_lse + round256(part_rows * sizeof(float));
+    const size_t total = off_ctr + round256(n_ctr * sizeof(unsigned));
     if (total > kScratchBytes) return ATTN_ERR_UNSUPPORTED;
 
     void* base = nullptr;
@@ -135,26 +173,20 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     unsigned char* sc = static_cast<unsigned char*>(base);
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-    // the error word must start at zero; everything else is fully overwritten below
-    if (cudaMemsetAsync(sc + off_err, 0, sizeof(int), stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (cudaMemcpyAsync(sc + off_work, items.data(), items.size() * sizeof(int), cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
+    // the schedule, in kernel parameters; the arrival counters must start at zero
+    if (upload_words(reinterpret_cast<unsigned*>(sc + off_work), items.data(), items.size(), stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    if (nG > 0 && cudaMemcpyAsync(sc + off_glob, G.data(), (size_t)nG * sizeof(int), cudaMemcpyHostToDevice,
-                                  stream) != cudaSuccess)
+    if (nG > 0 && upload_words(reinterpret_cast<unsigned*>(sc + off_glob), G.data(), G.size(), stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
-    if (cudaMemcpyAsync(sc + off_bits, bits.data(), bits.size() * sizeof(unsigned), cudaMemcpyHostToDevice,
-                        stream) != cudaSuccess)
+    if (upload_words(reinterpret_cast<unsigned*>(sc + off_bits), bits.data(), bits.size(), stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (n_ctr > 0 && cudaMemsetAsync(sc + off_ctr, 0, n_ctr * sizeof(unsigned), stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
 
     attn::TcParams p{};
     constexpr unsigned T = ATTN_TILE;
     if (!map3d(&p.tm_q, Q, d_k, S, (long)B * Hq, T) || !map3d(&p.tm_k, K, d_k, S, (long)B * Hkv, T) ||
         !map3d(&p.tm_v, V, d_k, S, (long)B * Hkv, T) || !map3d(&p.tm_o, O, d_k, S, (long)B * Hq, T))
-        return ATTN_ERR_CUDA;
-    if (nG > 0 && (!map3d(&p.tm_qg, sc + off_qg, d_k, nG, (long)B * Hq, T) ||
-                   !map3d(&p.tm_kg, sc + off_kg, d_k, nG, (long)B * Hkv, T) ||
-                   !map3d(&p.tm_vg, sc + off_vg, d_k, nG, (long)B * Hkv, T)))
         return ATTN_ERR_CUDA;
     p.work = reinterpret_cast<const int4*>(sc + off_work);
     p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;
@@ -165,38 +197,45 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     p.globals = reinterpret_cast<const int*>(sc + off_glob);
     p.n_global = nG;
     p.global_bits = reinterpret_cast<const unsigned*>(sc + off_bits);
+    p.q = static_cast<const uint16_t*>(Q);
+    p.k = static_cast<const uint16_t*>(K);
+    p.v = static_cast<const uint16_t*>(V);
     p.o = O;
     p.lse = LSE;
-    p.err = reinterpret_cast<int*>(sc + off_err);
-    p.watchdog_ns = 2000000000LL;
-    p.withhold_v = 0;
+    p.err = reinterpret_cast<int*>(sc + kOffErr);
+    p.watchdog_ns = g_watchdog_ns.load();
+    p.withhold_v = g_withhold_v.load();
     p.n_chunks = n_chunks;
     p.part_o = n_chunks > 1 ? reinterpret_cast<float*>(sc + off_part_o) : nullptr;
     p.part_lse = n_chunks > 1 ? reinterpret_cast<float*>(sc + off_part_lse) : nullptr;
+    p.counters = n_chunks > 1 ? reinterpret_cast<unsigned*>(sc + off_ctr) : nullptr;
+    p.n_gtiles = n_gtiles;
+    p.fp8 = 0;        // bf16 inputs
+    p.o_scale = 1.f;  // no output factor
+    p.alibi = nullptr;
+    p.bias = nullptr;
 
-    if (nG > 0) {
-        attn::GatherParams g{};
-        g.q = static_cast<const uint16_t*>(Q); g.k = static_cast<const uint16_t*>(K);
-        g.v = static_cast<const uint16_t*>(V);
-        g.qg = reinterpret_cast<uint16_t*>(sc + off_qg); g.kg = reinterpret_cast<uint16_t*>(sc + off_kg);
-        g.vg = reinterpret_cast<uint16_t*>(sc + off_vg);
-        g.globals = p.globals; g.n_global = nG;
-        g.BHq = B * Hq; g.BHkv = B * Hkv; g.S = S; g.d = d_k;
-        if (attn::launch_gather_globals(g, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    }
     p.item_offset = 0;
-    if (attn::launch_tc_forward(p, d_k, n_first, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (n_items > n_first) {
-        p.item_offset = n_first;
-        if (attn::launch_tc_forward(p, d_k, n_items - n_first, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (n_chunks > 1) {
-            attn::MergeParams mp{};
-            mp.part_o = p.part_o; mp.part_lse = p.part_lse;
-            mp.o = static_cast<uint16_t*>(O); mp.lse = LSE;
-            mp.globals = p.globals; mp.n_global = nG; mp.n_chunks = n_chunks;
-            mp.BHq = B * Hq; mp.S = S; mp.d = d_k;
-            if (attn::launch_merge_global_rows(mp, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-        }
-    }
+    if (attn::launch_tc_forward(p, d_k, n_items, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+extern "C" attn_status attn_forward_noalloc_poll_error(int* code) {
+    if (!code) return ATTN_ERR_INVALID_ARG;
+    *code = 0;
+    void* base = nullptr;
+    const attn_status st = scratch_address(&base);
+    if (st != ATTN_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned char* sc = static_cast<unsigned char*>(base);
+    if (cudaMemcpy(code, sc + kOffErr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (*code != 0 && cudaMemset(sc + kOffErr, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return *code ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+extern "C" attn_status attn_forward_noalloc_set_watchdog(long long limit_ns, int withhold) {
+    if (limit_ns <= 0 || (withhold != 0 && withhold != 1)) return ATTN_ERR_INVALID_ARG;
+    g_watchdog_ns.store(limit_ns);
+    g_withhold_v.store(withhold);
     return ATTN_OK;
 }

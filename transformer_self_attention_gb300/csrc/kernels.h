@@ -17,9 +17,6 @@ struct TcParams {
     CUtensorMap tm_k;    // K  [B*Hkv, S, d]
     CUtensorMap tm_v;    // V  [B*Hkv, S, d]
     CUtensorMap tm_o;    // O  [B*Hq,  S, d] (TMA store)
-    CUtensorMap tm_qg;   // gathered global query rows  [B*Hq,  nG, d]
-    CUtensorMap tm_kg;   // gathered global keys         [B*Hkv, nG, d]
-    CUtensorMap tm_vg;   // gathered global values       [B*Hkv, nG, d]
     const int4* work;    // 4 int4 per work item (attn.h schedule layout)
     int item_offset;     // first work item of this launch
     int S, Hq, Hkv, group;
@@ -27,16 +24,25 @@ struct TcParams {
     float scale_log2;    // scale * log2(e)
     const int* globals;  // sorted global positions (device)
     int n_global;
-    const unsigned* global_bits;  // 4 words per key tile
-    void* o;             // O base (scattered stores of the global rows)
+    const unsigned* global_bits;  // 4 words per 128-position tile (key tiles and query tiles alike)
+    // local + global: the bf16 bits of Q, K, V, from which the producer warp gathers the global
+    // rows (query rows of the global-row items, keys and values of the gathered key tiles)
+    const uint16_t* q;
+    const uint16_t* k;
+    const uint16_t* v;
+    void* o;             // O base (direct row stores)
     float* lse;          // may be null
     int* err;            // device error word
     long long watchdog_ns;
     int withhold_v;      // test hook: producer never loads V
-    // global-row pass split into key chunks (n_chunks > 1): partial results per chunk
+    // global-row items split into key chunks (n_chunks > 1): partial results per chunk, and per
+    // (batch-head, global-row tile) a counter of the chunks that have finished; the last chunk to
+    // finish merges them and puts the counter back to 0
     float* part_o;       // [B*Hq, n_global, n_chunks, d] fp32, each normalised by its own sum
     float* part_lse;     // [B*Hq, n_global, n_chunks]
     int n_chunks;
+    unsigned* counters;  // [B*Hq*n_gtiles]
+    int n_gtiles;        // global-row tiles per (batch, head): ceil(n_global / 128)
     const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
     int fp8;             // Q, K, V are E4M3 (scale_log2 includes their descales)
     float o_scale;       // factor on O at the end (the V descale for E4M3 inputs, else 1)
@@ -58,23 +64,6 @@ struct F32Params {
     const int* globals; int n_global;
     const unsigned char* is_global;  // [S] flags (local + global only)
     const float* alibi;  // [Hq] slopes of the additive bias -m_a |i - j| (device), or null
-};
-
-// Gather of the global rows of Q, K, V into dense scratch tensors.
-struct GatherParams {
-    const uint16_t* q; const uint16_t* k; const uint16_t* v;  // bf16 bits
-    uint16_t* qg; uint16_t* kg; uint16_t* vg;
-    const int* globals; int n_global;
-    int BHq, BHkv, S, d;
-};
-
-// Merge of the global-row pass's key chunks into O (bf16, rows G) and LSE.
-struct MergeParams {
-    const float* part_o; const float* part_lse;
-    uint16_t* o;         // bf16 bits of O [B*Hq, S, d]
-    float* lse;          // may be null
-    const int* globals; int n_global, n_chunks;
-    int BHq, S, d;
 };
 
 // Decode / key-value-cache attention (attn_decode.cu).  A persistent grid of n_cta
@@ -147,9 +136,7 @@ cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t s
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream);
 
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
-cudaError_t launch_merge_global_rows(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
-cudaError_t launch_gather_globals(const GatherParams& p, cudaStream_t stream);
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
 
 }  // namespace attn

@@ -8,8 +8,6 @@ namespace attn {
 namespace {
 
 constexpr int T = ATTN_TILE;
-// CTAs the global-row pass aims for (about two per SM of a 152-SM GPU)
-constexpr int kGlobalRowTargetCtas = 304;
 
 // Allowed key interval [lo(i), hi(i)] of row i for the window part of a mask
 // (global rows / columns are handled separately).  Both ends are
@@ -101,8 +99,9 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
         int flags = 0, ngt = 0;
         if (lg && nG > 0) {
             const long band_lo = (long)kv_begin * T, band_hi = (long)kv_end * T;  // [lo, hi)
-            const long inside = globals_in(band_lo, std::min<long>(band_hi, S) - 1);
-            if (inside < nG) { flags |= ATTN_WORK_GLOBAL_COLS; ngt = n_gtiles; }
+            const long outside = nG - globals_in(band_lo, std::min<long>(band_hi, S) - 1);
+            if (outside > 0) { flags |= ATTN_WORK_GLOBAL_COLS; ngt = (int)((outside + T - 1) / T); }
+            if (globals_in(r0, r1) > 0) flags |= ATTN_WORK_HAS_GLOBAL_ROWS;
         }
         protos.push_back({qt, kv_begin, kv_end, full_begin, full_end, flags, ngt});
     }
@@ -132,17 +131,17 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
     out->n_main = (int)protos.size() * BH;
 
     // dense pass for the global rows: every key, FULL except a ragged last tile.
-    // The key tiles are split into chunks (one work item each) so that the pass has
-    // enough CTAs; each chunk writes a partial result that a merge step combines.
+    // The key tiles are split into chunks no longer than the longest query-tile item
+    // (one work item each), so the global rows finish alongside the band items of the
+    // same launch; each chunk writes a partial result and the last to finish merges them.
     out->n_grows = 0;
     out->n_chunks = 1;
     if (lg && nG > 0) {
         const int full_end = (S % T == 0) ? nk : nk - 1;
-        const int base = BH * n_gtiles;
-        int chunks = (kGlobalRowTargetCtas + base - 1) / base;
-        chunks = std::max(1, std::min(chunks, nk));
-        const int per = (nk + chunks - 1) / chunks;
-        chunks = (nk + per - 1) / per;  // no empty chunk
+        int longest = 1;
+        for (const Proto& p : protos) longest = std::max(longest, cost(p));
+        const int per = std::min(nk, longest);
+        const int chunks = (nk + per - 1) / per;  // no empty chunk
         out->n_chunks = chunks;
         for (int c = 0; c < chunks; ++c)
             for (int gt = 0; gt < n_gtiles; ++gt)

@@ -25,12 +25,12 @@ struct ScheduleInput {
 
 struct Schedule {
     std::vector<int> items;   // ATTN_WORK_INTS ints per item
-    int n_main = 0;           // items of the first launch
-    int n_grows = 0;          // ATTN_WORK_GLOBAL_ROWS items (second launch)
-    int n_chunks = 1;         // key-range chunks of the global-row pass (merged afterwards)
+    int n_main = 0;           // query-tile items (first in the list)
+    int n_grows = 0;          // ATTN_WORK_GLOBAL_ROWS items (after them, in the same launch)
+    int n_chunks = 1;         // key-range chunks of the global rows (merged by the last to finish)
     int n_kv_tiles = 0;
     int n_global_tiles = 0;
-    std::vector<unsigned> global_bits;  // 4 words per key tile: bit c set if key tile*128+c is global
+    std::vector<unsigned> global_bits;  // 4 words per 128-position tile: bit c set if position tile*128+c is global
 };
 
 // Builds the schedule.  Returns ATTN_OK, or ATTN_ERR_UNSUPPORTED if a query
