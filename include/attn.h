@@ -155,9 +155,12 @@ const char* attn_status_string(attn_status s);
  *                   gathered row tile and head); each chunk yields a partial softmax
  *                   result and the chunk that finishes last combines them:
  *                   O = sum_c e^LSE_c O_c / sum_c e^LSE_c, LSE = ln sum_c e^LSE_c.
- * The query-tile items come first, ordered by decreasing number of tiles (longest
- * first); for LOCAL_GLOBAL the ATTN_WORK_GLOBAL_ROWS items follow them.  All items
- * run in one launch: rows in G are written only by ATTN_WORK_GLOBAL_ROWS items.
+ * The query-tile items come first: the (batch, kv head) units in groups of
+ * g = max(1, min(B*Hkv, 32 MiB / (512 S))) units (their K and V fit in 32 MiB at
+ * d_k = 128), group after group, and within a group by decreasing number of tiles
+ * (longest first), query heads of one kv head side by side.  For LOCAL_GLOBAL the
+ * ATTN_WORK_GLOBAL_ROWS items follow them.  All items run in one launch: rows in G
+ * are written only by ATTN_WORK_GLOBAL_ROWS items.
  */
 #define ATTN_TILE 128
 #define ATTN_WORK_INTS 8

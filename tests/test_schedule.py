@@ -106,9 +106,15 @@ def _check(kind, S, w=0, G=(), B=1, Hq=2, Hkv=1, check_classes=True):
     # every (bh, q_tile) exactly once among the first-launch items
     pairs = {(int(a), int(b)) for a, b in items[:n_first, :2]}
     assert pairs == {(bh, q) for bh in range(B * Hq) for q in range(nq)}
-    # longest first
+    # kv-head groups whose K and V fit in 32 MB (at d = 128) one after another, longest first in each
     cost = (items[:n_first, 3] - items[:n_first, 2]) + items[:n_first, 7]
-    assert np.all(np.diff(cost) <= 0)
+    g_kv = max(1, min(B * Hkv, (32 << 20) // (512 * S)))
+    bh = items[:n_first, 0]
+    unit = (bh // Hq) * Hkv + (bh % Hq) // (Hq // Hkv)
+    gidx = unit // g_kv
+    assert np.all(np.diff(gidx) >= 0)
+    for g in np.unique(gidx):
+        assert np.all(np.diff(cost[gidx == g]) <= 0)
     if len(items) > n_first:  # global-row chunks are no longer than the longest query-tile item
         assert np.all(items[n_first:, 3] - items[n_first:, 2] <= max(1, int(cost.max())))
     counts = _simulate(items, n_first, kind, S, w, set(G), check_classes)

@@ -29,6 +29,7 @@ struct attn_plan {
     int4* d_work = nullptr;
     int* d_globals = nullptr;
     unsigned* d_gbits = nullptr;
+    int* d_gsplit = nullptr;
     unsigned char* d_isg = nullptr;
     int* d_err = nullptr;
     float* d_part = nullptr;  // partial results of the chunked global-row items
@@ -154,7 +155,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 
 void free_plan(attn_plan* h) {
     if (!h) return;
-    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_isg, h->d_err, h->d_part, h->d_counters,
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_gsplit, h->d_isg, h->d_err, h->d_part, h->d_counters,
                     h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork};
     for (void* b : bufs)
         if (b) cudaFree(b);
@@ -222,6 +223,8 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
             return fail(e);
         if ((e = upload(&h->d_gbits, h->sched.global_bits.data(), h->sched.global_bits.size())) != cudaSuccess)
             return fail(e);
+        if ((e = upload(&h->d_gsplit, h->sched.gsplit.data(), h->sched.gsplit.size())) != cudaSuccess)
+            return fail(e);
         attn::TcParams& p = h->tp;
         p.n_gtiles = (nG + (int)kTileRows - 1) / (int)kTileRows;
         if (nG > 0 && h->sched.n_chunks > 1) {
@@ -240,6 +243,7 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         p.globals = h->d_globals;
         p.n_global = nG;
         p.global_bits = h->d_gbits;
+        p.gsplit = reinterpret_cast<const int2*>(h->d_gsplit);
         p.err = h->d_err;
         p.watchdog_ns = 2000000000LL;
         p.withhold_v = 0;

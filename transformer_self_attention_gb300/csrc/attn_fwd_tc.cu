@@ -27,10 +27,12 @@
 // Tensor memory: S/P in columns [0, 128), O in [128, 128 + d); 256 columns per
 // CTA, so two CTAs share an SM and one's softmax overlaps the other's MMAs.
 //
-// Local + global ("Transformer 演进与变体", section 稀疏注意力) runs as one launch:
+// Local + global ("Transformer 演进与变体", section 稀疏注意力) runs as one launch of
+// its own instantiation (LG):
 //   * a query tile's global keys outside its band of key tiles are gathered by the
 //     producer warp (plain loads into the swizzled layout) into narrow key tiles of
-//     32, 64, 96 or 128 columns, every column allowed for every row;
+//     32, 64, 96 or 128 columns, every column allowed for every row, taken before the
+//     band tiles;
 //   * the global rows are computed by their own items against every key, split into key
 //     chunks; each chunk writes a partial result and the last chunk of a row tile to
 //     finish (an arrival counter) merges them into O and LSE;
@@ -92,7 +94,6 @@ struct Shared {  // small control block after the tiles
     uint64_t bar[NBAR];
     uint32_t tmem_base;
     volatile int abort;
-    int g_lo, g_hi;          // gathered keys: the globals before the band are G[0, g_lo), after it G[g_hi, nG)
     volatile int merge_last; // global-row chunk items: this CTA finished last and merges the chunks
 };
 
@@ -414,17 +415,6 @@ __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMa
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// First index of the sorted list g[0, n) whose value is >= x.
-__device__ __forceinline__ int lower_bound_dev(const int* g, int n, long x) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if ((long)__ldg(g + mid) < x) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
 // Rows pos(r), r < n_rows, of one [S, D] bf16 head copied with plain loads into a 128-row tile in
 // the layout the TMA loads write (128-byte swizzle: 64-column blocks of BM * 128 bytes, the 16-byte
 // chunk c of row r at chunk position c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32 lanes of
@@ -555,7 +545,7 @@ __device__ __forceinline__ void merge_global_row(const TcParams& p, size_t slot0
     if (lse_out) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
-template <int D, int BIAS, bool F8>
+template <int D, int BIAS, bool F8, bool LG>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
     using C = Cfg<D, BIAS, F8>;
     constexpr bool ALIBI = BIAS == BIAS_ALIBI_ELEM;  // the per-element bias passes
@@ -575,12 +565,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     const int4 w1 = p.work[2 * item + 1];
     const int bh = w0.x, q_tile = w0.y, kv_begin = w0.z, kv_end = w0.w;
     const int full_begin = w1.x, full_end = w1.y, flags = w1.z, n_gt = w1.w;
-    const bool grows = (flags & ATTN_WORK_GLOBAL_ROWS) != 0;
+    const bool grows = LG && (flags & ATTN_WORK_GLOBAL_ROWS) != 0;
     const int n_band = kv_end - kv_begin;
-    const int n_iter = n_band + ((flags & ATTN_WORK_GLOBAL_COLS) ? n_gt : 0);
-    // Band key tile of iteration it.  With the causal ALiBi bias the tiles run from the diagonal
-    // downwards: the bias is 0 at j = i and falls with the distance, so a row's running max is
-    // set by its first tile and the lazy rescale stays rare.
+    // local + global: the gathered key tiles (n_gat of them) run first, then the band tiles
+    const int n_gat = (LG && (flags & ATTN_WORK_GLOBAL_COLS)) ? n_gt : 0;
+    const int n_iter = n_band + n_gat;
+    // Band key tile of iteration n_gat + it.  With the causal ALiBi bias the tiles run from the
+    // diagonal downwards: the bias is 0 at j = i and falls with the distance, so a row's running
+    // max is set by its first tile and the lazy rescale stays rare.
     constexpr bool REV = BIAS == BIAS_ALIBI_MMA;
     auto band_tile = [&](int it) { return REV ? kv_end - 1 - it : kv_begin + it; };
     const int b = bh / p.Hq, a = bh - b * p.Hq;
@@ -590,13 +582,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), (i == B_PFULL || i == B_PFULL1) ? 128u : 1u);
         sh->abort = 0;
         sh->merge_last = 0;
-        if (flags & ATTN_WORK_GLOBAL_COLS) {  // the global keys outside the band [kv_begin, kv_end) tiles
-            sh->g_lo = lower_bound_dev(p.globals, p.n_global, (long)kv_begin * BN);
-            sh->g_hi = lower_bound_dev(p.globals, p.n_global, (long)kv_end * BN);
-        } else {
-            sh->g_lo = 0;
-            sh->g_hi = p.n_global;
-        }
         fence_barrier_init();
     }
     if constexpr (BIAS == BIAS_ALIBI_MMA) {
@@ -633,24 +618,21 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
-    // gathered key tiles (after the band tiles): n_out global keys lie outside the band; tile k holds
-    // the outside keys k * BN .. k * BN + ncols(k) - 1, padded to a multiple of 32 columns
-    const int g_lo = sh->g_lo, g_hi = sh->g_hi;
+    // gathered key tiles: n_out global keys lie outside the band, G[0, g_lo) before it and
+    // G[g_hi, nG) after it (the schedule's split of G for this query tile); tile it < n_gat holds
+    // the outside keys it * BN .. it * BN + cols(it) - 1, padded to a multiple of 32 columns
+    const int2 gs = n_gat ? __ldg(p.gsplit + q_tile) : make_int2(0, p.n_global);
+    const int g_lo = gs.x, g_hi = gs.y;
     const int n_out = g_lo + (p.n_global - g_hi);
-    auto gathered_cols = [&](int it) { return min(BN, n_out - (it - n_band) * BN); };
+    auto gathered_cols = [&](int it) { return min(BN, n_out - it * BN); };
     auto outside_key = [&](int e) -> long { return __ldg(p.globals + (e < g_lo ? e : g_hi + (e - g_lo))); };
 
-    if (warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ producer
+    if (LG && warp == WARP_PRODUCER) {
+        // ------------------------------------------------------------ producer (local + global)
         // Lane 0 issues the TMA copies and waits for free buffers; all lanes gather the rows of the
         // global tokens (plain loads into the swizzled layout, then a proxy fence so the tensor core
-        // sees them, then one arrival).
-        const int bias_plane = (BIAS == BIAS_MATRIX)
-                                   ? (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
-                                   : 0;
-        if constexpr (BIAS == BIAS_MATRIX) {
-            if (lane == 0) prefetch_tmap(&p.tm_bias);
-        }
+        // sees them, then one arrival).  The gathered key tiles come first, so that their loads
+        // overlap the copy of the Q tile.
         if (grows) {  // query rows G[q_tile * BM + r]; rows past the list are zero
             const int r0 = q_tile * BM;
             gather_rows<D>(smem + C::OFF_Q, p.q + (size_t)bh * p.S * D, BM,
@@ -666,12 +648,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         int k_loaded = 0, v_loaded = 0;
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
-            const bool in_band = it < n_band;
-            const int row = in_band ? band_tile(it) * BN : 0;
-            // gathered tiles: the outside keys (it - n_band) * BN + r, r < ncols, padded with zero rows
+            const bool in_band = it >= n_gat;
+            const int row = in_band ? band_tile(it - n_gat) * BN : 0;
+            // gathered tiles: the outside keys it * BN + r, r < ncols, padded with zero rows
             const int gcols = in_band ? 0 : gathered_cols(it);
             const int grows_pad = (gcols + 31) & ~31;
-            auto gpos = [&](int r) -> long { return r < gcols ? outside_key((it - n_band) * BN + r) : -1L; };
+            auto gpos = [&](int r) -> long { return r < gcols ? outside_key(it * BN + r) : -1L; };
             if (it > 0) {
                 bool w = true;
                 if (lane == 0) w = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
@@ -689,9 +671,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 if (lane == 0) mbar_arrive(bar(B_KFULL));
             }
             ++k_loaded;
-            if constexpr (BIAS == BIAS_MATRIX) {  // the softmax reads this tile's bias rows a tile later
-                if (lane == 0) tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
-            }
             if (it > 0) {
                 bool w = true;
                 if (lane == 0) w = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
@@ -716,6 +695,40 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if (k_loaded) drain_wait(bar(B_KFULL), (k_loaded - 1) & 1, p);
             if (v_loaded) drain_wait(bar(B_VFULL), (v_loaded - 1) & 1, p);
         }
+    } else if (warp == WARP_PRODUCER) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const CUtensorMap* qmap = &p.tm_q;
+            const int bias_plane = (BIAS == BIAS_MATRIX)
+                                       ? (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a)
+                                       : 0;
+            if constexpr (BIAS == BIAS_MATRIX) prefetch_tmap(&p.tm_bias);
+            mbar_arrive_expect_tx(bar(B_Q), C::TILE_BYTES);
+            for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_q + s * C::SUB, qmap, bar(B_Q), s * C::XW, q_tile * BM, bh);
+            int k_loaded = 0, v_loaded = 0;
+            bool ok = true;
+            for (int it = 0; it < n_iter && ok; ++it) {
+                const CUtensorMap* km = &p.tm_k;
+                const CUtensorMap* vm = &p.tm_v;
+                const int row = band_tile(it) * BN;
+                if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
+                mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * C::XW, row, bkv);
+                ++k_loaded;
+                if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
+                    tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
+                if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
+                if (p.withhold_v) continue;
+                mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
+                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * C::XW, row, bkv);
+                ++v_loaded;
+            }
+            if (sh->abort) {  // let the copies this thread issued land before the CTA exits
+                drain_wait(bar(B_Q), 0, p);
+                if (k_loaded) drain_wait(bar(B_KFULL), (k_loaded - 1) & 1, p);
+                if (v_loaded) drain_wait(bar(B_VFULL), (v_loaded - 1) & 1, p);
+            }
+        }
     } else if (warp == WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -731,7 +744,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
                 // a gathered-key tile is ncols wide (a multiple of 32): N = ncols for S, K = ncols for P V
-                const bool narrow = it >= n_band;
+                const bool narrow = LG && it < n_gat;
                 const int ncols = narrow ? (gathered_cols(it) + 31) & ~31 : BN;
                 const uint32_t idesc_s = narrow ? idesc_bf16_f32(BM, ncols, false) : idesc_qk;
 #pragma unroll
@@ -807,7 +820,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             else if (p.kind == ATTN_MASK_SLIDING || p.kind == ATTN_MASK_LOCAL_GLOBAL) { lo = i - p.window; hi = i + p.window; }
             if (hi > p.S - 1) hi = p.S - 1;
         }
-        const bool lg = (p.kind == ATTN_MASK_LOCAL_GLOBAL) && !grows;
+        const bool lg = LG && !grows;
         const float sl2 = p.scale_log2;
         const float mL = (BIAS != BIAS_NONE) ? p.alibi[a] * 1.4426950408889634f : 0.f;  // ALiBi slope, log2 units
         const bool causal_kind = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
@@ -820,45 +833,44 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         for (int it = 0; it < n_iter; ++it) {
             uint4 bv[BIAS == BIAS_MATRIX ? 16 : 1];  // this row's bias for the tile (issued before the S wait)
             if constexpr (BIAS == BIAS_MATRIX) {
-                const long c0 = (long)band_tile(it) * BN;
+                const long c0 = (long)band_tile(it - n_gat) * BN;
                 const uint16_t* brow =
                     (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr;
                 load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
             }
             // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate).  It does
-            // not depend on S, so it is worked out before the wait for S.
+            // not depend on S, so it is worked out before the wait for S (the global-key bits of a
+            // local + global tile are loaded here and merged in after the wait).
             bool partial = true;
-            bool has_g = false;  // the tile holds global keys (local + global, band tiles)
-            const bool gathered = it >= n_band;
+            const bool gathered = LG && it < n_gat;
             int gcols = BN;      // gathered tiles: columns holding keys (all allowed: they lie outside the band)
             TileMask mk{0, -1, 0u, 0u, 0u, 0u};
             uint4 g4 = make_uint4(0u, 0u, 0u, 0u);
             if (!gathered) {
-                const int t = band_tile(it);
+                const int t = band_tile(it - n_gat);
                 partial = t < full_begin || t >= full_end;
                 if (partial) {
                     const long c0 = (long)t * BN;
                     mk.a0 = (int)max(-1L, min((long)BN, lo - c0));
                     mk.a1 = (int)max(-1L, min((long)BN, hi - c0));
-                    if (lg) {
-                        g4 = *reinterpret_cast<const uint4*>(p.global_bits + 4 * t);
-                        has_g = (g4.x | g4.y | g4.z | g4.w) != 0u;
-                    }
+                    if (lg) g4 = __ldg(reinterpret_cast<const uint4*>(p.global_bits + 4 * t));
                 }
             } else {
                 gcols = gathered_cols(it);
                 mk.a1 = gcols - 1;
             }
-            // no lower bound inside the tile and no global keys (causal diagonal tiles, the upper edge of
-            // a window): the cheap mask form, when every row of the warp qualifies
-            const bool upper = !gathered && __all_sync(0xffffffffu, partial && !has_g && mk.a0 <= 0);
+            // no lower bound inside the tile (causal diagonal tiles, the upper edge of a window): the
+            // cheap mask form, when every row of the warp qualifies (not for local + global, whose
+            // tiles may hold global keys)
+            const bool upper = !lg && !gathered && __all_sync(0xffffffffu, partial && mk.a0 <= 0);
             // the general form (and every partial tile of the biased passes, which take no other form):
             // the interval and the global keys as column bits
-            if (partial && !gathered && (!upper || BIAS != BIAS_NONE)) {
-                mk.w0 = interval_word(mk.a0, mk.a1, 0) | g4.x;
-                mk.w1 = interval_word(mk.a0, mk.a1, 1) | g4.y;
-                mk.w2 = interval_word(mk.a0, mk.a1, 2) | g4.z;
-                mk.w3 = interval_word(mk.a0, mk.a1, 3) | g4.w;
+            const bool bits = partial && !gathered && (!upper || BIAS != BIAS_NONE);
+            if (bits) {
+                mk.w0 = interval_word(mk.a0, mk.a1, 0);
+                mk.w1 = interval_word(mk.a0, mk.a1, 1);
+                mk.w2 = interval_word(mk.a0, mk.a1, 2);
+                mk.w3 = interval_word(mk.a0, mk.a1, 3);
             }
             // warp-uniform exit: the tensor-memory accesses below are warp-collective
             if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
@@ -866,11 +878,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
+            if (lg && bits) {
+                mk.w0 |= g4.x; mk.w1 |= g4.y; mk.w2 |= g4.z; mk.w3 |= g4.w;
+            }
             // ---- pass 1: row max of the (masked) scores, in log2 units
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
             if constexpr (ALIBI) {
-                base = (float)(i - (long)band_tile(it) * BN);
+                base = (float)(i - (long)band_tile(it - n_gat) * BN);
                 if (causal_kind)
                     mx = partial ? tile_row_max_alibi<MASK_ANY, false>(t_s, mk, sl2, mL, base)
                                  : tile_row_max_alibi<MASK_NONE, false>(t_s, mk, sl2, mL, base);
@@ -880,7 +895,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             } else if constexpr (BIAS == BIAS_MATRIX) {
                 mx = partial ? tile_row_max_matbias<MASK_ANY>(t_s, mk, sl2, bv) : tile_row_max_matbias<MASK_NONE>(t_s, mk, sl2, bv);
             } else {
-                if constexpr (BIAS == BIAS_NONE && !F8) {
+                if constexpr (LG) {
                     if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
                     else
                         mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
@@ -892,7 +907,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
                     // the tile's constant part of the bias, m_a (c0 - i), in log2 units
-                    base = mL * (float)((long)band_tile(it) * BN - i);
+                    base = mL * (float)((long)band_tile(it - n_gat) * BN - i);
                     mx += base;  // -inf stays -inf
                 }
             }
@@ -942,7 +957,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                               : tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL));
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
-                if (BIAS == BIAS_NONE && gathered)
+                if (LG && gathered)
                     sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, sl2, r_eff, bar(B_PFULL), fix);
                 else
                     sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
@@ -964,9 +979,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             // band items of local + global whose tile holds global rows leave those rows to the
             // global-row items and store the others directly
-            const bool skip_g = !grows && (flags & ATTN_WORK_HAS_GLOBAL_ROWS) &&
-                                ((__ldg(p.global_bits + 4 * q_tile + (r >> 5)) >> (r & 31)) & 1u);
-            if (!grows && (flags & ATTN_WORK_HAS_GLOBAL_ROWS)) {
+            const bool tile_has_g = LG && !grows && (flags & ATTN_WORK_HAS_GLOBAL_ROWS);
+            const bool skip_g = tile_has_g && ((__ldg(p.global_bits + 4 * q_tile + (r >> 5)) >> (r & 31)) & 1u);
+            if (tile_has_g) {
                 store_row_direct<D>(t_o, static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D, inv_l,
                                     row_valid && !skip_g);
             } else if (!grows) {
@@ -1048,12 +1063,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-template <int D, int BIAS, bool F8 = false>
+template <int D, int BIAS, bool F8 = false, bool LG = false>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
     using C = Cfg<D, BIAS, F8>;
-    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8>), C::SMEM_ALLOC);
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8, LG>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_fwd_tc_kernel<D, BIAS, F8><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_fwd_tc_kernel<D, BIAS, F8, LG><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1077,6 +1092,9 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
     } else if (p.alibi) {
         if (d == 128) return launch<128, BIAS_ALIBI_ELEM>(p, n_items, stream);
         if (d == 64) return launch<64, BIAS_ALIBI_ELEM>(p, n_items, stream);
+    } else if (p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0) {  // gathered keys, global-row chunks
+        if (d == 128) return launch<128, BIAS_NONE, false, true>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_NONE, false, true>(p, n_items, stream);
     } else {
         if (d == 128) return launch<128, BIAS_NONE>(p, n_items, stream);
         if (d == 64) return launch<64, BIAS_NONE>(p, n_items, stream);

@@ -5,8 +5,8 @@
 // processes that must keep their device footprint fixed after start-up.  For
 // them this entry point takes the problem description and the caller's Q, K,
 // V, O, LSE buffers and keeps every other device byte it needs (error word,
-// work list, global-token list and bits, partial results and arrival counters
-// of the global-row chunks) in one file-scope __device__ array of
+// work list, global-token list, bits and per-tile split, partial results and
+// arrival counters of the global-row chunks) in one file-scope __device__ array of
 // ATTN_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library holds
 // until the process exits.
 //
@@ -151,6 +151,14 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     const int nk = (S + ATTN_TILE - 1) / ATTN_TILE;
     std::vector<unsigned> bits((size_t)nk * 4, 0u);
     for (int g : G) bits[(size_t)(g / ATTN_TILE) * 4 + (g % ATTN_TILE) / 32] |= 1u << (g % 32);
+    // per query tile: the globals before its band of key tiles, and before the band's end
+    std::vector<int> gsplit((size_t)nk * 2, 0);
+    for (int t = 0; t < n_first; ++t) {
+        const int* it = &items[(size_t)t * ATTN_WORK_INTS];
+        const long lo = std::min<long>((long)it[2] * ATTN_TILE, S), hi = std::min<long>((long)it[3] * ATTN_TILE, S);
+        gsplit[(size_t)it[1] * 2] = (int)(std::lower_bound(G.begin(), G.end(), lo) - G.begin());
+        gsplit[(size_t)it[1] * 2 + 1] = (int)(std::lower_bound(G.begin(), G.end(), hi) - G.begin());
+    }
 
     // carve the fixed scratch area; refuse problems that do not fit
     const size_t off_work = 256;
@@ -162,7 +170,8 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     const int n_gtiles = (nG + ATTN_TILE - 1) / ATTN_TILE;
     const size_t part_rows = n_chunks > 1 ? (size_t)B * Hq * nG * n_chunks : 0;
     const size_t n_ctr = n_chunks > 1 ? (size_t)B * Hq * n_gtiles : 0;
-    const size_t off_part_o = off_bits + round256(bits.size() * sizeof(unsigned));
+    const size_t off_gsplit = off_bits + round256(bits.size() * sizeof(unsigned));
+    const size_t off_part_o = off_gsplit + round256(gsplit.size() * sizeof(int));
     const size_t off_part_lse = off_part_o + round256(part_rows * d_k * sizeof(float));
     const size_t off_ctr = off_part_lse + round256(part_rows * sizeof(float));
     const size_t total = off_ctr + round256(n_ctr * sizeof(unsigned));
@@ -179,6 +188,9 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     if (nG > 0 && upload_words(reinterpret_cast<unsigned*>(sc + off_glob), G.data(), G.size(), stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (upload_words(reinterpret_cast<unsigned*>(sc + off_bits), bits.data(), bits.size(), stream) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (upload_words(reinterpret_cast<unsigned*>(sc + off_gsplit), gsplit.data(), gsplit.size(), stream) !=
+        cudaSuccess)
         return ATTN_ERR_CUDA;
     if (n_ctr > 0 && cudaMemsetAsync(sc + off_ctr, 0, n_ctr * sizeof(unsigned), stream) != cudaSuccess)
         return ATTN_ERR_CUDA;
@@ -197,6 +209,7 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
     p.globals = reinterpret_cast<const int*>(sc + off_glob);
     p.n_global = nG;
     p.global_bits = reinterpret_cast<const unsigned*>(sc + off_bits);
+    p.gsplit = reinterpret_cast<const int2*>(sc + off_gsplit);
     p.q = static_cast<const uint16_t*>(Q);
     p.k = static_cast<const uint16_t*>(K);
     p.v = static_cast<const uint16_t*>(V);

@@ -25,6 +25,9 @@ struct TcParams {
     const int* globals;  // sorted global positions (device)
     int n_global;
     const unsigned* global_bits;  // 4 words per 128-position tile (key tiles and query tiles alike)
+    // per query tile {g_lo, g_hi}: the globals outside its band of key tiles are G[0, g_lo) and
+    // G[g_hi, n_global) (local + global)
+    const int2* gsplit;
     // local + global: the bf16 bits of Q, K, V, from which the producer warp gathers the global
     // rows (query rows of the global-row items, keys and values of the gathered key tiles)
     const uint16_t* q;

@@ -117,15 +117,30 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
         return protos[x].q_tile > protos[y].q_tile;
     });
 
+    // The (batch, kv head) units are taken in groups whose K and V fit in about 32 MB of L2
+    // (at d = 128, the larger head size): every item of a group, longest first, before the
+    // next group.  The query tiles that read the same K/V tiles then run together and the
+    // K/V tiles come from DRAM about once; the long items of one group overlap the next
+    // group, so only the last group's tail stands alone.
     const int BH = in.B * in.Hq;
+    const int group = in.Hq / in.Hkv;
+    const long kv_bytes = 512L * S;  // K and V of one kv head: 2 * S * 128 * 2 bytes
+    const int g_kv = (int)std::max(1L, std::min((long)in.B * in.Hkv, (32L << 20) / kv_bytes));
+    const int n_groups = (in.B * in.Hkv + g_kv - 1) / g_kv;
     out->items.clear();
     out->items.reserve((size_t)(protos.size() + (size_t)n_gtiles) * BH * ATTN_WORK_INTS);
-    for (int k : order) {
-        const Proto& p = protos[k];
-        for (int bh = 0; bh < BH; ++bh) {
-            const int it[ATTN_WORK_INTS] = {bh, p.q_tile, p.kv_begin, p.kv_end,
-                                            p.full_begin, p.full_end, p.flags, p.n_gtiles};
-            out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const int u0 = gi * g_kv, u1 = std::min(in.B * in.Hkv, u0 + g_kv);  // kv units [u0, u1)
+        for (int k : order) {
+            const Proto& p = protos[k];
+            for (int u = u0; u < u1; ++u) {
+                const int b = u / in.Hkv, g = u % in.Hkv;
+                for (int a = g * group; a < (g + 1) * group; ++a) {
+                    const int it[ATTN_WORK_INTS] = {b * in.Hq + a, p.q_tile, p.kv_begin, p.kv_end,
+                                                    p.full_begin, p.full_end, p.flags, p.n_gtiles};
+                    out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
+                }
+            }
         }
     }
     out->n_main = (int)protos.size() * BH;
@@ -152,6 +167,12 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
                     out->items.insert(out->items.end(), it, it + ATTN_WORK_INTS);
                     ++out->n_grows;
                 }
+    }
+    out->gsplit.assign((size_t)nq * 2, 0);
+    for (const Proto& p : protos) {  // #globals before the band, and #globals before its end
+        const long band_lo = std::min<long>((long)p.kv_begin * T, S), band_hi = std::min<long>((long)p.kv_end * T, S);
+        out->gsplit[(size_t)p.q_tile * 2] = cntG[band_lo];
+        out->gsplit[(size_t)p.q_tile * 2 + 1] = cntG[band_hi];
     }
     out->n_kv_tiles = nk;
     out->n_global_tiles = n_gtiles;

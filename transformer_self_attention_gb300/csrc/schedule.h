@@ -31,6 +31,7 @@ struct Schedule {
     int n_kv_tiles = 0;
     int n_global_tiles = 0;
     std::vector<unsigned> global_bits;  // 4 words per 128-position tile: bit c set if position tile*128+c is global
+    std::vector<int> gsplit;  // 2 ints per query tile: the globals outside its band are G[0, [0]) and G[[1], nG)
 };
 
 // Builds the schedule.  Returns ATTN_OK, or ATTN_ERR_UNSUPPORTED if a query
