@@ -75,24 +75,91 @@ def ncu_traffic(workload_name: str, kernel: str = "attn_fwd_tc", sources=KERNEL_
     return float(m_bytes.group(1))
 
 
+# The NVML sampler that ClockSampler runs in a child process (no torch import, so it starts in
+# milliseconds).  It reads the SM clock, its maximum, the power draw and the clock event reasons
+# every `interval` seconds, stamped with CLOCK_MONOTONIC, until its standard input closes.
+_NVML_SAMPLER = r"""
+import ctypes, sys, time, select
+bus, interval = sys.argv[1].encode(), float(sys.argv[2])
+nv = ctypes.CDLL("libnvidia-ml.so.1")
+assert nv.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+assert nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0
+get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+mhz, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+print("ready", flush=True)
+out = []
+k = 0
+while True:
+    t = time.monotonic()
+    nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))       # NVML_CLOCK_SM
+    get_reasons(h, ctypes.byref(rs))
+    if k % 16 == 0:                                          # the power reading is slower: every 16th
+        nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+    k += 1
+    out.append("%.6f %d %d %d %d" % (t, mhz.value, mx.value, mw.value, rs.value))
+    if select.select([sys.stdin], [], [], interval)[0] and not sys.stdin.readline():
+        break
+print("\n".join(out), flush=True)
+nv.nvmlShutdown()
+"""
+
+# NVML clock event reason bits (nvml.h)
+_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and throttle reasons sampled during the timed region.
+
+    NVML in a child process every 0.25 ms (its readings are stamped with the monotonic clock, and
+    the summary keeps those between mark_start() and mark_end(), weighting each reading by the
+    time until the next); nvidia-smi every 200 ms when NVML cannot be loaded.
+    """
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.proc = None
+    def __init__(self, gpu_index: int, device=None):
+        self.proc, self.kind, self.t0, self.t1 = None, None, None, None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (FileNotFoundError, OSError):
+            import torch
+            pr = torch.cuda.get_device_properties(device if device is not None else gpu_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_SAMPLER, bus, "0.00025"], stdin=subprocess.PIPE,
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            if self.proc.stdout.readline().strip() == "ready":
+                self.kind = "nvml"
+            else:
+                self.proc.kill()
+                self.proc = None
+        except Exception:
             self.proc = None
+        if self.proc is None:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.kind = "nvidia-smi"
+            except (FileNotFoundError, OSError):
+                self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
 
     def stop(self):
         if self.proc is None:
             return None
+        if self.kind == "nvml":
+            try:
+                out, _ = self.proc.communicate(input="", timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                return None
+            return self._summary_nvml(out)
         time.sleep(0.25)
         self.proc.terminate()
         try:
@@ -100,6 +167,48 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        return self._summary_smi(out)
+
+    def _summary_nvml(self, out):
+        rows = []
+        for line in out.strip().splitlines():
+            parts = line.split()
+            if len(parts) == 5:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), float(parts[3]), int(parts[4])))
+        if not rows:
+            return None
+        t0 = self.t0 if self.t0 is not None else rows[0][0]
+        t1 = self.t1 if self.t1 is not None else rows[-1][0]
+        # readings inside the timed region, plus the last one before it (in force at its start)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        before = [r for r in rows if r[0] < t0]
+        sel = ([before[-1]] if before else []) + inside
+        if not sel:
+            return None
+        # time-weighted median of the SM clock over [t0, t1]
+        spans = []
+        for k, r in enumerate(sel):
+            a = max(r[0], t0)
+            b = sel[k + 1][0] if k + 1 < len(sel) else t1
+            spans.append((r[1], max(0.0, b - a)))
+        total = sum(w for _, w in spans)
+        acc, med = 0.0, spans[0][0]
+        for mhz, wgt in sorted(spans):
+            acc += wgt
+            if acc >= 0.5 * total:
+                med = mhz
+                break
+        reasons = set()
+        for r in sel:
+            for bit, name in _REASON_BITS.items():
+                if r[4] & bit:
+                    reasons.add(name)
+        return {"sm_mhz": med, "sm_max_mhz": max(r[2] for r in sel), "reasons": sorted(reasons),
+                "samples": len(inside), "sampler": "NVML every 0.25 ms in a child process",
+                "sm_mhz_time_weighted_median": med, "sm_mhz_min": min(r[1] for r in sel),
+                "power_w_max": max(r[3] for r in sel) / 1000.0, "timed_region_s": t1 - t0}
+
+    def _summary_smi(self, out):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -118,7 +227,7 @@ class ClockSampler:
             return None
         loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sampler": "nvidia-smi every 200 ms"}
 
 
 def dist_setup():
@@ -173,6 +282,18 @@ def cpu_baseline(w: wl.Workload, target_s: float = 12.0, frac: float | None = No
                       f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
 
 
+def fwd_config(args, w, world: int = 1) -> dict:
+    """The workload description both arms print (identical keys and values for one command line)."""
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
+            "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
+            "useful_gflop_per_step": wl.useful_flops(w) / 1e9,
+            "l2": "flushed before every GPU step (256 MiB write)",
+            "score_bias": ("alibi, slopes 2^(-8(a+1)/H)" if args.alibi else
+                           "matrix [1, Hq, S, S] bf16 N(0, 2^2)" if args.bias else "none"),
+            "inputs": "E4M3, per-tensor scales" if args.fp8 else w.dtype,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -193,8 +314,7 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
-                       "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx)},
+            "config": fwd_config(args, w, max(1, args.gpus)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
                              "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -307,7 +427,9 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local) if rank == 0 else None
+    clocks = ClockSampler(local, dev) if rank == 0 else None
+    if clocks:
+        clocks.mark_start()
     wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.zero_()
@@ -316,6 +438,8 @@ def run_ours(args, w):
         ends[s].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    if clocks:
+        clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -365,12 +489,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if args.fp8 else ("bf16" if w.dtype == "bf16" else "f32"),
             "data": "synthetic" + (" (E4M3, per-tensor scales)" if args.fp8 else ""),
-            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
-                       "mask": wl.MASK_NAMES[w.kind], "window": w.window, "n_global": len(w.globals_idx),
-                       "useful_gflop_per_step": useful / 1e9, "l2": "flushed before every step (256 MiB write)",
-                       "score_bias": ("alibi, slopes 2^(-8(a+1)/H)" if args.alibi else
-                                      "matrix [1, Hq, S, S] bf16 N(0, 2^2)" if args.bias else "none"),
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": fwd_config(args, w, world),
             "pct_of_peak": {"measured": 100.0 * achieved / peak, "nominal": 100.0 * achieved / NOMINAL_BF16_TFLOPS,
                             "peak_source": pk_src},
             "roofline": roofline, "gpu_launches": args.steps * launches_per_fwd,
@@ -429,10 +548,12 @@ def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int 
                       f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
 
 
-def _bwd_config(w, useful):
+def _bwd_config(w, useful, world: int = 1):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
             "mask": wl.MASK_NAMES[w.kind], "window": w.window, "pass": "backward (dQ, dK, dV)",
-            "useful_gflop_per_step": useful / 1e9, "flops_per_pair": f"10 d (2.5 x the forward's 4 d)"}
+            "useful_gflop_per_step": useful / 1e9, "flops_per_pair": f"10 d (2.5 x the forward's 4 d)",
+            "l2": "flushed before every GPU step (256 MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def run_reference_backward(args, w):
@@ -450,7 +571,7 @@ def run_reference_backward(args, w):
     line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _bwd_config(w, wl.backward_flops(w)),
+            "config": _bwd_config(w, wl.backward_flops(w), max(1, args.gpus)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -494,7 +615,9 @@ def run_ours_backward(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local) if rank == 0 else None
+    clocks = ClockSampler(local, dev) if rank == 0 else None
+    if clocks:
+        clocks.mark_start()
     wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.zero_()
@@ -503,6 +626,8 @@ def run_ours_backward(args, w):
         ends[s].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    if clocks:
+        clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -546,8 +671,7 @@ def run_ours_backward(args, w):
     line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(_bwd_config(w, useful), l2="flushed before every step (256 MiB write)",
-                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "config": _bwd_config(w, useful, world),
             "roofline": roofline, "gpu_launches": 3 * args.steps, "wall_s_timed_region": wall}
     if e2e:
         line["e2e"] = e2e
@@ -595,10 +719,14 @@ def cpu_baseline_decode(w, target_s: float = 12.0, n_seq: int | None = None):
                       f"{fl / 1e9:.2f} useful GFLOP, fp64 C oracle with OpenMP"}
 
 
-def _decode_config(w, lens):
+def _decode_config(args, w, lens, world: int = 1):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S_q": w.S_q, "S_cap": w.S_cap, "d": w.d,
             "mask": wl.MASK_NAMES[w.kind], "window": w.window, "cache_len": list(lens),
-            "cache": "resident in HBM (the step's inputs are the new query rows)"}
+            "cache": "resident in HBM (the step's inputs are the new query rows)",
+            "useful_gflop_per_step": wl.decode_useful_flops(w, lens) / 1e9,
+            "score_bias": "alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
+            "l2": "flushed before every GPU step (256 MiB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def run_reference_decode(args, w):
@@ -617,7 +745,7 @@ def run_reference_decode(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _decode_config(w, lens),
+            "config": _decode_config(args, w, lens, max(1, args.gpus)),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -662,7 +790,9 @@ def run_ours_decode(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local) if rank == 0 else None
+    clocks = ClockSampler(local, dev) if rank == 0 else None
+    if clocks:
+        clocks.mark_start()
     wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.zero_()
@@ -671,6 +801,8 @@ def run_ours_decode(args, w):
         ends[s].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    if clocks:
+        clocks.mark_end()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -729,10 +861,7 @@ def run_ours_decode(args, w):
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(_decode_config(w, lens), useful_gflop_per_step=useful / 1e9,
-                           score_bias="alibi, slopes 2^(-8(a+1)/H)" if args.alibi else "none",
-                           l2="flushed before every step (256 MiB write)",
-                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "config": _decode_config(args, w, lens, world),
             "roofline": roofline, "gpu_launches": args.steps * launches_per_step, "wall_s_timed_region": wall}
     if e2e:
         line["e2e"] = e2e

@@ -158,7 +158,9 @@ const char* attn_status_string(attn_status s);
  * The query-tile items come first: the (batch, kv head) units in groups of
  * g = max(1, min(B*Hkv, 32 MiB / (512 S))) units (their K and V fit in 32 MiB at
  * d_k = 128), group after group, and within a group by decreasing number of tiles
- * (longest first), query heads of one kv head side by side.  For LOCAL_GLOBAL the
+ * (longest first), query heads of one kv head side by side.  When a group would
+ * hold fewer than 4096 items (g * (Hq/Hkv) * ceil(S/ATTN_TILE)), all units form one
+ * group.  For LOCAL_GLOBAL the
  * ATTN_WORK_GLOBAL_ROWS items follow them.  All items run in one launch: rows in G
  * are written only by ATTN_WORK_GLOBAL_ROWS items.
  */

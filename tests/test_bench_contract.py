@@ -24,6 +24,13 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys():
     assert line["unit"] == "TFLOP/s" and line["value"] > 0 and line["higher_is_better"] is True
     assert line["n_gpus"] == 1 and line["steps"] == 2 and line["warmup"] == 3
     assert line["config"]["workload"] == "tiny_full_f32_B1_H4_S256_d64"
+    # the GPU arm builds its config with the same function and arguments: identical dicts
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+    import workloads as wl
+    args = argparse.Namespace(alibi=False, bias=False, fp8=False)
+    assert line["config"] == json.loads(json.dumps(bench.fwd_config(args, wl.TINY_FULL_F32, 1)))
     assert line["data"] == "synthetic"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
@@ -42,3 +49,23 @@ def test_bias_matrix_with_backward_is_rejected():
     r = _bench("--bias", "--backward")
     assert r.returncode != 0
     assert "--bias" in r.stderr
+
+
+def test_clock_summary_is_time_weighted_over_the_timed_region():
+    """Readings outside [start, end] are dropped (the one in force at the start is kept), each
+    reading weighs the time until the next, and the NVML reason bits map to their names."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.t0, c.t1 = 100.0, 100.010
+    rows = [(99.990, 1500, 0)]                                   # before the region: dropped
+    rows += [(99.9995, 2070, 0)]                                 # in force at the start
+    rows += [(100.000 + 0.001 * k, 1800 if k < 3 else 2070, 0x4 if k == 5 else 0) for k in range(1, 10)]
+    rows += [(100.020, 900, 0x40)]                               # after the region: dropped
+    out = "\n".join("%.6f %d 2070 850000 %d" % r for r in rows)
+    s = c._summary_nvml(out)
+    assert s["samples"] == 9
+    # 2070 MHz holds for 0.001 + 0.007 s, 1800 MHz for 0.002 s: the weighted median is 2070
+    assert s["sm_mhz_time_weighted_median"] == 2070 and s["sm_mhz"] == 2070
+    assert s["sm_mhz_min"] == 1800 and s["reasons"] == ["sw_power_cap"]
+    assert abs(s["power_w_max"] - 850.0) < 1e-9 and s["sm_max_mhz"] == 2070

@@ -106,9 +106,12 @@ def _check(kind, S, w=0, G=(), B=1, Hq=2, Hkv=1, check_classes=True):
     # every (bh, q_tile) exactly once among the first-launch items
     pairs = {(int(a), int(b)) for a, b in items[:n_first, :2]}
     assert pairs == {(bh, q) for bh in range(B * Hq) for q in range(nq)}
-    # kv-head groups whose K and V fit in 32 MB (at d = 128) one after another, longest first in each
+    # kv-head groups whose K and V fit in 32 MB (at d = 128) one after another when every group holds
+    # at least 4096 items, longest first in each
     cost = (items[:n_first, 3] - items[:n_first, 2]) + items[:n_first, 7]
     g_kv = max(1, min(B * Hkv, (32 << 20) // (512 * S)))
+    if g_kv * (Hq // Hkv) * nq < 4096:  # short problems: longest first over all heads
+        g_kv = B * Hkv
     bh = items[:n_first, 0]
     unit = (bh // Hq) * Hkv + (bh % Hq) // (Hq // Hkv)
     gidx = unit // g_kv

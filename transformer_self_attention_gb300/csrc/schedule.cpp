@@ -117,15 +117,19 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
         return protos[x].q_tile > protos[y].q_tile;
     });
 
-    // The (batch, kv head) units are taken in groups whose K and V fit in about 32 MB of L2
-    // (at d = 128, the larger head size): every item of a group, longest first, before the
-    // next group.  The query tiles that read the same K/V tiles then run together and the
-    // K/V tiles come from DRAM about once; the long items of one group overlap the next
-    // group, so only the last group's tail stands alone.
+    // Long problems: the (batch, kv head) units are taken in groups whose K and V fit in about
+    // 32 MB of L2 (at d = 128, the larger head size), every item of a group, longest first,
+    // before the next group.  The query tiles that read the same K/V tiles then run together
+    // and the K/V tiles come from DRAM about once.  Grouping delays the long items of the later
+    // groups, which costs at the end of the launch; it is used only when every group holds at
+    // least kMinGroupItems items (many waves of CTAs), so that this tail is small next to the
+    // whole.  Otherwise one group: longest first over all heads.
+    constexpr long kMinGroupItems = 4096;
     const int BH = in.B * in.Hq;
     const int group = in.Hq / in.Hkv;
     const long kv_bytes = 512L * S;  // K and V of one kv head: 2 * S * 128 * 2 bytes
-    const int g_kv = (int)std::max(1L, std::min((long)in.B * in.Hkv, (32L << 20) / kv_bytes));
+    int g_kv = (int)std::max(1L, std::min((long)in.B * in.Hkv, (32L << 20) / kv_bytes));
+    if ((long)g_kv * group * nq < kMinGroupItems) g_kv = in.B * in.Hkv;
     const int n_groups = (in.B * in.Hkv + g_kv - 1) / g_kv;
     out->items.clear();
     out->items.reserve((size_t)(protos.size() + (size_t)n_gtiles) * BH * ATTN_WORK_INTS);
