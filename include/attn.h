@@ -196,24 +196,6 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
 attn_status attn_kv_schedule_host(int S, attn_mask_kind kind, int window, int* items, int cap, int* n_items);
 
 /*
- * attn_pair_schedule_host -- the work items of the CTA-pair forward kernel (host only), which
- * attn_forward runs for ATTN_BF16 handles with d_k = 128, the FULL / CAUSAL / SLIDING /
- * CAUSAL_SLIDING masks and no score bias.  Items come in adjacent pairs (the two CTAs of one
- * cluster, the first issuing the tensor-core products for both): two query heads of one kv head
- * at one query tile when Hq / Hkv is even, else two consecutive query tiles of one head (the second
- * one ceil(S / ATTN_TILE), past the sequence, when the number of query tiles is odd; it writes
- * nothing).  Both items of a pair carry the same kv head and the same key tiles [kv_begin, kv_end),
- * the union of the two query tiles' bands; full_begin / full_end are each query tile's own FULL
- * run, so the other tiles of the union are PARTIAL for it and masked row by row.  Fields as for
- * attn_schedule_host; pairs are ordered as its items (longest first, kv-head groups for long
- * problems).  items may be NULL with cap = 0 to query the count.
- * Errors: ATTN_ERR_INVALID_ARG (bad shape, cap too small), ATTN_ERR_UNSUPPORTED (LOCAL_GLOBAL).
- */
-attn_status attn_pair_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window, int* items,
-                                    int cap, int* n_items);
-
-/*
- * attn_bwd_dq_schedule_host/*
  * attn_bwd_dq_schedule_host -- the work items of the backward's dQ launch (host only):
  * the first-launch items of attn_schedule_host for these arguments (no global tokens),
  * stably regrouped so that the items of the kv heads whose K and V fit in 32 MB

@@ -233,73 +233,3 @@ def test_bwd_dq_order_is_a_grouped_permutation(B, Hq, Hkv, S, d, kind, w):
     assert keys == sorted(keys)
     for k in set(keys):
         assert [it for it in dq.tolist() if key(it) == k] == [it for it in fwd.tolist() if key(it) == k]
-
-
-def _check_pairs(kind, S, w=0, B=1, Hq=2, Hkv=1):
-    """The CTA-pair schedule: adjacent items share the kv head and the key tiles, every query tile of
-    every head appears once (plus padding tiles past S), each CTA's FULL run is its own, and the pairs
-    its rows evaluate, through the kernel's predicate on the other tiles, are exactly the allowed ones."""
-    items = tsa.attn_pair_schedule_host(B, Hq, Hkv, S, kind, w)
-    single, n_first = tsa.attn_schedule_host(B, Hq, Hkv, S, kind, w)
-    nq = (S + T - 1) // T
-    group = Hq // Hkv
-    assert len(items) % 2 == 0
-    own = {(int(it[0]), int(it[1])): it for it in single[:n_first]}
-    seen = set()
-    expect = oracle.row_counts(kind, S, w, [])
-    for k in range(0, len(items), 2):
-        x, y = items[k], items[k + 1]
-        unit = lambda it: (int(it[0]) // Hq) * Hkv + (int(it[0]) % Hq) // group
-        assert unit(x) == unit(y) and x[2] == y[2] and x[3] == y[3]
-        if group % 2 == 0:
-            assert y[0] == x[0] + 1 and y[1] == x[1] and x[0] % 2 == 0
-        else:
-            assert y[0] == x[0] and y[1] == x[1] + 1 and x[1] % 2 == 0
-        kb, ke = int(x[2]), int(x[3])
-        for it in (x, y):
-            bh, q, fb, fe = int(it[0]), int(it[1]), int(it[4]), int(it[5])
-            if q == nq:  # padding tile past S (odd number of query tiles)
-                assert group % 2 == 1 and nq % 2 == 1 and it is y
-                continue
-            assert (bh, q) not in seen
-            seen.add((bh, q))
-            ref = own[(bh, q)]
-            assert kb <= ref[2] and ref[3] <= ke and (fb, fe) == (int(ref[4]), int(ref[5]))
-            i = np.arange(q * T, min(S, (q + 1) * T))
-            lo, hi = _kernel_interval(kind, i, S, w)
-            counts = np.zeros(i.size, dtype=np.int64)
-            for t in range(kb, ke):
-                j = np.arange(t * T, min(S, (t + 1) * T))
-                if fb <= t < fe:
-                    counts += j.size
-                else:
-                    counts += ((j[None, :] >= lo[:, None]) & (j[None, :] <= hi[:, None])).sum(axis=1)
-            assert np.array_equal(counts, expect[i])
-    assert seen == {(bh, q) for bh in range(B * Hq) for q in range(nq)}
-    cost = items[0::2, 3] - items[0::2, 2]
-    g_kv = max(1, min(B * Hkv, (32 << 20) // (512 * S)))
-    if g_kv * group * nq < 4096:
-        g_kv = B * Hkv
-    gidx = ((items[0::2, 0] // Hq) * Hkv + (items[0::2, 0] % Hq) // group) // g_kv
-    assert np.all(np.diff(gidx) >= 0)
-    for g in np.unique(gidx):
-        assert np.all(np.diff(cost[gidx == g]) <= 0)
-
-
-@pytest.mark.parametrize("S", [1, 127, 128, 129, 300, 515])
-@pytest.mark.parametrize("heads", [(2, 2), (4, 1), (6, 2), (3, 1)])
-@pytest.mark.parametrize("kind,w", [(tsa.MASK_FULL, 0), (tsa.MASK_CAUSAL, 0), (tsa.MASK_SLIDING, 129),
-                                    (tsa.MASK_CAUSAL_SLIDING, 200), (tsa.MASK_CAUSAL_SLIDING, 0)])
-def test_pair_schedule(kind, w, S, heads):
-    _check_pairs(kind, S, w, B=2, Hq=heads[0], Hkv=heads[1])
-
-
-@pytest.mark.parametrize("w", [wl.CAUSAL_MHA_4K, wl.SWA_GQA_16K], ids=lambda w: w.name)
-def test_pair_schedule_workloads(w):
-    _check_pairs(w.kind, w.S, w.window, B=1, Hq=w.Hq // w.Hkv * 2 if w.Hq != w.Hkv else 2,
-                 Hkv=2 if w.Hq != w.Hkv else 2)
-
-
-def test_pair_schedule_refuses_local_global():
-    with pytest.raises(tsa.AttnError):
-        tsa.attn_pair_schedule_host(1, 2, 2, 256, tsa.MASK_LOCAL_GLOBAL, 8)

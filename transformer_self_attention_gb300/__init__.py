@@ -32,7 +32,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
             "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode",
             "attn_decode_launch_count", "attn_selftest_device_once", "attn_forward_noalloc_poll_error",
-            "attn_forward_noalloc_set_watchdog", "attn_pair_schedule_host")
+            "attn_forward_noalloc_set_watchdog")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -72,8 +72,6 @@ def _load():
     lib.attn_set_fp8_descale.restype = I
     lib.attn_kv_schedule_host.argtypes = [I, I, I, P, I, ctypes.POINTER(I)]
     lib.attn_kv_schedule_host.restype = I
-    lib.attn_pair_schedule_host.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
-    lib.attn_pair_schedule_host.restype = I
     lib.attn_backward.argtypes = [P] * 11
     lib.attn_backward.restype = I
     lib.attn_bwd_dq_schedule_host.argtypes = [I, I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
@@ -231,20 +229,6 @@ def attn_kv_schedule_host(S, kind, window=0):
                                     ctypes.byref(n))
     if st != ATTN_OK:
         raise AttnError(st, "attn_kv_schedule_host")
-    return items[: n.value]
-
-
-def attn_pair_schedule_host(B, Hq, Hkv, S, kind, window=0):
-    """CTA-pair forward schedule (host only): int32 [2 * pairs, 8], rank 0 of each pair first."""
-    n = ctypes.c_int(0)
-    args = (int(B), int(Hq), int(Hkv), int(S), int(kind), int(window))
-    st = _lib.attn_pair_schedule_host(*args, None, 0, ctypes.byref(n))
-    if st != ATTN_OK:
-        raise AttnError(st, "attn_pair_schedule_host")
-    items = np.zeros((max(n.value, 1), WORK_INTS), dtype=np.int32)
-    st = _lib.attn_pair_schedule_host(*args, items.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n))
-    if st != ATTN_OK:
-        raise AttnError(st, "attn_pair_schedule_host")
     return items[: n.value]
 
 

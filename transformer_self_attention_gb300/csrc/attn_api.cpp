@@ -27,8 +27,6 @@ struct attn_plan {
     attn::Schedule sched;
     // device buffers owned by the handle
     int4* d_work = nullptr;
-    int4* d_pairwork = nullptr;  // CTA-pair kernel items (bf16, d = 128, interval kinds), or null
-    int n_pairs = 0;
     int* d_globals = nullptr;
     unsigned* d_gbits = nullptr;
     int* d_gsplit = nullptr;
@@ -157,7 +155,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 
 void free_plan(attn_plan* h) {
     if (!h) return;
-    void* bufs[] = {h->d_work, h->d_pairwork, h->d_globals, h->d_gbits, h->d_gsplit, h->d_isg, h->d_err, h->d_part, h->d_counters,
+    void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_gsplit, h->d_isg, h->d_err, h->d_part, h->d_counters,
                     h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork};
     for (void* b : bufs)
         if (b) cudaFree(b);
@@ -228,15 +226,6 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
         if ((e = upload(&h->d_gsplit, h->sched.gsplit.data(), h->sched.gsplit.size())) != cudaSuccess)
             return fail(e);
         attn::TcParams& p = h->tp;
-        if (dtype == ATTN_BF16 && d_k == 128 && kind != ATTN_MASK_LOCAL_GLOBAL) {
-            std::vector<int> pair_items;
-            if (attn::build_pair_schedule(in, &pair_items) == ATTN_OK) {
-                if ((e = upload(reinterpret_cast<int**>(&h->d_pairwork), pair_items.data(), pair_items.size())) !=
-                    cudaSuccess)
-                    return fail(e);
-                h->n_pairs = (int)(pair_items.size() / (2 * ATTN_WORK_INTS));
-            }
-        }
         p.n_gtiles = (nG + (int)kTileRows - 1) / (int)kTileRows;
         if (nG > 0 && h->sched.n_chunks > 1) {
             const size_t rows = (size_t)B * Hq * nG * h->sched.n_chunks;
@@ -297,8 +286,6 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         }
         if (K != h->last_k) {
             if (!in_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
-            if (h->n_pairs > 0 && !encode_map(&p.tm_kh, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows / 2))
-                return ATTN_ERR_CUDA;
             h->last_k = K;
         }
         if (V != h->last_v) {
@@ -315,15 +302,8 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
         p.k = static_cast<const uint16_t*>(K);
         p.v = static_cast<const uint16_t*>(V);
         p.item_offset = 0;
-        if (h->n_pairs > 0 && !p.alibi && !p.bias) {
-            // bf16, d = 128, the interval masks: the CTA-pair kernel over the pair items
-            p.work = h->d_pairwork;
-            e = attn::launch_tc_forward_pairs(p, h->d, h->n_pairs, stream);
-            p.work = h->d_work;
-        } else {
-            // one launch: the query-tile items, then (local + global) the global-row chunks
-            e = attn::launch_tc_forward(p, h->d, h->sched.n_main + h->sched.n_grows, stream);
-        }
+        // one launch: the query-tile items, then (local + global) the global-row chunks
+        e = attn::launch_tc_forward(p, h->d, h->sched.n_main + h->sched.n_grows, stream);
     }
     if (e != cudaSuccess) return ATTN_ERR_CUDA;
     if (h->debug) {
@@ -358,24 +338,6 @@ attn_status attn_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kin
     if (cap == 0) return ATTN_OK;
     if (cap < n) return ATTN_ERR_INVALID_ARG;
     std::memcpy(items, sched.items.data(), sched.items.size() * sizeof(int));
-    return ATTN_OK;
-}
-
-attn_status attn_pair_schedule_host(int B, int Hq, int Hkv, int S, attn_mask_kind kind, int window, int* items,
-                                    int cap, int* n_items) {
-    if (!n_items || cap < 0 || (cap > 0 && !items)) return ATTN_ERR_INVALID_ARG;
-    attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, nullptr, 0);
-    if (vs != ATTN_OK) return vs;
-    if (kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
-    const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING;
-    attn::ScheduleInput in{B, Hq, Hkv, S, (int)kind, windowed ? window : 0, {}};
-    std::vector<int> v;
-    attn_status st = attn::build_pair_schedule(in, &v);
-    if (st != ATTN_OK) return st;
-    *n_items = (int)(v.size() / ATTN_WORK_INTS);
-    if (cap == 0) return ATTN_OK;
-    if (cap < *n_items) return ATTN_ERR_INVALID_ARG;
-    std::memcpy(items, v.data(), v.size() * sizeof(int));
     return ATTN_OK;
 }
 

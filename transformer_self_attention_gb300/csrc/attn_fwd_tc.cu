@@ -217,9 +217,9 @@ __device__ __forceinline__ void release_first_half(uint32_t bar_half) {
 // The first half is announced on bar_half as soon as it is stored.  fix() (the row's lazy O
 // rescale and running-sum update) runs after that half is computed and before it is announced:
 // it is off the path from S to the first exponentials, and O is rescaled before O += P V starts.
-template <int MASKED, typename FixO, typename Rel>
-__device__ __forceinline__ float tile_exp_store_r(uint32_t t_s, const TileMask& mk, float sl2, float ref, FixO&& fix,
-                                                 Rel&& release) {
+template <int MASKED, typename FixO>
+__device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                               uint32_t bar_half, FixO&& fix) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -245,16 +245,10 @@ __device__ __forceinline__ float tile_exp_store_r(uint32_t t_s, const TileMask& 
         tmem_st32(t_s + h * 32, pk);
         if (h == 0) {
             fix();
-            release();
+            release_first_half(bar_half);
         }
     }
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
-}
-
-template <int MASKED, typename FixO>
-__device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
-                                               uint32_t bar_half, FixO&& fix) {
-    return tile_exp_store_r<MASKED>(t_s, mk, sl2, ref, fix, [&] { release_first_half(bar_half); });
 }
 
 // tile_exp_store for E4M3 P: four keys per 32-bit tensor-memory column (the A operand
@@ -1069,307 +1063,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-// ---------------------------------------------------------------------------------------------
-// The same forward on a CTA pair (cta_group::2), d = 128, bf16, the interval masks, no bias.
-//
-// A cluster of two CTAs on the two SMs of a pair computes two 128-row query tiles that read the
-// same key/value tiles: two query heads of one GQA group at the same query tile, or (one query
-// head per kv head) two consecutive query tiles of one head.  Rank 0 issues every MMA for both:
-//   S = Q K^T   : M = 256 (each CTA's Q tile), N = 128 keys, each CTA holding 64 of the keys;
-//   O += P V    : M = 256 (each CTA's P in its tensor memory), N = d, each CTA holding V's
-//                 columns [64 r, 64 r + 64) of the 128 keys.
-// Every SM thus loads and reads half of each K and V tile: the shared-memory operand traffic of a
-// 128 x 128 x 16 score product drops from 8 KB to 6 KB per SM (the product is no longer bound by
-// shared-memory bandwidth) and each K/V byte is fetched once for both query tiles.  Each CTA keeps
-// its own softmax warps, mask, running max and epilogue.  The copies of both CTAs complete on the
-// mbarriers of rank 0 (which also expects their bytes); the MMA completions are multicast to the
-// barriers of both; the softmax warps of both announce P on rank 0's barriers (one arrival per
-// warp).  Every wait is bounded as in the one-CTA kernel.
-enum PBar { P_Q = 0, P_KFULL, P_KEMPTY, P_VFULL, P_VEMPTY, P_SFULL, P_PFULL, P_PFULL1, P_OFULL, P_NBAR };
-
-template <int D>
-struct PairCfg {
-    static constexpr int SUB = BM * 128;          // one 64-column block of the Q tile
-    static constexpr int NSUB = D / 64;
-    static constexpr int Q_BYTES = BM * D * 2;
-    static constexpr int KSUB = (BN / 2) * 128;   // one 64-column block of this CTA's 64 keys
-    static constexpr int K_BYTES = (BN / 2) * D * 2;
-    static constexpr int V_BYTES = BN * 64 * 2;   // 128 keys x this CTA's 64 value columns
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + K_BYTES;
-    static constexpr int OFF_BAR = OFF_V + V_BYTES;
-    static constexpr int SMEM_ALLOC = 82 * 1024;  // two CTAs per SM (tensor memory and registers hold two)
-    static constexpr uint32_t TMEM_COLS = 256;
-};
-
-struct PairShared {
-    uint64_t bar[P_NBAR];
-    uint32_t tmem_base;
-    volatile int abort;
-};
-
-template <bool CLUSTER>
-__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, PairShared* sh, const TcParams& p, int role) {
-    auto test = [&] { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (test()) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t n = 1;; ++n) {
-        if (test()) return true;
-        if ((n & 127u) == 0) {
-            if (sh->abort) return false;
-            if ((long long)(globaltimer() - t0) > p.watchdog_ns) {
-                sh->abort = 1;
-                atomicOr(p.err, role);
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void pdrain(uint32_t bar, uint32_t parity, const TcParams& p) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait_cluster(bar, parity))
-        if ((long long)(globaltimer() - t0) > p.watchdog_ns) return;
-}
-
-template <int D>
-__global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_pair_kernel(const __grid_constant__ TcParams p) {
-    using C = PairCfg<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    PairShared* sh = reinterpret_cast<PairShared*>(smem + C::OFF_BAR);
-    const uint32_t s_q = smem_u32(smem + C::OFF_Q);
-    const uint32_t s_k = smem_u32(smem + C::OFF_K);
-    const uint32_t s_v = smem_u32(smem + C::OFF_V);
-    auto bar = [&](int b) { return smem_u32(&sh->bar[b]); };
-    const uint32_t rank = cluster_ctarank();            // 0: issues the MMAs; 1: its peer
-    auto lead_bar = [&](int b) { return mapa_shared(bar(b), 0); };
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    // the pair's two items are adjacent, rank 0's first; both list the same key tiles
-    const int item = p.item_offset + blockIdx.x;
-    const int4 w0 = p.work[2 * item];
-    const int4 w1 = p.work[2 * item + 1];
-    const int bh = w0.x, q_tile = w0.y, kv_begin = w0.z, kv_end = w0.w;
-    const int full_begin = w1.x, full_end = w1.y;
-    const int n_iter = kv_end - kv_begin;
-    const int b = bh / p.Hq, a = bh - b * p.Hq;
-    const int bkv = b * p.Hkv + a / p.group;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < P_NBAR; ++i) mbar_init(bar(i), (i == P_PFULL || i == P_PFULL1) ? 8u : 1u);
-        sh->abort = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0) {
-        tmem_alloc_pair(smem_u32(&sh->tmem_base), C::TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    if (warp == WARP_PRODUCER && lane == 0) {
-        prefetch_tmap(&p.tm_q);
-        prefetch_tmap(&p.tm_kh);
-        prefetch_tmap(&p.tm_v);
-    }
-    tc_fence_before();
-    cluster_sync();  // both CTAs' barriers initialised and their tensor memory allocated
-    tc_fence_after();
-    const uint32_t tmem = sh->tmem_base;
-
-    if (warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ producer (both CTAs)
-        if (lane == 0) {
-            if (rank == 0) mbar_arrive_expect_tx(bar(P_Q), 2 * C::Q_BYTES);
-            for (int s = 0; s < C::NSUB; ++s)
-                tma_load_3d_pair(s_q + s * C::SUB, &p.tm_q, lead_bar(P_Q), s * 64, q_tile * BM, bh);
-            bool ok = true;
-            int it = 0;
-            for (; it < n_iter && ok; ++it) {
-                const int row = (kv_begin + it) * BN;
-                if (it > 0 && !(ok = pwait<true>(bar(P_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
-                if (rank == 0) mbar_arrive_expect_tx(bar(P_KFULL), 2 * C::K_BYTES);
-                for (int s = 0; s < C::NSUB; ++s)
-                    tma_load_3d_pair(s_k + s * C::KSUB, &p.tm_kh, lead_bar(P_KFULL), s * 64, row + (int)rank * (BN / 2),
-                                     bkv);
-                if (it > 0 && !(ok = pwait<true>(bar(P_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
-                if (p.withhold_v) continue;
-                if (rank == 0) mbar_arrive_expect_tx(bar(P_VFULL), 2 * C::V_BYTES);
-                tma_load_3d_pair(s_v, &p.tm_v, lead_bar(P_VFULL), (int)rank * 64, row, bkv);
-            }
-            // every completion multicast to this CTA (the last tile's buffer releases) lands before
-            // its shared memory is given back; and on an abort, the copies in flight
-            if (n_iter > 0) {
-                pdrain(bar(P_KEMPTY), (n_iter - 1) & 1, p);
-                pdrain(bar(P_VEMPTY), (n_iter - 1) & 1, p);
-            }
-            if (sh->abort && rank == 0) {
-                pdrain(bar(P_Q), 0, p);
-                if (it > 0) {
-                    pdrain(bar(P_KFULL), (it - 1) & 1, p);
-                    pdrain(bar(P_VFULL), (it - 1) & 1, p);
-                }
-            }
-        }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer (rank 0 only)
-        if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(2 * BM, BN, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(2 * BM, D, true);
-            const uint32_t t_s = tmem + C::TMEM_COLS * 0, t_o = tmem + 128;
-            int last_bar = -1, last_par = 0;
-            bool ok = pwait<false>(bar(P_Q), 0, sh, p, ERR_MMA);
-            for (int it = 0; it < n_iter && ok; ++it) {
-                if (!(ok = pwait<false>(bar(P_KFULL), it & 1, sh, p, ERR_MMA))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t offq = (k >> 2) * C::SUB + (k & 3) * 32;
-                    const uint32_t offk = (k >> 2) * C::KSUB + (k & 3) * 32;
-                    mma_ss_pair(t_s, sdesc_sw128(s_q + offq, 16, 1024), sdesc_sw128(s_k + offk, 16, 1024), idesc_qk,
-                                k > 0);
-                }
-                mma_commit_pair(bar(P_SFULL), 0x3);
-                mma_commit_pair(bar(P_KEMPTY), 0x3);
-                last_bar = P_KEMPTY; last_par = it & 1;
-                if (!(ok = pwait<true>(bar(P_PFULL), it & 1, sh, p, ERR_MMA))) break;
-                if (!(ok = pwait<false>(bar(P_VFULL), it & 1, sh, p, ERR_MMA))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    if (k == BN / 16 / 2) {  // the second half of P (keys 64-127)
-                        if (!(ok = pwait<true>(bar(P_PFULL1), it & 1, sh, p, ERR_MMA))) break;
-                        tc_fence_after();
-                    }
-                    mma_ts_pair(t_o, t_s + k * 8, sdesc_sw128(s_v + k * 16 * 128, C::SUB, 1024), idesc_pv,
-                                (it > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit_pair(bar(P_OFULL), 0x3);
-                mma_commit_pair(bar(P_VEMPTY), 0x3);
-                last_bar = P_VEMPTY; last_par = it & 1;
-                if (!ok) break;
-            }
-            if (sh->abort && last_bar >= 0) pdrain(bar(last_bar), last_par, p);
-        }
-    } else {
-        // ------------------------------------------------------------ softmax + epilogue (both CTAs)
-        const int r = threadIdx.x;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        const uint32_t t_s = t_lane, t_o = t_lane + 128;
-        const long i = (long)q_tile * BM + r;
-        const bool row_valid = i < p.S;
-        long lo = 0, hi = p.S - 1;
-        if (p.kind == ATTN_MASK_CAUSAL) hi = i;
-        else if (p.kind == ATTN_MASK_CAUSAL_SLIDING) { lo = i - p.window; hi = i; }
-        else if (p.kind == ATTN_MASK_SLIDING) { lo = i - p.window; hi = i + p.window; }
-        if (hi > p.S - 1) hi = p.S - 1;
-        const float sl2 = p.scale_log2;
-        // P is announced on rank 0's barriers: one arrival per warp once its lanes' stores landed
-        auto announce = [&](int which) {
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(lead_bar(which));
-        };
-        float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int it = 0; it < n_iter; ++it) {
-            const int t = kv_begin + it;
-            const bool partial = t < full_begin || t >= full_end;
-            TileMask mk{0, -1, 0u, 0u, 0u, 0u};
-            if (partial) {
-                const long c0 = (long)t * BN;
-                mk.a0 = (int)max(-1L, min((long)BN, lo - c0));
-                mk.a1 = (int)max(-1L, min((long)BN, hi - c0));
-            }
-            const bool upper = __all_sync(0xffffffffu, partial && mk.a0 <= 0);
-            if (partial && !upper) {
-                mk.w0 = interval_word(mk.a0, mk.a1, 0);
-                mk.w1 = interval_word(mk.a0, mk.a1, 1);
-                mk.w2 = interval_word(mk.a0, mk.a1, 2);
-                mk.w3 = interval_word(mk.a0, mk.a1, 3);
-            }
-            if (!__all_sync(0xffffffffu, pwait<true>(bar(P_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            float mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                       : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
-            mx *= sl2;
-            const bool grow = mx > m + RESCALE_THRESHOLD;
-            const float m_new = grow ? mx : m;
-            const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-            auto fix = [&]() {
-                float alpha = 1.f;
-                if (grow) alpha = ex2(m - m_new);
-                const bool fix_o = grow && it > 0 && m != -INFINITY;
-                if (__any_sync(0xffffffffu, fix_o)) {
-                    const float f = fix_o ? alpha : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < D / 16; ++c) {
-                        uint32_t o[16];
-                        tmem_ld16(t_o + c * 16, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                        tmem_st16(t_o + c * 16, o);
-                    }
-                }
-                l *= alpha;
-                m = m_new;
-            };
-            auto rel0 = [&] { announce(P_PFULL); };
-            const float sum = !partial ? tile_exp_store_r<MASK_NONE>(t_s, mk, sl2, ref, fix, rel0)
-                              : upper ? tile_exp_store_r<MASK_UPPER>(t_s, mk, sl2, ref, fix, rel0)
-                                      : tile_exp_store_r<MASK_ANY>(t_s, mk, sl2, ref, fix, rel0);
-            l += sum;
-            announce(P_PFULL1);
-        }
-        // ---- epilogue
-        if (ok) ok = __all_sync(0xffffffffu, pwait<true>(bar(P_OFULL), (n_iter - 1) & 1, sh, p, ERR_SOFTMAX));
-        tc_fence_after();
-        ok = named_bar_and(1, 128, ok);
-        if (ok) {
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            const float lse = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-            uint8_t* stage = smem + C::OFF_Q;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-                const int sub = c >> 1;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = (c & 1) * 4 + q;
-                    uint4* dst = reinterpret_cast<uint4*>(stage + sub * C::SUB + r * 128 + ((chunk ^ (r & 7)) << 4));
-                    *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0 && (long)q_tile * BM < p.S) {  // a padding tile past S stores nothing
-                for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
-                tma_store_commit_and_wait_read();
-            }
-            if (p.lse && row_valid) p.lse[(size_t)bh * p.S + i] = lse;
-        }
-    }
-
-    tc_fence_before();
-    cluster_sync();  // neither CTA gives back its memory while the other may still reach it
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, C::TMEM_COLS);
-    }
-}
-
 template <int D, int BIAS, bool F8 = false, bool LG = false>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
     using C = Cfg<D, BIAS, F8>;
@@ -1379,33 +1072,7 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t launch_pair(const TcParams& p, int n_pairs, cudaStream_t stream) {
-    using C = PairCfg<D>;
-    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_pair_kernel<D>), C::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2u * (unsigned)n_pairs, 1, 1);
-    cfg.blockDim = dim3(NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_fwd_pair_kernel<D>, p);
-}
-
 }  // namespace
-
-cudaError_t launch_tc_forward_pairs(const TcParams& p, int d, int n_pairs, cudaStream_t stream) {
-    if (n_pairs <= 0) return cudaSuccess;
-    if (d != 128 || p.fp8 || p.alibi || p.bias || p.kind == ATTN_MASK_LOCAL_GLOBAL) return cudaErrorInvalidValue;
-    return launch_pair<128>(p, n_pairs, stream);
-}
 
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;

@@ -17,7 +17,6 @@ struct TcParams {
     CUtensorMap tm_k;    // K  [B*Hkv, S, d]
     CUtensorMap tm_v;    // V  [B*Hkv, S, d]
     CUtensorMap tm_o;    // O  [B*Hq,  S, d] (TMA store)
-    CUtensorMap tm_kh;   // K with a 64-row box (the CTA-pair kernel: each CTA loads 64 keys of a tile)
     const int4* work;    // 4 int4 per work item (attn.h schedule layout)
     int item_offset;     // first work item of this launch
     int S, Hq, Hkv, group;
@@ -140,8 +139,6 @@ cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t s
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream);
 
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream);
-// CTA-pair kernel: n_pairs clusters of two CTAs, items 2k (rank 0) and 2k + 1 (rank 1) of p.work
-cudaError_t launch_tc_forward_pairs(const TcParams& p, int d, int n_pairs, cudaStream_t stream);
 cudaError_t launch_f32_forward(const F32Params& p, int d, cudaStream_t stream);
 cudaError_t launch_exp2_selftest(const float* x, float* y, int n, cudaStream_t stream);
 

@@ -185,64 +185,6 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
     return ATTN_OK;
 }
 
-attn_status build_pair_schedule(const ScheduleInput& in, std::vector<int>* items) {
-    if (in.kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
-    Schedule single;
-    attn_status st = build_schedule(in, &single);
-    if (st != ATTN_OK) return st;
-    const int S = in.S, nq = (S + T - 1) / T;
-    // per query tile: the key tiles and the FULL run (the same for every head)
-    struct QT { int kb, ke, fb, fe; };
-    std::vector<QT> qt(nq);
-    for (size_t k = 0; k + ATTN_WORK_INTS <= single.items.size(); k += ATTN_WORK_INTS) {
-        const int* it = &single.items[k];
-        if (it[0] == 0) qt[it[1]] = {it[2], it[3], it[4], it[5]};
-    }
-    const int group = in.Hq / in.Hkv;
-    struct Pair { int bh0, q0, bh1, q1, kb, ke, unit; };
-    std::vector<Pair> pairs;
-    if (group % 2 == 0) {  // two query heads of one kv head, same query tile: the same key tiles
-        for (int b = 0; b < in.B; ++b)
-            for (int g = 0; g < in.Hkv; ++g)
-                for (int q = 0; q < nq; ++q)
-                    for (int k = 0; k < group / 2; ++k) {
-                        const int bh0 = b * in.Hq + g * group + 2 * k;
-                        pairs.push_back({bh0, q, bh0 + 1, q, qt[q].kb, qt[q].ke, b * in.Hkv + g});
-                    }
-    } else {  // two consecutive query tiles of one head (the second past S when nq is odd)
-        for (int bh = 0; bh < in.B * in.Hq; ++bh) {
-            const int b = bh / in.Hq, a = bh % in.Hq;
-            for (int q0 = 0; q0 < nq; q0 += 2) {
-                const int q1 = q0 + 1;
-                int kb = qt[q0].kb, ke = qt[q0].ke;
-                if (q1 < nq) { kb = std::min(kb, qt[q1].kb); ke = std::max(ke, qt[q1].ke); }
-                pairs.push_back({bh, q0, bh, q1, kb, ke, b * in.Hkv + a / group});
-            }
-        }
-    }
-    // longest first (kv-head groups first for long problems, as in build_schedule)
-    const long kv_bytes = 512L * S;
-    int g_kv = (int)std::max(1L, std::min((long)in.B * in.Hkv, (32L << 20) / kv_bytes));
-    if ((long)g_kv * group * nq < 4096) g_kv = in.B * in.Hkv;
-    std::stable_sort(pairs.begin(), pairs.end(), [&](const Pair& x, const Pair& y) {
-        const int gx = x.unit / g_kv, gy = y.unit / g_kv;
-        if (gx != gy) return gx < gy;
-        if (x.ke - x.kb != y.ke - y.kb) return x.ke - x.kb > y.ke - y.kb;
-        return std::max(x.q0, x.q1) > std::max(y.q0, y.q1);
-    });
-    items->clear();
-    items->reserve(pairs.size() * 2 * ATTN_WORK_INTS);
-    for (const Pair& pr : pairs) {
-        for (int r = 0; r < 2; ++r) {
-            const int bh = r ? pr.bh1 : pr.bh0, q = r ? pr.q1 : pr.q0;
-            const int fb = q < nq ? qt[q].fb : pr.kb, fe = q < nq ? qt[q].fe : pr.kb;
-            const int it[ATTN_WORK_INTS] = {bh, q, pr.kb, pr.ke, fb, fe, 0, 0};
-            items->insert(items->end(), it, it + ATTN_WORK_INTS);
-        }
-    }
-    return ATTN_OK;
-}
-
 attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* items) {
     if (kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
     const long w = window;

@@ -38,13 +38,6 @@ struct Schedule {
 // tile's FULL key tiles are not contiguous (cannot happen for the five kinds).
 attn_status build_schedule(const ScheduleInput& in, Schedule* out);
 
-// Items of the CTA-pair forward kernel (interval kinds): two adjacent items per pair, rank 0 first,
-// with the same kv head and the same key tiles [kv_begin, kv_end) (the union of the two query tiles'
-// bands) and each CTA's own FULL run.  Pairs are two query heads of one kv head at one query tile
-// when Hq / Hkv is even, else two consecutive query tiles of one head (the second may be the padding
-// tile ceil(S / 128), which stores nothing).  Ordered as build_schedule orders its items.
-attn_status build_pair_schedule(const ScheduleInput& in, std::vector<int>* items);
-
 // Backward (dK, dV): one item per key tile, listing the query tiles whose rows may
 // see one of its keys ("transposed" band), for the interval kinds (not LOCAL_GLOBAL).
 // Item ints: [kv_tile, q_begin, q_end, full_begin, full_end, 0, 0, 0]; query tiles in
