@@ -548,10 +548,11 @@ def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int 
                       f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
 
 
-def _bwd_config(w, useful, world: int = 1):
+def _bwd_config(w, useful, world: int = 1, alibi: bool = False):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
             "mask": wl.MASK_NAMES[w.kind], "window": w.window, "pass": "backward (dQ, dK, dV)",
             "useful_gflop_per_step": useful / 1e9, "flops_per_pair": f"10 d (2.5 x the forward's 4 d)",
+            "score_bias": "alibi, slopes 2^(-8(a+1)/H)" if alibi else "none",
             "l2": "flushed before every GPU step (256 MiB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -571,7 +572,7 @@ def run_reference_backward(args, w):
     line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _bwd_config(w, wl.backward_flops(w), max(1, args.gpus)),
+            "config": _bwd_config(w, wl.backward_flops(w), max(1, args.gpus), args.alibi),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -595,6 +596,8 @@ def run_ours_backward(args, w):
     dOc = wl.make_grad_output(w)
     Q, K, V, dO = (t.to(dev) for t in (Qc, Kc, Vc, dOc))
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
+    if args.alibi:
+        plan.set_alibi(wl.alibi_slopes(w.Hq))
     O, LSE = plan(Q, K, V)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -671,7 +674,7 @@ def run_ours_backward(args, w):
     line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _bwd_config(w, useful, world),
+            "config": _bwd_config(w, useful, world, args.alibi),
             "roofline": roofline, "gpu_launches": 3 * args.steps, "wall_s_timed_region": wall}
     if e2e:
         line["e2e"] = e2e
@@ -899,8 +902,8 @@ def main():
     if args.bias and (args.fp8 or args.alibi or args.backward or args.workload not in wl.BY_NAME):
         ap.error("--bias takes a bf16 prefill workload without --fp8 / --alibi / --backward")
     if args.backward:
-        if args.workload not in wl.BY_NAME or args.fp8 or args.alibi:
-            ap.error("--backward takes a bf16 prefill workload without --fp8 / --alibi")
+        if args.workload not in wl.BY_NAME or args.fp8:
+            ap.error("--backward takes a bf16 prefill workload without --fp8")
         w = wl.BY_NAME[args.workload]
         return run_reference_backward(args, w) if args.impl == "reference" else run_ours_backward(args, w)
     if args.workload in wl.DECODE_BY_NAME:

@@ -31,8 +31,10 @@ def _plan(w):
     return tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
 
 
-def _run(w, Q, K, V, dO, plan=None):
+def _run(w, Q, K, V, dO, plan=None, alibi=None):
     plan = plan or _plan(w)
+    if alibi is not None:
+        plan.set_alibi(alibi)
     O, LSE = plan(Q, K, V)
     dQ, dK, dV = (torch.full_like(t, float("nan")) for t in (Q, K, V))
     plan.backward(Q, K, V, O, LSE, dO, dQ, dK, dV)
@@ -58,12 +60,12 @@ def _cmp(name, got, ref):
     return rel, mx
 
 
-def _check(w):
+def _check(w, alibi=None):
     Qc, Kc, Vc = wl.make_inputs(w)
     dOc = wl.make_grad_output(w)
-    dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda())
+    dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda(), alibi=alibi)
     ref = oracle.backward(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), dOc.float().numpy(), w.scale,
-                          w.kind, w.window)
+                          w.kind, w.window, alibi=alibi)
     one_key = w.S == 1 or (w.window == 0 and w.kind in (wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING))
     if one_key:
         # every row sees one key (S = 1, or a window of 0): the softmax is the constant 1, so the
@@ -120,12 +122,42 @@ def test_backward_unsupported_configurations():
     O, LSE = plan(Q, K, V)
     with pytest.raises(tsa.AttnError):
         plan.backward(Q, K, V, O, LSE, O)
-    plan2 = tsa.Attention(1, 2, 2, 256, 128, kind=wl.MASK_CAUSAL)
-    plan2.set_alibi(wl.alibi_slopes(2))
-    O, LSE = plan2(Q, K, V)
-    with pytest.raises(tsa.AttnError):
-        plan2.backward(Q, K, V, O, LSE, O)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("S", [1, 129, 300])
+@pytest.mark.parametrize("kind", KINDS)
+def test_backward_alibi_kinds(kind, S):
+    """ALiBi -m_a |i - j| in the forward: the backward recomputes P with it (symmetric kinds take
+    the absolute value, the causal kinds see j <= i only); every gradient against the oracle."""
+    _check(small("ba", 1, 4, 2, S, 128, "bf16", kind, window=37), alibi=wl.alibi_slopes(4))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_alibi_gqa_steep_slopes(d):
+    """Steep slopes (m_a up to 1): the bias dominates the scores and P is concentrated near the
+    diagonal; GQA sums dK and dV over the group."""
+    w = small("bas", 2, 8, 2, 400, d, "bf16", wl.MASK_CAUSAL)
+    _check(w, alibi=[2.0 ** (-a / 2.0) for a in range(8)])
+
+
+def test_backward_alibi_full_size_causal_mha_4k():
+    """The 4K causal workload with geometric ALiBi slopes: every gradient element against the
+    oracle (one call per (batch, head) slice, exact for MHA)."""
+    w = wl.CAUSAL_MHA_4K
+    slopes = wl.alibi_slopes(w.Hq)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    dOc = wl.make_grad_output(w)
+    dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda(), alibi=slopes)
+    refs = [np.empty(t.shape, dtype=np.float64) for t in (dQ, dK, dV)]
+    for b in range(w.B):
+        for a in range(w.Hq):
+            sl = lambda t: t[b:b + 1, a:a + 1].float().numpy()
+            out = oracle.backward(sl(Qc), sl(Kc), sl(Vc), sl(dOc), w.scale, w.kind, alibi=[slopes[a]])
+            for r, x in zip(refs, out):
+                r[b:b + 1, a:a + 1] = x
+    for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        _cmp(f"{n} + ALiBi (every element)", g, r)
 
 
 def test_backward_full_size_causal_mha_4k():

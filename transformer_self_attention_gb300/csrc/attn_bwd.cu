@@ -225,8 +225,12 @@ struct ColVec {  // one value per column, from a 16-byte aligned shared-memory v
     }
 };
 
-template <bool MASKED, bool STORE_P, class NL>
-__device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, float (&pv)[64]) {
+// With AL, the ALiBi bias -m_a |i - j| joins the exponent, in log2 units: -mL |base - c| for in-tile
+// column c (mL = m_a log2 e; base = the thread's own position minus the first position of the
+// tile's columns, for query rows and key columns alike).
+template <bool MASKED, bool STORE_P, bool AL, class NL>
+__device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, float mL, float base,
+                                         float (&pv)[64]) {
     const float2 sl = make_float2(sl2, sl2);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
@@ -241,9 +245,14 @@ __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, 
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int k = 2 * (e + u);
+                float2 add = u ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
+                if (AL) {
+                    add.x = fmaf(-mL, fabsf(base - (float)(cb + k)), add.x);
+                    add.y = fmaf(-mL, fabsf(base - (float)(cb + k + 1)), add.y);
+                }
                 const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cb + k, a0, a1),
                                                         masked<MASKED>(s[k + 1], cb + k + 1, a0, a1)),
-                                            sl, u ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y));
+                                            sl, add);
                 pv[ch * 32 + k] = ex2(x.x);
                 pv[ch * 32 + k + 1] = ex2(x.y);
                 if (STORE_P) pk[e + u] = pack_bf16x2(pv[ch * 32 + k], pv[ch * 32 + k + 1]);
@@ -319,7 +328,7 @@ struct BwdShared {
 __device__ __forceinline__ uint32_t region_s(int n) { return (uint32_t)((2 * n) % 3) * 128u; }
 __device__ __forceinline__ uint32_t region_dp(int n) { return (uint32_t)((2 * n + 1) % 3) * 128u; }
 
-template <int D>
+template <int D, bool AL>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -463,15 +472,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         long lo, hi;
         row_band(p.kind, p.window, p.S, i, &lo, &hi);
+        const float mL = AL ? p.alibi[a] * LOG2E : 0.f;  // ALiBi slope of this query head, log2 units
         float pv[64];
         for (int it = 0; it < n_iter; ++it) {
             const int t = kv_begin + it;
             int a0, a1;
             tile_interval(lo, hi, (long)t * BT, &a0, &a1);
+            const float base = (float)(i - (long)t * BT);
             wait_bounded(bar(Q_SFULL + (it & 1)), (it >> 1) & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            if (t < full_begin || t >= full_end) exp_pass<true, false>(t_lane + region_s(it), wg, sl2, nl, a0, a1, pv);
-            else exp_pass<false, false>(t_lane + region_s(it), wg, sl2, nl, a0, a1, pv);
+            if (t < full_begin || t >= full_end)
+                exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+            else
+                exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
             wait_bounded(bar(Q_DPFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
             ds_pass(t_lane + region_dp(it), wg, nd, pv);
@@ -532,7 +545,7 @@ enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMP
              KV_HDONE = KV_PDONE + 2, KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
 static_assert(KV_NBAR <= 24, "barrier slots");
 
-template <int D>
+template <int D, bool AL>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = KvCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -682,11 +695,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
             int a0, a1;
             tile_interval(ilo, ihi, (long)qt * BT, &a0, &a1);
             const uint32_t vec = s_vec + st * 1024;  // -LSE log2 e of the tile's 128 query rows, then -D
+            // ALiBi: the slope of this iteration's query head; |i - j| = |c - (j - first row of the tile)|
+            const float mL = AL ? p.alibi[iter_head(it) - b * p.Hq] * LOG2E : 0.f;
+            const float base = (float)(j - (long)qt * BT);
             wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
             wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            if (qt < full_begin || qt >= full_end) exp_pass<true, true>(t_s, wg, sl2, ColVec{vec}, a0, a1, pv);
-            else exp_pass<false, true>(t_s, wg, sl2, ColVec{vec}, a0, a1, pv);
+            if (qt < full_begin || qt >= full_end)
+                exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+            else
+                exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(KV_PDONE + wg));
@@ -737,34 +755,34 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int D, bool AL>
+cudaError_t launch_dq(const BwdParams& p, int n_items, cudaStream_t stream) {
+    cudaError_t e = configure(attn_bwd_dq_kernel<D, AL>, DqCfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dq_kernel<D, AL><<<n_items, NTHREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, bool AL>
+cudaError_t launch_dkdv(const BwdParams& p, int n_ctas, cudaStream_t stream) {
+    cudaError_t e = configure(attn_bwd_dkdv_kernel<D, AL>, KvCfg<D>::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    attn_bwd_dkdv_kernel<D, AL><<<n_ctas, NTHREADS, KvCfg<D>::SMEM_ALLOC, stream>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
-    cudaError_t e = cudaSuccess;
-    if (d == 128) {
-        if ((e = configure(attn_bwd_dq_kernel<128>, DqCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
-        attn_bwd_dq_kernel<128><<<n_items, NTHREADS, DqCfg<128>::SMEM_ALLOC, stream>>>(p);
-    } else if (d == 64) {
-        if ((e = configure(attn_bwd_dq_kernel<64>, DqCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
-        attn_bwd_dq_kernel<64><<<n_items, NTHREADS, DqCfg<64>::SMEM_ALLOC, stream>>>(p);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (d == 128) return p.alibi ? launch_dq<128, true>(p, n_items, stream) : launch_dq<128, false>(p, n_items, stream);
+    if (d == 64) return p.alibi ? launch_dq<64, true>(p, n_items, stream) : launch_dq<64, false>(p, n_items, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream) {
     if (n_ctas <= 0) return cudaSuccess;
-    cudaError_t e = cudaSuccess;
-    if (d == 128) {
-        if ((e = configure(attn_bwd_dkdv_kernel<128>, KvCfg<128>::SMEM_ALLOC)) != cudaSuccess) return e;
-        attn_bwd_dkdv_kernel<128><<<n_ctas, NTHREADS, KvCfg<128>::SMEM_ALLOC, stream>>>(p);
-    } else if (d == 64) {
-        if ((e = configure(attn_bwd_dkdv_kernel<64>, KvCfg<64>::SMEM_ALLOC)) != cudaSuccess) return e;
-        attn_bwd_dkdv_kernel<64><<<n_ctas, NTHREADS, KvCfg<64>::SMEM_ALLOC, stream>>>(p);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (d == 128) return p.alibi ? launch_dkdv<128, true>(p, n_ctas, stream) : launch_dkdv<128, false>(p, n_ctas, stream);
+    if (d == 64) return p.alibi ? launch_dkdv<64, true>(p, n_ctas, stream) : launch_dkdv<64, false>(p, n_ctas, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

@@ -125,6 +125,7 @@ struct BwdParams {
     float scale;
     const float* nlse2;   // [B*Hq, S_pad]: -LSE * log2(e); -inf past S
     const float* nd;      // [B*Hq, S_pad]: -D = -dO . O; 0 past S
+    const float* alibi;   // [Hq] ALiBi slopes of the forward (device), or null
     int* err;
     long long watchdog_ns;
 };
