@@ -43,6 +43,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
@@ -178,26 +180,39 @@ __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask&
     return tile_allowed(c, mk) ? __uint_as_float(raw) : -INFINITY;
 }
 
+// Classes of the two 64-column halves of a partial tile, decided warp-uniformly (2 bits per half):
+// every column allowed for every row of the warp (the half needs no mask), none allowed (the half
+// is skipped: no loads, its P is zero), or mixed (the tile's mask form).
+enum { HALF_FREE = 0, HALF_MASKED = 1, HALF_EMPTY = 2 };
+constexpr uint32_t HALVES_MASKED = HALF_MASKED | (HALF_MASKED << 2);
+
 // Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
 // three-input max instructions, eight independent chains.
 template <int MASKED>
-__device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
+__device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk, uint32_t halves = HALVES_MASKED) {
     float m8[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+        const uint32_t hc = MASKED == MASK_NONE ? (uint32_t)HALF_FREE : (halves >> (2 * h)) & 3u;
+        if (hc == HALF_EMPTY) continue;
         uint32_t r0[32], r1[32];
         tmem_ld32(t_s + h * 64, r0);
         tmem_ld32(t_s + h * 64 + 32, r1);
         tmem_wait_ld();
+        auto body = [&](auto form) {
+            constexpr int F = decltype(form)::value;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const int k = (e >> 1) & 7;
-            m8[k] = fmax3(m8[k], tile_score<MASKED>(r0[e], h * 64 + e, mk), tile_score<MASKED>(r0[e + 1], h * 64 + e + 1, mk));
-            m8[k] = fmax3(m8[k], tile_score<MASKED>(r1[e], h * 64 + 32 + e, mk),
-                          tile_score<MASKED>(r1[e + 1], h * 64 + 33 + e, mk));
-        }
+            for (int e = 0; e < 32; e += 2) {
+                const int k = (e >> 1) & 7;
+                m8[k] = fmax3(m8[k], tile_score<F>(r0[e], h * 64 + e, mk), tile_score<F>(r0[e + 1], h * 64 + e + 1, mk));
+                m8[k] = fmax3(m8[k], tile_score<F>(r1[e], h * 64 + 32 + e, mk),
+                              tile_score<F>(r1[e + 1], h * 64 + 33 + e, mk));
+            }
+        };
+        if (hc == HALF_FREE) body(std::integral_constant<int, MASK_NONE>{});
+        else body(std::integral_constant<int, MASKED>{});
     }
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
@@ -219,28 +234,40 @@ __device__ __forceinline__ void release_first_half(uint32_t bar_half) {
 // it is off the path from S to the first exponentials, and O is rescaled before O += P V starts.
 template <int MASKED, typename FixO>
 __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
-                                               uint32_t bar_half, FixO&& fix) {
+                                               uint32_t bar_half, FixO&& fix, uint32_t halves = HALVES_MASKED) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        uint32_t r0[32], r1[32], pk[32];
-        tmem_ld32(t_s + h * 64, r0);
-        tmem_ld32(t_s + h * 64 + 32, r1);
-        tmem_wait_ld();
+        const uint32_t hc = MASKED == MASK_NONE ? (uint32_t)HALF_FREE : (halves >> (2 * h)) & 3u;
+        uint32_t pk[32];
+        if (hc == HALF_EMPTY) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float2 x01 = __ffma2_rn(make_float2(tile_score<MASKED>(r0[2 * e], h * 64 + 2 * e, mk),
-                                                      tile_score<MASKED>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk)),
-                                          sl2x2, nref);
-            const float2 x23 = __ffma2_rn(make_float2(tile_score<MASKED>(r1[2 * e], h * 64 + 32 + 2 * e, mk),
-                                                      tile_score<MASKED>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk)),
-                                          sl2x2, nref);
-            const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
-            acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
-            acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
-            pk[e] = pack_bf16x2(p0, p1);
-            pk[16 + e] = pack_bf16x2(p2, p3);
+            for (int e = 0; e < 32; ++e) pk[e] = 0u;  // no key allowed in this half: P = 0
+        } else {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(t_s + h * 64, r0);
+            tmem_ld32(t_s + h * 64 + 32, r1);
+            tmem_wait_ld();
+            auto body = [&](auto form) {
+                constexpr int F = decltype(form)::value;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float2 x01 = __ffma2_rn(make_float2(tile_score<F>(r0[2 * e], h * 64 + 2 * e, mk),
+                                                              tile_score<F>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk)),
+                                                  sl2x2, nref);
+                    const float2 x23 = __ffma2_rn(make_float2(tile_score<F>(r1[2 * e], h * 64 + 32 + 2 * e, mk),
+                                                              tile_score<F>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk)),
+                                                  sl2x2, nref);
+                    const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+                    acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+                    acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
+                    pk[e] = pack_bf16x2(p0, p1);
+                    pk[16 + e] = pack_bf16x2(p2, p3);
+                }
+            };
+            if (hc == HALF_FREE) body(std::integral_constant<int, MASK_NONE>{});
+            else body(std::integral_constant<int, MASKED>{});
         }
         tmem_st32(t_s + h * 32, pk);
         if (h == 0) {
@@ -881,6 +908,30 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if (lg && bits) {
                 mk.w0 |= g4.x; mk.w1 |= g4.y; mk.w2 |= g4.z; mk.w3 |= g4.w;
             }
+            // classes of the two 64-column halves (bf16 path): a half with every column allowed for
+            // the whole warp takes no mask, a half with none is skipped
+            uint32_t halves = HALVES_MASKED;
+            if constexpr (BIAS == BIAS_NONE && !F8) {
+                if (partial && !gathered) {
+                    halves = 0u;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        bool all_in, none_in;
+                        if (upper) {
+                            all_in = mk.a1 >= 64 * h + 63;
+                            none_in = mk.a1 < 64 * h;
+                        } else {
+                            const uint32_t lo_w = h ? mk.w2 : mk.w0, hi_w = h ? mk.w3 : mk.w1;
+                            all_in = (lo_w & hi_w) == 0xffffffffu;
+                            none_in = (lo_w | hi_w) == 0u;
+                        }
+                        const uint32_t c = __all_sync(0xffffffffu, all_in)    ? (uint32_t)HALF_FREE
+                                           : __all_sync(0xffffffffu, none_in) ? (uint32_t)HALF_EMPTY
+                                                                               : (uint32_t)HALF_MASKED;
+                        halves |= c << (2 * h);
+                    }
+                }
+            }
             // ---- pass 1: row max of the (masked) scores, in log2 units
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
@@ -899,10 +950,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
                     else
                         mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk, halves)
+                                     : tile_row_max<MASK_ANY>(t_s, mk, halves);
                 } else {
                     mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk, halves) : tile_row_max<MASK_ANY>(t_s, mk, halves);
                 }
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
@@ -961,8 +1013,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, sl2, r_eff, bar(B_PFULL), fix);
                 else
                     sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                          : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                                  : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
+                          : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix, halves)
+                                  : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix, halves);
             }
             l += sum;
             tmem_wait_st();
