@@ -43,8 +43,6 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include <type_traits>
-
 #include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
@@ -67,7 +65,7 @@ enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 // causal kinds, added by the tensor core (see the MMA role); 3 a given bias matrix b_ij.
 enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2, BIAS_MATRIX = 3 };
 
-template <int D, int BIAS = BIAS_NONE, bool F8 = false, bool LG = false>
+template <int D, int BIAS = BIAS_NONE, bool F8 = false>
 struct Cfg {
     static constexpr int EB = F8 ? 1 : 2;         // bytes per element (E4M3 or bf16)
     static constexpr int SUB = BM * 128;          // bytes of one 128-row x 128-byte swizzled block
@@ -77,12 +75,7 @@ struct Cfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + TILE_BYTES;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
-    // local + global at d = 64: a key and a value tile of their own for the gathered global keys, so that
-    // they are loaded while the band tiles stream through the K and V tiles (room for two CTAs per SM)
-    static constexpr bool GATHER_OWN = LG && D == 64;
-    static constexpr int OFF_GK = OFF_V + TILE_BYTES;
-    static constexpr int OFF_GV = OFF_GK + (GATHER_OWN ? TILE_BYTES : 0);
-    static constexpr int OFF_BAR = OFF_GV + (GATHER_OWN ? TILE_BYTES : 0);
+    static constexpr int OFF_BAR = OFF_V + TILE_BYTES;
     // BIAS_ALIBI_MMA: a ones block and a bias block, each 128 rows x 16 bf16 (K-major, no swizzle)
     static constexpr int OFF_BA = OFF_BAR + 1024;
     static constexpr int OFF_BB = OFF_BA + 4096;
@@ -95,8 +88,7 @@ struct Cfg {
 };
 
 // B_PFULL / B_PFULL1: the first / second half of P (keys 0-63 / 64-127) is in tensor memory.
-// B_GFULL: the gathered global keys and values are in their own tiles (Cfg::GATHER_OWN).
-enum Bar { B_Q = 0, B_KFULL, B_KEMPTY, B_VFULL, B_VEMPTY, B_SFULL, B_PFULL, B_PFULL1, B_OFULL, B_GFULL, NBAR };
+enum Bar { B_Q = 0, B_KFULL, B_KEMPTY, B_VFULL, B_VEMPTY, B_SFULL, B_PFULL, B_PFULL1, B_OFULL, NBAR };
 
 struct Shared {  // small control block after the tiles
     uint64_t bar[NBAR];
@@ -186,39 +178,26 @@ __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask&
     return tile_allowed(c, mk) ? __uint_as_float(raw) : -INFINITY;
 }
 
-// Classes of the two 64-column halves of a partial tile, decided warp-uniformly (2 bits per half):
-// every column allowed for every row of the warp (the half needs no mask), none allowed (the half
-// is skipped: no loads, its P is zero), or mixed (the tile's mask form).
-enum { HALF_FREE = 0, HALF_MASKED = 1, HALF_EMPTY = 2 };
-constexpr uint32_t HALVES_MASKED = HALF_MASKED | (HALF_MASKED << 2);
-
 // Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
 // three-input max instructions, eight independent chains.
 template <int MASKED>
-__device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk, uint32_t halves = HALVES_MASKED) {
+__device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
     float m8[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const uint32_t hc = MASKED == MASK_NONE ? (uint32_t)HALF_FREE : (halves >> (2 * h)) & 3u;
-        if (hc == HALF_EMPTY) continue;
         uint32_t r0[32], r1[32];
         tmem_ld32(t_s + h * 64, r0);
         tmem_ld32(t_s + h * 64 + 32, r1);
         tmem_wait_ld();
-        auto body = [&](auto form) {
-            constexpr int F = decltype(form)::value;
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                const int k = (e >> 1) & 7;
-                m8[k] = fmax3(m8[k], tile_score<F>(r0[e], h * 64 + e, mk), tile_score<F>(r0[e + 1], h * 64 + e + 1, mk));
-                m8[k] = fmax3(m8[k], tile_score<F>(r1[e], h * 64 + 32 + e, mk),
-                              tile_score<F>(r1[e + 1], h * 64 + 33 + e, mk));
-            }
-        };
-        if (hc == HALF_FREE) body(std::integral_constant<int, MASK_NONE>{});
-        else body(std::integral_constant<int, MASKED>{});
+        for (int e = 0; e < 32; e += 2) {
+            const int k = (e >> 1) & 7;
+            m8[k] = fmax3(m8[k], tile_score<MASKED>(r0[e], h * 64 + e, mk), tile_score<MASKED>(r0[e + 1], h * 64 + e + 1, mk));
+            m8[k] = fmax3(m8[k], tile_score<MASKED>(r1[e], h * 64 + 32 + e, mk),
+                          tile_score<MASKED>(r1[e + 1], h * 64 + 33 + e, mk));
+        }
     }
     return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
 }
@@ -240,40 +219,28 @@ __device__ __forceinline__ void release_first_half(uint32_t bar_half) {
 // it is off the path from S to the first exponentials, and O is rescaled before O += P V starts.
 template <int MASKED, typename FixO>
 __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk, float sl2, float ref,
-                                               uint32_t bar_half, FixO&& fix, uint32_t halves = HALVES_MASKED) {
+                                               uint32_t bar_half, FixO&& fix) {
     const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const uint32_t hc = MASKED == MASK_NONE ? (uint32_t)HALF_FREE : (halves >> (2 * h)) & 3u;
-        uint32_t pk[32];
-        if (hc == HALF_EMPTY) {
+        uint32_t r0[32], r1[32], pk[32];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) pk[e] = 0u;  // no key allowed in this half: P = 0
-        } else {
-            uint32_t r0[32], r1[32];
-            tmem_ld32(t_s + h * 64, r0);
-            tmem_ld32(t_s + h * 64 + 32, r1);
-            tmem_wait_ld();
-            auto body = [&](auto form) {
-                constexpr int F = decltype(form)::value;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 x01 = __ffma2_rn(make_float2(tile_score<F>(r0[2 * e], h * 64 + 2 * e, mk),
-                                                              tile_score<F>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk)),
-                                                  sl2x2, nref);
-                    const float2 x23 = __ffma2_rn(make_float2(tile_score<F>(r1[2 * e], h * 64 + 32 + 2 * e, mk),
-                                                              tile_score<F>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk)),
-                                                  sl2x2, nref);
-                    const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
-                    acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
-                    acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
-                    pk[e] = pack_bf16x2(p0, p1);
-                    pk[16 + e] = pack_bf16x2(p2, p3);
-                }
-            };
-            if (hc == HALF_FREE) body(std::integral_constant<int, MASK_NONE>{});
-            else body(std::integral_constant<int, MASKED>{});
+        for (int e = 0; e < 16; ++e) {
+            const float2 x01 = __ffma2_rn(make_float2(tile_score<MASKED>(r0[2 * e], h * 64 + 2 * e, mk),
+                                                      tile_score<MASKED>(r0[2 * e + 1], h * 64 + 2 * e + 1, mk)),
+                                          sl2x2, nref);
+            const float2 x23 = __ffma2_rn(make_float2(tile_score<MASKED>(r1[2 * e], h * 64 + 32 + 2 * e, mk),
+                                                      tile_score<MASKED>(r1[2 * e + 1], h * 64 + 33 + 2 * e, mk)),
+                                          sl2x2, nref);
+            const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+            acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+            acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
+            pk[e] = pack_bf16x2(p0, p1);
+            pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
         if (h == 0) {
@@ -580,7 +547,7 @@ __device__ __forceinline__ void merge_global_row(const TcParams& p, size_t slot0
 
 template <int D, int BIAS, bool F8, bool LG>
 __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<D, BIAS, F8, LG>;
+    using C = Cfg<D, BIAS, F8>;
     constexpr bool ALIBI = BIAS == BIAS_ALIBI_ELEM;  // the per-element bias passes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -658,11 +625,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     const int g_lo = gs.x, g_hi = gs.y;
     const int n_out = g_lo + (p.n_global - g_hi);
     auto gathered_cols = [&](int it) { return min(BN, n_out - it * BN); };
-    // one gathered tile in its own K and V tiles: iteration 0 reads them, and the band tiles' copies (iterations
-    // 1 .. n_band) count their phases from 0 in the K and V tiles
-    const bool own_g = C::GATHER_OWN && n_gat == 1;
-    const int ph0 = own_g ? 1 : 0;  // phase of K / V tile copies = iteration - ph0
-    const uint32_t s_gk = smem_u32(smem + C::OFF_GK), s_gv = smem_u32(smem + C::OFF_GV);
     auto outside_key = [&](int e) -> long { return __ldg(p.globals + (e < g_lo ? e : g_hi + (e - g_lo))); };
 
     if (LG && warp == WARP_PRODUCER) {
@@ -685,17 +647,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         }
         int k_loaded = 0, v_loaded = 0;
         bool ok = true;
-        for (int it = ph0; it < n_iter && ok; ++it) {
-            const int bp = it - ph0;  // phase of this iteration's K / V tile copies
+        for (int it = 0; it < n_iter && ok; ++it) {
             const bool in_band = it >= n_gat;
             const int row = in_band ? band_tile(it - n_gat) * BN : 0;
             // gathered tiles: the outside keys it * BN + r, r < ncols, padded with zero rows
             const int gcols = in_band ? 0 : gathered_cols(it);
             const int grows_pad = (gcols + 31) & ~31;
             auto gpos = [&](int r) -> long { return r < gcols ? outside_key(it * BN + r) : -1L; };
-            if (bp > 0) {
+            if (it > 0) {
                 bool w = true;
-                if (lane == 0) w = wait_bounded(bar(B_KEMPTY), (bp - 1) & 1, sh, p, ERR_PRODUCER);
+                if (lane == 0) w = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
                 if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
             }
             if (in_band) {
@@ -710,9 +671,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 if (lane == 0) mbar_arrive(bar(B_KFULL));
             }
             ++k_loaded;
-            if (bp > 0) {
+            if (it > 0) {
                 bool w = true;
-                if (lane == 0) w = wait_bounded(bar(B_VEMPTY), (bp - 1) & 1, sh, p, ERR_PRODUCER);
+                if (lane == 0) w = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
                 if (!(ok = __shfl_sync(0xffffffffu, w, 0))) break;
             }
             if (p.withhold_v) continue;
@@ -728,17 +689,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 if (lane == 0) mbar_arrive(bar(B_VFULL));
             }
             ++v_loaded;
-            if (own_g && bp == 0) {
-                // the gathered global keys and values into their own tiles, while the first band tile's
-                // copies are in flight; iteration 0 of the MMA and softmax roles uses them
-                const int gc = gathered_cols(0), gpad = (gc + 31) & ~31;
-                auto gpos0 = [&](int r) -> long { return r < gc ? outside_key(r) : -1L; };
-                gather_rows<D>(smem + C::OFF_GK, p.k + (size_t)bkv * p.S * D, gpad, gpos0, lane);
-                gather_rows<D>(smem + C::OFF_GV, p.v + (size_t)bkv * p.S * D, gpad, gpos0, lane);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_GFULL));
-            }
         }
         if (lane == 0 && sh->abort) {  // let the copies this warp issued land before the CTA exits
             drain_wait(bar(B_Q), 0, p);
@@ -789,13 +739,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             int last_bar = -1, last_par = 0;
             bool ok = wait_bounded(bar(B_Q), 0, sh, p, ERR_MMA);
             for (int it = 0; it < n_iter && ok; ++it) {
-                // the gathered tile in its own K and V tiles (iteration 0), or the phase of the K / V tile copies
-                const bool own = own_g && it == 0;
-                const int bp = it - ph0;
-                if (!(ok = own ? wait_bounded(bar(B_GFULL), 0, sh, p, ERR_MMA)
-                               : wait_bounded(bar(B_KFULL), bp & 1, sh, p, ERR_MMA)))
-                    break;
-                const uint32_t kt = own ? s_gk : s_k, vt = own ? s_gv : s_v;
+                if (!(ok = wait_bounded(bar(B_KFULL), it & 1, sh, p, ERR_MMA))) break;
                 // S/P share tensor columns.  No wait for PV(it-1) here: the MMAs one thread issues
                 // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
@@ -807,27 +751,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 for (int k = 0; k < D / KS; ++k) {
                     const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
                     if constexpr (F8)
-                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(kt + off, 16, 1024), idesc_s,
+                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
                                   k > 0);
                     else
-                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(kt + off, 16, 1024), idesc_s,
+                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
                                k > 0);
                 }
                 if constexpr (BIAS == BIAS_ALIBI_MMA)
                     mma_ss(t_s, sdesc_plain(smem_u32(smem + C::OFF_BA), 128, 256),
                            sdesc_plain(smem_u32(smem + C::OFF_BB), 128, 256), idesc_qk, 1u);
                 mma_commit(bar(B_SFULL));
-                if (own) {
-                    last_bar = B_SFULL; last_par = it & 1;
-                } else {
-                    mma_commit(bar(B_KEMPTY));
-                    last_bar = B_KEMPTY; last_par = bp & 1;
-                }
+                mma_commit(bar(B_KEMPTY));
+                last_bar = B_KEMPTY; last_par = it & 1;
                 if (!(ok = spin_bounded(bar(B_PFULL), it & 1, sh, p, ERR_MMA))) break;
                 // a gathered tile's P is announced whole: wait for both arrivals before its products,
                 // so that QK(it+1) is issued only after every softmax thread is done with tile it
                 if (narrow && !(ok = spin_bounded(bar(B_PFULL1), it & 1, sh, p, ERR_MMA))) break;
-                if (!own && !(ok = wait_bounded(bar(B_VFULL), bp & 1, sh, p, ERR_MMA))) break;
+                if (!(ok = wait_bounded(bar(B_VFULL), it & 1, sh, p, ERR_MMA))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / KS; ++k) {
@@ -839,10 +779,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     // P: KS keys = 8 tensor-memory columns (2 bf16 or 4 E4M3 per column);
                     // V: KS key rows of 128 B each (MN-major: d runs along the row)
                     if constexpr (F8)
-                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(vt + k * KS * 128, C::SUB, 1024), idesc_pv,
+                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
                                   (it > 0 || k > 0) ? 1u : 0u);
                     else
-                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(vt + k * KS * 128, C::SUB, 1024), idesc_pv,
+                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
                                (it > 0 || k > 0) ? 1u : 0u);
                 }
                 if (!ok) {  // half of this PV was issued: track it so the drain below covers it
@@ -851,12 +791,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     break;
                 }
                 mma_commit(bar(B_OFULL));
-                if (own) {
-                    last_bar = B_OFULL; last_par = it & 1;
-                } else {
-                    mma_commit(bar(B_VEMPTY));
-                    last_bar = B_VEMPTY; last_par = bp & 1;
-                }
+                mma_commit(bar(B_VEMPTY));
+                last_bar = B_VEMPTY; last_par = it & 1;
             }
             if (sh->abort && last_bar >= 0) drain_wait(bar(last_bar), last_par, p);
         }
@@ -945,30 +881,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if (lg && bits) {
                 mk.w0 |= g4.x; mk.w1 |= g4.y; mk.w2 |= g4.z; mk.w3 |= g4.w;
             }
-            // classes of the two 64-column halves (bf16 path): a half with every column allowed for
-            // the whole warp takes no mask, a half with none is skipped
-            uint32_t halves = HALVES_MASKED;
-            if constexpr (BIAS == BIAS_NONE && !F8) {
-                if (partial && !gathered) {
-                    halves = 0u;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        bool all_in, none_in;
-                        if (upper) {
-                            all_in = mk.a1 >= 64 * h + 63;
-                            none_in = mk.a1 < 64 * h;
-                        } else {
-                            const uint32_t lo_w = h ? mk.w2 : mk.w0, hi_w = h ? mk.w3 : mk.w1;
-                            all_in = (lo_w & hi_w) == 0xffffffffu;
-                            none_in = (lo_w | hi_w) == 0u;
-                        }
-                        const uint32_t c = __all_sync(0xffffffffu, all_in)    ? (uint32_t)HALF_FREE
-                                           : __all_sync(0xffffffffu, none_in) ? (uint32_t)HALF_EMPTY
-                                                                               : (uint32_t)HALF_MASKED;
-                        halves |= c << (2 * h);
-                    }
-                }
-            }
             // ---- pass 1: row max of the (masked) scores, in log2 units
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
@@ -987,11 +899,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
                     else
                         mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk, halves)
-                                     : tile_row_max<MASK_ANY>(t_s, mk, halves);
+                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
                 } else {
                     mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk, halves) : tile_row_max<MASK_ANY>(t_s, mk, halves);
+                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
                 }
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
@@ -1050,8 +961,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                     sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, sl2, r_eff, bar(B_PFULL), fix);
                 else
                     sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
-                          : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix, halves)
-                                  : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix, halves);
+                          : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                                  : tile_exp_store<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
             }
             l += sum;
             tmem_wait_st();
@@ -1154,7 +1065,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
 
 template <int D, int BIAS, bool F8 = false, bool LG = false>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
-    using C = Cfg<D, BIAS, F8, LG>;
+    using C = Cfg<D, BIAS, F8>;
     cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8, LG>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     attn_fwd_tc_kernel<D, BIAS, F8, LG><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
