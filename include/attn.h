@@ -247,8 +247,10 @@ int attn_selftest_device_once(void);
  *   slopes : HOST array of Hq finite floats (query head a uses slopes[a]; copied),
  *            or NULL to remove the bias.
  * The bias enters the row max, the weights and the LSE (LSE = ln sum_j e^{logits_ij}).
+ * Every mask kind takes it; under LOCAL_GLOBAL the global keys and rows get the same
+ * distance term (|i - j| between the positions of the pair).
  * Errors: ATTN_ERR_INVALID_ARG (NULL handle, non-finite slope),
- *         ATTN_ERR_UNSUPPORTED (LOCAL_GLOBAL handles), ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ *         ATTN_ERR_UNSUPPORTED (ATTN_FP8_E4M3 handles, or a bias matrix set), ATTN_ERR_OOM, ATTN_ERR_CUDA.
  * Must not be called while a forward of this handle is in flight.
  */
 attn_status attn_set_alibi(attn_handle h, const float* slopes);

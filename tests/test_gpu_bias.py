@@ -63,12 +63,43 @@ def test_prefill_alibi_removed_gives_the_unbiased_output():
     assert not torch.equal(O0, O1)
 
 
-def test_prefill_alibi_local_global_is_unsupported():
+def _full_lg(w, slopes):
+    """Local + global with ALiBi: the global keys and rows take the distance term of their positions."""
     import transformer_self_attention_gb300 as tsa
-    plan = tsa.Attention(1, 2, 2, 300, 64, kind=wl.MASK_LOCAL_GLOBAL, window=5, global_idx=[0])
-    with pytest.raises(tsa.AttnError) as e:
-        plan.set_alibi([0.1, 0.2])
-    assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED
+    Qc, Kc, Vc = wl.make_inputs(w)
+    Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(w.globals_idx))
+    plan.set_alibi(slopes)
+    O = torch.full_like(Q, float("nan"))
+    L = torch.full((w.B, w.Hq, w.S), float("nan"), dtype=torch.float32, device=Q.device)
+    plan(Q, K, V, O=O, LSE=L)
+    torch.cuda.synchronize()
+    assert plan.poll_device_error() == (0, 0)
+    O_ref, L_ref = oracle.attention(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), w.scale, w.kind,
+                                    w.window, list(w.globals_idx), alibi=slopes)
+    return compare(w, O.float().cpu().numpy().reshape(-1, w.d), L.cpu().numpy().ravel(), O_ref.reshape(-1, w.d),
+                   L_ref.ravel())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [[0], [0, 300, 599], [5, 127, 128, 500], list(range(3, 600, 7))])
+def test_prefill_alibi_local_global(G, d):
+    """Gathered global keys (narrow tiles), chunked global rows and band tiles with the ALiBi term."""
+    _full_lg(small("alg", 1, 4, 2, 600, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G),
+             wl.alibi_slopes(4))
+
+
+def test_prefill_alibi_local_global_steep_and_fp32():
+    _full_lg(small("algs", 2, 3, 3, 520, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=33, globals_idx=(0, 260, 519)),
+             [0.0, 0.05, 1.0])
+    _full_lg(small("algf", 1, 2, 2, 300, 64, "f32", wl.MASK_LOCAL_GLOBAL, window=20, globals_idx=(0, 150)),
+             [0.02, 0.3])
+
+
+def test_prefill_alibi_local_global_full_size():
+    """The local + global workload (H12 S8192 d64 w512, 4 globals) with geometric slopes; every output."""
+    _full_lg(wl.LONGFORMER_8K, wl.alibi_slopes(wl.LONGFORMER_8K.Hq))
 
 
 def test_prefill_alibi_full_size_causal_4k():

@@ -481,6 +481,54 @@ __device__ __forceinline__ float narrow_exp_store(uint32_t t_s, int nch, int a1,
     return acc.x + acc.y;
 }
 
+// The two passes over a gathered-key tile with the ALiBi bias: x = s sl2 - mL |fi - pos(c)| in log2 units,
+// with pos(c) the sequence position of the key in column c and fi the row's; -inf past the tile's keys.
+template <class Pos>
+__device__ __forceinline__ float narrow_row_max_alibi(uint32_t t_s, int nch, int a1, float sl2, float mL, float fi,
+                                                      Pos pos) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const int c = ch * 32 + e;
+            const float x0 = c <= a1 ? fmaf(__uint_as_float(r[e]), sl2, -mL * fabsf(fi - pos(c))) : -INFINITY;
+            const float x1 = c + 1 <= a1 ? fmaf(__uint_as_float(r[e + 1]), sl2, -mL * fabsf(fi - pos(c + 1))) : -INFINITY;
+            m0 = fmaxf(m0, x0);
+            m1 = fmaxf(m1, x1);
+        }
+    }
+    return fmaxf(m0, m1);
+}
+
+template <class Pos>
+__device__ __forceinline__ float narrow_exp_store_alibi(uint32_t t_s, int nch, int a1, float sl2, float ref, float mL,
+                                                        float fi, Pos pos, uint32_t bar_p) {
+    float acc = 0.f;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c = ch * 32 + 2 * e;
+            const float x0 = c <= a1 ? fmaf(__uint_as_float(r[2 * e]), sl2, -mL * fabsf(fi - pos(c)) - ref) : -INFINITY;
+            const float x1 =
+                c + 1 <= a1 ? fmaf(__uint_as_float(r[2 * e + 1]), sl2, -mL * fabsf(fi - pos(c + 1)) - ref) : -INFINITY;
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            acc += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(t_s + ch * 16, pk);
+    }
+    release_first_half(bar_p);
+    return acc;
+}
+
 // This thread's O row (tensor memory, fp32) times inv_l, stored as bf16 at dst.  Every lane runs
 // the tensor-memory loads (they are warp-collective); only lanes with `store` write.
 template <int D>
@@ -884,9 +932,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             // ---- pass 1: row max of the (masked) scores, in log2 units
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
+            // gathered tile under ALiBi: the key position of column c (the padding columns are masked)
+            auto gpos_f = [&](int c) -> float { return c < gcols ? (float)outside_key(it * BN + c) : 0.f; };
             if constexpr (ALIBI) {
                 base = (float)(i - (long)band_tile(it - n_gat) * BN);
-                if (causal_kind)
+                if (LG && gathered)
+                    mx = narrow_row_max_alibi(t_s, (gcols + 31) >> 5, mk.a1, sl2, mL, (float)i, gpos_f);
+                else if (causal_kind)
                     mx = partial ? tile_row_max_alibi<MASK_ANY, false>(t_s, mk, sl2, mL, base)
                                  : tile_row_max_alibi<MASK_NONE, false>(t_s, mk, sl2, mL, base);
                 else
@@ -941,7 +993,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             float sum;
             if constexpr (ALIBI) {
                 fix();
-                if (causal_kind)
+                if (LG && gathered)
+                    sum = narrow_exp_store_alibi(t_s, (gcols + 31) >> 5, mk.a1, sl2, ref, mL, (float)i, gpos_f, bar(B_PFULL));
+                else if (causal_kind)
                     sum = partial ? tile_exp_store_alibi<MASK_ANY, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
                                   : tile_exp_store_alibi<MASK_NONE, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
                 else
@@ -1084,6 +1138,11 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
     if (p.bias) {  // a bias matrix (bf16 inputs, interval kinds; checked by the host)
         if (d == 128) return launch<128, BIAS_MATRIX>(p, n_items, stream);
         if (d == 64) return launch<64, BIAS_MATRIX>(p, n_items, stream);
+        return cudaErrorInvalidValue;
+    }
+    if (p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0 && p.alibi) {  // gathered keys under ALiBi
+        if (d == 128) return launch<128, BIAS_ALIBI_ELEM, false, true>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_ALIBI_ELEM, false, true>(p, n_items, stream);
         return cudaErrorInvalidValue;
     }
     if (p.alibi && causal) {
