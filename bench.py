@@ -76,8 +76,9 @@ def ncu_traffic(workload_name: str, kernel: str = "attn_fwd_tc", sources=KERNEL_
 
 
 # The NVML sampler that ClockSampler runs in a child process (no torch import, so it starts in
-# milliseconds).  It reads the SM clock, its maximum, the power draw and the clock event reasons
-# every `interval` seconds, stamped with CLOCK_MONOTONIC, until its standard input closes.
+# milliseconds).  It reads the SM clock and the clock event reasons (the power draw every 16th
+# time, the maximum clock once), sleeping `interval` seconds between readings, stamped with
+# CLOCK_MONOTONIC, until its standard input closes.
 _NVML_SAMPLER = r"""
 import ctypes, sys, time, select
 bus, interval = sys.argv[1].encode(), float(sys.argv[2])
@@ -99,8 +100,9 @@ while True:
         nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
     k += 1
     out.append("%.6f %d %d %d %d" % (t, mhz.value, mx.value, mw.value, rs.value))
-    if select.select([sys.stdin], [], [], interval)[0] and not sys.stdin.readline():
+    if select.select([sys.stdin], [], [], 0)[0] and not sys.stdin.readline():
         break
+    time.sleep(interval)
 print("\n".join(out), flush=True)
 nv.nvmlShutdown()
 """
@@ -112,7 +114,7 @@ _REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowd
 class ClockSampler:
     """SM clock and throttle reasons sampled during the timed region.
 
-    NVML in a child process every 0.25 ms (its readings are stamped with the monotonic clock, and
+    NVML in a child process about every 0.1-0.2 ms (its readings are stamped with the monotonic clock, and
     the summary keeps those between mark_start() and mark_end(), weighting each reading by the
     time until the next); nvidia-smi every 200 ms when NVML cannot be loaded.
     """
@@ -126,7 +128,7 @@ class ClockSampler:
             import torch
             pr = torch.cuda.get_device_properties(device if device is not None else gpu_index)
             bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
-            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_SAMPLER, bus, "0.00025"], stdin=subprocess.PIPE,
+            self.proc = subprocess.Popen([sys.executable, "-c", _NVML_SAMPLER, bus, "0.0001"], stdin=subprocess.PIPE,
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             if self.proc.stdout.readline().strip() == "ready":
                 self.kind = "nvml"
@@ -204,7 +206,7 @@ class ClockSampler:
                 if r[4] & bit:
                     reasons.add(name)
         return {"sm_mhz": med, "sm_max_mhz": max(r[2] for r in sel), "reasons": sorted(reasons),
-                "samples": len(inside), "sampler": "NVML every 0.25 ms in a child process",
+                "samples": len(inside), "sampler": "NVML about every 0.1-0.2 ms in a child process",
                 "sm_mhz_time_weighted_median": med, "sm_mhz_min": min(r[1] for r in sel),
                 "power_w_max": max(r[3] for r in sel) / 1000.0, "timed_region_s": t1 - t0}
 
