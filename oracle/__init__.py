@@ -79,6 +79,9 @@ def _load():
             lib.oracle_decode_bias.restype = I
             lib.oracle_backward.argtypes = [P, P, P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P, P, P, P]
             lib.oracle_backward.restype = I
+            lib.oracle_backward_bias.argtypes = [P, P, P, P, I, I, I, I, I, ctypes.c_double, I, I, P, I, P, P, I, I, L,
+                                                 P, P, P]
+            lib.oracle_backward_bias.restype = I
             _lib = lib
     return _lib
 
@@ -214,11 +217,13 @@ def decode(Q, K, V, cache_len, scale, kind, window=0, alibi=None):
     return O, LSE
 
 
-def backward(Q, K, V, dO, scale, kind, window=0, globals_idx=None, alibi=None):
+def backward(Q, K, V, dO, scale, kind, window=0, globals_idx=None, alibi=None, bias=None):
     """Gradients of the attention with respect to Q, K, V for the output gradient dO.
 
     Q, dO [B, Hq, S, d]; K, V [B, Hkv, S, d].  Returns (dQ, dK, dV) in float64 with the
     shapes of Q, K, V (dK and dV summed over the query heads of each kv head).
+    bias: optional float32-castable [Bb, Hb, S, ld] bias matrix added to the scaled scores, as
+    for attention_rows.
     """
     lib = _load()
     Q = np.ascontiguousarray(Q, dtype=np.float32)
@@ -233,9 +238,17 @@ def backward(Q, K, V, dO, scale, kind, window=0, globals_idx=None, alibi=None):
     dQ = np.empty(Q.shape, dtype=np.float64)
     dK = np.empty(K.shape, dtype=np.float64)
     dV = np.empty(V.shape, dtype=np.float64)
-    rc = lib.oracle_backward(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, Hq, Hkv, S, d, float(scale), int(kind),
-                             int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None, _ptr(dQ), _ptr(dK),
-                             _ptr(dV))
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+        Bb, Hb, Sb, ld = bias.shape
+        assert Sb == S and Bb in (1, B) and Hb in (1, Hq) and ld >= S
+    else:
+        Bb = Hb = 1
+        ld = 0
+    rc = lib.oracle_backward_bias(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), B, Hq, Hkv, S, d, float(scale), int(kind),
+                                  int(window), _ptr(g), ng, _ptr(sl) if sl is not None else None,
+                                  _ptr(bias) if bias is not None else None, Bb, Hb, ld, _ptr(dQ), _ptr(dK),
+                                  _ptr(dV))
     if rc != 0:
         raise ValueError("oracle_backward rejected its arguments")
     return dQ, dK, dV

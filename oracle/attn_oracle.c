@@ -420,12 +420,36 @@ int oracle_decode_bias(const float* Q, const float* K, const float* V,
  * and added at the end, in a fixed order.
  * Returns 0, or -1 on bad arguments or allocation failure.
  */
+/*
+ * The same gradients with a given additive bias matrix as well (bias == NULL: none): the
+ * logits are scale * q_i . k_j - alibi[a] |i - j| + bias[b', a', i, j] (b' = b if Bb == B
+ * else 0, a' = a if Hb == Hq else 0, row stride ld), the unified biased-logits form of
+ * "Transformer 架构及其变体" (aaai.latere.ai).  The bias does not depend on Q, K or V, so it
+ * enters only the weights P; dS, dQ, dK and dV keep their formulas.
+ */
+int oracle_backward_bias(const float* Q, const float* K, const float* V, const float* dO,
+                         int B, int Hq, int Hkv, int S, int d, double scale, int kind, int window,
+                         const int* G, int nG, const double* alibi,
+                         const float* bias, int Bb, int Hb, long ld,
+                         double* dQ, double* dK, double* dV);
+
 int oracle_backward(const float* Q, const float* K, const float* V, const float* dO,
                     int B, int Hq, int Hkv, int S, int d, double scale, int kind, int window,
                     const int* G, int nG, const double* alibi,
                     double* dQ, double* dK, double* dV)
 {
+    return oracle_backward_bias(Q, K, V, dO, B, Hq, Hkv, S, d, scale, kind, window, G, nG, alibi,
+                                NULL, 1, 1, 0, dQ, dK, dV);
+}
+
+int oracle_backward_bias(const float* Q, const float* K, const float* V, const float* dO,
+                         int B, int Hq, int Hkv, int S, int d, double scale, int kind, int window,
+                         const int* G, int nG, const double* alibi,
+                         const float* bias, int Bb, int Hb, long ld,
+                         double* dQ, double* dK, double* dV)
+{
     if (B < 1 || Hq < 1 || Hkv < 1 || S < 1 || d < 1 || Hq % Hkv != 0) return -1;
+    if (bias && ((Bb != 1 && Bb != B) || (Hb != 1 && Hb != Hq) || ld < S)) return -1;
     unsigned char* is_global = make_global_flags(S, G, nG);
     if (!is_global) return -1;
     const int group = Hq / Hkv;
@@ -471,6 +495,10 @@ int oracle_backward(const float* Q, const float* K, const float* V, const float*
                 for (int c = 0; c < d; ++c) dot += (double)q[c] * (double)K[kvh + (size_t)j * d + c];
                 s[j] = dot * scale;
                 if (alibi) s[j] -= alibi[a] * (double)labs(i - j);
+                if (bias) {
+                    const size_t plane = (size_t)(Bb == 1 ? 0 : b) * Hb + (size_t)(Hb == 1 ? 0 : a);
+                    s[j] += (double)bias[(plane * (size_t)S + (size_t)i) * (size_t)ld + (size_t)j];
+                }
                 if (s[j] > m) m = s[j];
             }
             double l = 0.0;

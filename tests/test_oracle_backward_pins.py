@@ -23,7 +23,7 @@ def _rand(shape, seed, scale=1.0):
     return (rng.standard_normal(shape) * scale).astype(np.float32)
 
 
-def _torch_grads(Q, K, V, dO, scale, kind, w, G, slopes=None):
+def _torch_grads(Q, K, V, dO, scale, kind, w, G, slopes=None, bias=None):
     B, Hq, S, d = Q.shape
     Hkv = K.shape[1]
     M = torch.zeros(S, S, dtype=torch.bool)
@@ -39,6 +39,8 @@ def _torch_grads(Q, K, V, dO, scale, kind, w, G, slopes=None):
     if slopes is not None:
         dist = (torch.arange(S)[:, None] - torch.arange(S)[None, :]).abs().double()
         s = s - torch.tensor(slopes, dtype=torch.float64)[None, :, None, None] * dist
+    if bias is not None:  # [Bb, Hb, S, ld]: broadcast over batch / heads, padding columns unused
+        s = s + torch.from_numpy(bias).double()[..., :S]
     s = s.masked_fill(~M, float("-inf"))
     o = torch.softmax(s, -1) @ vr
     (o * torch.from_numpy(dO).double()).sum().backward()
@@ -122,3 +124,32 @@ def test_backward_gqa_is_the_group_sum_of_mha():
     assert np.allclose(dQ, dQm, atol=1e-13)
     assert np.allclose(dK, dKm.reshape(B, Hkv, 3, S, d).sum(axis=2), atol=1e-12)
     assert np.allclose(dV, dVm.reshape(B, Hkv, 3, S, d).sum(axis=2), atol=1e-12)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("bshape", [(1, 1), (2, 1), (1, 4), (2, 4)])
+def test_backward_with_bias_matrix_matches_autograd(kind, bshape):
+    """A given bias matrix b_ij [Bb, Hb, S, ld] (batch / head broadcast, padded rows) in the logits:
+    the oracle's gradients equal float64 autograd through an independently written forward."""
+    B, Hq, Hkv, S, d = 2, 4, 2, 21, 5
+    Q, K, V, dO = _rand((B, Hq, S, d), 11), _rand((B, Hkv, S, d), 12), _rand((B, Hkv, S, d), 13), _rand((B, Hq, S, d), 14)
+    bias = _rand((bshape[0], bshape[1], S, S + 3), 15, scale=2.0)
+    G = [0, 9] if kind == oracle.MASK_LOCAL_GLOBAL else None
+    got = oracle.backward(Q, K, V, dO, 0.35, kind, 4, G, bias=bias)
+    ref = _torch_grads(Q, K, V, dO, 0.35, kind, 4, G, bias=bias)
+    for a, b in zip(got, ref):
+        assert np.allclose(a, b, atol=1e-11, rtol=0)
+
+
+def test_backward_bias_padding_columns_are_not_read():
+    """Values in the padding columns of the bias rows (ld > S) change nothing (up to the order in which
+    the threads' dK / dV partial sums are added)."""
+    B, Hq, S, d = 1, 2, 17, 4
+    Q, K, V, dO = _rand((B, Hq, S, d), 21), _rand((B, Hq, S, d), 22), _rand((B, Hq, S, d), 23), _rand((B, Hq, S, d), 24)
+    bias = _rand((1, Hq, S, S + 5), 25)
+    a = oracle.backward(Q, K, V, dO, 0.5, oracle.MASK_CAUSAL, bias=bias)
+    bias2 = bias.copy()
+    bias2[..., S:] = 1e30
+    b = oracle.backward(Q, K, V, dO, 0.5, oracle.MASK_CAUSAL, bias=bias2)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, atol=1e-13, rtol=0)
