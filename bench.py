@@ -249,8 +249,29 @@ def _oracle_inputs(w: wl.Workload):
     return _INPUTS[w.name]
 
 
-def cpu_baseline(w: wl.Workload, target_s: float = 12.0, frac: float | None = None):
-    """The fp64 oracle, as it stands, on a strided sample of the workload's rows."""
+def make_bias_matrix(w: wl.Workload):
+    """The per-head bias matrix [1, Hq, S, S] of `--bias`: bf16 N(0, 2^2), seeded by the workload."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 2)
+    return (torch.randn(1, w.Hq, w.S, w.S, generator=g) * 2).to(torch.bfloat16)
+
+
+def score_bias_host(args, w: wl.Workload):
+    """The score bias of the command line as the oracle takes it: (ALiBi slopes [Hq] or None,
+    float32 bias matrix [1, Hq, S, S] or None), the values the GPU arm sets."""
+    alibi = wl.alibi_slopes(w.Hq) if getattr(args, "alibi", False) else None
+    bias = None
+    if getattr(args, "bias", False):
+        key = ("bias", w.name)
+        if key not in _INPUTS:
+            _INPUTS[key] = make_bias_matrix(w).float().numpy()
+        bias = _INPUTS[key]
+    return alibi, bias
+
+
+def cpu_baseline(w: wl.Workload, target_s: float = 12.0, frac: float | None = None, sb=(None, None)):
+    """The fp64 oracle, as it stands, on a strided sample of the workload's rows (with the
+    score bias sb = (slopes, bias matrix) of the timed configuration)."""
     import numpy as np
     n_cores = len(os.sched_getaffinity(0))
     os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
@@ -264,7 +285,7 @@ def cpu_baseline(w: wl.Workload, target_s: float = 12.0, frac: float | None = No
         rb, ra, ri = bb.ravel(), aa.ravel(), ii.ravel()
         t0 = time.perf_counter()
         oracle.attention_rows(Kf, Vf, w.Hq, w.scale, w.kind, w.window, list(w.globals_idx), Qf[rb, ra, ri],
-                              rb, ra, ri)
+                              rb, ra, ri, alibi=sb[0], bias=sb[1])
         dt = time.perf_counter() - t0
         # useful flops of the sampled rows: rows are strided uniformly, so the sample holds 1/stride of the pairs
         rows_frac = len(ri) / (w.B * w.Hq * w.S)
@@ -303,11 +324,12 @@ def run_reference(args, w):
     n_cores = len(os.sched_getaffinity(0))
     os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
     # one calibration sample fixes the per-step sample so the whole run takes a few minutes
-    cal = cpu_baseline(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    sb = score_bias_host(args, w)
+    cal = cpu_baseline(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)), sb=sb)
     frac_stride = int(re.search(r"every (\d+)th", cal["sample"]).group(1))
     times, flops = [], 0.0
     for s in range(args.warmup + args.steps):
-        r = cpu_baseline(w, frac=1.0 / frac_stride)
+        r = cpu_baseline(w, frac=1.0 / frac_stride, sb=sb)
         if s >= args.warmup:
             times.append(r["seconds"])
             flops = r["value"] * r["seconds"] * 1e12
@@ -404,8 +426,7 @@ def run_ours(args, w):
     if args.alibi:
         plan.set_alibi(wl.alibi_slopes(w.Hq))
     if args.bias:  # a per-head bias matrix [1, Hq, S, S], bf16 N(0, 2^2), resident in HBM
-        g = torch.Generator(device="cpu").manual_seed(w.seed + 2)
-        bias = (torch.randn(1, w.Hq, w.S, w.S, generator=g) * 2).to(torch.bfloat16).to(dev)
+        bias = make_bias_matrix(w).to(dev)
         plan.set_bias(bias)
     O = torch.empty(Q.shape, dtype=torch.bfloat16 if args.fp8 else Q.dtype, device=dev)
     LSE = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
@@ -501,7 +522,7 @@ def run_ours(args, w):
     if clk:
         line["clocks"] = clk
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, sb=score_bias_host(args, w))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -515,9 +536,9 @@ BWD_KERNEL_SOURCES = ["transformer_self_attention_gb300/csrc/attn_bwd.cu",
                       "transformer_self_attention_gb300/csrc/kernels.h"]
 
 
-def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int | None = None):
+def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int | None = None, sb=(None, None)):
     """The fp64 backward oracle, as it stands, on whole (batch, kv head) slices of the workload
-    (every query head of the group, every row)."""
+    (every query head of the group, every row), with the score bias sb = (slopes, bias matrix)."""
     n_cores = len(os.sched_getaffinity(0))
     os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
     import oracle
@@ -536,7 +557,8 @@ def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int 
             b, g = divmod(k % (w.B * w.Hkv), w.Hkv)
             qs = slice(g * group, (g + 1) * group)
             oracle.backward(Qf[b:b + 1, qs], Kf[b:b + 1, g:g + 1], Vf[b:b + 1, g:g + 1], dOf[b:b + 1, qs], w.scale,
-                            w.kind, w.window)
+                            w.kind, w.window, alibi=None if sb[0] is None else sb[0][qs],
+                            bias=None if sb[1] is None else sb[1][:, qs])
         return time.perf_counter() - t0
 
     if n_slices is None:
@@ -550,11 +572,12 @@ def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int 
                       f"{fl / 1e9:.1f} useful GFLOP, fp64 C oracle with OpenMP"}
 
 
-def _bwd_config(w, useful, world: int = 1, alibi: bool = False):
+def _bwd_config(w, useful, world: int = 1, alibi: bool = False, bias: bool = False):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "d": w.d,
             "mask": wl.MASK_NAMES[w.kind], "window": w.window, "pass": "backward (dQ, dK, dV)",
             "useful_gflop_per_step": useful / 1e9, "flops_per_pair": f"10 d (2.5 x the forward's 4 d)",
-            "score_bias": "alibi, slopes 2^(-8(a+1)/H)" if alibi else "none",
+            "score_bias": ("alibi, slopes 2^(-8(a+1)/H)" if alibi else
+                           "matrix [1, Hq, S, S] bf16 N(0, 2^2)" if bias else "none"),
             "l2": "flushed before every GPU step (256 MiB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -563,10 +586,11 @@ def run_reference_backward(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    cal = cpu_baseline_backward(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    sb = score_bias_host(args, w)
+    cal = cpu_baseline_backward(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)), sb=sb)
     times, r = [], None
     for s in range(args.warmup + args.steps):
-        r = cpu_baseline_backward(w, n_slices=cal["n_slices"])
+        r = cpu_baseline_backward(w, n_slices=cal["n_slices"], sb=sb)
         if s >= args.warmup:
             times.append(r["seconds"])
     t = sum(times) / len(times)
@@ -574,7 +598,7 @@ def run_reference_backward(args, w):
     line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": _bwd_config(w, wl.backward_flops(w), max(1, args.gpus), args.alibi),
+            "config": _bwd_config(w, wl.backward_flops(w), max(1, args.gpus), args.alibi, args.bias),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -600,6 +624,9 @@ def run_ours_backward(args, w):
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
     if args.alibi:
         plan.set_alibi(wl.alibi_slopes(w.Hq))
+    if args.bias:  # the forward's per-head bias matrix, resident in HBM; both passes read it
+        bias = make_bias_matrix(w).to(dev)
+        plan.set_bias(bias)
     O, LSE = plan(Q, K, V)
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -676,14 +703,14 @@ def run_ours_backward(args, w):
     line = {"metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": _bwd_config(w, useful, world, args.alibi),
+            "config": _bwd_config(w, useful, world, args.alibi, args.bias),
             "roofline": roofline, "gpu_launches": 3 * args.steps, "wall_s_timed_region": wall}
     if e2e:
         line["e2e"] = e2e
     if clk:
         line["clocks"] = clk
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline_backward(w)
+        line["cpu_baseline"] = cpu_baseline_backward(w, sb=score_bias_host(args, w))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -699,8 +726,9 @@ def _decode_oracle_inputs(w):
     return _INPUTS[key]
 
 
-def cpu_baseline_decode(w, target_s: float = 12.0, n_seq: int | None = None):
-    """The fp64 decode oracle, as it stands, on the first n_seq sequences of the batch."""
+def cpu_baseline_decode(w, target_s: float = 12.0, n_seq: int | None = None, alibi=None):
+    """The fp64 decode oracle, as it stands, on the first n_seq sequences of the batch (with the
+    ALiBi slopes of the timed configuration, if any)."""
     n_cores = len(os.sched_getaffinity(0))
     os.environ.setdefault("OMP_NUM_THREADS", str(n_cores))
     import oracle
@@ -709,7 +737,7 @@ def cpu_baseline_decode(w, target_s: float = 12.0, n_seq: int | None = None):
 
     def run(nb):
         t0 = time.perf_counter()
-        oracle.decode(Qf[:nb], Kf[:nb], Vf[:nb], lens[:nb], w.scale, w.kind, w.window)
+        oracle.decode(Qf[:nb], Kf[:nb], Vf[:nb], lens[:nb], w.scale, w.kind, w.window, alibi=alibi)
         dt = time.perf_counter() - t0
         return dt, wl.decode_useful_flops(w, lens[:nb])
 
@@ -738,10 +766,11 @@ def run_reference_decode(args, w):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    cal = cpu_baseline_decode(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    alibi = score_bias_host(args, w)[0] if args.alibi else None
+    cal = cpu_baseline_decode(w, target_s=max(2.0, 150.0 / max(1, args.steps + args.warmup)), alibi=alibi)
     times, r = [], None
     for s in range(args.warmup + args.steps):
-        r = cpu_baseline_decode(w, n_seq=cal["n_seq"])
+        r = cpu_baseline_decode(w, n_seq=cal["n_seq"], alibi=alibi)
         if s >= args.warmup:
             times.append(r["seconds"])
     t = sum(times) / len(times)
@@ -873,7 +902,7 @@ def run_ours_decode(args, w):
     if clk:
         line["clocks"] = clk
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline_decode(w)
+        line["cpu_baseline"] = cpu_baseline_decode(w, alibi=wl.alibi_slopes(w.Hq) if args.alibi else None)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -901,8 +930,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.bias and (args.fp8 or args.alibi or args.backward or args.workload not in wl.BY_NAME):
-        ap.error("--bias takes a bf16 prefill workload without --fp8 / --alibi / --backward")
+    if args.bias and (args.fp8 or args.alibi or args.workload not in wl.BY_NAME):
+        ap.error("--bias takes a bf16 prefill workload without --fp8 / --alibi")
     if args.backward:
         if args.workload not in wl.BY_NAME or args.fp8:
             ap.error("--backward takes a bf16 prefill workload without --fp8")

@@ -273,7 +273,7 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes);
  * Errors: ATTN_ERR_INVALID_ARG (NULL handle, misaligned pointer, Bb / Hb / ld out of
  *         range); ATTN_ERR_UNSUPPORTED (dtype other than ATTN_BF16, LOCAL_GLOBAL, or
  *         with the ALiBi bias set).
- * attn_backward of a handle with a bias matrix returns ATTN_ERR_UNSUPPORTED.
+ * attn_backward of a handle with a bias matrix recomputes P with the same b_ij.
  * Must not be called while a forward of this handle is in flight.
  */
 attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long ld);
@@ -292,12 +292,14 @@ attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long 
  *                    outputs of attn_forward for these Q, K, V.
  *   LSE            : float32 [B, Hq, S] device array (required).
  *   dQ, dK, dV     : bf16 outputs with the shapes of Q, K, V (overwritten).
- * With the ALiBi bias set (attn_set_alibi), s_ij includes -m_a |i - j| as in the forward
- * (the bias does not depend on Q or K, so it enters only the recomputed P).
+ * With the ALiBi bias set (attn_set_alibi), s_ij includes -m_a |i - j| as in the forward,
+ * and with a bias matrix set (attn_set_bias) it includes b_ij, read from the caller's
+ * bias tensor, which must still hold the values the forward used (neither bias depends
+ * on Q or K, so each enters only the recomputed P).
  * Enqueued on `stream`; the first call allocates the handle's backward scratch
  * (2 * B*Hq*ceil(S/128)*128 floats and the key-tile schedule).
  * Errors: ATTN_ERR_INVALID_ARG (NULL or misaligned pointer); ATTN_ERR_UNSUPPORTED
- * (dtype other than ATTN_BF16, LOCAL_GLOBAL, or with a bias matrix set);
+ * (dtype other than ATTN_BF16, or LOCAL_GLOBAL);
  * ATTN_ERR_OOM; ATTN_ERR_CUDA.
  */
 attn_status attn_backward(attn_handle h, const void* Q, const void* K, const void* V, const void* O,

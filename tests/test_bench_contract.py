@@ -45,10 +45,29 @@ def test_fewer_than_three_warmup_steps_are_rejected():
     assert "--warmup" in r.stderr
 
 
-def test_bias_matrix_with_backward_is_rejected():
-    r = _bench("--bias", "--backward")
-    assert r.returncode != 0
-    assert "--bias" in r.stderr
+def test_bias_matrix_with_fp8_or_alibi_is_rejected():
+    for extra in (("--fp8",), ("--alibi",), ("--backward", "--alibi")):
+        r = _bench("--bias", *extra)
+        assert r.returncode != 0
+        assert "--bias" in r.stderr
+
+
+def test_reference_arm_takes_the_score_bias_of_the_command_line():
+    """With --bias the oracle leg adds the same bias matrix the GPU arm sets, and both arms
+    print the same config."""
+    r = _bench("--impl", "reference", "--workload", "tiny_full_f32_B1_H4_S256_d64", "--steps", "1", "--warmup", "3",
+               "--bias")
+    assert r.returncode == 0, r.stderr
+    line = json.loads([l for l in r.stdout.splitlines() if l.strip()][0])
+    sys.path.insert(0, ROOT)
+    import argparse
+    import bench
+    import workloads as wl
+    args = argparse.Namespace(alibi=False, bias=True, fp8=False)
+    assert line["config"] == json.loads(json.dumps(bench.fwd_config(args, wl.TINY_FULL_F32, 1)))
+    assert line["config"]["score_bias"].startswith("matrix")
+    alibi, bias = bench.score_bias_host(args, wl.TINY_FULL_F32)
+    assert alibi is None and bias.shape == (1, 4, 256, 256) and bias.dtype.name == "float32"
 
 
 def test_clock_summary_is_time_weighted_over_the_timed_region():

@@ -3,9 +3,10 @@
 Every output is compared on small shapes: the four interval kinds, the four broadcast
 shapes [Bb, Hb] of the bias, ragged lengths with padded rows (the padding holds NaN, so a
 kernel that reads it into a result fails), GQA and both head widths; the causal MHA 4K
-workload runs at full size with a per-head bias on sampled rows.  Bounds: those of the
+workload runs at full size with a per-head bias, every output.  Bounds: those of the
 bf16 forward (the bias is bf16, exact in the oracle's float32 copy, and adds one fp32
-multiply-add per score).
+multiply-add per score).  The backward with the same bias is compared with the fp64 backward
+oracle at the backward's bounds.
 """
 import numpy as np
 import pytest
@@ -108,11 +109,67 @@ def test_bias_matrix_unsupported_and_invalid():
     pl.set_bias(bias)
     with pytest.raises(tsa.AttnError):  # ALiBi and a bias matrix together
         pl.set_alibi(wl.alibi_slopes(2))
-    Q, K, V = (t.cuda() for t in wl.make_inputs(small("u", 1, 2, 2, 256, 128, "bf16", wl.MASK_CAUSAL)))
-    O, LSE = pl(Q, K, V)
-    with pytest.raises(tsa.AttnError):  # no backward with a bias matrix
-        pl.backward(Q, K, V, O, LSE, O)
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ backward with a bias matrix
+
+def _check_backward(w, Bb, Hb, ld, seed=5):
+    """dQ, dK, dV of the biased forward against the fp64 backward oracle with the same bias."""
+    from test_gpu_backward import _cmp
+    Qc, Kc, Vc = wl.make_inputs(w)
+    dOc = wl.make_grad_output(w)
+    bias = _bias(Bb, Hb, w.S, ld, seed)
+    Q, K, V, dO = Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda()
+    O, LSE, plan = _run(w, bias, Q, K, V)
+    dQ, dK, dV = (torch.full_like(t, float("nan")) for t in (Q, K, V))
+    plan.backward(Q, K, V, O, LSE, dO, dQ, dK, dV)
+    torch.cuda.synchronize()
+    assert plan.poll_device_error() == (0, 0)
+    ref = oracle.backward(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), dOc.float().numpy(), w.scale,
+                          w.kind, w.window, bias=bias.float().numpy())
+    return [_cmp(n, g, r) for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref)]
+
+
+@pytest.mark.parametrize("Bb,Hb", [(1, 1), (2, 1), (1, 4), (2, 4)])
+@pytest.mark.parametrize("kind", KINDS)
+def test_backward_bias_matrix_kinds_and_broadcasts(kind, Bb, Hb):
+    """The bias enters the recomputed P of both backward kernels: the dQ kernel reads it along the
+    query rows, the dK/dV kernel down the key columns; padded rows hold NaN."""
+    _check_backward(small("bbm", 2, 4, 2, 300, 128, "bf16", kind, window=70), Bb, Hb, ld=304)
+
+
+@pytest.mark.parametrize("S", [2, 129, 257])
+def test_backward_bias_matrix_lengths_d64(S):
+    ld = (S + 7) // 8 * 8 + 8
+    _check_backward(small("bbl", 1, 2, 1, S, 64, "bf16", wl.MASK_CAUSAL), 1, 2, ld=ld)
+
+
+def test_backward_bias_matrix_full_size_causal_mha_4k():
+    """The causal MHA workload with a per-head bias [1, 32, S, S]: every gradient element against the
+    oracle (one call per (batch, head) slice, exact for MHA)."""
+    from test_gpu_backward import _cmp
+    w = wl.CAUSAL_MHA_4K
+    Qc, Kc, Vc = wl.make_inputs(w)
+    dOc = wl.make_grad_output(w)
+    g = torch.Generator().manual_seed(11)
+    bias = (torch.randn(1, w.Hq, w.S, w.S, generator=g) * 2).to(torch.bfloat16)
+    Q, K, V, dO = Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda()
+    O, LSE, plan = _run(w, bias, Q, K, V)
+    dQ, dK, dV = (torch.full_like(t, float("nan")) for t in (Q, K, V))
+    plan.backward(Q, K, V, O, LSE, dO, dQ, dK, dV)
+    torch.cuda.synchronize()
+    assert plan.poll_device_error() == (0, 0)
+    bf = bias.float().numpy()
+    refs = [np.empty(t.shape, dtype=np.float64) for t in (dQ, dK, dV)]
+    for b in range(w.B):
+        for a in range(w.Hq):
+            sl = lambda t: t[b:b + 1, a:a + 1].float().numpy()
+            out = oracle.backward(sl(Qc), sl(Kc), sl(Vc), sl(dOc), w.scale, w.kind, bias=bf[:, a:a + 1])
+            for r, x in zip(refs, out):
+                r[b:b + 1, a:a + 1] = x
+    for n, gr, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        _cmp(f"{n} + bias matrix (every element)", gr, r)
 
 
 def test_bias_matrix_full_size_causal_mha_4k():

@@ -470,7 +470,7 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     for (const void* q : ptrs)
         if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(LSE) & 3u) return ATTN_ERR_INVALID_ARG;
-    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->tp.bias) return ATTN_ERR_UNSUPPORTED;
+    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int nq = (h->S + ATTN_TILE - 1) / ATTN_TILE;
     const int S_pad = nq * ATTN_TILE;
@@ -509,6 +509,10 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
         }
     }
     p.alibi = h->tp.alibi;  // the forward's ALiBi slopes (attn_set_alibi), or null
+    p.bias = h->tp.bias;    // the forward's bias matrix (attn_set_bias), or null
+    p.bias_Bb = h->tp.bias_Bb;
+    p.bias_Hb = h->tp.bias_Hb;
+    p.bias_ld = h->tp.bias_ld;
     attn::BwdPrepParams pp{};
     pp.o = static_cast<const uint16_t*>(O); pp.dout = static_cast<const uint16_t*>(dO); pp.lse = LSE;
     pp.nlse2 = h->d_lse2; pp.nd = h->d_dvec;

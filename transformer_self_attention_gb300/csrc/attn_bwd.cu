@@ -228,14 +228,22 @@ struct ColVec {  // one value per column, from a 16-byte aligned shared-memory v
 // With AL, the ALiBi bias -m_a |i - j| joins the exponent, in log2 units: -mL |base - c| for in-tile
 // column c (mL = m_a log2 e; base = the thread's own position minus the first position of the
 // tile's columns, for query rows and key columns alike).
-template <bool MASKED, bool STORE_P, bool AL, class NL>
+// With a bias matrix, bias.chunk(ch, b) fills b with the bf16 bits of b_ij for the 32 columns
+// cb .. cb + 31 (two per word, the lower column in the low half; zero where nothing is read), issued
+// before the scores are loaded; b_ij log2 e joins the exponent.
+struct NoBias {
+    static constexpr bool on = false;
+    __device__ __forceinline__ void chunk(int, uint32_t (&)[16]) const {}
+};
+template <bool MASKED, bool STORE_P, bool AL, class NL, class BV = NoBias>
 __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, float mL, float base,
-                                         float (&pv)[64]) {
+                                         float (&pv)[64], BV bias = BV{}) {
     const float2 sl = make_float2(sl2, sl2);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int cb = h * HALF + ch * 32;
-        uint32_t s[32], pk[16];
+        uint32_t s[32], pk[16], bw[16];
+        if constexpr (BV::on) bias.chunk(ch, bw);
         tmem_ld32(t_s + cb, s);
         tmem_wait_ld();
 #pragma unroll
@@ -250,6 +258,11 @@ __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, 
                     add.x = fmaf(-mL, fabsf(base - (float)(cb + k)), add.x);
                     add.y = fmaf(-mL, fabsf(base - (float)(cb + k + 1)), add.y);
                 }
+                if constexpr (BV::on) {
+                    const uint32_t wv = bw[k >> 1];
+                    add = __ffma2_rn(make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xffff0000u)),
+                                     make_float2(LOG2E, LOG2E), add);
+                }
                 const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cb + k, a0, a1),
                                                         masked<MASKED>(s[k + 1], cb + k + 1, a0, a1)),
                                             sl, add);
@@ -261,6 +274,49 @@ __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, 
         if (STORE_P) tmem_st16(t_s + h * HALF + ch * 16, pk);
     }
 }
+
+// The dQ kernel's bias reader: the thread's query row, 16-byte loads along the row (b points at the
+// row's bias at the first column of the warpgroup's half; n = columns of the half inside the
+// sequence, counted from there).
+struct RowBias {
+    static constexpr bool on = true;
+    const uint16_t* b;
+    int n;
+    __device__ __forceinline__ void chunk(int ch, uint32_t (&w)[16]) const {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int c = ch * 32 + q * 8;
+            // a load that starts inside the sequence stays inside the row (the stride is a multiple of 8);
+            // the row's padding past the sequence may hold anything, so those columns are zeroed here
+            // (their scores are masked to -inf, and -inf + NaN would not be)
+            const uint4 v = (b != nullptr && c < n) ? __ldg(reinterpret_cast<const uint4*>(b + c))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = c + 2 * e;
+                w[4 * q + e] = (col + 1 < n) ? vw[e] : (col < n) ? (vw[e] & 0xffffu) : 0u;
+            }
+        }
+    }
+};
+// The dK/dV kernel's bias reader: the thread's key column, one 2-byte load per query row (b points at
+// b[first query row of the warpgroup's half][key]; ld = the row stride; n = rows inside the sequence).
+struct ColBias {
+    static constexpr bool on = true;
+    const uint16_t* b;
+    long ld;
+    int n;
+    __device__ __forceinline__ void chunk(int ch, uint32_t (&w)[16]) const {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int c = ch * 32 + 2 * e;
+            const uint32_t lo = (b != nullptr && c < n) ? (uint32_t)__ldg(b + (long)c * ld) : 0u;
+            const uint32_t hi = (b != nullptr && c + 1 < n) ? (uint32_t)__ldg(b + (long)(c + 1) * ld) : 0u;
+            w[e] = lo | (hi << 16);
+        }
+    }
+};
 
 template <class ND>
 __device__ __forceinline__ void ds_pass(uint32_t t_dp, int h, ND nd, const float (&pv)[64]) {
@@ -328,7 +384,7 @@ struct BwdShared {
 __device__ __forceinline__ uint32_t region_s(int n) { return (uint32_t)((2 * n) % 3) * 128u; }
 __device__ __forceinline__ uint32_t region_dp(int n) { return (uint32_t)((2 * n + 1) % 3) * 128u; }
 
-template <int D, bool AL>
+template <int D, bool AL, bool BM>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -481,10 +537,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
             const float base = (float)(i - (long)t * BT);
             wait_bounded(bar(Q_SFULL + (it & 1)), (it >> 1) & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            if (t < full_begin || t >= full_end)
-                exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
-            else
-                exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+            if constexpr (BM) {  // the bias row of this query row over the warpgroup's 64 columns
+                const size_t plane = (size_t)(p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a);
+                const long c0 = (long)t * BT + wg * HALF;
+                const RowBias rb{i < p.S ? p.bias + (plane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr,
+                                 (int)min((long)HALF, (long)p.S - c0)};
+                if (t < full_begin || t >= full_end)
+                    exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv, rb);
+                else
+                    exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv, rb);
+            } else {
+                if (t < full_begin || t >= full_end)
+                    exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+                else
+                    exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+            }
             wait_bounded(bar(Q_DPFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
             ds_pass(t_lane + region_dp(it), wg, nd, pv);
@@ -545,7 +612,7 @@ enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMP
              KV_HDONE = KV_PDONE + 2, KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
 static_assert(KV_NBAR <= 24, "barrier slots");
 
-template <int D, bool AL>
+template <int D, bool AL, bool BM>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = KvCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -701,10 +768,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
             wait_bounded(bar(KV_QFULL + st), (it >> 1) & 1, wd, ERR_COMPUTE);  // the column vectors
             wait_bounded(bar(KV_SFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
-            if (qt < full_begin || qt >= full_end)
-                exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
-            else
-                exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+            if constexpr (BM) {  // the bias column of this key over the warpgroup's 64 query rows
+                const int a_it = iter_head(it) - b * p.Hq;
+                const size_t plane = (size_t)(p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a_it);
+                const long r0 = (long)qt * BT + wg * HALF;
+                const ColBias cbias{j < p.S ? p.bias + (plane * (size_t)p.S + (size_t)r0) * (size_t)p.bias_ld + j : nullptr,
+                                    p.bias_ld, (int)min((long)HALF, (long)p.S - r0)};
+                if (qt < full_begin || qt >= full_end)
+                    exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv, cbias);
+                else
+                    exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv, cbias);
+            } else {
+                if (qt < full_begin || qt >= full_end)
+                    exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+                else
+                    exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+            }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(KV_PDONE + wg));
@@ -755,33 +834,47 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int D, bool AL>
+template <int D, bool AL, bool BM>
 cudaError_t launch_dq(const BwdParams& p, int n_items, cudaStream_t stream) {
-    cudaError_t e = configure(attn_bwd_dq_kernel<D, AL>, DqCfg<D>::SMEM_ALLOC);
+    cudaError_t e = configure(attn_bwd_dq_kernel<D, AL, BM>, DqCfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_bwd_dq_kernel<D, AL><<<n_items, NTHREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(p);
+    attn_bwd_dq_kernel<D, AL, BM><<<n_items, NTHREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, bool AL>
+template <int D, bool AL, bool BM>
 cudaError_t launch_dkdv(const BwdParams& p, int n_ctas, cudaStream_t stream) {
-    cudaError_t e = configure(attn_bwd_dkdv_kernel<D, AL>, KvCfg<D>::SMEM_ALLOC);
+    cudaError_t e = configure(attn_bwd_dkdv_kernel<D, AL, BM>, KvCfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<D, AL><<<n_ctas, NTHREADS, KvCfg<D>::SMEM_ALLOC, stream>>>(p);
+    attn_bwd_dkdv_kernel<D, AL, BM><<<n_ctas, NTHREADS, KvCfg<D>::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BwdParams& p, int n_items, cudaStream_t stream) {
+    if (p.bias) return launch_dq<D, false, true>(p, n_items, stream);
+    if (p.alibi) return launch_dq<D, true, false>(p, n_items, stream);
+    return launch_dq<D, false, false>(p, n_items, stream);
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const BwdParams& p, int n_ctas, cudaStream_t stream) {
+    if (p.bias) return launch_dkdv<D, false, true>(p, n_ctas, stream);
+    if (p.alibi) return launch_dkdv<D, true, false>(p, n_ctas, stream);
+    return launch_dkdv<D, false, false>(p, n_ctas, stream);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
-    if (d == 128) return p.alibi ? launch_dq<128, true>(p, n_items, stream) : launch_dq<128, false>(p, n_items, stream);
-    if (d == 64) return p.alibi ? launch_dq<64, true>(p, n_items, stream) : launch_dq<64, false>(p, n_items, stream);
+    if (d == 128) return launch_dq_d<128>(p, n_items, stream);
+    if (d == 64) return launch_dq_d<64>(p, n_items, stream);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, int n_ctas, cudaStream_t stream) {
     if (n_ctas <= 0) return cudaSuccess;
-    if (d == 128) return p.alibi ? launch_dkdv<128, true>(p, n_ctas, stream) : launch_dkdv<128, false>(p, n_ctas, stream);
-    if (d == 64) return p.alibi ? launch_dkdv<64, true>(p, n_ctas, stream) : launch_dkdv<64, false>(p, n_ctas, stream);
+    if (d == 128) return launch_dkdv_d<128>(p, n_ctas, stream);
+    if (d == 64) return launch_dkdv_d<64>(p, n_ctas, stream);
     return cudaErrorInvalidValue;
 }
 

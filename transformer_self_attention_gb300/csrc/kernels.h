@@ -126,6 +126,9 @@ struct BwdParams {
     const float* nlse2;   // [B*Hq, S_pad]: -LSE * log2(e); -inf past S
     const float* nd;      // [B*Hq, S_pad]: -D = -dO . O; 0 past S
     const float* alibi;   // [Hq] ALiBi slopes of the forward (device), or null
+    const uint16_t* bias; // the forward's bias matrix (bf16 bits [bias_Bb, bias_Hb, S, bias_ld]), or null
+    int bias_Bb, bias_Hb;
+    long bias_ld;
     int* err;
     long long watchdog_ns;
 };
