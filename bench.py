@@ -557,7 +557,8 @@ def cpu_baseline_backward(w: wl.Workload, target_s: float = 12.0, n_slices: int 
             b, g = divmod(k % (w.B * w.Hkv), w.Hkv)
             qs = slice(g * group, (g + 1) * group)
             oracle.backward(Qf[b:b + 1, qs], Kf[b:b + 1, g:g + 1], Vf[b:b + 1, g:g + 1], dOf[b:b + 1, qs], w.scale,
-                            w.kind, w.window, alibi=None if sb[0] is None else sb[0][qs],
+                            w.kind, w.window, globals_idx=list(w.globals_idx),
+                            alibi=None if sb[0] is None else sb[0][qs],
                             bias=None if sb[1] is None else sb[1][:, qs])
         return time.perf_counter() - t0
 
@@ -621,7 +622,8 @@ def run_ours_backward(args, w):
     Qc, Kc, Vc = wl.make_inputs(w)
     dOc = wl.make_grad_output(w)
     Q, K, V, dO = (t.to(dev) for t in (Qc, Kc, Vc, dOc))
-    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(w.globals_idx))
     if args.alibi:
         plan.set_alibi(wl.alibi_slopes(w.Hq))
     if args.bias:  # the forward's per-head bias matrix, resident in HBM; both passes read it

@@ -208,6 +208,25 @@ attn_status attn_bwd_dq_schedule_host(int B, int Hq, int Hkv, int S, int d_k, at
                                       int* items, int cap, int* n_items);
 
 /*
+ * attn_bwd_lg_lists_host -- the per-tile lists both backward kernels walk under
+ * ATTN_MASK_LOCAL_GLOBAL (host only).  The mask |i - j| <= window, or i in G, or j in G
+ * ("Transformer 演进与变体" (ai.icyfenix.cn), section 稀疏注意力: global tokens attend
+ * to and are attended by every position) is symmetric, so one list per tile index x
+ * (0 <= x < n_tiles = ceil(S / ATTN_TILE)) gives both the key tiles of query tile x (dQ)
+ * and the query tiles of key tile x (dK, dV): ascending, every tile t holding at least
+ * one allowed pair against x, each entry t | ATTN_LIST_FULL when every pair of the two
+ * tiles lies inside [0, S) and is allowed.
+ *   globals  : global positions (any order, duplicates allowed), each in [0, S).
+ *   list     : output, room for `cap` entries; may be NULL with cap = 0 to query n_list.
+ *   offsets  : output, n_tiles + 1 ints (entries of tile x: offsets[x] .. offsets[x+1]-1);
+ *              may be NULL when cap = 0.
+ * Errors: ATTN_ERR_INVALID_ARG (bad S, window or position; cap nonzero but too small).
+ */
+#define ATTN_LIST_FULL (1 << 16)
+attn_status attn_bwd_lg_lists_host(int S, int window, const int* globals, int n_global, int* list, int cap,
+                                   int* offsets, int* n_list);
+
+/*
  * attn_poll_device_error -- synchronise the device, read the handle's device
  * error word into *code (0 = none, otherwise a bit set of the role whose
  * bounded wait ran out), clear it, and return ATTN_ERR_DEVICE_TIMEOUT if it
@@ -298,9 +317,11 @@ attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long 
  * on Q or K, so each enters only the recomputed P).
  * Enqueued on `stream`; the first call allocates the handle's backward scratch
  * (2 * B*Hq*ceil(S/128)*128 floats and the key-tile schedule).
+ * Under ATTN_MASK_LOCAL_GLOBAL both kernels walk per-tile lists of partner tiles
+ * (attn_bwd_lg_lists_host) with the window plus the global rows and columns as a bit
+ * mask; a global row's dQ and a global key's dK, dV take every position.
  * Errors: ATTN_ERR_INVALID_ARG (NULL or misaligned pointer); ATTN_ERR_UNSUPPORTED
- * (dtype other than ATTN_BF16, or LOCAL_GLOBAL);
- * ATTN_ERR_OOM; ATTN_ERR_CUDA.
+ * (dtype other than ATTN_BF16); ATTN_ERR_OOM; ATTN_ERR_CUDA.
  */
 attn_status attn_backward(attn_handle h, const void* Q, const void* K, const void* V, const void* O,
                           const float* LSE, const void* dO, void* dQ, void* dK, void* dV, void* stream);

@@ -28,7 +28,8 @@ KINDS = (wl.MASK_FULL, wl.MASK_CAUSAL, wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING)
 
 def _plan(w):
     import transformer_self_attention_gb300 as tsa
-    return tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window)
+    return tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype=w.dtype, scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(w.globals_idx))
 
 
 def _run(w, Q, K, V, dO, plan=None, alibi=None):
@@ -44,7 +45,7 @@ def _run(w, Q, K, V, dO, plan=None, alibi=None):
     return dQ, dK, dV, plan
 
 
-def _cmp(name, got, ref):
+def _cmp(name, got, ref, workload=wl.CAUSAL_MHA_4K.name):
     got = got.float().cpu().numpy().astype(np.float64) if torch.is_tensor(got) else got
     assert np.isfinite(got).all(), f"{name}: non-finite (unwritten?) gradient"
     diff = got - ref
@@ -55,7 +56,7 @@ def _cmp(name, got, ref):
     assert mx <= GRAD_MAX_REL, f"{name}: max error {mx:.3e} of max |ref|"
     print(f"GRADERR {name} rel_l2 {rel:.3e} max_rel {mx:.3e}")
     if "every element" in name:
-        REPORT[f"causal_mha_B2_H32_S4096_d128 backward {name}"] = (
+        REPORT[f"{workload} backward {name}"] = (
             f"elements {ref.size}  max |error| / max |gradient| {mx:.3e}  rel-L2 {rel:.3e}")
     return rel, mx
 
@@ -65,7 +66,7 @@ def _check(w, alibi=None):
     dOc = wl.make_grad_output(w)
     dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda(), alibi=alibi)
     ref = oracle.backward(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), dOc.float().numpy(), w.scale,
-                          w.kind, w.window, alibi=alibi)
+                          w.kind, w.window, globals_idx=list(w.globals_idx), alibi=alibi)
     one_key = w.S == 1 or (w.window == 0 and w.kind in (wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING))
     if one_key:
         # every row sees one key (S = 1, or a window of 0): the softmax is the constant 1, so the
@@ -115,14 +116,64 @@ def test_backward_repeated_calls_are_identical():
 
 
 def test_backward_unsupported_configurations():
+    """The backward takes bf16 plans only: an fp32 plan is refused before any launch."""
     import transformer_self_attention_gb300 as tsa
-    w = small("u", 1, 2, 2, 256, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=16, globals_idx=(0,))
+    w = small("u", 1, 2, 2, 256, 64, "f32", wl.MASK_CAUSAL)
     Q, K, V = (t.cuda() for t in wl.make_inputs(w))
-    plan = tsa.Attention(1, 2, 2, 256, 128, kind=wl.MASK_LOCAL_GLOBAL, window=16, global_idx=[0])
+    plan = tsa.Attention(1, 2, 2, 256, 64, dtype="f32", kind=wl.MASK_CAUSAL)
     O, LSE = plan(Q, K, V)
-    with pytest.raises(tsa.AttnError):
+    with pytest.raises(tsa.AttnError) as e:
         plan.backward(Q, K, V, O, LSE, O)
+    assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED
     torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ local + global
+# The window |i - j| <= w plus global tokens that attend to and are attended by every position
+# ("Transformer 演进与变体", section 稀疏注意力).  Both kernels walk per-tile lists with a bit mask;
+# a global row's dQ and a global key's dK, dV sum over every position.
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S,w_,G", [(1, 0, (0,)), (129, 5, (0, 128)), (300, 40, (0, 100, 299)),
+                                    (520, 130, (0, 127, 128, 255, 519)), (700, 64, ())])
+def test_backward_local_global(S, w_, G, d):
+    """Global tokens at the ends and on both sides of tile edges, windows inside and across tiles,
+    no global at all (the plain symmetric window through the list path)."""
+    _check(small("blg", 1, 2, 2, S, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=w_, globals_idx=G))
+
+
+def test_backward_local_global_many_globals_gqa():
+    """129 global tokens (more than a tile of them: every tile holds some, so every list is every
+    tile) and a GQA group of 4: dK and dV of a kv head sum over the group."""
+    _check(small("blgm", 2, 8, 2, 640, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=20,
+                 globals_idx=tuple(range(0, 640, 5))[:129]))
+
+
+def test_backward_local_global_alibi():
+    """ALiBi under local + global: -m_a |i - j| for the window and the global pairs alike."""
+    _check(small("blga", 1, 4, 2, 600, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=(0, 333, 599)),
+           alibi=wl.alibi_slopes(4))
+
+
+def test_backward_local_global_full_size():
+    """The 8K local + global workload (H 12, d 64, w 512, globals 0, 1000, 3000, 6000) at full size:
+    every element of dQ, dK and dV against the oracle, one oracle call per head (exact for MHA),
+    norms over the whole tensors."""
+    w = wl.LONGFORMER_8K
+    assert w.Hq == w.Hkv
+    Qc, Kc, Vc = wl.make_inputs(w)
+    dOc = wl.make_grad_output(w)
+    dQ, dK, dV, _ = _run(w, Qc.cuda(), Kc.cuda(), Vc.cuda(), dOc.cuda())
+    refs = [np.empty(t.shape, dtype=np.float64) for t in (dQ, dK, dV)]
+    for b in range(w.B):
+        for a in range(w.Hq):
+            sl = lambda t: t[b:b + 1, a:a + 1].float().numpy()
+            out = oracle.backward(sl(Qc), sl(Kc), sl(Vc), sl(dOc), w.scale, w.kind, w.window,
+                                  globals_idx=list(w.globals_idx))
+            for r, x in zip(refs, out):
+                r[b:b + 1, a:a + 1] = x
+    for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), refs):
+        _cmp(f"{n} (every element)", g, r, workload=w.name)
 
 
 @pytest.mark.parametrize("S", [1, 129, 300])

@@ -209,6 +209,79 @@ def test_kv_schedule_matches_brute_force(kind, S, w):
     assert np.all(np.diff(lengths) <= 0)
 
 
+def _lg_bwd_kernel_counts(S, w, G, lst, off):
+    """Per row (dQ view: a thread per query row over its list's key tiles) the pairs the
+    backward kernels evaluate as allowed: FULL entries whole, the others through the kernel's
+    bit mask (window interval, the interval [0, S - 1] for a global row, the tile's global
+    columns).  The mask is symmetric and the dK/dV kernel runs the same predicate with rows and
+    columns swapped, so the same counts hold per key column."""
+    isg = np.zeros(S, dtype=bool)
+    isg[list(G)] = True
+    counts = np.zeros(S, dtype=np.int64)
+    for i in range(S):
+        x = i // T
+        lo, hi = max(0, i - w), min(S - 1, i + w)
+        if isg[i]:
+            lo, hi = 0, S - 1
+        for e in lst[off[x]:off[x + 1]]:
+            t = int(e) & (tsa.LIST_FULL - 1)
+            cols = np.arange(t * T, t * T + T)
+            if int(e) & tsa.LIST_FULL:
+                counts[i] += T
+                continue
+            inside = cols < S
+            ok = ((cols >= lo) & (cols <= hi)) | (isg[np.minimum(cols, S - 1)] & inside)
+            counts[i] += int(np.count_nonzero(ok & inside))
+    return counts
+
+
+@pytest.mark.parametrize("S,w,G", [(1, 0, (0,)), (127, 3, (0, 126)), (128, 5, (64,)), (129, 0, (128,)),
+                                   (300, 40, (0, 100, 299)), (520, 130, (0, 127, 128, 255, 519)),
+                                   (700, 200, ()), (640, 63, tuple(range(0, 640, 5)))])
+def test_lg_backward_lists_match_brute_force(S, w, G):
+    """Local + global backward lists against the oracle's enumeration: tile x lists exactly the
+    tiles holding an allowed pair against it, ascending, FULL exactly where the oracle's class is
+    FULL; the kernels' bit-mask predicate over the listed tiles counts every row's allowed pairs
+    exactly once."""
+    lst, off = tsa.attn_bwd_lg_lists_host(S, w, G)
+    n = (S + T - 1) // T
+    assert off.shape == (n + 1,) and off[0] == 0 and off[-1] == lst.size
+    classes = oracle.tile_classes(tsa.MASK_LOCAL_GLOBAL, S, w, list(G))  # [query tile, key tile]
+    assert np.array_equal(classes, classes.T)  # the mask is symmetric
+    for x in range(n):
+        ent = [int(e) for e in lst[off[x]:off[x + 1]]]
+        tiles = [e & (tsa.LIST_FULL - 1) for e in ent]
+        assert tiles == sorted(set(tiles))
+        assert tiles == [t for t in range(n) if classes[x, t] != 0], x
+        for e, t in zip(ent, tiles):
+            assert bool(e & tsa.LIST_FULL) == (classes[x, t] == 1), (x, t)
+    counts = _lg_bwd_kernel_counts(S, w, G, lst, off)
+    assert np.array_equal(counts, oracle.row_counts(tsa.MASK_LOCAL_GLOBAL, S, w, list(G)))
+
+
+def test_lg_backward_lists_of_the_local_global_workload():
+    """The 8K local + global workload (w 512, globals 0, 1000, 3000, 6000): tile classes against
+    the oracle's enumeration; a tile holding a global lists every tile."""
+    w = wl.LONGFORMER_8K
+    lst, off = tsa.attn_bwd_lg_lists_host(w.S, w.window, w.globals_idx)
+    classes = oracle.tile_classes(tsa.MASK_LOCAL_GLOBAL, w.S, w.window, list(w.globals_idx))
+    n = w.S // T
+    gt = {g // T for g in w.globals_idx}
+    for x in range(n):
+        ent = [int(e) for e in lst[off[x]:off[x + 1]]]
+        assert [e & (tsa.LIST_FULL - 1) for e in ent] == [t for t in range(n) if classes[x, t] != 0]
+        assert [bool(e & tsa.LIST_FULL) for e in ent] == [classes[x, t] == 1 for t in range(n) if classes[x, t]]
+        if x in gt:
+            assert len(ent) == n
+
+
+def test_lg_backward_lists_reject_bad_arguments():
+    for S, w, G in ((0, 1, ()), (100, -1, ()), (100, 3, (100,)), (100, 3, (-1,))):
+        with pytest.raises(tsa.AttnError) as e:
+            tsa.attn_bwd_lg_lists_host(S, w, G)
+        assert e.value.status == tsa.ATTN_ERR_INVALID_ARG
+
+
 def test_kv_schedule_rejects_local_global():
     with pytest.raises(tsa.AttnError) as e:
         tsa.attn_kv_schedule_host(300, tsa.MASK_LOCAL_GLOBAL, 5)

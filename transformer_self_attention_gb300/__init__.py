@@ -23,6 +23,7 @@ MASK_FULL, MASK_CAUSAL, MASK_SLIDING, MASK_CAUSAL_SLIDING, MASK_LOCAL_GLOBAL = r
 ATTN_BF16, ATTN_F32, ATTN_FP8_E4M3 = 0, 1, 2
 TILE = 128
 WORK_INTS = 8
+LIST_FULL = 1 << 16  # ATTN_LIST_FULL: the FULL flag of a backward list entry
 WORK_GLOBAL_COLS, WORK_GLOBAL_ROWS, WORK_HAS_GLOBAL_ROWS = 1, 2, 4
 
 EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string", "attn_schedule_host",
@@ -32,7 +33,7 @@ EXPORTED = ("attn_create", "attn_forward", "attn_destroy", "attn_status_string",
             "attn_decode_set_alibi", "attn_set_fp8_descale", "attn_kv_schedule_host",
             "attn_backward", "attn_bwd_dq_schedule_host", "attn_set_bias", "attn_decode_set_merge_mode",
             "attn_decode_launch_count", "attn_selftest_device_once", "attn_forward_noalloc_poll_error",
-            "attn_forward_noalloc_set_watchdog")
+            "attn_forward_noalloc_set_watchdog", "attn_bwd_lg_lists_host")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 DECODE_MAX_BATCH = 1024
 DECODE_MAX_ROWS = 64
@@ -76,6 +77,8 @@ def _load():
     lib.attn_backward.restype = I
     lib.attn_bwd_dq_schedule_host.argtypes = [I, I, I, I, I, I, I, P, I, ctypes.POINTER(I)]
     lib.attn_bwd_dq_schedule_host.restype = I
+    lib.attn_bwd_lg_lists_host.argtypes = [I, I, P, I, P, I, P, ctypes.POINTER(I)]
+    lib.attn_bwd_lg_lists_host.restype = I
     lib.attn_set_bias.argtypes = [P, P, I, I, ctypes.c_long]
     lib.attn_set_bias.restype = I
     lib.attn_decode_set_merge_mode.argtypes = [P, I]
@@ -230,6 +233,24 @@ def attn_kv_schedule_host(S, kind, window=0):
     if st != ATTN_OK:
         raise AttnError(st, "attn_kv_schedule_host")
     return items[: n.value]
+
+
+def attn_bwd_lg_lists_host(S, window, globals_idx):
+    """The backward's per-tile partner lists under local + global (host only): (list, offsets),
+    int32 arrays; entries t | LIST_FULL.  Raises AttnError."""
+    g = np.ascontiguousarray(np.asarray(list(globals_idx), dtype=np.int32).reshape(-1))
+    gp = g.ctypes.data_as(ctypes.c_void_p) if g.size else None
+    n = ctypes.c_int(0)
+    st = _lib.attn_bwd_lg_lists_host(int(S), int(window), gp, int(g.size), None, 0, None, ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_lg_lists_host")
+    lst = np.zeros(max(n.value, 1), dtype=np.int32)
+    off = np.zeros((S + TILE - 1) // TILE + 1, dtype=np.int32)
+    st = _lib.attn_bwd_lg_lists_host(int(S), int(window), gp, int(g.size), lst.ctypes.data_as(ctypes.c_void_p),
+                                     n.value, off.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_lg_lists_host")
+    return lst[: n.value], off
 
 
 def attn_bwd_dq_schedule_host(B, Hq, Hkv, S, d_k, kind, window=0):

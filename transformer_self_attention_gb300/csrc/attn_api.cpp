@@ -40,7 +40,9 @@ struct attn_plan {
     float* d_dvec = nullptr;   // [B*Hq, S_pad]
     int4* d_kvwork = nullptr;  // key-tile items
     int4* d_dqwork = nullptr;  // forward items regrouped by kv head (dQ launch)
+    int* d_bwdlist = nullptr;  // local + global: the per-tile lists of partner tiles
     int n_kv_items = 0;
+    int n_dq_items = 0;
     const void* last_bwd[7] = {};
     attn::BwdParams bp{};
     // tensor maps of the last pointers seen (re-encoded when they change)
@@ -156,7 +158,7 @@ cudaError_t upload(T** dst, const T* src, size_t n) {
 void free_plan(attn_plan* h) {
     if (!h) return;
     void* bufs[] = {h->d_work, h->d_globals, h->d_gbits, h->d_gsplit, h->d_isg, h->d_err, h->d_part, h->d_counters,
-                    h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork};
+                    h->d_alibi, h->d_lse2, h->d_dvec, h->d_kvwork, h->d_dqwork, h->d_bwdlist};
     for (void* b : bufs)
         if (b) cudaFree(b);
     delete h;
@@ -375,6 +377,23 @@ attn_status attn_bwd_dq_schedule_host(int B, int Hq, int Hkv, int S, int d_k, at
     return ATTN_OK;
 }
 
+attn_status attn_bwd_lg_lists_host(int S, int window, const int* globals, int n_global, int* list, int cap,
+                                   int* offsets, int* n_list) {
+    if (!n_list || cap < 0 || (cap > 0 && (!list || !offsets)) || S < 1 || S > (1 << 20) || window < 0 ||
+        n_global < 0 || (n_global > 0 && !globals))
+        return ATTN_ERR_INVALID_ARG;
+    for (int k = 0; k < n_global; ++k)
+        if (globals[k] < 0 || globals[k] >= S) return ATTN_ERR_INVALID_ARG;
+    std::vector<int> l, off;
+    attn::build_lg_pair_lists(S, window, sorted_unique(globals, n_global), &l, &off);
+    *n_list = (int)l.size();
+    if (cap == 0) return ATTN_OK;
+    if (cap < *n_list) return ATTN_ERR_INVALID_ARG;
+    std::memcpy(list, l.data(), l.size() * sizeof(int));
+    std::memcpy(offsets, off.data(), off.size() * sizeof(int));
+    return ATTN_OK;
+}
+
 attn_status attn_poll_device_error(attn_handle h, int* code) {
     if (!h || !code) return ATTN_ERR_INVALID_ARG;
     *code = 0;
@@ -470,7 +489,9 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     for (const void* q : ptrs)
         if (!aligned16(q)) return ATTN_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(LSE) & 3u) return ATTN_ERR_INVALID_ARG;
-    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
+    if (h->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    const bool lg = h->kind == ATTN_MASK_LOCAL_GLOBAL;
+    if (lg && h->tp.bias) return ATTN_ERR_UNSUPPORTED;  // (attn_set_bias refuses it already)
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int nq = (h->S + ATTN_TILE - 1) / ATTN_TILE;
     const int S_pad = nq * ATTN_TILE;
@@ -478,17 +499,27 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     cudaError_t e = cudaSuccess;
     if (!h->d_lse2) {
         const size_t n = (size_t)h->B * h->Hq * S_pad;
-        std::vector<int> items;
-        attn_status st = attn::build_kv_schedule(h->S, h->kind, h->window, &items);
-        if (st != ATTN_OK) return st;
+        std::vector<int> items, dq_items, list;
+        if (lg) {  // both kernels walk per-tile lists (the global rows and columns break the band)
+            std::vector<int> offsets;
+            attn::build_lg_pair_lists(h->S, h->window, h->globals, &list, &offsets);
+            attn::build_lg_bwd_items(h->B, h->Hq, h->Hkv, h->S, h->d, offsets, &dq_items, &items);
+        } else {
+            attn_status st = attn::build_kv_schedule(h->S, h->kind, h->window, &items);
+            if (st != ATTN_OK) return st;
+            dq_items = attn::order_dq_items(h->sched.items, h->sched.n_main, h->Hq, h->Hkv,
+                                            attn::dq_kv_group(h->S, h->d));
+        }
         h->n_kv_items = (int)(items.size() / ATTN_WORK_INTS);
-        const std::vector<int> dq_items = attn::order_dq_items(h->sched.items, h->sched.n_main, h->Hq, h->Hkv,
-                                                               attn::dq_kv_group(h->S, h->d));
+        h->n_dq_items = (int)(dq_items.size() / ATTN_WORK_INTS);
         if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_lse2), n * sizeof(float))) != cudaSuccess ||
             (e = cudaMalloc(reinterpret_cast<void**>(&h->d_dvec), n * sizeof(float))) != cudaSuccess ||
             (e = upload(reinterpret_cast<int**>(&h->d_kvwork), items.data(), items.size())) != cudaSuccess ||
-            (e = upload(reinterpret_cast<int**>(&h->d_dqwork), dq_items.data(), dq_items.size())) != cudaSuccess)
+            (e = upload(reinterpret_cast<int**>(&h->d_dqwork), dq_items.data(), dq_items.size())) != cudaSuccess ||
+            (lg && (e = upload(&h->d_bwdlist, list.data(), list.size())) != cudaSuccess))
             return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;
+        p.list = h->d_bwdlist;
+        p.gbits = lg ? h->d_gbits : nullptr;
         p.S = h->S; p.S_pad = S_pad; p.Hq = h->Hq; p.Hkv = h->Hkv; p.group = h->Hq / h->Hkv;
         p.kind = h->kind; p.window = h->window;
         p.scale = h->scale;
@@ -518,8 +549,8 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     pp.nlse2 = h->d_lse2; pp.nd = h->d_dvec;
     pp.BHq = (int)BHq; pp.S = h->S; pp.S_pad = S_pad; pp.d = h->d;
     if ((e = attn::launch_bwd_prep(pp, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-    p.work = h->d_dqwork;  // the forward's first-launch items, grouped by kv head
-    if ((e = attn::launch_bwd_dq(p, h->d, h->sched.n_main, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    p.work = h->d_dqwork;  // one item per (batch x query head, query tile), grouped by kv head
+    if ((e = attn::launch_bwd_dq(p, h->d, h->n_dq_items, stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     p.work = h->d_kvwork;
     p.n_items = h->n_kv_items;
     if ((e = attn::launch_bwd_dkdv(p, h->d, (int)BHkv * h->n_kv_items, stream)) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -88,13 +88,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
-// Allowed key interval [lo, hi] of query row i (interval kinds), and the query interval of key j.
+// Allowed key interval [lo, hi] of query row i, and the query interval of key j: the whole mask for
+// the interval kinds, the window part of it for local + global (whose global rows and columns the
+// kernels add as bits).
 __device__ __forceinline__ void row_band(int kind, int window, long S, long i, long* lo, long* hi) {
     *lo = 0;
     *hi = S - 1;
     if (kind == ATTN_MASK_CAUSAL) *hi = i;
     else if (kind == ATTN_MASK_CAUSAL_SLIDING) { *lo = i - window; *hi = i; }
-    else if (kind == ATTN_MASK_SLIDING) { *lo = i - window; *hi = i + window; }
+    else if (kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_LOCAL_GLOBAL) { *lo = i - window; *hi = i + window; }
     if (*hi > S - 1) *hi = S - 1;
 }
 __device__ __forceinline__ void key_band(int kind, int window, long S, long j, long* lo, long* hi) {
@@ -102,7 +104,7 @@ __device__ __forceinline__ void key_band(int kind, int window, long S, long j, l
     *hi = S - 1;
     if (kind == ATTN_MASK_CAUSAL) *lo = j;
     else if (kind == ATTN_MASK_CAUSAL_SLIDING) { *lo = j; *hi = j + window; }
-    else if (kind == ATTN_MASK_SLIDING) { *lo = j - window; *hi = j + window; }
+    else if (kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_LOCAL_GLOBAL) { *lo = j - window; *hi = j + window; }
     if (*hi > S - 1) *hi = S - 1;
 }
 
@@ -110,6 +112,30 @@ __device__ __forceinline__ void key_band(int kind, int window, long S, long j, l
 __device__ __forceinline__ void tile_interval(long lo, long hi, long c0, int* a0, int* a1) {
     *a0 = (int)max(-1L, min((long)BT, lo - c0));
     *a1 = (int)max(-1L, min((long)BT, hi - c0));
+}
+
+// Bits of the in-tile columns [32k, 32k + 32) that lie inside [a0, a1].
+__device__ __forceinline__ uint32_t interval_word(int a0, int a1, int k) {
+    const int lo = max(a0 - 32 * k, 0), hi = min(a1 - 32 * k + 1, 32);  // [lo, hi)
+    if (hi <= lo) return 0u;
+    const uint32_t up = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    return up & ~((1u << lo) - 1u);
+}
+
+// Whether position x is a global token (local + global): bit x % 32 of word x / 32 of the
+// per-tile global bits (4 words per 128 positions).
+__device__ __forceinline__ bool is_global_pos(const unsigned* gbits, long x) {
+    return (__ldg(gbits + (x >> 5)) >> (x & 31)) & 1u;
+}
+
+// Local + global, a tile that is not FULL: the allowed columns of the warpgroup's half h as two
+// words of bits (columns 64h .. 64h + 31, then 64h + 32 .. 64h + 63) -- the window interval
+// [a0, a1] of the thread's own row (or column) plus the global positions among the tile's
+// columns (or rows), gb = the tile's four words.  An own position that is global has the
+// interval [0, S - 1] already.
+__device__ __forceinline__ uint2 lg_half_bits(int a0, int a1, const unsigned* gb, int h) {
+    return make_uint2(interval_word(a0, a1, 2 * h) | __ldg(gb + 2 * h),
+                      interval_word(a0, a1, 2 * h + 1) | __ldg(gb + 2 * h + 1));
 }
 
 // ------------------------------------------------------------------ pre-pass
@@ -194,11 +220,17 @@ __device__ __forceinline__ void stage_groups(uint8_t* stage, uint32_t t_lane, ui
     }
 }
 
-// Score of in-tile column c, -inf outside the allowed columns [a0, a1] on masked tiles.
-template <bool MASKED>
-__device__ __forceinline__ float masked(uint32_t raw, int c, int a0, int a1) {
-    if (!MASKED) return __uint_as_float(raw);
-    return (c >= a0 && c <= a1) ? __uint_as_float(raw) : -INFINITY;
+// Mask forms of a tile: none (FULL), the interval [a0, a1] of in-tile columns, or column bits
+// (local + global: bit c % 32 of the word of the column's 32-column chunk).
+enum { MK_NONE = 0, MK_INTERVAL = 1, MK_BITS = 2 };
+
+// Score of in-tile column c, -inf where the tile's mask form excludes it (w: the bits of the
+// column's chunk).
+template <int MK>
+__device__ __forceinline__ float masked(uint32_t raw, int c, int a0, int a1, uint32_t w) {
+    if (MK == MK_NONE) return __uint_as_float(raw);
+    if (MK == MK_INTERVAL) return (c >= a0 && c <= a1) ? __uint_as_float(raw) : -INFINITY;
+    return ((w >> (c & 31)) & 1u) ? __uint_as_float(raw) : -INFINITY;
 }
 
 // The element-wise work of one warpgroup on its half of a tile (columns 64h .. 64h+63 of the
@@ -235,9 +267,9 @@ struct NoBias {
     static constexpr bool on = false;
     __device__ __forceinline__ void chunk(int, uint32_t (&)[16]) const {}
 };
-template <bool MASKED, bool STORE_P, bool AL, class NL, class BV = NoBias>
-__device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, float mL, float base,
-                                         float (&pv)[64], BV bias = BV{}) {
+template <int MK, bool STORE_P, bool AL, class NL, class BV = NoBias>
+__device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, int a0, int a1, uint2 mw, float mL,
+                                         float base, float (&pv)[64], BV bias = BV{}) {
     const float2 sl = make_float2(sl2, sl2);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
@@ -263,8 +295,9 @@ __device__ __forceinline__ void exp_pass(uint32_t t_s, int h, float sl2, NL nl, 
                     add = __ffma2_rn(make_float2(__uint_as_float(wv << 16), __uint_as_float(wv & 0xffff0000u)),
                                      make_float2(LOG2E, LOG2E), add);
                 }
-                const float2 x = __ffma2_rn(make_float2(masked<MASKED>(s[k], cb + k, a0, a1),
-                                                        masked<MASKED>(s[k + 1], cb + k + 1, a0, a1)),
+                const uint32_t w = ch ? mw.y : mw.x;
+                const float2 x = __ffma2_rn(make_float2(masked<MK>(s[k], cb + k, a0, a1, w),
+                                                        masked<MK>(s[k + 1], cb + k + 1, a0, a1, w)),
                                             sl, add);
                 pv[ch * 32 + k] = ex2(x.x);
                 pv[ch * 32 + k + 1] = ex2(x.y);
@@ -384,7 +417,7 @@ struct BwdShared {
 __device__ __forceinline__ uint32_t region_s(int n) { return (uint32_t)((2 * n) % 3) * 128u; }
 __device__ __forceinline__ uint32_t region_dp(int n) { return (uint32_t)((2 * n + 1) % 3) * 128u; }
 
-template <int D, bool AL, bool BM>
+template <int D, bool AL, bool BM, bool LG>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using C = DqCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -402,6 +435,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
     const int n_iter = kv_end - kv_begin;
     const int b = bh / p.Hq, a = bh - b * p.Hq;
     const int bkv = b * p.Hkv + a / p.group;
+    // key tile of iteration it: a contiguous range, or (local + global) the query tile's list
+    auto key_tile = [&](int it) { return LG ? (__ldg(p.list + kv_begin + it) & (kListFull - 1)) : kv_begin + it; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Q_NBAR; ++i) mbar_init(bar(i), (i == Q_HDONE || i == Q_HDONE + 1) ? 128u : 1u);
@@ -429,7 +464,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
             }
             int k_loaded = 0, v_loaded = 0;
             for (int it = 0; it < n_iter; ++it) {
-                const int row = (kv_begin + it) * BT, ks = it % 3, vs = it & 1;
+                const int row = key_tile(it) * BT, ks = it % 3, vs = it & 1;
                 if (it >= 3 && !wait_bounded(bar(Q_KEMPTY + ks), (it / 3 - 1) & 1, wd, ERR_PRODUCER)) break;
                 mbar_arrive_expect_tx(bar(Q_KFULL + ks), C::TB);
                 for (int s = 0; s < D / 64; ++s)
@@ -528,29 +563,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dq_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         long lo, hi;
         row_band(p.kind, p.window, p.S, i, &lo, &hi);
+        if (LG && i < p.S && is_global_pos(p.gbits, i)) { lo = 0; hi = p.S - 1; }  // a global row sees every key
         const float mL = AL ? p.alibi[a] * LOG2E : 0.f;  // ALiBi slope of this query head, log2 units
         float pv[64];
         for (int it = 0; it < n_iter; ++it) {
-            const int t = kv_begin + it;
+            const int e = LG ? __ldg(p.list + kv_begin + it) : 0;
+            const int t = LG ? (e & (kListFull - 1)) : kv_begin + it;
+            const bool full = LG ? (e & kListFull) != 0 : (t >= full_begin && t < full_end);
             int a0, a1;
             tile_interval(lo, hi, (long)t * BT, &a0, &a1);
+            // local + global: the window interval plus the tile's global keys, as bits
+            const uint2 bw = (LG && !full) ? lg_half_bits(a0, a1, p.gbits + 4 * t, wg) : make_uint2(0u, 0u);
             const float base = (float)(i - (long)t * BT);
             wait_bounded(bar(Q_SFULL + (it & 1)), (it >> 1) & 1, wd, ERR_COMPUTE);
             tc_fence_after();
+            constexpr int MKP = LG ? MK_BITS : MK_INTERVAL;  // the mask form of the tiles that are not FULL
             if constexpr (BM) {  // the bias row of this query row over the warpgroup's 64 columns
                 const size_t plane = (size_t)(p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a);
                 const long c0 = (long)t * BT + wg * HALF;
                 const RowBias rb{i < p.S ? p.bias + (plane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr,
                                  (int)min((long)HALF, (long)p.S - c0)};
-                if (t < full_begin || t >= full_end)
-                    exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv, rb);
+                if (!full)
+                    exp_pass<MKP, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, bw, mL, base, pv, rb);
                 else
-                    exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv, rb);
+                    exp_pass<MK_NONE, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, bw, mL, base, pv, rb);
             } else {
-                if (t < full_begin || t >= full_end)
-                    exp_pass<true, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+                if (!full)
+                    exp_pass<MKP, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, bw, mL, base, pv);
                 else
-                    exp_pass<false, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, mL, base, pv);
+                    exp_pass<MK_NONE, false, AL>(t_lane + region_s(it), wg, sl2, nl, a0, a1, bw, mL, base, pv);
             }
             wait_bounded(bar(Q_DPFULL), it & 1, wd, ERR_COMPUTE);
             tc_fence_after();
@@ -612,7 +653,7 @@ enum KvBar { KV_LOAD = 0, KV_QFULL, KV_QEMPTY = KV_QFULL + 2, KV_SFULL = KV_QEMP
              KV_HDONE = KV_PDONE + 2, KV_DONE = KV_HDONE + 2, KV_DRAIN, KV_NBAR };
 static_assert(KV_NBAR <= 24, "barrier slots");
 
-template <int D, bool AL, bool BM>
+template <int D, bool AL, bool BM, bool LG>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using C = KvCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -632,7 +673,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
     const int n_iter = p.group * n_q;  // query heads of the group x query tiles
     const int b = bkv / p.Hkv, g = bkv - b * p.Hkv;
     auto iter_head = [&](int it) { return b * p.Hq + g * p.group + it / n_q; };
-    auto iter_qtile = [&](int it) { return q_begin + it % n_q; };
+    // query tile of iteration it: a contiguous range, or (local + global) the key tile's list
+    auto iter_entry = [&](int it) { return LG ? __ldg(p.list + q_begin + it % n_q) : q_begin + it % n_q; };
+    auto iter_qtile = [&](int it) { return LG ? (iter_entry(it) & (kListFull - 1)) : q_begin + it % n_q; };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < KV_NBAR; ++i) {
@@ -755,12 +798,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
         const float sl2 = p.scale_log2;
         long ilo, ihi;
         key_band(p.kind, p.window, p.S, j, &ilo, &ihi);
+        if (LG && j < p.S && is_global_pos(p.gbits, j)) { ilo = 0; ihi = p.S - 1; }  // a global key is seen by every row
         if (j >= p.S) { ilo = 1; ihi = 0; }  // a padding key sees no row
         float pv[64];
         for (int it = 0; it < n_iter; ++it) {
             const int st = it & 1, qt = iter_qtile(it);
+            const bool full = LG ? (iter_entry(it) & kListFull) != 0 : (qt >= full_begin && qt < full_end);
             int a0, a1;
             tile_interval(ilo, ihi, (long)qt * BT, &a0, &a1);
+            // local + global: the window interval plus the tile's global rows, as bits (none for a
+            // padding key)
+            uint2 bw = (LG && !full) ? lg_half_bits(a0, a1, p.gbits + 4 * qt, wg) : make_uint2(0u, 0u);
+            if (j >= p.S) bw = make_uint2(0u, 0u);
+            constexpr int MKP = LG ? MK_BITS : MK_INTERVAL;  // the mask form of the tiles that are not FULL
             const uint32_t vec = s_vec + st * 1024;  // -LSE log2 e of the tile's 128 query rows, then -D
             // ALiBi: the slope of this iteration's query head; |i - j| = |c - (j - first row of the tile)|
             const float mL = AL ? p.alibi[iter_head(it) - b * p.Hq] * LOG2E : 0.f;
@@ -774,15 +824,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_bwd_dkdv_kernel(const __grid
                 const long r0 = (long)qt * BT + wg * HALF;
                 const ColBias cbias{j < p.S ? p.bias + (plane * (size_t)p.S + (size_t)r0) * (size_t)p.bias_ld + j : nullptr,
                                     p.bias_ld, (int)min((long)HALF, (long)p.S - r0)};
-                if (qt < full_begin || qt >= full_end)
-                    exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv, cbias);
+                if (!full)
+                    exp_pass<MKP, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, bw, mL, base, pv, cbias);
                 else
-                    exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv, cbias);
+                    exp_pass<MK_NONE, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, bw, mL, base, pv, cbias);
             } else {
-                if (qt < full_begin || qt >= full_end)
-                    exp_pass<true, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+                if (!full)
+                    exp_pass<MKP, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, bw, mL, base, pv);
                 else
-                    exp_pass<false, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, mL, base, pv);
+                    exp_pass<MK_NONE, true, AL>(t_s, wg, sl2, ColVec{vec}, a0, a1, bw, mL, base, pv);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -834,34 +884,45 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <int D, bool AL, bool BM>
+template <int D, bool AL, bool BM, bool LG>
 cudaError_t launch_dq(const BwdParams& p, int n_items, cudaStream_t stream) {
-    cudaError_t e = configure(attn_bwd_dq_kernel<D, AL, BM>, DqCfg<D>::SMEM_ALLOC);
+    cudaError_t e = configure(attn_bwd_dq_kernel<D, AL, BM, LG>, DqCfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_bwd_dq_kernel<D, AL, BM><<<n_items, NTHREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(p);
+    attn_bwd_dq_kernel<D, AL, BM, LG><<<n_items, NTHREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, bool AL, bool BM>
+template <int D, bool AL, bool BM, bool LG>
 cudaError_t launch_dkdv(const BwdParams& p, int n_ctas, cudaStream_t stream) {
-    cudaError_t e = configure(attn_bwd_dkdv_kernel<D, AL, BM>, KvCfg<D>::SMEM_ALLOC);
+    cudaError_t e = configure(attn_bwd_dkdv_kernel<D, AL, BM, LG>, KvCfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_bwd_dkdv_kernel<D, AL, BM><<<n_ctas, NTHREADS, KvCfg<D>::SMEM_ALLOC, stream>>>(p);
+    attn_bwd_dkdv_kernel<D, AL, BM, LG><<<n_ctas, NTHREADS, KvCfg<D>::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
+// local + global (p.list set): plain or with ALiBi; a bias matrix is not taken with it
 template <int D>
 cudaError_t launch_dq_d(const BwdParams& p, int n_items, cudaStream_t stream) {
-    if (p.bias) return launch_dq<D, false, true>(p, n_items, stream);
-    if (p.alibi) return launch_dq<D, true, false>(p, n_items, stream);
-    return launch_dq<D, false, false>(p, n_items, stream);
+    if (p.list) {
+        if (p.bias) return cudaErrorInvalidValue;
+        if (p.alibi) return launch_dq<D, true, false, true>(p, n_items, stream);
+        return launch_dq<D, false, false, true>(p, n_items, stream);
+    }
+    if (p.bias) return launch_dq<D, false, true, false>(p, n_items, stream);
+    if (p.alibi) return launch_dq<D, true, false, false>(p, n_items, stream);
+    return launch_dq<D, false, false, false>(p, n_items, stream);
 }
 
 template <int D>
 cudaError_t launch_dkdv_d(const BwdParams& p, int n_ctas, cudaStream_t stream) {
-    if (p.bias) return launch_dkdv<D, false, true>(p, n_ctas, stream);
-    if (p.alibi) return launch_dkdv<D, true, false>(p, n_ctas, stream);
-    return launch_dkdv<D, false, false>(p, n_ctas, stream);
+    if (p.list) {
+        if (p.bias) return cudaErrorInvalidValue;
+        if (p.alibi) return launch_dkdv<D, true, false, true>(p, n_ctas, stream);
+        return launch_dkdv<D, false, false, true>(p, n_ctas, stream);
+    }
+    if (p.bias) return launch_dkdv<D, false, true, false>(p, n_ctas, stream);
+    if (p.alibi) return launch_dkdv<D, true, false, false>(p, n_ctas, stream);
+    return launch_dkdv<D, false, false, false>(p, n_ctas, stream);
 }
 
 cudaError_t launch_bwd_dq(const BwdParams& p, int d, int n_items, cudaStream_t stream) {

@@ -129,9 +129,15 @@ struct BwdParams {
     const uint16_t* bias; // the forward's bias matrix (bf16 bits [bias_Bb, bias_Hb, S, bias_ld]), or null
     int bias_Bb, bias_Hb;
     long bias_ld;
+    // local + global: the per-tile lists of partner tiles (entries t | kListFull when every pair
+    // of the two tiles is allowed; the items index them) and the global positions as 4 words of
+    // bits per 128-position tile; null otherwise
+    const int* list;
+    const unsigned* gbits;
     int* err;
     long long watchdog_ns;
 };
+constexpr int kListFull = ATTN_LIST_FULL;  // the FULL flag of a list entry (the tile index is below it)
 struct BwdPrepParams {
     const uint16_t* o; const uint16_t* dout;  // bf16 bits [B*Hq, S, d]
     const float* lse;                          // [B*Hq, S] (natural log)

@@ -257,6 +257,66 @@ std::vector<int> order_dq_items(const std::vector<int>& items, int n_items, int 
     return out;
 }
 
+void build_lg_pair_lists(int S, int window, const std::vector<int>& globals, std::vector<int>* list,
+                         std::vector<int>* offsets) {
+    const int n = (S + T - 1) / T;
+    RowBand band{ATTN_MASK_LOCAL_GLOBAL, S, window};
+    std::vector<int> is_g(S, 0), cntG(S + 1, 0);
+    for (int g : globals) is_g[g] = 1;
+    for (int x = 0; x < S; ++x) cntG[x + 1] = cntG[x] + is_g[x];
+    auto globals_in = [&](long a, long b) -> long { return b < a ? 0 : cntG[b + 1] - cntG[a]; };
+    list->clear();
+    offsets->assign((size_t)n + 1, 0);
+    for (int x = 0; x < n; ++x) {
+        const long r0 = (long)x * T, r1 = std::min<long>(S, r0 + T) - 1;
+        const bool x_has_g = globals_in(r0, r1) > 0;
+        const int band_lo = (int)(band.lo(r0) / T), band_hi = (int)(band.hi(r1) / T);  // inclusive
+        for (int t = 0; t < n; ++t) {
+            const long c0 = (long)t * T, c1 = c0 + T - 1, c1s = std::min<long>(c1, S - 1);
+            const bool t_has_g = globals_in(c0, c1s) > 0;
+            if (!x_has_g && !t_has_g && (t < band_lo || t > band_hi)) continue;
+            // every pair allowed: both tiles whole, and each row global or its window plus the
+            // global columns covering [c0, c1]
+            bool full = r0 + T - 1 < S && c1 < S;
+            for (long i = r0; i <= r0 + T - 1 && full; ++i) {
+                if (is_g[i]) continue;
+                const long lo = band.lo(i), hi = band.hi(i);
+                const long a1 = c0, b1 = std::min(c1, lo - 1), a2 = std::max(c0, hi + 1), b2 = c1;
+                long need = 0, have = 0;
+                if (b1 >= a1) { need += b1 - a1 + 1; have += globals_in(a1, b1); }
+                if (b2 >= a2) { need += b2 - a2 + 1; have += globals_in(a2, b2); }
+                full = need == have;
+            }
+            list->push_back(t | (full ? ATTN_LIST_FULL : 0));
+        }
+        (*offsets)[(size_t)x + 1] = (int)list->size();
+    }
+}
+
+void build_lg_bwd_items(int B, int Hq, int Hkv, int S, int d_k, const std::vector<int>& offsets, std::vector<int>* dq_items,
+                        std::vector<int>* kv_items) {
+    const int n = (int)offsets.size() - 1;
+    std::vector<int> order(n);
+    for (int x = 0; x < n; ++x) order[x] = x;
+    // longest first; equal length -> tile order
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+        return offsets[x + 1] - offsets[x] > offsets[y + 1] - offsets[y];
+    });
+    kv_items->clear();
+    for (int x : order) {
+        const int it[ATTN_WORK_INTS] = {x, offsets[x], offsets[x + 1], 0, 0, 0, 0, 0};
+        kv_items->insert(kv_items->end(), it, it + ATTN_WORK_INTS);
+    }
+    std::vector<int> q;
+    q.reserve((size_t)n * B * Hq * ATTN_WORK_INTS);
+    for (int x : order)
+        for (int bh = 0; bh < B * Hq; ++bh) {
+            const int it[ATTN_WORK_INTS] = {bh, x, offsets[x], offsets[x + 1], 0, 0, 0, 0};
+            q.insert(q.end(), it, it + ATTN_WORK_INTS);
+        }
+    *dq_items = order_dq_items(q, n * B * Hq, Hq, Hkv, dq_kv_group(S, d_k));
+}
+
 void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi) {
     *lo = kind == ATTN_MASK_CAUSAL_SLIDING ? std::max(0, L - S_q - window) / T : 0;
     *hi = (L + T - 1) / T;

@@ -51,6 +51,22 @@ attn_status build_kv_schedule(int S, int kind, int window, std::vector<int>* ite
 // number of kv heads whose K and V (2 S d_k bf16 each) fit in 32 MB.  Longest first within
 // a group, as in the forward order.
 int dq_kv_group(int S, int d_k);
+
+// Backward under LOCAL_GLOBAL.  The mask |i - j| <= w or i in G or j in G is symmetric in i and j,
+// so one list per tile index x serves both kernels: the key tiles of query tile x (dQ) and the
+// query tiles of key tile x (dK, dV).  For every x in [0, ceil(S/128)) the list holds, ascending,
+// every tile t with at least one allowed pair against x -- the band tiles, the tiles holding a
+// global position, and every tile when x holds one -- each as t | (ATTN_LIST_FULL if every pair
+// of the two tiles lies inside the sequence and is allowed).  offsets[x] .. offsets[x + 1] - 1
+// index the entries of x.
+void build_lg_pair_lists(int S, int window, const std::vector<int>& globals, std::vector<int>* list,
+                         std::vector<int>* offsets);
+// The items of both backward kernels over these lists (ATTN_WORK_INTS ints each):
+//   dQ    [b * Hq + a, q_tile, list_begin, list_end, 0, 0, 0, 0], longest first, then grouped by
+//         kv head as order_dq_items does;
+//   dK/dV [kv_tile, list_begin, list_end, 0, 0, 0, 0, 0], longest first.
+void build_lg_bwd_items(int B, int Hq, int Hkv, int S, int d_k, const std::vector<int>& offsets, std::vector<int>* dq_items,
+                        std::vector<int>* kv_items);
 std::vector<int> order_dq_items(const std::vector<int>& items, int n_items, int Hq, int Hkv, int kv_group);
 
 // Decode: key tiles per sequence and the size of the persistent grid
