@@ -39,6 +39,42 @@ def test_bf16_d128_kinds_and_ragged_lengths(kind, S):
     _full_compare(small("s", 1, 2, 2, S, 128, "bf16", kind, window=37, globals_idx=G))
 
 
+@pytest.mark.parametrize("S", [1, 63, 64, 65, 127, 129, 191, 193, 300])
+@pytest.mark.parametrize("kind", K_ALL)
+def test_bf16_d64_kinds_and_ragged_lengths(kind, S):
+    """d = 64 runs 64-key tiles (four CTAs per SM): lengths on both sides of 64-key boundaries, the
+    band trimmed to the rows' interval, FULL decided per warp."""
+    G = sorted({0, S // 2, S - 1}) if kind == wl.MASK_LOCAL_GLOBAL else ()
+    _full_compare(small("s64", 1, 2, 2, S, 64, "bf16", kind, window=37, globals_idx=G))
+
+
+@pytest.mark.parametrize("w_", [0, 31, 63, 64, 65, 191, 192])
+@pytest.mark.parametrize("kind", [wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING, wl.MASK_LOCAL_GLOBAL])
+def test_bf16_d64_windows_straddling_64_key_edges(kind, w_):
+    G = (0, 200, 449) if kind == wl.MASK_LOCAL_GLOBAL else ()
+    _full_compare(small("w64", 1, 2, 1, 450, 64, "bf16", kind, window=w_, globals_idx=G))
+
+
+def test_bf16_d64_sharp_softmax_triggers_rescale():
+    """Scores growing along the row force the lazy O rescale on many 64-key tiles."""
+    w = small("sharp64", 1, 2, 2, 1000, 64, "bf16", wl.MASK_CAUSAL)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    ramp = torch.linspace(0, 6, w.S).view(1, 1, w.S, 1)
+    Kc = (Kc.float() + ramp * Qc.float().mean(dim=2, keepdim=True).sign()).to(torch.bfloat16)
+    Qc = (Qc.float() * 3).to(torch.bfloat16)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    O_ref, L_ref = oracle_rows(w, Qc, Kc, Vc, all_rows(w))
+    compare(w, *gather_rows(O, LSE), O_ref, L_ref)
+
+
+def test_bf16_d64_window_zero_returns_own_value_row():
+    """w = 0 with 64-key tiles: each row sees only itself, so O_i = v_i exactly."""
+    w = small("w0_64", 1, 2, 2, 300, 64, "bf16", wl.MASK_SLIDING, window=0)
+    Qc, Kc, Vc = wl.make_inputs(w)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    assert torch.equal(O.cpu(), Vc)
+
+
 @pytest.mark.parametrize("Hkv", [1, 2, 8])
 @pytest.mark.parametrize("d", [64, 128])
 def test_bf16_gqa_and_mqa(Hkv, d):

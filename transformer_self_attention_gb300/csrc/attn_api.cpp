@@ -287,11 +287,11 @@ attn_status attn_forward(attn_handle h, const void* Q, const void* K, const void
             h->last_q = Q;
         }
         if (K != h->last_k) {
-            if (!in_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
+            if (!in_map(&p.tm_k, K, h->d, h->S, (long)h->B * h->Hkv, attn::tc_kv_box_rows(h->d))) return ATTN_ERR_CUDA;
             h->last_k = K;
         }
         if (V != h->last_v) {
-            if (!in_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv, kTileRows)) return ATTN_ERR_CUDA;
+            if (!in_map(&p.tm_v, V, h->d, h->S, (long)h->B * h->Hkv, attn::tc_kv_box_rows(h->d))) return ATTN_ERR_CUDA;
             h->last_v = V;
         }
         if (O != h->last_o) {

@@ -31,8 +31,8 @@
 // its own instantiation (LG):
 //   * a query tile's global keys outside its band of key tiles are gathered by the
 //     producer warp (plain loads into the swizzled layout) into narrow key tiles of
-//     32, 64, 96 or 128 columns, every column allowed for every row, taken before the
-//     band tiles;
+//     32, 64, 96 or 128 columns (at most the kernel's tile width), every column allowed
+//     for every row, taken before the band tiles;
 //   * the global rows are computed by their own items against every key, split into key
 //     chunks; each chunk writes a partial result and the last chunk of a row tile to
 //     finish (an arrival counter) merges them into O and LSE;
@@ -53,7 +53,7 @@ namespace {
 using namespace ptx;
 
 constexpr int BM = 128;            // query rows per CTA
-constexpr int BN = 128;            // keys per tile
+constexpr int KT = 128;            // keys per tile of the host schedule (a kernel tile is KT or KT / 2 keys)
 constexpr int NTHREADS = 192;      // 4 softmax warps + producer + MMA
 constexpr int WARP_PRODUCER = 4;
 constexpr int WARP_MMA = 5;
@@ -65,26 +65,42 @@ enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 // causal kinds, added by the tensor core (see the MMA role); 3 a given bias matrix b_ij.
 enum { BIAS_NONE = 0, BIAS_ALIBI_ELEM = 1, BIAS_ALIBI_MMA = 2, BIAS_MATRIX = 3 };
 
-template <int D, int BIAS = BIAS_NONE, bool F8 = false>
+// BN_: keys per kernel tile.  128 everywhere except d = 64 without a score bias, which takes 64-key
+// tiles: S (64 columns) and O (64) then fit in 128 tensor-memory columns, so four CTAs -- four
+// S -> softmax -> PV chains -- share an SM instead of two.  At d = 64 a 128-key tile carries half the
+// products of d = 128 but the same softmax and hand-off latency, and two chains leave the tensor pipe
+// idle most of the time.
+template <int D, int BIAS = BIAS_NONE, bool F8 = false, int BN_ = 128>
 struct Cfg {
+    static_assert(BN_ == 128 || (BN_ == 64 && D == 64 && BIAS == BIAS_NONE && !F8), "64-key tiles: d = 64, bf16, no bias");
+    static constexpr int BN = BN_;                // keys per kernel tile
+    static constexpr int SUBT = KT / BN;          // kernel tiles per schedule tile
     static constexpr int EB = F8 ? 1 : 2;         // bytes per element (E4M3 or bf16)
-    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 128-byte swizzled block
+    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 128-byte swizzled block (Q, O staging)
+    static constexpr int KV_SUB = BN * 128;       // the same for a K / V tile of BN rows
     static constexpr int XW = 128 / EB;           // elements per 128-byte row of a block
     static constexpr int NSUB = D / XW;           // blocks per row
-    static constexpr int TILE_BYTES = BM * D * EB; // one Q / K / V tile
+    static constexpr int TILE_BYTES = BM * D * EB; // one Q tile
+    static constexpr int KV_BYTES = BN * D * EB;  // one K / V tile
+    // rows of the K / V tensor maps' box (the host encodes 64 at d = 64, 128 otherwise); a tile of BN
+    // rows is BN / KV_BOX copies per 64-column block
+    static constexpr int KV_BOX = (D == 64) ? 64 : 128;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + TILE_BYTES;
-    static constexpr int OFF_V = OFF_K + TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + KV_BYTES;
     // BIAS_ALIBI_MMA: a ones block and a bias block, each 128 rows x 16 bf16 (K-major, no swizzle)
     static constexpr int OFF_BA = OFF_BAR + 1024;
     static constexpr int OFF_BB = OFF_BA + 4096;
     static constexpr int SMEM_USED = (BIAS == BIAS_ALIBI_MMA) ? OFF_BB + 4096 : OFF_BAR + 128;
-    // at least ~80 KB so no more than two CTAs share an SM (tensor memory holds two)
-    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > 82 * 1024) ? SMEM_USED + 1024 : 82 * 1024;
-    static constexpr uint32_t TMEM_COLS = 256;
+    // CTAs per SM: as many as tensor memory holds (two of 256 columns, or four of 128); the shared
+    // memory request keeps the count from going higher (a CTA beyond them would wait for its columns)
+    static constexpr int CTAS_PER_SM = (BN == 64) ? 4 : 2;
+    static constexpr int SMEM_MIN = (BN == 64) ? 46 * 1024 : 82 * 1024;
+    static constexpr int SMEM_ALLOC = (SMEM_USED + 1024 > SMEM_MIN) ? SMEM_USED + 1024 : SMEM_MIN;
+    static constexpr uint32_t TMEM_COLS = (BN == 64) ? 128 : 256;
     static constexpr uint32_t TMEM_S = 0;
-    static constexpr uint32_t TMEM_O = 128;
+    static constexpr uint32_t TMEM_O = BN;
 };
 
 // B_PFULL / B_PFULL1: the first / second half of P (keys 0-63 / 64-127) is in tensor memory.
@@ -143,7 +159,7 @@ __device__ __forceinline__ bool spin_bounded(uint32_t bar, uint32_t parity, Shar
 }
 
 // Mask of one PARTIAL tile as seen by one query row: the allowed in-tile columns are
-// [a0, a1] (clamped to [-1, BN]) plus the global keys of the tile.  w0..w3 hold them as
+// [a0, a1] (clamped to [-1, tile width]) plus the global keys of the tile.  w0..w3 hold them as
 // one bit per column (filled for the MASK_ANY form only), so that testing a column is one
 // bit test and one select.
 struct TileMask {
@@ -178,15 +194,15 @@ __device__ __forceinline__ float tile_score(uint32_t raw, int c, const TileMask&
     return tile_allowed(c, mk) ? __uint_as_float(raw) : -INFINITY;
 }
 
-// Row maximum of the (masked) raw scores of this thread's row, columns [0, BN):
+// Row maximum of the (masked) raw scores of this thread's row, columns [0, NB):
 // three-input max instructions, eight independent chains.
-template <int MASKED>
+template <int MASKED, int NB = 128>
 __device__ __forceinline__ float tile_row_max(uint32_t t_s, const TileMask& mk) {
     float m8[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < NB / 64; ++h) {
         uint32_t r0[32], r1[32];
         tmem_ld32(t_s + h * 64, r0);
         tmem_ld32(t_s + h * 64 + 32, r1);
@@ -243,6 +259,43 @@ __device__ __forceinline__ float tile_exp_store(uint32_t t_s, const TileMask& mk
             pk[16 + e] = pack_bf16x2(p2, p3);
         }
         tmem_st32(t_s + h * 32, pk);
+        if (h == 0) {
+            fix();
+            release_first_half(bar_half);
+        }
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+// tile_exp_store for 64-key tiles: halves of 32 keys (S columns [32h, 32h + 32) in, bf16 P columns
+// [16h, 16h + 16) out, again only over S columns already read), the first half announced on
+// bar_half after fix().
+template <int MASKED, typename FixO>
+__device__ __forceinline__ float tile_exp_store_n64(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                                   uint32_t bar_half, FixO&& fix) {
+    const float2 sl2x2 = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(t_s + h * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int c = h * 32 + 4 * e;
+            const float2 x01 = __ffma2_rn(make_float2(tile_score<MASKED>(r[4 * e], c, mk),
+                                                      tile_score<MASKED>(r[4 * e + 1], c + 1, mk)),
+                                          sl2x2, nref);
+            const float2 x23 = __ffma2_rn(make_float2(tile_score<MASKED>(r[4 * e + 2], c + 2, mk),
+                                                      tile_score<MASKED>(r[4 * e + 3], c + 3, mk)),
+                                          sl2x2, nref);
+            const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+            acc0 = __fadd2_rn(acc0, make_float2(p0, p1));
+            acc1 = __fadd2_rn(acc1, make_float2(p2, p3));
+            pk[2 * e] = pack_bf16x2(p0, p1);
+            pk[2 * e + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(t_s + h * 16, pk);
         if (h == 0) {
             fix();
             release_first_half(bar_half);
@@ -415,19 +468,20 @@ __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMa
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// Rows pos(r), r < n_rows, of one [S, D] bf16 head copied with plain loads into a 128-row tile in
-// the layout the TMA loads write (128-byte swizzle: 64-column blocks of BM * 128 bytes, the 16-byte
-// chunk c of row r at chunk position c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32 lanes of
-// one warp take part.
+// Rows pos(r), r < n_rows, of one [S, D] bf16 head copied with plain loads into a tile of `rows`
+// rows in the layout the TMA loads write (128-byte swizzle: 64-column blocks of rows * 128 bytes, the
+// 16-byte chunk c of row r at chunk position c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32
+// lanes of one warp take part.
 template <int D, class Pos>
-__device__ __forceinline__ void gather_rows(uint8_t* tile, const uint16_t* head, int n_rows, Pos pos, int lane) {
+__device__ __forceinline__ void gather_rows(uint8_t* tile, int rows, const uint16_t* head, int n_rows, Pos pos,
+                                            int lane) {
     constexpr int CH = D / 8;  // 16-byte chunks per row
     for (int e = lane; e < n_rows * CH; e += 32) {
         const int r = e / CH, c = e - r * CH;
         const long j = pos(r);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (j >= 0) v = __ldg(reinterpret_cast<const uint4*>(head + j * D) + c);
-        *reinterpret_cast<uint4*>(tile + (c >> 3) * (BM * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(tile + (c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
 }
 
@@ -553,49 +607,60 @@ __device__ __forceinline__ void store_row_direct(uint32_t t_o, void* dst_row, fl
     }
 }
 
-// One global row from its key chunks.  Chunk c holds O_c (its own softmax-weighted average, fp32)
-// and LSE_c (natural log of its sum of exponentials), so with M = max_c LSE_c the row is
+// One global row from its key chunks, merged by one warp.  Chunk c holds O_c (its own
+// softmax-weighted average, fp32) and LSE_c (natural log of its sum of exponentials), so with
+// M = max_c LSE_c the row is
 //   O = sum_c e^(LSE_c - M) O_c / sum_c e^(LSE_c - M),   LSE = M + ln sum_c e^(LSE_c - M):
-// the softmax normalisation carried across chunks.  The partials were written by other CTAs, so
-// they are read through L2 (ld.global.cg).
+// the softmax normalisation carried across chunks.  The lanes split the chunks for M and the
+// weights, then the columns (D / 32 each) for the weighted sum, with four chunks' loads in
+// flight.  The partials were written by other CTAs, so they are read through L2 (ld.global.cg).
 template <int D>
-__device__ __forceinline__ void merge_global_row(const TcParams& p, size_t slot0, void* dst_row, float* lse_out) {
+__device__ __forceinline__ void merge_global_row(const TcParams& p, size_t slot0, void* dst_row, float* lse_out,
+                                                 int lane) {
+    constexpr int CPL = D / 32;  // columns per lane
     float M = -INFINITY;
-    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, __ldcg(p.part_lse + slot0 + c));
+    for (int c = lane; c < p.n_chunks; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot0 + c));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float acc[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = 0.f;
     float W = 0.f;
-    for (int c = 0; c < p.n_chunks; ++c) W += expf(__ldcg(p.part_lse + slot0 + c) - M);
-    const float inv_w = W > 0.f ? 1.f / W : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(dst_row);
-#pragma unroll 1
-    for (int cb = 0; cb < D; cb += 32) {
-        float acc[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-        for (int c = 0; c < p.n_chunks; ++c) {
-            const float w = expf(__ldcg(p.part_lse + slot0 + c) - M);
-            const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot0 + c) * D + cb);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = __ldcg(src + q);
-                acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
-                acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+    for (int c0 = 0; c0 < p.n_chunks; c0 += 32) {
+        const int nc = min(32, p.n_chunks - c0);
+        // lane k holds the weight of chunk c0 + k
+        const float wl = lane < nc ? expf(__ldcg(p.part_lse + slot0 + c0 + lane) - M) : 0.f;
+        W += wl;
+#pragma unroll 4
+        for (int k = 0; k < nc; ++k) {
+            const float w = __shfl_sync(0xffffffffu, wl, k);
+            const float* src = p.part_o + (slot0 + c0 + k) * D + lane * CPL;
+            if constexpr (CPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+                acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
             }
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            dst[cb / 8 + q] = make_uint4(pack_bf16x2(acc[8 * q] * inv_w, acc[8 * q + 1] * inv_w),
-                                         pack_bf16x2(acc[8 * q + 2] * inv_w, acc[8 * q + 3] * inv_w),
-                                         pack_bf16x2(acc[8 * q + 4] * inv_w, acc[8 * q + 5] * inv_w),
-                                         pack_bf16x2(acc[8 * q + 6] * inv_w, acc[8 * q + 7] * inv_w));
     }
-    if (lse_out) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+    const float inv_w = W > 0.f ? 1.f / W : 0.f;
+    if constexpr (CPL == 4) {
+        reinterpret_cast<uint2*>(dst_row)[lane] =
+            make_uint2(pack_bf16x2(acc[0] * inv_w, acc[1] * inv_w), pack_bf16x2(acc[2] * inv_w, acc[3] * inv_w));
+    } else {
+        reinterpret_cast<uint32_t*>(dst_row)[lane] = pack_bf16x2(acc[0] * inv_w, acc[1] * inv_w);
+    }
+    if (lse_out && lane == 0) *lse_out = W > 0.f ? M + logf(W) : -INFINITY;
 }
 
-template <int D, int BIAS, bool F8, bool LG>
-__global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
-    using C = Cfg<D, BIAS, F8>;
+template <int D, int BIAS, bool F8, bool LG, int BN>
+__global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
+    attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+    using C = Cfg<D, BIAS, F8, BN>;
     constexpr bool ALIBI = BIAS == BIAS_ALIBI_ELEM;  // the per-element bias passes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -614,15 +679,43 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     const int bh = w0.x, q_tile = w0.y, kv_begin = w0.z, kv_end = w0.w;
     const int full_begin = w1.x, full_end = w1.y, flags = w1.z, n_gt = w1.w;
     const bool grows = LG && (flags & ATTN_WORK_GLOBAL_ROWS) != 0;
-    const int n_band = kv_end - kv_begin;
-    // local + global: the gathered key tiles (n_gat of them) run first, then the band tiles
-    const int n_gat = (LG && (flags & ATTN_WORK_GLOBAL_COLS)) ? n_gt : 0;
+    // Band key tiles, in kernel tiles of BN keys: the schedule's tiles [kv_begin, kv_end) of KT keys.
+    // With 64-key tiles the ends are trimmed to what the rows can see: the query tile's key interval
+    // (interval kinds; local + global keeps the schedule's band, outside which its globals are
+    // gathered) and, for every item, the sequence end.
+    int t_begin = kv_begin * C::SUBT, t_end = kv_end * C::SUBT;
+    if constexpr (BN < KT) {
+        t_end = min(t_end, (p.S + BN - 1) / BN);
+        if (!LG) {
+            const long r0 = (long)q_tile * BM, r1 = min(r0 + BM, (long)p.S) - 1;
+            long lo0 = 0, hi1 = p.S - 1;
+            if (p.kind == ATTN_MASK_CAUSAL) hi1 = r1;
+            else if (p.kind == ATTN_MASK_CAUSAL_SLIDING) { lo0 = max(0L, r0 - p.window); hi1 = r1; }
+            else if (p.kind == ATTN_MASK_SLIDING) { lo0 = max(0L, r0 - p.window); hi1 = min((long)p.S - 1, r1 + p.window); }
+            t_begin = max(t_begin, (int)(lo0 / BN));
+            t_end = min(t_end, (int)(hi1 / BN) + 1);
+        }
+    }
+    const int n_band = t_end - t_begin;
+    // local + global: the gathered key tiles (n_gat of them, BN keys at most) run before the band tiles,
+    // so that the producer warp's plain loads of their rows overlap the copy of the Q tile (measured
+    // 3% faster than running them last).  The globals outside the band are G[0, g_lo) and
+    // G[g_hi, n_G) (the schedule's split).
+    const bool gcols_item = LG && (flags & ATTN_WORK_GLOBAL_COLS);
+    const int2 gs = gcols_item ? __ldg(p.gsplit + q_tile) : make_int2(0, p.n_global);
+    const int g_lo = gs.x, g_hi = gs.y;
+    const int n_out = g_lo + (p.n_global - g_hi);
+    const int n_gat = gcols_item ? (n_out + BN - 1) / BN : 0;
     const int n_iter = n_band + n_gat;
-    // Band key tile of iteration n_gat + it.  With the causal ALiBi bias the tiles run from the
+    constexpr bool GATHER_FIRST = true;
+    auto is_gathered = [&](int it) { return LG && (GATHER_FIRST ? it < n_gat : it >= n_band); };
+    auto gat_index = [&](int it) { return GATHER_FIRST ? it : it - n_band; };    // gathered tile of iteration it
+    auto band_index = [&](int it) { return GATHER_FIRST ? it - n_gat : it; };   // band position of iteration it
+    // Band key tile at band position it.  With the causal ALiBi bias the tiles run from the
     // diagonal downwards: the bias is 0 at j = i and falls with the distance, so a row's running
     // max is set by its first tile and the lazy rescale stays rare.
     constexpr bool REV = BIAS == BIAS_ALIBI_MMA;
-    auto band_tile = [&](int it) { return REV ? kv_end - 1 - it : kv_begin + it; };
+    auto band_tile = [&](int it) { return REV ? t_end - 1 - it : t_begin + it; };
     const int b = bh / p.Hq, a = bh - b * p.Hq;
     const int bkv = b * p.Hkv + a / p.group;  // g(a) = a / (Hq / Hkv)
 
@@ -666,13 +759,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
-    // gathered key tiles: n_out global keys lie outside the band, G[0, g_lo) before it and
-    // G[g_hi, nG) after it (the schedule's split of G for this query tile); tile it < n_gat holds
-    // the outside keys it * BN .. it * BN + cols(it) - 1, padded to a multiple of 32 columns
-    const int2 gs = n_gat ? __ldg(p.gsplit + q_tile) : make_int2(0, p.n_global);
-    const int g_lo = gs.x, g_hi = gs.y;
-    const int n_out = g_lo + (p.n_global - g_hi);
-    auto gathered_cols = [&](int it) { return min(BN, n_out - it * BN); };
+    // gathered key tiles: tile g < n_gat holds the outside keys g * BN .. g * BN + cols(g) - 1,
+    // padded to a multiple of 32 columns
+    auto gathered_cols = [&](int g) { return min(BN, n_out - g * BN); };
     auto outside_key = [&](int e) -> long { return __ldg(p.globals + (e < g_lo ? e : g_hi + (e - g_lo))); };
 
     if (LG && warp == WARP_PRODUCER) {
@@ -683,7 +772,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         // overlap the copy of the Q tile.
         if (grows) {  // query rows G[q_tile * BM + r]; rows past the list are zero
             const int r0 = q_tile * BM;
-            gather_rows<D>(smem + C::OFF_Q, p.q + (size_t)bh * p.S * D, BM,
+            gather_rows<D>(smem + C::OFF_Q, BM, p.q + (size_t)bh * p.S * D, BM,
                            [&](int r) -> long { return r0 + r < p.n_global ? (long)__ldg(p.globals + r0 + r) : -1L; },
                            lane);
             fence_proxy_async_smem();
@@ -696,12 +785,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         int k_loaded = 0, v_loaded = 0;
         bool ok = true;
         for (int it = 0; it < n_iter && ok; ++it) {
-            const bool in_band = it >= n_gat;
-            const int row = in_band ? band_tile(it - n_gat) * BN : 0;
-            // gathered tiles: the outside keys it * BN + r, r < ncols, padded with zero rows
-            const int gcols = in_band ? 0 : gathered_cols(it);
+            const bool in_band = !is_gathered(it);
+            const int row = in_band ? band_tile(band_index(it)) * BN : 0;
+            // gathered tile g: the outside keys g * BN + r, r < ncols, padded with zero rows
+            const int gcols = in_band ? 0 : gathered_cols(gat_index(it));
             const int grows_pad = (gcols + 31) & ~31;
-            auto gpos = [&](int r) -> long { return r < gcols ? outside_key(it * BN + r) : -1L; };
+            auto gpos = [&](int r) -> long { return r < gcols ? outside_key(gat_index(it) * BN + r) : -1L; };
             if (it > 0) {
                 bool w = true;
                 if (lane == 0) w = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER);
@@ -709,11 +798,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             }
             if (in_band) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
-                    for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, &p.tm_k, bar(B_KFULL), s * C::XW, row, bkv);
+                    mbar_arrive_expect_tx(bar(B_KFULL), C::KV_BYTES);
+                    for (int s = 0; s < C::NSUB; ++s)
+                        for (int r = 0; r < BN; r += C::KV_BOX)
+                            tma_load_3d(s_k + s * C::KV_SUB + r * 128, &p.tm_k, bar(B_KFULL), s * C::XW, row + r, bkv);
                 }
             } else {
-                gather_rows<D>(smem + C::OFF_K, p.k + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                gather_rows<D>(smem + C::OFF_K, BN, p.k + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_KFULL));
@@ -727,11 +818,13 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             if (p.withhold_v) continue;
             if (in_band) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
-                    for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, &p.tm_v, bar(B_VFULL), s * C::XW, row, bkv);
+                    mbar_arrive_expect_tx(bar(B_VFULL), C::KV_BYTES);
+                    for (int s = 0; s < C::NSUB; ++s)
+                        for (int r = 0; r < BN; r += C::KV_BOX)
+                            tma_load_3d(s_v + s * C::KV_SUB + r * 128, &p.tm_v, bar(B_VFULL), s * C::XW, row + r, bkv);
                 }
             } else {
-                gather_rows<D>(smem + C::OFF_V, p.v + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                gather_rows<D>(smem + C::OFF_V, BN, p.v + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_VFULL));
@@ -760,15 +853,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 const CUtensorMap* vm = &p.tm_v;
                 const int row = band_tile(it) * BN;
                 if (it > 0 && !(ok = wait_bounded(bar(B_KEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
-                mbar_arrive_expect_tx(bar(B_KFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_k + s * C::SUB, km, bar(B_KFULL), s * C::XW, row, bkv);
+                mbar_arrive_expect_tx(bar(B_KFULL), C::KV_BYTES);
+                for (int s = 0; s < C::NSUB; ++s)
+                    for (int r = 0; r < BN; r += C::KV_BOX)
+                        tma_load_3d(s_k + s * C::KV_SUB + r * 128, km, bar(B_KFULL), s * C::XW, row + r, bkv);
                 ++k_loaded;
                 if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
                     tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
                 if (it > 0 && !(ok = wait_bounded(bar(B_VEMPTY), (it - 1) & 1, sh, p, ERR_PRODUCER))) break;
                 if (p.withhold_v) continue;
-                mbar_arrive_expect_tx(bar(B_VFULL), C::TILE_BYTES);
-                for (int s = 0; s < C::NSUB; ++s) tma_load_3d(s_v + s * C::SUB, vm, bar(B_VFULL), s * C::XW, row, bkv);
+                mbar_arrive_expect_tx(bar(B_VFULL), C::KV_BYTES);
+                for (int s = 0; s < C::NSUB; ++s)
+                    for (int r = 0; r < BN; r += C::KV_BOX)
+                        tma_load_3d(s_v + s * C::KV_SUB + r * 128, vm, bar(B_VFULL), s * C::XW, row + r, bkv);
                 ++v_loaded;
             }
             if (sh->abort) {  // let the copies this thread issued land before the CTA exits
@@ -792,17 +889,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 // execute in issue order, so QK(it) overwrites P(it-1) only after PV(it-1) read it.
                 tc_fence_after();
                 // a gathered-key tile is ncols wide (a multiple of 32): N = ncols for S, K = ncols for P V
-                const bool narrow = LG && it < n_gat;
-                const int ncols = narrow ? (gathered_cols(it) + 31) & ~31 : BN;
+                const bool narrow = is_gathered(it);
+                const int ncols = narrow ? (gathered_cols(gat_index(it)) + 31) & ~31 : BN;
                 const uint32_t idesc_s = narrow ? idesc_bf16_f32(BM, ncols, false) : idesc_qk;
 #pragma unroll
                 for (int k = 0; k < D / KS; ++k) {
-                    const uint32_t off = (k >> 2) * C::SUB + (k & 3) * 32;
+                    const uint32_t offq = (k >> 2) * C::SUB + (k & 3) * 32, offk = (k >> 2) * C::KV_SUB + (k & 3) * 32;
                     if constexpr (F8)
-                        mma_ss_f8(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
+                        mma_ss_f8(t_s, sdesc_sw128(s_q + offq, 16, 1024), sdesc_sw128(s_k + offk, 16, 1024), idesc_s,
                                   k > 0);
                     else
-                        mma_ss(t_s, sdesc_sw128(s_q + off, 16, 1024), sdesc_sw128(s_k + off, 16, 1024), idesc_s,
+                        mma_ss(t_s, sdesc_sw128(s_q + offq, 16, 1024), sdesc_sw128(s_k + offk, 16, 1024), idesc_s,
                                k > 0);
                 }
                 if constexpr (BIAS == BIAS_ALIBI_MMA)
@@ -820,17 +917,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
 #pragma unroll
                 for (int k = 0; k < BN / KS; ++k) {
                     if (k * KS >= ncols) break;
-                    if (!narrow && k == BN / KS / 2) {  // the second half of P (keys 64-127)
+                    if (!narrow && k == BN / KS / 2) {  // the second half of P (keys BN/2 .. BN-1)
                         if (!(ok = spin_bounded(bar(B_PFULL1), it & 1, sh, p, ERR_MMA))) break;
                         tc_fence_after();
                     }
                     // P: KS keys = 8 tensor-memory columns (2 bf16 or 4 E4M3 per column);
                     // V: KS key rows of 128 B each (MN-major: d runs along the row)
                     if constexpr (F8)
-                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
+                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::KV_SUB, 1024), idesc_pv,
                                   (it > 0 || k > 0) ? 1u : 0u);
                     else
-                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::SUB, 1024), idesc_pv,
+                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::KV_SUB, 1024), idesc_pv,
                                (it > 0 || k > 0) ? 1u : 0u);
                 }
                 if (!ok) {  // half of this PV was issued: track it so the drain below covers it
@@ -881,7 +978,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
         for (int it = 0; it < n_iter; ++it) {
             uint4 bv[BIAS == BIAS_MATRIX ? 16 : 1];  // this row's bias for the tile (issued before the S wait)
             if constexpr (BIAS == BIAS_MATRIX) {
-                const long c0 = (long)band_tile(it - n_gat) * BN;
+                const long c0 = (long)band_tile(band_index(it)) * BN;
                 const uint16_t* brow =
                     (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr;
                 load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
@@ -890,35 +987,52 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             // not depend on S, so it is worked out before the wait for S (the global-key bits of a
             // local + global tile are loaded here and merged in after the wait).
             bool partial = true;
-            const bool gathered = LG && it < n_gat;
+            const bool gathered = is_gathered(it);
             int gcols = BN;      // gathered tiles: columns holding keys (all allowed: they lie outside the band)
             TileMask mk{0, -1, 0u, 0u, 0u, 0u};
             uint4 g4 = make_uint4(0u, 0u, 0u, 0u);
             if (!gathered) {
-                const int t = band_tile(it - n_gat);
-                partial = t < full_begin || t >= full_end;
+                const int t = band_tile(band_index(it));
+                const long c0 = (long)t * BN;
+                if constexpr (BN == KT) {
+                    partial = t < full_begin || t >= full_end;
+                } else {
+                    // 64-key tiles: FULL when every row of the warp (rows past the sequence or the
+                    // global list are never stored) sees the whole tile through its window interval;
+                    // decided per warp, as the mask forms are
+                    partial = !__all_sync(0xffffffffu, !row_valid || (lo <= c0 && hi >= c0 + BN - 1));
+                }
                 if (partial) {
-                    const long c0 = (long)t * BN;
                     mk.a0 = (int)max(-1L, min((long)BN, lo - c0));
                     mk.a1 = (int)max(-1L, min((long)BN, hi - c0));
-                    if (lg) g4 = __ldg(reinterpret_cast<const uint4*>(p.global_bits + 4 * t));
+                    if (lg) {
+                        if constexpr (BN == KT) {
+                            g4 = __ldg(reinterpret_cast<const uint4*>(p.global_bits + 4 * t));
+                        } else {  // the tile's 64 positions are words 2t, 2t + 1 of the per-tile bits
+                            const uint2 g2 = __ldg(reinterpret_cast<const uint2*>(p.global_bits + 2 * t));
+                            g4 = make_uint4(g2.x, g2.y, 0u, 0u);
+                        }
+                    }
                 }
             } else {
-                gcols = gathered_cols(it);
+                gcols = gathered_cols(gat_index(it));
                 mk.a1 = gcols - 1;
             }
             // no lower bound inside the tile (causal diagonal tiles, the upper edge of a window): the
-            // cheap mask form, when every row of the warp qualifies (not for local + global, whose
-            // tiles may hold global keys)
-            const bool upper = !lg && !gathered && __all_sync(0xffffffffu, partial && mk.a0 <= 0);
+            // cheap mask form, when every row of the warp qualifies (for local + global only on tiles
+            // holding no global key, whose columns past the window would be allowed)
+            const bool no_gkeys = !lg || (g4.x | g4.y | g4.z | g4.w) == 0u;
+            const bool upper = no_gkeys && !gathered && __all_sync(0xffffffffu, partial && mk.a0 <= 0);
             // the general form (and every partial tile of the biased passes, which take no other form):
             // the interval and the global keys as column bits
             const bool bits = partial && !gathered && (!upper || BIAS != BIAS_NONE);
             if (bits) {
                 mk.w0 = interval_word(mk.a0, mk.a1, 0);
                 mk.w1 = interval_word(mk.a0, mk.a1, 1);
-                mk.w2 = interval_word(mk.a0, mk.a1, 2);
-                mk.w3 = interval_word(mk.a0, mk.a1, 3);
+                if constexpr (BN == KT) {
+                    mk.w2 = interval_word(mk.a0, mk.a1, 2);
+                    mk.w3 = interval_word(mk.a0, mk.a1, 3);
+                }
             }
             // warp-uniform exit: the tensor-memory accesses below are warp-collective
             if (!__all_sync(0xffffffffu, wait_bounded(bar(B_SFULL), it & 1, sh, p, ERR_SOFTMAX))) {
@@ -933,9 +1047,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             float mx;
             float base = 0.f;  // ALiBi: i - (first key of this tile); band tiles only (no local + global)
             // gathered tile under ALiBi: the key position of column c (the padding columns are masked)
-            auto gpos_f = [&](int c) -> float { return c < gcols ? (float)outside_key(it * BN + c) : 0.f; };
+            auto gpos_f = [&](int c) -> float { return c < gcols ? (float)outside_key(gat_index(it) * BN + c) : 0.f; };
             if constexpr (ALIBI) {
-                base = (float)(i - (long)band_tile(it - n_gat) * BN);
+                base = (float)(i - (long)band_tile(band_index(it)) * BN);
                 if (LG && gathered)
                     mx = narrow_row_max_alibi(t_s, (gcols + 31) >> 5, mk.a1, sl2, mL, (float)i, gpos_f);
                 else if (causal_kind)
@@ -950,16 +1064,16 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 if constexpr (LG) {
                     if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
                     else
-                        mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                             : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                        mx = !partial ? tile_row_max<MASK_NONE, BN>(t_s, mk)
+                             : upper ? tile_row_max<MASK_UPPER, BN>(t_s, mk) : tile_row_max<MASK_ANY, BN>(t_s, mk);
                 } else {
-                    mx = !partial ? tile_row_max<MASK_NONE>(t_s, mk)
-                         : upper ? tile_row_max<MASK_UPPER>(t_s, mk) : tile_row_max<MASK_ANY>(t_s, mk);
+                    mx = !partial ? tile_row_max<MASK_NONE, BN>(t_s, mk)
+                         : upper ? tile_row_max<MASK_UPPER, BN>(t_s, mk) : tile_row_max<MASK_ANY, BN>(t_s, mk);
                 }
                 mx *= sl2;  // scale > 0 keeps the order; -inf stays -inf
                 if constexpr (BIAS == BIAS_ALIBI_MMA) {
                     // the tile's constant part of the bias, m_a (c0 - i), in log2 units
-                    base = mL * (float)((long)band_tile(it - n_gat) * BN - i);
+                    base = mL * (float)((long)band_tile(band_index(it)) * BN - i);
                     mx += base;  // -inf stays -inf
                 }
             }
@@ -1013,6 +1127,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
                 if (LG && gathered)
                     sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, sl2, r_eff, bar(B_PFULL), fix);
+                else if constexpr (BN == 64)
+                    sum = !partial ? tile_exp_store_n64<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                          : upper ? tile_exp_store_n64<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
+                                  : tile_exp_store_n64<MASK_ANY>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix);
                 else
                     sum = !partial ? tile_exp_store<MASK_NONE>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
                           : upper ? tile_exp_store<MASK_UPPER>(t_s, mk, sl2, r_eff, bar(B_PFULL), fix)
@@ -1100,10 +1218,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
             named_bar_sync(1, 128);
             if (sh->merge_last) {
                 __threadfence();
-                if (row_valid)
-                    merge_global_row<D>(p, ((size_t)bh * p.n_global + (q_tile * BM + r)) * p.n_chunks,
-                                        static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + i) * D,
-                                        p.lse ? p.lse + (size_t)bh * p.S + i : nullptr);
+                // one warp per global row of the tile (the four softmax warps take turns)
+                const int n_rows = min(BM, p.n_global - q_tile * BM);
+                for (int rr = warp; rr < n_rows; rr += 4) {
+                    const long ig = __ldg(p.globals + q_tile * BM + rr);
+                    merge_global_row<D>(p, ((size_t)bh * p.n_global + (q_tile * BM + rr)) * p.n_chunks,
+                                        static_cast<__nv_bfloat16*>(p.o) + ((size_t)bh * p.S + ig) * D,
+                                        p.lse ? p.lse + (size_t)bh * p.S + ig : nullptr, lane);
+                }
                 if (threadIdx.x == 0) *counter = 0u;
             }
         }
@@ -1117,12 +1239,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) attn_fwd_tc_kernel(const __grid_c
     }
 }
 
-template <int D, int BIAS, bool F8 = false, bool LG = false>
+template <int D, int BIAS, bool F8 = false, bool LG = false, int BN = 128>
 cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
-    using C = Cfg<D, BIAS, F8>;
-    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8, LG>), C::SMEM_ALLOC);
+    using C = Cfg<D, BIAS, F8, BN>;
+    cudaError_t e = smem_opt_in(reinterpret_cast<const void*>(attn_fwd_tc_kernel<D, BIAS, F8, LG, BN>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    attn_fwd_tc_kernel<D, BIAS, F8, LG><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
+    attn_fwd_tc_kernel<D, BIAS, F8, LG, BN><<<n_items, NTHREADS, C::SMEM_ALLOC, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1153,10 +1275,10 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
         if (d == 64) return launch<64, BIAS_ALIBI_ELEM>(p, n_items, stream);
     } else if (p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0) {  // gathered keys, global-row chunks
         if (d == 128) return launch<128, BIAS_NONE, false, true>(p, n_items, stream);
-        if (d == 64) return launch<64, BIAS_NONE, false, true>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_NONE, false, true, 64>(p, n_items, stream);
     } else {
         if (d == 128) return launch<128, BIAS_NONE>(p, n_items, stream);
-        if (d == 64) return launch<64, BIAS_NONE>(p, n_items, stream);
+        if (d == 64) return launch<64, BIAS_NONE, false, false, 64>(p, n_items, stream);
     }
     return cudaErrorInvalidValue;
 }

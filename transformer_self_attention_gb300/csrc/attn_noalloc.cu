@@ -197,8 +197,9 @@ extern "C" attn_status attn_forward_noalloc(int B, int Hq, int Hkv, int S, int d
 
     attn::TcParams p{};
     constexpr unsigned T = ATTN_TILE;
-    if (!map3d(&p.tm_q, Q, d_k, S, (long)B * Hq, T) || !map3d(&p.tm_k, K, d_k, S, (long)B * Hkv, T) ||
-        !map3d(&p.tm_v, V, d_k, S, (long)B * Hkv, T) || !map3d(&p.tm_o, O, d_k, S, (long)B * Hq, T))
+    const unsigned kvb = attn::tc_kv_box_rows(d_k);
+    if (!map3d(&p.tm_q, Q, d_k, S, (long)B * Hq, T) || !map3d(&p.tm_k, K, d_k, S, (long)B * Hkv, kvb) ||
+        !map3d(&p.tm_v, V, d_k, S, (long)B * Hkv, kvb) || !map3d(&p.tm_o, O, d_k, S, (long)B * Hq, T))
         return ATTN_ERR_CUDA;
     p.work = reinterpret_cast<const int4*>(sc + off_work);
     p.S = S; p.Hq = Hq; p.Hkv = Hkv; p.group = Hq / Hkv;

@@ -14,8 +14,8 @@ namespace attn {
 // as a __grid_constant__ so the TMA descriptors live in parameter space.
 struct TcParams {
     CUtensorMap tm_q;    // Q  [B*Hq,  S, d] bf16, box {64, 128, 1}, 128B swizzle
-    CUtensorMap tm_k;    // K  [B*Hkv, S, d]
-    CUtensorMap tm_v;    // V  [B*Hkv, S, d]
+    CUtensorMap tm_k;    // K  [B*Hkv, S, d], box {64, tc_kv_box_rows(d), 1}
+    CUtensorMap tm_v;    // V  [B*Hkv, S, d], box {64, tc_kv_box_rows(d), 1}
     CUtensorMap tm_o;    // O  [B*Hq,  S, d] (TMA store)
     const int4* work;    // 4 int4 per work item (attn.h schedule layout)
     int item_offset;     // first work item of this launch
@@ -56,6 +56,10 @@ struct TcParams {
     int bias_Bb, bias_Hb;
     long bias_ld;
 };
+
+// Rows of the box of the forward's K and V tensor maps (tm_k, tm_v): 64 at d = 64, where the
+// tensor-core kernel may take 64-key tiles (a 128-key tile is then two copies), 128 otherwise.
+constexpr unsigned tc_kv_box_rows(int d) { return d == 64 ? 64u : 128u; }
 
 // Parameters of the fp32 CUDA-core kernel.
 struct F32Params {

@@ -150,16 +150,17 @@ attn_status build_schedule(const ScheduleInput& in, Schedule* out) {
     out->n_main = (int)protos.size() * BH;
 
     // dense pass for the global rows: every key, FULL except a ragged last tile.
-    // The key tiles are split into chunks no longer than the longest query-tile item
-    // (one work item each), so the global rows finish alongside the band items of the
-    // same launch; each chunk writes a partial result and the last to finish merges them.
+    // The key tiles are split into chunks of about half the longest query-tile item (one
+    // work item each).  They come after the band items, longest first, and fill the last,
+    // partly empty wave of the launch instead of lengthening it; each chunk writes a partial
+    // result and the last to finish merges them.
     out->n_grows = 0;
     out->n_chunks = 1;
     if (lg && nG > 0) {
         const int full_end = (S % T == 0) ? nk : nk - 1;
         int longest = 1;
         for (const Proto& p : protos) longest = std::max(longest, cost(p));
-        const int per = std::min(nk, longest);
+        const int per = std::max(1, std::min(nk, (longest + 1) / 2));
         const int chunks = (nk + per - 1) / per;  // no empty chunk
         out->n_chunks = chunks;
         for (int c = 0; c < chunks; ++c)
