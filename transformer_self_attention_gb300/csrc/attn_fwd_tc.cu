@@ -1040,6 +1040,15 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 break;
             }
             tc_fence_after();
+            // global-row items: a warp none of whose rows is a global row (padding of the gathered
+            // query tile) has nothing to compute; it still takes part in every phase of the P
+            // barriers.  Its P rows keep stale values, which reach only O rows that are never stored
+            // (the rows of P V are independent of one another).
+            if (LG && grows && !__any_sync(0xffffffffu, row_valid)) {
+                mbar_arrive(bar(B_PFULL));
+                mbar_arrive(bar(B_PFULL1));
+                continue;
+            }
             if (lg && bits) {
                 mk.w0 |= g4.x; mk.w1 |= g4.y; mk.w2 |= g4.z; mk.w3 |= g4.w;
             }
