@@ -1,9 +1,10 @@
 """A given bias matrix b_ij added to the scores (attn_set_bias), GPU vs the fp64 oracle.
 
-Every output is compared on small shapes: the four interval kinds, the four broadcast
-shapes [Bb, Hb] of the bias, ragged lengths with padded rows (the padding holds NaN, so a
-kernel that reads it into a result fails), GQA and both head widths; the causal MHA 4K
-workload runs at full size with a per-head bias, every output.  Bounds: those of the
+Every output is compared on small shapes: every mask kind (local + global with its global keys
+and rows reading the bias at their own positions), the four broadcast shapes [Bb, Hb] of the
+bias, ragged lengths with padded rows (the padding holds NaN, so a kernel that reads it into a
+result fails), GQA and both head widths; the causal MHA 4K and the local + global 8K workloads
+run at full size with a per-head bias, every output.  Bounds: those of the
 bf16 forward (the bias is bf16, exact in the oracle's float32 copy, and adds one fp32
 multiply-add per score).  The backward with the same bias is compared with the fp64 backward
 oracle at the backward's bounds.
@@ -30,7 +31,8 @@ def _bias(Bb, Hb, S, ld, seed, scale=2.0):
 
 def _run(w, bias, Q, K, V):
     import transformer_self_attention_gb300 as tsa
-    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, scale=w.scale, kind=w.kind, window=w.window)
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(w.globals_idx))
     plan.set_bias(bias.cuda())
     O = torch.full_like(Q, float("nan"))
     LSE = torch.full((w.B, w.Hq, w.S), float("nan"), dtype=torch.float32, device=Q.device)
@@ -46,7 +48,7 @@ def _check(w, Bb, Hb, ld, seed=3):
     bias = _bias(Bb, Hb, w.S, ld, seed)
     O, LSE, _ = _run(w, bias, Qc.cuda(), Kc.cuda(), Vc.cuda())
     O_ref, L_ref = oracle.attention(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), w.scale, w.kind,
-                                    w.window, bias=bias.float().numpy())
+                                    w.window, list(w.globals_idx), bias=bias.float().numpy())
     return compare(w, O.float().cpu().numpy(), LSE.cpu().numpy(), O_ref, L_ref)
 
 
@@ -91,12 +93,32 @@ def test_removing_the_bias_restores_the_plain_result():
     compare(w, O2.float().cpu().numpy(), L2.cpu().numpy(), O_ref, L_ref)
 
 
+@pytest.mark.parametrize("Bb,Hb", [(1, 1), (2, 4)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bias_matrix_local_global(d, Bb, Hb):
+    """Local + global: the band tiles read the bias row by row, the gathered global keys one key at
+    a time at their own positions, the global rows (their own items, key chunks merged) their own
+    rows; globals at both ends and on both sides of tile edges."""
+    _check(small("blg", 2, 4, 4, 520, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=40,
+                 globals_idx=(0, 127, 128, 300, 519)), Bb, Hb, ld=520)
+
+
+@pytest.mark.parametrize("S", [1, 129, 300])
+def test_bias_matrix_local_global_lengths(S):
+    G = sorted({0, S // 2, S - 1})
+    _check(small("blgl", 1, 2, 1, S, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=19, globals_idx=G), 1, 2,
+           ld=(S + 7) // 8 * 8 + 8)
+
+
+def test_bias_matrix_local_global_many_globals():
+    """129 global tokens: two gathered key tiles per query tile and two global-row tiles."""
+    _check(small("blgm", 1, 2, 2, 700, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=9,
+                 globals_idx=list(range(3, 700, 5))[:129]), 1, 2, ld=704)
+
+
 def test_bias_matrix_unsupported_and_invalid():
     import transformer_self_attention_gb300 as tsa
     bias = _bias(1, 1, 256, 256, 6).cuda()
-    lg = tsa.Attention(1, 2, 2, 256, 128, kind=wl.MASK_LOCAL_GLOBAL, window=8, global_idx=[0])
-    with pytest.raises(tsa.AttnError):
-        lg.set_bias(bias)
     al = tsa.Attention(1, 2, 2, 256, 128, kind=wl.MASK_CAUSAL)
     al.set_alibi(wl.alibi_slopes(2))
     with pytest.raises(tsa.AttnError):
@@ -127,7 +149,7 @@ def _check_backward(w, Bb, Hb, ld, seed=5):
     torch.cuda.synchronize()
     assert plan.poll_device_error() == (0, 0)
     ref = oracle.backward(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), dOc.float().numpy(), w.scale,
-                          w.kind, w.window, bias=bias.float().numpy())
+                          w.kind, w.window, globals_idx=list(w.globals_idx), bias=bias.float().numpy())
     return [_cmp(n, g, r) for n, g, r in zip(("dQ", "dK", "dV"), (dQ, dK, dV), ref)]
 
 
@@ -184,4 +206,28 @@ def test_bias_matrix_full_size_causal_mha_4k():
     O_ref, L_ref = oracle.attention_rows(Kc.float().numpy(), Vc.float().numpy(), w.Hq, w.scale, w.kind, w.window,
                                          [], Qc.float().numpy().reshape(-1, w.d), rows[:, 0], rows[:, 1],
                                          rows[:, 2], bias=bias.float().numpy())
+    compare(w, *gather_rows(O, LSE), O_ref, L_ref, report=f"{w.name} + bias matrix (every row)")
+
+
+@pytest.mark.parametrize("Bb,Hb", [(1, 1), (2, 4)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_bias_matrix_local_global(d, Bb, Hb):
+    """Backward under local + global with a bias matrix: both kernels walk the partner lists and
+    read b_ij along the row (dQ) or down the column (dK, dV) of every listed tile."""
+    _check_backward(small("bblg", 2, 4, 2, 520, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=40,
+                          globals_idx=(0, 127, 128, 300, 519)), Bb, Hb, ld=520)
+
+
+def test_bias_matrix_full_size_local_global_8k():
+    """The 8K local + global workload (H 12, d 64, w 512, globals 0, 1000, 3000, 6000) with a per-head
+    bias [1, 12, S, S] N(0, 2^2) at full size: every output against the oracle."""
+    w = wl.LONGFORMER_8K
+    Qc, Kc, Vc = wl.make_inputs(w)
+    g = torch.Generator().manual_seed(12)
+    bias = (torch.randn(1, w.Hq, w.S, w.S, generator=g) * 2).to(torch.bfloat16)
+    O, LSE, _ = _run(w, bias, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    rows = all_rows(w)
+    O_ref, L_ref = oracle.attention_rows(Kc.float().numpy(), Vc.float().numpy(), w.Hq, w.scale, w.kind, w.window,
+                                         list(w.globals_idx), Qc.float().numpy().reshape(-1, w.d), rows[:, 0],
+                                         rows[:, 1], rows[:, 2], bias=bias.float().numpy())
     compare(w, *gather_rows(O, LSE), O_ref, L_ref, report=f"{w.name} + bias matrix (every row)")

@@ -473,7 +473,7 @@ attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long 
     }
     if (!aligned16(bias) || (Bb != 1 && Bb != h->B) || (Hb != 1 && Hb != h->Hq) || ld < h->S || ld % 8 != 0)
         return ATTN_ERR_INVALID_ARG;
-    if (h->dtype != ATTN_BF16 || h->kind == ATTN_MASK_LOCAL_GLOBAL || h->tp.alibi) return ATTN_ERR_UNSUPPORTED;
+    if (h->dtype != ATTN_BF16 || h->tp.alibi) return ATTN_ERR_UNSUPPORTED;
     if (!encode_map_bias(&h->tp.tm_bias, bias, ld, h->S, (long)Bb * Hb)) return ATTN_ERR_CUDA;
     h->tp.bias = static_cast<const uint16_t*>(bias);
     h->tp.bias_Bb = Bb;
@@ -491,7 +491,6 @@ attn_status attn_backward(attn_handle h, const void* Q, const void* K, const voi
     if (reinterpret_cast<uintptr_t>(LSE) & 3u) return ATTN_ERR_INVALID_ARG;
     if (h->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
     const bool lg = h->kind == ATTN_MASK_LOCAL_GLOBAL;
-    if (lg && h->tp.bias) return ATTN_ERR_UNSUPPORTED;  // (attn_set_bias refuses it already)
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
     const int nq = (h->S + ATTN_TILE - 1) / ATTN_TILE;
     const int S_pad = nq * ATTN_TILE;

@@ -900,11 +900,11 @@ cudaError_t launch_dkdv(const BwdParams& p, int n_ctas, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// local + global (p.list set): plain or with ALiBi; a bias matrix is not taken with it
+// local + global (p.list set): plain, with ALiBi or with a bias matrix
 template <int D>
 cudaError_t launch_dq_d(const BwdParams& p, int n_items, cudaStream_t stream) {
     if (p.list) {
-        if (p.bias) return cudaErrorInvalidValue;
+        if (p.bias) return launch_dq<D, false, true, true>(p, n_items, stream);
         if (p.alibi) return launch_dq<D, true, false, true>(p, n_items, stream);
         return launch_dq<D, false, false, true>(p, n_items, stream);
     }
@@ -916,7 +916,7 @@ cudaError_t launch_dq_d(const BwdParams& p, int n_items, cudaStream_t stream) {
 template <int D>
 cudaError_t launch_dkdv_d(const BwdParams& p, int n_ctas, cudaStream_t stream) {
     if (p.list) {
-        if (p.bias) return cudaErrorInvalidValue;
+        if (p.bias) return launch_dkdv<D, false, true, true>(p, n_ctas, stream);
         if (p.alibi) return launch_dkdv<D, true, false, true>(p, n_ctas, stream);
         return launch_dkdv<D, false, false, true>(p, n_ctas, stream);
     }

@@ -583,6 +583,38 @@ __device__ __forceinline__ float narrow_exp_store_alibi(uint32_t t_s, int nch, i
     return acc;
 }
 
+// Pass 1 over a gathered-key tile with a bias matrix: x = s sl2 + b(i, pos(c)) log2(e) for the
+// first 32 * nch columns (-inf past the tile's keys, c > a1), written back over S as fp32 for
+// narrow_exp_store with unit scale.  brow: this row's bias (position 0), or null for rows past the
+// sequence (their bias reads as 0); pos(c): the key position of column c.  One 2-byte load per key.
+template <class Pos>
+__device__ __forceinline__ float narrow_row_max_matbias(uint32_t t_s, int nch, int a1, float sl2,
+                                                        const uint16_t* brow, Pos pos) {
+    constexpr float LOG2E_F = 1.4426950408889634f;
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const int c = ch * 32 + e;
+            const float b0 = (brow && c <= a1) ? __uint_as_float((uint32_t)__ldg(brow + pos(c)) << 16) : 0.f;
+            const float b1 = (brow && c + 1 <= a1) ? __uint_as_float((uint32_t)__ldg(brow + pos(c + 1)) << 16) : 0.f;
+            const float x0 = c <= a1 ? fmaf(__uint_as_float(r[e]), sl2, b0 * LOG2E_F) : -INFINITY;
+            const float x1 = c + 1 <= a1 ? fmaf(__uint_as_float(r[e + 1]), sl2, b1 * LOG2E_F) : -INFINITY;
+            r[e] = __float_as_uint(x0);
+            r[e + 1] = __float_as_uint(x1);
+            m0 = fmaxf(m0, x0);
+            m1 = fmaxf(m1, x1);
+        }
+        tmem_st32(t_s + ch * 32, r);
+    }
+    tmem_wait_st();
+    return fmaxf(m0, m1);
+}
+
 // This thread's O row (tensor memory, fp32) times inv_l, stored as bf16 at dst.  Every lane runs
 // the tensor-memory loads (they are warp-collective); only lanes with `store` write.
 template <int D>
@@ -802,6 +834,10 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     for (int s = 0; s < C::NSUB; ++s)
                         for (int r = 0; r < BN; r += C::KV_BOX)
                             tma_load_3d(s_k + s * C::KV_SUB + r * 128, &p.tm_k, bar(B_KFULL), s * C::XW, row + r, bkv);
+                    if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
+                        if (!grows)
+                            tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM,
+                                               (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a));
                 }
             } else {
                 gather_rows<D>(smem + C::OFF_K, BN, p.k + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
@@ -978,10 +1014,13 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
         for (int it = 0; it < n_iter; ++it) {
             uint4 bv[BIAS == BIAS_MATRIX ? 16 : 1];  // this row's bias for the tile (issued before the S wait)
             if constexpr (BIAS == BIAS_MATRIX) {
-                const long c0 = (long)band_tile(band_index(it)) * BN;
-                const uint16_t* brow =
-                    (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0 : nullptr;
-                load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
+                if (!is_gathered(it)) {  // a gathered tile reads its scattered keys' bias in pass 1
+                    const long c0 = (long)band_tile(band_index(it)) * BN;
+                    const uint16_t* brow = (row_valid && i < p.S)
+                                               ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld + c0
+                                               : nullptr;
+                    load_bias_row(bv, brow, (int)min((long)BN, (long)p.S - c0));
+                }
             }
             // ---- mask of this tile (decided once per tile; FULL tiles evaluate no predicate).  It does
             // not depend on S, so it is worked out before the wait for S (the global-key bits of a
@@ -1068,7 +1107,15 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     mx = partial ? tile_row_max_alibi<MASK_ANY, true>(t_s, mk, sl2, mL, base)
                                  : tile_row_max_alibi<MASK_NONE, true>(t_s, mk, sl2, mL, base);
             } else if constexpr (BIAS == BIAS_MATRIX) {
-                mx = partial ? tile_row_max_matbias<MASK_ANY>(t_s, mk, sl2, bv) : tile_row_max_matbias<MASK_NONE>(t_s, mk, sl2, bv);
+                if (LG && gathered) {
+                    const uint16_t* brow0 =
+                        (row_valid && i < p.S) ? p.bias + (bplane * (size_t)p.S + (size_t)i) * (size_t)p.bias_ld : nullptr;
+                    mx = narrow_row_max_matbias(t_s, (gcols + 31) >> 5, mk.a1, sl2, brow0,
+                                                [&](int c) -> long { return outside_key(gat_index(it) * BN + c); });
+                } else {
+                    mx = partial ? tile_row_max_matbias<MASK_ANY>(t_s, mk, sl2, bv)
+                                 : tile_row_max_matbias<MASK_NONE>(t_s, mk, sl2, bv);
+                }
             } else {
                 if constexpr (LG) {
                     if (gathered) mx = narrow_row_max(t_s, (gcols + 31) >> 5, mk.a1);
@@ -1126,7 +1173,11 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                                   : tile_exp_store_alibi<MASK_NONE, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
             } else if constexpr (BIAS == BIAS_MATRIX) {
                 fix();
-                sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);  // x is already scaled, biased and masked
+                // x is already scaled, biased and masked
+                if (LG && gathered)
+                    sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, 1.f, ref, bar(B_PFULL), no_fix);
+                else
+                    sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);
             } else if constexpr (F8) {
                 fix();
                 sum = !partial ? tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL))
@@ -1266,7 +1317,12 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
         if (d == 128 && !p.alibi) return launch<128, BIAS_NONE, true>(p, n_items, stream);
         return cudaErrorInvalidValue;
     }
-    if (p.bias) {  // a bias matrix (bf16 inputs, interval kinds; checked by the host)
+    if (p.bias) {  // a bias matrix (bf16 inputs; checked by the host)
+        if (p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0) {
+            if (d == 128) return launch<128, BIAS_MATRIX, false, true>(p, n_items, stream);
+            if (d == 64) return launch<64, BIAS_MATRIX, false, true>(p, n_items, stream);
+            return cudaErrorInvalidValue;
+        }
         if (d == 128) return launch<128, BIAS_MATRIX>(p, n_items, stream);
         if (d == 64) return launch<64, BIAS_MATRIX>(p, n_items, stream);
         return cudaErrorInvalidValue;
