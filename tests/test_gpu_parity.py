@@ -92,6 +92,23 @@ def test_bf16_local_global_placements(G):
     _full_compare(small("lg", 1, 3, 3, 520, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_local_global_every_position_global(d):
+    """Every position is a global token: every row sees every key (the full mask); the band items
+    store no row and the global-row items, in key chunks, compute all of them."""
+    w = small("lgall", 1, 2, 2, 300, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=5, globals_idx=tuple(range(300)))
+    Qc, Kc, Vc = wl.make_inputs(w)
+    O, LSE, _ = run_cuda(w, Qc.cuda(), Kc.cuda(), Vc.cuda())
+    O_ref, L_ref = oracle_rows(w.with_(kind=wl.MASK_FULL, globals_idx=()), Qc, Kc, Vc, all_rows(w))
+    compare(w, *gather_rows(O, LSE), O_ref, L_ref)
+
+
+def test_bf16_local_global_globals_beyond_one_64_key_tile():
+    """d = 64 (64-key tiles): 100 globals outside a query tile's band need two gathered key tiles."""
+    G = list(range(2, 1000, 10))
+    _full_compare(small("lg64g", 1, 2, 1, 1000, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=30, globals_idx=G))
+
+
 def test_bf16_local_global_many_globals():
     """More than one gathered tile of global tokens (129 globals)."""
     _full_compare(small("lg2", 1, 2, 1, 700, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=9,
