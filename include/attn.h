@@ -290,9 +290,10 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes);
  * Masked pairs stay masked whatever their bias; the bias enters the row max, the
  * weights and the LSE.  Every mask kind takes it; under LOCAL_GLOBAL the global keys and
  * the global rows read b_ij at their own positions.
+ * With ATTN_FP8_E4M3 inputs the bias is added to the descaled scores, in the same
+ * logit units.
  * Errors: ATTN_ERR_INVALID_ARG (NULL handle, misaligned pointer, Bb / Hb / ld out of
- *         range); ATTN_ERR_UNSUPPORTED (dtype other than ATTN_BF16, or with the ALiBi
- *         bias set).
+ *         range); ATTN_ERR_UNSUPPORTED (ATTN_F32 inputs, or with the ALiBi bias set).
  * attn_backward of a handle with a bias matrix recomputes P with the same b_ij.
  * Must not be called while a forward of this handle is in flight.
  */

@@ -50,11 +50,13 @@ def _allowed(kind, S, window):
     raise ValueError(kind)
 
 
-def _e4m3_model(w, Q8, K8, V8, dq, dk, dv):
+def _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=None):
     """O as the E4M3 kernel rounds it (see the module docstring), float64 [B, Hq, S, d].
 
     The scores are fp32 sums of exact E4M3 products, as on the tensor core; the weights are
-    fp32 exponentials rounded to E4M3; O is accumulated in float64 and rounded to bf16."""
+    fp32 exponentials rounded to E4M3; O is accumulated in float64 and rounded to bf16.  An
+    optional bias matrix [Bb, Hb, S, >= S] (float32 values of the bf16 tensor) joins the
+    scores in log2 units, x = s sl2 + b log2 e, as the kernel's pass 1 forms it."""
     q = Q8.float().numpy()
     k = K8.float().numpy()
     v = V8.float().double().numpy()
@@ -68,7 +70,11 @@ def _e4m3_model(w, Q8, K8, V8, dq, dk, dv):
     for b in range(B):
         for a in range(Hq):
             x = np.full((S, nt * T), -np.inf, dtype=np.float32)
-            x[:, :S] = np.where(ok, (q[b, a] @ k[b, a // g].T) * sl2, np.float32(-np.inf))
+            sc = (q[b, a] @ k[b, a // g].T) * sl2
+            if bias is not None:
+                bm = bias[0 if bias.shape[0] == 1 else b, 0 if bias.shape[1] == 1 else a, :, :S]
+                sc = sc + bm.astype(np.float32) * np.float32(LOG2E)
+            x[:, :S] = np.where(ok, sc, np.float32(-np.inf))
             tmax = x.reshape(S, nt, T).max(axis=2)
             ref = np.empty_like(tmax)
             m = np.full(S, -np.inf, dtype=np.float32)
@@ -87,11 +93,13 @@ def _e4m3_model(w, Q8, K8, V8, dq, dk, dv):
     return torch.from_numpy(out).float().to(torch.bfloat16).double().numpy()
 
 
-def _run(w):
+def _run(w, bias=None):
     import transformer_self_attention_gb300 as tsa
     Q8, K8, V8, (dq, dk, dv) = wl.make_fp8_inputs(w)
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind, window=w.window)
     plan.set_fp8_descale(dq, dk, dv)
+    if bias is not None:
+        plan.set_bias(bias.cuda())
     O = torch.full((w.B, w.Hq, w.S, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
     L = torch.full((w.B, w.Hq, w.S), float("nan"), dtype=torch.float32, device="cuda")
     plan(Q8.cuda(), K8.cuda(), V8.cuda(), O=O, LSE=L)
@@ -131,6 +139,22 @@ def test_fp8_kinds(kind, S):
     O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
                                     w.kind, w.window)
     _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv))
+
+
+@pytest.mark.parametrize("Bb,Hb", [(1, 1), (2, 4)])
+@pytest.mark.parametrize("kind", [wl.MASK_CAUSAL, wl.MASK_SLIDING])
+def test_fp8_bias_matrix(kind, Bb, Hb):
+    """E4M3 inputs with a bias matrix b_ij (bf16 N(0, 2^2), NaN row padding): the bias joins the
+    descaled scores; bounds from the rounding model with the same bias."""
+    w = small("f8b", 2, 4, 2, 300, 128, "bf16", kind, window=37)
+    g = torch.Generator().manual_seed(21)
+    bias = (torch.randn(Bb, Hb, w.S, 304, generator=g) * 2).to(torch.bfloat16)
+    bias[..., w.S:] = float("nan")
+    O, L, (Q8, K8, V8, dq, dk, dv) = _run(w, bias)
+    bf = bias.float().numpy()
+    O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                    w.kind, w.window, bias=bf)
+    _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=bf))
 
 
 def test_fp8_rounding_model_is_not_trivial():

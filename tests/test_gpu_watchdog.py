@@ -16,8 +16,9 @@ from gpu_util import compare, oracle_rows, run_cuda, small
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_load_times_out_and_context_survives():
-    w = small("wd", 1, 2, 2, 256, 128, "bf16", wl.MASK_CAUSAL)
+@pytest.mark.parametrize("d", [128, 64])  # d = 64: the 64-key-tile kernel, four CTAs per SM
+def test_withheld_load_times_out_and_context_survives(d):
+    w = small("wd", 1, 2, 2, 256, d, "bf16", wl.MASK_CAUSAL)
     Qc, Kc, Vc = wl.make_inputs(w)
     Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, kind=w.kind)

@@ -473,7 +473,7 @@ attn_status attn_set_bias(attn_handle h, const void* bias, int Bb, int Hb, long 
     }
     if (!aligned16(bias) || (Bb != 1 && Bb != h->B) || (Hb != 1 && Hb != h->Hq) || ld < h->S || ld % 8 != 0)
         return ATTN_ERR_INVALID_ARG;
-    if (h->dtype != ATTN_BF16 || h->tp.alibi) return ATTN_ERR_UNSUPPORTED;
+    if (h->dtype == ATTN_F32 || h->tp.alibi) return ATTN_ERR_UNSUPPORTED;
     if (!encode_map_bias(&h->tp.tm_bias, bias, ld, h->S, (long)Bb * Hb)) return ATTN_ERR_CUDA;
     h->tp.bias = static_cast<const uint16_t*>(bias);
     h->tp.bias_Bb = Bb;

@@ -1176,6 +1176,8 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 // x is already scaled, biased and masked
                 if (LG && gathered)
                     sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, 1.f, ref, bar(B_PFULL), no_fix);
+                else if constexpr (F8)
+                    sum = tile_exp_store_e4m3<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL));
                 else
                     sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);
             } else if constexpr (F8) {
@@ -1313,8 +1315,11 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    if (p.fp8) {  // E4M3 inputs: d = 128, no bias, no local + global (checked by the host)
-        if (d == 128 && !p.alibi) return launch<128, BIAS_NONE, true>(p, n_items, stream);
+    if (p.fp8) {  // E4M3 inputs: d = 128, no ALiBi, no local + global (checked by the host)
+        if (d == 128 && !p.alibi) {
+            if (p.bias) return launch<128, BIAS_MATRIX, true>(p, n_items, stream);
+            return launch<128, BIAS_NONE, true>(p, n_items, stream);
+        }
         return cudaErrorInvalidValue;
     }
     if (p.bias) {  // a bias matrix (bf16 inputs; checked by the host)
