@@ -36,9 +36,13 @@ FLOOR_MAX_ABS, FLOOR_REL_L2 = 4e-3, 1e-3
 LOG2E = 1.4426950408889634
 
 
-def _allowed(kind, S, window):
+def _allowed(kind, S, window, G=()):
     i = np.arange(S)[:, None]
     j = np.arange(S)[None, :]
+    if kind == wl.MASK_LOCAL_GLOBAL:
+        g = np.zeros(S, dtype=bool)
+        g[list(G)] = True
+        return (np.abs(i - j) <= window) | g[:, None] | g[None, :]
     if kind == wl.MASK_FULL:
         return np.ones((S, S), dtype=bool)
     if kind == wl.MASK_CAUSAL:
@@ -64,7 +68,7 @@ def _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=None):
     g = Hq // k.shape[1]
     T = 128
     nt = (S + T - 1) // T
-    ok = _allowed(w.kind, S, w.window)
+    ok = _allowed(w.kind, S, w.window, w.globals_idx)
     sl2 = np.float32(w.scale * dq * dk * LOG2E)
     out = np.empty((B, Hq, S, d), dtype=np.float64)
     for b in range(B):
@@ -96,7 +100,8 @@ def _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=None):
 def _run(w, bias=None):
     import transformer_self_attention_gb300 as tsa
     Q8, K8, V8, (dq, dk, dv) = wl.make_fp8_inputs(w)
-    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind, window=w.window)
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(w.globals_idx))
     plan.set_fp8_descale(dq, dk, dv)
     if bias is not None:
         plan.set_bias(bias.cuda())
@@ -113,7 +118,10 @@ def _norms(O, O_ref):
     return float(np.abs(d).max()), float(np.linalg.norm(d) / np.linalg.norm(O_ref))
 
 
-def _check(O, L, O_ref, L_ref, O_model, report=None):
+def _check(O, L, O_ref, L_ref, O_model, report=None, track=True):
+    """track=False: the rounding model walks the keys in plain tile order, which the kernel does not
+    do for local + global (gathered global keys first, global rows in key chunks), so the two need
+    not take the same rounding decisions; the bounds against the oracle still come from the model."""
     assert np.isfinite(O).all() and np.isfinite(L).all()
     max_abs, rel = _norms(O.reshape(O_ref.shape), O_ref)
     m_abs, m_rel = _norms(O_model.reshape(O_ref.shape), O_ref)
@@ -128,7 +136,9 @@ def _check(O, L, O_ref, L_ref, O_model, report=None):
     print("fp8 errors:", line)
     if report:
         REPORT[report] = line
-    assert max_abs <= bound_abs and rel <= bound_rel and g_rel <= bound_track and lse <= LSE_ABS, line
+    assert max_abs <= bound_abs and rel <= bound_rel and lse <= LSE_ABS, line
+    if track:
+        assert g_rel <= bound_track, line
 
 
 @pytest.mark.parametrize("S", [1, 129, 300])
@@ -157,6 +167,24 @@ def test_fp8_bias_matrix(kind, Bb, Hb):
     _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=bf))
 
 
+@pytest.mark.parametrize("bias", [False, True])
+@pytest.mark.parametrize("S,G", [(300, (0, 150, 299)), (700, tuple(range(3, 700, 5))[:129])])
+def test_fp8_local_global(S, G, bias):
+    """E4M3 under local + global: gathered global keys in E4M3 narrow tiles, global rows in key chunks;
+    with and without a bias matrix."""
+    w = small("f8lg", 1, 4, 2, S, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G)
+    bm = None
+    if bias:
+        g = torch.Generator().manual_seed(22)
+        bm = (torch.randn(1, 4, S, (S + 7) // 8 * 8, generator=g) * 2).to(torch.bfloat16)
+        bm[..., S:] = float("nan")
+    O, L, (Q8, K8, V8, dq, dk, dv) = _run(w, bm)
+    bf = None if bm is None else bm.float().numpy()
+    O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                    w.kind, w.window, list(G), bias=bf)
+    _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=bf), track=False)
+
+
 def test_fp8_rounding_model_is_not_trivial():
     """The model's own error is the E4M3 rounding of P: well above bf16 rounding, well below
     the raw 2^-4 worst case, on the 300-token causal case."""
@@ -180,7 +208,7 @@ def test_fp8_full_size_causal_4k():
 
 def test_fp8_unsupported_shapes():
     import transformer_self_attention_gb300 as tsa
-    for kw in (dict(d=64, kind=wl.MASK_CAUSAL), dict(d=128, kind=wl.MASK_LOCAL_GLOBAL, global_idx=[0])):
+    for kw in (dict(d=64, kind=wl.MASK_CAUSAL), dict(d=64, kind=wl.MASK_LOCAL_GLOBAL, global_idx=[0])):
         with pytest.raises(tsa.AttnError) as e:
             tsa.Attention(1, 2, 2, 256, kw["d"], dtype="e4m3", kind=kw["kind"], window=3,
                           global_idx=kw.get("global_idx"))

@@ -468,19 +468,20 @@ __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMa
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// Rows pos(r), r < n_rows, of one [S, D] bf16 head copied with plain loads into a tile of `rows`
-// rows in the layout the TMA loads write (128-byte swizzle: 64-column blocks of rows * 128 bytes, the
-// 16-byte chunk c of row r at chunk position c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32
-// lanes of one warp take part.
-template <int D, class Pos>
-__device__ __forceinline__ void gather_rows(uint8_t* tile, int rows, const uint16_t* head, int n_rows, Pos pos,
+// Rows pos(r), r < n_rows, of one head of ROWB-byte rows (d bf16 or E4M3 values) copied with plain
+// loads into a tile of `rows` rows in the layout the TMA loads write (128-byte swizzle: blocks of
+// rows * 128 bytes, one per 128 bytes of a row, the 16-byte chunk c of row r at chunk position
+// c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32 lanes of one warp take part.
+template <int ROWB, class Pos>
+__device__ __forceinline__ void gather_rows(uint8_t* tile, int rows, const void* head, int n_rows, Pos pos,
                                             int lane) {
-    constexpr int CH = D / 8;  // 16-byte chunks per row
+    constexpr int CH = ROWB / 16;  // 16-byte chunks per row
+    const uint8_t* h = static_cast<const uint8_t*>(head);
     for (int e = lane; e < n_rows * CH; e += 32) {
         const int r = e / CH, c = e - r * CH;
         const long j = pos(r);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (j >= 0) v = __ldg(reinterpret_cast<const uint4*>(head + j * D) + c);
+        if (j >= 0) v = __ldg(reinterpret_cast<const uint4*>(h + j * ROWB) + c);
         *reinterpret_cast<uint4*>(tile + (c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
 }
@@ -533,6 +534,40 @@ __device__ __forceinline__ float narrow_exp_store(uint32_t t_s, int nch, int a1,
     fix();
     release_first_half(bar_p);
     return acc.x + acc.y;
+}
+
+// narrow_exp_store for E4M3 P: 64 keys at a time (the columns past 32 * nch hold no key and are
+// masked), four keys per tensor-memory column in the A operand layout of the 8-bit MMA (keys
+// 4q .. 4q + 3 of a 64-key group h in column 16h + q).  fix() runs once every exponential is
+// computed, then the whole of P is announced on bar_p.
+template <typename FixO>
+__device__ __forceinline__ float narrow_exp_store_e4m3(uint32_t t_s, int nch, int a1, float sl2, float ref,
+                                                       uint32_t bar_p, FixO&& fix) {
+    float acc = 0.f;
+#pragma unroll 1
+    for (int h = 0; 2 * h < nch; ++h) {
+        uint32_t r0[32], r1[32], pk[16];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float pa[4], pb[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int ca = h * 64 + 4 * q + u, cb = ca + 32;
+                pa[u] = ex2(ca <= a1 ? fmaf(__uint_as_float(r0[4 * q + u]), sl2, -ref) : -INFINITY);
+                pb[u] = ex2(cb <= a1 ? fmaf(__uint_as_float(r1[4 * q + u]), sl2, -ref) : -INFINITY);
+                acc += pa[u] + pb[u];
+            }
+            pk[q] = pack_e4m3x4(pa[0], pa[1], pa[2], pa[3]);
+            pk[8 + q] = pack_e4m3x4(pb[0], pb[1], pb[2], pb[3]);
+        }
+        tmem_st16(t_s + h * 16, pk);
+    }
+    fix();
+    release_first_half(bar_p);
+    return acc;
 }
 
 // The two passes over a gathered-key tile with the ALiBi bias: x = s sl2 - mL |fi - pos(c)| in log2 units,
@@ -804,7 +839,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
         // overlap the copy of the Q tile.
         if (grows) {  // query rows G[q_tile * BM + r]; rows past the list are zero
             const int r0 = q_tile * BM;
-            gather_rows<D>(smem + C::OFF_Q, BM, p.q + (size_t)bh * p.S * D, BM,
+            gather_rows<D * C::EB>(smem + C::OFF_Q, BM, reinterpret_cast<const uint8_t*>(p.q) + (size_t)bh * p.S * D * C::EB, BM,
                            [&](int r) -> long { return r0 + r < p.n_global ? (long)__ldg(p.globals + r0 + r) : -1L; },
                            lane);
             fence_proxy_async_smem();
@@ -840,7 +875,8 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                                                (p.bias_Bb == 1 ? 0 : b) * p.bias_Hb + (p.bias_Hb == 1 ? 0 : a));
                 }
             } else {
-                gather_rows<D>(smem + C::OFF_K, BN, p.k + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                gather_rows<D * C::EB>(smem + C::OFF_K, BN, reinterpret_cast<const uint8_t*>(p.k) + (size_t)bkv * p.S * D * C::EB,
+                                       grows_pad, gpos, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_KFULL));
@@ -860,7 +896,8 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                             tma_load_3d(s_v + s * C::KV_SUB + r * 128, &p.tm_v, bar(B_VFULL), s * C::XW, row + r, bkv);
                 }
             } else {
-                gather_rows<D>(smem + C::OFF_V, BN, p.v + (size_t)bkv * p.S * D, grows_pad, gpos, lane);
+                gather_rows<D * C::EB>(smem + C::OFF_V, BN, reinterpret_cast<const uint8_t*>(p.v) + (size_t)bkv * p.S * D * C::EB,
+                                       grows_pad, gpos, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_VFULL));
@@ -927,7 +964,8 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 // a gathered-key tile is ncols wide (a multiple of 32): N = ncols for S, K = ncols for P V
                 const bool narrow = is_gathered(it);
                 const int ncols = narrow ? (gathered_cols(gat_index(it)) + 31) & ~31 : BN;
-                const uint32_t idesc_s = narrow ? idesc_bf16_f32(BM, ncols, false) : idesc_qk;
+                const uint32_t idesc_s =
+                    narrow ? (F8 ? idesc_e4m3_f32(BM, ncols, false) : idesc_bf16_f32(BM, ncols, false)) : idesc_qk;
 #pragma unroll
                 for (int k = 0; k < D / KS; ++k) {
                     const uint32_t offq = (k >> 2) * C::SUB + (k & 3) * 32, offk = (k >> 2) * C::KV_SUB + (k & 3) * 32;
@@ -1175,16 +1213,21 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 fix();
                 // x is already scaled, biased and masked
                 if (LG && gathered)
-                    sum = narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, 1.f, ref, bar(B_PFULL), no_fix);
+                    sum = F8 ? narrow_exp_store_e4m3(t_s, (gcols + 31) >> 5, mk.a1, 1.f, ref, bar(B_PFULL), no_fix)
+                             : narrow_exp_store(t_s, (gcols + 31) >> 5, mk.a1, 1.f, ref, bar(B_PFULL), no_fix);
                 else if constexpr (F8)
                     sum = tile_exp_store_e4m3<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL));
                 else
                     sum = tile_exp_store<MASK_NONE>(t_s, mk, 1.f, ref, bar(B_PFULL), no_fix);
             } else if constexpr (F8) {
-                fix();
-                sum = !partial ? tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL))
-                      : upper ? tile_exp_store_e4m3<MASK_UPPER>(t_s, mk, sl2, ref, bar(B_PFULL))
-                              : tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL));
+                if (LG && gathered) {
+                    sum = narrow_exp_store_e4m3(t_s, (gcols + 31) >> 5, mk.a1, sl2, ref, bar(B_PFULL), fix);
+                } else {
+                    fix();
+                    sum = !partial ? tile_exp_store_e4m3<MASK_NONE>(t_s, mk, sl2, ref, bar(B_PFULL))
+                          : upper ? tile_exp_store_e4m3<MASK_UPPER>(t_s, mk, sl2, ref, bar(B_PFULL))
+                                  : tile_exp_store_e4m3<MASK_ANY>(t_s, mk, sl2, ref, bar(B_PFULL));
+                }
             } else {
                 const float r_eff = (BIAS == BIAS_ALIBI_MMA) ? ref - base : ref;  // x = s sl2 + base - ref
                 if (LG && gathered)
@@ -1315,10 +1358,13 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    if (p.fp8) {  // E4M3 inputs: d = 128, no ALiBi, no local + global (checked by the host)
+    if (p.fp8) {  // E4M3 inputs: d = 128, no ALiBi (checked by the host)
         if (d == 128 && !p.alibi) {
-            if (p.bias) return launch<128, BIAS_MATRIX, true>(p, n_items, stream);
-            return launch<128, BIAS_NONE, true>(p, n_items, stream);
+            const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0;
+            if (p.bias) return lg ? launch<128, BIAS_MATRIX, true, true>(p, n_items, stream)
+                                  : launch<128, BIAS_MATRIX, true>(p, n_items, stream);
+            return lg ? launch<128, BIAS_NONE, true, true>(p, n_items, stream)
+                      : launch<128, BIAS_NONE, true>(p, n_items, stream);
         }
         return cudaErrorInvalidValue;
     }
