@@ -80,8 +80,8 @@ typedef enum {
  * fp32 ("Transformer 演进与变体" (ai.icyfenix.cn), section Flash Attention, FP8
  * support: matrix products in FP8, softmax and accumulation in higher precision;
  * "第 8 章 现代大模型架构", 8.6.5: scale before the multiply-add, descale at the
- * output).  d_k = 128 only; every mask kind, with or without a bias matrix; not
- * with the ALiBi bias. */
+ * output).  d_k = 128 only; every mask kind, with the ALiBi bias, a bias matrix
+ * or neither. */
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 typedef struct attn_plan* attn_handle;
@@ -267,10 +267,11 @@ int attn_selftest_device_once(void);
  *   slopes : HOST array of Hq finite floats (query head a uses slopes[a]; copied),
  *            or NULL to remove the bias.
  * The bias enters the row max, the weights and the LSE (LSE = ln sum_j e^{logits_ij}).
- * Every mask kind takes it; under LOCAL_GLOBAL the global keys and rows get the same
- * distance term (|i - j| between the positions of the pair).
+ * Every mask kind and every dtype takes it; under LOCAL_GLOBAL the global keys and rows
+ * get the same distance term (|i - j| between the positions of the pair); with E4M3
+ * inputs it joins the descaled scores, element by element.
  * Errors: ATTN_ERR_INVALID_ARG (NULL handle, non-finite slope),
- *         ATTN_ERR_UNSUPPORTED (ATTN_FP8_E4M3 handles, or a bias matrix set), ATTN_ERR_OOM, ATTN_ERR_CUDA.
+ *         ATTN_ERR_UNSUPPORTED (a bias matrix set), ATTN_ERR_OOM, ATTN_ERR_CUDA.
  * Must not be called while a forward of this handle is in flight.
  */
 attn_status attn_set_alibi(attn_handle h, const float* slopes);

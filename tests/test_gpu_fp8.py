@@ -185,6 +185,37 @@ def test_fp8_local_global(S, G, bias):
     _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=bf), track=False)
 
 
+def _alibi_bias(slopes, S):
+    """The ALiBi bias -m_a |i - j| as a [1, Hq, S, S] float32 matrix (the model's bias form)."""
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    return np.stack([-np.float32(m) * np.abs(i - j).astype(np.float32) for m in slopes])[None]
+
+
+@pytest.mark.parametrize("kind,G", [(wl.MASK_CAUSAL, ()), (wl.MASK_SLIDING, ()), (wl.MASK_CAUSAL_SLIDING, ()),
+                                    (wl.MASK_LOCAL_GLOBAL, (0, 150, 299))])
+def test_fp8_alibi(kind, G):
+    """E4M3 inputs with ALiBi slopes: the distance term joins the descaled scores element by element;
+    bounds from the rounding model given the same bias as a matrix."""
+    import transformer_self_attention_gb300 as tsa
+    w = small("f8a", 1, 4, 2, 300, 128, "bf16", kind, window=37, globals_idx=G)
+    slopes = wl.alibi_slopes(4)
+    Q8, K8, V8, (dq, dk, dv) = wl.make_fp8_inputs(w)
+    plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind, window=w.window,
+                         global_idx=list(G))
+    plan.set_fp8_descale(dq, dk, dv)
+    plan.set_alibi(slopes)
+    O = torch.full((w.B, w.Hq, w.S, w.d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L = torch.full((w.B, w.Hq, w.S), float("nan"), dtype=torch.float32, device="cuda")
+    plan(Q8.cuda(), K8.cuda(), V8.cuda(), O=O, LSE=L)
+    torch.cuda.synchronize()
+    assert plan.poll_device_error() == (0, 0)
+    O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                    w.kind, w.window, list(G), alibi=slopes)
+    model = _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=_alibi_bias(slopes, w.S))
+    _check(O.float().cpu().numpy(), L.cpu().numpy(), O_ref * dv, L_ref, model, track=kind != wl.MASK_LOCAL_GLOBAL)
+
+
 def test_fp8_rounding_model_is_not_trivial():
     """The model's own error is the E4M3 rounding of P: well above bf16 rounding, well below
     the raw 2^-4 worst case, on the 300-token causal case."""
@@ -214,5 +245,6 @@ def test_fp8_unsupported_shapes():
                           global_idx=kw.get("global_idx"))
         assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED
     plan = tsa.Attention(1, 2, 2, 256, 128, dtype="e4m3", kind=wl.MASK_CAUSAL)
-    with pytest.raises(tsa.AttnError):
-        plan.set_alibi([0.1, 0.2])
+    plan.set_alibi([0.1, 0.2])
+    with pytest.raises(tsa.AttnError):  # ALiBi and a bias matrix are exclusive
+        plan.set_bias(torch.zeros(1, 1, 256, 256, dtype=torch.bfloat16, device="cuda"))

@@ -452,7 +452,7 @@ attn_status attn_set_alibi(attn_handle h, const float* slopes) {
     }
     for (int a = 0; a < h->Hq; ++a)
         if (!std::isfinite(slopes[a])) return ATTN_ERR_INVALID_ARG;
-    if (h->dtype == ATTN_FP8_E4M3 || h->tp.bias) return ATTN_ERR_UNSUPPORTED;
+    if (h->tp.bias) return ATTN_ERR_UNSUPPORTED;  // ALiBi and a bias matrix are exclusive
     if (!h->d_alibi) {
         cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&h->d_alibi), sizeof(float) * h->Hq);
         if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? ATTN_ERR_OOM : ATTN_ERR_CUDA;

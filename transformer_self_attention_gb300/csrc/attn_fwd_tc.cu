@@ -416,6 +416,44 @@ __device__ __forceinline__ float tile_exp_store_alibi(uint32_t t_s, const TileMa
     return (acc0.x + acc0.y) + (acc1.x + acc1.y);
 }
 
+// tile_exp_store_alibi for E4M3 P (four keys per tensor-memory column, as tile_exp_store_e4m3).
+template <int MASKED, bool ABS>
+__device__ __forceinline__ float tile_exp_store_alibi_e4m3(uint32_t t_s, const TileMask& mk, float sl2, float ref,
+                                                           float mL, float base, uint32_t bar_half) {
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r0[32], r1[32], pk[16];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float pa[4], pb[4];
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+                const int c0 = h * 64 + 4 * q + u, c1 = h * 64 + 32 + 4 * q + u;
+                const float2 xa = __ffma2_rn(make_float2(tile_score<MASKED>(r0[4 * q + u], c0, mk),
+                                                         tile_score<MASKED>(r0[4 * q + u + 1], c0 + 1, mk)),
+                                             sl2x2, alibi_pair<ABS>(base, c0, mL, ref));
+                const float2 xb = __ffma2_rn(make_float2(tile_score<MASKED>(r1[4 * q + u], c1, mk),
+                                                         tile_score<MASKED>(r1[4 * q + u + 1], c1 + 1, mk)),
+                                             sl2x2, alibi_pair<ABS>(base, c1, mL, ref));
+                pa[u] = ex2(xa.x); pa[u + 1] = ex2(xa.y);
+                pb[u] = ex2(xb.x); pb[u + 1] = ex2(xb.y);
+                acc0 = __fadd2_rn(acc0, make_float2(pa[u], pa[u + 1]));
+                acc1 = __fadd2_rn(acc1, make_float2(pb[u], pb[u + 1]));
+            }
+            pk[q] = pack_e4m3x4(pa[0], pa[1], pa[2], pa[3]);
+            pk[8 + q] = pack_e4m3x4(pb[0], pb[1], pb[2], pb[3]);
+        }
+        tmem_st16(t_s + h * 16, pk);
+        if (h == 0) release_first_half(bar_half);
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
 // The bias row of this thread for one key tile: 16 loads of 16 bytes (8 keys each), issued
 // before the wait for S so that their latency hides behind it.  brow: the row's bias at the
 // tile's first key (16-byte aligned), or null for rows past the sequence; chunks of 8 keys are
@@ -613,6 +651,38 @@ __device__ __forceinline__ float narrow_exp_store_alibi(uint32_t t_s, int nch, i
             pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(t_s + ch * 16, pk);
+    }
+    release_first_half(bar_p);
+    return acc;
+}
+
+// narrow_exp_store_alibi for E4M3 P: 64 keys at a time, four per tensor-memory column.
+template <class Pos>
+__device__ __forceinline__ float narrow_exp_store_alibi_e4m3(uint32_t t_s, int nch, int a1, float sl2, float ref,
+                                                             float mL, float fi, Pos pos, uint32_t bar_p) {
+    float acc = 0.f;
+#pragma unroll 1
+    for (int h = 0; 2 * h < nch; ++h) {
+        uint32_t r0[32], r1[32], pk[16];
+        tmem_ld32(t_s + h * 64, r0);
+        tmem_ld32(t_s + h * 64 + 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float pa[4], pb[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int ca = h * 64 + 4 * q + u, cb = ca + 32;
+                pa[u] = ex2(ca <= a1 ? fmaf(__uint_as_float(r0[4 * q + u]), sl2, -mL * fabsf(fi - pos(ca)) - ref)
+                                     : -INFINITY);
+                pb[u] = ex2(cb <= a1 ? fmaf(__uint_as_float(r1[4 * q + u]), sl2, -mL * fabsf(fi - pos(cb)) - ref)
+                                     : -INFINITY);
+                acc += pa[u] + pb[u];
+            }
+            pk[q] = pack_e4m3x4(pa[0], pa[1], pa[2], pa[3]);
+            pk[8 + q] = pack_e4m3x4(pb[0], pb[1], pb[2], pb[3]);
+        }
+        tmem_st16(t_s + h * 16, pk);
     }
     release_first_half(bar_p);
     return acc;
@@ -1199,7 +1269,18 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
             auto no_fix = []() {};
             // ---- pass 2: P = exp2(s * scale * log2 e - m), row sum, bf16 P over the S columns
             float sum;
-            if constexpr (ALIBI) {
+            if constexpr (ALIBI && F8) {  // E4M3 P
+                fix();
+                if (LG && gathered)
+                    sum = narrow_exp_store_alibi_e4m3(t_s, (gcols + 31) >> 5, mk.a1, sl2, ref, mL, (float)i, gpos_f,
+                                                      bar(B_PFULL));
+                else if (causal_kind)
+                    sum = partial ? tile_exp_store_alibi_e4m3<MASK_ANY, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi_e4m3<MASK_NONE, false>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
+                else
+                    sum = partial ? tile_exp_store_alibi_e4m3<MASK_ANY, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL))
+                                  : tile_exp_store_alibi_e4m3<MASK_NONE, true>(t_s, mk, sl2, ref, mL, base, bar(B_PFULL));
+            } else if constexpr (ALIBI) {
                 fix();
                 if (LG && gathered)
                     sum = narrow_exp_store_alibi(t_s, (gcols + 31) >> 5, mk.a1, sl2, ref, mL, (float)i, gpos_f, bar(B_PFULL));
@@ -1358,9 +1439,12 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    if (p.fp8) {  // E4M3 inputs: d = 128, no ALiBi (checked by the host)
-        if (d == 128 && !p.alibi) {
-            const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0;
+    if (p.fp8) {  // E4M3 inputs: d = 128 (checked by the host)
+        const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0;
+        if (d == 128 && p.alibi)  // ALiBi added per element for every kind (no bf16 bias product with E4M3 operands)
+            return lg ? launch<128, BIAS_ALIBI_ELEM, true, true>(p, n_items, stream)
+                      : launch<128, BIAS_ALIBI_ELEM, true>(p, n_items, stream);
+        if (d == 128) {
             if (p.bias) return lg ? launch<128, BIAS_MATRIX, true, true>(p, n_items, stream)
                                   : launch<128, BIAS_MATRIX, true>(p, n_items, stream);
             return lg ? launch<128, BIAS_NONE, true, true>(p, n_items, stream)
