@@ -141,22 +141,24 @@ def _check(O, L, O_ref, L_ref, O_model, report=None, track=True):
         assert g_rel <= bound_track, line
 
 
+@pytest.mark.parametrize("d", [128, 64])  # d = 64: 64-byte rows in the 64-byte swizzle layout
 @pytest.mark.parametrize("S", [1, 129, 300])
 @pytest.mark.parametrize("kind", [wl.MASK_FULL, wl.MASK_CAUSAL, wl.MASK_SLIDING, wl.MASK_CAUSAL_SLIDING])
-def test_fp8_kinds(kind, S):
-    w = small("f8", 2, 4, 2, S, 128, "bf16", kind, window=37)
+def test_fp8_kinds(kind, S, d):
+    w = small("f8", 2, 4, 2, S, d, "bf16", kind, window=37)
     O, L, (Q8, K8, V8, dq, dk, dv) = _run(w)
     O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
                                     w.kind, w.window)
     _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv))
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("Bb,Hb", [(1, 1), (2, 4)])
 @pytest.mark.parametrize("kind", [wl.MASK_CAUSAL, wl.MASK_SLIDING])
-def test_fp8_bias_matrix(kind, Bb, Hb):
+def test_fp8_bias_matrix(kind, Bb, Hb, d):
     """E4M3 inputs with a bias matrix b_ij (bf16 N(0, 2^2), NaN row padding): the bias joins the
     descaled scores; bounds from the rounding model with the same bias."""
-    w = small("f8b", 2, 4, 2, 300, 128, "bf16", kind, window=37)
+    w = small("f8b", 2, 4, 2, 300, d, "bf16", kind, window=37)
     g = torch.Generator().manual_seed(21)
     bias = (torch.randn(Bb, Hb, w.S, 304, generator=g) * 2).to(torch.bfloat16)
     bias[..., w.S:] = float("nan")
@@ -192,13 +194,14 @@ def _alibi_bias(slopes, S):
     return np.stack([-np.float32(m) * np.abs(i - j).astype(np.float32) for m in slopes])[None]
 
 
-@pytest.mark.parametrize("kind,G", [(wl.MASK_CAUSAL, ()), (wl.MASK_SLIDING, ()), (wl.MASK_CAUSAL_SLIDING, ()),
-                                    (wl.MASK_LOCAL_GLOBAL, (0, 150, 299))])
-def test_fp8_alibi(kind, G):
+@pytest.mark.parametrize("kind,G,d", [(wl.MASK_CAUSAL, (), 128), (wl.MASK_SLIDING, (), 128),
+                                      (wl.MASK_CAUSAL_SLIDING, (), 128), (wl.MASK_LOCAL_GLOBAL, (0, 150, 299), 128),
+                                      (wl.MASK_CAUSAL, (), 64), (wl.MASK_SLIDING, (), 64)])
+def test_fp8_alibi(kind, G, d):
     """E4M3 inputs with ALiBi slopes: the distance term joins the descaled scores element by element;
     bounds from the rounding model given the same bias as a matrix."""
     import transformer_self_attention_gb300 as tsa
-    w = small("f8a", 1, 4, 2, 300, 128, "bf16", kind, window=37, globals_idx=G)
+    w = small("f8a", 1, 4, 2, 300, d, "bf16", kind, window=37, globals_idx=G)
     slopes = wl.alibi_slopes(4)
     Q8, K8, V8, (dq, dk, dv) = wl.make_fp8_inputs(w)
     plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind, window=w.window,
@@ -239,7 +242,7 @@ def test_fp8_full_size_causal_4k():
 
 def test_fp8_unsupported_shapes():
     import transformer_self_attention_gb300 as tsa
-    for kw in (dict(d=64, kind=wl.MASK_CAUSAL), dict(d=64, kind=wl.MASK_LOCAL_GLOBAL, global_idx=[0])):
+    for kw in (dict(d=64, kind=wl.MASK_LOCAL_GLOBAL, global_idx=[0]),):
         with pytest.raises(tsa.AttnError) as e:
             tsa.Attention(1, 2, 2, 256, kw["d"], dtype="e4m3", kind=kw["kind"], window=3,
                           global_idx=kw.get("global_idx"))

@@ -98,11 +98,12 @@ bool encode_map_e4m3(CUtensorMap* map, const void* base, int d, long rows, long 
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)rows * d};
-    cuuint32_t box[3] = {128, box_rows, 1};
+    // rows of d bytes: one 128-byte swizzled block at d = 128, one 64-byte swizzled block at d = 64
+    cuuint32_t box[3] = {(cuuint32_t)(d >= 128 ? 128 : 64), box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, d >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -189,7 +190,7 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
     attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, global_idx, n_global);
     if (vs != ATTN_OK) return vs;
     if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
-    if (dtype == ATTN_FP8_E4M3 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
+    if (dtype == ATTN_FP8_E4M3 && d_k == 64 && kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
     const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
                           kind == ATTN_MASK_LOCAL_GLOBAL;
 

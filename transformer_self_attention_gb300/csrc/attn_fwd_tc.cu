@@ -76,12 +76,20 @@ struct Cfg {
     static constexpr int BN = BN_;                // keys per kernel tile
     static constexpr int SUBT = KT / BN;          // kernel tiles per schedule tile
     static constexpr int EB = F8 ? 1 : 2;         // bytes per element (E4M3 or bf16)
-    static constexpr int SUB = BM * 128;          // bytes of one 128-row x 128-byte swizzled block (Q, O staging)
-    static constexpr int KV_SUB = BN * 128;       // the same for a K / V tile of BN rows
-    static constexpr int XW = 128 / EB;           // elements per 128-byte row of a block
-    static constexpr int NSUB = D / XW;           // blocks per row
-    static constexpr int TILE_BYTES = BM * D * EB; // one Q tile
-    static constexpr int KV_BYTES = BN * D * EB;  // one K / V tile
+    static constexpr int ROWB = D * EB;           // bytes per row of Q, K, V
+    // swizzle width: 128-byte blocks, or one 64-byte block for 64-byte rows (E4M3 at d = 64)
+    static constexpr int SWB = ROWB < 128 ? ROWB : 128;
+    static_assert(SWB == 128 || SWB == 64, "row layout");
+    static constexpr uint32_t SW_MODE = SWB == 128 ? 2u : 4u;  // shared-memory descriptor swizzle field
+    static constexpr int SBO = 8 * SWB;           // descriptor stride between 8-row groups
+    static constexpr int SPB = SWB / 32;          // 32-byte K steps per block row
+    static constexpr int SUB = BM * SWB;          // bytes of one 128-row swizzled block of Q
+    static constexpr int KV_SUB = BN * SWB;       // the same for a K / V tile of BN rows
+    static constexpr int OSUB = BM * 128;         // one 64-column block of the bf16 O staging
+    static constexpr int XW = SWB / EB;           // elements per row of a block
+    static constexpr int NSUB = ROWB / SWB;       // blocks per row
+    static constexpr int TILE_BYTES = BM * ROWB;  // one Q tile
+    static constexpr int KV_BYTES = BN * ROWB;    // one K / V tile
     // rows of the K / V tensor maps' box (the host encodes 64 at d = 64, 128 otherwise); a tile of BN
     // rows is BN / KV_BOX copies per 64-column block
     static constexpr int KV_BOX = (D == 64) ? 64 : 128;
@@ -938,7 +946,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     mbar_arrive_expect_tx(bar(B_KFULL), C::KV_BYTES);
                     for (int s = 0; s < C::NSUB; ++s)
                         for (int r = 0; r < BN; r += C::KV_BOX)
-                            tma_load_3d(s_k + s * C::KV_SUB + r * 128, &p.tm_k, bar(B_KFULL), s * C::XW, row + r, bkv);
+                            tma_load_3d(s_k + s * C::KV_SUB + r * C::SWB, &p.tm_k, bar(B_KFULL), s * C::XW, row + r, bkv);
                     if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
                         if (!grows)
                             tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM,
@@ -963,7 +971,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     mbar_arrive_expect_tx(bar(B_VFULL), C::KV_BYTES);
                     for (int s = 0; s < C::NSUB; ++s)
                         for (int r = 0; r < BN; r += C::KV_BOX)
-                            tma_load_3d(s_v + s * C::KV_SUB + r * 128, &p.tm_v, bar(B_VFULL), s * C::XW, row + r, bkv);
+                            tma_load_3d(s_v + s * C::KV_SUB + r * C::SWB, &p.tm_v, bar(B_VFULL), s * C::XW, row + r, bkv);
                 }
             } else {
                 gather_rows<D * C::EB>(smem + C::OFF_V, BN, reinterpret_cast<const uint8_t*>(p.v) + (size_t)bkv * p.S * D * C::EB,
@@ -999,7 +1007,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 mbar_arrive_expect_tx(bar(B_KFULL), C::KV_BYTES);
                 for (int s = 0; s < C::NSUB; ++s)
                     for (int r = 0; r < BN; r += C::KV_BOX)
-                        tma_load_3d(s_k + s * C::KV_SUB + r * 128, km, bar(B_KFULL), s * C::XW, row + r, bkv);
+                        tma_load_3d(s_k + s * C::KV_SUB + r * C::SWB, km, bar(B_KFULL), s * C::XW, row + r, bkv);
                 ++k_loaded;
                 if constexpr (BIAS == BIAS_MATRIX)  // the softmax reads this tile's bias rows a tile later
                     tma_prefetch_l2_3d(&p.tm_bias, row, q_tile * BM, bias_plane);
@@ -1008,7 +1016,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 mbar_arrive_expect_tx(bar(B_VFULL), C::KV_BYTES);
                 for (int s = 0; s < C::NSUB; ++s)
                     for (int r = 0; r < BN; r += C::KV_BOX)
-                        tma_load_3d(s_v + s * C::KV_SUB + r * 128, vm, bar(B_VFULL), s * C::XW, row + r, bkv);
+                        tma_load_3d(s_v + s * C::KV_SUB + r * C::SWB, vm, bar(B_VFULL), s * C::XW, row + r, bkv);
                 ++v_loaded;
             }
             if (sh->abort) {  // let the copies this thread issued land before the CTA exits
@@ -1038,13 +1046,14 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     narrow ? (F8 ? idesc_e4m3_f32(BM, ncols, false) : idesc_bf16_f32(BM, ncols, false)) : idesc_qk;
 #pragma unroll
                 for (int k = 0; k < D / KS; ++k) {
-                    const uint32_t offq = (k >> 2) * C::SUB + (k & 3) * 32, offk = (k >> 2) * C::KV_SUB + (k & 3) * 32;
+                    const uint32_t offq = (k / C::SPB) * C::SUB + (k % C::SPB) * 32,
+                                   offk = (k / C::SPB) * C::KV_SUB + (k % C::SPB) * 32;
                     if constexpr (F8)
-                        mma_ss_f8(t_s, sdesc_sw128(s_q + offq, 16, 1024), sdesc_sw128(s_k + offk, 16, 1024), idesc_s,
-                                  k > 0);
+                        mma_ss_f8(t_s, sdesc_sw(s_q + offq, 16, C::SBO, C::SW_MODE),
+                                  sdesc_sw(s_k + offk, 16, C::SBO, C::SW_MODE), idesc_s, k > 0);
                     else
-                        mma_ss(t_s, sdesc_sw128(s_q + offq, 16, 1024), sdesc_sw128(s_k + offk, 16, 1024), idesc_s,
-                               k > 0);
+                        mma_ss(t_s, sdesc_sw(s_q + offq, 16, C::SBO, C::SW_MODE),
+                               sdesc_sw(s_k + offk, 16, C::SBO, C::SW_MODE), idesc_s, k > 0);
                 }
                 if constexpr (BIAS == BIAS_ALIBI_MMA)
                     mma_ss(t_s, sdesc_plain(smem_u32(smem + C::OFF_BA), 128, 256),
@@ -1068,10 +1077,10 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                     // P: KS keys = 8 tensor-memory columns (2 bf16 or 4 E4M3 per column);
                     // V: KS key rows of 128 B each (MN-major: d runs along the row)
                     if constexpr (F8)
-                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::KV_SUB, 1024), idesc_pv,
+                        mma_ts_f8(t_o, t_s + k * 8, sdesc_sw(s_v + k * KS * C::SWB, C::KV_SUB, C::SBO, C::SW_MODE), idesc_pv,
                                   (it > 0 || k > 0) ? 1u : 0u);
                     else
-                        mma_ts(t_o, t_s + k * 8, sdesc_sw128(s_v + k * KS * 128, C::KV_SUB, 1024), idesc_pv,
+                        mma_ts(t_o, t_s + k * 8, sdesc_sw(s_v + k * KS * C::SWB, C::KV_SUB, C::SBO, C::SW_MODE), idesc_pv,
                                (it > 0 || k > 0) ? 1u : 0u);
                 }
                 if (!ok) {  // half of this PV was issued: track it so the drain below covers it
@@ -1358,7 +1367,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int chunk = (c & 1) * 4 + q;  // 16-byte chunk within the 128-byte row
-                        uint4* dst = reinterpret_cast<uint4*>(stage + sub * C::SUB + r * 128 + ((chunk ^ (r & 7)) << 4));
+                        uint4* dst = reinterpret_cast<uint4*>(stage + sub * C::OSUB + r * 128 + ((chunk ^ (r & 7)) << 4));
                         *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                     }
                 }
@@ -1367,7 +1376,7 @@ __global__ void __launch_bounds__(NTHREADS, (Cfg<D, BIAS, F8, BN>::CTAS_PER_SM))
                 if (threadIdx.x == 0) {
                     // O is bf16 (64 columns per 128-byte block); with E4M3 inputs the staging runs on
                     // into the (idle) K buffer that follows the Q buffer
-                    for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_o, s_q + s * C::SUB, s * 64, q_tile * BM, bh);
+                    for (int s = 0; s < D / 64; ++s) tma_store_3d(&p.tm_o, s_q + s * C::OSUB, s * 64, q_tile * BM, bh);
                     tma_store_commit_and_wait_read();
                 }
             } else if (p.n_chunks == 1) {
@@ -1439,7 +1448,7 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    if (p.fp8) {  // E4M3 inputs: d = 128 (checked by the host)
+    if (p.fp8) {  // E4M3 inputs: d = 128, or d = 64 without local + global (checked by the host)
         const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0;
         if (d == 128 && p.alibi)  // ALiBi added per element for every kind (no bf16 bias product with E4M3 operands)
             return lg ? launch<128, BIAS_ALIBI_ELEM, true, true>(p, n_items, stream)
@@ -1449,6 +1458,11 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
                                   : launch<128, BIAS_MATRIX, true>(p, n_items, stream);
             return lg ? launch<128, BIAS_NONE, true, true>(p, n_items, stream)
                       : launch<128, BIAS_NONE, true>(p, n_items, stream);
+        }
+        if (d == 64 && !lg) {  // 64-byte rows: the 64-byte swizzle layout
+            if (p.alibi) return launch<64, BIAS_ALIBI_ELEM, true>(p, n_items, stream);
+            if (p.bias) return launch<64, BIAS_MATRIX, true>(p, n_items, stream);
+            return launch<64, BIAS_NONE, true>(p, n_items, stream);
         }
         return cudaErrorInvalidValue;
     }
