@@ -416,7 +416,7 @@ def run_ours(args, w):
     if args.fp8:
         Qc, Kc, Vc, descales = wl.make_fp8_inputs(w)
         plan = tsa.Attention(w.B, w.Hq, w.Hkv, w.S, w.d, dtype="e4m3", scale=w.scale, kind=w.kind,
-                             window=w.window)
+                             window=w.window, global_idx=list(w.globals_idx))
         plan.set_fp8_descale(*descales)
     else:
         Qc, Kc, Vc = wl.make_inputs(w)

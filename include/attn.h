@@ -80,8 +80,8 @@ typedef enum {
  * fp32 ("Transformer 演进与变体" (ai.icyfenix.cn), section Flash Attention, FP8
  * support: matrix products in FP8, softmax and accumulation in higher precision;
  * "第 8 章 现代大模型架构", 8.6.5: scale before the multiply-add, descale at the
- * output).  d_k = 128 with every mask kind, d_k = 64 with every kind but
- * LOCAL_GLOBAL; with the ALiBi bias, a bias matrix or neither. */
+ * output).  Every mask kind, d_k = 64 or 128, with the ALiBi bias, a bias matrix
+ * or neither. */
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1, ATTN_FP8_E4M3 = 2 } attn_dtype;
 
 typedef struct attn_plan* attn_handle;

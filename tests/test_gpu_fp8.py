@@ -169,12 +169,13 @@ def test_fp8_bias_matrix(kind, Bb, Hb, d):
     _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv, bias=bf))
 
 
+@pytest.mark.parametrize("d", [128, 64])  # d = 64: gathered rows written in the 64-byte swizzle layout
 @pytest.mark.parametrize("bias", [False, True])
 @pytest.mark.parametrize("S,G", [(300, (0, 150, 299)), (700, tuple(range(3, 700, 5))[:129])])
-def test_fp8_local_global(S, G, bias):
+def test_fp8_local_global(S, G, bias, d):
     """E4M3 under local + global: gathered global keys in E4M3 narrow tiles, global rows in key chunks;
     with and without a bias matrix."""
-    w = small("f8lg", 1, 4, 2, S, 128, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G)
+    w = small("f8lg", 1, 4, 2, S, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=G)
     bm = None
     if bias:
         g = torch.Generator().manual_seed(22)
@@ -196,7 +197,8 @@ def _alibi_bias(slopes, S):
 
 @pytest.mark.parametrize("kind,G,d", [(wl.MASK_CAUSAL, (), 128), (wl.MASK_SLIDING, (), 128),
                                       (wl.MASK_CAUSAL_SLIDING, (), 128), (wl.MASK_LOCAL_GLOBAL, (0, 150, 299), 128),
-                                      (wl.MASK_CAUSAL, (), 64), (wl.MASK_SLIDING, (), 64)])
+                                      (wl.MASK_CAUSAL, (), 64), (wl.MASK_SLIDING, (), 64),
+                                      (wl.MASK_LOCAL_GLOBAL, (0, 150, 299), 64)])
 def test_fp8_alibi(kind, G, d):
     """E4M3 inputs with ALiBi slopes: the distance term joins the descaled scores element by element;
     bounds from the rounding model given the same bias as a matrix."""
@@ -240,14 +242,20 @@ def test_fp8_full_size_causal_4k():
            report=f"{w.name} E4M3 (every row)")
 
 
-def test_fp8_unsupported_shapes():
+def test_fp8_unsupported_combinations():
     import transformer_self_attention_gb300 as tsa
-    for kw in (dict(d=64, kind=wl.MASK_LOCAL_GLOBAL, global_idx=[0]),):
-        with pytest.raises(tsa.AttnError) as e:
-            tsa.Attention(1, 2, 2, 256, kw["d"], dtype="e4m3", kind=kw["kind"], window=3,
-                          global_idx=kw.get("global_idx"))
-        assert e.value.status == tsa.ATTN_ERR_UNSUPPORTED
     plan = tsa.Attention(1, 2, 2, 256, 128, dtype="e4m3", kind=wl.MASK_CAUSAL)
     plan.set_alibi([0.1, 0.2])
     with pytest.raises(tsa.AttnError):  # ALiBi and a bias matrix are exclusive
         plan.set_bias(torch.zeros(1, 1, 256, 256, dtype=torch.bfloat16, device="cuda"))
+
+
+def test_fp8_full_size_local_global_8k():
+    """The 8K local + global workload (d 64) in E4M3: every output against the oracle, bounds from the
+    rounding model (plain tile order: no tracking bound)."""
+    w = wl.LONGFORMER_8K
+    O, L, (Q8, K8, V8, dq, dk, dv) = _run(w)
+    O_ref, L_ref = oracle.attention(Q8.float().numpy(), K8.float().numpy(), V8.float().numpy(), w.scale * dq * dk,
+                                    w.kind, w.window, list(w.globals_idx))
+    _check(O, L, O_ref * dv, L_ref, _e4m3_model(w, Q8, K8, V8, dq, dk, dv), report=f"{w.name} E4M3 (every row)",
+           track=False)

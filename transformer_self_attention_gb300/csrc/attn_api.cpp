@@ -190,7 +190,6 @@ attn_status attn_create(attn_handle* out, int B, int Hq, int Hkv, int S, int d_k
     attn_status vs = validate_shape(B, Hq, Hkv, S, kind, window, global_idx, n_global);
     if (vs != ATTN_OK) return vs;
     if (d_k != 64 && d_k != 128) return ATTN_ERR_UNSUPPORTED;
-    if (dtype == ATTN_FP8_E4M3 && d_k == 64 && kind == ATTN_MASK_LOCAL_GLOBAL) return ATTN_ERR_UNSUPPORTED;
     const bool windowed = kind == ATTN_MASK_SLIDING || kind == ATTN_MASK_CAUSAL_SLIDING ||
                           kind == ATTN_MASK_LOCAL_GLOBAL;
 

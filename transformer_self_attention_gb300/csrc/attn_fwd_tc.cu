@@ -515,9 +515,10 @@ __device__ __forceinline__ float tile_row_max_matbias(uint32_t t_s, const TileMa
 }
 
 // Rows pos(r), r < n_rows, of one head of ROWB-byte rows (d bf16 or E4M3 values) copied with plain
-// loads into a tile of `rows` rows in the layout the TMA loads write (128-byte swizzle: blocks of
-// rows * 128 bytes, one per 128 bytes of a row, the 16-byte chunk c of row r at chunk position
-// c ^ (r & 7)).  pos(r) < 0 gives a zero row.  All 32 lanes of one warp take part.
+// loads into a tile of `rows` rows in the layout the TMA loads write.  128-byte swizzle (rows of 128
+// bytes or more): blocks of rows * 128 bytes, one per 128 bytes of a row, the 16-byte chunk c of row r
+// at chunk position c ^ (r & 7).  64-byte swizzle (64-byte rows): the chunk c (of 4) of row r at
+// position c ^ ((r >> 1) & 3).  pos(r) < 0 gives a zero row.  All 32 lanes of one warp take part.
 template <int ROWB, class Pos>
 __device__ __forceinline__ void gather_rows(uint8_t* tile, int rows, const void* head, int n_rows, Pos pos,
                                             int lane) {
@@ -528,7 +529,10 @@ __device__ __forceinline__ void gather_rows(uint8_t* tile, int rows, const void*
         const long j = pos(r);
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (j >= 0) v = __ldg(reinterpret_cast<const uint4*>(h + j * ROWB) + c);
-        *reinterpret_cast<uint4*>(tile + (c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        if constexpr (ROWB >= 128)
+            *reinterpret_cast<uint4*>(tile + (c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        else
+            *reinterpret_cast<uint4*>(tile + r * 64 + ((c ^ ((r >> 1) & 3)) << 4)) = v;
     }
 }
 
@@ -1448,7 +1452,7 @@ cudaError_t launch(const TcParams& p, int n_items, cudaStream_t stream) {
 cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_t stream) {
     if (n_items <= 0) return cudaSuccess;
     const bool causal = p.kind == ATTN_MASK_CAUSAL || p.kind == ATTN_MASK_CAUSAL_SLIDING;
-    if (p.fp8) {  // E4M3 inputs: d = 128, or d = 64 without local + global (checked by the host)
+    if (p.fp8) {  // E4M3 inputs: d = 128 or 64 (checked by the host)
         const bool lg = p.kind == ATTN_MASK_LOCAL_GLOBAL && p.n_global > 0;
         if (d == 128 && p.alibi)  // ALiBi added per element for every kind (no bf16 bias product with E4M3 operands)
             return lg ? launch<128, BIAS_ALIBI_ELEM, true, true>(p, n_items, stream)
@@ -1459,10 +1463,13 @@ cudaError_t launch_tc_forward(const TcParams& p, int d, int n_items, cudaStream_
             return lg ? launch<128, BIAS_NONE, true, true>(p, n_items, stream)
                       : launch<128, BIAS_NONE, true>(p, n_items, stream);
         }
-        if (d == 64 && !lg) {  // 64-byte rows: the 64-byte swizzle layout
-            if (p.alibi) return launch<64, BIAS_ALIBI_ELEM, true>(p, n_items, stream);
-            if (p.bias) return launch<64, BIAS_MATRIX, true>(p, n_items, stream);
-            return launch<64, BIAS_NONE, true>(p, n_items, stream);
+        if (d == 64) {  // 64-byte rows: the 64-byte swizzle layout
+            if (p.alibi) return lg ? launch<64, BIAS_ALIBI_ELEM, true, true>(p, n_items, stream)
+                                   : launch<64, BIAS_ALIBI_ELEM, true>(p, n_items, stream);
+            if (p.bias) return lg ? launch<64, BIAS_MATRIX, true, true>(p, n_items, stream)
+                                  : launch<64, BIAS_MATRIX, true>(p, n_items, stream);
+            return lg ? launch<64, BIAS_NONE, true, true>(p, n_items, stream)
+                      : launch<64, BIAS_NONE, true>(p, n_items, stream);
         }
         return cudaErrorInvalidValue;
     }
