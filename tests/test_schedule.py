@@ -237,7 +237,8 @@ def _lg_bwd_kernel_counts(S, w, G, lst, off):
 
 @pytest.mark.parametrize("S,w,G", [(1, 0, (0,)), (127, 3, (0, 126)), (128, 5, (64,)), (129, 0, (128,)),
                                    (300, 40, (0, 100, 299)), (520, 130, (0, 127, 128, 255, 519)),
-                                   (700, 200, ()), (640, 63, tuple(range(0, 640, 5)))])
+                                   (700, 200, ()), (640, 63, tuple(range(0, 640, 5))),
+                                   (520, 10, tuple(range(128, 256))), (640, 3, tuple(range(0, 128)) + (600,))])
 def test_lg_backward_lists_match_brute_force(S, w, G):
     """Local + global backward lists against the oracle's enumeration: tile x lists exactly the
     tiles holding an allowed pair against it, ascending, FULL exactly where the oracle's class is

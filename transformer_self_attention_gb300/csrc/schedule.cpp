@@ -272,13 +272,21 @@ void build_lg_pair_lists(int S, int window, const std::vector<int>& globals, std
         const long r0 = (long)x * T, r1 = std::min<long>(S, r0 + T) - 1;
         const bool x_has_g = globals_in(r0, r1) > 0;
         const int band_lo = (int)(band.lo(r0) / T), band_hi = (int)(band.hi(r1) / T);  // inclusive
+        const bool x_all_g = r0 + T - 1 < S && globals_in(r0, r0 + T - 1) == T;
         for (int t = 0; t < n; ++t) {
             const long c0 = (long)t * T, c1 = c0 + T - 1, c1s = std::min<long>(c1, S - 1);
             const bool t_has_g = globals_in(c0, c1s) > 0;
-            if (!x_has_g && !t_has_g && (t < band_lo || t > band_hi)) continue;
+            const bool in_band = t >= band_lo && t <= band_hi;
+            if (!x_has_g && !t_has_g && !in_band) continue;
             // every pair allowed: both tiles whole, and each row global or its window plus the
-            // global columns covering [c0, c1]
+            // global columns covering [c0, c1].  Outside the band no row's window reaches the tile
+            // (the band is the union of the rows' windows), so only a tile of global rows or of
+            // global columns is FULL there: an O(1) test instead of the per-row one.
             bool full = r0 + T - 1 < S && c1 < S;
+            if (full && !in_band) {
+                list->push_back(t | ((x_all_g || globals_in(c0, c1) == T) ? ATTN_LIST_FULL : 0));
+                continue;
+            }
             for (long i = r0; i <= r0 + T - 1 && full; ++i) {
                 if (is_g[i]) continue;
                 const long lo = band.lo(i), hi = band.hi(i);
