@@ -149,6 +149,13 @@ def test_backward_local_global_many_globals_gqa():
                  globals_idx=tuple(range(0, 640, 5))[:129]))
 
 
+def test_backward_local_global_whole_global_tile():
+    """A whole 128-position tile of global tokens: every pair against it is allowed, so the list
+    entries of the tiles outside its band are FULL (no mask) in both kernels."""
+    _check(small("blgt", 1, 2, 1, 520, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=10,
+                 globals_idx=tuple(range(128, 256))))
+
+
 def test_backward_local_global_alibi():
     """ALiBi under local + global: -m_a |i - j| for the window and the global pairs alike."""
     _check(small("blga", 1, 4, 2, 600, 64, "bf16", wl.MASK_LOCAL_GLOBAL, window=40, globals_idx=(0, 333, 599)),

@@ -103,6 +103,13 @@ def test_bf16_local_global_every_position_global(d):
     compare(w, *gather_rows(O, LSE), O_ref, L_ref)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_local_global_whole_global_tile(d):
+    """A whole 128-position tile of global tokens (a full gathered key tile, a full global-row tile)."""
+    _full_compare(small("lgt", 1, 2, 1, 520, d, "bf16", wl.MASK_LOCAL_GLOBAL, window=10,
+                        globals_idx=tuple(range(128, 256))))
+
+
 def test_bf16_local_global_globals_beyond_one_64_key_tile():
     """d = 64 (64-key tiles): 100 globals outside a query tile's band need two gathered key tiles."""
     G = list(range(2, 1000, 10))
