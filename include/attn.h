@@ -465,9 +465,11 @@ attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, 
  *   cache_len       : HOST array of B lengths, each in [1, S_cap], and >= S_q
  *                     for the causal kinds; read before the call returns.
  * The (sequence, kv head) units are laid end to end as one list of 128-key
- * tiles and a persistent grid of one CTA per multiprocessor takes equal shares
- * of it; a unit cut between CTAs is combined on the device by the last of them
- * to finish.
+ * tiles and a persistent grid of one CTA per multiprocessor takes contiguous
+ * shares of it, weighted by tiles and by the units begun inside a share
+ * (attn_decode_schedule_host); a unit cut between CTAs is combined on the
+ * device by a second, small kernel enqueued behind the first (see
+ * attn_decode_set_merge_mode).
  * Errors: ATTN_ERR_INVALID_ARG (pointers, lengths), ATTN_ERR_CUDA.  Device
  * watchdog errors are read by attn_decode_poll_device_error; the outputs of
  * that call are then undefined (the poll resets the handle's counters, so the
@@ -497,10 +499,11 @@ attn_status attn_decode_set_grid_limit(attn_decode_handle h, int max_ctas);
  * attn_decode_set_merge_mode -- where the partial results of a unit (b, g) split over
  * several CTAs are combined (O = sum_c e^{LSE_c - M} O_c / W, LSE = M + ln W with
  * M = max_c LSE_c, W = sum_c e^{LSE_c - M}, the same merge either way):
- *   0 (default): by a second, small kernel when some unit of the call has 6 or more
- *                partials, else by the last CTA to finish a part of the unit;
- *   1          : always by that last CTA;
- *   2          : always by the merge kernel (one warp per packed row).
+ *   0 (default): by a second, small kernel (one warp per packed row), launched as a
+ *                programmatic dependent of the decode kernel so that its launch overlaps
+ *                the decode kernel; it is not enqueued when no unit is split;
+ *   1          : by the last CTA to finish a part of the unit, inside the decode kernel;
+ *   2          : by the merge kernel (as 0).
  * Errors: ATTN_ERR_INVALID_ARG (NULL handle, mode outside 0..2).
  */
 attn_status attn_decode_set_merge_mode(attn_decode_handle h, int mode);
@@ -522,13 +525,20 @@ attn_status attn_decode_destroy(attn_decode_handle h);
  * lo_b = max(0, cache_len[b] - S_q - window) / ATTN_TILE.  With
  * n_b = hi_b - lo_b, tile_prefix[b] = n_0 + ... + n_{b-1}; unit (b, g) covers
  * the indices [Hkv * tile_prefix[b] + g * n_b, ... + n_b) of one list of
- * T = Hkv * tile_prefix[B] tiles, and CTA k of the *n_cta = min(n_sm, T) CTAs
- * takes the indices [k * T / n_cta, (k + 1) * T / n_cta) (integer division).
+ * T = Hkv * tile_prefix[B] tiles.  CTA k of the *n_cta = min(n_sm, 256, T) CTAs
+ * takes the indices [share[k], share[k + 1]): share[0] = 0, share[n_cta] = T,
+ * every share non-empty, and the boundaries sit at equal steps of
+ * F(i) = i + 2 * (number of unit begins u with 0 < u <= i), so that a share's
+ * weight is its tiles plus two for every unit it begins inside it (the cost of
+ * one more stretch: an epilogue and a pipeline refill, about two tiles' time).
  *   tile_prefix : output, B + 1 ints.
- * Errors: ATTN_ERR_INVALID_ARG (n_sm < 1, shape or lengths as for the calls above).
+ *   share       : output, *n_cta + 1 long longs (room for min(n_sm, 256) + 1).
+ * Errors: ATTN_ERR_INVALID_ARG (n_sm < 1, NULL outputs, shape or lengths as for
+ * the calls above).
  */
 attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_mask_kind kind, int window,
-                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix);
+                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix,
+                                      long long* share);
 
 #ifdef __cplusplus
 }

@@ -2,12 +2,13 @@
 
 The kernel's arithmetic is restated here: unit (b, g) covers the indices
 [Hkv * prefix[b] + g * n_b, ... + n_b) of one list of T tiles, and CTA k takes
-[k*T/n_cta, (k+1)*T/n_cta).  Checked bit-exactly, without a GPU:
+[share[k], share[k+1]).  Checked bit-exactly, without a GPU:
   * every key tile a sequence needs (some query row may see one of its keys, by
     enumeration of the oracle's predicate) is in its range, and the range starts
     and ends at such tiles;
-  * every tile of every unit belongs to exactly one CTA, and the shares differ in
-    size by at most one tile;
+  * every tile of every unit belongs to exactly one CTA; the shares are contiguous
+    and non-empty, and their boundaries sit at equal steps of the weight
+    F(i) = i + 2 * (unit begins in (0, i]) (tiles plus two per extra stretch);
   * only a CTA's first and last stretches can be partial units, and the partial-
     result slots the writers use (2k for a first stretch, 2k+1 for a last one)
     are exactly the slots the merge of each unit enumerates.
@@ -37,9 +38,12 @@ def _needed_tiles(kind, S_q, window, L):
     return tiles
 
 
-def _stretches(Hkv, prefix, n_cta, total, k):
+STRETCH_COST = 2
+
+
+def _stretches(Hkv, prefix, share, k):
     """The kernel's walk over CTA k's share: list of (b, g, first_tile_in_unit, count, whole)."""
-    i, end = k * total // n_cta, (k + 1) * total // n_cta
+    i, end = int(share[k]), int(share[k + 1])
     out = []
     while i < end:
         b = max(x for x in range(len(prefix) - 1) if Hkv * prefix[x] <= i)
@@ -53,15 +57,38 @@ def _stretches(Hkv, prefix, n_cta, total, k):
     return out
 
 
-def _share_of(i, n_cta, total):
-    return ((i + 1) * n_cta + total - 1) // total - 1
+def _share_of(i, share):
+    """The CTA whose share holds index i (the last one beginning at or before i)."""
+    return max(k for k in range(len(share) - 1) if share[k] <= i)
+
+
+def _unit_begins(Hkv, prefix):
+    return [Hkv * prefix[b] + g * (prefix[b + 1] - prefix[b]) for b in range(len(prefix) - 1) for g in range(Hkv)]
+
+
+def _weight(i, begins):
+    """F(i): tiles before i plus the stretch cost of every unit begun in (0, i]."""
+    return i + STRETCH_COST * sum(1 for u in begins if 0 < u <= i)
+
+
+def _check_shares(share, n_cta, total, begins):
+    share = [int(x) for x in share]
+    assert len(share) == n_cta + 1 and share[0] == 0 and share[-1] == total
+    assert all(share[k] < share[k + 1] for k in range(n_cta)), "an empty share"
+    F_T = total + STRETCH_COST * (len(begins) - 1)
+    for k in range(1, n_cta):
+        tau = F_T * k / n_cta
+        lo, hi = share[k - 1] + 1, total - (n_cta - k)  # room for one tile per remaining CTA
+        ideal = next(i for i in range(total + 1) if _weight(i, begins) >= tau - 1e-9)
+        assert share[k] == min(max(ideal, lo), hi), (k, share[k], ideal, lo, hi)
 
 
 def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
-    n_cta, prefix = tsa.attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, lens, n_sm)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, lens, n_sm)
     prefix = [int(x) for x in prefix]
     total = Hkv * prefix[B]
-    assert n_cta == min(n_sm, total)
+    assert n_cta == min(n_sm, 256, total)
+    _check_shares(share, n_cta, total, _unit_begins(Hkv, prefix))
     # ranges of the sequences
     for b, L in enumerate(lens):
         lo = _tile_lo(kind, S_q, window, L)
@@ -74,7 +101,7 @@ def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
     writer_slots = {}
     sizes = []
     for k in range(n_cta):
-        st = _stretches(Hkv, prefix, n_cta, total, k)
+        st = _stretches(Hkv, prefix, share, k)
         sizes.append(sum(c for _, _, _, c, _ in st))
         for idx, (b, g, t_in, count, whole) in enumerate(st):
             for t in range(t_in, t_in + count):
@@ -84,12 +111,11 @@ def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
                 assert idx == 0 or idx == len(st) - 1, "a partial stretch in the middle of a share"
                 writer_slots.setdefault((b, g), set()).add(2 * k + (0 if idx == 0 else 1))
     assert len(seen) == total
-    assert max(sizes) - min(sizes) <= 1
     for (b, g), slots in writer_slots.items():
         n_b = prefix[b + 1] - prefix[b]
         unit_begin = Hkv * prefix[b] + g * n_b
-        k0, k1 = _share_of(unit_begin, n_cta, total), _share_of(unit_begin + n_b - 1, n_cta, total)
-        k0_first = k0 * total // n_cta == unit_begin
+        k0, k1 = _share_of(unit_begin, share), _share_of(unit_begin + n_b - 1, share)
+        k0_first = share[k0] == unit_begin
         merge = {2 * k0 + (0 if k0_first else 1)} | {2 * kk for kk in range(k0 + 1, k1 + 1)}
         assert slots == merge, (b, g, slots, merge)
         assert len(slots) == k1 - k0 + 1 >= 2
@@ -110,30 +136,41 @@ def test_decode_split_covers_the_allowed_keys(kind, S_q):
 
 
 def test_decode_split_long_ragged_batch():
-    """Eight ragged 16K..30K caches with 8 kv heads on 152 SMs: equal shares, units cut across CTAs."""
+    """Eight ragged 16K..30K caches with 8 kv heads on 152 SMs: units cut across CTAs, and the
+    shares' weights (tiles plus the cost of every extra stretch) equal to within one stretch."""
     lens = [16384 + 2000 * b for b in range(8)]
-    n_cta, prefix = tsa.attn_decode_schedule_host(8, 8, 1, 32768, tsa.MASK_CAUSAL, 0, lens, 152)
-    total = 8 * int(prefix[-1])
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(8, 8, 1, 32768, tsa.MASK_CAUSAL, 0, lens, 152)
+    prefix = [int(x) for x in prefix]
+    total = 8 * prefix[-1]
     assert n_cta == 152
-    sizes = [(k + 1) * total // 152 - k * total // 152 for k in range(152)]
-    assert max(sizes) - min(sizes) <= 1
+    begins = _unit_begins(8, prefix)
+    _check_shares(share, n_cta, total, begins)
+    cost = [int(share[k + 1] - share[k]) + STRETCH_COST * sum(1 for u in begins if share[k] < u < share[k + 1])
+            for k in range(n_cta)]
+    assert max(cost) - min(cost) <= 1 + STRETCH_COST
+    # a share holding an extra stretch is shorter than one that does not
+    two = [int(share[k + 1] - share[k]) for k in range(n_cta) if any(share[k] < u < share[k + 1] for u in begins)]
+    one = [int(share[k + 1] - share[k]) for k in range(n_cta) if not any(share[k] < u < share[k + 1] for u in begins)]
+    assert two and one and max(two) < min(one) + 1
 
 
 def test_decode_split_single_huge_unit():
     """One long sequence with one kv head is spread over every CTA."""
-    n_cta, prefix = tsa.attn_decode_schedule_host(1, 1, 1, 1 << 20, tsa.MASK_CAUSAL, 0, [1 << 20], 152)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(1, 1, 1, 1 << 20, tsa.MASK_CAUSAL, 0, [1 << 20], 152)
     assert n_cta == 152 and prefix[1] == (1 << 20) // T
+    sizes = [int(share[k + 1] - share[k]) for k in range(n_cta)]
+    assert max(sizes) - min(sizes) <= 1  # one unit: no stretch to weigh
 
 
 def test_decode_split_fewer_tiles_than_sms():
-    n_cta, prefix = tsa.attn_decode_schedule_host(2, 1, 1, 300, tsa.MASK_CAUSAL, 0, [1, 200], 152)
-    assert n_cta == 3 and list(prefix) == [0, 1, 3]
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(2, 1, 1, 300, tsa.MASK_CAUSAL, 0, [1, 200], 152)
+    assert n_cta == 3 and list(prefix) == [0, 1, 3] and list(share) == [0, 1, 2, 3]
 
 
 def test_decode_sliding_window_skips_old_tiles():
     """The causal window reads only the tiles of the last window + S_q positions."""
     L, w = 16384, 4095
-    n_cta, prefix = tsa.attn_decode_schedule_host(1, 8, 1, L, tsa.MASK_CAUSAL_SLIDING, w, [L], 152)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(1, 8, 1, L, tsa.MASK_CAUSAL_SLIDING, w, [L], 152)
     assert prefix[1] == L // T - (L - 1 - w) // T
 
 
@@ -155,7 +192,7 @@ def test_decode_schedule_validation(args, status):
 
 
 def test_cross_attention_lengths_may_be_shorter_than_the_query_rows():
-    n_cta, prefix = tsa.attn_decode_schedule_host(2, 4, 32, 4096, tsa.MASK_FULL, 0, [3, 4096], 152)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(2, 4, 32, 4096, tsa.MASK_FULL, 0, [3, 4096], 152)
     assert list(prefix) == [0, 1, 33]
 
 

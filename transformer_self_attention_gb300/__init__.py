@@ -103,7 +103,7 @@ def _load():
     lib.attn_decode_poll_device_error.restype = I
     lib.attn_decode_destroy.argtypes = [P]
     lib.attn_decode_destroy.restype = I
-    lib.attn_decode_schedule_host.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I), P]
+    lib.attn_decode_schedule_host.argtypes = [I, I, I, I, I, I, P, I, ctypes.POINTER(I), P, P]
     lib.attn_decode_schedule_host.restype = I
     lib.attn_decode_set_grid_limit.argtypes = [P, I]
     lib.attn_decode_set_grid_limit.restype = I
@@ -298,16 +298,19 @@ def attn_decode_destroy(handle: int) -> int:
 
 
 def attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, cache_len, n_sm):
-    """Host-only decode work split: (n_cta, tile_prefix int32 [B + 1]).  Raises AttnError."""
+    """Host-only decode work split: (n_cta, tile_prefix int32 [B + 1], share int64 [n_cta + 1]).
+    CTA k takes the tile-list indices [share[k], share[k + 1]).  Raises AttnError."""
     lens, n = _int_array(cache_len)
     n_cta = ctypes.c_int(0)
     prefix = np.zeros(int(B) + 1, dtype=np.int32)
+    share = np.zeros(max(1, int(n_sm)) + 1, dtype=np.int64)
     st = _lib.attn_decode_schedule_host(int(B), int(Hkv), int(S_q), int(S_cap), int(kind), int(window),
                                         ctypes.cast(lens, ctypes.c_void_p), int(n_sm), ctypes.byref(n_cta),
-                                        prefix.ctypes.data_as(ctypes.c_void_p))
+                                        prefix.ctypes.data_as(ctypes.c_void_p),
+                                        share.ctypes.data_as(ctypes.c_void_p))
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode_schedule_host")
-    return n_cta.value, prefix
+    return n_cta.value, prefix, share[:n_cta.value + 1].copy()
 
 
 class DecodeAttention:

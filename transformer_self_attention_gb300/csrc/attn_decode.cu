@@ -29,8 +29,11 @@
 // that wraps back to zero).
 //
 //   warp 4 (producer) : TMA loads of each unit's packed Q rows (double-
-//                       buffered) and of the K and V tiles into a STAGES-deep
-//                       ring of 128B-swizzled tiles.
+//                       buffered) and of the K and V tiles into one ring of
+//                       tile-sized 128B-swizzled slots (K of tile n, then V of
+//                       tile n, in consecutive slots; K's slot is freed by its
+//                       QK product, V's by its PV product, so as many slots as
+//                       shared memory holds are in flight).
 //   warp 5 (MMA)      : one thread issues QK(n+1) before PV(n) so that the
 //                       softmax of tile n+1 overlaps the PV of tile n (S^T is
 //                       double-buffered in tensor memory, P^T in shared memory).
@@ -52,6 +55,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "device_once.h"
 #include "kernels.h"
 #include "sm103_ptx.h"
@@ -65,7 +70,7 @@ constexpr int BN = 128;         // keys per tile (the MMA's M)
 constexpr int NTHREADS = 192;   // 4 softmax warps + producer + MMA
 constexpr int WARP_PRODUCER = 4;
 constexpr int WARP_MMA = 5;
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_SLOTS = 12;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 constexpr int SMEM_LIMIT = 227 * 1024;
 
@@ -81,12 +86,11 @@ struct DCfg {
     static constexpr int ZERO = (D == 64) ? SUB : 0;  // rows 64..127 of V^T when d = 64 (zeros)
     static constexpr int CTL = 8192;
     static constexpr int FIXED = 2 * QT + 2 * 2 * PB + ZERO + CTL + 1024;
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / (2 * TB);
-    static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
-    static_assert(STAGES >= 2, "shared memory");
-    static constexpr int OFF_V = 0;
-    static constexpr int OFF_K = OFF_V + STAGES * TB;
-    static constexpr int OFF_Z = OFF_K + STAGES * TB;
+    static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TB;
+    static constexpr int SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;  // K/V ring
+    static_assert(SLOTS >= 4, "shared memory");
+    static constexpr int OFF_KV = 0;
+    static constexpr int OFF_Z = OFF_KV + SLOTS * TB;
     static constexpr int OFF_Q = OFF_Z + ZERO;
     static constexpr int OFF_P = OFF_Q + 2 * QT;
     static constexpr int OFF_CTL = OFF_P + 2 * 2 * PB;
@@ -99,11 +103,9 @@ struct DCfg {
 enum Bar {
     B_QFULL = 0,                      // 2: packed Q tile loaded
     B_QEMPTY = B_QFULL + 2,           // 2: last QK of its unit done (MMA commit)
-    B_KFULL = B_QEMPTY + 2,
-    B_KEMPTY = B_KFULL + MAX_STAGES,
-    B_VFULL = B_KEMPTY + MAX_STAGES,
-    B_VEMPTY = B_VFULL + MAX_STAGES,
-    B_SFULL = B_VEMPTY + MAX_STAGES,  // 2: S^T buffer ready (MMA commit)
+    B_FULL = B_QEMPTY + 2,            // SLOTS: K/V slot loaded
+    B_EMPTY = B_FULL + MAX_SLOTS,     // SLOTS: K/V slot read by its product (MMA commit)
+    B_SFULL = B_EMPTY + MAX_SLOTS,    // 2: S^T buffer ready (MMA commit)
     B_PFULL = B_SFULL + 2,            // 2: P^T written, S^T read, O^T rescaled / read out (128 arrivals)
     B_PFREE = B_PFULL + 2,            // 2: PV(n) done, n of that parity (MMA commit)
     NBAR = B_PFREE + 2
@@ -162,8 +164,18 @@ __device__ __forceinline__ int ordered(float f) {
 }
 __device__ __forceinline__ float unordered(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+// 32 lanes x 16 columns of 32 bit into elements [OFF, OFF + 16) of a larger register array
+template <int OFF, int N>
+__device__ __forceinline__ void tmem_ld16_at(uint32_t taddr, uint32_t (&r)[N]) {
+    static_assert(OFF + 16 <= N, "range");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]),
+          "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7]), "=r"(r[OFF + 8]), "=r"(r[OFF + 9]),
+          "=r"(r[OFF + 10]), "=r"(r[OFF + 11]), "=r"(r[OFF + 12]), "=r"(r[OFF + 13]), "=r"(r[OFF + 14]),
+          "=r"(r[OFF + 15])
+        : "r"(taddr));
 }
 
 // named barrier with an OR reduction of one predicate
@@ -182,11 +194,16 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
 
 // ---------------------------------------------------------------- the shared tile list
 // First index of CTA k's share, and the CTA whose share holds index i.
-__device__ __forceinline__ long long share_begin(const DecodeParams& p, int k) {
-    return (long long)k * p.total_tiles / p.n_cta;
-}
+// The shares are contiguous, non-empty and in CTA order (the host weights them by tiles and
+// by the units begun inside them).
+__device__ __forceinline__ long long share_begin(const DecodeParams& p, int k) { return p.share[k]; }
 __device__ __forceinline__ int share_of(const DecodeParams& p, long long i) {
-    return (int)(((i + 1) * p.n_cta + p.total_tiles - 1) / p.total_tiles - 1);
+    int lo = 0, hi = p.n_cta - 1;  // the last CTA whose share begins at or before i
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.share[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // One unit's stretch of a CTA's share.
@@ -367,10 +384,12 @@ template <int D, int NP, bool ALIBI>
 __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<D, NP>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
     DShared<NP>* sh = reinterpret_cast<DShared<NP>*>(smem + C::OFF_CTL);
-    const uint32_t s_v = smem_u32(smem + C::OFF_V);
-    const uint32_t s_k = smem_u32(smem + C::OFF_K);
+    const uint32_t s_kv = smem_u32(smem + C::OFF_KV);
+    // ring position of K (item 2n) and V (item 2n + 1) of the CTA's tile n
+    auto slot_of = [](int item) { return item % C::SLOTS; };
+    auto parity_of = [](int item) { return (uint32_t)((item / C::SLOTS) & 1); };
     const uint32_t s_z = smem_u32(smem + C::OFF_Z);
     const uint32_t s_q = smem_u32(smem + C::OFF_Q);
     const uint32_t s_p = smem_u32(smem + C::OFF_P);
@@ -407,12 +426,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    // the merge kernel, launched as a programmatic dependent of this grid, may be scheduled
+    // from here on: it waits for this grid's completion before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int n = 0, j = 0, k_loaded = 0, v_loaded = 0, q_loaded = 0;
+            int n = 0, j = 0, items = 0, q_loaded = 0;
             bool ok = true;
+            // the next K or V tile into the next slot, once its previous occupant has been read
+            auto load_kv = [&](const CUtensorMap* tm, int key, int bkv) -> bool {
+                const int sl = slot_of(items);
+                if (items >= C::SLOTS && !wait_bounded(bar(B_EMPTY + sl), parity_of(items) ^ 1u, wd, ERR_PRODUCER))
+                    return false;
+                mbar_arrive_expect_tx(bar(B_FULL + sl), C::TB);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(s_kv + sl * C::TB + c * C::SUB, tm, bar(B_FULL + sl), c * 64, key, bkv);
+                ++items;
+                return true;
+            };
             for (long long i = share0; i < share1 && ok; ++j) {
                 const Seg s = seg_at(p, i, share1);
                 i += s.count;
@@ -425,29 +458,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 q_loaded = j + 1;
                 const int bkv = s.b * p.Hkv + s.g;
                 for (int q = 0; q < s.count && ok; ++q, ++n) {
-                    const int st = n % C::STAGES, round = n / C::STAGES;
                     const int key = (s.tile0 + (ALIBI ? s.count - 1 - q : q)) * BN;
-                    if (n >= C::STAGES && !(ok = wait_bounded(bar(B_KEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
-                        break;
-                    mbar_arrive_expect_tx(bar(B_KFULL + st), C::TB);
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_3d(s_k + st * C::TB + c * C::SUB, &p.tm_k, bar(B_KFULL + st), c * 64, key, bkv);
-                    k_loaded = n + 1;
-                    if (n >= C::STAGES && !(ok = wait_bounded(bar(B_VEMPTY + st), (round - 1) & 1, wd, ERR_PRODUCER)))
-                        break;
-                    mbar_arrive_expect_tx(bar(B_VFULL + st), C::TB);
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_3d(s_v + st * C::TB + c * C::SUB, &p.tm_v, bar(B_VFULL + st), c * 64, key, bkv);
-                    v_loaded = n + 1;
+                    ok = load_kv(&p.tm_k, key, bkv) && load_kv(&p.tm_v, key, bkv);
                 }
             }
             if (sh->abort) {  // let the copies in flight land before the CTA exits
                 for (int jj = max(0, q_loaded - 2); jj < q_loaded; ++jj)
                     drain_wait(bar(B_QFULL + (jj & 1)), (jj >> 1) & 1, wd);
-                for (int nn = max(0, k_loaded - C::STAGES); nn < k_loaded; ++nn)
-                    drain_wait(bar(B_KFULL + nn % C::STAGES), (nn / C::STAGES) & 1, wd);
-                for (int nn = max(0, v_loaded - C::STAGES); nn < v_loaded; ++nn)
-                    drain_wait(bar(B_VFULL + nn % C::STAGES), (nn / C::STAGES) & 1, wd);
+                for (int it = max(0, items - C::SLOTS); it < items; ++it)
+                    drain_wait(bar(B_FULL + slot_of(it)), parity_of(it), wd);
             }
         }
     } else if (warp == WARP_MMA) {
@@ -457,25 +476,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
         // V^T as an MN-major A operand: d is contiguous; the second 64-row block of d
         // (or the zero block when d = 64) sits LBO bytes after the first
         auto v_lbo = [&](int st) -> uint32_t {
-            return D == 128 ? (uint32_t)C::SUB : (uint32_t)(s_z - (s_v + st * C::TB));
+            return D == 128 ? (uint32_t)C::SUB : (uint32_t)(s_z - (s_kv + st * C::TB));
         };
         int last_bar = -1, last_par = 0;  // the last commit (drained after an abort)
         // QK of the CTA's tile n at walk position w (lane 0 only)
         auto issue_qk = [&](int n, const Walk& w) -> bool {
-            const int st = n % C::STAGES;
+            const int st = slot_of(2 * n);
             if (w.q == 0 && !wait_bounded(bar(B_QFULL + (w.j & 1)), (w.j >> 1) & 1, wd, ERR_MMA)) return false;
-            if (!wait_bounded(bar(B_KFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA)) return false;
+            if (!wait_bounded(bar(B_FULL + st), parity_of(2 * n), wd, ERR_MMA)) return false;
             tc_fence_after();
             const uint32_t t_s = tmem + C::TMEM_S + (n & 1) * NP;
             const uint32_t sq = s_q + (w.j & 1) * C::QT;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a = s_k + st * C::TB + (kk >> 2) * C::SUB + (kk & 3) * 32;
+                const uint32_t a = s_kv + st * C::TB + (kk >> 2) * C::SUB + (kk & 3) * 32;
                 const uint32_t bq = sq + (kk >> 2) * C::QB + (kk & 3) * 32;
                 mma_ss(t_s, sdesc_sw128(a, 16, 1024), sdesc_sw128(bq, 16, 1024), idesc_qk, kk > 0);
             }
             mma_commit(bar(B_SFULL + (n & 1)));
-            mma_commit(bar(B_KEMPTY + st));
+            mma_commit(bar(B_EMPTY + st));
             last_bar = B_SFULL + (n & 1);
             last_par = (n >> 1) & 1;
             if (w.q == w.s.count - 1) mma_commit(bar(B_QEMPTY + (w.j & 1)));
@@ -489,11 +508,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
         ok = __shfl_sync(0xffffffffu, ok, 0);
         // The whole warp runs the loop (the exit is warp-uniform); lane 0 waits and issues.
         for (int n = 0; n < n_tiles && ok; ++n) {
-            const int st = n % C::STAGES;
+            const int st = slot_of(2 * n + 1);  // V of tile n
             if (lane == 0) {
                 if (wq.valid) ok = issue_qk(n + 1, wq);  // S^T buffer (n+1)&1 was released before PV(n-1)
                 if (ok) ok = wait_bounded(bar(B_PFULL + (n & 1)), (n >> 1) & 1, wd, ERR_MMA);
-                if (ok) ok = wait_bounded(bar(B_VFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA);
+                if (ok) ok = wait_bounded(bar(B_FULL + st), parity_of(2 * n + 1), wd, ERR_MMA);
             }
             walk_next(p, wq, share1);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -503,12 +522,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
             if (tail != 0 && tile == (wp.s.L - 1) / BN) {
                 // a sequence's last cache tile: zero the V rows at and past its length.  Every
                 // lane observes the completed copy itself (the phase cannot advance before this PV).
-                const bool seen = lane == 0 || wait_bounded(bar(B_VFULL + st), (n / C::STAGES) & 1, wd, ERR_MMA);
+                const bool seen = lane == 0 || wait_bounded(bar(B_FULL + st), parity_of(2 * n + 1), wd, ERR_MMA);
                 if (!__all_sync(0xffffffffu, seen)) {
                     ok = false;
                     break;
                 }
-                uint8_t* vt = smem + C::OFF_V + st * C::TB;
+                uint8_t* vt = smem + C::OFF_KV + st * C::TB;
                 const int nbytes = (BN - tail) * 128;
                 for (int c = 0; c < D / 64; ++c)
                     for (int x = lane * 16; x < nbytes; x += 32 * 16)
@@ -522,12 +541,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 const uint32_t pb = s_p + (n & 1) * 2 * C::PB;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint32_t a = s_v + st * C::TB + kk * 16 * 128;  // 16 keys of 128-byte rows
+                    const uint32_t a = s_kv + st * C::TB + kk * 16 * 128;  // 16 keys of 128-byte rows
                     const uint32_t bp = pb + (kk >> 2) * C::PB + (kk & 3) * 32;
                     mma_ss(t_o, sdesc_sw128(a, v_lbo(st), 1024), sdesc_sw128(bp, 16, 1024), idesc_pv,
                            (wp.q > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(B_VEMPTY + st));
+                mma_commit(bar(B_EMPTY + st));
                 mma_commit(bar(B_PFREE + (n & 1)));
                 last_bar = B_PFREE + (n & 1);
                 last_par = (n >> 1) & 1;
@@ -592,53 +611,62 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                 const int jkey = tile * BN + t;  // this thread's key
                 const bool full = tile * BN >= max_lo && tile * BN + BN - 1 <= min_hi;
                 const uint32_t t_s = t_lane + C::TMEM_S + par * NP;
-                const uint32_t pb = s_p + par * 2 * C::PB + (t >> 6) * C::PB;
                 const int kk = t & 63;
+                // this thread's column of the P^T buffer: K-major, 128B swizzle (16-byte chunk kk / 8
+                // of row r sits at chunk (kk / 8) ^ (r mod 8)), the two bytes of key kk
+                uint8_t* const pcol = smem + C::OFF_P + par * 2 * C::PB + (t >> 6) * C::PB + (kk & 7) * 2;
+                const int kc = kk >> 3;
                 float ts[NP];  // this tile's share of every row's sum
-                // P = exp2(s * scale * log2 e - m) against the running max m -> bf16 P^T (K-major,
-                // 128B swizzle); returns whether an allowed score exceeds m by more than the threshold
-                auto exp_pass = [&]() -> bool {
-                    bool over = false;
+                // P = exp2(s * scale * log2 e - m) against the running max m -> bf16 P^T; returns
+                // whether an allowed score exceeds m by more than the threshold.  A chunk's columns
+                // are all loaded before one wait; masked scores become -inf (ex2 gives 0).  Plain
+                // shared stores: the proxy fence before the P-full arrival orders them for the MMA.
+                auto exp_pass = [&](auto full_c) -> bool {
+                    constexpr bool FULL = decltype(full_c)::value;
+                    constexpr int CH = NP < 32 ? NP : 32;  // columns per tensor-memory wait
+                    float xmax = -INFINITY;
 #pragma unroll
-                    for (int c = 0; c < NP / 16; ++c) {
-                        uint32_t v[16];
-                        float mr[16];
-                        tmem_ld16(t_s + c * 16, v);
+                    for (int c0 = 0; c0 < NP; c0 += CH) {
+                        uint32_t v[CH];
+                        float mr[CH];
+                        tmem_ld16_at<0>(t_s + c0, v);
+                        if constexpr (CH == 32) tmem_ld16_at<16>(t_s + c0 + 16, v);
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            const float4 m4 = *reinterpret_cast<const float4*>(sh->m + c * 16 + e);
+                        for (int e = 0; e < CH; e += 4) {
+                            const float4 m4 = *reinterpret_cast<const float4*>(sh->m + c0 + e);
                             mr[e] = m4.x; mr[e + 1] = m4.y; mr[e + 2] = m4.z; mr[e + 3] = m4.w;
                         }
                         if constexpr (ALIBI) {  // fold the bias into the subtracted max
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                mr[e] = fmaf(sh->bm[c * 16 + e], fabsf(sh->bp[c * 16 + e] - (float)jkey), mr[e]);
+                            for (int e = 0; e < CH; ++e)
+                                mr[e] = fmaf(sh->bm[c0 + e], fabsf(sh->bp[c0 + e] - (float)jkey), mr[e]);
                         }
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            float pr[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int r = c * 16 + e + u;
-                                const bool in = full || (jkey >= sh->lo[r] && jkey <= sh->hi[r]);
-                                const float x = fmaf(__uint_as_float(v[e + u]), sl2, -mr[e + u]);
-                                over |= in && x > RESCALE_THRESHOLD;
-                                pr[u] = in ? ex2(x) : 0.f;
-                                ts[r] = pr[u];
+                        for (int e = 0; e < CH; e += 2) {
+                            const int r = c0 + e;
+                            float x0 = fmaf(__uint_as_float(v[e]), sl2, -mr[e]);
+                            float x1 = fmaf(__uint_as_float(v[e + 1]), sl2, -mr[e + 1]);
+                            if constexpr (!FULL) {
+                                x0 = (jkey >= sh->lo[r] && jkey <= sh->hi[r]) ? x0 : -INFINITY;
+                                x1 = (jkey >= sh->lo[r + 1] && jkey <= sh->hi[r + 1]) ? x1 : -INFINITY;
                             }
-                            const uint32_t pk = pack_bf16x2(pr[0], pr[1]);
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int r = c * 16 + e + u;
-                                const uint32_t addr = pb + r * 128 + (((kk >> 3) ^ (r & 7)) << 4) + (kk & 7) * 2;
-                                st_shared_u16(addr, (uint16_t)(u ? (pk >> 16) : (pk & 0xffffu)));
-                            }
+                            xmax = fmax3(xmax, x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            ts[r] = p0;
+                            ts[r + 1] = p1;
+                            const uint32_t pk = pack_bf16x2(p0, p1);
+                            *reinterpret_cast<uint16_t*>(pcol + r * 128 + ((kc ^ (r & 7)) << 4)) = (uint16_t)pk;
+                            *reinterpret_cast<uint16_t*>(pcol + (r + 1) * 128 + ((kc ^ ((r + 1) & 7)) << 4)) =
+                                (uint16_t)(pk >> 16);
                         }
                     }
-                    return over;
+                    return xmax > RESCALE_THRESHOLD;
                 };
-                if (named_bar_or(1, 128, exp_pass())) {
+                auto exp_pass_tile = [&]() -> bool {
+                    return full ? exp_pass(std::true_type{}) : exp_pass(std::false_type{});
+                };
+                if (named_bar_or(1, 128, exp_pass_tile())) {
                     // ---- a row's max grew (always on a unit's first tile): exact masked tile maxima,
                     // new running maxima and rescale factors, then P again.  Every reader of the
                     // previous flag has passed the barrier above.
@@ -689,7 +717,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
                         }
                         tmem_wait_st();
                     }
-                    exp_pass();  // cannot exceed now (every row's m is at least its tile max)
+                    exp_pass_tile();  // cannot exceed now (every row's m is at least its tile max)
                 }
 #pragma unroll
                 for (int r = 0; r < NP; ++r) lp[r] += ts[r];
@@ -771,10 +799,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_c
 // warp w of CTA x takes packed row 4 (x mod R) + w of split unit x / R, R = ceil(rows / 4).
 //   M = max_c LSE_c, W = sum_c e^{LSE_c - M}, O = sum_c e^{LSE_c - M} O_c / W, LSE = M + ln W
 // over the unit's partials c (each normalised by its own sum).  Lane l owns d components
-// [l D/32, (l+1) D/32); eight partials' loads are in flight at a time.
+// [l D/32, (l+1) D/32).  Lane c loads LSE_c (c < 32) while the O values of the first PF
+// partials are already in flight, so a unit of up to PF partials costs one round trip to L2.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeMergeParams p) {
+    // launched as a programmatic dependent of the decode kernel: wait for that grid to complete
+    // (its partial results written and visible); a no-op when launched without the attribute
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int PER = D / 32;
+    constexpr int PF = 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_unit = (p.rows + 3) >> 2;
     const int u = blockIdx.x / per_unit, r = (blockIdx.x - u * per_unit) * 4 + warp;
@@ -783,45 +816,63 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
     const int b = e.x, g = e.y, k0 = e.z, nseg = e.w >> 1;
     const bool k0_first = (e.w & 1) != 0;
     auto slot = [&](int c) -> size_t { return (size_t)(c == 0 ? 2 * k0 + (k0_first ? 0 : 1) : 2 * (k0 + c)); };
-    float M = -INFINITY;
-    for (int c = lane; c < nseg; c += 32) M = fmaxf(M, __ldcg(p.part_lse + slot(c) * p.np + r));
+    auto lse_of = [&](int c) { return __ldcg(p.part_lse + slot(c) * p.np + r); };
+    auto load_o = [&](int c, float (&o)[PER]) {
+        const float* src = p.part_o + (slot(c) * p.np + r) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+            o[0] = x.x; o[1 % PER] = x.y; o[2 % PER] = x.z; o[3 % PER] = x.w;
+        } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            o[0] = x.x; o[1 % PER] = x.y;
+        }
+    };
+    const float l0 = lane < nseg ? lse_of(lane) : -INFINITY;
+    float ov[PF][PER];
+#pragma unroll
+    for (int v = 0; v < PF; ++v) {
+#pragma unroll
+        for (int q = 0; q < PER; ++q) ov[v][q] = 0.f;
+        if (v < nseg) load_o(v, ov[v]);
+    }
+    float M = l0;
+    for (int c = lane + 32; c < nseg; c += 32) M = fmaxf(M, lse_of(c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float W = 0.f;
-    for (int c = lane; c < nseg; c += 32) {
-        const float lv = __ldcg(p.part_lse + slot(c) * p.np + r);
+    float W = l0 == -INFINITY ? 0.f : __expf(l0 - M);
+    for (int c = lane + 32; c < nseg; c += 32) {
+        const float lv = lse_of(c);
         W += lv == -INFINITY ? 0.f : __expf(lv - M);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
     const float inv_w = W > 0.f ? 1.f / W : 0.f;
+    const float w0 = l0 == -INFINITY ? 0.f : __expf(l0 - M) * inv_w;  // weight of partial `lane`
+    // the weight of partial c (uniform over the warp)
+    auto weight = [&](int c) -> float {
+        if (c < 32) return __shfl_sync(0xffffffffu, w0, c);
+        const float lv = lse_of(c);
+        return lv == -INFINITY ? 0.f : __expf(lv - M) * inv_w;
+    };
     float acc[PER];
 #pragma unroll
     for (int q = 0; q < PER; ++q) acc[q] = 0.f;
-    for (int c0 = 0; c0 < nseg; c0 += 8) {
-        float ov[8][PER], lv[8];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const int c = c0 + v;
-            lv[v] = -INFINITY;
+    for (int v = 0; v < PF; ++v) {
+        const float w = weight(v);  // 0 past nseg (lane v >= nseg holds l0 = -inf)
+#pragma unroll
+        for (int q = 0; q < PER; ++q) acc[q] = fmaf(w, ov[v][q], acc[q]);
+    }
+    for (int c0 = PF; c0 < nseg; c0 += PF) {
+#pragma unroll
+        for (int v = 0; v < PF; ++v) {
 #pragma unroll
             for (int q = 0; q < PER; ++q) ov[v][q] = 0.f;
-            if (c < nseg) {
-                const size_t sl = slot(c);
-                lv[v] = __ldcg(p.part_lse + sl * p.np + r);
-                const float* src = p.part_o + (sl * p.np + r) * D + lane * PER;
-                if constexpr (PER == 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-                    ov[v][0] = x.x; ov[v][1 % PER] = x.y; ov[v][2 % PER] = x.z; ov[v][3 % PER] = x.w;
-                } else {
-                    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-                    ov[v][0] = x.x; ov[v][1 % PER] = x.y;
-                }
-            }
+            if (c0 + v < nseg) load_o(c0 + v, ov[v]);
         }
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const float w = lv[v] == -INFINITY ? 0.f : __expf(lv[v] - M) * inv_w;
+        for (int v = 0; v < PF; ++v) {
+            const float w = c0 + v < nseg ? weight(c0 + v) : 0.f;
 #pragma unroll
             for (int q = 0; q < PER; ++q) acc[q] = fmaf(w, ov[v][q], acc[q]);
         }
@@ -851,11 +902,20 @@ cudaError_t launch(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode_merge(const DecodeMergeParams& p, int d, cudaStream_t stream) {
     if (p.n_split <= 0) return cudaSuccess;
-    const int grid = p.n_split * ((p.rows + 3) / 4);
-    if (d == 128) decode_merge_kernel<128><<<grid, 128, 0, stream>>>(p);
-    else if (d == 64) decode_merge_kernel<64><<<grid, 128, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    // a programmatic dependent launch: the grid is set up while the decode kernel still runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_split * ((p.rows + 3) / 4)));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (d == 128) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, p);
+    if (d == 64) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream) {

@@ -172,25 +172,27 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
         h->last_v = V;
     }
     attn::DecodeSchedule sched;
-    const int ctas = h->grid_limit > 0 ? std::min(h->grid_limit, h->n_sm) : h->n_sm;
+    const int ctas = std::min(h->grid_limit > 0 ? std::min(h->grid_limit, h->n_sm) : h->n_sm, attn::kDecodeMaxCta);
     attn::build_decode_schedule(h->B, h->Hkv, h->S_q, h->kind, h->window, cache_len, ctas, &sched);
     if (2 * (size_t)sched.n_cta > h->part_slots) return ATTN_ERR_UNSUPPORTED;  // cannot happen: n_cta <= n_sm
     for (int b = 0; b < h->B; ++b) p.len[b] = cache_len[b];
     for (int b = 0; b <= h->B; ++b) p.tile_prefix[b] = sched.tile_prefix[b];
+    for (int k = 0; k <= sched.n_cta; ++k) p.share[k] = sched.share[k];
     p.n_cta = sched.n_cta;
     p.total_tiles = sched.total_tiles;
     p.o = O;
     p.lse = LSE;
-    // Units split over several CTAs, with the kernel's share arithmetic (CTA k takes the
-    // indices [k T / n, (k + 1) T / n)).  Many partials per unit make the in-kernel merge a
-    // long serial tail on one CTA; from 6 partials on they go to the merge kernel instead
-    // (below that the second launch costs more than it saves).
+    // Units split over several CTAs (CTA k takes the indices [share[k], share[k + 1])).  By
+    // default their partial results are combined by the merge kernel, launched as a dependent
+    // of the decode kernel so that its launch overlaps the decode kernel's tail: a merge by the
+    // last CTA to finish a part sits at the end of that CTA's share (a serial tail of L2 round
+    // trips the share weights do not see).
     attn::DecodeMergeParams& mp = h->mp;
-    const long long T = sched.total_tiles;
-    const int n = sched.n_cta;
-    auto share_of = [&](long long i) { return (int)(((i + 1) * n + T - 1) / T - 1); };
+    const std::vector<long long>& share = sched.share;
+    auto share_of = [&](long long i) {  // the CTA whose share holds index i
+        return (int)(std::upper_bound(share.begin(), share.end() - 1, i) - share.begin()) - 1;
+    };
     mp.n_split = 0;
-    int max_seg = 1;
     bool overflow = false;
     for (int b = 0; b < h->B; ++b) {
         const int n_unit = sched.tile_prefix[b + 1] - sched.tile_prefix[b];
@@ -198,13 +200,12 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
             const long long ub = (long long)h->Hkv * sched.tile_prefix[b] + (long long)g * n_unit;
             const int k0 = share_of(ub), k1 = share_of(ub + n_unit - 1);
             if (k1 == k0) continue;
-            max_seg = std::max(max_seg, k1 - k0 + 1);
             if (mp.n_split == attn::kDecodeMaxSplit) { overflow = true; continue; }
-            const bool first = (long long)k0 * T / n == ub;
+            const bool first = share[k0] == ub;
             mp.list[mp.n_split++] = make_int4(b, g, k0, 2 * (k1 - k0 + 1) + (first ? 1 : 0));
         }
     }
-    const bool defer = !overflow && mp.n_split > 0 && (h->merge_mode == 2 || (h->merge_mode == 0 && max_seg >= 6));
+    const bool defer = !overflow && mp.n_split > 0 && h->merge_mode != 1;
     p.defer_merge = defer ? 1 : 0;
     cudaError_t e = attn::launch_decode(p, h->d, h->np, static_cast<cudaStream_t>(stream));
     h->last_launches = defer ? 2 : 1;
@@ -278,17 +279,19 @@ attn_status attn_decode_destroy(attn_decode_handle h) {
 }
 
 attn_status attn_decode_schedule_host(int B, int Hkv, int S_q, int S_cap, attn_mask_kind kind, int window,
-                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix) {
-    if (!n_cta || !tile_prefix || n_sm < 1) return ATTN_ERR_INVALID_ARG;
+                                      const int* cache_len, int n_sm, int* n_cta, int* tile_prefix,
+                                      long long* share) {
+    if (!n_cta || !tile_prefix || !share || n_sm < 1) return ATTN_ERR_INVALID_ARG;
     attn_status vs = validate_decode(B, Hkv, Hkv, S_q, S_cap, kind, window);
     if (vs != ATTN_OK) return vs;
     vs = validate_lengths(B, S_q, S_cap, kind, cache_len);
     if (vs != ATTN_OK) return vs;
     attn::DecodeSchedule sched;
-    attn::build_decode_schedule(B, Hkv, S_q, kind, kind == ATTN_MASK_CAUSAL_SLIDING ? window : 0, cache_len, n_sm,
-                                &sched);
+    attn::build_decode_schedule(B, Hkv, S_q, kind, kind == ATTN_MASK_CAUSAL_SLIDING ? window : 0, cache_len,
+                                std::min(n_sm, attn::kDecodeMaxCta), &sched);
     *n_cta = sched.n_cta;
     for (int b = 0; b <= B; ++b) tile_prefix[b] = sched.tile_prefix[b];
+    for (int k = 0; k <= sched.n_cta; ++k) share[k] = sched.share[k];
     return ATTN_OK;
 }
 

@@ -80,6 +80,7 @@ struct F32Params {
 // [k * T / n_cta, (k+1) * T / n_cta), T = Hkv * tile_prefix[B].  A CTA processes the
 // query rows of a kv head's group (group * S_q rows, padded to NP columns).
 constexpr int kDecodeMaxBatch = 1024;
+constexpr int kDecodeMaxCta = 256;  // the persistent grid is min(multiprocessors, this, tiles) CTAs
 struct DecodeParams {
     CUtensorMap tm_q;    // Q as 2-D [B*Hq*S_q, d] bf16, box {64, NP}, 128B swizzle
     CUtensorMap tm_k;    // K cache [B*Hkv, S_cap, d], box {64, 128, 1}
@@ -100,6 +101,7 @@ struct DecodeParams {
     int defer_merge;                         // split units: leave the partials to the merge kernel
     int len[kDecodeMaxBatch];                // cache length of each sequence
     int tile_prefix[kDecodeMaxBatch + 1];    // key tiles of the sequences before b (per kv head)
+    long long share[kDecodeMaxCta + 1];      // CTA k takes the list indices [share[k], share[k+1])
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);

@@ -2,6 +2,7 @@
 #include "schedule.h"
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 
 namespace attn {
@@ -341,6 +342,31 @@ void build_decode_schedule(int B, int Hkv, int S_q, int kind, int window, const 
     }
     out->total_tiles = (long long)Hkv * out->tile_prefix[B];
     out->n_cta = (int)std::min<long long>(std::max(1, n_sm), out->total_tiles);
+    // Share boundaries at equal steps of F(i) = i + a * (unit begins in (0, i]): within unit j
+    // (indices [ub[j], ub[j+1])) F(i) = i + a * j, so the weight of a share is its tiles plus a
+    // for every unit begun inside it.  Every share keeps at least one tile.
+    const int n = out->n_cta;
+    const long long T = out->total_tiles;
+    const double a = kDecodeStretchCost;
+    std::vector<long long> ub;  // unit begins in list order; ub[0] = 0
+    ub.reserve((size_t)B * Hkv + 1);
+    for (int b = 0; b < B; ++b) {
+        const int n_b = out->tile_prefix[b + 1] - out->tile_prefix[b];
+        for (int g = 0; g < Hkv && n_b > 0; ++g) ub.push_back((long long)Hkv * out->tile_prefix[b] + (long long)g * n_b);
+    }
+    ub.push_back(T);  // sentinel
+    const double F_T = (double)T + a * (double)(ub.size() - 2);
+    out->share.assign(n + 1, 0);
+    out->share[n] = T;
+    size_t j = 0;
+    for (int k = 1; k < n; ++k) {
+        const double tau = F_T * k / n;
+        while (j + 2 < ub.size() && (double)(ub[j + 1] - 1) + a * (double)j < tau) ++j;
+        long long i = std::max(ub[j], (long long)std::ceil(tau - a * (double)j));
+        i = std::max(i, out->share[k - 1] + 1);
+        i = std::min(i, T - (n - k));
+        out->share[k] = i;
+    }
 }
 
 }  // namespace attn

@@ -75,7 +75,13 @@ struct DecodeSchedule {
     int n_cta = 1;
     long long total_tiles = 0;
     std::vector<int> tile_prefix;  // B + 1 entries
+    std::vector<long long> share;  // n_cta + 1 entries: CTA k takes the list indices [share[k], share[k+1])
 };
+
+// What one more stretch costs a CTA of the persistent decode grid (the epilogue of the
+// previous stretch, the first tile's exact maxima and the refill of the pipeline), in key
+// tiles: a CTA's share is weighted tiles + kDecodeStretchCost * (units begun inside it).
+constexpr double kDecodeStretchCost = 2.0;
 
 // First and one-past-last key tile a sequence with L cached positions needs.
 void decode_tile_range(int kind, int S_q, int window, int L, int* lo, int* hi);
