@@ -13,6 +13,7 @@ The kernel's arithmetic is restated here: unit (b, g) covers the indices
     result slots the writers use (2k for a first stretch, 2k+1 for a last one)
     are exactly the slots the merge of each unit enumerates.
 """
+import bisect
 import random
 
 import pytest
@@ -68,7 +69,8 @@ def _unit_begins(Hkv, prefix):
 
 def _weight(i, begins):
     """F(i): tiles before i plus the stretch cost of every unit begun in (0, i]."""
-    return i + STRETCH_COST * sum(1 for u in begins if 0 < u <= i)
+    pos = sorted(u for u in begins if u > 0)
+    return i + STRETCH_COST * bisect.bisect_right(pos, i)
 
 
 def _check_shares(share, n_cta, total, begins):
@@ -76,11 +78,19 @@ def _check_shares(share, n_cta, total, begins):
     assert len(share) == n_cta + 1 and share[0] == 0 and share[-1] == total
     assert all(share[k] < share[k + 1] for k in range(n_cta)), "an empty share"
     F_T = total + STRETCH_COST * (len(begins) - 1)
+    pos = sorted(u for u in begins if u > 0)
+    F = lambda i: i + STRETCH_COST * bisect.bisect_right(pos, i)  # non-decreasing in i
     for k in range(1, n_cta):
         tau = F_T * k / n_cta
         lo, hi = share[k - 1] + 1, total - (n_cta - k)  # room for one tile per remaining CTA
-        ideal = next(i for i in range(total + 1) if _weight(i, begins) >= tau - 1e-9)
-        assert share[k] == min(max(ideal, lo), hi), (k, share[k], ideal, lo, hi)
+        a, b = 0, total  # smallest i with F(i) >= tau, by bisection (F(total) >= tau)
+        while a < b:
+            mid = (a + b) // 2
+            if F(mid) >= tau - 1e-9:
+                b = mid
+            else:
+                a = mid + 1
+        assert share[k] == min(max(a, lo), hi), (k, share[k], a, lo, hi)
 
 
 def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
@@ -208,3 +218,29 @@ def test_decode_create_rejects_bad_arguments_before_any_cuda_call(kw, status):
     with pytest.raises(tsa.AttnError) as e:
         tsa.attn_decode_create(**kw)
     assert e.value.status == status
+
+
+def test_decode_split_grid_capped_at_256_ctas():
+    """More multiprocessors than the parameter table holds: the grid stops at 256 CTAs, and the
+    shares still cover the list with the weighted boundaries."""
+    lens = [4096] * 64
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(64, 8, 1, 4096, tsa.MASK_CAUSAL, 0, lens, 400)
+    prefix = [int(x) for x in prefix]
+    total = 8 * prefix[-1]
+    assert n_cta == 256 and len(share) == 257
+    _check_shares(share, n_cta, total, _unit_begins(8, prefix))
+
+
+def test_decode_split_many_short_units():
+    """Many two-tile units (ragged short caches): shares span several units, every tile is still
+    covered once, partial units stay at the ends of a share, and the weights balance."""
+    rng = random.Random(7)
+    lens = [rng.randint(129, 256) for _ in range(96)]
+    _check(96, 4, 1, 256, tsa.MASK_CAUSAL, 0, lens, 152)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(96, 4, 1, 256, tsa.MASK_CAUSAL, 0, lens, 152)
+    prefix = [int(x) for x in prefix]
+    begins = _unit_begins(4, prefix)
+    # each boundary sits within one step (a tile plus a unit begin) above its target of F, so two
+    # shares' weights F(share[k + 1]) - F(share[k]) differ by less than two steps
+    weight = [_weight(int(share[k + 1]), begins) - _weight(int(share[k]), begins) for k in range(n_cta)]
+    assert max(weight) - min(weight) < 2 * (1 + STRETCH_COST)
