@@ -21,12 +21,14 @@
 //   O^T [d x NP]        += V_tile^T [d x 128] . P^T [128 x NP]   (V MN-major)
 //
 // Balance: the grid is persistent (one CTA per SM).  All (sequence, kv head)
-// units are laid end to end as one list of key tiles and every CTA takes an
-// equal contiguous share of it, so a CTA may finish the end of one unit and
+// units are laid end to end as one list of key tiles and every CTA takes a
+// contiguous share of it (the host weights a share by its tiles plus the cost
+// of every unit begun inside it), so a CTA may finish the end of one unit and
 // start the next.  A unit cut between CTAs yields partial results (O
-// normalised by its own sum, and its LSE) that the last CTA of the unit to
-// finish combines with weights e^{LSE_c - LSE} (an arrival counter per unit
-// that wraps back to zero).
+// normalised by its own sum, and its LSE), combined with weights
+// e^{LSE_c - LSE} by decode_merge_kernel, a programmatic dependent launch behind
+// this kernel, or (merge mode 1) by the last CTA of the unit to finish (an
+// arrival counter per unit that wraps back to zero).
 //
 //   warp 4 (producer) : TMA loads of each unit's packed Q rows (double-
 //                       buffered) and of the K and V tiles into one ring of
