@@ -227,7 +227,41 @@ def test_decode_launch_count_follows_the_merge():
     Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
     plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind, window=w.window)
     assert plan.launch_count() == 0
-    for mode, n in ((1, 1), (2, 2), (0, 2)):  # this workload splits units into more than 6 partials
+    for mode, n in ((1, 1), (2, 2), (0, 2)):  # this workload splits units over several CTAs
         plan.set_merge_mode(mode)
         _run(w, Q, K, V, lens, plan=plan)
         assert plan.launch_count() == n
+    # no unit split (one tile per unit, as many CTAs as units): no merge kernel
+    wt = _dw("one", 2, 4, 2, 1, 100, 64, wl.MASK_CAUSAL, len_min=50)
+    Qt, Kt, Vt, lt = wl.make_decode_inputs(wt, stale_fill=float("nan"))
+    outs, pt = _run(wt, Qt.cuda(), Kt.cuda(), Vt.cuda(), lt)
+    assert pt.launch_count() == 1
+    O_ref, L_ref = oracle.decode(Qt.float().numpy(), Kt.float().numpy(), Vt.float().numpy(), lt, wt.scale, wt.kind)
+    _compare(*outs[0], O_ref, L_ref)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_decode_back_to_back_calls_without_sync(mode):
+    """Three steps enqueued on one handle before any synchronisation, each with its own query rows
+    and lengths: every step's merge reads its own partials (the merge kernel waits for its decode
+    grid, and the next decode grid for that merge), and every output matches the oracle."""
+    import transformer_self_attention_gb300 as tsa
+    w = _dw("b2b", 4, 32, 1, 1, 6000, 128, wl.MASK_CAUSAL, len_min=3000)
+    plan = tsa.DecodeAttention(w.B, w.Hq, w.Hkv, w.S_q, w.S_cap, w.d, scale=w.scale, kind=w.kind)
+    plan.set_merge_mode(mode)
+    steps = []
+    for k in range(3):
+        Qc, Kc, Vc, lens = wl.make_decode_inputs(w.with_(seed=40 + k), stale_fill=float("nan"))
+        Q, K, V = Qc.cuda(), Kc.cuda(), Vc.cuda()
+        O = torch.full_like(Q, float("nan"))
+        LSE = torch.full((w.B, w.Hq, w.S_q), float("nan"), dtype=torch.float32, device=Q.device)
+        plan(Q, K, V, lens, O=O, LSE=LSE)
+        steps.append((Qc, Kc, Vc, lens, O, LSE, (Q, K, V)))
+    torch.cuda.synchronize()
+    st, code = plan.poll_device_error()
+    assert st == 0 and code == 0
+    assert plan.launch_count() == (2 if mode == 0 else 1)
+    for Qc, Kc, Vc, lens, O, LSE, _ in steps:
+        O_ref, L_ref = oracle.decode(Qc.float().numpy(), Kc.float().numpy(), Vc.float().numpy(), lens, w.scale,
+                                     w.kind)
+        _compare(O.float().cpu().numpy(), LSE.cpu().numpy(), O_ref, L_ref)
