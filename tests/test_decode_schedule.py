@@ -97,7 +97,7 @@ def _check(B, Hkv, S_q, S_cap, kind, window, lens, n_sm):
     n_cta, prefix, share = tsa.attn_decode_schedule_host(B, Hkv, S_q, S_cap, kind, window, lens, n_sm)
     prefix = [int(x) for x in prefix]
     total = Hkv * prefix[B]
-    assert n_cta == min(n_sm, 256, total)
+    assert n_cta == min(n_sm, 512, total)
     _check_shares(share, n_cta, total, _unit_begins(Hkv, prefix))
     # ranges of the sequences
     for b, L in enumerate(lens):
@@ -220,14 +220,14 @@ def test_decode_create_rejects_bad_arguments_before_any_cuda_call(kw, status):
     assert e.value.status == status
 
 
-def test_decode_split_grid_capped_at_256_ctas():
-    """More multiprocessors than the parameter table holds: the grid stops at 256 CTAs, and the
+def test_decode_split_grid_capped_at_512_ctas():
+    """More multiprocessors than the parameter table holds: the grid stops at 512 CTAs, and the
     shares still cover the list with the weighted boundaries."""
     lens = [4096] * 64
-    n_cta, prefix, share = tsa.attn_decode_schedule_host(64, 8, 1, 4096, tsa.MASK_CAUSAL, 0, lens, 400)
+    n_cta, prefix, share = tsa.attn_decode_schedule_host(64, 8, 1, 4096, tsa.MASK_CAUSAL, 0, lens, 700)
     prefix = [int(x) for x in prefix]
     total = 8 * prefix[-1]
-    assert n_cta == 256 and len(share) == 257
+    assert n_cta == 512 and len(share) == 513
     _check_shares(share, n_cta, total, _unit_begins(8, prefix))
 
 

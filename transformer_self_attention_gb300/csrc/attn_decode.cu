@@ -74,7 +74,8 @@ constexpr int WARP_PRODUCER = 4;
 constexpr int WARP_MMA = 5;
 constexpr int MAX_SLOTS = 12;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
-constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;   // one CTA per SM
+constexpr int SMEM_HALF = 228 * 1024 / 2 - 1024;  // each of two CTAs per SM (1 KB reserved per CTA)
 
 enum : int { ERR_PRODUCER = 1, ERR_MMA = 2, ERR_SOFTMAX = 4 };
 
@@ -86,9 +87,13 @@ struct DCfg {
     static constexpr int QB = NP * 128;           // one 64-column block of it
     static constexpr int PB = NP * 128;           // one 64-key half of a P^T buffer
     static constexpr int ZERO = (D == 64) ? SUB : 0;  // rows 64..127 of V^T when d = 64 (zeros)
-    static constexpr int CTL = 8192;
+    static constexpr int CTL = NP == 64 ? 8192 : 4096;  // DShared<NP>
+    // At d = 64 with up to 32 packed rows the single MMA-issuing thread, not the memory, sets a
+    // tile's pace (12 small products per 32 KB of K and V): two CTAs per SM, each with its own
+    // issuing thread and half the shared memory.
+    static constexpr int CTAS = (D == 64 && NP <= 32) ? 2 : 1;
     static constexpr int FIXED = 2 * QT + 2 * 2 * PB + ZERO + CTL + 1024;
-    static constexpr int SLOTS_FIT = (SMEM_LIMIT - FIXED) / TB;
+    static constexpr int SLOTS_FIT = ((CTAS == 2 ? SMEM_HALF : SMEM_LIMIT) - FIXED) / TB;
     static constexpr int SLOTS = SLOTS_FIT > MAX_SLOTS ? MAX_SLOTS : SLOTS_FIT;  // K/V ring
     static_assert(SLOTS >= 4, "shared memory");
     static constexpr int OFF_KV = 0;
@@ -383,8 +388,9 @@ __device__ void merge_unit(const DecodeParams& p, const Seg& s, int warp, int la
 }
 
 template <int D, int NP, bool ALIBI>
-__global__ void __launch_bounds__(NTHREADS, 1) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(NTHREADS, DCfg<D, NP>::CTAS) attn_decode_kernel(const __grid_constant__ DecodeParams p) {
     using C = DCfg<D, NP>;
+    static_assert(sizeof(DShared<NP>) <= C::CTL, "control block");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned
     DShared<NP>* sh = reinterpret_cast<DShared<NP>*>(smem + C::OFF_CTL);
@@ -918,6 +924,12 @@ cudaError_t launch_decode_merge(const DecodeMergeParams& p, int d, cudaStream_t 
     if (d == 128) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, p);
     if (d == 64) return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, p);
     return cudaErrorInvalidValue;
+}
+
+// CTAs of the persistent grid per multiprocessor for a head width and packed-row width.
+int decode_ctas_per_sm(int d, int np) {
+    if (d == 64) return np == 16 ? DCfg<64, 16>::CTAS : np == 32 ? DCfg<64, 32>::CTAS : DCfg<64, 64>::CTAS;
+    return np == 16 ? DCfg<128, 16>::CTAS : np == 32 ? DCfg<128, 32>::CTAS : DCfg<128, 64>::CTAS;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream) {

@@ -13,8 +13,13 @@
 #include "kernels.h"
 #include "schedule.h"
 
+namespace attn {
+int decode_ctas_per_sm(int d, int np);  // attn_decode.cu
+}
+
 struct attn_decode_plan {
     int B = 0, Hq = 0, Hkv = 0, S_q = 0, S_cap = 0, d = 0, np = 0;
+    int ctas_per_sm = 1;  // CTAs of the persistent grid per multiprocessor
     int kind = 0, window = 0;
     float scale = 0.f;
     int n_sm = 0;
@@ -127,7 +132,8 @@ attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(e);
     // two partial-result slots per CTA of the persistent grid (its first and last stretch)
-    h->part_slots = 2 * (size_t)h->n_sm;
+    h->ctas_per_sm = attn::decode_ctas_per_sm(d_k, h->np);
+    h->part_slots = 2 * (size_t)h->n_sm * h->ctas_per_sm;
     if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_err), sizeof(int))) != cudaSuccess) return fail(e);
     if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess) return fail(e);
     if ((e = cudaMalloc(reinterpret_cast<void**>(&h->d_counters), sizeof(unsigned) * B * Hkv)) != cudaSuccess)
@@ -172,9 +178,10 @@ attn_status attn_decode_forward(attn_decode_handle h, const void* Q, const void*
         h->last_v = V;
     }
     attn::DecodeSchedule sched;
-    const int ctas = std::min(h->grid_limit > 0 ? std::min(h->grid_limit, h->n_sm) : h->n_sm, attn::kDecodeMaxCta);
+    const int grid = h->n_sm * h->ctas_per_sm;
+    const int ctas = std::min(h->grid_limit > 0 ? std::min(h->grid_limit, grid) : grid, attn::kDecodeMaxCta);
     attn::build_decode_schedule(h->B, h->Hkv, h->S_q, h->kind, h->window, cache_len, ctas, &sched);
-    if (2 * (size_t)sched.n_cta > h->part_slots) return ATTN_ERR_UNSUPPORTED;  // cannot happen: n_cta <= n_sm
+    if (2 * (size_t)sched.n_cta > h->part_slots) return ATTN_ERR_UNSUPPORTED;  // cannot happen: n_cta <= grid
     for (int b = 0; b < h->B; ++b) p.len[b] = cache_len[b];
     for (int b = 0; b <= h->B; ++b) p.tile_prefix[b] = sched.tile_prefix[b];
     for (int k = 0; k <= sched.n_cta; ++k) p.share[k] = sched.share[k];

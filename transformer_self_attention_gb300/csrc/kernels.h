@@ -80,7 +80,7 @@ struct F32Params {
 // [k * T / n_cta, (k+1) * T / n_cta), T = Hkv * tile_prefix[B].  A CTA processes the
 // query rows of a kv head's group (group * S_q rows, padded to NP columns).
 constexpr int kDecodeMaxBatch = 1024;
-constexpr int kDecodeMaxCta = 256;  // the persistent grid is min(multiprocessors, this, tiles) CTAs
+constexpr int kDecodeMaxCta = 512;  // the persistent grid is min(CTAs per SM x multiprocessors, this, tiles)
 struct DecodeParams {
     CUtensorMap tm_q;    // Q as 2-D [B*Hq*S_q, d] bf16, box {64, NP}, 128B swizzle
     CUtensorMap tm_k;    // K cache [B*Hkv, S_cap, d], box {64, 128, 1}
@@ -107,7 +107,7 @@ struct DecodeParams {
 cudaError_t launch_decode(const DecodeParams& p, int d, int np, cudaStream_t stream);
 
 // Merge of the units split over several CTAs, as a kernel of its own: one warp per packed row.
-constexpr int kDecodeMaxSplit = 256;
+constexpr int kDecodeMaxSplit = 512;
 struct DecodeMergeParams {
     const float* part_o;    // the decode kernel's partial slots
     const float* part_lse;
