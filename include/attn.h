@@ -465,8 +465,8 @@ attn_status attn_decode_create(attn_decode_handle* out, int B, int Hq, int Hkv, 
  *   cache_len       : HOST array of B lengths, each in [1, S_cap], and >= S_q
  *                     for the causal kinds; read before the call returns.
  * The (sequence, kv head) units are laid end to end as one list of 128-key
- * tiles and a persistent grid of one CTA per multiprocessor takes contiguous
- * shares of it, weighted by tiles and by the units begun inside a share
+ * tiles and a persistent grid (one CTA per multiprocessor; two at d_k = 64
+ * with at most 32 packed rows) takes contiguous shares of it, weighted by tiles and by the units begun inside a share
  * (attn_decode_schedule_host); a unit cut between CTAs is combined on the
  * device by a second, small kernel enqueued behind the first (see
  * attn_decode_set_merge_mode).
@@ -525,14 +525,16 @@ attn_status attn_decode_destroy(attn_decode_handle h);
  * lo_b = max(0, cache_len[b] - S_q - window) / ATTN_TILE.  With
  * n_b = hi_b - lo_b, tile_prefix[b] = n_0 + ... + n_{b-1}; unit (b, g) covers
  * the indices [Hkv * tile_prefix[b] + g * n_b, ... + n_b) of one list of
- * T = Hkv * tile_prefix[B] tiles.  CTA k of the *n_cta = min(n_sm, 256, T) CTAs
+ * T = Hkv * tile_prefix[B] tiles.  CTA k of the *n_cta = min(n_sm, 512, T) CTAs
  * takes the indices [share[k], share[k + 1]): share[0] = 0, share[n_cta] = T,
  * every share non-empty, and the boundaries sit at equal steps of
  * F(i) = i + 2 * (number of unit begins u with 0 < u <= i), so that a share's
  * weight is its tiles plus two for every unit it begins inside it (the cost of
  * one more stretch: an epilogue and a pipeline refill, about two tiles' time).
  *   tile_prefix : output, B + 1 ints.
- *   share       : output, *n_cta + 1 long longs (room for min(n_sm, 256) + 1).
+ *   share       : output, *n_cta + 1 long longs (room for min(n_sm, 512) + 1).
+ * n_sm is the CTA budget: attn_decode_forward passes the multiprocessor count,
+ * or twice it at d_k = 64 with at most 32 packed rows.
  * Errors: ATTN_ERR_INVALID_ARG (n_sm < 1, NULL outputs, shape or lengths as for
  * the calls above).
  */
