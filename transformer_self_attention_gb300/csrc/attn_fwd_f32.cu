@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(F32_THREADS) attn_fwd_f32_kernel(F32Params p) 
     }
 }
 
-// Evaluates the softmax warps' FMA-pipe exp2 (exp2_poly2) elementwise, for its test.
+// Evaluates the FMA-pipe exp2 (exp2_poly2, kept for the exponential-offload experiments) elementwise, for its test.
 __global__ void exp2_selftest_kernel(const float* x, float* y, int n) {
     const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (i >= n) return;
