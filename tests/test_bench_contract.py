@@ -88,3 +88,35 @@ def test_clock_summary_is_time_weighted_over_the_timed_region():
     assert s["sm_mhz_time_weighted_median"] == 2070 and s["sm_mhz"] == 2070
     assert s["sm_mhz_min"] == 1800 and s["reasons"] == ["sw_power_cap"]
     assert abs(s["power_w_max"] - 850.0) < 1e-9 and s["sm_max_mhz"] == 2070
+
+
+def test_traffic_is_read_only_from_a_summary_of_the_current_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only while the summary's source hash
+    equals the hash of the kernel sources as they are; any other hash, or no summary, gives None."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// kernel v1\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sources = ["k.cu"]
+    h1 = bench.kernel_hash(sources)
+    (prof / "kern_w.md").write_text(f"kernel_source_hash: {h1}\ndram_bytes_per_full_launch: 123456\n")
+    assert bench.ncu_traffic("w", "kern", sources) == 123456.0
+    assert bench.ncu_traffic("other", "kern", sources) is None  # no summary for that workload
+    src.write_text("// kernel v2\n")  # the source moved on: the counters are stale
+    assert bench.kernel_hash(sources) != h1
+    assert bench.ncu_traffic("w", "kern", sources) is None
+
+
+def test_every_committed_summary_names_its_hash_and_bytes():
+    """Each profile the bench reads traffic from carries both fields (current or marked stale)."""
+    import re
+    names = [n for n in os.listdir(os.path.join(ROOT, "profiles"))
+             if n.startswith(("attn_fwd_tc_", "attn_bwd_", "attn_decode_"))]
+    assert names
+    for n in names:
+        text = open(os.path.join(ROOT, "profiles", n)).read()
+        assert re.search(r"kernel_source_hash:\s*[0-9a-f]{16}\b", text), n
+        assert re.search(r"dram_bytes_per_full_launch:\s*[0-9]+", text), n
